@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged decode-attention path on one GB300 (or N replicas).
+
+One step = one decode step of the 8B-shaped batch: pa_reshape_and_cache of
+the step's new token for every sequence, then pa_decode (partition kernel +
+log-sum-exp merge kernel) over the whole batch.  Inputs are resident in HBM;
+the KV bytes a step reads (about 604 MB) exceed the 129 MB L2, so no flush
+is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  The value is decode KV GB/s: the algorithmic bytes of
+a step (every cached K/V row read once, q, out, block tables, context
+lengths, and the new rows read and written) divided by the step time.
+--impl reference times the CPU oracle on a bounded sample of the same
+workload instead.
+"""
+import os
+
+# The oracle's NumPy work is timed single-threaded; fix BLAS threads before
+# NumPy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import dataclasses  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import re  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_124_gb300 import inputs as I  # noqa: E402
+
+METRIC = "paged decode-attn KV GB/s (frac of HBM peak); seqs/s at 8B GQA shape"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_partition_kernel_batch64_8b.md")
+KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_decode.cu")
+
+WORKLOADS = {
+    "batch64_8b": lambda seed, B: I.batch64_8b(seed, B),
+    "long_context": lambda seed, B: I.long_context(seed, B),
+    "cow_sampling": lambda seed, B: I.cow_sampling(seed, block_size=B),
+    "mixed_batch": lambda seed, B: I.mixed_batch(seed, B, n_layers=1),
+    "tiny_gqa": lambda seed, B: I.tiny_gqa(seed),
+}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_timing(elapsed_s, units, world, device="cpu"):
+    """Max of the elapsed times and sum of the units over all ranks: the
+    whole job runs as long as its slowest replica."""
+    if world == 1:
+        return float(elapsed_s), float(units)
+    t = torch.tensor([float(elapsed_s)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.all_reduce(u, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def replica_seed(base_seed, rank):
+    """Each replica decodes its own batch (weak scaling)."""
+    return int(base_seed) + 1000 * int(rank)
+
+
+# ----------------------------------------------------------------------------
+# byte accounting
+# ----------------------------------------------------------------------------
+
+def algorithmic_bytes(sc, ctx, n_new_tokens):
+    """Bytes one step must move at minimum: decode reads each cached K and V
+    row of each KV head once, q, the block-table entries in use and the
+    context lengths, and writes out; reshape_and_cache reads and writes each
+    new token's K and V rows."""
+    ctx = np.asarray(ctx, dtype=np.int64)
+    row = sc.d_head * 2
+    kv = int(ctx.sum()) * sc.n_kv_heads * row * 2
+    S = len(ctx)
+    qo = 2 * S * sc.n_q_heads * row
+    tables = int((-(-ctx // sc.block_size)).sum()) * 4 + S * 4
+    decode = kv + qo + tables
+    cache_write = 2 * n_new_tokens * sc.n_kv_heads * row * 2
+    return decode, cache_write
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+        src_hash = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()[:16]
+        m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+        m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+        if m_hash and m_tr and m_hash.group(1) == src_hash:
+            return int(m_tr.group(1))
+    except OSError:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "100"] + self.sel, stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# our implementation
+# ----------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    from paged_kv_cache_124_gb300 import api
+    from paged_kv_cache_124_gb300.runner import ScenarioRunner
+
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    seed = replica_seed(args.seed, rank)
+    sc = WORKLOADS[args.workload](seed, args.block_size)
+    run = ScenarioRunner(sc, device=dev, data_device="cpu").replay()
+    tables, ctx, max_ctx = run.decode_metadata()
+    S = len(sc.decode_seqs)
+    ctx_h = ctx.cpu().numpy()
+    # the step's new token per sequence: the last position of each context
+    slots_h = np.array([run.alloc.slot_mapping(s, run.alloc.seq_len(s) - 1, 1)[0] for s in sc.decode_seqs])
+    slots = torch.from_numpy(slots_h).to(dev)
+    k_new, v_new = I.append_kv(sc.seed, 0, 10 ** 6, S, sc.n_kv_heads, sc.d_head)
+    k_new, v_new = k_new.to(dev), v_new.to(dev)
+    q = I.decode_q(sc.seed, 0, S, sc.n_q_heads, sc.d_head).to(dev)
+    out = torch.empty_like(q)
+    P = args.partition
+    ws = api.decode_workspace(S, sc.n_q_heads, sc.d_head, max_ctx, P, device=dev)
+    kc, vc = run.k_caches[0], run.v_caches[0]
+    stream = torch.cuda.current_stream(dev)
+    dec_bytes, write_bytes = algorithmic_bytes(sc, ctx_h, S)
+    max_parts = -(-max_ctx // (P or api.pa_decode_default_partition_size(max_ctx)))
+    launches_per_step = 1 + 1 + (1 if max_parts > 1 else 0)
+
+    def step():
+        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
+        api.pa_decode(out, q, kc, vc, tables, ctx, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
+                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=stream)
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    for _ in range(args.warmup):
+        step()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        ev[i][0].record(stream)
+        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
+        ev[i][1].record(stream)
+        api.pa_decode(out, q, kc, vc, tables, ctx, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
+                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    step_s = ev[0][0].elapsed_time(ev[K - 1][2]) / 1e3
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    dec_s_avg = sum(dec_ms) / K / 1e3
+    total_s, total_bytes = reduce_timing(step_s, (dec_bytes + write_bytes) * K, world, dev)
+    _, total_seqs = reduce_timing(step_s, S * K, world, dev)
+
+    # ---- end to end through the public API with host buffers ---------------
+    q_h = q.cpu().pin_memory()
+    k_h, v_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    slots_hp = slots.cpu().pin_memory()
+    tables_h, ctx_hp = tables.cpu().pin_memory(), ctx.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, k_d, v_d = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    slots_d, tables_d, ctx_d = torch.empty_like(slots), torch.empty_like(tables), torch.empty_like(ctx)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, slots_hp, tables_h, ctx_hp))
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for dst, src in ((q_d, q_h), (k_d, k_h), (v_d, v_h), (slots_d, slots_hp), (tables_d, tables_h),
+                         (ctx_d, ctx_hp)):
+            dst.copy_(src, non_blocking=True)
+        api.pa_reshape_and_cache(kc, vc, k_d, v_d, slots_d, stream=stream)
+        api.pa_decode(out, q_d, kc, vc, tables_d, ctx_d, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
+                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = time.perf_counter() - t0
+    barrier(world)
+    e2e_total_s, e2e_bytes = reduce_timing(e2e_s, (dec_bytes + write_bytes) * K, world, dev)
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    achieved = dec_bytes / dec_s_avg / 1e9
+    value = total_bytes / total_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "bf16", "data": "synthetic",
+        "config": {"workload": sc.name, "num_seqs": S, "context_lens": "uniform [512, 4096]" if
+                   args.workload == "batch64_8b" else "see workload", "total_context": int(ctx_h.sum()),
+                   "n_q_heads": sc.n_q_heads, "n_kv_heads": sc.n_kv_heads, "d_head": sc.d_head,
+                   "block_size": sc.block_size, "num_blocks": sc.num_blocks, "placement": "seeded random",
+                   "partition_size": P or api.pa_decode_default_partition_size(max_ctx),
+                   "l2": "inputs larger than L2 (%.0f MB KV read per step vs 129 MB L2); no flush" %
+                         (dec_bytes / 1e6),
+                   "parallelism": "replicas (one batch per GPU)" if world > 1 else "single GPU"},
+        "seqs_per_s": round(total_seqs / total_s, 1),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_partition_kernel + lse_merge_kernel)",
+                     "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": int(dec_bytes),
+                     "avg_launch_us": round(dec_s_avg * 1e6, 2)},
+        "e2e": {"value": round(e2e_bytes / e2e_total_s / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_total_s / K * 1e3, 4)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sc, args.cpu_seconds)
+    return line
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (the cpu_baseline leg and --impl reference)
+# ----------------------------------------------------------------------------
+
+def _oracle_sample(sc, seqs):
+    """Oracle replay of the workload with only `seqs` materialised."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from _oracle_replay import OracleReplay
+    sub = dataclasses.replace(sc, decode_seqs=list(seqs))
+    rep = OracleReplay(sub).replay()
+    tab, lens = rep.tables()
+    q = I.bf16_bits(I.decode_q(sc.seed, 0, len(sc.decode_seqs), sc.n_q_heads, sc.d_head))[list(seqs)]
+    return rep, tab, lens, q
+
+
+def _oracle_time(sc, rep, tab, lens, q):
+    from oracle import attention as A
+    t0 = time.perf_counter()
+    A.paged_decode(q, rep.k[0], rep.v[0], tab, lens, sc.scale, sc.block_size)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(sc, budget_s):
+    """The oracle as it stands, on a bounded sample: the first sequences of
+    the workload, as many as fit the time budget (about budget_s)."""
+    n = 1
+    seqs = [0]
+    rep, tab, lens, q = _oracle_sample(sc, seqs)
+    t = _oracle_time(sc, rep, tab, lens, q)
+    while t < budget_s / 2 and n < len(sc.decode_seqs):
+        n = min(len(sc.decode_seqs), max(n + 1, int(n * min(8.0, budget_s / max(t, 1e-3)))))
+        seqs = list(range(n))
+        rep, tab, lens, q = _oracle_sample(sc, seqs)
+        t = _oracle_time(sc, rep, tab, lens, q)
+    dec_bytes, _ = algorithmic_bytes(sc, lens, 0)
+    return {"value": round(dec_bytes / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "fp64 oracle decode of the first %d of %d sequences (%d positions, all %d query heads) "
+                      "of %s, %.1f s" % (n, len(sc.decode_seqs), int(np.sum(lens)), sc.n_q_heads, sc.name, t)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    sc = WORKLOADS[args.workload](args.seed, args.block_size)
+    per_step = max(1, args.ref_seqs_per_step)
+    samples = []
+    S = len(sc.decode_seqs)
+    for i in range(args.warmup + args.steps):
+        seqs = [(i * per_step + j) % S for j in range(per_step)]
+        rep, tab, lens, q = _oracle_sample(sc, seqs)
+        t = _oracle_time(sc, rep, tab, lens, q)
+        if i >= args.warmup:
+            samples.append((t, algorithmic_bytes(sc, lens, 0)[0], len(seqs)))
+    tot_t = sum(s[0] for s in samples)
+    tot_b = sum(s[1] for s in samples)
+    value = tot_b / tot_t / 1e9
+    desc = ("fp64 oracle decode, %d sequence(s) of %s per step (rotating), all %d query heads"
+            % (per_step, sc.name, sc.n_q_heads))
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / len(samples) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": sc.name, "num_seqs_per_step": per_step},
+            "seqs_per_s": round(sum(s[2] for s in samples) / tot_t, 3),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="batch64_8b")
+    p.add_argument("--block-size", type=int, default=16)
+    p.add_argument("--partition", type=int, default=0, help="positions per partition (0 = library default)")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--ref-seqs-per-step", type=int, default=2)
+    args = p.parse_args(argv)
+    world, rank, local = dist_env()
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

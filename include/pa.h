@@ -1,0 +1,296 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged decode-attention library.
+ *
+ * The library computes single-query (decode) attention over a KV cache that
+ * is stored in fixed-size physical blocks, together with the two kernels that
+ * feed that cache and a host-side block manager.  Sources for the method:
+ *   [P1] "PagedAttention: Virtual Memory for the KV Cache" (int8ai.pages.dev)
+ *   [P2] "PagedAttention in vLLM: scattered memory, exact attention"
+ *        (abhiram1809.github.io)
+ *   [P3] "PagedAttention and KV Memory" (blog.michaelsam94.com)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensors are caller-owned.  Device pointers point to CUDA device
+ *    memory of the current device; the library never allocates, frees or
+ *    retains device memory.  Host pointers are only read during the call.
+ *  - Element types: K/V caches, q, new keys/values are bf16 (2 bytes);
+ *    attention output is bf16 or fp32 (see PA_DTYPE_*).  Integers are the
+ *    fixed-width types named in each signature.
+ *  - Cache layout (one pair of tensors per layer): k_cache and v_cache are
+ *    contiguous [num_blocks][n_kv_heads][block_size][d_head].  The keys of one
+ *    (block, kv head) are one contiguous block_size * d_head * 2 byte run.
+ *  - Supported shapes: block_size in {8, 16, 32}; d_head in {64, 128};
+ *    n_q_heads a multiple of n_kv_heads with G = n_q_heads / n_kv_heads in
+ *    {1, 2, 4, 8, 16}.  Other shapes return PA_ERR_UNSUPPORTED.
+ *  - Device pointers must be 16-byte aligned (PA_ERR_MISALIGNED otherwise).
+ *  - GPU work is enqueued asynchronously on `stream` (a cudaStream_t passed
+ *    as void*; NULL is the legacy default stream).  A return of PA_OK means
+ *    the launch was enqueued; errors detected on the host are returned before
+ *    anything is enqueued.
+ *  - Errors that only the device can see (a block id outside
+ *    [0, num_blocks), a slot outside [0, num_blocks * block_size), a context
+ *    length above max_blocks_per_seq * block_size or max_context_len) never
+ *    trap: the offending access is skipped or clamped and a PA_DEV_* bit is
+ *    OR-ed into *status_dev, if status_dev is not NULL (a device int32 the
+ *    caller zeroes and reads back).  Outputs touched by such an error are
+ *    unspecified.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (returned) ---------------------------------------------- */
+#define PA_OK                 0
+#define PA_FAIL_NO_BLOCKS     1   /* pool exhausted; nothing was changed        */
+#define PA_ERR_INVALID_ARG   -1
+#define PA_ERR_UNSUPPORTED   -2
+#define PA_ERR_MISALIGNED    -3
+#define PA_ERR_CUDA          -4   /* a CUDA runtime call failed                 */
+#define PA_ERR_WORKSPACE     -5   /* workspace missing or too small             */
+#define PA_ERR_UNKNOWN_SEQ   -6
+#define PA_ERR_DUPLICATE_SEQ -7
+
+/* ---- device-side status bits (OR-ed into *status_dev) ---------------------- */
+#define PA_DEV_BAD_BLOCK_ID   1   /* table entry or copy pair outside the pool  */
+#define PA_DEV_BAD_SLOT       2   /* slot_mapping entry outside the pool        */
+#define PA_DEV_BAD_CONTEXT    4   /* context length above the stated maximum    */
+#define PA_DEV_WAIT_TIMEOUT   8   /* a bounded wait for a bulk copy gave up     */
+
+/* ---- output element types ------------------------------------------------- */
+#define PA_DTYPE_BF16 0
+#define PA_DTYPE_F32  1
+
+/* Library version string and a short text for a status code. */
+const char* pa_version(void);
+const char* pa_status_string(int status);
+
+/* ===========================================================================
+ * Decode attention
+ * ===========================================================================
+ * Operation ([P1] section 1; [P2] section 10; [P1] sections 7 and 13):
+ * for every sequence s and query head g, with G = n_q_heads / n_kv_heads and
+ * KV head h = g / G (contiguous groups; [P1] section 1 and [P2] section 7 fix
+ * that G query heads share a KV head, not which ones),
+ *
+ *   out[s][g][:] = sum_j a_j V_j,   a = softmax(scale * q[s][g] . K_j),
+ *
+ * over positions j = 0 .. context_lens[s]-1, where position j of sequence s
+ * is read from physical block block_tables[s][j / block_size] at offset
+ * j % block_size ([P1] section 7).  Positions at and beyond the context
+ * length are never read into the result ([P1] section 13, item 4).  The
+ * softmax is computed online in fp32 with a running maximum and sum
+ * ([P1] section 13; [P2] section 11).  A context length of 0 gives a zero
+ * row.  The token this step appended is part of the context: context_lens
+ * counts it.
+ *
+ * Long contexts are split into partitions of partition_size positions that
+ * are processed by different thread blocks; each writes its partial
+ * maximum m, weight sum z and unnormalised weighted value sum u (the
+ * statistics of [P2] section 11) to `workspace`, and a second kernel merges
+ * them exactly (the "secondary reduction" of [P1] section 13).  A sequence
+ * that fits one partition is finished by the first kernel directly.
+ *
+ * Arguments
+ *   out           device [num_seqs][n_q_heads][d_head], PA_DTYPE_BF16 (round
+ *                 to nearest even) or PA_DTYPE_F32, per out_dtype.
+ *   q             device bf16 [num_seqs][n_q_heads][d_head].
+ *   k_cache,
+ *   v_cache       device bf16 [num_blocks][n_kv_heads][block_size][d_head].
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq], row-major;
+ *                 only the first ceil(context_lens[s] / block_size) entries of
+ *                 row s are read.
+ *   context_lens  device int32 [num_seqs].
+ *   scale         score scale, normally 1 / sqrt(d_head).
+ *   max_context_len  host upper bound on every context_lens[s]; it sizes the
+ *                 launch grid.  Larger device values are clamped to it and
+ *                 flagged with PA_DEV_BAD_CONTEXT.
+ *   partition_size   positions per partition: 0 picks the library default
+ *                 (pa_decode_default_partition_size); otherwise a multiple
+ *                 of 64 in [64, 8192].
+ *   workspace     device scratch of at least pa_decode_workspace_size(...)
+ *                 bytes, 256-byte aligned; may be NULL (with bytes 0) when
+ *                 max_context_len <= the partition size.  Its contents are
+ *                 not preserved across calls; calls that share a workspace
+ *                 must be stream-ordered.
+ *   status_dev    optional device int32, see PA_DEV_* above.
+ * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED,
+ * PA_ERR_WORKSPACE or PA_ERR_CUDA (launch failure).
+ */
+int pa_decode_default_partition_size(int max_context_len);
+
+size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int d_head,
+                                int max_context_len, int partition_size);
+
+int pa_decode(void* out, int out_dtype, const void* q,
+              const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens,
+              int block_size, float scale, int n_q_heads, int n_kv_heads,
+              int d_head, int num_seqs, int max_blocks_per_seq, int num_blocks,
+              int max_context_len, int partition_size,
+              void* workspace, size_t workspace_bytes,
+              int32_t* status_dev, void* stream);
+
+/* Exact merge of partition statistics ([P2] section 11):
+ *   M = max_p m_p,  Z = sum_p exp(m_p - M) z_p,  U = sum_p exp(m_p - M) u_p,
+ *   out = U / Z,
+ * over partitions p = 0 .. ceil(context_lens[s] / partition_size) - 1 of each
+ * (sequence s, query head g).  m is in the units of the scores themselves
+ * (natural-log domain).  This is the second kernel of pa_decode, exposed so
+ * that partition statistics from any source can be merged.
+ *   part_max, part_sum  device f32 [num_seqs][n_q_heads][max_parts]
+ *   part_acc            device f32 [num_seqs][n_q_heads][max_parts][d_head]
+ *   context_lens        device int32 [num_seqs]; partitions counted as above,
+ *                       capped at max_parts; a count of 0 writes zeros.
+ *   partition_size      any value >= 1.
+ * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED
+ * or PA_ERR_CUDA. */
+int pa_lse_merge(void* out, int out_dtype, const float* part_max,
+                 const float* part_sum, const float* part_acc,
+                 const int32_t* context_lens, int partition_size, int max_parts,
+                 int num_seqs, int n_q_heads, int d_head, void* stream);
+
+/* ===========================================================================
+ * Cache writes
+ * ===========================================================================
+ * reshape_and_cache ([P1] section 16 item 3 and section 20: each newly
+ * computed position's key and value are written to its place in the pool):
+ * for every token t with slot = slot_mapping[t] >= 0, and every KV head h,
+ *   k_cache[slot / block_size][h][slot % block_size][:] = k[t][h][:]
+ *   v_cache[slot / block_size][h][slot % block_size][:] = v[t][h][:]
+ * The slot number is physical_block * block_size + offset, the
+ * frame * size + offset form of [P2] section 2.  Negative slots are skipped
+ * (padding); slots >= num_blocks * block_size are skipped and flagged
+ * PA_DEV_BAD_SLOT.  The copy is bit-exact.  Two tokens with the same slot in
+ * one call race (one of them wins).
+ *   k, v          device bf16 [num_tokens][n_kv_heads][d_head], contiguous.
+ *   slot_mapping  device int64 [num_tokens].
+ * num_tokens == 0 is a no-op returning PA_OK.
+ */
+int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* k,
+                         const void* v, const int64_t* slot_mapping,
+                         int num_tokens, int n_kv_heads, int d_head,
+                         int block_size, int num_blocks, int32_t* status_dev,
+                         void* stream);
+
+/* copy_blocks: the copy-on-write clone of a shared tail block ([P1]
+ * sections 15 and 16): for every pair (src, dst) = (block_pairs[2i],
+ * block_pairs[2i+1]) and every layer l, block dst of k_caches[l] and
+ * v_caches[l] becomes a bit-exact copy of block src (all heads, all
+ * block_size slots).  Pairs are copied concurrently, so no dst may repeat
+ * and no dst may be another pair's src (the block manager never emits
+ * such pairs: dst is always a freshly taken block).  Ids outside
+ * [0, num_blocks) are skipped and flagged PA_DEV_BAD_BLOCK_ID.
+ *   k_caches, v_caches  HOST arrays of num_layers device pointers, each a
+ *                       cache laid out as above (same shape for all layers).
+ *   block_pairs         device int32 [num_pairs][2].
+ * num_pairs == 0 or num_layers == 0 is a no-op returning PA_OK.
+ * Must be ordered before the reshape_and_cache that writes into dst in the
+ * same step (same stream, earlier launch). */
+int pa_copy_blocks(void* const* k_caches, void* const* v_caches,
+                   int num_layers, const int32_t* block_pairs, int num_pairs,
+                   int n_kv_heads, int d_head, int block_size, int num_blocks,
+                   int32_t* status_dev, void* stream);
+
+/* ===========================================================================
+ * Host block manager ([P1] sections 14-17 and 20)
+ * ===========================================================================
+ * A pool of num_blocks blocks of block_size positions.  The free list is a
+ * stack: a fresh manager hands out blocks 0, 1, 2, ... and released blocks
+ * are reused last-released-first ([P1] section 20).  Every block carries a
+ * reference count; sequences are named by caller-chosen int64 ids.
+ * Appending only plans a step: it returns the slot for the new position and,
+ * when the tail block was shared, the (src, dst) block pair that the caller
+ * must pass to pa_copy_blocks before writing with pa_reshape_and_cache.
+ * Every call that can fail for lack of blocks is transactional: on
+ * PA_FAIL_NO_BLOCKS nothing changes ([P1] section 20, test 4).
+ * A handle is not thread-safe; use one per thread or lock around it. */
+typedef struct pa_alloc pa_alloc_t;
+
+typedef struct pa_alloc_stats {
+    int32_t num_blocks;
+    int32_t num_free;
+    int32_t num_used;
+    int32_t num_seqs;
+    int64_t num_cow_copies;     /* CoW pairs emitted since creation        */
+} pa_alloc_stats_t;
+
+/* NULL if num_blocks <= 0 or block_size <= 0 or on allocation failure. */
+pa_alloc_t* pa_alloc_create(int num_blocks, int block_size);
+void pa_alloc_destroy(pa_alloc_t* a);
+
+/* Replace the free list by order[0 .. n-1] (blocks leave from the end), e.g.
+ * to place sequences at seeded random physical blocks.  Only while no block
+ * is in use; order must be a permutation of 0 .. num_blocks-1.
+ * PA_ERR_INVALID_ARG otherwise. */
+int pa_alloc_set_free_order(pa_alloc_t* a, const int32_t* order, int n);
+
+/* Take ceil(num_tokens / block_size) blocks (ref 1) for a new sequence of
+ * num_tokens prompt positions.  PA_ERR_DUPLICATE_SEQ if seq exists,
+ * PA_ERR_INVALID_ARG if num_tokens <= 0, PA_FAIL_NO_BLOCKS if too few free. */
+int pa_alloc_sequence(pa_alloc_t* a, int64_t seq, int num_tokens);
+
+/* child gets a copy of parent's table and length; every block's count +1
+ * ([P1] section 16, step 2).  PA_ERR_UNKNOWN_SEQ / PA_ERR_DUPLICATE_SEQ. */
+int pa_alloc_fork(pa_alloc_t* a, int64_t parent, int64_t child);
+
+/* Plan one appended position at index L = current length ([P1] sections
+ * 15, 16): tail shared and partly filled -> new block, *cow_src = old tail,
+ * *cow_dst = new block; tail private with room -> in place; tail full ->
+ * new block.  *slot_out = block * block_size + (L % block_size); the length
+ * becomes L + 1.  *cow_src = *cow_dst = -1 when no copy is needed.
+ * PA_ERR_UNKNOWN_SEQ, PA_FAIL_NO_BLOCKS (no change). */
+int pa_alloc_append_slot(pa_alloc_t* a, int64_t seq, int64_t* slot_out,
+                         int32_t* cow_src, int32_t* cow_dst);
+
+/* Batch form: plans one position for each of seqs[0..n-1] in order.  Writes
+ * slots_out[i]; CoW pairs go to cow_pairs_out[2k], [2k+1] (capacity
+ * cow_capacity pairs, n is always enough) and their count to *num_cow.
+ * Stops at the first failure: *num_done (if not NULL) tells how many
+ * sequences were planned; their changes stay.  Returns the first failure's
+ * status or PA_OK. */
+int pa_alloc_append_slots(pa_alloc_t* a, const int64_t* seqs, int n,
+                          int64_t* slots_out, int32_t* cow_pairs_out,
+                          int cow_capacity, int* num_cow, int* num_done);
+
+/* Release: every block in seq's table loses one reference and returns to
+ * the free list at 0, in table order ([P1] section 17).  Unknown seq: no-op,
+ * PA_OK.  Blocks are reusable only after GPU work that reads or writes them
+ * has completed; the caller orders that (same stream). */
+int pa_alloc_free(pa_alloc_t* a, int64_t seq);
+
+/* Copy seq's block table into out[0 .. cap-1]; *n_out = its length.
+ * PA_ERR_UNKNOWN_SEQ; PA_ERR_INVALID_ARG if cap is too small. */
+int pa_alloc_block_table(const pa_alloc_t* a, int64_t seq, int32_t* out,
+                         int cap, int* n_out);
+
+/* Decode metadata for a batch: row i of tables (row stride max_blocks) gets
+ * seqs[i]'s table, padded with -1; context_lens[i] its length.
+ * PA_ERR_UNKNOWN_SEQ, PA_ERR_INVALID_ARG if a table is longer than
+ * max_blocks. */
+int pa_alloc_build_tables(const pa_alloc_t* a, const int64_t* seqs, int n,
+                          int32_t* tables, int max_blocks, int32_t* context_lens);
+
+/* Slots of positions start .. start+n-1 of seq ([P1] section 7):
+ * table[i / B] * B + i % B.  PA_ERR_INVALID_ARG if the range is outside
+ * [0, length). */
+int pa_alloc_slot_mapping(const pa_alloc_t* a, int64_t seq, int start, int n,
+                          int64_t* out);
+
+int pa_alloc_seq_len(const pa_alloc_t* a, int64_t seq);      /* -1 if unknown */
+int pa_alloc_ref_count(const pa_alloc_t* a, int32_t block);  /* -1 if out of range */
+int pa_alloc_num_free(const pa_alloc_t* a);
+/* Copy the free stack bottom-to-top into out (cap entries); returns its size. */
+int pa_alloc_free_list(const pa_alloc_t* a, int32_t* out, int cap);
+int pa_alloc_get_stats(const pa_alloc_t* a, pa_alloc_stats_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H_ */

@@ -52,7 +52,8 @@ def translate(i, block_size, block_table_row):
 def gather_kv(k_cache, v_cache, block_table_row, context_len, block_size):
     """Gather one sequence's keys and values into contiguous arrays.
 
-    k_cache, v_cache: [num_blocks, n_kv_heads, block_size, d_head], float64.
+    k_cache, v_cache: [num_blocks, n_kv_heads, block_size, d_head], float64,
+    or uint16 bf16 bit patterns (decoded exactly as they are gathered).
     Returns K, V of shape [n_kv_heads, context_len, d_head] in logical token
     order: the contiguous layout of [P1] section 12 for one sequence.
 
@@ -60,14 +61,15 @@ def gather_kv(k_cache, v_cache, block_table_row, context_len, block_size):
     contributes only its valid positions ([P1] section 13, items 2 and 4;
     [P1] section 20, the valid length of the final block)."""
     n_kv_heads, d_head = k_cache.shape[1], k_cache.shape[3]
+    to_f64 = bf16_to_f64 if k_cache.dtype == np.uint16 else (lambda x: x)
     K = np.empty((n_kv_heads, context_len, d_head), dtype=np.float64)
     V = np.empty((n_kv_heads, context_len, d_head), dtype=np.float64)
     n_blocks = -(-context_len // block_size)
     for b in range(n_blocks):
         phys, _ = translate(b * block_size, block_size, block_table_row)
         valid = min(block_size, context_len - b * block_size)
-        K[:, b * block_size: b * block_size + valid, :] = k_cache[phys, :, :valid, :]
-        V[:, b * block_size: b * block_size + valid, :] = v_cache[phys, :, :valid, :]
+        K[:, b * block_size: b * block_size + valid, :] = to_f64(k_cache[phys, :, :valid, :])
+        V[:, b * block_size: b * block_size + valid, :] = to_f64(v_cache[phys, :, :valid, :])
     return K, V
 
 
@@ -89,12 +91,15 @@ def kv_head_of(q_head, n_q_heads, n_kv_heads):
 def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale, block_size):
     """Decode attention for a batch, through the block tables.
 
-    q:            [S, n_q_heads, d_head] float64
+    q:            [S, n_q_heads, d_head] float64 (or uint16 bf16 bits)
     k/v_cache:    [num_blocks, n_kv_heads, block_size, d_head] float64
+                  (or uint16 bf16 bits)
     block_tables: [S, max_blocks_per_seq] integer
     context_lens: [S] integer
     returns       [S, n_q_heads, d_head] float64
     """
+    if q.dtype == np.uint16:
+        q = bf16_to_f64(q)
     S, n_q_heads, d_head = q.shape
     n_kv_heads = k_cache.shape[1]
     assert n_q_heads % n_kv_heads == 0

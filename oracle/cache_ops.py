@@ -20,10 +20,9 @@ import numpy as np
 
 
 def reshape_and_cache(k_cache, v_cache, k, v, slot_mapping, block_size):
-    """Return copies of the pools with token t's rows k[t], v[t]
-    ([n_kv_heads, d_head] each) written at slot_mapping[t]."""
-    k_out = np.array(k_cache, copy=True)
-    v_out = np.array(v_cache, copy=True)
+    """Write token t's rows k[t], v[t] ([n_kv_heads, d_head] each) at
+    slot_mapping[t], in place; returns the two pools."""
+    k_out, v_out = k_cache, v_cache
     for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
         if slot < 0:
             continue
@@ -34,10 +33,9 @@ def reshape_and_cache(k_cache, v_cache, k, v, slot_mapping, block_size):
 
 
 def copy_blocks(k_caches, v_caches, pairs):
-    """Return copies of every layer's pools with block dst overwritten by
-    block src for each (src, dst) pair, applied in order."""
-    k_out = [np.array(k, copy=True) for k in k_caches]
-    v_out = [np.array(v, copy=True) for v in v_caches]
+    """Overwrite block dst by block src in every layer's pools, for each
+    (src, dst) pair in order, in place; returns the two lists of pools."""
+    k_out, v_out = k_caches, v_caches
     for layer in range(len(k_out)):
         for src, dst in np.asarray(pairs).reshape(-1, 2).tolist():
             k_out[layer][dst] = k_out[layer][src]

@@ -1,0 +1,134 @@
+// Cache-feeding kernels for sm_103a: reshape_and_cache (scatter each new
+// token's key/value rows into its slot) and copy_blocks (copy-on-write block
+// clone).  Both are pure byte copies: 16-byte vector loads and stores, one
+// 16-byte chunk per thread per step, coalesced along the d_head rows.
+//
+// Slot arithmetic ("PagedAttention: Virtual Memory for the KV Cache",
+// section 7; "PagedAttention in vLLM: scattered memory, exact attention",
+// section 2): slot = physical_block * B + offset.
+
+#include "pa_common.cuh"
+
+namespace {
+
+constexpr int kCopyThreads = 256;
+constexpr int kMaxLayersPerLaunch = 64;
+
+// One thread block per token: K rows of all heads, then V rows of all heads.
+__global__ void __launch_bounds__(128) reshape_and_cache_kernel(
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const uint4* __restrict__ k,
+    const uint4* __restrict__ v, const int64_t* __restrict__ slot_mapping, int n_kv_heads, int chunks_per_row,
+    int block_size, long long num_slots, int32_t* status) {
+    const int t = blockIdx.x;
+    const long long slot = slot_mapping[t];
+    if (slot < 0) return;                                   // padding token
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0) pa::set_status(status, PA_DEV_BAD_SLOT);
+        return;
+    }
+    const long long blk = slot / block_size;
+    const int off = (int)(slot - blk * block_size);
+    const int per_token = n_kv_heads * chunks_per_row;     // 16-B chunks of one token's K
+    const uint4* ksrc = k + (size_t)t * per_token;
+    const uint4* vsrc = v + (size_t)t * per_token;
+    for (int c = threadIdx.x; c < 2 * per_token; c += blockDim.x) {
+        const bool is_v = c >= per_token;
+        const int cc = is_v ? c - per_token : c;
+        const int h = cc / chunks_per_row;
+        const int x = cc - h * chunks_per_row;
+        const size_t dst = (((size_t)blk * n_kv_heads + h) * block_size + off) * chunks_per_row + x;
+        if (is_v)
+            v_cache[dst] = vsrc[cc];
+        else
+            k_cache[dst] = ksrc[cc];
+    }
+}
+
+struct LayerPtrs {
+    uint4* k[kMaxLayersPerLaunch];
+    uint4* v[kMaxLayersPerLaunch];
+};
+
+// grid: (pair, layer, 0 = K / 1 = V); each thread block copies one whole
+// block (n_kv_heads * B * d_head bf16) with 4 independent 16-B loads in
+// flight per thread.
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const __grid_constant__ LayerPtrs ptrs,
+                                                                   const int32_t* __restrict__ pairs,
+                                                                   long long chunks_per_block, int num_blocks,
+                                                                   int32_t* status) {
+    const int p = blockIdx.x;
+    const int layer = blockIdx.y;
+    const int src = pairs[2 * p];
+    const int dst = pairs[2 * p + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+        if (threadIdx.x == 0) pa::set_status(status, PA_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    uint4* base = blockIdx.z == 0 ? ptrs.k[layer] : ptrs.v[layer];
+    const uint4* s = base + (size_t)src * chunks_per_block;
+    uint4* d = base + (size_t)dst * chunks_per_block;
+    constexpr int U = 4;
+    long long i = threadIdx.x;
+    for (; i + (U - 1) * kCopyThreads < chunks_per_block; i += U * kCopyThreads) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) r[u] = s[i + u * kCopyThreads];
+#pragma unroll
+        for (int u = 0; u < U; ++u) d[i + u * kCopyThreads] = r[u];
+    }
+    for (; i < chunks_per_block; i += kCopyThreads) d[i] = s[i];
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* k, const void* v,
+                         const int64_t* slot_mapping, int num_tokens, int n_kv_heads, int d_head, int block_size,
+                         int num_blocks, int32_t* status_dev, void* stream) {
+    if (num_tokens < 0 || n_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head))
+        return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_cache || !v_cache || !k || !v || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!pa_host::aligned16(k_cache) || !pa_host::aligned16(v_cache) || !pa_host::aligned16(k) ||
+        !pa_host::aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_MISALIGNED;
+    reshape_and_cache_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<const uint4*>(k),
+        static_cast<const uint4*>(v), slot_mapping, n_kv_heads, d_head / 8, block_size,
+        (long long)num_blocks * block_size, status_dev);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers, const int32_t* block_pairs,
+                   int num_pairs, int n_kv_heads, int d_head, int block_size, int num_blocks, int32_t* status_dev,
+                   void* stream) {
+    if (num_layers < 0 || num_pairs < 0 || n_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head))
+        return PA_ERR_UNSUPPORTED;
+    if (num_layers == 0 || num_pairs == 0) return PA_OK;
+    if (!k_caches || !v_caches || !block_pairs) return PA_ERR_INVALID_ARG;
+    if (num_pairs > 2147483647 / 2) return PA_ERR_UNSUPPORTED;
+    for (int l = 0; l < num_layers; ++l) {
+        if (!k_caches[l] || !v_caches[l]) return PA_ERR_INVALID_ARG;
+        if (!pa_host::aligned16(k_caches[l]) || !pa_host::aligned16(v_caches[l])) return PA_ERR_MISALIGNED;
+    }
+    if (reinterpret_cast<uintptr_t>(block_pairs) & 3u) return PA_ERR_MISALIGNED;
+    const long long chunks = (long long)n_kv_heads * block_size * d_head / 8;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
+        const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
+        LayerPtrs ptrs{};
+        for (int l = 0; l < nl; ++l) {
+            ptrs.k[l] = static_cast<uint4*>(k_caches[l0 + l]);
+            ptrs.v[l] = static_cast<uint4*>(v_caches[l0 + l]);
+        }
+        dim3 grid(num_pairs, nl, 2);
+        copy_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(ptrs, block_pairs, chunks, num_blocks, status_dev);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// Shared device helpers: mbarrier + bulk-copy PTX wrappers, bf16 unpacking,
+// argument checks.  Used by the kernels of this library only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// mbarrier (shared::cta) and 1-D bulk async copy global -> shared
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+// One bounded probe of the barrier phase with the given parity.  Returns true
+// once the phase has completed.  The hint lets the hardware suspend the
+// thread for up to ~1 us instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(1000u)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after max_probes probes (each suspends <= ~1 us).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int max_probes) {
+    for (int i = 0; i < max_probes; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// cp.async.bulk: `bytes` (multiple of 16) from global `src` (16-B aligned)
+// to shared `dst` (16-B aligned); completion is counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// bf16 helpers
+// ---------------------------------------------------------------------------
+
+// Two bf16 packed in a 32-bit word -> two floats (exact: bf16 is the upper
+// half of a binary32).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+}  // namespace pa
+
+// ---------------------------------------------------------------------------
+// host-side helpers shared by the C-ABI entry points
+// ---------------------------------------------------------------------------
+namespace pa_host {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline bool supported_block_size(int b) { return b == 8 || b == 16 || b == 32; }
+inline bool supported_d_head(int d) { return d == 64 || d == 128; }
+
+// Opt a kernel into more than 48 KiB of dynamic shared memory, once per
+// device and kernel.
+template <typename K>
+inline cudaError_t ensure_smem_attr(K kernel, int bytes, int* done_mask_by_device) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && (done_mask_by_device[dev] >= bytes)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev < 64) done_mask_by_device[dev] = bytes;
+    return e;
+}
+
+}  // namespace pa_host

@@ -203,3 +203,40 @@ def mixed_batch(seed=0, block_size=16, num_seqs=256, n_layers=32, median=700, si
     ops += [("append", i) for i, c in enumerate(ctx) if c > 1] + [("step",)]
     return Scenario(f"mixed_s{num_seqs}_lognorm{median}_L{n_layers}_b{block_size}", 32, 8, 128,
                     block_size, nb, n_layers, ops, list(range(num_seqs)), seed)
+
+
+# ----------------------------------------------------------------------------
+# Token data: a deterministic function of (seed, kind, layer, index), so that
+# each side can draw exactly the tensors it needs.
+# ----------------------------------------------------------------------------
+
+def _mix(seed, kind, a, b):
+    return (int(seed) * 1000003 + kind * 7919 + int(a) * 104729 + int(b) * 15485863) % (1 << 62)
+
+
+def _normal(shape, seed, device):
+    if str(device) == "cpu":
+        return bf16_normal(shape, seed)
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    return torch.randn(*shape, generator=g, dtype=torch.float32, device=device).to(torch.bfloat16)
+
+
+def prefill_kv(seed, layer, seq, n_tokens, n_kv_heads, d_head, device="cpu"):
+    """Keys and values [n_tokens, n_kv_heads, d_head] of a sequence's prompt
+    in one layer."""
+    k = _normal((n_tokens, n_kv_heads, d_head), _mix(seed, 1, layer, seq), device)
+    v = _normal((n_tokens, n_kv_heads, d_head), _mix(seed, 2, layer, seq), device)
+    return k, v
+
+
+def append_kv(seed, layer, step, n_tokens, n_kv_heads, d_head, device="cpu"):
+    """Keys and values of the n_tokens positions appended in engine step
+    `step` (one per appending sequence, in operation order)."""
+    k = _normal((n_tokens, n_kv_heads, d_head), _mix(seed, 3, layer, step), device)
+    v = _normal((n_tokens, n_kv_heads, d_head), _mix(seed, 4, layer, step), device)
+    return k, v
+
+
+def decode_q(seed, layer, num_seqs, n_q_heads, d_head, device="cpu"):
+    """Queries [num_seqs, n_q_heads, d_head] of one decode step in one layer."""
+    return _normal((num_seqs, n_q_heads, d_head), _mix(seed, 5, layer, 0), device)

@@ -116,7 +116,7 @@ def test_os_analogue_slot_arithmetic():
     assert phys * e["page_size"] + off == e["physical_address"]
     k = np.zeros((10, 1, e["page_size"], 1), dtype=np.uint16)
     row = np.array([[7]], dtype=np.uint16)
-    k2, _ = C.reshape_and_cache(k, k, row[None], row[None], [e["physical_address"]], e["page_size"])
+    k2, _ = C.reshape_and_cache(k.copy(), k.copy(), row[None], row[None], [e["physical_address"]], e["page_size"])
     assert k2[e["frame"], 0, e["offset"], 0] == 7 and int(k2.sum()) == 7
 
 
@@ -316,7 +316,7 @@ def test_reshape_and_cache_writes_only_its_slots():
     kn = rng.integers(0, 1 << 16, size=(4, H, D), dtype=np.uint16)
     vn = rng.integers(0, 1 << 16, size=(4, H, D), dtype=np.uint16)
     slots = [5, -1, 23, 0]
-    k2, v2 = C.reshape_and_cache(k, v, kn, vn, slots, B)
+    k2, v2 = C.reshape_and_cache(k.copy(), v.copy(), kn, vn, slots, B)
     touched = np.zeros((NB, B), dtype=bool)
     for t, s in enumerate(slots):
         if s < 0:
@@ -334,7 +334,7 @@ def test_copy_blocks_cow_trace_payload():
     rng = np.random.default_rng(8)
     layers = [rng.integers(0, 1 << 16, size=(16, 2, 16, 4), dtype=np.uint16) for _ in range(3)]
     vlayers = [rng.integers(0, 1 << 16, size=(16, 2, 16, 4), dtype=np.uint16) for _ in range(3)]
-    k2, v2 = C.copy_blocks(layers, vlayers, [[12, 13]])
+    k2, v2 = C.copy_blocks([x.copy() for x in layers], [x.copy() for x in vlayers], [[12, 13]])
     for l in range(3):
         assert np.array_equal(k2[l][13, :, :3], layers[l][12, :, :3])
         assert np.array_equal(k2[l][13], layers[l][12]) and np.array_equal(v2[l][13], vlayers[l][12])
