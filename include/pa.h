@@ -156,6 +156,41 @@ int pa_lse_merge(void* out, int out_dtype, const float* part_max,
                  const int32_t* context_lens, int partition_size, int max_parts,
                  int num_seqs, int n_q_heads, int d_head, void* stream);
 
+/* pa_decode without a caller-supplied workspace.  The pages have no
+ * counterpart of this entry point; it exists for callers that cannot hand the
+ * library device memory: code that runs where cudaMalloc is not allowed or
+ * not wanted (inside an allocator callback, in a process whose memory pool is
+ * fixed up front, or in a host framework that owns every device allocation
+ * and offers no scratch buffer).  Arguments and results are those of
+ * pa_decode minus workspace/workspace_bytes; the split path keeps its
+ * partition statistics in a static device array of PA_STATIC_SCRATCH_BYTES
+ * bytes that the library itself declares, so this call never allocates.
+ *  - The array is part of the library's device image: every GPU that loads
+ *    the library holds PA_STATIC_SCRATCH_BYTES of it until the process exits.
+ *  - Problems whose pa_decode_workspace_size(...) exceeds
+ *    PA_STATIC_SCRATCH_BYTES are rejected with PA_ERR_WORKSPACE before
+ *    anything is launched.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps whatever the last call left
+ *    there.  Nothing in it needs to start at zero: every value the merge
+ *    reads was written earlier in the same call.  Calls whose kernels
+ *    overlap on the GPU (other streams, other host threads) race on it; order
+ *    them on one stream.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u << 20)
+
+int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
+                             const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables,
+                             const int32_t* context_lens, int block_size,
+                             float scale, int n_q_heads, int n_kv_heads,
+                             int d_head, int num_seqs, int max_blocks_per_seq,
+                             int num_blocks, int max_context_len,
+                             int partition_size, int32_t* status_dev,
+                             void* stream);
+
 /* ===========================================================================
  * Cache writes
  * ===========================================================================

@@ -64,6 +64,8 @@ _SIGS = {
     "pa_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_int, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
+    "pa_decode_static_scratch": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_int, _c_int,
+                                          _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "pa_lse_merge": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                       _vp]),
@@ -197,6 +199,36 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, block_size, 
                         int(k_cache.shape[0]), int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
                         _opt_dev(status, torch.int32, "status"), _stream(stream))
     return _check(st, "pa_decode")
+
+
+PA_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def pa_decode_static_scratch(out, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, n_q_heads,
+                             n_kv_heads, d_head, max_context_len, partition_size=0, status=None, stream=None):
+    """pa_decode for callers that cannot supply device scratch memory: the
+    library keeps the split path's partition statistics in its own static
+    device array (PA_STATIC_SCRATCH_BYTES) and allocates nothing.  Larger
+    problems raise PAError(PA_ERR_WORKSPACE).  Calls share that array, so
+    calls running at the same time on the GPU must not overlap."""
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("out must be bfloat16 or float32")
+    num_seqs = q.shape[0]
+    if tuple(q.shape) != (num_seqs, n_q_heads, d_head) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("q/out must be [num_seqs, n_q_heads, d_head]")
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (n_kv_heads, block_size, d_head) or \
+            k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, n_kv_heads, block_size, d_head]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or context_lens.shape != (num_seqs,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks], context_lens [num_seqs]")
+    out_dtype = PA_DTYPE_F32 if out.dtype == torch.float32 else PA_DTYPE_BF16
+    st = _lib.pa_decode_static_scratch(
+        _dev(out, out.dtype, "out"), out_dtype, _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
+        _dev(context_lens, torch.int32, "context_lens"), int(block_size), float(scale), int(n_q_heads),
+        int(n_kv_heads), int(d_head), int(num_seqs), int(block_tables.shape[1]), int(k_cache.shape[0]),
+        int(max_context_len), int(partition_size), _opt_dev(status, torch.int32, "status"), _stream(stream))
+    return _check(st, "pa_decode_static_scratch")
 
 
 def pa_lse_merge(out, part_max, part_sum, part_acc, context_lens, partition_size, stream=None):

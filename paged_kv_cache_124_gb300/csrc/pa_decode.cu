@@ -649,3 +649,56 @@ int pa_lse_merge(void* out, int out_dtype, const float* part_max, const float* p
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// pa_decode for callers that cannot provide device scratch memory.
+//
+// The split path's partition statistics live in this file-scope device
+// array instead of a caller workspace.  Host code must not use the name
+// `g_static_scratch` as an address (on the host it is only a stand-in
+// symbol); the device address is looked up once per device with
+// cudaGetSymbolAddress and cached.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+static __device__ __align__(256) uint8_t g_static_scratch[PA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxScratchDevices] = {nullptr};
+
+// Device address of g_static_scratch on the current device (looked up on the
+// first call for that device).  Returns nullptr on failure.
+void* static_scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return nullptr;
+        g_scratch_addr[dev] = ptr;
+    }
+    return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" int pa_decode_static_scratch(void* out, int out_dtype, const void* q, const void* k_cache,
+                                        const void* v_cache, const int32_t* block_tables,
+                                        const int32_t* context_lens, int block_size, float scale, int n_q_heads,
+                                        int n_kv_heads, int d_head, int num_seqs, int max_blocks_per_seq,
+                                        int num_blocks, int max_context_len, int partition_size,
+                                        int32_t* status_dev, void* stream) {
+    const size_t need = pa_decode_workspace_size(num_seqs, n_q_heads, d_head, max_context_len, partition_size);
+    if (need > PA_STATIC_SCRATCH_BYTES) return PA_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if (need > 0) {
+        scratch = static_scratch_address();
+        if (!scratch) return PA_ERR_CUDA;
+    }
+    return pa_decode(out, out_dtype, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, n_q_heads,
+                     n_kv_heads, d_head, num_seqs, max_blocks_per_seq, num_blocks, max_context_len, partition_size,
+                     scratch, need, status_dev, stream);
+}
