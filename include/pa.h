@@ -90,12 +90,13 @@ const char* pa_status_string(int status);
  * row.  The token this step appended is part of the context: context_lens
  * counts it.
  *
- * Long contexts are split into partitions of partition_size positions that
- * are processed by different thread blocks; each writes its partial
- * maximum m, weight sum z and unnormalised weighted value sum u (the
- * statistics of [P2] section 11) to `workspace`, and a second kernel merges
- * them exactly (the "secondary reduction" of [P1] section 13).  A sequence
- * that fits one partition is finished by the first kernel directly.
+ * Each sequence is split into partitions of partition_size positions, one
+ * thread block per (sequence, group of up to 8 query heads, partition).  A
+ * sequence that fits one partition is finished by its block.  Otherwise
+ * every block leaves its partition's maximum m, weight sum z and
+ * unnormalised weighted value sum u (the statistics of [P2] section 11) in
+ * `workspace`, and a second kernel merges them exactly (the "secondary
+ * reduction" of [P1] section 13).
  *
  * Arguments
  *   out           device [num_seqs][n_q_heads][d_head], PA_DTYPE_BF16 (round
@@ -108,23 +109,25 @@ const char* pa_status_string(int status);
  *                 row s are read.
  *   context_lens  device int32 [num_seqs].
  *   scale         score scale, normally 1 / sqrt(d_head).
- *   max_context_len  host upper bound on every context_lens[s]; it sizes the
- *                 launch grid.  Larger device values are clamped to it and
- *                 flagged with PA_DEV_BAD_CONTEXT.
- *   partition_size   positions per partition: 0 picks the library default
- *                 (pa_decode_default_partition_size); otherwise a multiple
- *                 of 64 in [64, 8192].
+ *   max_context_len  host upper bound on every context_lens[s].  Larger
+ *                 device values are clamped to it and flagged with
+ *                 PA_DEV_BAD_CONTEXT.
+ *   partition_size   positions per partition: 0 lets the library choose
+ *                 from the batch shape and the device (256 to 1024), else a
+ *                 multiple of 64 in [64, 8192].
  *   workspace     device scratch of at least pa_decode_workspace_size(...)
- *                 bytes, 256-byte aligned; may be NULL (with bytes 0) when
- *                 max_context_len <= the partition size.  Its contents are
- *                 not preserved across calls; calls that share a workspace
- *                 must be stream-ordered.
+ *                 bytes (same arguments, same current device), 256-byte
+ *                 aligned; may be NULL (bytes 0) when that size is 0 (every
+ *                 sequence fits one partition).  Nothing in it needs to be
+ *                 initialised; its contents are not preserved across calls,
+ *                 and calls that share a workspace must be stream-ordered.
  *   status_dev    optional device int32, see PA_DEV_* above.
  * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED,
  * PA_ERR_WORKSPACE or PA_ERR_CUDA (launch failure).
  */
-int pa_decode_default_partition_size(int max_context_len);
-
+/* Workspace bytes pa_decode needs for these sizes on the current device
+ * (the default partition size depends on the device's SM count); 0 when no
+ * sequence can span more than one partition. */
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int d_head,
                                 int max_context_len, int partition_size);
 
@@ -143,7 +146,7 @@ int pa_decode(void* out, int out_dtype, const void* q,
  * over partitions p = 0 .. ceil(context_lens[s] / partition_size) - 1 of each
  * (sequence s, query head g).  m is in the units of the scores themselves
  * (natural-log domain).  This is the second kernel of pa_decode, exposed so
- * that partition statistics from any source can be merged.
+ * that partition statistics from any source can be merged; d_head <= 256.
  *   part_max, part_sum  device f32 [num_seqs][n_q_heads][max_parts]
  *   part_acc            device f32 [num_seqs][n_q_heads][max_parts][d_head]
  *   context_lens        device int32 [num_seqs]; partitions counted as above,

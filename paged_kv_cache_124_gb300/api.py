@@ -60,7 +60,6 @@ class AllocStats(ctypes.Structure):
 _SIGS = {
     "pa_version": (ctypes.c_char_p, []),
     "pa_status_string": (ctypes.c_char_p, [_c_int]),
-    "pa_decode_default_partition_size": (_c_int, [_c_int]),
     "pa_decode_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_decode": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_int, _c_int, _c_int,
                            _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
@@ -150,10 +149,6 @@ def _stream(stream):
 # ----------------------------------------------------------------------------
 # kernels
 # ----------------------------------------------------------------------------
-
-def pa_decode_default_partition_size(max_context_len):
-    return int(_lib.pa_decode_default_partition_size(int(max_context_len)))
-
 
 def pa_decode_workspace_size(num_seqs, n_q_heads, d_head, max_context_len, partition_size=0):
     return int(_lib.pa_decode_workspace_size(num_seqs, n_q_heads, d_head, max_context_len, partition_size))

@@ -1,5 +1,5 @@
-// Shared device helpers: mbarrier + bulk-copy PTX wrappers, bf16 unpacking,
-// argument checks.  Used by the kernels of this library only.
+// Shared device helpers: mbarrier PTX wrappers, bf16 unpacking, argument
+// checks.  Used by the kernels of this library only.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -11,7 +11,7 @@
 namespace pa {
 
 // ---------------------------------------------------------------------------
-// mbarrier (shared::cta) and 1-D bulk async copy global -> shared
+// mbarrier (shared::cta)
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -59,17 +59,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return pol;
 }
 
-// cp.async.bulk: `bytes` (multiple of 16) from global `src` (16-B aligned)
-// to shared `dst` (16-B aligned); completion is counted on `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                         uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;"
-        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // bf16 helpers
 // ---------------------------------------------------------------------------
@@ -105,6 +94,9 @@ inline cudaError_t ensure_smem_attr(K kernel, int bytes, int* done_mask_by_devic
     if (e != cudaSuccess) return e;
     if (dev < 64 && (done_mask_by_device[dev] >= bytes)) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && dev < 64) done_mask_by_device[dev] = bytes;
     return e;
 }

@@ -7,48 +7,67 @@
 // position j lives in physical block block_table[j / B] at offset j % B.
 //
 // How (GB300 design):
-//  * One thread block (4 warps) per (sequence, KV head [, head sub-group],
-//    partition of partition_size positions).  All query heads of the GQA
-//    group (up to 4 per block) are computed from the same K/V bytes, so the
-//    cache is read once per KV head.
-//  * Each warp owns a ring of kStages shared-memory stages.  A stage holds
-//    16 positions of K and of V (16 x d_head bf16 each), brought in by 1-D
-//    bulk async copies (cp.async.bulk, the TMA engine's untiled form) of the
-//    contiguous rows of the physical block(s) the block table points to,
-//    counted on an mbarrier.  The ring keeps several copies in flight per
-//    warp while the warp computes on an earlier stage.
-//  * Scores: 8 lanes per position, 4 positions per pass, fp32 products with
-//    packed (f32x2) FMAs, reduce-scatter over the 8 lanes with shuffles.
-//    Softmax: online, fp32, running maximum per head in the log2 domain,
-//    lane-local running sums merged once at the end.
-//  * Weighted values: d_head/8 lanes per position row, each lane owns 8
-//    dimensions for every head of the group; rows are merged once at the end.
-//  * The 4 warps' states are merged exactly in shared memory.  A sequence
-//    that fits one partition is normalised and written directly; otherwise
-//    (m, z, u) go to the workspace and lse_merge_kernel finishes them
-//    ("secondary reduction", section 13 of the first page; statistics of
-//    section 11 of the second).
+//  * Work is cut into tiles of 16 positions of one (sequence, KV head).  A
+//    warp consumes tiles from a ring of shared-memory stages it owns; each
+//    stage holds the tile's K and V rows, brought in by TMA tensor copies
+//    (cp.async.bulk.tensor over a 2-D view of the cache as rows of d_head,
+//    boxes of 64 columns x 16 rows -- 8 rows for 8-position blocks -- with
+//    128-byte swizzle) addressed through the block table and counted on an
+//    mbarrier.  Lane 0 refills a stage as soon as the warp is done with it.
+//  * All query heads of a GQA group (up to 8) are computed from the same K/V
+//    bytes: the cache is read once per KV head.
+//  * Both contractions of a tile run on the tensor pipe with warp-level
+//    mma.m16n8k16 (bf16 in, fp32 accumulate): S[16 x 8 heads] = K . Q^T,
+//    then O^T[d_head x 8] += V^T . P^T.  The ncu profile of the CUDA-core
+//    form of this kernel showed it issue- and latency-bound (about 800
+//    instructions per tile at 48% issue efficiency, DRAM 72% busy); the MMA
+//    form needs about 150.
+//  * Softmax is online, in fp32, with a running maximum per head in the log2
+//    domain.  P enters P.V as two bf16 terms (hi + lo), which keeps its
+//    rounding near 2^-17 relative instead of bf16's 2^-9.
+//  * One thread block of 4 warps per (sequence, head group, partition of
+//    partition_size positions); the hardware hands blocks to SMs as others
+//    finish, which balances ragged batches.  The 4 warps of a block are
+//    merged in shared memory; a sequence that fits one partition is written
+//    directly.  Otherwise each block leaves its partition's statistics
+//    (m, z, u) in the workspace and lse_merge_kernel -- launched as a
+//    programmatic dependent so that its launch overlaps the first kernel's
+//    drain -- merges them: the exact block merge of the second page,
+//    section 11, as the "secondary reduction kernel" of the first page,
+//    section 13.
 
+#include <cuda.h>            // CUtensorMap and its enums (types only)
+#include <cudaTypedefs.h>    // PFN_cuTensorMapEncodeTiled
 #include <math.h>
+
+#include <mutex>
 
 #include "pa_common.cuh"
 
 namespace {
 
+#ifndef PA_DECODE_STAGES
+#define PA_DECODE_STAGES 2         // stages per warp ring
+#endif
+#ifndef PA_DECODE_MIN_BLOCKS
+#define PA_DECODE_MIN_BLOCKS 3     // resident thread blocks per SM the kernels are built for
+#endif
+
 constexpr int kTile = 16;          // positions per stage
 constexpr int kWarps = 4;          // warps per thread block
-constexpr int kStages = 3;         // stages per warp ring
+constexpr int kStages = PA_DECODE_STAGES;
 constexpr int kThreads = kWarps * 32;
+constexpr int kHeads = 8;          // query heads per MMA (the n = 8 of m16n8k16)
 constexpr int kMaxProbes = 2000000;   // ~2 s bound on any single wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxPartition = 8192;
+constexpr int kMergeChunk = 1024;  // partitions whose weights are staged at once by the merging block
 
+// Arguments shared by both schedules.
 struct DecodeArgs {
     void* out;
     const __nv_bfloat16* q;
-    const __nv_bfloat16* k_cache;
-    const __nv_bfloat16* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
     float* part_max;
@@ -62,29 +81,24 @@ struct DecodeArgs {
     int n_q_heads;
     int n_kv_heads;
     int group;               // G = n_q_heads / n_kv_heads
-    int n_sub;               // G / (heads per thread block)
+    int heads_per_block;     // hpb = min(G, 8): query heads computed per K/V read
+    int n_sub;               // G / hpb
     int max_blocks_per_seq;
     int num_blocks;
     int ctx_cap;             // min(max_blocks_per_seq * B, max_context_len)
+    int num_seqs;
     int partition_size;
     int max_parts;
 };
 
 template <int D>
 struct Geo {
-    static constexpr int kRowBytes = D * 2;
-    static constexpr int kTileBytes = kTile * kRowBytes;           // K or V
+    static constexpr int kHalves = D / 64;                // 64-column (128-byte) boxes per row
+    static constexpr int kBoxBytes = kTile * 128;         // one swizzled 16 x 128-byte region
+    static constexpr int kTileBytes = kHalves * kBoxBytes;   // K or V of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
-    static constexpr int kQkChunks = D / 64;      // 16-B chunks per lane per row
-    static constexpr int kPvLanes = D / 8;        // lanes per value row
-    static constexpr int kPvRows = 32 / kPvLanes; // rows per pass
-    static constexpr int kPvPasses = kTile / kPvRows;
-};
-
-template <int GP>
-struct Own {                                      // scores a lane keeps
-    static constexpr int kN = GP >= 2 ? GP / 2 : 1;
+    static constexpr int kSteps = D / 16;                 // k-steps of S, m-tiles of O^T
 };
 
 __device__ __forceinline__ void store_out(void* out, int f32, size_t i, float v) {
@@ -94,169 +108,296 @@ __device__ __forceinline__ void store_out(void* out, int f32, size_t i, float v)
         static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
 }
 
-__device__ __forceinline__ void unpack8(const uint4& w, float2 (&f)[4]) {
-    f[0] = pa::bf16x2_to_float2(w.x);
-    f[1] = pa::bf16x2_to_float2(w.y);
-    f[2] = pa::bf16x2_to_float2(w.z);
-    f[3] = pa::bf16x2_to_float2(w.w);
+__device__ __forceinline__ float fast_exp2(float x) {      // 2^x; 2^-inf = +0
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// Sum `v` (N values per lane) over the 8 lanes that share lane >> 3, leaving
-// each lane with N/8 of the sums (at least one).  Value index after the call
-// for lane bits b2 b1 b0 (of lane & 7): see owned_pass / owned_head.
-template <int N>
-__device__ __forceinline__ void reduce_scatter8(float (&v)[N], int lane) {
-    constexpr int H1 = N / 2 > 0 ? N / 2 : 1;
-    constexpr int H2 = H1 / 2 > 0 ? H1 / 2 : 1;
-    constexpr int H3 = H2 / 2 > 0 ? H2 / 2 : 1;
-    // step xor 4
-    if (N >= 2) {
-        const bool hi = lane & 4;
-#pragma unroll
-        for (int k = 0; k < H1; ++k) {
-            float send = hi ? v[k] : v[k + H1];
-            float keep = hi ? v[k + H1] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-    } else {
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
-    }
-    // step xor 2
-    if (H1 >= 2) {
-        const bool hi = lane & 2;
-#pragma unroll
-        for (int k = 0; k < H2; ++k) {
-            float send = hi ? v[k] : v[k + H2];
-            float keep = hi ? v[k + H2] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-        }
-    } else {
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-    }
-    // step xor 1
-    if (H2 >= 2) {
-        const bool hi = lane & 1;
-#pragma unroll
-        for (int k = 0; k < H3; ++k) {
-            float send = hi ? v[k] : v[k + H3];
-            float keep = hi ? v[k + H3] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-        }
-    } else {
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-    }
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a region the
+// TMA wrote with 128-byte swizzle (region base 1024-byte aligned): the chunk
+// index is XOR-ed with the row index modulo 8.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D, int GP>
-__global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const DecodeArgs a) {
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// D[16 x 8] += A[16 x 16] . B[16 x 8], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(pa::smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+        "r"(pa::smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Enqueue the TMA copies of one tile (16 positions of one KV head) into a
+// stage: K and V rows of block blk0 from offset off0 (and, for 8-position
+// blocks, the next 8 rows from block blk1).  Returns nothing; the stage's
+// barrier expects exactly the bytes issued.  Boxes are always full: rows
+// past the context come along and are masked in the math.
+template <int D>
+__device__ __forceinline__ void issue_tile(uint8_t* stage, uint64_t* bar, const CUtensorMap* mk,
+                                           const CUtensorMap* mv, int blk0, int blk1, int off0, int nv, int kvh,
+                                           const DecodeArgs& a, uint64_t policy) {
     using G = Geo<D>;
-    constexpr int NO = Own<GP>::kN;
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* ring = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::kRingBytes);
-    float* probs = reinterpret_cast<float*>(bars + kWarps * kStages);    // [warp][pos][GP]
-    int32_t* table = reinterpret_cast<int32_t*>(probs + kWarps * kTile * GP);
+    const int B = a.block_size;
+    const int box_rows = B < kTile ? B : kTile;
+    const int n_rows = (nv + box_rows - 1) / box_rows;          // 1, or 2 for 8-position blocks
+    pa::mbar_arrive_expect_tx(bar, (uint32_t)(2 * G::kHalves * n_rows * box_rows * 128));
+    for (int r = 0; r < n_rows; ++r) {
+        int blk = r == 0 ? blk0 : blk1;
+        if (blk < 0 || blk >= a.num_blocks) {
+            pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            blk = 0;
+        }
+        const int row = (blk * a.n_kv_heads + kvh) * B + (r == 0 ? off0 : 0);
+#pragma unroll
+        for (int h = 0; h < G::kHalves; ++h) {
+            uint8_t* dst = stage + h * G::kBoxBytes + r * box_rows * 128;
+            tma_load_2d(dst, mk, h * 64, row, bar, policy);
+            tma_load_2d(dst + G::kTileBytes, mv, h * 64, row, bar, policy);
+        }
+    }
+}
+
+// Per-warp running state of one (unit, range): heads h0 = 2 t4, h1 = 2 t4 + 1
+// of the 8-head MMA group, lane-local sums, and O^T in the MMA C layout
+// (acc[m] = O^T rows 16 m + g and 16 m + g + 8, columns h0 and h1).
+template <int D>
+struct WarpState {
+    float m0, m1, l0, l1;
+    float acc[Geo<D>::kSteps][4];
+
+    __device__ __forceinline__ void reset() {
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < Geo<D>::kSteps; ++m) acc[m][0] = acc[m][1] = acc[m][2] = acc[m][3] = 0.f;
+    }
+
+    // Sum the lane-local l over the 8 lanes of a column group.
+    __device__ __forceinline__ void finish_sums() {
+#pragma unroll
+        for (int msk = 4; msk <= 16; msk <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, msk);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, msk);
+        }
+    }
+};
+
+// Fold one tile (stage at shared addresses ks / vs, nv valid positions) into
+// the warp's state.  qb: q as the B operand of S = K . Q^T.
+template <int D>
+__device__ __forceinline__ void consume_tile(WarpState<D>& st, uint32_t ks, uint32_t vs, int nv,
+                                             const uint32_t (&qb)[Geo<D>::kSteps][2], float scale_log2, int lane) {
+    using G = Geo<D>;
+    const int g = lane >> 2, t4 = lane & 3, mi = lane >> 3;
+    // ldmatrix lane addressing (see swz): for S the lanes of matrix mi point at
+    // K rows (mi & 1) * 8 + lane % 8, chunk +(mi >> 1); for O^T they point at V
+    // rows (mi >> 1) * 8 + lane % 8, chunk +(mi & 1).
+    const int k_row = ((mi & 1) << 3) + (lane & 7), k_cadd = mi >> 1;
+    const int v_row = ((mi >> 1) << 3) + (lane & 7), v_cadd = mi & 1;
+
+    // ---- S = K . Q^T (two accumulators for a shorter dependency chain) ----
+    float s_a[4] = {0.f, 0.f, 0.f, 0.f}, s_b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < G::kSteps; ++kk) {
+        uint32_t af[4];
+        ldsm_x4(ks + (kk >> 2) * G::kBoxBytes + swz(k_row, 2 * (kk & 3) + k_cadd), af);
+        if (kk & 1)
+            mma16816(s_b, af, qb[kk][0], qb[kk][1]);
+        else
+            mma16816(s_a, af, qb[kk][0], qb[kk][1]);
+    }
+    // s[0]: (position g, head h0), s[1]: (g, h1), s[2]: (g + 8, h0), s[3]: (g + 8, h1)
+    float s[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = (s_a[i] + s_b[i]) * scale_log2;
+    if (g >= nv) s[0] = s[1] = -INFINITY;          // positions past the context
+    if (g + 8 >= nv) s[2] = s[3] = -INFINITY;
+
+    // ---- online softmax -------------------------------------------------------
+    float b0 = fmaxf(s[0], s[2]), b1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int msk = 4; msk <= 16; msk <<= 1) {
+        b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, msk));
+        b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, msk));
+    }
+    const float n0 = fmaxf(st.m0, b0), n1 = fmaxf(st.m1, b1);
+    const float al0 = fast_exp2(st.m0 - n0), al1 = fast_exp2(st.m1 - n1);
+    st.m0 = n0;
+    st.m1 = n1;
+    const float p0 = fast_exp2(s[0] - n0), p1 = fast_exp2(s[1] - n1);
+    const float p2 = fast_exp2(s[2] - n0), p3 = fast_exp2(s[3] - n1);
+    st.l0 = st.l0 * al0 + (p0 + p2);
+    st.l1 = st.l1 * al1 + (p1 + p3);
+#pragma unroll
+    for (int m = 0; m < G::kSteps; ++m) {
+        st.acc[m][0] *= al0;
+        st.acc[m][1] *= al1;
+        st.acc[m][2] *= al0;
+        st.acc[m][3] *= al1;
+    }
+
+    // ---- P^T as the B operand, split into bf16 hi + lo -------------------------
+    const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+    const float2 f01 = pa::bf16x2_to_float2(h01), f23 = pa::bf16x2_to_float2(h23);
+    const uint32_t l01 = pack_bf16(p0 - f01.x, p1 - f01.y), l23 = pack_bf16(p2 - f23.x, p3 - f23.y);
+    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+    const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+
+    // ---- O^T += V^T . P^T --------------------------------------------------------
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;      // zero V rows past the context
+    if (nv < kTile) {
+        const int t = 2 * t4;
+        mlo = (t < nv ? 0x0000ffffu : 0u) | (t + 1 < nv ? 0xffff0000u : 0u);
+        mhi = (t + 8 < nv ? 0x0000ffffu : 0u) | (t + 9 < nv ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int m = 0; m < G::kSteps; ++m) {
+        uint32_t af[4];
+        ldsm_x4_trans(vs + (m >> 2) * G::kBoxBytes + swz(v_row, 2 * (m & 3) + v_cadd), af);
+        af[0] &= mlo;
+        af[1] &= mlo;
+        af[2] &= mhi;
+        af[3] &= mhi;
+        mma16816(st.acc[m], af, bh0, bh1);
+        mma16816(st.acc[m], af, bl0, bl1);
+    }
+}
+
+// q of query heads [qh0, qh0 + hpb) of one sequence as the B operand of
+// S = K . Q^T: lane holds q[head g][16 k + 2 t4 + {0,1}] and
+// q[head g][16 k + 8 + 2 t4 + {0,1}]; heads past hpb are zero.
+template <int D>
+__device__ __forceinline__ void load_q(uint32_t (&qb)[Geo<D>::kSteps][2], const __nv_bfloat16* qrow0, int hpb,
+                                       int lane) {
+    const int g = lane >> 2, t4 = lane & 3;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qrow0 + (size_t)(g < hpb ? g : 0) * D);
+#pragma unroll
+    for (int k = 0; k < Geo<D>::kSteps; ++k) {
+        qb[k][0] = g < hpb ? qrow[8 * k + t4] : 0u;
+        qb[k][1] = g < hpb ? qrow[8 * k + 4 + t4] : 0u;
+    }
+}
+
+// Every lane waits for the stage itself (visibility of the async copies);
+// the decision to give up is warp-uniform.  On a timeout the status is
+// flagged and the warp's other stages are given a short bounded wait.
+__device__ __forceinline__ bool wait_stage(uint64_t* bars, int k, int lane, int32_t* status) {
+    const bool ok = __all_sync(0xffffffffu, pa::mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1, kMaxProbes));
+    if (!ok) {
+        if (lane == 0) pa::set_status(status, PA_DEV_WAIT_TIMEOUT);
+        for (int kk = k + 1; kk < k + kStages; ++kk) pa::mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, 1000);
+    }
+    return ok;
+}
+
+// ============================================================================
+// Fixed partitions: one thread block per (sequence, head group, partition)
+// ============================================================================
+template <int D>
+__global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
+    decode_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                            const DecodeArgs a) {
+    using G = Geo<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + G::kRingBytes);
+    int32_t* table = reinterpret_cast<int32_t*>(bars + kWarps * kStages);
 
     const int part = blockIdx.x;
     const int seq = blockIdx.z;
     const int kvh = blockIdx.y / a.n_sub;
-    const int qh0 = kvh * a.group + (blockIdx.y % a.n_sub) * GP;
+    const int hpb = a.heads_per_block;
+    const int qh0 = kvh * a.group + (blockIdx.y % a.n_sub) * hpb;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    int ctx = a.context_lens[seq];
-    if (ctx < 0 || ctx > a.ctx_cap) {
-        if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
-        ctx = ctx < 0 ? 0 : a.ctx_cap;
-    }
-    const int P = a.partition_size;
-    const int nparts = (ctx + P - 1) / P;
-    if (part >= (nparts > 0 ? nparts : 1)) return;
-    const size_t row0 = ((size_t)seq * a.n_q_heads + qh0) * D;   // q / out offset
-    if (ctx == 0) {
-        for (int i = threadIdx.x; i < GP * D; i += kThreads) store_out(a.out, a.out_f32, row0 + i, 0.f);
-        return;
-    }
-
+    // Independent loads first: the context length, a speculative slice of the
+    // block table (this partition's entries, read before the length is known)
+    // and q; one memory round trip instead of three.
     const int B = a.block_size;
-    const int t_begin = part * P;
-    const int t_end = min(t_begin + P, ctx);
-    const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
-    const int lb0 = t_begin >> a.log2_block;
-    const int n_lb = ((t_end - 1) >> a.log2_block) - lb0 + 1;
+    const int P = a.partition_size;
+    const int lb0 = (part * P) >> a.log2_block;
     const int32_t* trow = a.block_tables + (size_t)seq * a.max_blocks_per_seq;
-    for (int i = threadIdx.x; i < n_lb; i += kThreads) {
-        int b = trow[lb0 + i];
-        if (b < 0 || b >= a.num_blocks) {
-            pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
-            b = 0;
-        }
-        table[i] = b;
-    }
+    const int n_spec = max(0, min(P >> a.log2_block, a.max_blocks_per_seq - lb0));
+    int ctx = a.context_lens[seq];
+    for (int i = threadIdx.x; i < n_spec; i += kThreads) table[i] = trow[lb0 + i];
+    const size_t row0 = ((size_t)seq * a.n_q_heads + qh0) * D;   // q / out offset of the block's first head
+    uint32_t qb[G::kSteps][2];
+    load_q<D>(qb, a.q + row0, hpb, lane);
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWarps * kStages; ++i) pa::mbar_init(&bars[i], 1);
         pa::fence_mbar_init();
     }
 
-    // q of the group's heads, fp32, pre-scaled into the log2 domain; lane
-    // keeps the 8 (or 16) dimensions it multiplies in the score pass.
-    const int j8 = lane & 7;
-    float2 qf[GP][G::kQkChunks * 4];
-#pragma unroll
-    for (int h = 0; h < GP; ++h) {
-        const uint4* qrow = reinterpret_cast<const uint4*>(a.q + row0 + (size_t)h * D);
-#pragma unroll
-        for (int c = 0; c < G::kQkChunks; ++c) {
-            float2 f[4];
-            unpack8(qrow[j8 + 8 * c], f);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                qf[h][c * 4 + e] = make_float2(f[e].x * a.scale_log2, f[e].y * a.scale_log2);
-        }
+    if (ctx < 0 || ctx > a.ctx_cap) {
+        if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
+        ctx = ctx < 0 ? 0 : a.ctx_cap;
     }
+    const int nparts = (ctx + P - 1) / P;
+    if (part >= (nparts > 0 ? nparts : 1)) return;
+    if (ctx == 0) {
+        for (int i = threadIdx.x; i < hpb * D; i += kThreads) store_out(a.out, a.out_f32, row0 + i, 0.f);
+        return;
+    }
+    const int t_begin = part * P;
+    const int t_end = min(t_begin + P, ctx);
+    const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+    // Once every block has started, the merge kernel may be scheduled onto
+    // free SM slots; it waits for this grid's results before reading them.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
 
     const uint64_t policy = pa::l2_evict_first_policy();
+    uint64_t* wbars = bars + warp * kStages;
+    uint8_t* wring = ring + warp * kStages * G::kStageBytes;
     auto issue = [&](int tile, int stage) {
-        uint8_t* ks = ring + (warp * kStages + stage) * G::kStageBytes;
-        uint8_t* vs = ks + G::kTileBytes;
         const int t0 = t_begin + tile * kTile;
         const int nv = min(kTile, t_end - t0);
-        uint64_t* bar = &bars[warp * kStages + stage];
-        pa::mbar_arrive_expect_tx(bar, 2u * nv * G::kRowBytes);
-        for (int r = 0; r < nv;) {
-            const int pos = t0 + r;
-            const int off = pos & (B - 1);
-            const int rows = min(nv - r, B - off);
-            const int blk = table[(pos >> a.log2_block) - lb0];
-            const size_t src = (((size_t)blk * a.n_kv_heads + kvh) * B + off) * D;
-            pa::bulk_g2s(ks + r * G::kRowBytes, a.k_cache + src, rows * G::kRowBytes, bar, policy);
-            pa::bulk_g2s(vs + r * G::kRowBytes, a.v_cache + src, rows * G::kRowBytes, bar, policy);
-            r += rows;
-        }
+        const int e0 = (t0 >> a.log2_block) - lb0;
+        const int blk1 = (B < kTile && nv > B) ? table[e0 + 1] : 0;
+        issue_tile<D>(wring + stage * G::kStageBytes, &wbars[stage], &tmap_k, &tmap_v, table[e0], blk1,
+                      t0 & (B - 1), nv, kvh, a, policy);
     };
 
-    // ---- per-lane state -----------------------------------------------------
-    float m_run[GP];
-    float l_own[NO];
-    float2 acc[GP][4];
-#pragma unroll
-    for (int h = 0; h < GP; ++h) {
-        m_run[h] = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[h][e] = make_float2(0.f, 0.f);
-    }
-#pragma unroll
-    for (int i = 0; i < NO; ++i) l_own[i] = 0.f;
-
-    const int r4 = lane >> 3;                     // row within a score pass
-    const int b1 = lane & 1;
-    const int own_pos = (j8 >> 1) * 4 + r4;        // position of the kept scores
-    // kept heads: GP=4 -> 2*b1, 2*b1+1; GP=2 -> b1; GP=1 -> 0
-    const int pv_row = lane / G::kPvLanes;
-    const int pv_col = lane % G::kPvLanes;
-    float* pw = probs + warp * kTile * GP;
-
+    WarpState<D> st;
+    st.reset();
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k) {
@@ -264,204 +405,51 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
             if (tile < n_tiles) issue(tile, k);
         }
     }
-
     int k = 0;
     for (int tile = warp; tile < n_tiles; tile += kWarps, ++k) {
-        const int stage = k % kStages;
-        uint64_t* bar = &bars[warp * kStages + stage];
-        // every lane observes the phase itself (visibility of the async
-        // copies); the decision to give up is made warp-uniform
-        const bool landed = __all_sync(0xffffffffu, pa::mbar_wait_bounded(bar, (k / kStages) & 1, kMaxProbes));
-        if (!landed) {
-            if (lane == 0) pa::set_status(a.status, PA_DEV_WAIT_TIMEOUT);
-            // drain the other stages this warp may still have in flight
-            for (int kk = k + 1; kk < k + kStages; ++kk) {
-                const int t2 = warp + kk * kWarps;
-                if (t2 < n_tiles) pa::mbar_wait_bounded(&bars[warp * kStages + kk % kStages], (kk / kStages) & 1, 1000);
-            }
-            break;
-        }
-        const uint8_t* ks = ring + (warp * kStages + stage) * G::kStageBytes;
-        const uint8_t* vs = ks + G::kTileBytes;
-        const int nv = min(kTile, t_end - (t_begin + tile * kTile));
-
-        // ---- scores: 4 passes x 4 rows, 8 lanes per row ----------------------
-        float sc[4 * GP];
-#pragma unroll
-        for (int pass = 0; pass < 4; ++pass) {
-            const uint8_t* row = ks + (pass * 4 + r4) * G::kRowBytes;
-            float2 p2[GP];
-#pragma unroll
-            for (int h = 0; h < GP; ++h) p2[h] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int c = 0; c < G::kQkChunks; ++c) {
-                const uint4 w = *reinterpret_cast<const uint4*>(row + (j8 + 8 * c) * 16);
-                float2 kf[4];
-                unpack8(w, kf);
-#pragma unroll
-                for (int h = 0; h < GP; ++h)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) p2[h] = __ffma2_rn(qf[h][c * 4 + e], kf[e], p2[h]);
-            }
-#pragma unroll
-            for (int h = 0; h < GP; ++h) sc[pass * GP + h] = p2[h].x + p2[h].y;
-        }
-        reduce_scatter8<4 * GP>(sc, lane);
-
-        // ---- online softmax ---------------------------------------------------
-        float own[NO], bm[NO];
-#pragma unroll
-        for (int i = 0; i < NO; ++i) {
-            own[i] = own_pos < nv ? sc[i] : -INFINITY;
-            bm[i] = own[i];
-        }
-#pragma unroll
-        for (int msk = 2; msk <= 16; msk <<= 1)
-#pragma unroll
-            for (int i = 0; i < NO; ++i) bm[i] = fmaxf(bm[i], __shfl_xor_sync(0xffffffffu, bm[i], msk));
-        float bmax[GP];
-        if constexpr (GP == 4) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float other = __shfl_xor_sync(0xffffffffu, bm[i], 1);
-                bmax[i] = b1 ? other : bm[i];
-                bmax[2 + i] = b1 ? bm[i] : other;
-            }
-        } else if constexpr (GP == 2) {
-            const float other = __shfl_xor_sync(0xffffffffu, bm[0], 1);
-            bmax[0] = b1 ? other : bm[0];
-            bmax[1] = b1 ? bm[0] : other;
-        } else {
-            bmax[0] = bm[0];
-        }
-        float alpha[GP];
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-            const float mn = fmaxf(m_run[h], bmax[h]);
-            alpha[h] = exp2f(m_run[h] - mn);
-            m_run[h] = mn;
-        }
-#pragma unroll
-        for (int i = 0; i < NO; ++i) {
-            const float mh = GP == 4 ? (b1 ? m_run[2 + i] : m_run[i]) : (GP == 2 ? (b1 ? m_run[1] : m_run[0]) : m_run[0]);
-            const float al = GP == 4 ? (b1 ? alpha[2 + i] : alpha[i]) : (GP == 2 ? (b1 ? alpha[1] : alpha[0]) : alpha[0]);
-            const float p = exp2f(own[i] - mh);
-            l_own[i] = l_own[i] * al + p;
-            own[i] = p;
-        }
-        if constexpr (GP == 4) {
-            *reinterpret_cast<float2*>(pw + own_pos * 4 + 2 * b1) = make_float2(own[0], own[1]);
-        } else if constexpr (GP == 2) {
-            pw[own_pos * 2 + b1] = own[0];
-        } else {
-            if (b1 == 0) pw[own_pos] = own[0];
-        }
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-            const float2 al2 = make_float2(alpha[h], alpha[h]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[h][e] = __fmul2_rn(acc[h][e], al2);
-        }
+        if (!wait_stage(wbars, k, lane, a.status)) break;
+        const uint32_t ks = pa::smem_addr(wring + (k % kStages) * G::kStageBytes);
+        consume_tile<D>(st, ks, ks + G::kTileBytes, min(kTile, t_end - (t_begin + tile * kTile)), qb, a.scale_log2,
+                        lane);
         __syncwarp();
-
-        // ---- weighted values ------------------------------------------------
-        auto pv_row_step = [&](int pos) {
-            const uint4 w = *reinterpret_cast<const uint4*>(vs + pos * G::kRowBytes + pv_col * 16);
-            float2 vf[4];
-            unpack8(w, vf);
-            float pr[GP];
-            if constexpr (GP == 4) {
-                const float4 t = *reinterpret_cast<const float4*>(pw + pos * 4);
-                pr[0] = t.x; pr[1] = t.y; pr[2] = t.z; pr[3] = t.w;
-            } else if constexpr (GP == 2) {
-                const float2 t = *reinterpret_cast<const float2*>(pw + pos * 2);
-                pr[0] = t.x; pr[1] = t.y;
-            } else {
-                pr[0] = pw[pos];
-            }
-#pragma unroll
-            for (int h = 0; h < GP; ++h) {
-                const float2 ph = make_float2(pr[h], pr[h]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[h][e] = __ffma2_rn(ph, vf[e], acc[h][e]);
-            }
-        };
-        if (nv == kTile) {
-#pragma unroll
-            for (int pass = 0; pass < G::kPvPasses; ++pass) pv_row_step(pass * G::kPvRows + pv_row);
-        } else {
-#pragma unroll
-            for (int pass = 0; pass < G::kPvPasses; ++pass) {
-                const int pos = pass * G::kPvRows + pv_row;
-                if (pos < nv) pv_row_step(pos);    // rows past the context are never read
-            }
-        }
-        __syncwarp();
-        if (lane == 0 && tile + kWarps * kStages < n_tiles) issue(tile + kWarps * kStages, stage);
+        if (lane == 0 && tile + kWarps * kStages < n_tiles) issue(tile + kWarps * kStages, k % kStages);
     }
+    st.finish_sums();
 
-    // ---- finish the warp's state -------------------------------------------
-#pragma unroll
-    for (int msk = 2; msk <= 16; msk <<= 1)
-#pragma unroll
-        for (int i = 0; i < NO; ++i) l_own[i] += __shfl_xor_sync(0xffffffffu, l_own[i], msk);
-    float l_run[GP];
-    if constexpr (GP == 4) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, l_own[i], 1);
-            l_run[i] = b1 ? other : l_own[i];
-            l_run[2 + i] = b1 ? l_own[i] : other;
-        }
-    } else if constexpr (GP == 2) {
-        const float other = __shfl_xor_sync(0xffffffffu, l_own[0], 1);
-        l_run[0] = b1 ? other : l_own[0];
-        l_run[1] = b1 ? l_own[0] : other;
-    } else {
-        l_run[0] = l_own[0];
-    }
-#pragma unroll
-    for (int msk = G::kPvLanes; msk < 32; msk <<= 1)
-#pragma unroll
-        for (int h = 0; h < GP; ++h)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                acc[h][e].x += __shfl_xor_sync(0xffffffffu, acc[h][e].x, msk);
-                acc[h][e].y += __shfl_xor_sync(0xffffffffu, acc[h][e].y, msk);
-            }
-
-    // ---- merge the 4 warps (exact, as in the block merge) --------------------
+    // ---- merge the 4 warps (exact, as in the block merge) ----------------------
     __syncthreads();                                   // ring no longer in use
-    float* mw = reinterpret_cast<float*>(ring);        // [warp][GP]
-    float* lw = mw + kWarps * GP;                      // [warp][GP]
-    float* uw = lw + kWarps * GP;                      // [warp][GP][D]
-    if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < GP; ++h) {
-            mw[warp * GP + h] = m_run[h];
-            lw[warp * GP + h] = l_run[h];
-        }
+    float* mw = reinterpret_cast<float*>(ring);        // [warp][8]
+    float* lw = mw + kWarps * kHeads;                  // [warp][8]
+    float* uw = lw + kWarps * kHeads;                  // [warp][8][D]
+    const int g = lane >> 2, h0 = 2 * (lane & 3);
+    if (g == 0) {
+        mw[warp * kHeads + h0] = st.m0;
+        mw[warp * kHeads + h0 + 1] = st.m1;
+        lw[warp * kHeads + h0] = st.l0;
+        lw[warp * kHeads + h0 + 1] = st.l1;
     }
-    if (lane < G::kPvLanes) {
 #pragma unroll
-        for (int h = 0; h < GP; ++h)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                *reinterpret_cast<float2*>(uw + (warp * GP + h) * D + pv_col * 8 + 2 * e) = acc[h][e];
+    for (int m = 0; m < G::kSteps; ++m) {
+        float* u0 = uw + (warp * kHeads + h0) * D + 16 * m + g;
+        float* u1 = u0 + D;
+        u0[0] = st.acc[m][0];
+        u1[0] = st.acc[m][1];
+        u0[8] = st.acc[m][2];
+        u1[8] = st.acc[m][3];
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < GP * D; idx += kThreads) {
+    for (int idx = threadIdx.x; idx < hpb * D; idx += kThreads) {
         const int h = idx / D;
         const int d = idx % D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * GP + h]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * kHeads + h]);
         float Z = 0.f, U = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-            const float f = exp2f(mw[w * GP + h] - M);
-            Z += f * lw[w * GP + h];
-            U += f * uw[(w * GP + h) * D + d];
+            const float f = fast_exp2(mw[w * kHeads + h] - M);
+            Z += f * lw[w * kHeads + h];
+            U += f * uw[(w * kHeads + h) * D + d];
         }
         if (nparts == 1) {
             store_out(a.out, a.out_f32, row0 + idx, U / Z);
@@ -478,14 +466,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 
 // Exact merge of partition statistics (second page, section 11):
 // M = max m_p, Z = sum exp(m_p - M) z_p, U = sum exp(m_p - M) u_p, out = U / Z.
-// One thread block per (query head, sequence), one thread per dimension.
-__global__ void lse_merge_kernel(void* out, int out_f32, const float* __restrict__ pmax,
-                                 const float* __restrict__ psum, const float* __restrict__ pacc,
-                                 const int32_t* __restrict__ context_lens, int ctx_cap, int partition_size,
-                                 int max_parts, int n_q_heads, int d_head, int skip_single) {
+// One thread block of kThreads per (query head, sequence).  Warp 0 reduces M
+// and Z over the partitions; the weights exp(m_p - M) / Z are staged in
+// shared memory in chunks of kMergeChunk and every thread sums its dimension
+// with independent loads.  When launched as a programmatic dependent of the
+// partition kernel, it waits for that grid's results before reading them.
+__global__ void __launch_bounds__(kThreads) lse_merge_kernel(void* out, int out_f32, const float* __restrict__ pmax,
+                                                             const float* __restrict__ psum,
+                                                             const float* __restrict__ pacc,
+                                                             const int32_t* __restrict__ context_lens, int ctx_cap,
+                                                             int partition_size, int max_parts, int n_q_heads,
+                                                             int d_head, int skip_single) {
+    __shared__ float wgt[kMergeChunk];
+    __shared__ float sM, sInv;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int h = blockIdx.x;
     const int seq = blockIdx.y;
-    const int d = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int ctx = context_lens[seq];
     ctx = ctx < 0 ? 0 : (ctx > ctx_cap ? ctx_cap : ctx);
     int np = (int)(((long long)ctx + partition_size - 1) / partition_size);
@@ -493,30 +490,122 @@ __global__ void lse_merge_kernel(void* out, int out_f32, const float* __restrict
     if (skip_single && np <= 1) return;             // finished by the partition kernel
     const size_t orow = ((size_t)seq * n_q_heads + h) * d_head;
     if (np == 0) {
-        if (d < d_head) store_out(out, out_f32, orow + d, 0.f);
+        for (int d = threadIdx.x; d < d_head; d += blockDim.x) store_out(out, out_f32, orow + d, 0.f);
         return;
     }
     const size_t base = ((size_t)seq * n_q_heads + h) * max_parts;
-    float M = -INFINITY;
-    for (int p = 0; p < np; ++p) M = fmaxf(M, pmax[base + p]);
-    float Z = 0.f, U = 0.f;
-    for (int p = 0; p < np; ++p) {
-        const float w = exp2f((pmax[base + p] - M) * kLog2e);
-        Z += w * psum[base + p];
-        if (d < d_head) U += w * pacc[(base + p) * d_head + d];
+    if (warp == 0) {
+        float M = -INFINITY;
+        for (int p = lane; p < np; p += 32) M = fmaxf(M, pmax[base + p]);
+#pragma unroll
+        for (int msk = 16; msk >= 1; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, msk));
+        float Z = 0.f;
+        for (int p = lane; p < np; p += 32) Z += fast_exp2((pmax[base + p] - M) * kLog2e) * psum[base + p];
+#pragma unroll
+        for (int msk = 16; msk >= 1; msk >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, msk);
+        if (lane == 0) {
+            sM = M;
+            sInv = 1.f / Z;
+        }
     }
-    if (d < d_head) store_out(out, out_f32, orow + d, U / Z);
+    __syncthreads();
+    const float M = sM, inv = sInv;
+    float acc[2] = {0.f, 0.f};                      // d_head <= 2 * kThreads
+    for (int c0 = 0; c0 < np; c0 += kMergeChunk) {
+        const int nc = min(kMergeChunk, np - c0);
+        for (int p = threadIdx.x; p < nc; p += blockDim.x)
+            wgt[p] = fast_exp2((pmax[base + c0 + p] - M) * kLog2e) * inv;
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int d = threadIdx.x + it * blockDim.x;
+            if (d >= d_head) break;
+            const float* src = pacc + (base + c0) * d_head + d;
+            float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+            int p = 0;
+            for (; p + 3 < nc; p += 4) {
+                u0 += wgt[p] * src[(size_t)p * d_head];
+                u1 += wgt[p + 1] * src[(size_t)(p + 1) * d_head];
+                u2 += wgt[p + 2] * src[(size_t)(p + 2) * d_head];
+                u3 += wgt[p + 3] * src[(size_t)(p + 3) * d_head];
+            }
+            for (; p < nc; ++p) u0 += wgt[p] * src[(size_t)p * d_head];
+            acc[it] += (u0 + u1) + (u2 + u3);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int d = threadIdx.x + it * blockDim.x;
+        if (d < d_head) store_out(out, out_f32, orow + d, acc[it]);
+    }
 }
 
-template <int D, int GP>
-int launch_decode(const DecodeArgs& a, int num_seqs, int smem_bytes, cudaStream_t stream) {
-    static int attr_done[64] = {0};
-    auto kernel = decode_partition_kernel<D, GP>;
-    if (pa_host::ensure_smem_attr(kernel, smem_bytes, attr_done) != cudaSuccess) return PA_ERR_CUDA;
-    dim3 grid(a.max_parts, a.n_kv_heads * a.n_sub, num_seqs);
-    kernel<<<grid, kThreads, smem_bytes, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+// Launch lse_merge_kernel; as a programmatic dependent launch (its grid may
+// be set up while the previous kernel on the stream drains) when pdl is set.
+int launch_merge(bool pdl, cudaStream_t st, void* out, int out_f32, const float* pm, const float* ps, const float* pa,
+                 const int32_t* ctx, int ctx_cap, int P, int max_parts, int n_q_heads, int num_seqs, int d_head,
+                 int skip_single) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_q_heads, num_seqs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel, out, out_f32, pm, ps, pa, ctx, ctx_cap, P,
+                                             max_parts, n_q_heads, d_head, skip_single);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// 2-D view of a cache [num_blocks * n_kv_heads * B rows][d_head] bf16 with
+// boxes of 64 columns x box_rows rows and 128-byte swizzle.
+bool make_cache_map(CUtensorMap* map, const void* base, long long rows, int d_head, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)d_head, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d_head * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 64 && cached[dev]) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
+
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -526,22 +615,69 @@ int ilog2(int x) {
     return r;
 }
 
+
+// Positions per partition when the caller passes 0: enough thread blocks for
+// about two waves of 3 blocks per SM (counting 4 query heads per block), at
+// least 256 and at most 1024 positions.
+int default_partition(int num_seqs, int n_q_heads, int max_context_len) {
+    const long long work = (long long)num_seqs * n_q_heads * max_context_len;
+    const long long target = 4LL * 2 * PA_DECODE_MIN_BLOCKS * sm_count();
+    long long p = target > 0 ? (work + target - 1) / target : 1024;
+    p = (p + 63) / 64 * 64;
+    return (int)(p < 256 ? 256 : (p > 1024 ? 1024 : p));
+}
+
+// Workspace layout for max_parts partitions: part_max and part_sum
+// [S][Hq][max_parts] f32, then part_acc [S][Hq][max_parts][D] f32; every
+// section 256-byte aligned.
+size_t workspace_bytes_for(int num_seqs, int n_q_heads, int d_head, int max_parts) {
+    if (max_parts <= 1) return 0;
+    const size_t n = (size_t)num_seqs * n_q_heads * max_parts;
+    return 2 * align256(4 * n) + align256(4 * n * d_head);
+}
+
+template <typename K>
+int launch(K kernel, dim3 grid, int smem, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv,
+           const DecodeArgs& a, int* attr_done) {
+    if (pa_host::ensure_smem_attr(kernel, smem, attr_done) != cudaSuccess) return PA_ERR_CUDA;
+    kernel<<<grid, kThreads, smem, st>>>(mk, mv, a);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, void* workspace,
+        size_t workspace_bytes, cudaStream_t st) {
+    static int attr128[64] = {0}, attr64[64] = {0};
+    const int P = a.partition_size;
+    a.max_parts = (a.ctx_cap + P - 1) / P;
+    if (a.max_parts < 1) a.max_parts = 1;
+    if (a.max_parts > 1) {
+        if (!workspace || workspace_bytes < workspace_bytes_for(a.num_seqs, a.n_q_heads, d_head, a.max_parts))
+            return PA_ERR_WORKSPACE;
+        const size_t n = (size_t)a.num_seqs * a.n_q_heads * a.max_parts;
+        uint8_t* w = static_cast<uint8_t*>(workspace);
+        a.part_max = reinterpret_cast<float*>(w);
+        a.part_sum = reinterpret_cast<float*>(w + align256(4 * n));
+        a.part_acc = reinterpret_cast<float*>(w + 2 * align256(4 * n));
+    }
+    const int table_ints = P / a.block_size + 2;
+    const int smem = 1024 + kWarps * kStages * 2 * kTile * d_head * 2 + kWarps * kStages * 8 + table_ints * 4;
+    dim3 grid(a.max_parts, a.n_kv_heads * a.n_sub, a.num_seqs);
+    const int rc = d_head == 128 ? launch(decode_partition_kernel<128>, grid, smem, st, mk, mv, a, attr128)
+                                 : launch(decode_partition_kernel<64>, grid, smem, st, mk, mv, a, attr64);
+    if (rc != PA_OK || a.max_parts <= 1) return rc;
+    return launch_merge(true, st, a.out, a.out_f32, a.part_max, a.part_sum, a.part_acc, a.context_lens, a.ctx_cap, P,
+                        a.max_parts, a.n_q_heads, a.num_seqs, d_head, 1);
+}
+
 }  // namespace
 
 extern "C" {
 
-int pa_decode_default_partition_size(int max_context_len) {
-    return max_context_len > 16384 ? 1024 : 512;
-}
-
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int d_head, int max_context_len,
                                 int partition_size) {
-    if (num_seqs <= 0 || n_q_heads <= 0 || d_head <= 0 || max_context_len < 0) return 0;
-    const int P = partition_size > 0 ? partition_size : pa_decode_default_partition_size(max_context_len);
-    const size_t np = (size_t)((max_context_len + P - 1) / P);
-    if (np <= 1) return 0;
-    const size_t n = (size_t)num_seqs * n_q_heads * np;
-    return 2 * align256(n * sizeof(float)) + align256(n * d_head * sizeof(float));
+    if (num_seqs <= 0 || n_q_heads <= 0 || d_head <= 0 || max_context_len < 0 || partition_size < 0) return 0;
+    const int P = partition_size > 0 ? partition_size : default_partition(num_seqs, n_q_heads, max_context_len);
+    return workspace_bytes_for(num_seqs, n_q_heads, d_head, (max_context_len + P - 1) / P);
 }
 
 int pa_decode(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
@@ -563,17 +699,18 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_cache, cons
     if (!pa_host::aligned16(out) || !pa_host::aligned16(q) || !pa_host::aligned16(k_cache) ||
         !pa_host::aligned16(v_cache))
         return PA_ERR_MISALIGNED;
-    const int P = partition_size > 0 ? partition_size : pa_decode_default_partition_size(max_context_len);
-    if (P % 64 || P < 64 || P > kMaxPartition) return PA_ERR_INVALID_ARG;
-    const int gp = group < 4 ? group : 4;
-    const int n_sub = group / gp;
+    if (partition_size < 0 || (partition_size > 0 && (partition_size % 64 || partition_size > kMaxPartition)))
+        return PA_ERR_INVALID_ARG;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_WORKSPACE;
+    const int hpb = group < kHeads ? group : kHeads;
+    const int n_sub = group / hpb;
     if ((long long)n_kv_heads * n_sub > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    const long long cache_rows = (long long)num_blocks * n_kv_heads * block_size;
+    if (cache_rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
 
     DecodeArgs a{};
     a.out = out;
     a.q = static_cast<const __nv_bfloat16*>(q);
-    a.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-    a.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     a.status = status_dev;
@@ -584,48 +721,22 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_cache, cons
     a.n_q_heads = n_q_heads;
     a.n_kv_heads = n_kv_heads;
     a.group = group;
+    a.heads_per_block = hpb;
     a.n_sub = n_sub;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;
     const long long cap_tbl = (long long)max_blocks_per_seq * block_size;
     a.ctx_cap = (int)(cap_tbl < max_context_len ? cap_tbl : max_context_len);
-    a.partition_size = P;
-    a.max_parts = (max_context_len + P - 1) / P;
-    if (a.max_parts < 1) a.max_parts = 1;
+    a.num_seqs = num_seqs;
+    a.partition_size = partition_size > 0 ? partition_size : default_partition(num_seqs, n_q_heads, max_context_len);
 
-    if (a.max_parts > 1) {
-        const size_t need = pa_decode_workspace_size(num_seqs, n_q_heads, d_head, max_context_len, P);
-        if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-            return PA_ERR_WORKSPACE;
-        const size_t n = (size_t)num_seqs * n_q_heads * a.max_parts;
-        uint8_t* w = static_cast<uint8_t*>(workspace);
-        a.part_max = reinterpret_cast<float*>(w);
-        a.part_sum = reinterpret_cast<float*>(w + align256(n * sizeof(float)));
-        a.part_acc = reinterpret_cast<float*>(w + 2 * align256(n * sizeof(float)));
-    }
-
-    const int table_ints = P / block_size + 2;
-    auto smem_for = [&](int D, int GP) {
-        const int ring = kWarps * kStages * 2 * kTile * D * 2;
-        return ring + kWarps * kStages * 8 + kWarps * kTile * GP * 4 + table_ints * 4;
-    };
+    const int box_rows = block_size < kTile ? block_size : kTile;
+    CUtensorMap mk, mv;
+    if (!make_cache_map(&mk, k_cache, cache_rows, d_head, box_rows) ||
+        !make_cache_map(&mv, v_cache, cache_rows, d_head, box_rows))
+        return PA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int rc;
-    const int smem = smem_for(d_head, gp);
-    if (d_head == 128) {
-        rc = gp == 4 ? launch_decode<128, 4>(a, num_seqs, smem, st)
-           : gp == 2 ? launch_decode<128, 2>(a, num_seqs, smem, st)
-                     : launch_decode<128, 1>(a, num_seqs, smem, st);
-    } else {
-        rc = gp == 4 ? launch_decode<64, 4>(a, num_seqs, smem, st)
-           : gp == 2 ? launch_decode<64, 2>(a, num_seqs, smem, st)
-                     : launch_decode<64, 1>(a, num_seqs, smem, st);
-    }
-    if (rc != PA_OK || a.max_parts <= 1) return rc;
-    dim3 grid(n_q_heads, num_seqs);
-    lse_merge_kernel<<<grid, d_head, 0, st>>>(out, a.out_f32, a.part_max, a.part_sum, a.part_acc, context_lens,
-                                              a.ctx_cap, P, a.max_parts, n_q_heads, d_head, 1);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return run(a, mk, mv, d_head, workspace, workspace_bytes, st);
 }
 
 int pa_lse_merge(void* out, int out_dtype, const float* part_max, const float* part_sum, const float* part_acc,
@@ -636,16 +747,12 @@ int pa_lse_merge(void* out, int out_dtype, const float* part_max, const float* p
     if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!out || !part_max || !part_sum || !part_acc || !context_lens) return PA_ERR_INVALID_ARG;
-    if (d_head > 1024 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    if (d_head > 2 * kThreads || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(out) & 3u) || (reinterpret_cast<uintptr_t>(part_max) & 3u) ||
         (reinterpret_cast<uintptr_t>(part_sum) & 3u) || (reinterpret_cast<uintptr_t>(part_acc) & 3u))
         return PA_ERR_MISALIGNED;
-    dim3 grid(n_q_heads, num_seqs);
-    const int threads = (d_head + 31) / 32 * 32;
-    lse_merge_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-        out, out_dtype == PA_DTYPE_F32, part_max, part_sum, part_acc, context_lens, 0x7fffffff, partition_size,
-        max_parts, n_q_heads, d_head, 0);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_merge(false, static_cast<cudaStream_t>(stream), out, out_dtype == PA_DTYPE_F32, part_max, part_sum,
+                        part_acc, context_lens, 0x7fffffff, partition_size, max_parts, n_q_heads, num_seqs, d_head, 0);
 }
 
 }  // extern "C"

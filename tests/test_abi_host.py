@@ -22,12 +22,11 @@ def test_library_exports_every_declared_symbol():
     assert api.status_string(api.PA_FAIL_NO_BLOCKS).startswith("no free blocks")
 
 
-def test_workspace_size_and_default_partition():
+def test_fixed_partition_workspace_size():
     assert api.pa_decode_workspace_size(64, 32, 128, 512, 512) == 0
     n = api.pa_decode_workspace_size(64, 32, 128, 4096, 512)
     parts = 64 * 32 * 8
     assert n >= parts * 4 * 2 + parts * 128 * 4 and n % 256 == 0
-    assert api.pa_decode_default_partition_size(4096) % 64 == 0
 
 
 STATUS_MAP = {AL.OK: api.PA_OK, AL.FAIL_NO_BLOCKS: api.PA_FAIL_NO_BLOCKS, AL.ERR_INVALID_ARG: api.PA_ERR_INVALID_ARG,

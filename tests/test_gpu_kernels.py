@@ -225,8 +225,9 @@ def test_decode_host_argument_errors():
     with pytest.raises(api.PAError) as e:
         api.pa_decode(d, d, kc, kc, tb, cl, 16, 0.1, 4, 2, 64, 16, partition_size=96)
     assert e.value.status == api.PA_ERR_INVALID_ARG
+    tb256 = torch.zeros(1, 256, dtype=torch.int32, device="cuda")   # room for 4096 positions
     with pytest.raises(api.PAError) as e:
-        api.pa_decode(d, d, kc, kc, tb, cl, 16, 0.1, 4, 2, 64, 4096, partition_size=64)
+        api.pa_decode(d, d, kc, kc, tb256, cl, 16, 0.1, 4, 2, 64, 4096, partition_size=64)
     assert e.value.status == api.PA_ERR_WORKSPACE
     q3 = torch.zeros(1, 6, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(api.PAError) as e:

@@ -123,8 +123,9 @@ def test_fork_siblings_decode_identically_on_shared_prefix():
     q1 = I.decode_q(5, 0, 1, sc.n_q_heads, sc.d_head).cuda()
     q = q1.expand(8, -1, -1).contiguous()
     out = torch.empty_like(q, dtype=torch.float32)
+    ws = api.decode_workspace(8, sc.n_q_heads, sc.d_head, max_ctx)
     api.pa_decode(out, q, run.k_caches[0], run.v_caches[0], tables, ctx, sc.block_size, sc.scale,
-                  sc.n_q_heads, sc.n_kv_heads, sc.d_head, max_ctx)
+                  sc.n_q_heads, sc.n_kv_heads, sc.d_head, max_ctx, workspace=ws)
     torch.cuda.synchronize()
     o = out.cpu()
     for p in range(2):
