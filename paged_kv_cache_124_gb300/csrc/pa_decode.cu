@@ -53,8 +53,12 @@ namespace {
 #define PA_DECODE_MIN_BLOCKS 3     // resident thread blocks per SM the kernels are built for
 #endif
 
+#ifndef PA_DECODE_WARPS
+#define PA_DECODE_WARPS 4          // warps per thread block
+#endif
+
 constexpr int kTile = 16;          // positions per stage
-constexpr int kWarps = 4;          // warps per thread block
+constexpr int kWarps = PA_DECODE_WARPS;
 constexpr int kStages = PA_DECODE_STAGES;
 constexpr int kThreads = kWarps * 32;
 constexpr int kHeads = 8;          // query heads per MMA (the n = 8 of m16n8k16)
