@@ -228,9 +228,9 @@ def run_ours(args, world, rank, local):
     kc, vc = run.k_caches[0], run.v_caches[0]
     stream = torch.cuda.current_stream(dev)
     dec_bytes, write_bytes = algorithmic_bytes(sc, ctx_h, S)
-    # our kernels per step: reshape_and_cache and the decode kernel (which also
-    # merges split sequences); the ticket reset is a driver memset
-    launches_per_step = 2
+    # our kernels per step: reshape_and_cache, the partition kernel and, when a
+    # sequence can span several partitions, the merge kernel
+    launches_per_step = 2 + (1 if api.pa_decode_workspace_size(S, sc.n_q_heads, sc.d_head, max_ctx, P) else 0)
 
     def step():
         api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
@@ -313,7 +313,7 @@ def run_ours(args, world, rank, local):
                          (dec_bytes / 1e6),
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "single GPU"},
         "seqs_per_s": round(total_seqs / total_s, 1),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_partition_kernel with in-launch merge)",
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_partition_kernel + lse_merge_kernel)",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "algorithmic_bytes_per_launch": int(dec_bytes),
