@@ -15,32 +15,48 @@ constexpr int kCopyThreads = 256;
 constexpr int kMaxLayersPerLaunch = 64;
 
 // One thread block per token: K rows of all heads, then V rows of all heads.
+// The slot and the token's rows are loaded together (one memory round trip),
+// then stored.  Launched as a programmatic dependent: it waits for the work
+// before it on the stream before reading its inputs, and lets the next kernel
+// start its launch right away.
 __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const uint4* __restrict__ k,
     const uint4* __restrict__ v, const int64_t* __restrict__ slot_mapping, int n_kv_heads, int chunks_per_row,
     int block_size, long long num_slots, int32_t* status) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int t = blockIdx.x;
     const long long slot = slot_mapping[t];
-    if (slot < 0) return;                                   // padding token
-    if (slot >= num_slots) {
-        if (threadIdx.x == 0) pa::set_status(status, PA_DEV_BAD_SLOT);
-        return;
-    }
-    const long long blk = slot / block_size;
-    const int off = (int)(slot - blk * block_size);
     const int per_token = n_kv_heads * chunks_per_row;     // 16-B chunks of one token's K
+    const int total = 2 * per_token;
     const uint4* ksrc = k + (size_t)t * per_token;
     const uint4* vsrc = v + (size_t)t * per_token;
-    for (int c = threadIdx.x; c < 2 * per_token; c += blockDim.x) {
-        const bool is_v = c >= per_token;
-        const int cc = is_v ? c - per_token : c;
-        const int h = cc / chunks_per_row;
-        const int x = cc - h * chunks_per_row;
-        const size_t dst = (((size_t)blk * n_kv_heads + h) * block_size + off) * chunks_per_row + x;
-        if (is_v)
-            v_cache[dst] = vsrc[cc];
-        else
-            k_cache[dst] = ksrc[cc];
+    constexpr int R = 4;                                    // chunks in flight per thread
+    for (int c0 = threadIdx.x; c0 < total; c0 += R * blockDim.x) {
+        uint4 r[R];
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const int c = c0 + u * blockDim.x;
+            if (c < total) r[u] = c < per_token ? ksrc[c] : vsrc[c - per_token];
+        }
+        if (slot < 0) return;                               // padding token
+        if (slot >= num_slots) {
+            if (threadIdx.x == 0) pa::set_status(status, PA_DEV_BAD_SLOT);
+            return;
+        }
+        const long long blk = slot / block_size;
+        const int off = (int)(slot - blk * block_size);
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const int c = c0 + u * blockDim.x;
+            if (c >= total) break;
+            const bool is_v = c >= per_token;
+            const int cc = is_v ? c - per_token : c;
+            const int h = cc / chunks_per_row;
+            const int x = cc - h * chunks_per_row;
+            const size_t dst = (((size_t)blk * n_kv_heads + h) * block_size + off) * chunks_per_row + x;
+            (is_v ? v_cache : k_cache)[dst] = r[u];
+        }
     }
 }
 
@@ -94,11 +110,12 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* k, const void
     if (!pa_host::aligned16(k_cache) || !pa_host::aligned16(v_cache) || !pa_host::aligned16(k) ||
         !pa_host::aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
         return PA_ERR_MISALIGNED;
-    reshape_and_cache_kernel<<<num_tokens, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+    const cudaError_t e = pa_host::launch_dependent(
+        reshape_and_cache_kernel, dim3(num_tokens), dim3(128), 0, static_cast<cudaStream_t>(stream),
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<const uint4*>(k),
         static_cast<const uint4*>(v), slot_mapping, n_kv_heads, d_head / 8, block_size,
         (long long)num_blocks * block_size, status_dev);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers, const int32_t* block_pairs,

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pa.h"
 
 namespace pa {
@@ -99,6 +101,25 @@ inline cudaError_t ensure_smem_attr(K kernel, int bytes, int* done_mask_by_devic
                                  (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && dev < 64) done_mask_by_device[dev] = bytes;
     return e;
+}
+
+// Launch `kernel` as a programmatic dependent of the work before it on the
+// stream: its thread blocks may become resident while that work drains, and
+// the kernel itself executes griddepcontrol.wait before it reads any input.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                   Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace pa_host

@@ -352,6 +352,9 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // Launched as a programmatic dependent: inputs may come from the kernel
+    // before this one on the stream, so nothing is read before this wait.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Independent loads first: the context length, a speculative slice of the
     // block table (this partition's entries, read before the length is known)
     // and q; one memory round trip instead of three.
@@ -644,8 +647,8 @@ template <typename K>
 int launch(K kernel, dim3 grid, int smem, cudaStream_t st, const CUtensorMap& mk, const CUtensorMap& mv,
            const DecodeArgs& a, int* attr_done) {
     if (pa_host::ensure_smem_attr(kernel, smem, attr_done) != cudaSuccess) return PA_ERR_CUDA;
-    kernel<<<grid, kThreads, smem, st>>>(mk, mv, a);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return pa_host::launch_dependent(kernel, grid, dim3(kThreads), smem, st, mk, mv, a) == cudaSuccess ? PA_OK
+                                                                                                      : PA_ERR_CUDA;
 }
 
 int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, void* workspace,
