@@ -243,26 +243,46 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         step()
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # Timed region: K steps between two events.  The decode call of every
+    # SAMPLE-th step is also bracketed by events (an event between two kernels
+    # stops the second from overlapping the first's drain, so only a sample of
+    # steps carries them); their mean is the kernels' average duration.
+    SAMPLE = 8
+    ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range((K + SAMPLE - 1) // SAMPLE)]
+
+    def decode(q_, tables_, ctx_):
+        api.pa_decode(out, q_, kc, vc, tables_, ctx_, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
+                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=stream)
+
     barrier(world)
     torch.cuda.synchronize(dev)
+    ev_start.record(stream)
     for i in range(K):
-        ev[i][0].record(stream)
         api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
-        ev[i][1].record(stream)
-        api.pa_decode(out, q, kc, vc, tables, ctx, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
-                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=stream)
-        ev[i][2].record(stream)
+        if i % SAMPLE == 0:
+            a, b = ev_dec[i // SAMPLE]
+            a.record(stream)
+            decode(q, tables, ctx)
+            b.record(stream)
+        else:
+            decode(q, tables, ctx)
+    ev_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop() if clocks else None
-    step_s = ev[0][0].elapsed_time(ev[K - 1][2]) / 1e3
-    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    dec_s_avg = sum(dec_ms) / K / 1e3
+    step_s = ev_start.elapsed_time(ev_end) / 1e3
+    dec_s_avg = sum(a.elapsed_time(b) for a, b in ev_dec) / len(ev_dec) / 1e3
     total_s, total_bytes = reduce_timing(step_s, (dec_bytes + write_bytes) * K, world, dev)
     _, total_seqs = reduce_timing(step_s, S * K, world, dev)
 
     # ---- end to end through the public API with host buffers ---------------
+    # Every step copies its inputs from pinned host memory (q, the new K/V
+    # rows, slot mapping, block tables, context lengths), runs the cache write
+    # and the decode, copies the output back and waits for it.  The step is
+    # issued once into a CUDA graph (the library's calls are capturable) and
+    # replayed; the eager form is timed too.
     q_h = q.cpu().pin_memory()
     k_h, v_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
     slots_hp = slots.cpu().pin_memory()
@@ -273,27 +293,43 @@ def run_ours(args, world, rank, local):
     h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, slots_hp, tables_h, ctx_hp))
     d2h = out_h.numel() * out_h.element_size()
 
-    def e2e_step():
+    def e2e_body(st):
         for dst, src in ((q_d, q_h), (k_d, k_h), (v_d, v_h), (slots_d, slots_hp), (tables_d, tables_h),
                          (ctx_d, ctx_hp)):
             dst.copy_(src, non_blocking=True)
-        api.pa_reshape_and_cache(kc, vc, k_d, v_d, slots_d, stream=stream)
+        api.pa_reshape_and_cache(kc, vc, k_d, v_d, slots_d, stream=st)
         api.pa_decode(out, q_d, kc, vc, tables_d, ctx_d, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
-                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=stream)
+                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=st)
         out_h.copy_(out, non_blocking=True)
+
+    def eager_step():
+        e2e_body(stream)
         stream.synchronize()
 
+    graph = torch.cuda.CUDAGraph()
     for _ in range(args.warmup):
-        e2e_step()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(K):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    e2e_s = time.perf_counter() - t0
-    barrier(world)
-    e2e_total_s, e2e_bytes = reduce_timing(e2e_s, (dec_bytes + write_bytes) * K, world, dev)
+        eager_step()
+    with torch.cuda.graph(graph):
+        e2e_body(torch.cuda.current_stream(dev))
+
+    def graph_step():
+        graph.replay()
+        stream.synchronize()
+
+    e2e_times = {}
+    for name, fn in (("graph", graph_step), ("eager", eager_step)):
+        for _ in range(args.warmup):
+            fn()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(K):
+            fn()
+        torch.cuda.synchronize(dev)
+        e2e_times[name] = time.perf_counter() - t0
+        barrier(world)
+    e2e_total_s, e2e_bytes = reduce_timing(e2e_times["graph"], (dec_bytes + write_bytes) * K, world, dev)
+    eager_total_s, _ = reduce_timing(e2e_times["eager"], 0, world, dev)
 
     if rank != 0:
         return None
@@ -320,8 +356,11 @@ def run_ours(args, world, rank, local):
                      "avg_launch_us": round(dec_s_avg * 1e6, 2)},
         "e2e": {"value": round(e2e_bytes / e2e_total_s / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_total_s / K * 1e3, 4)},
+                "ms_per_step": round(e2e_total_s / K * 1e3, 4), "issue": "CUDA graph of the step, replayed",
+                "eager_value": round(e2e_bytes / eager_total_s / 1e9, 2),
+                "eager_ms_per_step": round(eager_total_s / K * 1e3, 4)},
         "gpu_launches": launches_per_step * K,
+        "decode_timing": "events around pa_decode on every %d-th timed step (%d samples)" % (SAMPLE, len(ev_dec)),
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
