@@ -146,7 +146,7 @@ int pa_decode(void* out, int out_dtype, const void* q,
  * over partitions p = 0 .. ceil(context_lens[s] / partition_size) - 1 of each
  * (sequence s, query head g).  m is in the units of the scores themselves
  * (natural-log domain).  This is the second kernel of pa_decode, exposed so
- * that partition statistics from any source can be merged; d_head <= 256.
+ * that partition statistics from any source can be merged; d_head <= 1024.
  *   part_max, part_sum  device f32 [num_seqs][n_q_heads][max_parts]
  *   part_acc            device f32 [num_seqs][n_q_heads][max_parts][d_head]
  *   context_lens        device int32 [num_seqs]; partitions counted as above,

@@ -66,7 +66,6 @@ constexpr int kMaxProbes = 2000000;   // ~2 s bound on any single wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxPartition = 8192;
-constexpr int kMergeChunk = 1024;  // partitions whose weights are staged at once by the merging block
 
 // Arguments shared by both schedules.
 struct DecodeArgs {
@@ -471,81 +470,71 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
     }
 }
 
+// Fold partitions [0, np) of one (sequence, head) row into (M, Z, U) for
+// dimension d: kChunk partitions' statistics and values are loaded at once
+// (independent loads, one memory round trip per chunk), then merged into the
+// running values with the same rule.
+template <int kChunk>
+__device__ __forceinline__ float merge_row(const float* __restrict__ pmax, const float* __restrict__ psum,
+                                           const float* __restrict__ pacc, size_t base, int np, int d_head, int d) {
+    float M = -INFINITY, Z = 0.f, U = 0.f;
+    for (int c0 = 0; c0 < np; c0 += kChunk) {
+        float m[kChunk], z[kChunk], u[kChunk];
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) {
+            const int p = c0 + r;
+            const bool ok = p < np;
+            m[r] = ok ? pmax[base + p] : -INFINITY;
+            z[r] = ok ? psum[base + p] : 0.f;
+            u[r] = ok ? pacc[(base + p) * d_head + d] : 0.f;
+        }
+        float mc = M;
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) mc = fmaxf(mc, m[r]);
+        const float sc = fast_exp2((M - mc) * kLog2e);   // 0 on the first chunk (M = -inf)
+        Z *= sc;
+        U *= sc;
+#pragma unroll
+        for (int r = 0; r < kChunk; ++r) {
+            const float w = fast_exp2((m[r] - mc) * kLog2e);
+            Z += w * z[r];
+            U += w * u[r];
+        }
+        M = mc;
+    }
+    return U / Z;
+}
+
 // Exact merge of partition statistics (second page, section 11):
 // M = max m_p, Z = sum exp(m_p - M) z_p, U = sum exp(m_p - M) u_p, out = U / Z.
-// One thread block of kThreads per (query head, sequence).  Warp 0 reduces M
-// and Z over the partitions; the weights exp(m_p - M) / Z are staged in
-// shared memory in chunks of kMergeChunk and every thread sums its dimension
-// with independent loads.  When launched as a programmatic dependent of the
-// partition kernel, it waits for that grid's results before reading them.
-__global__ void __launch_bounds__(kThreads) lse_merge_kernel(void* out, int out_f32, const float* __restrict__ pmax,
-                                                             const float* __restrict__ psum,
-                                                             const float* __restrict__ pacc,
-                                                             const int32_t* __restrict__ context_lens, int ctx_cap,
-                                                             int partition_size, int max_parts, int n_q_heads,
-                                                             int d_head, int skip_single) {
-    __shared__ float wgt[kMergeChunk];
-    __shared__ float sM, sInv;
+// One thread block per (query head, sequence), one thread per dimension,
+// kChunk partitions loaded per memory round trip (4 when no sequence can have
+// more than 4 partitions, else 8: wider chunks cost registers that the many
+// short rows of a ragged batch do not repay).  When launched as a
+// programmatic dependent of the partition kernel, it waits for that grid's
+// results before reading them.
+template <int kChunk>
+__global__ void lse_merge_kernel(void* out, int out_f32, const float* __restrict__ pmax,
+                                 const float* __restrict__ psum, const float* __restrict__ pacc,
+                                 const int32_t* __restrict__ context_lens, int ctx_cap, int partition_size,
+                                 int max_parts, int n_q_heads, int d_head, int skip_single) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int h = blockIdx.x;
     const int seq = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int d = threadIdx.x;
     int ctx = context_lens[seq];
     ctx = ctx < 0 ? 0 : (ctx > ctx_cap ? ctx_cap : ctx);
     int np = (int)(((long long)ctx + partition_size - 1) / partition_size);
     np = np > max_parts ? max_parts : np;
     if (skip_single && np <= 1) return;             // finished by the partition kernel
+    if (d >= d_head) return;
     const size_t orow = ((size_t)seq * n_q_heads + h) * d_head;
     if (np == 0) {
-        for (int d = threadIdx.x; d < d_head; d += blockDim.x) store_out(out, out_f32, orow + d, 0.f);
+        store_out(out, out_f32, orow + d, 0.f);
         return;
     }
     const size_t base = ((size_t)seq * n_q_heads + h) * max_parts;
-    if (warp == 0) {
-        float M = -INFINITY;
-        for (int p = lane; p < np; p += 32) M = fmaxf(M, pmax[base + p]);
-#pragma unroll
-        for (int msk = 16; msk >= 1; msk >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, msk));
-        float Z = 0.f;
-        for (int p = lane; p < np; p += 32) Z += fast_exp2((pmax[base + p] - M) * kLog2e) * psum[base + p];
-#pragma unroll
-        for (int msk = 16; msk >= 1; msk >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, msk);
-        if (lane == 0) {
-            sM = M;
-            sInv = 1.f / Z;
-        }
-    }
-    __syncthreads();
-    const float M = sM, inv = sInv;
-    float acc[2] = {0.f, 0.f};                      // d_head <= 2 * kThreads
-    for (int c0 = 0; c0 < np; c0 += kMergeChunk) {
-        const int nc = min(kMergeChunk, np - c0);
-        for (int p = threadIdx.x; p < nc; p += blockDim.x)
-            wgt[p] = fast_exp2((pmax[base + c0 + p] - M) * kLog2e) * inv;
-        __syncthreads();
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int d = threadIdx.x + it * blockDim.x;
-            if (d >= d_head) break;
-            const float* src = pacc + (base + c0) * d_head + d;
-            float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
-            int p = 0;
-            for (; p + 3 < nc; p += 4) {
-                u0 += wgt[p] * src[(size_t)p * d_head];
-                u1 += wgt[p + 1] * src[(size_t)(p + 1) * d_head];
-                u2 += wgt[p + 2] * src[(size_t)(p + 2) * d_head];
-                u3 += wgt[p + 3] * src[(size_t)(p + 3) * d_head];
-            }
-            for (; p < nc; ++p) u0 += wgt[p] * src[(size_t)p * d_head];
-            acc[it] += (u0 + u1) + (u2 + u3);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int d = threadIdx.x + it * blockDim.x;
-        if (d < d_head) store_out(out, out_f32, orow + d, acc[it]);
-    }
+    store_out(out, out_f32, orow + d, merge_row<kChunk>(pmax, psum, pacc, base, np, d_head, d));
 }
 
 // Launch lse_merge_kernel; as a programmatic dependent launch (its grid may
@@ -555,7 +544,7 @@ int launch_merge(bool pdl, cudaStream_t st, void* out, int out_f32, const float*
                  int skip_single) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(n_q_heads, num_seqs);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3((d_head + 31) / 32 * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -563,8 +552,9 @@ int launch_merge(bool pdl, cudaStream_t st, void* out, int out_f32, const float*
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, lse_merge_kernel, out, out_f32, pm, ps, pa, ctx, ctx_cap, P,
-                                             max_parts, n_q_heads, d_head, skip_single);
+    auto kernel = max_parts <= 4 ? lse_merge_kernel<4> : lse_merge_kernel<8>;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, out, out_f32, pm, ps, pa, ctx, ctx_cap, P, max_parts,
+                                             n_q_heads, d_head, skip_single);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -754,7 +744,7 @@ int pa_lse_merge(void* out, int out_dtype, const float* part_max, const float* p
     if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!out || !part_max || !part_sum || !part_acc || !context_lens) return PA_ERR_INVALID_ARG;
-    if (d_head > 2 * kThreads || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    if (d_head > 1024 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(out) & 3u) || (reinterpret_cast<uintptr_t>(part_max) & 3u) ||
         (reinterpret_cast<uintptr_t>(part_sum) & 3u) || (reinterpret_cast<uintptr_t>(part_acc) & 3u))
         return PA_ERR_MISALIGNED;
