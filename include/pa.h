@@ -253,10 +253,14 @@ typedef struct pa_alloc pa_alloc_t;
 
 typedef struct pa_alloc_stats {
     int32_t num_blocks;
-    int32_t num_free;
-    int32_t num_used;
+    int32_t num_free;           /* on the free list                        */
+    int32_t num_used;           /* count >= 1                              */
     int32_t num_seqs;
     int64_t num_cow_copies;     /* CoW pairs emitted since creation        */
+    int32_t num_cached;         /* count 0, kept for prefix reuse          */
+    int32_t reserved;
+    int64_t num_prompt_tokens;  /* prompt positions admitted since creation */
+    int64_t num_cached_tokens;  /* of those, found in the prefix cache     */
 } pa_alloc_stats_t;
 
 /* NULL if num_blocks <= 0 or block_size <= 0 or on allocation failure. */
@@ -271,8 +275,59 @@ int pa_alloc_set_free_order(pa_alloc_t* a, const int32_t* order, int n);
 
 /* Take ceil(num_tokens / block_size) blocks (ref 1) for a new sequence of
  * num_tokens prompt positions.  PA_ERR_DUPLICATE_SEQ if seq exists,
- * PA_ERR_INVALID_ARG if num_tokens <= 0, PA_FAIL_NO_BLOCKS if too few free. */
+ * PA_ERR_INVALID_ARG if num_tokens <= 0, PA_FAIL_NO_BLOCKS if too few free.
+ * Its token ids are unknown, so none of its blocks is ever cached. */
 int pa_alloc_sequence(pa_alloc_t* a, int64_t seq, int num_tokens);
+
+/* ---------------------------------------------------------------------------
+ * Automatic prefix caching ([P1] section 18; [P2] section 6; [P3] "Prefix
+ * caching").  Off by default.  When on, a FULL block whose token ids are
+ * known is registered under a key made of its block_size token ids and the
+ * key of the block before it (the root key for block 0), so two blocks match
+ * only when the whole prefix up to and including them is identical.  A
+ * registered block whose count falls to 0 is not put on the free list but
+ * queued for eviction (least recently released first; within one release,
+ * the deepest block of the table is queued first).  Fresh blocks come from
+ * the free list first and only when it is empty from the front of the
+ * eviction queue, which drops that block's key.  Partly filled blocks are
+ * never registered; when a block fills under a key that another block
+ * already holds, it is left unregistered and returns to the free list when
+ * released.  Keys are 64-bit chained hashes; a lookup also compares the
+ * block's token ids and parent key.
+ * ------------------------------------------------------------------------- */
+
+/* Switch caching on (enable != 0) or off.  Only while no sequence exists;
+ * switching off forgets every key and moves the queued blocks to the free
+ * list (oldest first, so the newest is handed out first).
+ * PA_ERR_INVALID_ARG otherwise. */
+int pa_alloc_enable_prefix_caching(pa_alloc_t* a, int enable);
+
+/* New sequence with known prompt token ids tokens[0 .. num_tokens-1].
+ * With caching on, its leading full blocks are looked up in order and the
+ * search stops at the first miss; each hit is shared (count + 1; a queued
+ * block leaves the queue and goes from 0 back to 1) and its positions need
+ * no prefill: *num_cached_tokens = hits * block_size.  The rest are fresh
+ * blocks; the full ones among them are registered at once (the caller must
+ * write their KV before any other sequence can read it, i.e. before the next
+ * decode on the same stream).  With caching off it behaves as
+ * pa_alloc_sequence and *num_cached_tokens = 0.
+ * PA_ERR_DUPLICATE_SEQ, PA_ERR_INVALID_ARG, PA_FAIL_NO_BLOCKS when the free
+ * list plus the queue (less the hits taken from it) is short: no change. */
+int pa_alloc_sequence_tokens(pa_alloc_t* a, int64_t seq, const int32_t* tokens,
+                             int num_tokens, int* num_cached_tokens);
+
+/* pa_alloc_append_slot for a position whose token id is known.  When that
+ * position fills the block and caching is on, the block is registered.  A
+ * sequence extended with pa_alloc_append_slot loses its token ids and is
+ * not registered from then on. */
+int pa_alloc_append_token(pa_alloc_t* a, int64_t seq, int32_t token,
+                          int64_t* slot_out, int32_t* cow_src, int32_t* cow_dst);
+
+/* Blocks with count 0 held for reuse (-1 for a NULL handle). */
+int pa_alloc_num_cached(const pa_alloc_t* a);
+/* Copy the eviction queue front (next evicted) to back into out (cap
+ * entries); returns its size. */
+int pa_alloc_cached_list(const pa_alloc_t* a, int32_t* out, int cap);
 
 /* child gets a copy of parent's table and length; every block's count +1
  * ([P1] section 16, step 2).  PA_ERR_UNKNOWN_SEQ / PA_ERR_DUPLICATE_SEQ. */
@@ -298,7 +353,8 @@ int pa_alloc_append_slots(pa_alloc_t* a, const int64_t* seqs, int n,
                           int cow_capacity, int* num_cow, int* num_done);
 
 /* Release: every block in seq's table loses one reference and returns to
- * the free list at 0, in table order ([P1] section 17).  Unknown seq: no-op,
+ * the free list at 0, in table order ([P1] section 17); with caching on, a
+ * registered block at 0 is queued for eviction instead (see above).  Unknown seq: no-op,
  * PA_OK.  Blocks are reusable only after GPU work that reads or writes them
  * has completed; the caller orders that (same stream). */
 int pa_alloc_free(pa_alloc_t* a, int64_t seq);

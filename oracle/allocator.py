@@ -26,7 +26,31 @@ Semantics restated:
   * Release drops one reference per table entry, in table order, and puts a
     block back on the free list when its count reaches 0 ([P1] section 17).
     Releasing an unknown sequence does nothing.
+
+Automatic prefix caching ([P1] section 18; [P2] section 6; [P3] "Prefix
+caching"), off until enable_prefix_caching(True):
+  * Only full blocks whose token ids are known are cached.  A block's key is
+    the exact tuple of every token id from position 0 to the block's end, so
+    two blocks match only when the whole prefix up to them is identical
+    ([P2] section 6: equal text after a different prefix does not match).
+  * A new prompt with known token ids looks its full blocks up from the
+    first one and stops at the first miss; every hit is shared (count + 1),
+    and a hit with count 0 leaves the eviction queue and goes back to 1
+    ([P1] section 18).  The hits' positions need no prefill.  The remaining
+    blocks are taken fresh and the full ones are registered under their
+    keys at once, unless another block already holds that key.
+  * A registered block whose count reaches 0 is queued for eviction rather
+    than freed; within one release the deepest block is queued first.
+  * A fresh block comes from the free list while it has any, else from the
+    front (oldest) of the eviction queue, which forgets its key ([P1]
+    section 19, item 2; [P2] section 6, the LRU-style free queue).
+  * Appending a position with a known token id that fills the block
+    registers it; appending without a token id forgets the sequence's
+    tokens, so none of its later blocks is registered.
+  * Running short is checked against the free list plus the queue (less the
+    hits taken out of the queue); on failure nothing changes.
 """
+from collections import OrderedDict
 
 OK = 0
 FAIL_NO_BLOCKS = 1
@@ -46,6 +70,35 @@ class RefAllocator:
         self.block_tables = {}
         self.seq_lengths = {}
         self.num_cow_copies = 0
+        # prefix cache
+        self.caching = False
+        self.cache_index = {}          # prefix key -> block
+        self.block_key = {}            # block -> prefix key (registered blocks)
+        self.evict_queue = OrderedDict()   # zero-count registered blocks, oldest first
+        self.seq_tokens = {}           # seq -> list of token ids, or None when unknown
+        self.num_prompt_tokens = 0
+        self.num_cached_tokens = 0
+
+    # -- prefix-cache helpers ----------------------------------------------
+    def _available(self):
+        return len(self.free_blocks) + len(self.evict_queue)
+
+    def _take(self):
+        """A fresh block with count 1: free list first, else evict the oldest
+        zero-count cached block and forget its key."""
+        if self.free_blocks:
+            b = self.free_blocks.pop()
+        else:
+            b, _ = self.evict_queue.popitem(last=False)
+            del self.cache_index[self.block_key.pop(b)]
+        self.ref_counts[b] = 1
+        return b
+
+    def _register(self, b, key):
+        if key in self.cache_index:
+            return
+        self.cache_index[key] = b
+        self.block_key[b] = key
 
     # -- set-up -------------------------------------------------------------
     def set_free_order(self, order):
@@ -53,7 +106,7 @@ class RefAllocator:
         as [P1] section 20, test 3 does to force a non-identity placement.
         Allowed only while no block is in use."""
         order = [int(b) for b in order]
-        if self.block_tables or sorted(order) != list(range(self.num_blocks)):
+        if self.block_tables or self.evict_queue or sorted(order) != list(range(self.num_blocks)):
             return ERR_INVALID_ARG
         self.free_blocks = order
         return OK
@@ -65,16 +118,65 @@ class RefAllocator:
         if num_tokens <= 0:
             return ERR_INVALID_ARG
         needed = -(-num_tokens // self.block_size)
-        if len(self.free_blocks) < needed:
+        if self._available() < needed:
             return FAIL_NO_BLOCKS
-        table = []
-        for _ in range(needed):
-            b = self.free_blocks.pop()
-            self.ref_counts[b] = 1
-            table.append(b)
-        self.block_tables[seq] = table
+        self.block_tables[seq] = [self._take() for _ in range(needed)]
         self.seq_lengths[seq] = num_tokens
+        self.seq_tokens[seq] = None
+        self.num_prompt_tokens += num_tokens
         return OK
+
+    def enable_prefix_caching(self, enable=True):
+        """Only while no sequence exists.  Switching off moves the queue to
+        the free list, oldest first, and forgets every key."""
+        if self.block_tables:
+            return ERR_INVALID_ARG
+        if not enable:
+            for b in self.evict_queue:
+                self.free_blocks.append(b)
+            self.evict_queue.clear()
+            self.cache_index.clear()
+            self.block_key.clear()
+        self.caching = bool(enable)
+        return OK
+
+    def allocate_tokens(self, seq, tokens):
+        """New sequence with known prompt token ids.  Returns (status,
+        number of leading positions found in the prefix cache)."""
+        tokens = [int(t) for t in tokens]
+        if seq in self.block_tables:
+            return ERR_DUPLICATE_SEQ, 0
+        if not tokens:
+            return ERR_INVALID_ARG, 0
+        B = self.block_size
+        needed = -(-len(tokens) // B)
+        full = len(tokens) // B
+        keys = [tuple(tokens[:(i + 1) * B]) for i in range(full)]
+        hits = []
+        if self.caching:
+            for key in keys:
+                if key not in self.cache_index:
+                    break
+                hits.append(self.cache_index[key])
+        from_queue = sum(1 for b in hits if b in self.evict_queue)
+        if self._available() - from_queue < needed - len(hits):
+            return FAIL_NO_BLOCKS, 0
+        table = []
+        for b in hits:
+            self.evict_queue.pop(b, None)
+            self.ref_counts[b] += 1
+            table.append(b)
+        for i in range(len(hits), needed):
+            b = self._take()
+            table.append(b)
+            if self.caching and i < full:
+                self._register(b, keys[i])
+        self.block_tables[seq] = table
+        self.seq_lengths[seq] = len(tokens)
+        self.seq_tokens[seq] = tokens
+        self.num_prompt_tokens += len(tokens)
+        self.num_cached_tokens += len(hits) * B
+        return OK, len(hits) * B
 
     def fork(self, parent, child):
         if parent not in self.block_tables:
@@ -85,11 +187,20 @@ class RefAllocator:
             self.ref_counts[b] += 1
         self.block_tables[child] = list(self.block_tables[parent])
         self.seq_lengths[child] = self.seq_lengths[parent]
+        toks = self.seq_tokens.get(parent)
+        self.seq_tokens[child] = None if toks is None else list(toks)
         return OK
 
     def append_slot(self, seq):
         """Plan one appended position.  Returns (status, slot, cow_src, cow_dst);
         slot is -1 and cow_src/cow_dst are -1 when there is nothing to do."""
+        return self._append(seq, None)
+
+    def append_token(self, seq, token):
+        """append_slot for a position whose token id is known."""
+        return self._append(seq, int(token))
+
+    def _append(self, seq, token):
         if seq not in self.block_tables:
             return ERR_UNKNOWN_SEQ, -1, -1, -1
         B = self.block_size
@@ -100,10 +211,9 @@ class RefAllocator:
         if offset != 0:
             tail = table[-1]
             if self.ref_counts[tail] > 1:
-                if not self.free_blocks:
+                if not self._available():
                     return FAIL_NO_BLOCKS, -1, -1, -1
-                new = self.free_blocks.pop()
-                self.ref_counts[new] = 1
+                new = self._take()
                 self.ref_counts[tail] -= 1
                 table[-1] = new
                 cow_src, cow_dst = tail, new
@@ -112,24 +222,37 @@ class RefAllocator:
             else:
                 slot = tail * B + offset
         else:
-            if not self.free_blocks:
+            if not self._available():
                 return FAIL_NO_BLOCKS, -1, -1, -1
-            new = self.free_blocks.pop()
-            self.ref_counts[new] = 1
+            new = self._take()
             table.append(new)
             slot = new * B
         self.seq_lengths[seq] = length + 1
+        toks = self.seq_tokens.get(seq)
+        if token is None or toks is None:
+            self.seq_tokens[seq] = None
+        else:
+            toks.append(token)
+            if self.caching and offset == B - 1:      # this position filled the block
+                self._register(slot // B, tuple(toks))
         return OK, slot, cow_src, cow_dst
 
     def free(self, seq):
         if seq not in self.block_tables:
             return OK
+        idle_cached = []
         for b in self.block_tables[seq]:
             self.ref_counts[b] -= 1
             if self.ref_counts[b] == 0:
-                self.free_blocks.append(b)
+                if b in self.block_key:
+                    idle_cached.append(b)
+                else:
+                    self.free_blocks.append(b)
+        for b in reversed(idle_cached):
+            self.evict_queue[b] = None
         del self.block_tables[seq]
         del self.seq_lengths[seq]
+        self.seq_tokens.pop(seq, None)
         return OK
 
     # -- queries --------------------------------------------------------------
@@ -140,3 +263,10 @@ class RefAllocator:
 
     def num_free(self):
         return len(self.free_blocks)
+
+    def num_cached(self):
+        return len(self.evict_queue)
+
+    def cached_list(self):
+        """Zero-count cached blocks, next to be evicted first."""
+        return list(self.evict_queue)

@@ -54,7 +54,9 @@ _f32p = ctypes.POINTER(ctypes.c_float)
 
 class AllocStats(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("num_free", ctypes.c_int32), ("num_used", ctypes.c_int32),
-                ("num_seqs", ctypes.c_int32), ("num_cow_copies", ctypes.c_int64)]
+                ("num_seqs", ctypes.c_int32), ("num_cow_copies", ctypes.c_int64), ("num_cached", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("num_prompt_tokens", ctypes.c_int64),
+                ("num_cached_tokens", ctypes.c_int64)]
 
 
 _SIGS = {
@@ -87,6 +89,11 @@ _SIGS = {
     "pa_alloc_num_free": (_c_int, [_vp]),
     "pa_alloc_free_list": (_c_int, [_vp, _i32p, _c_int]),
     "pa_alloc_get_stats": (_c_int, [_vp, ctypes.POINTER(AllocStats)]),
+    "pa_alloc_enable_prefix_caching": (_c_int, [_vp, _c_int]),
+    "pa_alloc_sequence_tokens": (_c_int, [_vp, ctypes.c_int64, _i32p, _c_int, ctypes.POINTER(_c_int)]),
+    "pa_alloc_append_token": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int32, _i64p, _i32p, _i32p]),
+    "pa_alloc_num_cached": (_c_int, [_vp]),
+    "pa_alloc_cached_list": (_c_int, [_vp, _i32p, _c_int]),
 }
 
 for _name, (_res, _args) in _SIGS.items():
@@ -313,6 +320,34 @@ class BlockAllocator:
     def fork(self, parent, child):
         return _lib.pa_alloc_fork(self._h, int(parent), int(child))
 
+    def enable_prefix_caching(self, enable=True):
+        return _lib.pa_alloc_enable_prefix_caching(self._h, 1 if enable else 0)
+
+    def allocate_tokens(self, seq, tokens):
+        """New sequence with known prompt token ids.  Returns (status,
+        num_cached_tokens): the leading positions found in the prefix cache,
+        whose KV is already in the pool."""
+        arr, p = _i32(tokens)
+        hit = ctypes.c_int(0)
+        st = _lib.pa_alloc_sequence_tokens(self._h, int(seq), p, len(arr), ctypes.byref(hit))
+        return st, hit.value
+
+    def append_token(self, seq, token):
+        slot, src, dst = ctypes.c_int64(-1), ctypes.c_int32(-1), ctypes.c_int32(-1)
+        st = _lib.pa_alloc_append_token(self._h, int(seq), int(token), ctypes.byref(slot), ctypes.byref(src),
+                                        ctypes.byref(dst))
+        return st, slot.value, src.value, dst.value
+
+    def num_cached(self):
+        return _lib.pa_alloc_num_cached(self._h)
+
+    def cached_list(self):
+        """Zero-count cached blocks, next to be evicted first."""
+        n = _lib.pa_alloc_cached_list(self._h, None, 0)
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        _lib.pa_alloc_cached_list(self._h, out.ctypes.data_as(_i32p), n)
+        return out[:n].tolist()
+
     def append_slot(self, seq):
         slot, src, dst = ctypes.c_int64(-1), ctypes.c_int32(-1), ctypes.c_int32(-1)
         st = _lib.pa_alloc_append_slot(self._h, int(seq), ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst))
@@ -376,4 +411,6 @@ class BlockAllocator:
     def stats(self):
         s = AllocStats()
         _check(_lib.pa_alloc_get_stats(self._h, ctypes.byref(s)), "pa_alloc_get_stats")
-        return {f: getattr(s, f) for f, _ in AllocStats._fields_}
+        d = {f: getattr(s, f) for f, _ in AllocStats._fields_ if f != "reserved"}
+        d["prefix_cache_hit_rate"] = d["num_cached_tokens"] / d["num_prompt_tokens"] if d["num_prompt_tokens"] else 0.0
+        return d

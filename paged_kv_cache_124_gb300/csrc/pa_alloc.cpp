@@ -1,5 +1,5 @@
 // Host block manager: free list, reference counts, fork, append with
-// copy-on-write planning, release.
+// copy-on-write planning, release, and automatic prefix caching.
 //
 // Semantics follow "PagedAttention: Virtual Memory for the KV Cache"
 // (sections 14-17 and the section 20 teaching model): the free list is a
@@ -9,9 +9,22 @@
 // zero; running out of blocks changes nothing.  The payload is not kept
 // here: the planned slot and copy pair drive pa_reshape_and_cache and
 // pa_copy_blocks on the GPU.
+//
+// Prefix caching (same page, section 18; "PagedAttention in vLLM: scattered
+// memory, exact attention", section 6; "PagedAttention and KV Memory"): a
+// full block whose token ids are known is registered under a key made of its
+// tokens and its parent's key, so two blocks match only when their whole
+// prefix matches.  A registered block whose count drops to zero is not freed
+// but kept, least recently released first, in an eviction queue; a later
+// prompt with the same prefix revives it (count 0 -> 1) instead of writing
+// it again.  Fresh blocks come from the free list first and only then by
+// evicting the queue's oldest block.  Keys are 64-bit chained hashes; a
+// lookup also compares the block's own tokens and its parent's key, so a
+// wrong match needs two different prefixes whose 64-bit parent keys collide.
 
 #include <algorithm>
 #include <cstdint>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -20,9 +33,27 @@
 
 namespace {
 
+constexpr uint64_t kRootKey = 0x9E3779B97F4A7C15ull;
+
+uint64_t mix64(uint64_t x) {                 // splitmix64 finaliser
+    x += 0x9E3779B97F4A7C15ull;
+    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+    return x ^ (x >> 31);
+}
+
+uint64_t block_key(uint64_t parent, const int32_t* tokens, int n) {
+    uint64_t h = mix64(parent);
+    for (int i = 0; i < n; ++i) h = mix64(h ^ (uint64_t)(uint32_t)tokens[i]);
+    return h;
+}
+
 struct Sequence {
     std::vector<int32_t> table;   // logical block -> physical block
     int32_t length = 0;           // cached positions
+    bool has_tokens = false;      // token ids known: full blocks can be registered
+    std::vector<int32_t> tokens;  // token id of every position (when has_tokens)
+    std::vector<uint64_t> keys;   // key of every full block (when has_tokens)
 };
 
 }  // namespace
@@ -34,20 +65,74 @@ struct pa_alloc {
     std::vector<int32_t> refs;
     std::unordered_map<int64_t, Sequence> seqs;
     int64_t num_cow_copies = 0;
+    // prefix cache
+    bool caching = false;
+    std::unordered_map<uint64_t, int32_t> index;       // key -> registered block
+    std::vector<char> registered;
+    std::vector<uint64_t> reg_key, reg_parent;
+    std::vector<std::vector<int32_t>> reg_tokens;
+    std::list<int32_t> lru;                             // zero-count registered blocks, oldest first
+    std::vector<std::list<int32_t>::iterator> lru_pos;
+    std::vector<char> in_lru;
+    int64_t prompt_tokens = 0, cached_tokens = 0;
 
-    pa_alloc(int nb, int bs) : num_blocks(nb), block_size(bs), refs(nb, 0) {
+    pa_alloc(int nb, int bs)
+        : num_blocks(nb), block_size(bs), refs(nb, 0), registered(nb, 0), reg_key(nb, 0), reg_parent(nb, 0),
+          reg_tokens(nb), lru_pos(nb), in_lru(nb, 0) {
         free_stack.reserve(nb);
         for (int b = nb - 1; b >= 0; --b) free_stack.push_back(b);
     }
 
+    int64_t available() const { return (int64_t)free_stack.size() + (int64_t)lru.size(); }
+
+    void unregister(int32_t b) {
+        if (!registered[b]) return;
+        auto it = index.find(reg_key[b]);
+        if (it != index.end() && it->second == b) index.erase(it);
+        registered[b] = 0;
+        reg_tokens[b].clear();
+    }
+
+    void register_block(int32_t b, uint64_t key, uint64_t parent, const int32_t* tokens) {
+        if (index.count(key)) return;           // another block already holds this content
+        index.emplace(key, b);
+        registered[b] = 1;
+        reg_key[b] = key;
+        reg_parent[b] = parent;
+        reg_tokens[b].assign(tokens, tokens + block_size);
+    }
+
+    // Registered block with this key, parent and tokens, or -1.
+    int32_t lookup(uint64_t key, uint64_t parent, const int32_t* tokens) const {
+        auto it = index.find(key);
+        if (it == index.end()) return -1;
+        const int32_t b = it->second;
+        if (reg_parent[b] != parent || !std::equal(tokens, tokens + block_size, reg_tokens[b].begin())) return -1;
+        return b;
+    }
+
+    void lru_remove(int32_t b) {
+        if (!in_lru[b]) return;
+        lru.erase(lru_pos[b]);
+        in_lru[b] = 0;
+    }
+
+    // A fresh block with count 1: from the free list, else the queue's oldest.
     int32_t take() {
-        int32_t b = free_stack.back();
-        free_stack.pop_back();
+        int32_t b;
+        if (!free_stack.empty()) {
+            b = free_stack.back();
+            free_stack.pop_back();
+        } else {
+            b = lru.front();
+            lru_remove(b);
+            unregister(b);
+        }
         refs[b] = 1;
         return b;
     }
 
-    int append(int64_t seq, int64_t* slot, int32_t* src, int32_t* dst) {
+    int append(int64_t seq, int64_t* slot, int32_t* src, int32_t* dst, const int32_t* token) {
         auto it = seqs.find(seq);
         if (it == seqs.end()) return PA_ERR_UNKNOWN_SEQ;
         Sequence& s = it->second;
@@ -56,7 +141,7 @@ struct pa_alloc {
         if (off != 0) {
             const int32_t tail = s.table.back();
             if (refs[tail] > 1) {                       // shared tail: clone first
-                if (free_stack.empty()) return PA_FAIL_NO_BLOCKS;
+                if (available() == 0) return PA_FAIL_NO_BLOCKS;
                 blk = take();
                 refs[tail] -= 1;
                 s.table.back() = blk;
@@ -67,7 +152,7 @@ struct pa_alloc {
                 blk = tail;                              // private tail: in place
             }
         } else {
-            if (free_stack.empty()) return PA_FAIL_NO_BLOCKS;
+            if (available() == 0) return PA_FAIL_NO_BLOCKS;
             blk = take();                                // tail full: new block
             s.table.push_back(blk);
         }
@@ -75,7 +160,42 @@ struct pa_alloc {
         *src = cs;
         *dst = cd;
         s.length += 1;
+        if (!token) {
+            s.has_tokens = false;                        // content no longer known
+            s.tokens.clear();
+            s.keys.clear();
+        } else if (s.has_tokens) {
+            s.tokens.push_back(*token);
+            if (caching && off == block_size - 1) {      // the block just became full
+                const uint64_t parent = s.keys.empty() ? kRootKey : s.keys.back();
+                const int32_t* t = s.tokens.data() + (s.length - block_size);
+                const uint64_t key = block_key(parent, t, block_size);
+                s.keys.push_back(key);
+                register_block(blk, key, parent, t);
+            }
+        }
         return PA_OK;
+    }
+
+    // Drop one reference; a block that reaches zero goes to the free list, or
+    // to the eviction queue when it is registered.
+    void release_table(const std::vector<int32_t>& table) {
+        std::vector<int32_t> to_queue;
+        for (int32_t b : table) {
+            refs[b] -= 1;
+            if (refs[b] == 0) {
+                if (registered[b])
+                    to_queue.push_back(b);
+                else
+                    free_stack.push_back(b);
+            }
+        }
+        // deeper blocks first, so that a chain is evicted from its tail end
+        for (auto it = to_queue.rbegin(); it != to_queue.rend(); ++it) {
+            lru.push_back(*it);
+            lru_pos[*it] = std::prev(lru.end());
+            in_lru[*it] = 1;
+        }
     }
 };
 
@@ -89,7 +209,7 @@ pa_alloc_t* pa_alloc_create(int num_blocks, int block_size) {
 void pa_alloc_destroy(pa_alloc_t* a) { delete a; }
 
 int pa_alloc_set_free_order(pa_alloc_t* a, const int32_t* order, int n) {
-    if (!a || !order || n != a->num_blocks || !a->seqs.empty()) return PA_ERR_INVALID_ARG;
+    if (!a || !order || n != a->num_blocks || !a->seqs.empty() || !a->lru.empty()) return PA_ERR_INVALID_ARG;
     if ((int)a->free_stack.size() != a->num_blocks) return PA_ERR_INVALID_ARG;
     std::vector<char> seen(a->num_blocks, 0);
     for (int i = 0; i < n; ++i) {
@@ -105,12 +225,72 @@ int pa_alloc_sequence(pa_alloc_t* a, int64_t seq, int num_tokens) {
     if (a->seqs.count(seq)) return PA_ERR_DUPLICATE_SEQ;
     if (num_tokens <= 0) return PA_ERR_INVALID_ARG;
     const int64_t need = ((int64_t)num_tokens + a->block_size - 1) / a->block_size;
-    if ((int64_t)a->free_stack.size() < need) return PA_FAIL_NO_BLOCKS;
+    if (a->available() < need) return PA_FAIL_NO_BLOCKS;
     Sequence s;
     s.table.reserve(need);
     for (int64_t i = 0; i < need; ++i) s.table.push_back(a->take());
     s.length = num_tokens;
     a->seqs.emplace(seq, std::move(s));
+    a->prompt_tokens += num_tokens;
+    return PA_OK;
+}
+
+int pa_alloc_sequence_tokens(pa_alloc_t* a, int64_t seq, const int32_t* tokens, int num_tokens,
+                             int* num_cached_tokens) {
+    if (!a || !num_cached_tokens) return PA_ERR_INVALID_ARG;
+    *num_cached_tokens = 0;
+    if (a->seqs.count(seq)) return PA_ERR_DUPLICATE_SEQ;
+    if (num_tokens <= 0 || !tokens) return PA_ERR_INVALID_ARG;
+    const int B = a->block_size;
+    const int64_t need = ((int64_t)num_tokens + B - 1) / B;
+    const int full = num_tokens / B;
+    // plan: keys of the full blocks, and the leading blocks already cached
+    std::vector<uint64_t> keys, parents;
+    std::vector<int32_t> hits;
+    int64_t revived_from_queue = 0;
+    if (a->caching) {
+        uint64_t parent = kRootKey;
+        bool matching = true;
+        for (int i = 0; i < full; ++i) {
+            const int32_t* t = tokens + (size_t)i * B;
+            const uint64_t key = block_key(parent, t, B);
+            if (matching) {
+                const int32_t b = a->lookup(key, parent, t);
+                if (b >= 0) {
+                    hits.push_back(b);
+                    revived_from_queue += a->in_lru[b] ? 1 : 0;
+                } else {
+                    matching = false;
+                }
+            }
+            keys.push_back(key);
+            parents.push_back(parent);
+            parent = key;
+        }
+    }
+    const int64_t fresh = need - (int64_t)hits.size();
+    if (a->available() - revived_from_queue < fresh) return PA_FAIL_NO_BLOCKS;
+    // apply
+    Sequence s;
+    s.table.reserve(need);
+    for (int32_t b : hits) {
+        a->lru_remove(b);                  // a cached block with count 0 comes back to 1
+        a->refs[b] += 1;
+        s.table.push_back(b);
+    }
+    for (int64_t i = (int64_t)hits.size(); i < need; ++i) {
+        const int32_t b = a->take();
+        s.table.push_back(b);
+        if (a->caching && i < full) a->register_block(b, keys[i], parents[i], tokens + (size_t)i * B);
+    }
+    s.length = num_tokens;
+    s.has_tokens = true;
+    s.tokens.assign(tokens, tokens + num_tokens);
+    s.keys = std::move(keys);
+    a->seqs.emplace(seq, std::move(s));
+    *num_cached_tokens = (int)hits.size() * B;
+    a->prompt_tokens += num_tokens;
+    a->cached_tokens += *num_cached_tokens;
     return PA_OK;
 }
 
@@ -128,7 +308,13 @@ int pa_alloc_fork(pa_alloc_t* a, int64_t parent, int64_t child) {
 int pa_alloc_append_slot(pa_alloc_t* a, int64_t seq, int64_t* slot_out,
                          int32_t* cow_src, int32_t* cow_dst) {
     if (!a || !slot_out || !cow_src || !cow_dst) return PA_ERR_INVALID_ARG;
-    return a->append(seq, slot_out, cow_src, cow_dst);
+    return a->append(seq, slot_out, cow_src, cow_dst, nullptr);
+}
+
+int pa_alloc_append_token(pa_alloc_t* a, int64_t seq, int32_t token, int64_t* slot_out, int32_t* cow_src,
+                          int32_t* cow_dst) {
+    if (!a || !slot_out || !cow_src || !cow_dst) return PA_ERR_INVALID_ARG;
+    return a->append(seq, slot_out, cow_src, cow_dst, &token);
 }
 
 int pa_alloc_append_slots(pa_alloc_t* a, const int64_t* seqs, int n, int64_t* slots_out,
@@ -145,7 +331,7 @@ int pa_alloc_append_slots(pa_alloc_t* a, const int64_t* seqs, int n, int64_t* sl
                 a->refs[it->second.table.back()] > 1)
                 return PA_ERR_INVALID_ARG;
         }
-        int st = a->append(seqs[i], &slots_out[i], &src, &dst);
+        int st = a->append(seqs[i], &slots_out[i], &src, &dst, nullptr);
         if (st != PA_OK) return st;
         if (src >= 0) {
             cow_pairs_out[2 * (*num_cow)] = src;
@@ -161,10 +347,7 @@ int pa_alloc_free(pa_alloc_t* a, int64_t seq) {
     if (!a) return PA_ERR_INVALID_ARG;
     auto it = a->seqs.find(seq);
     if (it == a->seqs.end()) return PA_OK;
-    for (int32_t b : it->second.table) {
-        a->refs[b] -= 1;
-        if (a->refs[b] == 0) a->free_stack.push_back(b);
-    }
+    a->release_table(it->second.table);
     a->seqs.erase(it);
     return PA_OK;
 }
@@ -235,10 +418,40 @@ int pa_alloc_get_stats(const pa_alloc_t* a, pa_alloc_stats_t* out) {
     if (!a || !out) return PA_ERR_INVALID_ARG;
     out->num_blocks = a->num_blocks;
     out->num_free = (int32_t)a->free_stack.size();
-    out->num_used = a->num_blocks - out->num_free;
+    out->num_cached = (int32_t)a->lru.size();
+    out->num_used = a->num_blocks - out->num_free - out->num_cached;
     out->num_seqs = (int32_t)a->seqs.size();
     out->num_cow_copies = a->num_cow_copies;
+    out->num_prompt_tokens = a->prompt_tokens;
+    out->num_cached_tokens = a->cached_tokens;
     return PA_OK;
+}
+
+int pa_alloc_enable_prefix_caching(pa_alloc_t* a, int enable) {
+    if (!a || !a->seqs.empty()) return PA_ERR_INVALID_ARG;
+    if (!enable) {                                  // forget the cache: queued blocks become free
+        for (int32_t b : a->lru) {
+            a->in_lru[b] = 0;
+            a->free_stack.push_back(b);
+        }
+        a->lru.clear();
+        for (int32_t b = 0; b < a->num_blocks; ++b) a->unregister(b);
+        a->index.clear();
+    }
+    a->caching = enable != 0;
+    return PA_OK;
+}
+
+int pa_alloc_num_cached(const pa_alloc_t* a) { return a ? (int)a->lru.size() : -1; }
+
+int pa_alloc_cached_list(const pa_alloc_t* a, int32_t* out, int cap) {
+    if (!a) return -1;
+    int i = 0;
+    for (int32_t b : a->lru) {
+        if (out && i < cap) out[i] = b;
+        ++i;
+    }
+    return i;
 }
 
 }  // extern "C"

@@ -240,3 +240,56 @@ def append_kv(seed, layer, step, n_tokens, n_kv_heads, d_head, device="cpu"):
 def decode_q(seed, layer, num_seqs, n_q_heads, d_head, device="cpu"):
     """Queries [num_seqs, n_q_heads, d_head] of one decode step in one layer."""
     return _normal((num_seqs, n_q_heads, d_head), _mix(seed, 5, layer, 0), device)
+
+
+# ----------------------------------------------------------------------------
+# Prefix-cache workloads: prompts built from shared documents, and KV that is
+# a deterministic function of the whole prefix up to each position, so that a
+# reused block is right only if it holds exactly its own prefix's KV.
+# ----------------------------------------------------------------------------
+
+_M64 = (1 << 64) - 1
+
+
+def _splitmix(x):
+    x = (x + 0x9E3779B97F4A7C15) & _M64
+    x = ((x ^ (x >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    x = ((x ^ (x >> 27)) * 0x94D049BB133111EB) & _M64
+    return x ^ (x >> 31)
+
+
+def prompt_documents(seed, lengths, vocab=32000):
+    """Shared documents (system prompts, retrieved passages): token id lists
+    of the given lengths."""
+    rng = np.random.default_rng(int(seed))
+    return [[int(t) for t in rng.integers(0, vocab, size=int(n))] for n in lengths]
+
+
+def prefix_digests(tokens):
+    """One 64-bit digest per position, each covering every token up to and
+    including that position."""
+    out, h = [], 0x243F6A8885A308D3
+    for t in tokens:
+        h = _splitmix(h ^ (int(t) & 0xFFFFFFFF))
+        out.append(h)
+    return out
+
+
+def prefix_kv(seed, layer, tokens, start, end, n_kv_heads, d_head):
+    """Keys and values [end - start, n_kv_heads, d_head] (CPU bf16) for
+    positions start .. end-1 of a token sequence: each position's rows are
+    uniform on [-2, 2), drawn from a counter generator keyed by the digest of
+    its whole prefix, the layer and the seed."""
+    dig = np.array(prefix_digests(tokens[:end])[start:], dtype=np.uint64)
+    n = n_kv_heads * d_head
+    ctr = np.arange(2 * n, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        x = dig[:, None] ^ np.uint64((int(seed) * 0x632BE59BD9B4E019 + int(layer) * 0x8CB92BA72F3D8DD7) & _M64)
+        x = x + ctr[None, :] * np.uint64(0x9E3779B97F4A7C15)
+        x = (x ^ (x >> np.uint64(30))) * np.uint64(0xBF58476D1CE4E5B9)
+        x = (x ^ (x >> np.uint64(27))) * np.uint64(0x94D049BB133111EB)
+        x = x ^ (x >> np.uint64(31))
+    u = (x >> np.uint64(40)).astype(np.float64) / float(1 << 24) * 4.0 - 2.0
+    t = torch.from_numpy(u.astype(np.float32)).to(torch.bfloat16)
+    t = t.view(len(dig), 2, n_kv_heads, d_head)
+    return t[:, 0].contiguous(), t[:, 1].contiguous()
