@@ -195,6 +195,57 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
                              void* stream);
 
 /* ===========================================================================
+ * Prefill attention (causal, many query positions per sequence)
+ * ===========================================================================
+ * Operation ([P2] sections 4 and 8; [P1] sections 7 and 13): sequence s has
+ * context length C = context_lens[s], of which the last n = query_start[s+1]
+ * - query_start[s] positions are new; their keys and values must already be
+ * in the cache (pa_reshape_and_cache, earlier on the stream).  New position
+ * p = C - n + i (i = 0 .. n-1) is query row query_start[s] + i, and for each
+ * query head g (KV head g / G, as for decode)
+ *
+ *   out[row][g][:] = sum_{j <= p} a_j V_j,   a = softmax(scale * q[row][g] . K_j)
+ *
+ * over positions 0 .. p only (causal).  A whole prompt is n = C; a later
+ * chunk of a prompt, or the part of a prompt after a prefix-cache hit, is
+ * n < C.  Positions are read through block_tables as for decode.
+ *
+ * Scores and sums are fp32 (tensor cores, bf16 inputs); the softmax weights
+ * are rounded to bf16 before the weighted sum of values, so an output
+ * element can differ from the exact value by up to 2^-8 * sum_j a_j
+ * |V_j - out| besides fp32 rounding.
+ *
+ * Arguments
+ *   out           device [num_tokens][n_q_heads][d_head], bf16 or fp32 per
+ *                 out_dtype, 16-byte aligned.  Rows of tokens not covered by
+ *                 any sequence are not written.
+ *   q             device bf16 [num_tokens][n_q_heads][d_head], 16-byte aligned.
+ *   k_cache,
+ *   v_cache       device bf16 [num_blocks][n_kv_heads][block_size][d_head].
+ *   block_tables  device int32 [num_seqs][max_blocks_per_seq].
+ *   query_start   device int32 [num_seqs + 1], non-decreasing, query_start[0]
+ *                 >= 0 and query_start[num_seqs] <= num_tokens.
+ *   context_lens  device int32 [num_seqs], each >= its n.  A sequence with
+ *                 C < n, or C above max_blocks_per_seq * block_size, is
+ *                 flagged PA_DEV_BAD_CONTEXT (the first is skipped, the
+ *                 second clamped).
+ *   max_query_len host upper bound on every n (query rows beyond it are not
+ *                 computed).
+ *   n_q_heads / n_kv_heads must be a power of two <= 128; d_head 64 or 128;
+ *   block_size 8, 16 or 32.
+ *   status_dev    optional device int32, see PA_DEV_* above.
+ * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED or
+ * PA_ERR_CUDA.
+ */
+int pa_prefill(void* out, int out_dtype, const void* q,
+               const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int max_blocks_per_seq,
+               const int32_t* query_start, const int32_t* context_lens,
+               int num_seqs, int num_tokens, int max_query_len, int num_blocks,
+               int block_size, float scale, int n_q_heads, int n_kv_heads,
+               int d_head, int32_t* status_dev, void* stream);
+
+/* ===========================================================================
  * Cache writes
  * ===========================================================================
  * reshape_and_cache ([P1] section 16 item 3 and section 20: each newly

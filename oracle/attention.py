@@ -1,4 +1,5 @@
-"""Paged single-query (decode) attention, restated from its definition.
+"""Paged attention (single-query decode and causal prefill), restated from
+its definition.
 
 Oracle; test infrastructure only.  Everything here is float64 NumPy with
 plain loops over sequences, heads and blocks, so that a reader can check it
@@ -130,6 +131,60 @@ def dense_decode(q, K_dense, V_dense, context_lens, scale):
             h = kv_head_of(g, n_q_heads, n_kv_heads)
             out[s, g] = softmax_attention(q[s, g], K_dense[s, h, :ctx], V_dense[s, h, :ctx], scale)
     return out
+
+
+# ----------------------------------------------------------------------------
+# Prefill: many query positions per sequence, causal ([P2] sections 4 and 8)
+# ----------------------------------------------------------------------------
+
+def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, scale, block_size,
+                  with_spread=False):
+    """Causal attention of the new positions of each sequence.
+
+    Sequence s has context length C = context_lens[s]; its last
+    n = query_start[s+1] - query_start[s] positions are new.  New position
+    p = C - n + i is query row query_start[s] + i and attends to positions
+    0 .. p of its sequence only: during prefill a token cannot depend on the
+    tokens after it ([P2] section 4, causal attention; [P2] section 8, n
+    queries against up to n keys).  Keys and values are read through the
+    block table exactly as for decode.
+
+    q: [T, n_q_heads, d_head] float64 or uint16 bf16 bits; returns
+    [T, n_q_heads, d_head] float64 (rows not covered by any sequence are 0),
+    and with with_spread also weight_spread of every output row.
+    """
+    if q.dtype == np.uint16:
+        q = bf16_to_f64(q)
+    T, n_q_heads, d_head = q.shape
+    n_kv_heads = k_cache.shape[1]
+    out = np.zeros((T, n_q_heads, d_head), dtype=np.float64)
+    spread = np.zeros((T, n_q_heads, d_head), dtype=np.float64) if with_spread else None
+    for s in range(len(context_lens)):
+        C = int(context_lens[s])
+        row0, n = int(query_start[s]), int(query_start[s + 1]) - int(query_start[s])
+        if n <= 0:
+            continue
+        K, V = gather_kv(k_cache, v_cache, block_tables[s], C, block_size)
+        for i in range(n):
+            p = C - n + i
+            for g in range(n_q_heads):
+                h = kv_head_of(g, n_q_heads, n_kv_heads)
+                out[row0 + i, g] = softmax_attention(q[row0 + i, g], K[h, :p + 1], V[h, :p + 1], scale)
+                if with_spread:
+                    spread[row0 + i, g] = weight_spread(q[row0 + i, g], K[h, :p + 1], V[h, :p + 1], scale)
+    return (out, spread) if with_spread else out
+
+
+def weight_spread(q, K, V, scale):
+    """sum_j a_j |V_j - o| per output element, with a = softmax(scale q.K^T)
+    and o = a V: how far an output moves when every weight is perturbed by a
+    relative amount eps and the weights are renormalised (at most
+    eps / (1 - eps) times this)."""
+    s = scale * (K @ q)
+    e = np.exp(s - s.max())
+    a = e / e.sum()
+    o = a @ V
+    return a @ np.abs(V - o)
 
 
 # ----------------------------------------------------------------------------

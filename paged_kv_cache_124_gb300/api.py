@@ -67,6 +67,8 @@ _SIGS = {
                            _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
     "pa_decode_static_scratch": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_int, _c_int,
                                           _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
+    "pa_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                            _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp]),
     "pa_lse_merge": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                       _vp]),
@@ -201,6 +203,35 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, block_size, 
                         int(k_cache.shape[0]), int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
                         _opt_dev(status, torch.int32, "status"), _stream(stream))
     return _check(st, "pa_decode")
+
+
+def pa_prefill(out, q, k_cache, v_cache, block_tables, query_start, context_lens, max_query_len, block_size,
+               scale, n_q_heads, n_kv_heads, d_head, status=None, stream=None):
+    """out [T, Hq, D] (bf16 or f32) <- causal paged prefill attention of the
+    new positions of each sequence; see pa.h."""
+    if out.dtype == torch.bfloat16:
+        out_dtype = PA_DTYPE_BF16
+    elif out.dtype == torch.float32:
+        out_dtype = PA_DTYPE_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    num_tokens = q.shape[0]
+    if tuple(q.shape) != (num_tokens, n_q_heads, d_head) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("q/out must be [num_tokens, n_q_heads, d_head]")
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (n_kv_heads, block_size, d_head) or \
+            k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, n_kv_heads, block_size, d_head]")
+    num_seqs = block_tables.shape[0]
+    if block_tables.dim() != 2 or context_lens.shape != (num_seqs,) or query_start.shape != (num_seqs + 1,):
+        raise ValueError("block_tables [S, max_blocks], query_start [S + 1], context_lens [S]")
+    st = _lib.pa_prefill(_opt_dev(out, out.dtype, "out"), out_dtype, _dev(q, torch.bfloat16, "q"),
+                         _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+                         _dev(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
+                         _dev(query_start, torch.int32, "query_start"), _dev(context_lens, torch.int32, "context_lens"),
+                         int(num_seqs), int(num_tokens), int(max_query_len), int(k_cache.shape[0]), int(block_size),
+                         float(scale), int(n_q_heads), int(n_kv_heads), int(d_head),
+                         _opt_dev(status, torch.int32, "status"), _stream(stream))
+    return _check(st, "pa_prefill")
 
 
 PA_STATIC_SCRATCH_BYTES = 16 << 20

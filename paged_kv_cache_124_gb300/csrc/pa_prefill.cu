@@ -1,0 +1,627 @@
+// Paged prefill attention for sm_103a on the 5th-generation tensor cores.
+//
+// Operation ("PagedAttention in vLLM: scattered memory, exact attention",
+// sections 4 and 8; "PagedAttention: Virtual Memory for the KV Cache",
+// sections 7 and 13): a sequence with context length ctx whose last n
+// positions are new (their keys and values already written to the paged
+// cache) gets, for each new position p = ctx - n + i and each query head,
+//     o = softmax(scale * q . K[0..p]) V[0..p]
+// with K and V read through the block table (causal: a query sees only the
+// positions up to its own).  The whole prompt (n = ctx), a later chunk of it
+// (chunked prefill), or the suffix after a prefix-cache hit are all this
+// same call.
+//
+// Design (one CTA per 128 query rows of one KV head):
+//   * Rows are (token, grouped query head) pairs: 128 / G consecutive new
+//     tokens times the G query heads that share KV head h, so every K/V tile
+//     is read once for all G heads (GQA).  The Q tile is one 3-D TMA box.
+//   * K/V tiles of 128 positions are gathered through the block table with
+//     one 2-D TMA box (64 columns x B rows, 128-byte swizzle) per block and
+//     64-column half; blocks past the needed range, and bad table entries,
+//     are loaded from outside the tensor, which fills zeros and reads no HBM.
+//   * S = Q K^T (M 128, N 128, K d) and O += P V (M 128, N d, K 128) are
+//     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) issued by one thread;
+//     S is double-buffered in tensor memory (2 x 128 columns), O lives in
+//     tensor memory for the whole tile loop.  V is an MN-major operand read
+//     straight from the TMA layout.
+//   * Four softmax warps own one row each per thread (tensor-memory lane =
+//     row): mask, online maximum in the log2 domain, exp2, P rounded to bf16
+//     into shared memory (swizzled, K-major) for the second product, running
+//     sum.  O is rescaled in tensor memory only when a row's maximum grows by
+//     more than 2^8 (the weights stay below 256 otherwise), which is rare
+//     after the first tiles.
+//   * One warp issues the TMA copies two tiles ahead (2 stages); one warp
+//     issues the MMAs.  Every wait is bounded; on a timeout the CTA flags
+//     PA_DEV_WAIT_TIMEOUT, waits (bounded) for its own copies and products
+//     in flight, frees its tensor memory and returns.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <mutex>
+
+#include "pa_common.cuh"
+
+namespace {
+
+constexpr int kRows = 128;                 // MMA M: query rows per CTA
+constexpr int kKv = 128;                   // positions per K/V tile
+constexpr int kSoftmaxWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;        // S0, S1 (128 each), O (d)
+constexpr uint32_t kTmemO = 256;
+constexpr int kMaxProbes = 2000000;        // x <= ~1 us per probe
+constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest weight allowed before a rescale
+
+template <int D>
+struct PGeo {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kHalfBytes = kRows * 128;            // 128 rows of 64 bf16
+    static constexpr int kQBytes = kHalves * kHalfBytes;      // Q tile
+    static constexpr int kKVBytes = kHalves * kHalfBytes;     // one K (or V) tile of 128 positions
+    static constexpr int kPBytes = 2 * kHalfBytes;            // P tile: 128 rows x 128 positions
+    static constexpr int kQ = 0;
+    static constexpr int kStage0 = kQBytes;                   // stage s: K at +2s*KV, V right after
+    static constexpr int kP = kStage0 + 4 * kKVBytes;
+    static constexpr int kBars = kP + kPBytes;
+    // barriers, slots and alignment slack; at least 120 KiB so that two CTAs
+    // never share an SM (each holds 512 tensor-memory columns)
+    static constexpr int kSmem = kBars + 256 + 1024 > 120 * 1024 ? kBars + 256 + 1024 : 120 * 1024;
+};
+
+struct PrefillArgs {
+    void* out;
+    int out_f32;
+    const int32_t* block_tables;
+    int max_blocks;
+    const int32_t* query_start;
+    const int32_t* context_lens;
+    int num_seqs;
+    int num_tokens;
+    int tiles_per_seq;
+    int block_size;
+    int n_kv_heads;
+    int group;            // query heads per KV head
+    int tq;               // tokens per CTA = 128 / group
+    int n_q_heads;
+    int num_blocks;
+    int oob_row;          // a row coordinate past the end of the cache view
+    float scale_log2;     // scale * log2(e)
+    int32_t* status;
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t k_full[2];
+    uint64_t v_full[2];
+    uint64_t kv_empty[2];
+    uint64_t s_full[2];
+    uint64_t s_free[2];
+    uint64_t p_full;
+    uint64_t pv_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// --- tcgen05 / TMA wrappers --------------------------------------------------
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    // start address, leading and stride byte offsets (all >> 4), descriptor
+    // version 1, 128-byte swizzle
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo & 0x3FFFF) >> 4) << 16) |
+           ((uint64_t)((sbo & 0x3FFFF) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     pa::smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(pa::smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(pa::smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// --- bounded waits -------------------------------------------------------------
+
+// One thread.  Gives up when another role has aborted or after kMaxProbes
+// probes (then aborts the CTA and flags the timeout).
+__device__ bool wait1(uint64_t* bar, uint32_t parity, Bars* b, int32_t* status) {
+    for (int i = 0; i < kMaxProbes; ++i) {
+        if (pa::mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 63 && *reinterpret_cast<volatile int*>(&b->abort)) return false;
+    }
+    *reinterpret_cast<volatile int*>(&b->abort) = 1;
+    pa::set_status(status, PA_DEV_WAIT_TIMEOUT);
+    return false;
+}
+
+// Whole warp, warp-uniform result.
+__device__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* b, int32_t* status) {
+    for (int i = 0; i < kMaxProbes; ++i) {
+        const bool done = pa::mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, done)) return true;
+        if ((i & 63) == 63 && __any_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&b->abort) != 0))
+            return false;
+    }
+    if ((threadIdx.x & 31) == 0) {
+        *reinterpret_cast<volatile int*>(&b->abort) = 1;
+        pa::set_status(status, PA_DEV_WAIT_TIMEOUT);
+    }
+    __syncwarp();
+    return false;
+}
+
+// --- the kernel ------------------------------------------------------------------
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, const PrefillArgs a) {
+    using G = PGeo<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Bars* bars = reinterpret_cast<Bars*>(sm + G::kBars);
+    const uint32_t s_q = pa::smem_addr(sm + G::kQ);
+    const uint32_t s_p = pa::smem_addr(sm + G::kP);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // work item: heaviest tiles (latest tokens) launch first
+    const int seq = blockIdx.x % a.num_seqs;
+    const int tile = a.tiles_per_seq - 1 - (int)(blockIdx.x / a.num_seqs);
+    const int h = blockIdx.y;
+    const int q0 = a.query_start[seq];
+    const int n = a.query_start[seq + 1] - q0;
+    int ctx = a.context_lens[seq];
+    if (tile * a.tq >= n || q0 < 0) return;
+    if (ctx > a.max_blocks * a.block_size) {
+        if (threadIdx.x == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
+        ctx = a.max_blocks * a.block_size;
+    }
+    if (ctx < n) {
+        if (threadIdx.x == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
+        return;
+    }
+    const int last_tok = min(n, (tile + 1) * a.tq) - 1;
+    const int kv_end = ctx - n + last_tok + 1;          // keys needed: positions [0, kv_end)
+    const int n_tiles = (kv_end + kKv - 1) / kKv;
+    const int* table = a.block_tables + (size_t)seq * a.max_blocks;
+
+    if (threadIdx.x == 0) {
+        pa::mbar_init(&bars->q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            pa::mbar_init(&bars->k_full[i], 1);
+            pa::mbar_init(&bars->v_full[i], 1);
+            pa::mbar_init(&bars->kv_empty[i], 1);
+            pa::mbar_init(&bars->s_full[i], 1);
+            pa::mbar_init(&bars->s_free[i], kSoftmaxWarps * 32);
+        }
+        pa::mbar_init(&bars->p_full, kSoftmaxWarps * 32);
+        pa::mbar_init(&bars->pv_done, 1);
+        bars->abort = 0;
+        pa::fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         pa::smem_addr(&bars->tmem_base)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const int bpt = kKv / a.block_size;              // blocks per tile
+            pa::mbar_arrive_expect_tx(&bars->q_full, G::kQBytes);
+#pragma unroll
+            for (int hh = 0; hh < G::kHalves; ++hh)
+                tma_3d(s_q + hh * G::kHalfBytes, &mq, hh * 64, h * a.group, q0 + tile * a.tq, &bars->q_full);
+            int uses[2] = {0, 0};
+            for (int j = 0; j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !wait1(&bars->kv_empty[st], ((j >> 1) - 1) & 1, bars, a.status)) break;
+                int rows[16];
+                for (int i = 0; i < bpt; ++i) {
+                    const int pos = j * kKv + i * a.block_size;
+                    rows[i] = a.oob_row;
+                    if (pos < kv_end) {
+                        const int blk = table[pos / a.block_size];
+                        if (blk < 0 || blk >= a.num_blocks)
+                            pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
+                        else
+                            rows[i] = (blk * a.n_kv_heads + h) * a.block_size;
+                    }
+                }
+                const uint32_t s_k = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes);
+                const uint32_t s_v = s_k + G::kKVBytes;
+                pa::mbar_arrive_expect_tx(&bars->k_full[st], G::kKVBytes);
+                for (int i = 0; i < bpt; ++i)
+#pragma unroll
+                    for (int hh = 0; hh < G::kHalves; ++hh)
+                        tma_2d(s_k + hh * G::kHalfBytes + i * a.block_size * 128, &mk, hh * 64, rows[i],
+                               &bars->k_full[st]);
+                pa::mbar_arrive_expect_tx(&bars->v_full[st], G::kKVBytes);
+                for (int i = 0; i < bpt; ++i)
+#pragma unroll
+                    for (int hh = 0; hh < G::kHalves; ++hh)
+                        tma_2d(s_v + hh * G::kHalfBytes + i * a.block_size * 128, &mv, hh * 64, rows[i],
+                               &bars->v_full[st]);
+                ++uses[st];
+            }
+            // the copies this thread started must land before the CTA exits
+            pa::mbar_wait_bounded(&bars->q_full, 0, kMaxProbes);
+            for (int st = 0; st < 2; ++st)
+                if (uses[st]) {
+                    pa::mbar_wait_bounded(&bars->k_full[st], (uses[st] - 1) & 1, kMaxProbes);
+                    pa::mbar_wait_bounded(&bars->v_full[st], (uses[st] - 1) & 1, kMaxProbes);
+                }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_qk = idesc_bf16(kRows, kKv, 0);
+            constexpr uint32_t id_pv = idesc_bf16(kRows, D, 1);
+            uint64_t* last = nullptr;
+            uint32_t last_par = 0;
+            auto issue_qk = [&](int st, int sb) {
+                const uint32_t s_k = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * G::kHalfBytes + (kk & 3) * 32;
+                    mma_bf16(tmem + sb * kKv, smem_desc(s_q + off, 16, 1024), smem_desc(s_k + off, 16, 1024), id_qk,
+                             kk > 0);
+                }
+            };
+            bool ok = wait1(&bars->q_full, 0, bars, a.status) && wait1(&bars->k_full[0], 0, bars, a.status);
+            if (ok) {
+                tc_fence_after();
+                issue_qk(0, 0);
+                mma_commit(&bars->s_full[0]);
+                last = &bars->s_full[0];
+                last_par = 0;
+            }
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (j + 1 < n_tiles) {
+                    const int nst = (j + 1) & 1;
+                    ok = wait1(&bars->k_full[nst], ((j + 1) >> 1) & 1, bars, a.status);
+                    if (ok && j >= 1) ok = wait1(&bars->s_free[nst], ((j - 1) >> 1) & 1, bars, a.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_qk(nst, nst);
+                    mma_commit(&bars->s_full[nst]);
+                    last = &bars->s_full[nst];
+                    last_par = ((j + 1) >> 1) & 1;
+                }
+                ok = wait1(&bars->p_full, j & 1, bars, a.status) && wait1(&bars->v_full[st], (j >> 1) & 1, bars, a.status);
+                if (!ok) break;
+                const uint32_t s_v = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes + G::kKVBytes);
+                const int valid = min(kKv, kv_end - j * kKv);   // positions of this tile that are needed
+                const int ksteps = (valid + 15) >> 4;
+                // Positions past kv_end inside the last loaded block may hold
+                // anything (NaN included); their weights are 0, but 0 * NaN is
+                // not, so clear those V rows before the product reads them.
+                const int zero_end = min(ksteps * 16, ((kv_end + a.block_size - 1) / a.block_size) * a.block_size -
+                                                          j * kKv);
+                if (valid < zero_end) {
+                    uint8_t* v = sm + G::kStage0 + st * 2 * G::kKVBytes + G::kKVBytes;
+                    for (int r = valid; r < zero_end; ++r)
+#pragma unroll
+                        for (int hh = 0; hh < G::kHalves; ++hh) {
+                            uint4* row = reinterpret_cast<uint4*>(v + hh * G::kHalfBytes + r * 128);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                        }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                tc_fence_after();
+                for (int kk = 0; kk < ksteps; ++kk) {
+                    const uint64_t pa_ = smem_desc(s_p + (kk >> 2) * G::kHalfBytes + (kk & 3) * 32, 16, 1024);
+                    const uint64_t pb_ = smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024);
+                    mma_bf16(tmem + kTmemO, pa_, pb_, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars->pv_done);
+                mma_commit(&bars->kv_empty[st]);
+                last = &bars->kv_empty[st];
+                last_par = (j >> 1) & 1;
+            }
+            // products in flight must finish before the tensor memory is freed
+            if (last) pa::mbar_wait_bounded(last, last_par, kMaxProbes);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int r = threadIdx.x;                        // row = tensor-memory lane
+        const int t = r / a.group, g = r - t * a.group;
+        const int tok = tile * a.tq + t;
+        const bool valid_row = tok < n && q0 + tok < a.num_tokens;
+        const int row_lim = valid_row ? min(ctx - n + tok + 1, kv_end) : kv_end;   // keys [0, row_lim)
+        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        const uint32_t p_row = s_p + r * 128;
+        const uint32_t sw = (uint32_t)(r & 7);
+        for (int j = 0; j < n_tiles; ++j) {
+            const int sb = j & 1;
+            ok = wait_warp(&bars->s_full[sb], (j >> 1) & 1, bars, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            float s[kKv];
+#pragma unroll
+            for (int c = 0; c < kKv / 32; ++c) tmem_ld32(t_lane + sb * kKv + c * 32, s + c * 32);
+            tmem_wait_ld();
+            tc_fence_before();
+            pa::mbar_arrive(&bars->s_free[sb]);
+            const int lim = row_lim - j * kKv;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kKv; ++c) {
+                s[c] = c < lim ? s[c] * a.scale_log2 : -INFINITY;
+                mt = fmaxf(mt, s[c]);
+            }
+            const bool rescale = mt > m_used + kRescaleThreshold;
+            const float m_new = rescale ? mt : m_used;
+            const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;   // exp2(-inf) = 0 on the first tile
+            if (j >= 1) {
+                ok = wait_warp(&bars->pv_done, (j - 1) & 1, bars, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(t_lane + kTmemO + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(t_lane + kTmemO + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            l *= alpha;
+            m_used = m_new;
+#pragma unroll
+            for (int c8 = 0; c8 < kKv / 8; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = fast_exp2(s[c8 * 8 + 2 * e] - m_used);
+                    const float p1 = fast_exp2(s[c8 * 8 + 2 * e + 1] - m_used);
+                    w[e] = pack_bf16_rn(p0, p1);
+                    const float2 pr = pa::bf16x2_to_float2(w[e]);
+                    l += pr.x + pr.y;
+                }
+                const uint32_t addr = p_row + (c8 >> 3) * G::kHalfBytes + ((((uint32_t)c8 & 7) ^ sw) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                             "r"(w[2]), "r"(w[3])
+                             : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            pa::mbar_arrive(&bars->p_full);
+        }
+        if (ok) ok = wait_warp(&bars->pv_done, (n_tiles - 1) & 1, bars, a.status);
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            const size_t orow = ((size_t)(q0 + tok) * a.n_q_heads + (size_t)h * a.group + g) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(t_lane + kTmemO + c * 32, o);
+                tmem_wait_ld();
+                if (valid_row) {
+                    if (a.out_f32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                                 o[4 * i + 3] * inv);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(pack_bf16_rn(o[8 * i] * inv, o[8 * i + 1] * inv),
+                                                pack_bf16_rn(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                                                pack_bf16_rn(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                                                pack_bf16_rn(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// --- host side -------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_smem_done[64];
+
+template <int D>
+int launch(const PrefillArgs& a, const void* q, const void* k_cache, const void* v_cache, int num_tokens,
+           long long cache_rows, dim3 grid, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    const cuuint64_t qdims[3] = {(cuuint64_t)D, (cuuint64_t)a.n_q_heads, (cuuint64_t)num_tokens};
+    const cuuint64_t qstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.n_q_heads * D * 2};
+    const cuuint32_t qbox[3] = {64u, (cuuint32_t)a.group, (cuuint32_t)a.tq};
+    const cuuint64_t cdims[2] = {(cuuint64_t)D, (cuuint64_t)cache_rows};
+    const cuuint64_t cstr[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t cbox[2] = {64u, (cuuint32_t)a.block_size};
+    if (!encode(&mq, q, 3, qdims, qstr, qbox) || !encode(&mk, k_cache, 2, cdims, cstr, cbox) ||
+        !encode(&mv, v_cache, 2, cdims, cstr, cbox))
+        return PA_ERR_CUDA;
+    if (pa_host::ensure_smem_attr(prefill_kernel<D>, PGeo<D>::kSmem, g_smem_done) != cudaSuccess)
+        return PA_ERR_CUDA;
+    prefill_kernel<D><<<grid, kThreads, PGeo<D>::kSmem, st>>>(mq, mk, mv, a);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start,
+               const int32_t* context_lens, int num_seqs, int num_tokens, int max_query_len, int num_blocks,
+               int block_size, float scale, int n_q_heads, int n_kv_heads, int d_head, int32_t* status_dev,
+               void* stream) {
+    if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_blocks <= 0 || max_blocks_per_seq < 0 ||
+        n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
+        return PA_ERR_INVALID_ARG;
+    if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
+    if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head)) return PA_ERR_UNSUPPORTED;
+    const int group = n_q_heads / n_kv_heads;
+    if (group > kRows || kRows % group != 0) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !query_start || !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!pa_host::aligned16(out) || !pa_host::aligned16(q) || !pa_host::aligned16(k_cache) ||
+        !pa_host::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(query_start) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PA_ERR_MISALIGNED;
+    const long long cache_rows = (long long)num_blocks * n_kv_heads * block_size;
+    if (cache_rows > INT_MAX - 64 || (long long)max_blocks_per_seq * block_size > INT_MAX / 2 ||
+        n_kv_heads > 65535)
+        return PA_ERR_UNSUPPORTED;
+    const int tq = kRows / group;
+    const long long tiles = (max_query_len + tq - 1) / tq;
+    if (tiles * num_seqs > INT_MAX) return PA_ERR_UNSUPPORTED;
+
+    PrefillArgs a;
+    a.out = out;
+    a.out_f32 = out_dtype == PA_DTYPE_F32;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks_per_seq;
+    a.query_start = query_start;
+    a.context_lens = context_lens;
+    a.num_seqs = num_seqs;
+    a.num_tokens = num_tokens;
+    a.tiles_per_seq = (int)tiles;
+    a.block_size = block_size;
+    a.n_kv_heads = n_kv_heads;
+    a.group = group;
+    a.tq = tq;
+    a.n_q_heads = n_q_heads;
+    a.num_blocks = num_blocks;
+    a.oob_row = (int)cache_rows;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.status = status_dev;
+    const dim3 grid((unsigned)(tiles * num_seqs), (unsigned)n_kv_heads);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return d_head == 128 ? launch<128>(a, q, k_cache, v_cache, num_tokens, cache_rows, grid, st)
+                         : launch<64>(a, q, k_cache, v_cache, num_tokens, cache_rows, grid, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+"""GPU parity of pa_prefill (causal paged prefill on the tensor cores)
+against the oracle's paged_prefill, element by element, on seeded inputs:
+whole prompts, later chunks over a cached prefix, single new tokens, GQA
+group sizes 1 to 8, d_head 64 and 128, block sizes 8 to 32, bf16 and fp32
+outputs, NaN-filled pools (junk past every context), random placement."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from _gpu_util import assert_prefill_close, from_bits, out_to_f64, to_bits
+
+pytestmark = pytest.mark.gpu
+
+api = pytest.importorskip("paged_kv_cache_124_gb300.api")
+from paged_kv_cache_124_gb300 import inputs as I  # noqa: E402
+
+
+def _problem(seed, Hq, Hkv, D, B, ctxs, news, extra_blocks=7, extra_rows=0):
+    S = len(ctxs)
+    nblk = [-(-c // B) for c in ctxs]
+    NB = sum(nblk) + extra_blocks
+    perm = I.permutation(NB, seed)
+    MB = max(nblk + [1]) + 2
+    tables = np.full((S, MB), -1, dtype=np.int32)
+    kb = np.full((NB, Hkv, B, D), I.NAN_BF16_BITS, dtype=np.uint16)
+    vb = kb.copy()
+    pos = 0
+    for s, c in enumerate(ctxs):
+        k = to_bits(I.bf16_normal((Hkv, c, D), seed * 1000 + 2 * s))
+        v = to_bits(I.bf16_normal((Hkv, c, D), seed * 1000 + 2 * s + 1))
+        for lb in range(nblk[s]):
+            phys = int(perm[pos])
+            pos += 1
+            tables[s, lb] = phys
+            m = min(B, c - lb * B)
+            kb[phys, :, :m] = k[:, lb * B:lb * B + m]
+            vb[phys, :, :m] = v[:, lb * B:lb * B + m]
+    qs = np.concatenate([[0], np.cumsum(news)]).astype(np.int32)
+    T = int(qs[-1]) + extra_rows
+    qb = to_bits(I.bf16_normal((T, Hq, D), seed * 1000 + 999))
+    return qb, kb, vb, tables, qs, np.array(ctxs, dtype=np.int32)
+
+
+def _run(qb, kb, vb, tables, qs, ctx, B, Hq, Hkv, D, out_dtype, max_q=None, fill=None):
+    dev = lambda a: torch.from_numpy(a).cuda()
+    out = torch.full((qb.shape[0], Hq, D), float("nan") if fill is None else fill, dtype=out_dtype, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mq = int(np.diff(qs).max()) if max_q is None else max_q
+    api.pa_prefill(out, from_bits(qb), from_bits(kb), from_bits(vb), dev(tables), dev(qs), dev(ctx), mq, B,
+                   1.0 / math.sqrt(D), Hq, Hkv, D, status=status)
+    torch.cuda.synchronize()
+    return out, int(status.item())
+
+
+CASES = [
+    # name, Hq, Hkv, D, B, ctxs, news
+    ("g2_d64_b16_ragged", 4, 2, 64, 16, [1, 15, 16, 17, 40, 130], [1, 15, 16, 17, 7, 130]),
+    ("g4_d128_b16_8b", 32, 8, 128, 16, [300, 1000, 129, 257], [300, 129, 1, 33]),
+    ("g1_d128_b32_mha", 8, 8, 128, 32, [200, 500], [200, 64]),
+    ("g8_d128_b8", 32, 4, 128, 8, [100, 77, 260], [100, 20, 3]),
+    ("g4_d64_b32_chunks", 16, 4, 64, 32, [1024, 513], [256, 513]),
+]
+
+
+@pytest.mark.parametrize("name,Hq,Hkv,D,B,ctxs,news", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_prefill_matches_oracle(name, Hq, Hkv, D, B, ctxs, news, out_dtype):
+    qb, kb, vb, tab, qs, ctx = _problem(3, Hq, Hkv, D, B, ctxs, news)
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B, with_spread=True)
+    got, status = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, out_dtype)
+    assert status == 0
+    assert_prefill_close(out_to_f64(got), want, spread, out_dtype == torch.float32, name)
+
+
+def test_prefill_uncovered_rows_and_empty_sequences_untouched():
+    # a sequence with no new tokens in the middle, and two rows past the last sequence
+    qb, kb, vb, tab, qs, ctx = _problem(4, 8, 2, 128, 16, [50, 30, 90], [50, 0, 17], extra_rows=2)
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16, with_spread=True)
+    got, status = _run(qb, kb, vb, tab, qs, ctx, 16, 8, 2, 128, torch.float32, fill=-7.0)
+    assert status == 0
+    g = out_to_f64(got)
+    assert (g[67:] == -7.0).all()
+    assert_prefill_close(g[:67], want[:67], spread[:67], True, "covered rows")
+
+
+def test_prefill_equals_decode_for_single_tokens():
+    """n = 1 for every sequence is a decode step: both kernels agree with the
+    oracle, and with each other within the two tolerances."""
+    ctxs = [1, 17, 300, 1024]
+    qb, kb, vb, tab, qs, ctx = _problem(5, 32, 8, 128, 16, ctxs, [1] * 4)
+    got, status = _run(qb, kb, vb, tab, qs, ctx, 16, 32, 8, 128, torch.float32)
+    assert status == 0
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16, with_spread=True)
+    assert_prefill_close(out_to_f64(got), want, spread, True, "n=1")
+    np.testing.assert_array_equal(want, A.paged_decode(qb, kb, vb, tab, ctx, 1.0 / math.sqrt(128), 16))
+
+
+def test_prefill_chunked_equals_whole_prompt():
+    """The last chunk of a prompt computed alone over the cached prefix gives
+    the rows of the whole-prompt pass (same kernel, same tiles of keys)."""
+    L, cut = 700, 300
+    qb, kb, vb, tab, qs, ctx = _problem(6, 32, 8, 128, 16, [L], [L])
+    whole, st1 = _run(qb, kb, vb, tab, qs, ctx, 16, 32, 8, 128, torch.float32)
+    part, st2 = _run(qb[cut:], kb, vb, tab, np.array([0, L - cut], np.int32), ctx, 16, 32, 8, 128, torch.float32)
+    assert st1 == st2 == 0
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16, with_spread=True)
+    assert_prefill_close(out_to_f64(part), want[cut:], spread[cut:], True, "chunk")
+    assert_prefill_close(out_to_f64(whole), want, spread, True, "whole")
+
+
+def test_prefill_device_flags():
+    qb, kb, vb, tab, qs, ctx = _problem(7, 8, 2, 64, 16, [40, 20], [40, 20])
+    bad_ctx = ctx.copy()
+    bad_ctx[1] = 10                                 # fewer positions than new tokens
+    got, status = _run(qb, kb, vb, tab, qs, bad_ctx, 16, 8, 2, 64, torch.float32, fill=-3.0)
+    assert status & api.PA_DEV_BAD_CONTEXT
+    assert (out_to_f64(got)[40:] == -3.0).all()
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs[:2], ctx[:1], 1.0 / 8.0, 16, with_spread=True)
+    assert_prefill_close(out_to_f64(got)[:40], want[:40], spread[:40], True, "good sequence")
+    bad_tab = tab.copy()
+    bad_tab[0, 1] = kb.shape[0] + 5                 # outside the pool
+    _, status = _run(qb, kb, vb, bad_tab, qs, ctx, 16, 8, 2, 64, torch.float32)
+    assert status & api.PA_DEV_BAD_BLOCK_ID
+
+
+def test_prefill_host_errors():
+    qb, kb, vb, tab, qs, ctx = _problem(8, 6, 2, 64, 16, [20], [20])
+    with pytest.raises(api.PAError) as e:         # G = 3 does not divide 128
+        _run(qb, kb, vb, tab, qs, ctx, 16, 6, 2, 64, torch.float32)
+    assert e.value.status == api.PA_ERR_UNSUPPORTED
+    qb, kb, vb, tab, qs, ctx = _problem(8, 8, 2, 64, 16, [20], [20])
+    q, k, v = from_bits(qb), from_bits(kb), from_bits(vb)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    out = torch.full(q.shape, -1.0, dtype=torch.float32, device="cuda")
+    # nothing to compute: returns at once and writes nothing
+    api.pa_prefill(out, q, k, v, dev(tab), dev(qs), dev(ctx), 0, 16, 0.125, 8, 2, 64)
+    torch.cuda.synchronize()
+    assert (out == -1.0).all()
+    with pytest.raises(api.PAError) as e:         # misaligned q
+        flat = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+        q_mis = flat[1:1 + q.numel()].view(q.shape)
+        api.pa_prefill(out, q_mis, k, v, dev(tab), dev(qs), dev(ctx), 20, 16, 0.125, 8, 2, 64)
+    assert e.value.status == api.PA_ERR_MISALIGNED
