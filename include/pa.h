@@ -211,9 +211,9 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
  * n < C.  Positions are read through block_tables as for decode.
  *
  * Scores and sums are fp32 (tensor cores, bf16 inputs); the softmax weights
- * are rounded to bf16 before the weighted sum of values, so an output
- * element can differ from the exact value by up to 2^-8 * sum_j a_j
- * |V_j - out| besides fp32 rounding.
+ * are rounded to bf16 before the weighted sum of values (the normaliser sums
+ * them unrounded), so an output element can differ from the exact value by
+ * up to 2^-8 * sum_j a_j |V_j| besides fp32 rounding.
  *
  * Arguments
  *   out           device [num_tokens][n_q_heads][d_head], bf16 or fp32 per

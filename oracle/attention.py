@@ -176,15 +176,14 @@ def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, 
 
 
 def weight_spread(q, K, V, scale):
-    """sum_j a_j |V_j - o| per output element, with a = softmax(scale q.K^T)
-    and o = a V: how far an output moves when every weight is perturbed by a
-    relative amount eps and the weights are renormalised (at most
-    eps / (1 - eps) times this)."""
+    """sum_j a_j |V_j| per output element, with a = softmax(scale q.K^T):
+    how far o = a V can move when every weight in the weighted sum is
+    perturbed by a relative amount eps while the normaliser is kept (at most
+    eps times this)."""
     s = scale * (K @ q)
     e = np.exp(s - s.max())
     a = e / e.sum()
-    o = a @ V
-    return a @ np.abs(V - o)
+    return a @ np.abs(V)
 
 
 # ----------------------------------------------------------------------------

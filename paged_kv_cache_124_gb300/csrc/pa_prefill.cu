@@ -11,29 +11,34 @@
 // (chunked prefill), or the suffix after a prefix-cache hit are all this
 // same call.
 //
-// Design (one CTA per 128 query rows of one KV head):
+// Design (one CTA per two tiles of 128 query rows of one KV head):
 //   * Rows are (token, grouped query head) pairs: 128 / G consecutive new
 //     tokens times the G query heads that share KV head h, so every K/V tile
-//     is read once for all G heads (GQA).  The Q tile is one 3-D TMA box.
+//     is read once for all G heads (GQA).  Each Q tile is one 3-D TMA box;
+//     the CTA's two tiles (A, B) are consecutive token ranges and share every
+//     K/V tile.
 //   * K/V tiles of 128 positions are gathered through the block table with
 //     one 2-D TMA box (64 columns x B rows, 128-byte swizzle) per block and
-//     64-column half; blocks past the needed range, and bad table entries,
-//     are loaded from outside the tensor, which fills zeros and reads no HBM.
+//     64-column half, two tiles ahead; blocks past the needed range, and bad
+//     table entries, are loaded from outside the tensor, which fills zeros
+//     and reads no HBM.
 //   * S = Q K^T (M 128, N 128, K d) and O += P V (M 128, N d, K 128) are
-//     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) issued by one thread;
-//     S is double-buffered in tensor memory (2 x 128 columns), O lives in
-//     tensor memory for the whole tile loop.  V is an MN-major operand read
-//     straight from the TMA layout.
-//   * Four softmax warps own one row each per thread (tensor-memory lane =
-//     row): mask, online maximum in the log2 domain, exp2, P rounded to bf16
-//     into shared memory (swizzled, K-major) for the second product, running
-//     sum.  O is rescaled in tensor memory only when a row's maximum grows by
-//     more than 2^8 (the weights stay below 256 otherwise), which is rare
-//     after the first tiles.
-//   * One warp issues the TMA copies two tiles ahead (2 stages); one warp
-//     issues the MMAs.  Every wait is bounded; on a timeout the CTA flags
-//     PA_DEV_WAIT_TIMEOUT, waits (bounded) for its own copies and products
-//     in flight, frees its tensor memory and returns.
+//     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) issued by one thread.
+//     Tensor memory holds S_A, S_B (128 columns each) and O_A, O_B (d
+//     columns each) for the whole loop.  P (bf16) is written over the first
+//     64 columns of its own S and read from there as the A operand of the
+//     second product; V is an MN-major operand read straight from the TMA
+//     layout.
+//   * Two softmax warpgroups, one per Q tile, own one row per thread
+//     (tensor-memory lane = row): mask, online maximum in the log2 domain,
+//     exp2, running sum, P.  The product order S_A(j), S_B(j), PV_A(j),
+//     S_A(j+1), PV_B(j), S_B(j+1), ... keeps the tensor pipe busy with one
+//     tile while the other tile's softmax runs.  O is rescaled in tensor
+//     memory only when a row's maximum grows by more than 2^8 (the weights
+//     stay below 256 otherwise), which is rare after the first tiles.
+//   * Every wait is bounded; on a timeout the CTA flags PA_DEV_WAIT_TIMEOUT,
+//     waits (bounded) for its own copies and products in flight, frees its
+//     tensor memory and returns.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -45,14 +50,14 @@
 
 namespace {
 
-constexpr int kRows = 128;                 // MMA M: query rows per CTA
+constexpr int kRows = 128;                 // MMA M: query rows per tile
 constexpr int kKv = 128;                   // positions per K/V tile
-constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;        // S0, S1 (128 each), O (d)
-constexpr uint32_t kTmemO = 256;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;              // 2 softmax warpgroups, producer, MMA
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS0 = 0;            // S_A; S_B at +128
+constexpr uint32_t kTmemO0 = 256;          // O_A; O_B at +128
 constexpr int kMaxProbes = 2000000;        // x <= ~1 us per probe
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest weight allowed before a rescale
 
@@ -60,13 +65,11 @@ template <int D>
 struct PGeo {
     static constexpr int kHalves = D / 64;
     static constexpr int kHalfBytes = kRows * 128;            // 128 rows of 64 bf16
-    static constexpr int kQBytes = kHalves * kHalfBytes;      // Q tile
+    static constexpr int kQBytes = kHalves * kHalfBytes;      // one Q tile
     static constexpr int kKVBytes = kHalves * kHalfBytes;     // one K (or V) tile of 128 positions
-    static constexpr int kPBytes = 2 * kHalfBytes;            // P tile: 128 rows x 128 positions
-    static constexpr int kQ = 0;
-    static constexpr int kStage0 = kQBytes;                   // stage s: K at +2s*KV, V right after
-    static constexpr int kP = kStage0 + 4 * kKVBytes;
-    static constexpr int kBars = kP + kPBytes;
+    static constexpr int kQ = 0;                              // Q_A, then Q_B
+    static constexpr int kStage0 = 2 * kQBytes;               // stage s: K at +2s*KV, V right after
+    static constexpr int kBars = kStage0 + 4 * kKVBytes;
     // barriers, slots and alignment slack; at least 120 KiB so that two CTAs
     // never share an SM (each holds 512 tensor-memory columns)
     static constexpr int kSmem = kBars + 256 + 1024 > 120 * 1024 ? kBars + 256 + 1024 : 120 * 1024;
@@ -81,11 +84,11 @@ struct PrefillArgs {
     const int32_t* context_lens;
     int num_seqs;
     int num_tokens;
-    int tiles_per_seq;
+    int tiles_per_seq;    // CTAs per sequence (each covers 2 * tq tokens)
     int block_size;
     int n_kv_heads;
     int group;            // query heads per KV head
-    int tq;               // tokens per CTA = 128 / group
+    int tq;               // tokens per Q tile = 128 / group
     int n_q_heads;
     int num_blocks;
     int oob_row;          // a row coordinate past the end of the cache view
@@ -98,10 +101,9 @@ struct Bars {
     uint64_t k_full[2];
     uint64_t v_full[2];
     uint64_t kv_empty[2];
-    uint64_t s_full[2];
-    uint64_t s_free[2];
-    uint64_t p_full;
-    uint64_t pv_done;
+    uint64_t s_full[2];   // per Q tile: its scores are in tensor memory
+    uint64_t p_full[2];   // per Q tile: its weights are in tensor memory (and O rescaled)
+    uint64_t o_done[2];   // per Q tile: its last product has finished
     uint32_t tmem_base;
     int abort;
 };
@@ -167,6 +169,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]),
+        "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]),
+        "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]), "r"(w[24]),
+        "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31]));
+}
+
+// A operand from tensor memory (M rows in lanes, two bf16 per column).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                            uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -239,7 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars* bars = reinterpret_cast<Bars*>(sm + G::kBars);
     const uint32_t s_q = pa::smem_addr(sm + G::kQ);
-    const uint32_t s_p = pa::smem_addr(sm + G::kP);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // work item: heaviest tiles (latest tokens) launch first
@@ -249,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q0 = a.query_start[seq];
     const int n = a.query_start[seq + 1] - q0;
     int ctx = a.context_lens[seq];
-    if (tile * a.tq >= n || q0 < 0) return;
+    const int t0 = tile * 2 * a.tq;                      // first token of tile A
+    if (t0 >= n || q0 < 0) return;
     if (ctx > a.max_blocks * a.block_size) {
         if (threadIdx.x == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
         ctx = a.max_blocks * a.block_size;
@@ -258,9 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
         return;
     }
-    const int last_tok = min(n, (tile + 1) * a.tq) - 1;
-    const int kv_end = ctx - n + last_tok + 1;          // keys needed: positions [0, kv_end)
-    const int n_tiles = (kv_end + kKv - 1) / kKv;
+    const bool has_b = t0 + a.tq < n;
+    // keys needed by each Q tile: positions [0, kv_end[x])
+    const int kv_end0 = ctx - n + min(n, t0 + a.tq);
+    const int kv_end1 = ctx - n + min(n, t0 + 2 * a.tq);
+    const int nt0 = (kv_end0 + kKv - 1) / kKv;
+    const int nt1 = has_b ? (kv_end1 + kKv - 1) / kKv : 0;
+    const int kv_all = has_b ? kv_end1 : kv_end0;
+    const int n_tiles = has_b ? nt1 : nt0;
     const int* table = a.block_tables + (size_t)seq * a.max_blocks;
 
     if (threadIdx.x == 0) {
@@ -270,10 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             pa::mbar_init(&bars->v_full[i], 1);
             pa::mbar_init(&bars->kv_empty[i], 1);
             pa::mbar_init(&bars->s_full[i], 1);
-            pa::mbar_init(&bars->s_free[i], kSoftmaxWarps * 32);
+            pa::mbar_init(&bars->p_full[i], kRows);
+            pa::mbar_init(&bars->o_done[i], 1);
         }
-        pa::mbar_init(&bars->p_full, kSoftmaxWarps * 32);
-        pa::mbar_init(&bars->pv_done, 1);
         bars->abort = 0;
         pa::fence_mbar_init();
     }
@@ -292,10 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const int bpt = kKv / a.block_size;              // blocks per tile
-            pa::mbar_arrive_expect_tx(&bars->q_full, G::kQBytes);
+            pa::mbar_arrive_expect_tx(&bars->q_full, (has_b ? 2 : 1) * G::kQBytes);
+            for (int x = 0; x < (has_b ? 2 : 1); ++x)
 #pragma unroll
-            for (int hh = 0; hh < G::kHalves; ++hh)
-                tma_3d(s_q + hh * G::kHalfBytes, &mq, hh * 64, h * a.group, q0 + tile * a.tq, &bars->q_full);
+                for (int hh = 0; hh < G::kHalves; ++hh)
+                    tma_3d(s_q + x * G::kQBytes + hh * G::kHalfBytes, &mq, hh * 64, h * a.group,
+                           q0 + t0 + x * a.tq, &bars->q_full);
             int uses[2] = {0, 0};
             for (int j = 0; j < n_tiles; ++j) {
                 const int st = j & 1;
@@ -304,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < bpt; ++i) {
                     const int pos = j * kKv + i * a.block_size;
                     rows[i] = a.oob_row;
-                    if (pos < kv_end) {
+                    if (pos < kv_all) {
                         const int blk = table[pos / a.block_size];
                         if (blk < 0 || blk >= a.num_blocks)
                             pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
@@ -341,154 +368,164 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(kRows, kKv, 0);
             constexpr uint32_t id_pv = idesc_bf16(kRows, D, 1);
+            const int nt[2] = {nt0, nt1};
+            const int kv_end[2] = {kv_end0, kv_end1};
             uint64_t* last = nullptr;
             uint32_t last_par = 0;
-            auto issue_qk = [&](int st, int sb) {
+            auto commit = [&](uint64_t* bar, uint32_t par) {
+                mma_commit(bar);
+                last = bar;
+                last_par = par;
+            };
+            auto issue_s = [&](int x, int st) {
                 const uint32_t s_k = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes);
+                const uint32_t qx = s_q + x * G::kQBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * G::kHalfBytes + (kk & 3) * 32;
-                    mma_bf16(tmem + sb * kKv, smem_desc(s_q + off, 16, 1024), smem_desc(s_k + off, 16, 1024), id_qk,
-                             kk > 0);
+                    mma_bf16(tmem + kTmemS0 + x * 128, smem_desc(qx + off, 16, 1024),
+                             smem_desc(s_k + off, 16, 1024), id_qk, kk > 0);
                 }
             };
             bool ok = wait1(&bars->q_full, 0, bars, a.status) && wait1(&bars->k_full[0], 0, bars, a.status);
             if (ok) {
                 tc_fence_after();
-                issue_qk(0, 0);
-                mma_commit(&bars->s_full[0]);
-                last = &bars->s_full[0];
-                last_par = 0;
+                issue_s(0, 0);
+                commit(&bars->s_full[0], 0);
+                if (has_b) {
+                    issue_s(1, 0);
+                    commit(&bars->s_full[1], 0);
+                }
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j & 1;
-                if (j + 1 < n_tiles) {
-                    const int nst = (j + 1) & 1;
-                    ok = wait1(&bars->k_full[nst], ((j + 1) >> 1) & 1, bars, a.status);
-                    if (ok && j >= 1) ok = wait1(&bars->s_free[nst], ((j - 1) >> 1) & 1, bars, a.status);
+                ok = wait1(&bars->v_full[st], (j >> 1) & 1, bars, a.status);
+                if (!ok) break;
+                uint8_t* vbase = sm + G::kStage0 + st * 2 * G::kKVBytes + G::kKVBytes;
+                const uint32_t s_v = pa::smem_addr(vbase);
+                if (j == n_tiles - 1) {
+                    // Positions past the last needed one inside its block may
+                    // hold anything (NaN included); their weights are 0, but
+                    // 0 * NaN is not, so clear those V rows first.
+                    const int valid = kv_all - j * kKv;
+                    const int zero_end = min(((valid + 15) >> 4) << 4,
+                                             ((kv_all + a.block_size - 1) / a.block_size) * a.block_size - j * kKv);
+                    if (valid < zero_end) {
+                        for (int r = valid; r < zero_end; ++r)
+#pragma unroll
+                            for (int hh = 0; hh < G::kHalves; ++hh) {
+                                uint4* row = reinterpret_cast<uint4*>(vbase + hh * G::kHalfBytes + r * 128);
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                            }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                }
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if (j >= nt[x]) continue;
+                    ok = wait1(&bars->p_full[x], j & 1, bars, a.status);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk(nst, nst);
-                    mma_commit(&bars->s_full[nst]);
-                    last = &bars->s_full[nst];
-                    last_par = ((j + 1) >> 1) & 1;
+                    const int ksteps = (min(kKv, kv_end[x] - j * kKv) + 15) >> 4;
+                    for (int kk = 0; kk < ksteps; ++kk)
+                        mma_bf16_ta(tmem + kTmemO0 + x * 128, tmem + kTmemS0 + x * 128 + kk * 8,
+                                    smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    if (j == nt[x] - 1) commit(&bars->o_done[x], 0);
+                    if (j + 1 < nt[x]) {
+                        const int nst = (j + 1) & 1;
+                        ok = wait1(&bars->k_full[nst], ((j + 1) >> 1) & 1, bars, a.status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(x, nst);
+                        commit(&bars->s_full[x], (j + 1) & 1);
+                    }
                 }
-                ok = wait1(&bars->p_full, j & 1, bars, a.status) && wait1(&bars->v_full[st], (j >> 1) & 1, bars, a.status);
                 if (!ok) break;
-                const uint32_t s_v = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes + G::kKVBytes);
-                const int valid = min(kKv, kv_end - j * kKv);   // positions of this tile that are needed
-                const int ksteps = (valid + 15) >> 4;
-                // Positions past kv_end inside the last loaded block may hold
-                // anything (NaN included); their weights are 0, but 0 * NaN is
-                // not, so clear those V rows before the product reads them.
-                const int zero_end = min(ksteps * 16, ((kv_end + a.block_size - 1) / a.block_size) * a.block_size -
-                                                          j * kKv);
-                if (valid < zero_end) {
-                    uint8_t* v = sm + G::kStage0 + st * 2 * G::kKVBytes + G::kKVBytes;
-                    for (int r = valid; r < zero_end; ++r)
-#pragma unroll
-                        for (int hh = 0; hh < G::kHalves; ++hh) {
-                            uint4* row = reinterpret_cast<uint4*>(v + hh * G::kHalfBytes + r * 128);
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
-                        }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                }
-                tc_fence_after();
-                for (int kk = 0; kk < ksteps; ++kk) {
-                    const uint64_t pa_ = smem_desc(s_p + (kk >> 2) * G::kHalfBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t pb_ = smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024);
-                    mma_bf16(tmem + kTmemO, pa_, pb_, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(&bars->pv_done);
-                mma_commit(&bars->kv_empty[st]);
-                last = &bars->kv_empty[st];
-                last_par = (j >> 1) & 1;
+                commit(&bars->kv_empty[st], (j >> 1) & 1);
             }
             // products in flight must finish before the tensor memory is freed
             if (last) pa::mbar_wait_bounded(last, last_par, kMaxProbes);
         }
     } else {
-        // ------------------------------------------------------------ softmax warps
-        const int r = threadIdx.x;                        // row = tensor-memory lane
+        // ------------------------------------------------------------ softmax warpgroups
+        const int x = warp >> 2;                          // Q tile of this warpgroup
+        const int r = threadIdx.x & (kRows - 1);          // row = tensor-memory lane
         const int t = r / a.group, g = r - t * a.group;
-        const int tok = tile * a.tq + t;
+        const int tok = t0 + x * a.tq + t;
         const bool valid_row = tok < n && q0 + tok < a.num_tokens;
+        const int kv_end = x ? kv_end1 : kv_end0;
+        const int ntx = x ? nt1 : nt0;
         const int row_lim = valid_row ? min(ctx - n + tok + 1, kv_end) : kv_end;   // keys [0, row_lim)
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t t_s = t_lane + kTmemS0 + x * 128;
+        const uint32_t t_o = t_lane + kTmemO0 + x * 128;
+        const float c2 = a.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        const uint32_t p_row = s_p + r * 128;
-        const uint32_t sw = (uint32_t)(r & 7);
-        for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j & 1;
-            ok = wait_warp(&bars->s_full[sb], (j >> 1) & 1, bars, a.status);
+        for (int j = 0; j < ntx; ++j) {
+            ok = wait_warp(&bars->s_full[x], j & 1, bars, a.status);
             if (!ok) break;
             tc_fence_after();
             float s[kKv];
 #pragma unroll
-            for (int c = 0; c < kKv / 32; ++c) tmem_ld32(t_lane + sb * kKv + c * 32, s + c * 32);
+            for (int c = 0; c < kKv / 32; ++c) tmem_ld32(t_s + c * 32, s + c * 32);
             tmem_wait_ld();
-            tc_fence_before();
-            pa::mbar_arrive(&bars->s_free[sb]);
             const int lim = row_lim - j * kKv;
             float mt = -INFINITY;
+            if (lim >= kKv) {
 #pragma unroll
-            for (int c = 0; c < kKv; ++c) {
-                s[c] = c < lim ? s[c] * a.scale_log2 : -INFINITY;
-                mt = fmaxf(mt, s[c]);
+                for (int c = 0; c < kKv; ++c) mt = fmaxf(mt, s[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kKv; ++c) {
+                    s[c] = c < lim ? s[c] : -INFINITY;
+                    mt = fmaxf(mt, s[c]);
+                }
             }
-            const bool rescale = mt > m_used + kRescaleThreshold;
-            const float m_new = rescale ? mt : m_used;
+            const float mts = mt * c2;                    // scale > 0: the maximum commutes with it
+            const bool rescale = mts > m_used + kRescaleThreshold;
+            const float m_new = rescale ? mts : m_used;
             const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;   // exp2(-inf) = 0 on the first tile
-            if (j >= 1) {
-                ok = wait_warp(&bars->pv_done, (j - 1) & 1, bars, a.status);
-                if (!ok) break;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
+            if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+                // O holds the products of tiles < j (complete: this tile's
+                // scores were issued after them) and not yet this tile's
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(t_lane + kTmemO + c * 32, o);
-                        tmem_wait_ld();
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(t_o + c * 32, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(t_lane + kTmemO + c * 32, o);
-                    }
-                    tmem_wait_st();
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tmem_st32(t_o + c * 32, o);
                 }
             }
             l *= alpha;
             m_used = m_new;
+            const float neg = -m_used;
+            uint32_t w[kKv / 2];
 #pragma unroll
-            for (int c8 = 0; c8 < kKv / 8; ++c8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(s[c8 * 8 + 2 * e] - m_used);
-                    const float p1 = fast_exp2(s[c8 * 8 + 2 * e + 1] - m_used);
-                    w[e] = pack_bf16_rn(p0, p1);
-                    const float2 pr = pa::bf16x2_to_float2(w[e]);
-                    l += pr.x + pr.y;
-                }
-                const uint32_t addr = p_row + (c8 >> 3) * G::kHalfBytes + ((((uint32_t)c8 & 7) ^ sw) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                             "r"(w[2]), "r"(w[3])
-                             : "memory");
+            for (int i = 0; i < kKv / 2; ++i) {
+                const float p0 = fast_exp2(fmaf(s[2 * i], c2, neg));
+                const float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg));
+                l += p0 + p1;
+                w[i] = pack_bf16_rn(p0, p1);
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tmem_st32u(t_s, w);
+            tmem_st32u(t_s + 32, w + 32);
+            tmem_wait_st();
             tc_fence_before();
-            pa::mbar_arrive(&bars->p_full);
+            pa::mbar_arrive(&bars->p_full[x]);
         }
-        if (ok) ok = wait_warp(&bars->pv_done, (n_tiles - 1) & 1, bars, a.status);
-        if (ok) {
+        if (ok && ntx > 0) ok = wait_warp(&bars->o_done[x], 0, bars, a.status);
+        if (ok && ntx > 0) {
             tc_fence_after();
             const float inv = 1.f / l;
             const size_t orow = ((size_t)(q0 + tok) * a.n_q_heads + (size_t)h * a.group + g) * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
-                tmem_ld32(t_lane + kTmemO + c * 32, o);
+                tmem_ld32(t_o + c * 32, o);
                 tmem_wait_ld();
                 if (valid_row) {
                     if (a.out_f32) {
@@ -547,7 +584,8 @@ bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_smem_done[64];
+template <int D>
+int g_smem_done[64];   // per kernel instantiation: bytes opted in, by device
 
 template <int D>
 int launch(const PrefillArgs& a, const void* q, const void* k_cache, const void* v_cache, int num_tokens,
@@ -562,7 +600,7 @@ int launch(const PrefillArgs& a, const void* q, const void* k_cache, const void*
     if (!encode(&mq, q, 3, qdims, qstr, qbox) || !encode(&mk, k_cache, 2, cdims, cstr, cbox) ||
         !encode(&mv, v_cache, 2, cdims, cstr, cbox))
         return PA_ERR_CUDA;
-    if (pa_host::ensure_smem_attr(prefill_kernel<D>, PGeo<D>::kSmem, g_smem_done) != cudaSuccess)
+    if (pa_host::ensure_smem_attr(prefill_kernel<D>, PGeo<D>::kSmem, g_smem_done<D>) != cudaSuccess)
         return PA_ERR_CUDA;
     prefill_kernel<D><<<grid, kThreads, PGeo<D>::kSmem, st>>>(mq, mk, mv, a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -596,7 +634,7 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
         n_kv_heads > 65535)
         return PA_ERR_UNSUPPORTED;
     const int tq = kRows / group;
-    const long long tiles = (max_query_len + tq - 1) / tq;
+    const long long tiles = (max_query_len + 2 * tq - 1) / (2 * tq);
     if (tiles * num_seqs > INT_MAX) return PA_ERR_UNSUPPORTED;
 
     PrefillArgs a;

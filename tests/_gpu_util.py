@@ -42,11 +42,11 @@ def assert_attention_close(got, ref, f32_out, what=""):
 
 
 # Prefill rounds the softmax weights to bf16 (unit roundoff 2^-8) before the
-# weighted sum of values.  Perturbing every weight by a relative eps and
-# renormalising moves an output element by at most eps / (1 - eps) times
-# sum_j a_j |V_j - o| (the oracle's weight_spread), so that term is added to
-# the decode tolerance.
-P_ROUND = 2.0 ** -8 / (1 - 2.0 ** -8)
+# weighted sum of values, and normalises by the sum of the unrounded weights.
+# Perturbing every weight of the sum by a relative eps moves an output
+# element by at most eps times sum_j a_j |V_j| (the oracle's weight_spread),
+# so that term is added to the decode tolerance.
+P_ROUND = 2.0 ** -8
 
 
 def assert_prefill_close(got, ref, spread, f32_out, what=""):

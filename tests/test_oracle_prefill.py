@@ -129,14 +129,14 @@ def test_rows_outside_every_sequence_stay_zero():
 
 
 def test_weight_spread_closed_forms():
-    # one dominant position: the output is its value row and nothing spreads
+    # one dominant position: the weighted absolute value is that row's
     K = np.array([[1000.0], [0.0]])
-    V = np.array([[3.0, -1.0], [5.0, 7.0]])
-    np.testing.assert_allclose(A.weight_spread(np.array([1.0]), K, V, 1.0), [0.0, 0.0], atol=1e-300)
-    # two equal weights: o is the mean and the spread is half the gap
+    V = np.array([[3.0, -1.0], [5.0, -7.0]])
+    np.testing.assert_allclose(A.weight_spread(np.array([1.0]), K, V, 1.0), [3.0, 1.0])
+    # two equal weights: the mean absolute value
     K = np.array([[0.0], [0.0]])
-    np.testing.assert_allclose(A.weight_spread(np.array([1.0]), K, V, 1.0), [1.0, 4.0])
-    # perturbing weights by at most eps moves o by at most eps/(1-eps) * spread
+    np.testing.assert_allclose(A.weight_spread(np.array([1.0]), K, V, 1.0), [4.0, 4.0])
+    # perturbing each weight by at most eps (normaliser kept) moves o by at most eps * spread
     rng = np.random.default_rng(58)
     K, V, q = rng.normal(size=(50, 4)), rng.normal(size=(50, 3)), rng.normal(size=4)
     s = K @ q
@@ -145,5 +145,5 @@ def test_weight_spread_closed_forms():
     worst = np.zeros(3)
     for _ in range(200):
         at = a * (1 + rng.uniform(-eps, eps, size=50))
-        worst = np.maximum(worst, np.abs((at / at.sum()) @ V - a @ V))
-    assert (worst <= eps / (1 - eps) * A.weight_spread(q, K, V, 1.0)).all()
+        worst = np.maximum(worst, np.abs(at @ V - a @ V))
+    assert (worst <= eps * A.weight_spread(q, K, V, 1.0)).all()
