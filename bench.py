@@ -8,6 +8,7 @@ the KV bytes a step reads (about 604 MB) exceed the 129 MB L2, so no flush
 is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --workload prefill_prompts_8b|chunked_prefill_8b   (prefill path)
 
 Prints one JSON line.  The value is decode KV GB/s: the algorithmic bytes of
 a step (every cached K/V row read once, q, out, block tables, context
@@ -46,6 +47,12 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_partition_kernel_batch64_8b.md")
 KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_decode.cu")
+
+PREFILL_METRIC = "paged prefill-attn TFLOP/s (causal, 8B GQA shape; frac of bf16 tensor peak)"
+PREFILL_WORKLOADS = {
+    "prefill_prompts_8b": lambda seed, B: I.prefill_prompts(seed, B),
+    "chunked_prefill_8b": lambda seed, B: I.chunked_prefill(seed, B),
+}
 
 WORKLOADS = {
     "batch64_8b": lambda seed, B: I.batch64_8b(seed, B),
@@ -115,13 +122,24 @@ def algorithmic_bytes(sc, ctx, n_new_tokens):
     return decode, cache_write
 
 
-def measured_peak():
+def measured_peak(key="hbm_gbs", fallback=FALLBACK_HBM_GBS):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
-            return float(json.load(f)["hbm_gbs"]), "measured"
+            return float(json.load(f)[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return fallback, "fallback"
+
+
+def prefill_flops(ctxs, news, n_q_heads, d_head):
+    """Algorithmic FLOPs of causal prefill attention: new position p of a
+    sequence scores p + 1 keys and sums p + 1 value rows, 2 * d_head FLOPs
+    each, for every query head.  Masked work is not counted."""
+    f = 0.0
+    for c, n in zip(ctxs, news):
+        p = np.arange(c - n, c, dtype=np.float64)
+        f += float((p + 1).sum()) * 4 * d_head * n_q_heads
+    return f
 
 
 def profiled_traffic():
@@ -369,6 +387,211 @@ def run_ours(args, world, rank, local):
 
 
 # ----------------------------------------------------------------------------
+# prefill (causal attention of many new positions per sequence)
+# ----------------------------------------------------------------------------
+
+def _prefill_metadata(sc, api):
+    """Block tables and the new positions' slots from the C++ block manager
+    (seeded free order), for every sequence's full context."""
+    alloc = api.BlockAllocator(sc.num_blocks, sc.block_size)
+    assert alloc.set_free_order(sc.free_order) == 0
+    for s, c in enumerate(sc.ctxs):
+        assert alloc.allocate(s, c) == 0
+    seqs = list(range(len(sc.ctxs)))
+    tables, ctx = alloc.build_tables(seqs, max(len(alloc.block_table(s)) for s in seqs))
+    slots = np.concatenate([alloc.slot_mapping(s, c - n, n) for s, (c, n) in enumerate(zip(sc.ctxs, sc.news))])
+    return tables, ctx, slots
+
+
+def run_prefill_ours(args, world, rank, local):
+    from paged_kv_cache_124_gb300 import api
+
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    seed = replica_seed(args.seed, rank)
+    sc = PREFILL_WORKLOADS[args.workload](seed, args.block_size)
+    tables_h, ctx_h, slots_h = _prefill_metadata(sc, api)
+    kc, vc = I.prefill_pool(sc, dev)
+    q = I.prefill_q(sc, dev)
+    k_new, v_new = I.prefill_new_kv(sc, dev)
+    out = torch.empty_like(q)
+    tables, ctx = torch.from_numpy(tables_h).to(dev), torch.from_numpy(ctx_h).to(dev)
+    qs = torch.from_numpy(sc.query_start).to(dev)
+    slots = torch.from_numpy(slots_h).to(dev)
+    max_q = max(sc.news)
+    stream = torch.cuda.current_stream(dev)
+    flops = prefill_flops(sc.ctxs, sc.news, sc.n_q_heads, sc.d_head)
+    T = int(sum(sc.news))
+
+    def attention(q_, tables_, qs_, ctx_, st):
+        api.pa_prefill(out, q_, kc, vc, tables_, qs_, ctx_, max_q, sc.block_size, sc.scale, sc.n_q_heads,
+                       sc.n_kv_heads, sc.d_head, stream=st)
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    for _ in range(args.warmup):
+        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
+        attention(q, tables, qs, ctx, stream)
+    K = args.steps
+    SAMPLE = 4
+    ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev_att = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range((K + SAMPLE - 1) // SAMPLE)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev_start.record(stream)
+    for i in range(K):
+        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
+        if i % SAMPLE == 0:
+            a, b = ev_att[i // SAMPLE]
+            a.record(stream)
+            attention(q, tables, qs, ctx, stream)
+            b.record(stream)
+        else:
+            attention(q, tables, qs, ctx, stream)
+    ev_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    step_s = ev_start.elapsed_time(ev_end) / 1e3
+    att_s = sum(a.elapsed_time(b) for a, b in ev_att) / len(ev_att) / 1e3
+    total_s, total_flops = reduce_timing(step_s, flops * K, world, dev)
+    _, total_tokens = reduce_timing(step_s, T * K, world, dev)
+
+    # end to end with host buffers: q, the new K/V rows, slots, tables, query
+    # starts and context lengths in; the attention output back
+    q_h = q.cpu().pin_memory()
+    k_h, v_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    slots_hp, tables_hp = slots.cpu().pin_memory(), tables.cpu().pin_memory()
+    qs_hp, ctx_hp = qs.cpu().pin_memory(), ctx.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, k_d, v_d = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    slots_d, tables_d, qs_d, ctx_d = (torch.empty_like(slots), torch.empty_like(tables), torch.empty_like(qs),
+                                      torch.empty_like(ctx))
+    pairs = ((q_d, q_h), (k_d, k_h), (v_d, v_h), (slots_d, slots_hp), (tables_d, tables_hp), (qs_d, qs_hp),
+             (ctx_d, ctx_hp))
+    h2d = sum(src.numel() * src.element_size() for _, src in pairs)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for dst, src in pairs:
+            dst.copy_(src, non_blocking=True)
+        api.pa_reshape_and_cache(kc, vc, k_d, v_d, slots_d, stream=stream)
+        attention(q_d, tables_d, qs_d, ctx_d, stream)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s, e2e_flops = reduce_timing(time.perf_counter() - t0, flops * K, world, dev)
+    barrier(world)
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak("bf16_tflops", 1900.0)
+    peak_sus, _ = measured_peak("bf16_tflops_sustained", 1700.0)
+    achieved = flops / att_s / 1e12
+    kv_bytes = sum(sc.ctxs) * sc.n_kv_heads * sc.d_head * 2 * 2
+    line = {
+        "metric": PREFILL_METRIC, "value": round(total_flops / total_s / 1e12, 2), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": sc.name, "num_seqs": len(sc.ctxs), "new_tokens": T, "context_lens":
+                   "all %d" % sc.ctxs[0] if len(set(sc.ctxs)) == 1 else "prefix U[2048, 8192] + 512",
+                   "total_context": int(sum(sc.ctxs)), "n_q_heads": sc.n_q_heads, "n_kv_heads": sc.n_kv_heads,
+                   "d_head": sc.d_head, "block_size": sc.block_size, "num_blocks": sc.num_blocks,
+                   "placement": "seeded random (block manager free order)",
+                   "l2": "inputs larger than L2 (%.0f MB K/V + %.0f MB q/out vs 129 MB L2); no flush" %
+                         (kv_bytes / 1e6, 2 * q.numel() * 2 / 1e6),
+                   "parallelism": "replicas (one batch per GPU)" if world > 1 else "single GPU"},
+        "tokens_per_s": round(total_tokens / total_s, 1),
+        "roofline": {"bound": "tensor", "kernel": "pa_prefill (prefill_kernel<128>)", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind + " bf16 burst", "peak_sustained": peak_sus,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "algorithmic_flops_per_launch": flops, "avg_launch_us": round(att_s * 1e6, 2)},
+        "e2e": {"value": round(e2e_flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_s / K * 1e3, 4)},
+        "gpu_launches": 2 * K,
+        "attention_timing": "events around pa_prefill on every %d-th timed step (%d samples)" % (SAMPLE, len(ev_att)),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(sc, args.cpu_seconds)
+    return line
+
+
+def _prefill_oracle_sample(sc, seq, rows):
+    """The oracle's inputs for the last `rows` new positions of one sequence
+    (its whole context is gathered), drawn on the CPU."""
+    c, n = sc.ctxs[seq], sc.news[seq]
+    B = sc.block_size
+    nb = -(-c // B)
+    rng_k = I.bf16_bits(I.bf16_normal((nb, sc.n_kv_heads, B, sc.d_head), 11 + seq))
+    rng_v = I.bf16_bits(I.bf16_normal((nb, sc.n_kv_heads, B, sc.d_head), 12 + seq))
+    q = I.bf16_bits(I.bf16_normal((rows, sc.n_q_heads, sc.d_head), 13 + seq))
+    tables = np.arange(nb, dtype=np.int32)[None, :]
+    return q, rng_k, rng_v, tables, np.array([0, rows], dtype=np.int32), np.array([c - n + n], dtype=np.int32)
+
+
+def _prefill_oracle_time(sc, seq, rows):
+    from oracle import attention as A
+    q, kc, vc, tables, qs, ctx = _prefill_oracle_sample(sc, seq, rows)
+    t0 = time.perf_counter()
+    A.paged_prefill(q, kc, vc, tables, qs, ctx, sc.scale, sc.block_size)
+    t = time.perf_counter() - t0
+    c = int(ctx[0])
+    return t, prefill_flops([c], [rows], sc.n_q_heads, sc.d_head)
+
+
+def prefill_cpu_baseline(sc, budget_s):
+    """The oracle as it stands, on a bounded sample: the last query rows of
+    the first sequence (all heads, over its whole context), as many as fit
+    about budget_s."""
+    rows = 1
+    t, f = _prefill_oracle_time(sc, 0, rows)
+    while t < budget_s / 2 and rows < sc.news[0]:
+        rows = min(sc.news[0], max(rows + 1, int(rows * min(8.0, budget_s / max(t, 1e-3)))))
+        t, f = _prefill_oracle_time(sc, 0, rows)
+    return {"value": round(f / t / 1e12, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": "fp64 oracle prefill of the last %d of %d new positions of sequence 0 (context %d, all %d "
+                      "query heads) of %s, %.1f s" % (rows, sc.news[0], sc.ctxs[0], sc.n_q_heads, sc.name, t)}
+
+
+def run_prefill_reference(args, world, rank):
+    if rank != 0:
+        return None
+    sc = PREFILL_WORKLOADS[args.workload](args.seed, args.block_size)
+    rows = max(1, args.ref_seqs_per_step)
+    samples = []
+    for i in range(args.warmup + args.steps):
+        seq = i % len(sc.ctxs)
+        t, f = _prefill_oracle_time(sc, seq, rows)
+        if i >= args.warmup:
+            samples.append((t, f))
+    tot_t = sum(x[0] for x in samples)
+    value = sum(x[1] for x in samples) / tot_t / 1e12
+    desc = ("fp64 oracle prefill, the last %d new position(s) of one sequence of %s per step (rotating), all %d "
+            "query heads" % (rows, sc.name, sc.n_q_heads))
+    return {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 8), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_t / len(samples) * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": sc.name, "rows_per_step": rows},
+            "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------
 # CPU oracle (the cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------
 
@@ -441,7 +664,7 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS), default="batch64_8b")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(PREFILL_WORKLOADS), default="batch64_8b")
     p.add_argument("--block-size", type=int, default=16)
     p.add_argument("--partition", type=int, default=0, help="positions per partition (0 = library default)")
     p.add_argument("--seed", type=int, default=0)
@@ -452,10 +675,11 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
+    prefill = args.workload in PREFILL_WORKLOADS
     if args.impl == "reference":
-        line = run_reference(args, world, rank)
+        line = (run_prefill_reference if prefill else run_reference)(args, world, rank)
     else:
-        line = run_ours(args, world, rank, local)
+        line = (run_prefill_ours if prefill else run_ours)(args, world, rank, local)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1 and torch.distributed.is_initialized():

@@ -100,7 +100,8 @@ struct Bars {
     uint64_t q_full;
     uint64_t k_full[2];
     uint64_t v_full[2];
-    uint64_t kv_empty[2];
+    uint64_t k_empty[2];  // per stage: the score products reading its K are done
+    uint64_t v_empty[2];  // per stage: the value products reading its V are done
     uint64_t s_full[2];   // per Q tile: its scores are in tensor memory
     uint64_t p_full[2];   // per Q tile: its weights are in tensor memory (and O rescaled)
     uint64_t o_done[2];   // per Q tile: its last product has finished
@@ -208,6 +209,12 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
         : "memory");
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -251,6 +258,8 @@ __device__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* b, int32_t* stat
 
 // --- the kernel ------------------------------------------------------------------
 
+// Ten warps on four SM sub-partitions: three share one 16K-register file,
+// so at most 168 registers per thread.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -294,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             pa::mbar_init(&bars->k_full[i], 1);
             pa::mbar_init(&bars->v_full[i], 1);
-            pa::mbar_init(&bars->kv_empty[i], 1);
+            pa::mbar_init(&bars->k_empty[i], 1);
+            pa::mbar_init(&bars->v_empty[i], 1);
             pa::mbar_init(&bars->s_full[i], 1);
             pa::mbar_init(&bars->p_full[i], kRows);
             pa::mbar_init(&bars->o_done[i], 1);
@@ -315,47 +325,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
+        // Lane i handles block i of each K/V tile: it reads that block's
+        // table entry before the stage is free (one memory round trip per
+        // tile, hidden behind the wait) and issues the block's copies.
+        const int bpt = kKv / a.block_size;              // blocks per tile
         if (lane == 0) {
-            const int bpt = kKv / a.block_size;              // blocks per tile
             pa::mbar_arrive_expect_tx(&bars->q_full, (has_b ? 2 : 1) * G::kQBytes);
             for (int x = 0; x < (has_b ? 2 : 1); ++x)
 #pragma unroll
                 for (int hh = 0; hh < G::kHalves; ++hh)
                     tma_3d(s_q + x * G::kQBytes + hh * G::kHalfBytes, &mq, hh * 64, h * a.group,
                            q0 + t0 + x * a.tq, &bars->q_full);
-            int uses[2] = {0, 0};
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !wait1(&bars->kv_empty[st], ((j >> 1) - 1) & 1, bars, a.status)) break;
-                int rows[16];
-                for (int i = 0; i < bpt; ++i) {
-                    const int pos = j * kKv + i * a.block_size;
-                    rows[i] = a.oob_row;
-                    if (pos < kv_all) {
-                        const int blk = table[pos / a.block_size];
-                        if (blk < 0 || blk >= a.num_blocks)
-                            pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
-                        else
-                            rows[i] = (blk * a.n_kv_heads + h) * a.block_size;
-                    }
-                }
-                const uint32_t s_k = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes);
-                const uint32_t s_v = s_k + G::kKVBytes;
-                pa::mbar_arrive_expect_tx(&bars->k_full[st], G::kKVBytes);
-                for (int i = 0; i < bpt; ++i)
-#pragma unroll
-                    for (int hh = 0; hh < G::kHalves; ++hh)
-                        tma_2d(s_k + hh * G::kHalfBytes + i * a.block_size * 128, &mk, hh * 64, rows[i],
-                               &bars->k_full[st]);
-                pa::mbar_arrive_expect_tx(&bars->v_full[st], G::kKVBytes);
-                for (int i = 0; i < bpt; ++i)
-#pragma unroll
-                    for (int hh = 0; hh < G::kHalves; ++hh)
-                        tma_2d(s_v + hh * G::kHalfBytes + i * a.block_size * 128, &mv, hh * 64, rows[i],
-                               &bars->v_full[st]);
-                ++uses[st];
+        }
+        int uses[2] = {0, 0};
+        int row = a.oob_row;
+        auto table_row = [&](int j) {
+            int r_ = a.oob_row;
+            const int pos = j * kKv + lane * a.block_size;
+            if (lane < bpt && pos < kv_all) {
+                const int blk = table[pos / a.block_size];
+                if (blk < 0 || blk >= a.num_blocks)
+                    pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
+                else
+                    r_ = (blk * a.n_kv_heads + h) * a.block_size;
             }
-            // the copies this thread started must land before the CTA exits
+            return r_;
+        };
+        if (n_tiles > 0) row = table_row(0);
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j & 1;
+            const uint32_t s_k = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes);
+            const uint32_t s_v = s_k + G::kKVBytes;
+            const uint32_t dst = lane * a.block_size * 128;
+            if (j >= 2 && !wait_warp(&bars->k_empty[st], ((j >> 1) - 1) & 1, bars, a.status)) break;
+            if (lane == 0) pa::mbar_arrive_expect_tx(&bars->k_full[st], G::kKVBytes);
+            __syncwarp();
+            if (lane < bpt)
+#pragma unroll
+                for (int hh = 0; hh < G::kHalves; ++hh)
+                    tma_2d(s_k + hh * G::kHalfBytes + dst, &mk, hh * 64, row, &bars->k_full[st]);
+            if (j >= 2 && !wait_warp(&bars->v_empty[st], ((j >> 1) - 1) & 1, bars, a.status)) break;
+            if (lane == 0) pa::mbar_arrive_expect_tx(&bars->v_full[st], G::kKVBytes);
+            __syncwarp();
+            if (lane < bpt)
+#pragma unroll
+                for (int hh = 0; hh < G::kHalves; ++hh)
+                    tma_2d(s_v + hh * G::kHalfBytes + dst, &mv, hh * 64, row, &bars->v_full[st]);
+            ++uses[st];
+            if (j + 1 < n_tiles) row = table_row(j + 1);
+        }
+        // the copies this warp started must land before the CTA exits
+        if (lane == 0) {
             pa::mbar_wait_bounded(&bars->q_full, 0, kMaxProbes);
             for (int st = 0; st < 2; ++st)
                 if (uses[st]) {
@@ -396,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_s(1, 0);
                     commit(&bars->s_full[1], 0);
                 }
+                commit(&bars->k_empty[0], 0);
             }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int st = j & 1;
@@ -432,6 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
                                     (j > 0 || kk > 0) ? 1u : 0u);
                     if (j == nt[x] - 1) commit(&bars->o_done[x], 0);
+                    const bool last_v = x == 1 || j >= nt[1];      // no later product reads V(j)
+                    if (last_v) commit(&bars->v_empty[st], (j >> 1) & 1);
                     if (j + 1 < nt[x]) {
                         const int nst = (j + 1) & 1;
                         ok = wait1(&bars->k_full[nst], ((j + 1) >> 1) & 1, bars, a.status);
@@ -439,10 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         issue_s(x, nst);
                         commit(&bars->s_full[x], (j + 1) & 1);
+                        if (x == 1 || j + 1 >= nt[1])               // no later product reads K(j+1)
+                            commit(&bars->k_empty[nst], ((j + 1) >> 1) & 1);
                     }
                 }
-                if (!ok) break;
-                commit(&bars->kv_empty[st], (j >> 1) & 1);
             }
             // products in flight must finish before the tensor memory is freed
             if (last) pa::mbar_wait_bounded(last, last_par, kMaxProbes);
@@ -472,17 +495,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kKv / 32; ++c) tmem_ld32(t_s + c * 32, s + c * 32);
             tmem_wait_ld();
             const int lim = row_lim - j * kKv;
-            float mt = -INFINITY;
-            if (lim >= kKv) {
+            if (lim < kKv) {
 #pragma unroll
-                for (int c = 0; c < kKv; ++c) mt = fmaxf(mt, s[c]);
-            } else {
-#pragma unroll
-                for (int c = 0; c < kKv; ++c) {
-                    s[c] = c < lim ? s[c] : -INFINITY;
-                    mt = fmaxf(mt, s[c]);
-                }
+                for (int c = 0; c < kKv; ++c) s[c] = c < lim ? s[c] : -INFINITY;
             }
+            // row maximum: 8 independent chains of 3-input maxima
+            float mp[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mp[k] = max3(s[k], s[8 + k], s[16 + k]);
+#pragma unroll
+            for (int c = 24; c + 16 <= kKv; c += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mp[k] = max3(mp[k], s[c + k], s[c + 8 + k]);
+            if ((kKv - 24) % 16 == 8) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[kKv - 8 + k]);
+            }
+            const float mt = fmaxf(max3(mp[0], mp[1], mp[2]), fmaxf(max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])));
             const float mts = mt * c2;                    // scale > 0: the maximum commutes with it
             const bool rescale = mts > m_used + kRescaleThreshold;
             const float m_new = rescale ? mts : m_used;
@@ -504,13 +533,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_used = m_new;
             const float neg = -m_used;
             uint32_t w[kKv / 2];
+            float lp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // independent partial sums
 #pragma unroll
             for (int i = 0; i < kKv / 2; ++i) {
                 const float p0 = fast_exp2(fmaf(s[2 * i], c2, neg));
                 const float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg));
-                l += p0 + p1;
+                lp[i & 7] += p0 + p1;
                 w[i] = pack_bf16_rn(p0, p1);
             }
+            l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
             tmem_st32u(t_s, w);
             tmem_st32u(t_s + 32, w + 32);
             tmem_wait_st();

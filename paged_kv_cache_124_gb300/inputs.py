@@ -293,3 +293,75 @@ def prefix_kv(seed, layer, tokens, start, end, n_kv_heads, d_head):
     t = torch.from_numpy(u.astype(np.float32)).to(torch.bfloat16)
     t = t.view(len(dig), 2, n_kv_heads, d_head)
     return t[:, 0].contiguous(), t[:, 1].contiguous()
+
+
+# ----------------------------------------------------------------------------
+# Prefill workloads: each sequence has ctx positions, the last n of them new
+# (a whole prompt when n = ctx, a chunk over a cached prefix otherwise).
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class PrefillScenario:
+    name: str
+    n_q_heads: int
+    n_kv_heads: int
+    d_head: int
+    block_size: int
+    ctxs: List[int]
+    news: List[int]
+    num_blocks: int
+    free_order: np.ndarray        # block manager free list (seeded random placement)
+    seed: int
+
+    @property
+    def scale(self):
+        return 1.0 / math.sqrt(self.d_head)
+
+    @property
+    def query_start(self):
+        return np.concatenate([[0], np.cumsum(self.news)]).astype(np.int32)
+
+
+def _prefill_scenario(name, seed, block_size, ctxs, news, n_q_heads=32, n_kv_heads=8, d_head=128):
+    nblk = [_blocks(c, block_size) for c in ctxs]
+    num_blocks = int(math.ceil(sum(nblk) * 1.1)) + 1
+    return PrefillScenario(name, n_q_heads, n_kv_heads, d_head, block_size, [int(c) for c in ctxs],
+                           [int(n) for n in news], num_blocks, permutation(num_blocks, seed + 17), seed)
+
+
+def prefill_prompts(seed=0, block_size=16, num_seqs=16, prompt_len=2003):
+    """Whole-prompt prefill: the 16 prompts of 2,003 tokens of the parallel
+    sampling workload, before they are forked."""
+    return _prefill_scenario("prefill_prompts_8b", seed, block_size, [prompt_len] * num_seqs, [prompt_len] * num_seqs)
+
+
+def chunked_prefill(seed=0, block_size=16, num_seqs=8, chunk=512, lo=2048, hi=8192):
+    """Chunked prefill: a 512-token chunk per sequence on top of a cached
+    prefix of U[2048, 8192] positions."""
+    prefix = uniform_ints(num_seqs, lo, hi, seed + 5)
+    return _prefill_scenario("chunked_prefill_8b", seed, block_size, [int(p) + chunk for p in prefix],
+                             [chunk] * num_seqs)
+
+
+def prefill_pool(sc, device):
+    """K and V pools [num_blocks, Hkv, B, D] bf16 with N(0,1) values in every
+    slot (the cached prefix, and placeholders where the new positions will be
+    written); drawn on `device`."""
+    shape = (sc.num_blocks, sc.n_kv_heads, sc.block_size, sc.d_head)
+    k = _normal(shape, _mix(sc.seed, 6, 0, 0), device)
+    v = _normal(shape, _mix(sc.seed, 7, 0, 0), device)
+    return k, v
+
+
+def prefill_q(sc, device):
+    """Queries [sum(news), Hq, D] of the new positions."""
+    return _normal((int(sum(sc.news)), sc.n_q_heads, sc.d_head), _mix(sc.seed, 8, 0, 0), device)
+
+
+def prefill_new_kv(sc, device):
+    """Keys and values [sum(news), Hkv, D] of the new positions (written into
+    the pool by reshape_and_cache before the attention)."""
+    T = int(sum(sc.news))
+    k = _normal((T, sc.n_kv_heads, sc.d_head), _mix(sc.seed, 9, 0, 0), device)
+    v = _normal((T, sc.n_kv_heads, sc.d_head), _mix(sc.seed, 10, 0, 0), device)
+    return k, v
