@@ -53,13 +53,17 @@ namespace {
 constexpr int kRows = 128;                 // MMA M: query rows per tile
 constexpr int kKv = 128;                   // positions per K/V tile
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;              // 2 softmax warpgroups, producer, MMA
+constexpr int kMmaWarp0 = 9;               // MMA warps 9 (tile A) and 10 (tile B); 9 owns the tensor memory
+constexpr int kThreads = 352;              // 2 softmax warpgroups, producer, 2 MMA warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS0 = 0;            // S_A; S_B at +128
 constexpr uint32_t kTmemO0 = 256;          // O_A; O_B at +128
 constexpr int kMaxProbes = 2000000;        // x <= ~1 us per probe
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest weight allowed before a rescale
+// K tiles are released as soon as their score products finish; V tiles only
+// after the value products, a whole tile pair later, so V gets a deeper ring.
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
 
 template <int D>
 struct PGeo {
@@ -68,8 +72,9 @@ struct PGeo {
     static constexpr int kQBytes = kHalves * kHalfBytes;      // one Q tile
     static constexpr int kKVBytes = kHalves * kHalfBytes;     // one K (or V) tile of 128 positions
     static constexpr int kQ = 0;                              // Q_A, then Q_B
-    static constexpr int kStage0 = 2 * kQBytes;               // stage s: K at +2s*KV, V right after
-    static constexpr int kBars = kStage0 + 4 * kKVBytes;
+    static constexpr int kK0 = 2 * kQBytes;                   // K stages (kKStages)
+    static constexpr int kV0 = kK0 + kKStages * kKVBytes;     // V stages (kVStages)
+    static constexpr int kBars = kV0 + kVStages * kKVBytes;
     // barriers, slots and alignment slack; at least 120 KiB so that two CTAs
     // never share an SM (each holds 512 tensor-memory columns)
     static constexpr int kSmem = kBars + 256 + 1024 > 120 * 1024 ? kBars + 256 + 1024 : 120 * 1024;
@@ -98,10 +103,10 @@ struct PrefillArgs {
 
 struct Bars {
     uint64_t q_full;
-    uint64_t k_full[2];
-    uint64_t v_full[2];
-    uint64_t k_empty[2];  // per stage: the score products reading its K are done
-    uint64_t v_empty[2];  // per stage: the value products reading its V are done
+    uint64_t k_full[kKStages];
+    uint64_t v_full[kVStages];
+    uint64_t k_empty[2][kKStages];  // per Q tile and stage: its score products reading K are done
+    uint64_t v_empty[2][kVStages];  // per Q tile and stage: its value products reading V are done
     uint64_t s_full[2];   // per Q tile: its scores are in tensor memory
     uint64_t p_full[2];   // per Q tile: its weights are in tensor memory (and O rescaled)
     uint64_t o_done[2];   // per Q tile: its last product has finished
@@ -300,11 +305,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         pa::mbar_init(&bars->q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             pa::mbar_init(&bars->k_full[i], 1);
+            pa::mbar_init(&bars->k_empty[0][i], 1);
+            pa::mbar_init(&bars->k_empty[1][i], 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
             pa::mbar_init(&bars->v_full[i], 1);
-            pa::mbar_init(&bars->k_empty[i], 1);
-            pa::mbar_init(&bars->v_empty[i], 1);
+            pa::mbar_init(&bars->v_empty[0][i], 1);
+            pa::mbar_init(&bars->v_empty[1][i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             pa::mbar_init(&bars->s_full[i], 1);
             pa::mbar_init(&bars->p_full[i], kRows);
             pa::mbar_init(&bars->o_done[i], 1);
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bars->abort = 0;
         pa::fence_mbar_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          pa::smem_addr(&bars->tmem_base)),
                      "r"(kTmemCols));
@@ -337,7 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_3d(s_q + x * G::kQBytes + hh * G::kHalfBytes, &mq, hh * 64, h * a.group,
                            q0 + t0 + x * a.tq, &bars->q_full);
         }
-        int uses[2] = {0, 0};
         int row = a.oob_row;
         auto table_row = [&](int j) {
             int r_ = a.oob_row;
@@ -352,44 +362,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             return r_;
         };
         if (n_tiles > 0) row = table_row(0);
+        int issued = 0;
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1;
-            const uint32_t s_k = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes);
-            const uint32_t s_v = s_k + G::kKVBytes;
+            const int ks = j % kKStages, vs = j % kVStages;
+            const uint32_t s_k = pa::smem_addr(sm + G::kK0 + ks * G::kKVBytes);
+            const uint32_t s_v = pa::smem_addr(sm + G::kV0 + vs * G::kKVBytes);
             const uint32_t dst = lane * a.block_size * 128;
-            if (j >= 2 && !wait_warp(&bars->k_empty[st], ((j >> 1) - 1) & 1, bars, a.status)) break;
-            if (lane == 0) pa::mbar_arrive_expect_tx(&bars->k_full[st], G::kKVBytes);
+            // the stage's previous tile must be done with by each Q tile that used it
+            if (j >= kKStages && !((j - kKStages >= nt0 ||
+                                    wait_warp(&bars->k_empty[0][ks], (j / kKStages - 1) & 1, bars, a.status)) &&
+                                   (j - kKStages >= nt1 ||
+                                    wait_warp(&bars->k_empty[1][ks], (j / kKStages - 1) & 1, bars, a.status))))
+                break;
+            if (lane == 0) pa::mbar_arrive_expect_tx(&bars->k_full[ks], G::kKVBytes);
             __syncwarp();
             if (lane < bpt)
 #pragma unroll
                 for (int hh = 0; hh < G::kHalves; ++hh)
-                    tma_2d(s_k + hh * G::kHalfBytes + dst, &mk, hh * 64, row, &bars->k_full[st]);
-            if (j >= 2 && !wait_warp(&bars->v_empty[st], ((j >> 1) - 1) & 1, bars, a.status)) break;
-            if (lane == 0) pa::mbar_arrive_expect_tx(&bars->v_full[st], G::kKVBytes);
+                    tma_2d(s_k + hh * G::kHalfBytes + dst, &mk, hh * 64, row, &bars->k_full[ks]);
+            if (j >= kVStages &&
+                !((j - kVStages >= nt0 || wait_warp(&bars->v_empty[0][vs], (j / kVStages - 1) & 1, bars, a.status)) &&
+                  (j - kVStages >= nt1 || wait_warp(&bars->v_empty[1][vs], (j / kVStages - 1) & 1, bars, a.status)))) {
+                issued = j * 2 + 1;                       // K of tile j is in flight, V is not
+                break;
+            }
+            if (lane == 0) pa::mbar_arrive_expect_tx(&bars->v_full[vs], G::kKVBytes);
             __syncwarp();
             if (lane < bpt)
 #pragma unroll
                 for (int hh = 0; hh < G::kHalves; ++hh)
-                    tma_2d(s_v + hh * G::kHalfBytes + dst, &mv, hh * 64, row, &bars->v_full[st]);
-            ++uses[st];
+                    tma_2d(s_v + hh * G::kHalfBytes + dst, &mv, hh * 64, row, &bars->v_full[vs]);
+            issued = j * 2 + 2;
             if (j + 1 < n_tiles) row = table_row(j + 1);
         }
-        // the copies this warp started must land before the CTA exits
+        // the copies this warp started must land before the CTA exits: the
+        // last use of each stage (earlier uses completed before it was reused)
         if (lane == 0) {
             pa::mbar_wait_bounded(&bars->q_full, 0, kMaxProbes);
-            for (int st = 0; st < 2; ++st)
-                if (uses[st]) {
-                    pa::mbar_wait_bounded(&bars->k_full[st], (uses[st] - 1) & 1, kMaxProbes);
-                    pa::mbar_wait_bounded(&bars->v_full[st], (uses[st] - 1) & 1, kMaxProbes);
-                }
+            const int nk = (issued + 1) / 2, nv = issued / 2;   // tiles whose K / V copies were issued
+            for (int i = 0; i < kKStages && i < nk; ++i) {
+                const int j = nk - 1 - i;
+                pa::mbar_wait_bounded(&bars->k_full[j % kKStages], (j / kKStages) & 1, kMaxProbes);
+            }
+            for (int i = 0; i < kVStages && i < nv; ++i) {
+                const int j = nv - 1 - i;
+                pa::mbar_wait_bounded(&bars->v_full[j % kVStages], (j / kVStages) & 1, kMaxProbes);
+            }
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+    } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
+        // ------------------------------------------------------------ MMA issuers
+        // One thread per Q tile: a single thread cannot issue N=128 products
+        // fast enough to keep the tensor pipe busy, two can.
+        const int x = warp - kMmaWarp0;
+        const int ntx = x ? nt1 : nt0;
+        const int kv_endx = x ? kv_end1 : kv_end0;
+        if (lane == 0 && ntx > 0) {
             constexpr uint32_t id_qk = idesc_bf16(kRows, kKv, 0);
             constexpr uint32_t id_pv = idesc_bf16(kRows, D, 1);
-            const int nt[2] = {nt0, nt1};
-            const int kv_end[2] = {kv_end0, kv_end1};
+            const uint32_t t_s = tmem + kTmemS0 + x * 128;
+            const uint32_t t_o = tmem + kTmemO0 + x * 128;
+            const uint32_t qx = s_q + x * G::kQBytes;
             uint64_t* last = nullptr;
             uint32_t last_par = 0;
             auto commit = [&](uint64_t* bar, uint32_t par) {
@@ -397,74 +429,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 last = bar;
                 last_par = par;
             };
-            auto issue_s = [&](int x, int st) {
-                const uint32_t s_k = pa::smem_addr(sm + G::kStage0 + st * 2 * G::kKVBytes);
-                const uint32_t qx = s_q + x * G::kQBytes;
+            auto issue_s = [&](int ks) {
+                const uint32_t s_k = pa::smem_addr(sm + G::kK0 + ks * G::kKVBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * G::kHalfBytes + (kk & 3) * 32;
-                    mma_bf16(tmem + kTmemS0 + x * 128, smem_desc(qx + off, 16, 1024),
-                             smem_desc(s_k + off, 16, 1024), id_qk, kk > 0);
+                    mma_bf16(t_s, smem_desc(qx + off, 16, 1024), smem_desc(s_k + off, 16, 1024), id_qk, kk > 0);
                 }
             };
             bool ok = wait1(&bars->q_full, 0, bars, a.status) && wait1(&bars->k_full[0], 0, bars, a.status);
             if (ok) {
                 tc_fence_after();
-                issue_s(0, 0);
-                commit(&bars->s_full[0], 0);
-                if (has_b) {
-                    issue_s(1, 0);
-                    commit(&bars->s_full[1], 0);
-                }
-                commit(&bars->k_empty[0], 0);
+                issue_s(0);
+                commit(&bars->s_full[x], 0);
+                commit(&bars->k_empty[x][0], 0);
             }
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int st = j & 1;
-                ok = wait1(&bars->v_full[st], (j >> 1) & 1, bars, a.status);
+            for (int j = 0; ok && j < ntx; ++j) {
+                const int vs = j % kVStages;
+                ok = wait1(&bars->v_full[vs], (j / kVStages) & 1, bars, a.status);
                 if (!ok) break;
-                uint8_t* vbase = sm + G::kStage0 + st * 2 * G::kKVBytes + G::kKVBytes;
+                uint8_t* vbase = sm + G::kV0 + vs * G::kKVBytes;
                 const uint32_t s_v = pa::smem_addr(vbase);
-                if (j == n_tiles - 1) {
-                    // Positions past the last needed one inside its block may
-                    // hold anything (NaN included); their weights are 0, but
-                    // 0 * NaN is not, so clear those V rows first.
-                    const int valid = kv_all - j * kKv;
-                    const int zero_end = min(((valid + 15) >> 4) << 4,
-                                             ((kv_all + a.block_size - 1) / a.block_size) * a.block_size - j * kKv);
-                    if (valid < zero_end) {
-                        for (int r = valid; r < zero_end; ++r)
+                const int valid = min(kKv, kv_endx - j * kKv);
+                const int ksteps = (valid + 15) >> 4;
+                // Rows at and past the context length inside the last block may
+                // hold anything (NaN included); their weights are 0, but 0 * NaN
+                // is not, so clear those V rows before the product reads them.
+                // Only rows past the context are touched (both issuers may clear
+                // the same rows; they write the same zeros).
+                const int zero_begin = max(valid, ctx - j * kKv);
+                const int zero_end = min(ksteps * 16, ((ctx + a.block_size - 1) / a.block_size) * a.block_size - j * kKv);
+                if (zero_begin < zero_end) {
+                    for (int r = zero_begin; r < zero_end; ++r)
 #pragma unroll
-                            for (int hh = 0; hh < G::kHalves; ++hh) {
-                                uint4* row = reinterpret_cast<uint4*>(vbase + hh * G::kHalfBytes + r * 128);
+                        for (int hh = 0; hh < G::kHalves; ++hh) {
+                            uint4* row = reinterpret_cast<uint4*>(vbase + hh * G::kHalfBytes + r * 128);
 #pragma unroll
-                                for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
-                            }
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    }
+                            for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                        }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                for (int x = 0; x < 2 && ok; ++x) {
-                    if (j >= nt[x]) continue;
-                    ok = wait1(&bars->p_full[x], j & 1, bars, a.status);
+                ok = wait1(&bars->p_full[x], j & 1, bars, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                for (int kk = 0; kk < ksteps; ++kk)
+                    mma_bf16_ta(t_o, t_s + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                commit(&bars->v_empty[x][vs], (j / kVStages) & 1);
+                if (j == ntx - 1) {
+                    commit(&bars->o_done[x], 0);
+                } else {
+                    const int nks = (j + 1) % kKStages;
+                    ok = wait1(&bars->k_full[nks], ((j + 1) / kKStages) & 1, bars, a.status);
                     if (!ok) break;
                     tc_fence_after();
-                    const int ksteps = (min(kKv, kv_end[x] - j * kKv) + 15) >> 4;
-                    for (int kk = 0; kk < ksteps; ++kk)
-                        mma_bf16_ta(tmem + kTmemO0 + x * 128, tmem + kTmemS0 + x * 128 + kk * 8,
-                                    smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
-                    if (j == nt[x] - 1) commit(&bars->o_done[x], 0);
-                    const bool last_v = x == 1 || j >= nt[1];      // no later product reads V(j)
-                    if (last_v) commit(&bars->v_empty[st], (j >> 1) & 1);
-                    if (j + 1 < nt[x]) {
-                        const int nst = (j + 1) & 1;
-                        ok = wait1(&bars->k_full[nst], ((j + 1) >> 1) & 1, bars, a.status);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_s(x, nst);
-                        commit(&bars->s_full[x], (j + 1) & 1);
-                        if (x == 1 || j + 1 >= nt[1])               // no later product reads K(j+1)
-                            commit(&bars->k_empty[nst], ((j + 1) >> 1) & 1);
-                    }
+                    issue_s(nks);
+                    commit(&bars->s_full[x], (j + 1) & 1);
+                    commit(&bars->k_empty[x][nks], ((j + 1) / kKStages) & 1);
                 }
             }
             // products in flight must finish before the tensor memory is freed
@@ -581,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp0) {
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
