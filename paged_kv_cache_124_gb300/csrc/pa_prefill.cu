@@ -64,6 +64,12 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest weight allowed
 // after the value products, a whole tile pair later, so V gets a deeper ring.
 constexpr int kKStages = 2;
 constexpr int kVStages = 3;
+// Of every 8 pairs of weights in an unmasked tile, this many are exponentiated
+// by the cubic on the FMA pipe, the rest by the MUFU unit.
+#ifndef PA_PREFILL_POLY_PAIRS
+#define PA_PREFILL_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairsPer8 = PA_PREFILL_POLY_PAIRS;
 
 template <int D>
 struct PGeo {
@@ -110,6 +116,7 @@ struct Bars {
     uint64_t s_full[2];   // per Q tile: its scores are in tensor memory
     uint64_t p_full[2];   // per Q tile: its weights are in tensor memory (and O rescaled)
     uint64_t o_done[2];   // per Q tile: its last product has finished
+    uint64_t sm_done[2];  // per Q tile: its softmax warpgroup finished a tile
     uint32_t tmem_base;
     int abort;
 };
@@ -226,6 +233,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// 2^x on the FMA pipe, for x in [-125, 128): x = n + f with n = round(x)
+// (by the 1.5 * 2^23 rounding trick) and f in [-1/2, 1/2]; 2^f is the cubic of
+// least maximum relative error on [-1/2, 1/2] (Remez exchange, coefficients
+// from exp2_poly_fit.py; relative error below 7.5e-5); 2^n is added to the
+// exponent field.  Inputs below -125 give 2^-125, not 0: use it only where no
+// weight is masked.
+constexpr float kExp2C0 = 9.999280735e-01f;
+constexpr float kExp2C1 = 6.932609855e-01f;
+constexpr float kExp2C2 = 2.426111222e-01f;
+constexpr float kExp2C3 = 5.517166906e-02f;
+
+__device__ __forceinline__ float exp2_poly(float x) {
+    x = fmaxf(x, -125.f);
+    const float t = x + 12582912.f;
+    const float f = x - (t - 12582912.f);
+    const float p = fmaf(fmaf(fmaf(kExp2C3, f, kExp2C2), f, kExp2C1), f, kExp2C0);
+    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -319,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pa::mbar_init(&bars->s_full[i], 1);
             pa::mbar_init(&bars->p_full[i], kRows);
             pa::mbar_init(&bars->o_done[i], 1);
+            pa::mbar_init(&bars->sm_done[i], kRows);
         }
         bars->abort = 0;
         pa::fence_mbar_init();
@@ -469,7 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                ok = wait1(&bars->p_full[x], j & 1, bars, a.status);
+                // K of the next tile too, so that the products of this one and
+                // the scores of the next go out back to back once P is ready
+                const int nks = (j + 1) % kKStages;
+                if (j + 1 < ntx) ok = wait1(&bars->k_full[nks], ((j + 1) / kKStages) & 1, bars, a.status);
+                if (ok) ok = wait1(&bars->p_full[x], j & 1, bars, a.status);
                 if (!ok) break;
                 tc_fence_after();
                 for (int kk = 0; kk < ksteps; ++kk)
@@ -479,10 +510,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j == ntx - 1) {
                     commit(&bars->o_done[x], 0);
                 } else {
-                    const int nks = (j + 1) % kKStages;
-                    ok = wait1(&bars->k_full[nks], ((j + 1) / kKStages) & 1, bars, a.status);
-                    if (!ok) break;
-                    tc_fence_after();
                     issue_s(nks);
                     commit(&bars->s_full[x], (j + 1) & 1);
                     commit(&bars->k_empty[x][nks], ((j + 1) / kKStages) & 1);
@@ -509,6 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int j = 0; j < ntx; ++j) {
             ok = wait_warp(&bars->s_full[x], j & 1, bars, a.status);
+            // The two warpgroups take turns (A on tile j, then B on tile j, then
+            // A on tile j + 1, ...), so that each runs alone on the SM's
+            // sub-partitions while the tensor pipe works for the other.
+            if (ok && x == 0 && j >= 1 && j - 1 < nt1) ok = wait_warp(&bars->sm_done[1], (j - 1) & 1, bars, a.status);
+            if (ok && x == 1 && j < nt0) ok = wait_warp(&bars->sm_done[0], j & 1, bars, a.status);
             if (!ok) break;
             tc_fence_after();
             float s[kKv];
@@ -555,12 +587,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float neg = -m_used;
             uint32_t w[kKv / 2];
             float lp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // independent partial sums
+            if (lim >= kKv) {
+                // no masked weight: part of the exponentials on the FMA pipe
 #pragma unroll
-            for (int i = 0; i < kKv / 2; ++i) {
-                const float p0 = fast_exp2(fmaf(s[2 * i], c2, neg));
-                const float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg));
-                lp[i & 7] += p0 + p1;
-                w[i] = pack_bf16_rn(p0, p1);
+                for (int i = 0; i < kKv / 2; ++i) {
+                    const float x0 = fmaf(s[2 * i], c2, neg), x1 = fmaf(s[2 * i + 1], c2, neg);
+                    const bool poly = (i & 7) >= 8 - kPolyPairsPer8;
+                    const float p0 = poly ? exp2_poly(x0) : fast_exp2(x0);
+                    const float p1 = poly ? exp2_poly(x1) : fast_exp2(x1);
+                    lp[i & 7] += p0 + p1;
+                    w[i] = pack_bf16_rn(p0, p1);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kKv / 2; ++i) {
+                    const float p0 = fast_exp2(fmaf(s[2 * i], c2, neg));
+                    const float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg));
+                    lp[i & 7] += p0 + p1;
+                    w[i] = pack_bf16_rn(p0, p1);
+                }
             }
             l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
             tmem_st32u(t_s, w);
@@ -568,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             pa::mbar_arrive(&bars->p_full[x]);
+            pa::mbar_arrive(&bars->sm_done[x]);
         }
         if (ok && ntx > 0) ok = wait_warp(&bars->o_done[x], 0, bars, a.status);
         if (ok && ntx > 0) {
