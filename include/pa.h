@@ -212,9 +212,8 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
  *
  * Scores and sums are fp32 (tensor cores, bf16 inputs); the softmax weights
  * are rounded to bf16 before the weighted sum of values (the normaliser sums
- * them unrounded) and some are computed by a cubic for 2^x (relative error
- * below 7.5e-5), so an output element can differ from the exact value by up
- * to about (2^-8 + 1.5e-4) * sum_j a_j |V_j| besides fp32 rounding.
+ * them unrounded), so an output element can differ from the exact value by
+ * up to 2^-8 * sum_j a_j |V_j| besides fp32 rounding.
  *
  * Arguments
  *   out           device [num_tokens][n_q_heads][d_head], bf16 or fp32 per

@@ -29,13 +29,17 @@
 //     64 columns of its own S and read from there as the A operand of the
 //     second product; V is an MN-major operand read straight from the TMA
 //     layout.
-//   * Two softmax warpgroups, one per Q tile, own one row per thread
-//     (tensor-memory lane = row): mask, online maximum in the log2 domain,
-//     exp2, running sum, P.  The product order S_A(j), S_B(j), PV_A(j),
-//     S_A(j+1), PV_B(j), S_B(j+1), ... keeps the tensor pipe busy with one
-//     tile while the other tile's softmax runs.  O is rescaled in tensor
-//     memory only when a row's maximum grows by more than 2^8 (the weights
-//     stay below 256 otherwise), which is rare after the first tiles.
+//   * Eight softmax warps work on tile A, then on tile B, then on tile A of
+//     the next K/V tile, ...: warps w and w + 4 share the 32 rows of lane
+//     quarter w (tensor-memory lane = row), each taking 64 of the 128
+//     columns; the two halves of a row exchange their maxima (and, at the
+//     end, their sums) through shared memory.  Per row: mask, online maximum
+//     in the log2 domain, exp2, running sum, P.  One MMA warp per Q tile
+//     issues PV(j) and S(j+1) as soon as that tile's P is ready, so the
+//     tensor pipe works for one tile while the other tile's softmax runs.
+//     O is rescaled in tensor memory only when a row's maximum grows by more
+//     than 2^8 (the weights stay below 256 otherwise), which is rare after
+//     the first tiles.
 //   * Every wait is bounded; on a timeout the CTA flags PA_DEV_WAIT_TIMEOUT,
 //     waits (bounded) for its own copies and products in flight, frees its
 //     tensor memory and returns.
@@ -54,7 +58,7 @@ constexpr int kRows = 128;                 // MMA M: query rows per tile
 constexpr int kKv = 128;                   // positions per K/V tile
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp0 = 9;               // MMA warps 9 (tile A) and 10 (tile B); 9 owns the tensor memory
-constexpr int kThreads = 352;              // 2 softmax warpgroups, producer, 2 MMA warps
+constexpr int kThreads = 352;              // 8 softmax warps, producer, 2 MMA warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS0 = 0;            // S_A; S_B at +128
 constexpr uint32_t kTmemO0 = 256;          // O_A; O_B at +128
@@ -63,13 +67,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest weight allowed
 // K tiles are released as soon as their score products finish; V tiles only
 // after the value products, a whole tile pair later, so V gets a deeper ring.
 constexpr int kKStages = 2;
-constexpr int kVStages = 3;
-// Of every 8 pairs of weights in an unmasked tile, this many are exponentiated
-// by the cubic on the FMA pipe, the rest by the MUFU unit.
-#ifndef PA_PREFILL_POLY_PAIRS
-#define PA_PREFILL_POLY_PAIRS 0
-#endif
-constexpr int kPolyPairsPer8 = PA_PREFILL_POLY_PAIRS;
+constexpr int kVStages = 2;
+constexpr int kSoftmaxThreads = 256;
 
 template <int D>
 struct PGeo {
@@ -80,7 +79,8 @@ struct PGeo {
     static constexpr int kQ = 0;                              // Q_A, then Q_B
     static constexpr int kK0 = 2 * kQBytes;                   // K stages (kKStages)
     static constexpr int kV0 = kK0 + kKStages * kKVBytes;     // V stages (kVStages)
-    static constexpr int kBars = kV0 + kVStages * kKVBytes;
+    static constexpr int kRed = kV0 + kVStages * kKVBytes;     // row-half exchange: [tile][parity][half][row] fp32
+    static constexpr int kBars = kRed + 2 * 2 * 2 * kRows * 4;
     // barriers, slots and alignment slack; at least 120 KiB so that two CTAs
     // never share an SM (each holds 512 tensor-memory columns)
     static constexpr int kSmem = kBars + 256 + 1024 > 120 * 1024 ? kBars + 256 + 1024 : 120 * 1024;
@@ -116,7 +116,7 @@ struct Bars {
     uint64_t s_full[2];   // per Q tile: its scores are in tensor memory
     uint64_t p_full[2];   // per Q tile: its weights are in tensor memory (and O rescaled)
     uint64_t o_done[2];   // per Q tile: its last product has finished
-    uint64_t sm_done[2];  // per Q tile: its softmax warpgroup finished a tile
+    uint64_t red[2];      // per Q tile: both halves of every row posted their value
     uint32_t tmem_base;
     int abort;
 };
@@ -233,25 +233,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// 2^x on the FMA pipe, for x in [-125, 128): x = n + f with n = round(x)
-// (by the 1.5 * 2^23 rounding trick) and f in [-1/2, 1/2]; 2^f is the cubic of
-// least maximum relative error on [-1/2, 1/2] (Remez exchange, coefficients
-// from exp2_poly_fit.py; relative error below 7.5e-5); 2^n is added to the
-// exponent field.  Inputs below -125 give 2^-125, not 0: use it only where no
-// weight is masked.
-constexpr float kExp2C0 = 9.999280735e-01f;
-constexpr float kExp2C1 = 6.932609855e-01f;
-constexpr float kExp2C2 = 2.426111222e-01f;
-constexpr float kExp2C3 = 5.517166906e-02f;
-
-__device__ __forceinline__ float exp2_poly(float x) {
-    x = fmaxf(x, -125.f);
-    const float t = x + 12582912.f;
-    const float f = x - (t - 12582912.f);
-    const float p = fmaf(fmaf(fmaf(kExp2C3, f, kExp2C2), f, kExp2C1), f, kExp2C0);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
@@ -262,6 +243,9 @@ __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
 // One thread.  Gives up when another role has aborted or after kMaxProbes
 // probes (then aborts the CTA and flags the timeout).
 __device__ bool wait1(uint64_t* bar, uint32_t parity, Bars* b, int32_t* status) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)                 // short spin first: most waits are nearly over
+        if (pa::mbar_test_wait(bar, parity)) return true;
     for (int i = 0; i < kMaxProbes; ++i) {
         if (pa::mbar_try_wait(bar, parity)) return true;
         if ((i & 63) == 63 && *reinterpret_cast<volatile int*>(&b->abort)) return false;
@@ -273,6 +257,9 @@ __device__ bool wait1(uint64_t* bar, uint32_t parity, Bars* b, int32_t* status) 
 
 // Whole warp, warp-uniform result.
 __device__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* b, int32_t* status) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+        if (__all_sync(0xffffffffu, pa::mbar_test_wait(bar, parity))) return true;
     for (int i = 0; i < kMaxProbes; ++i) {
         const bool done = pa::mbar_try_wait(bar, parity);
         if (__all_sync(0xffffffffu, done)) return true;
@@ -343,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             pa::mbar_init(&bars->s_full[i], 1);
-            pa::mbar_init(&bars->p_full[i], kRows);
+            pa::mbar_init(&bars->p_full[i], kSoftmaxThreads);
             pa::mbar_init(&bars->o_done[i], 1);
-            pa::mbar_init(&bars->sm_done[i], kRows);
+            pa::mbar_init(&bars->red[i], kSoftmaxThreads);
         }
         bars->abort = 0;
         pa::fence_mbar_init();
@@ -519,113 +506,117 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (last) pa::mbar_wait_bounded(last, last_par, kMaxProbes);
         }
     } else {
-        // ------------------------------------------------------------ softmax warpgroups
-        const int x = warp >> 2;                          // Q tile of this warpgroup
-        const int r = threadIdx.x & (kRows - 1);          // row = tensor-memory lane
+        // ------------------------------------------------------------ softmax warps
+        const int quarter = warp & 3, hc = warp >> 2;     // lane quarter, column half
+        const int r = quarter * 32 + lane;                // row = tensor-memory lane
         const int t = r / a.group, g = r - t * a.group;
-        const int tok = t0 + x * a.tq + t;
-        const bool valid_row = tok < n && q0 + tok < a.num_tokens;
-        const int kv_end = x ? kv_end1 : kv_end0;
-        const int ntx = x ? nt1 : nt0;
-        const int row_lim = valid_row ? min(ctx - n + tok + 1, kv_end) : kv_end;   // keys [0, row_lim)
-        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const uint32_t t_s = t_lane + kTmemS0 + x * 128;
-        const uint32_t t_o = t_lane + kTmemO0 + x * 128;
+        const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+        float* red = reinterpret_cast<float*>(sm + G::kRed);
         const float c2 = a.scale_log2;
-        float m_used = -INFINITY, l = 0.f;
+        constexpr int kHalfCols = kKv / 2;                // score columns per thread
+        constexpr int kOCols = D / 2;                     // output columns per thread
+        float m_used[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        int row_lim[2];
+        bool valid_row[2];
+        for (int x = 0; x < 2; ++x) {
+            const int tok = t0 + x * a.tq + t;
+            valid_row[x] = tok < n && q0 + tok < a.num_tokens;
+            const int kv_end = x ? kv_end1 : kv_end0;
+            row_lim[x] = valid_row[x] ? min(ctx - n + tok + 1, kv_end) : kv_end;    // keys [0, row_lim)
+        }
+        // Post this half's value for row r of tile x and read the other half's.
+        auto exchange = [&](int x, int phase, float v, bool& ok_) {
+            float* slot = red + (((x * 2 + (phase & 1)) * 2) * kRows);
+            slot[hc * kRows + r] = v;
+            pa::mbar_arrive(&bars->red[x]);
+            ok_ = wait_warp(&bars->red[x], phase & 1, bars, a.status);
+            return ok_ ? slot[(1 - hc) * kRows + r] : v;
+        };
         bool ok = true;
-        for (int j = 0; j < ntx; ++j) {
-            ok = wait_warp(&bars->s_full[x], j & 1, bars, a.status);
-            // The two warpgroups take turns (A on tile j, then B on tile j, then
-            // A on tile j + 1, ...), so that each runs alone on the SM's
-            // sub-partitions while the tensor pipe works for the other.
-            if (ok && x == 0 && j >= 1 && j - 1 < nt1) ok = wait_warp(&bars->sm_done[1], (j - 1) & 1, bars, a.status);
-            if (ok && x == 1 && j < nt0) ok = wait_warp(&bars->sm_done[0], j & 1, bars, a.status);
-            if (!ok) break;
-            tc_fence_after();
-            float s[kKv];
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            for (int x = 0; x < 2; ++x) {
+                if (j >= (x ? nt1 : nt0)) continue;
+                ok = wait_warp(&bars->s_full[x], j & 1, bars, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t t_s = t_lane + kTmemS0 + x * 128;
+                float s[kHalfCols];
 #pragma unroll
-            for (int c = 0; c < kKv / 32; ++c) tmem_ld32(t_s + c * 32, s + c * 32);
-            tmem_wait_ld();
-            const int lim = row_lim - j * kKv;
-            if (lim < kKv) {
+                for (int c = 0; c < kHalfCols / 32; ++c) tmem_ld32(t_s + hc * kHalfCols + c * 32, s + c * 32);
+                tmem_wait_ld();
+                const int lim = row_lim[x] - j * kKv - hc * kHalfCols;     // valid columns of this half
+                if (lim < kHalfCols) {
 #pragma unroll
-                for (int c = 0; c < kKv; ++c) s[c] = c < lim ? s[c] : -INFINITY;
-            }
-            // row maximum: 8 independent chains of 3-input maxima
-            float mp[8];
+                    for (int c = 0; c < kHalfCols; ++c) s[c] = c < lim ? s[c] : -INFINITY;
+                }
+                float mp[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mp[k] = max3(s[k], s[8 + k], s[16 + k]);
+                for (int k = 0; k < 8; ++k) mp[k] = max3(s[k], s[8 + k], s[16 + k]);
 #pragma unroll
-            for (int c = 24; c + 16 <= kKv; c += 16)
+                for (int c = 24; c + 16 <= kHalfCols; c += 16)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mp[k] = max3(mp[k], s[c + k], s[c + 8 + k]);
-            if ((kKv - 24) % 16 == 8) {
+                    for (int k = 0; k < 8; ++k) mp[k] = max3(mp[k], s[c + k], s[c + 8 + k]);
+                if ((kHalfCols - 24) % 16 == 8) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[kKv - 8 + k]);
-            }
-            const float mt = fmaxf(max3(mp[0], mp[1], mp[2]), fmaxf(max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-            const float mts = mt * c2;                    // scale > 0: the maximum commutes with it
-            const bool rescale = mts > m_used + kRescaleThreshold;
-            const float m_new = rescale ? mts : m_used;
-            const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;   // exp2(-inf) = 0 on the first tile
-            if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-                // O holds the products of tiles < j (complete: this tile's
-                // scores were issued after them) and not yet this tile's
+                    for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[kHalfCols - 8 + k]);
+                }
+                float mt = fmaxf(max3(mp[0], mp[1], mp[2]), fmaxf(max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                mt = fmaxf(mt, exchange(x, j, mt, ok));
+                if (!ok) break;
+                const float mts = mt * c2;                // scale > 0: the maximum commutes with it
+                const bool rescale = mts > m_used[x] + kRescaleThreshold;
+                const float m_new = rescale ? mts : m_used[x];
+                const float alpha = rescale ? fast_exp2(m_used[x] - m_new) : 1.f;   // exp2(-inf) = 0 at first
+                if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+                    // O holds the products of tiles < j (complete: this tile's
+                    // scores were issued after them) and not yet this tile's
+                    const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(t_o + c * 32, o);
-                    tmem_wait_ld();
+                    for (int c = 0; c < kOCols / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(t_o + c * 32, o);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(t_o + c * 32, o);
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(t_o + c * 32, o);
+                    }
                 }
-            }
-            l *= alpha;
-            m_used = m_new;
-            const float neg = -m_used;
-            uint32_t w[kKv / 2];
-            float lp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // independent partial sums
-            if (lim >= kKv) {
-                // no masked weight: part of the exponentials on the FMA pipe
+                l[x] *= alpha;
+                m_used[x] = m_new;
+                const float neg = -m_used[x];
+                uint32_t w[kHalfCols / 2];
+                float lp[4] = {0.f, 0.f, 0.f, 0.f};       // independent partial sums
 #pragma unroll
-                for (int i = 0; i < kKv / 2; ++i) {
-                    const float x0 = fmaf(s[2 * i], c2, neg), x1 = fmaf(s[2 * i + 1], c2, neg);
-                    const bool poly = (i & 7) >= 8 - kPolyPairsPer8;
-                    const float p0 = poly ? exp2_poly(x0) : fast_exp2(x0);
-                    const float p1 = poly ? exp2_poly(x1) : fast_exp2(x1);
-                    lp[i & 7] += p0 + p1;
-                    w[i] = pack_bf16_rn(p0, p1);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kKv / 2; ++i) {
+                for (int i = 0; i < kHalfCols / 2; ++i) {
                     const float p0 = fast_exp2(fmaf(s[2 * i], c2, neg));
                     const float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg));
-                    lp[i & 7] += p0 + p1;
+                    lp[i & 3] += p0 + p1;
                     w[i] = pack_bf16_rn(p0, p1);
                 }
+                l[x] += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+                tmem_st32u(t_s + hc * (kHalfCols / 2), w);   // P columns over the first half of S
+                tmem_wait_st();
+                tc_fence_before();
+                pa::mbar_arrive(&bars->p_full[x]);
             }
-            l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
-            tmem_st32u(t_s, w);
-            tmem_st32u(t_s + 32, w + 32);
-            tmem_wait_st();
-            tc_fence_before();
-            pa::mbar_arrive(&bars->p_full[x]);
-            pa::mbar_arrive(&bars->sm_done[x]);
         }
-        if (ok && ntx > 0) ok = wait_warp(&bars->o_done[x], 0, bars, a.status);
-        if (ok && ntx > 0) {
+        for (int x = 0; x < 2 && ok; ++x) {
+            const int ntx = x ? nt1 : nt0;
+            if (ntx == 0) continue;
+            const float l_all = l[x] + exchange(x, ntx, l[x], ok);
+            if (ok) ok = wait_warp(&bars->o_done[x], 0, bars, a.status);
+            if (!ok) break;
             tc_fence_after();
-            const float inv = 1.f / l;
-            const size_t orow = ((size_t)(q0 + tok) * a.n_q_heads + (size_t)h * a.group + g) * D;
+            const int tok = t0 + x * a.tq + t;
+            const float inv = 1.f / l_all;
+            const size_t orow = ((size_t)(q0 + tok) * a.n_q_heads + (size_t)h * a.group + g) * D + hc * kOCols;
+            const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < kOCols / 32; ++c) {
                 float o[32];
                 tmem_ld32(t_o + c * 32, o);
                 tmem_wait_ld();
-                if (valid_row) {
+                if (valid_row[x]) {
                     if (a.out_f32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c * 32);
 #pragma unroll
