@@ -47,6 +47,8 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_partition_kernel_batch64_8b.md")
 KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_decode.cu")
+PREFILL_PROFILE = os.path.join(ROOT, "profiles", "prefill_kernel_prefill_prompts_8b.md")
+PREFILL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_prefill.cu")
 
 PREFILL_METRIC = "paged prefill-attn TFLOP/s (causal, 8B GQA shape; frac of bf16 tensor peak)"
 PREFILL_WORKLOADS = {
@@ -142,12 +144,12 @@ def prefill_flops(ctxs, news, n_q_heads, d_head):
     return f
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
+def profiled_traffic(summary=PROFILE_SUMMARY, source=KERNEL_SOURCE):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if
+    the summary was taken on the current kernel source; else None."""
     try:
-        text = open(PROFILE_SUMMARY).read()
-        src_hash = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()[:16]
+        text = open(summary).read()
+        src_hash = hashlib.sha256(open(source, "rb").read()).hexdigest()[:16]
         m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
         m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
         if m_hash and m_tr and m_hash.group(1) == src_hash:
@@ -516,7 +518,9 @@ def run_prefill_ours(args, world, rank, local):
         "tokens_per_s": round(total_tokens / total_s, 1),
         "roofline": {"bound": "tensor", "kernel": "pa_prefill (prefill_kernel<128>)", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind + " bf16 burst", "peak_sustained": peak_sus,
-                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(PREFILL_PROFILE, PREFILL_SOURCE) if sc.name == "prefill_prompts_8b"
+                     else None,
                      "algorithmic_flops_per_launch": flops, "avg_launch_us": round(att_s * 1e6, 2)},
         "e2e": {"value": round(e2e_flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_s / K * 1e3, 4)},
