@@ -56,6 +56,7 @@ extern "C" {
 #define PA_ERR_WORKSPACE     -5   /* workspace missing or too small             */
 #define PA_ERR_UNKNOWN_SEQ   -6
 #define PA_ERR_DUPLICATE_SEQ -7
+#define PA_ERR_SWAPPED       -8   /* the sequence's blocks are in host memory  */
 
 /* ---- device-side status bits (OR-ed into *status_dev) ---------------------- */
 #define PA_DEV_BAD_BLOCK_ID   1   /* table entry or copy pair outside the pool  */
@@ -287,6 +288,28 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches,
                    int n_kv_heads, int d_head, int block_size, int num_blocks,
                    int32_t* status_dev, void* stream);
 
+/* Copy whole blocks between two pools with the cache layout: for every pair
+ * (src, dst) in block_pairs and every layer, the K block src of src_k[l] goes
+ * to block dst of dst_k[l], and likewise for V.  Either side may be device
+ * memory or page-locked host memory (cudaHostAlloc / cudaHostRegister), which
+ * the kernel reads or writes directly (over NVLink-C2C on Grace hosts): this
+ * is the payload move of swapping ([P1] section 19, item 4).
+ *   dst_k, dst_v, src_k, src_v  HOST arrays of num_layers pointers; each pool
+ *                 [num_blocks][n_kv_heads][block_size][d_head] bf16, 16-byte
+ *                 aligned.  Host pools are translated with
+ *                 cudaPointerGetAttributes; pageable memory is rejected.
+ *   block_pairs   int32 [num_pairs][2] (src, dst), device or page-locked host.
+ * Ids outside [0, src_num_blocks) or [0, dst_num_blocks) are skipped and
+ * flagged PA_DEV_BAD_BLOCK_ID.  Destinations must be distinct.
+ * PA_ERR_INVALID_ARG (NULL, pageable or unknown pointer), PA_ERR_UNSUPPORTED,
+ * PA_ERR_MISALIGNED, PA_ERR_CUDA. */
+int pa_swap_blocks(void* const* dst_k, void* const* dst_v,
+                   const void* const* src_k, const void* const* src_v,
+                   int num_layers, const int32_t* block_pairs, int num_pairs,
+                   int n_kv_heads, int d_head, int block_size,
+                   int src_num_blocks, int dst_num_blocks,
+                   int32_t* status_dev, void* stream);
+
 /* ===========================================================================
  * Host block manager ([P1] sections 14-17 and 20)
  * ===========================================================================
@@ -376,6 +399,51 @@ int pa_alloc_append_token(pa_alloc_t* a, int64_t seq, int32_t token,
 
 /* Blocks with count 0 held for reuse (-1 for a NULL handle). */
 int pa_alloc_num_cached(const pa_alloc_t* a);
+
+/* ---------------------------------------------------------------------------
+ * Swap space ([P1] section 19, item 4: preemption by moving a request's
+ * blocks to host memory and back; item 3, preemption by recomputation, is
+ * pa_alloc_free now and pa_alloc_sequence_tokens later, which finds whatever
+ * the prefix cache still holds).  A pool of host blocks, numbered
+ * 0 .. num_host_blocks-1 and handed out like device blocks (a stack that
+ * starts with 0, 1, 2, ...).  The payload lives in caller-owned host pools
+ * laid out like the device caches; pa_swap_blocks moves it.
+ * ------------------------------------------------------------------------- */
+
+/* Size the host pool (0 disables swapping).  Only while no sequence is
+ * swapped out; PA_ERR_INVALID_ARG otherwise. */
+int pa_alloc_enable_swap(pa_alloc_t* a, int num_host_blocks);
+
+/* Swap out the running sequences seqs[0..n-1] (distinct).  Every distinct
+ * device block in their tables gets one host block, whose reference count
+ * is the number of these sequences that use it; the device blocks lose those
+ * references (freed, or queued by the prefix cache, at 0; blocks shared with
+ * other running sequences stay).  The sequences keep their lengths and token
+ * ids; until swapped in, only pa_alloc_free, pa_alloc_block_table (which then
+ * returns host block ids) and pa_alloc_seq_len accept them, the rest return
+ * PA_ERR_SWAPPED.  Writes the (device block, host block) pairs, first
+ * appearance order, to pairs_out[2i], [2i+1] and their count to *num_pairs;
+ * the caller copies them with pa_swap_blocks before the freed device blocks
+ * are written again (same stream).
+ * PA_ERR_UNKNOWN_SEQ, PA_ERR_SWAPPED (a sequence is already out),
+ * PA_ERR_INVALID_ARG (duplicates, or pair_capacity < *num_pairs: nothing
+ * changes, *num_pairs says how many are needed), PA_FAIL_NO_BLOCKS (too few
+ * free host blocks: nothing changes). */
+int pa_alloc_swap_out(pa_alloc_t* a, const int64_t* seqs, int n,
+                      int32_t* pairs_out, int pair_capacity, int* num_pairs);
+
+/* Swap in the swapped-out sequences seqs[0..n-1]: the mirror image.  Every
+ * distinct host block gets a fresh device block (free list first, then the
+ * prefix cache's eviction queue) with as many references as sequences of
+ * the batch use it; the host blocks lose those references.  Pairs are
+ * (host block, device block).  PA_ERR_INVALID_ARG also when a sequence is
+ * not swapped out; PA_FAIL_NO_BLOCKS when too few device blocks: nothing
+ * changes. */
+int pa_alloc_swap_in(pa_alloc_t* a, const int64_t* seqs, int n,
+                     int32_t* pairs_out, int pair_capacity, int* num_pairs);
+
+int pa_alloc_num_free_host(const pa_alloc_t* a);        /* -1 for NULL */
+int pa_alloc_is_swapped(const pa_alloc_t* a, int64_t seq); /* 1 out, 0 in, -1 unknown */
 /* Copy the eviction queue front (next evicted) to back into out (cap
  * entries); returns its size. */
 int pa_alloc_cached_list(const pa_alloc_t* a, int32_t* out, int cap);

@@ -49,6 +49,22 @@ caching"), off until enable_prefix_caching(True):
     tokens, so none of its later blocks is registered.
   * Running short is checked against the free list plus the queue (less the
     hits taken out of the queue); on failure nothing changes.
+
+Swapping ([P1] section 19, item 4: move a preempted request's blocks to host
+memory and back), enabled with a host pool of its own (a stack handing out
+host blocks 0, 1, 2, ...):
+  * swap_out(seqs) takes the distinct device blocks of the batch's tables in
+    first-appearance order and gives each one host block whose count is the
+    number of batch sequences using it; then each sequence, in batch order,
+    releases its device table as free() would; its table now names host
+    blocks.  Too few host blocks: nothing changes.
+  * swap_in(seqs) is the mirror image: distinct host blocks in
+    first-appearance order each get a fresh device block (free list, then the
+    eviction queue) with the batch count; each sequence drops one reference
+    per host block, and host blocks at 0 go back on the host stack.  Too few
+    device blocks: nothing changes.
+  * A swapped-out sequence accepts only free (which releases its host
+    blocks); appends, forks and table reads report it as swapped.
 """
 from collections import OrderedDict
 
@@ -57,6 +73,7 @@ FAIL_NO_BLOCKS = 1
 ERR_INVALID_ARG = -1
 ERR_UNKNOWN_SEQ = -6
 ERR_DUPLICATE_SEQ = -7
+ERR_SWAPPED = -8
 
 
 class RefAllocator:
@@ -78,6 +95,10 @@ class RefAllocator:
         self.seq_tokens = {}           # seq -> list of token ids, or None when unknown
         self.num_prompt_tokens = 0
         self.num_cached_tokens = 0
+        # swap space
+        self.host_free = []
+        self.host_refs = []
+        self.swapped = set()
 
     # -- prefix-cache helpers ----------------------------------------------
     def _available(self):
@@ -183,6 +204,8 @@ class RefAllocator:
             return ERR_UNKNOWN_SEQ
         if child in self.block_tables:
             return ERR_DUPLICATE_SEQ
+        if parent in self.swapped:
+            return ERR_SWAPPED
         for b in self.block_tables[parent]:
             self.ref_counts[b] += 1
         self.block_tables[child] = list(self.block_tables[parent])
@@ -203,6 +226,8 @@ class RefAllocator:
     def _append(self, seq, token):
         if seq not in self.block_tables:
             return ERR_UNKNOWN_SEQ, -1, -1, -1
+        if seq in self.swapped:
+            return ERR_SWAPPED, -1, -1, -1
         B = self.block_size
         length = self.seq_lengths[seq]
         table = self.block_tables[seq]
@@ -240,6 +265,16 @@ class RefAllocator:
     def free(self, seq):
         if seq not in self.block_tables:
             return OK
+        if seq in self.swapped:
+            for h in self.block_tables[seq]:
+                self.host_refs[h] -= 1
+                if self.host_refs[h] == 0:
+                    self.host_free.append(h)
+            self.swapped.discard(seq)
+            del self.block_tables[seq]
+            del self.seq_lengths[seq]
+            self.seq_tokens.pop(seq, None)
+            return OK
         idle_cached = []
         for b in self.block_tables[seq]:
             self.ref_counts[b] -= 1
@@ -263,6 +298,80 @@ class RefAllocator:
 
     def num_free(self):
         return len(self.free_blocks)
+
+    def enable_swap(self, num_host_blocks):
+        if num_host_blocks < 0 or self.swapped:
+            return ERR_INVALID_ARG
+        self.host_free = list(reversed(range(num_host_blocks)))
+        self.host_refs = [0] * num_host_blocks
+        return OK
+
+    def _swap_batch(self, seqs, from_swapped):
+        """Check a swap batch; return (status, distinct blocks in first-appearance
+        order, number of batch sequences using each)."""
+        seen, blocks, counts = set(), [], {}
+        for q in seqs:
+            if q not in self.block_tables:
+                return ERR_UNKNOWN_SEQ, None, None
+            if (q in self.swapped) != from_swapped:
+                return (ERR_INVALID_ARG if from_swapped else ERR_SWAPPED), None, None
+            if q in seen:
+                return ERR_INVALID_ARG, None, None
+            seen.add(q)
+            for b in self.block_tables[q]:
+                if b not in counts:
+                    counts[b] = 0
+                    blocks.append(b)
+                counts[b] += 1
+        return OK, blocks, counts
+
+    def swap_out(self, seqs):
+        """Returns (status, [(device block, host block), ...])."""
+        st, blocks, counts = self._swap_batch(seqs, False)
+        if st != OK:
+            return st, []
+        if len(blocks) > len(self.host_free):
+            return FAIL_NO_BLOCKS, []
+        to_host = {}
+        for b in blocks:
+            h = self.host_free.pop()
+            self.host_refs[h] = counts[b]
+            to_host[b] = h
+        for q in seqs:
+            idle_cached = []
+            for b in self.block_tables[q]:          # the device references go, as in free()
+                self.ref_counts[b] -= 1
+                if self.ref_counts[b] == 0:
+                    if b in self.block_key:
+                        idle_cached.append(b)
+                    else:
+                        self.free_blocks.append(b)
+            for b in reversed(idle_cached):
+                self.evict_queue[b] = None
+            self.block_tables[q] = [to_host[b] for b in self.block_tables[q]]
+            self.swapped.add(q)
+        return OK, [(b, to_host[b]) for b in blocks]
+
+    def swap_in(self, seqs):
+        """Returns (status, [(host block, device block), ...])."""
+        st, blocks, counts = self._swap_batch(seqs, True)
+        if st != OK:
+            return st, []
+        if len(blocks) > self._available():
+            return FAIL_NO_BLOCKS, []
+        to_dev = {}
+        for h in blocks:
+            b = self._take()
+            self.ref_counts[b] = counts[h]
+            to_dev[h] = b
+        for q in seqs:
+            for h in self.block_tables[q]:
+                self.host_refs[h] -= 1
+                if self.host_refs[h] == 0:
+                    self.host_free.append(h)
+            self.block_tables[q] = [to_dev[h] for h in self.block_tables[q]]
+            self.swapped.discard(q)
+        return OK, [(h, to_dev[h]) for h in blocks]
 
     def num_cached(self):
         return len(self.evict_queue)

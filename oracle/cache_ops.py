@@ -41,3 +41,13 @@ def copy_blocks(k_caches, v_caches, pairs):
             k_out[layer][dst] = k_out[layer][src]
             v_out[layer][dst] = v_out[layer][src]
     return k_out, v_out
+
+
+def swap_blocks(dst_k, dst_v, src_k, src_v, pairs):
+    """Move whole blocks between two pools of the same block shape (the
+    payload side of swapping, [P1] section 19, item 4): for each (src, dst)
+    pair, block src of the source pools is copied onto block dst of the
+    destination pools, K and V.  In place on the destination."""
+    for src, dst in pairs:
+        dst_k[dst] = src_k[src]
+        dst_v[dst] = src_v[src]

@@ -25,6 +25,7 @@ PA_ERR_CUDA = -4
 PA_ERR_WORKSPACE = -5
 PA_ERR_UNKNOWN_SEQ = -6
 PA_ERR_DUPLICATE_SEQ = -7
+PA_ERR_SWAPPED = -8
 
 PA_DEV_BAD_BLOCK_ID = 1
 PA_DEV_BAD_SLOT = 2
@@ -95,6 +96,13 @@ _SIGS = {
     "pa_alloc_sequence_tokens": (_c_int, [_vp, ctypes.c_int64, _i32p, _c_int, ctypes.POINTER(_c_int)]),
     "pa_alloc_append_token": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int32, _i64p, _i32p, _i32p]),
     "pa_alloc_num_cached": (_c_int, [_vp]),
+    "pa_alloc_enable_swap": (_c_int, [_vp, _c_int]),
+    "pa_alloc_swap_out": (_c_int, [_vp, _i64p, _c_int, _i32p, _c_int, ctypes.POINTER(_c_int)]),
+    "pa_alloc_swap_in": (_c_int, [_vp, _i64p, _c_int, _i32p, _c_int, ctypes.POINTER(_c_int)]),
+    "pa_alloc_num_free_host": (_c_int, [_vp]),
+    "pa_alloc_is_swapped": (_c_int, [_vp, ctypes.c_int64]),
+    "pa_swap_blocks": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
+                                _vp]),
     "pa_alloc_cached_list": (_c_int, [_vp, _i32p, _c_int]),
 }
 
@@ -311,6 +319,45 @@ def pa_copy_blocks(k_caches, v_caches, block_pairs, status=None, stream=None):
     return _check(st, "pa_copy_blocks")
 
 
+def _dev_or_pinned(t, dtype, name):
+    """Pointer of a CUDA tensor or of a page-locked host tensor."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("%s must be a CUDA tensor or a page-locked (pinned) host tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def pa_swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs, status=None, stream=None):
+    """For every (src, dst) row of block_pairs (int32 [P, 2]) copy block src
+    of every src pool onto block dst of the matching dst pool.  Pools are
+    lists (one per layer) of CUDA or pinned host bf16 tensors
+    [num_blocks, Hkv, B, D]; source and destination may differ in num_blocks."""
+    L = len(src_k)
+    if not (len(src_v) == len(dst_k) == len(dst_v) == L):
+        raise ValueError("the four pool lists must have the same length")
+    P = block_pairs.shape[0] if block_pairs is not None else 0
+    if L == 0 or P == 0:
+        return PA_OK
+    SNB, Hkv, B, D = src_k[0].shape
+    DNB = dst_k[0].shape[0]
+    for t in list(src_k) + list(src_v):
+        if tuple(t.shape) != (SNB, Hkv, B, D):
+            raise ValueError("source pools must share one shape")
+    for t in list(dst_k) + list(dst_v):
+        if tuple(t.shape) != (DNB, Hkv, B, D):
+            raise ValueError("destination pools must share one shape")
+    arr = lambda ts, nm: (ctypes.c_void_p * L)(*[_dev_or_pinned(t, torch.bfloat16, nm).value for t in ts])
+    st = _lib.pa_swap_blocks(arr(dst_k, "dst_k"), arr(dst_v, "dst_v"), arr(src_k, "src_k"), arr(src_v, "src_v"), L,
+                             _dev_or_pinned(block_pairs, torch.int32, "block_pairs"), int(P), int(Hkv), int(D), int(B),
+                             int(SNB), int(DNB), _opt_dev(status, torch.int32, "status"), _stream(stream))
+    return _check(st, "pa_swap_blocks")
+
+
 # ----------------------------------------------------------------------------
 # host block manager
 # ----------------------------------------------------------------------------
@@ -371,6 +418,31 @@ class BlockAllocator:
 
     def num_cached(self):
         return _lib.pa_alloc_num_cached(self._h)
+
+    def enable_swap(self, num_host_blocks):
+        return _lib.pa_alloc_enable_swap(self._h, int(num_host_blocks))
+
+    def _swap(self, fn, seqs):
+        seqs, sp = _i64(seqs)
+        cap = max(1, sum(len(self.block_table(int(q))) for q in seqs if self.seq_len(int(q)) >= 0))
+        pairs = np.zeros((cap, 2), dtype=np.int32)
+        n = ctypes.c_int(0)
+        st = fn(self._h, sp, len(seqs), pairs.ctypes.data_as(_i32p), cap, ctypes.byref(n))
+        return st, (pairs[:n.value].copy() if st == 0 else np.zeros((0, 2), dtype=np.int32))
+
+    def swap_out(self, seqs):
+        """Returns (status, pairs [k, 2] int32 of (device block, host block))."""
+        return self._swap(_lib.pa_alloc_swap_out, seqs)
+
+    def swap_in(self, seqs):
+        """Returns (status, pairs [k, 2] int32 of (host block, device block))."""
+        return self._swap(_lib.pa_alloc_swap_in, seqs)
+
+    def num_free_host(self):
+        return _lib.pa_alloc_num_free_host(self._h)
+
+    def is_swapped(self, seq):
+        return _lib.pa_alloc_is_swapped(self._h, int(seq))
 
     def cached_list(self):
         """Zero-count cached blocks, next to be evicted first."""

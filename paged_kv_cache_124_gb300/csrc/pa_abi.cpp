@@ -16,6 +16,7 @@ const char* pa_status_string(int status) {
         case PA_ERR_WORKSPACE: return "workspace missing or too small";
         case PA_ERR_UNKNOWN_SEQ: return "unknown sequence";
         case PA_ERR_DUPLICATE_SEQ: return "sequence already exists";
+        case PA_ERR_SWAPPED: return "sequence is swapped out";
         default: return "unknown status";
     }
 }

@@ -10,6 +10,13 @@
 // here: the planned slot and copy pair drive pa_reshape_and_cache and
 // pa_copy_blocks on the GPU.
 //
+// Swapping (same page, section 19, item 4): a batch of sequences can move
+// to a pool of host blocks and back.  Every distinct device block of the
+// batch gets one host block, referenced by as many sequences of the batch
+// as shared it; the device blocks lose those references (and are freed or
+// queued as usual).  Swapping in is the mirror image.  Both plan only: the
+// returned (source, destination) pairs drive pa_swap_blocks.
+//
 // Prefix caching (same page, section 18; "PagedAttention in vLLM: scattered
 // memory, exact attention", section 6; "PagedAttention and KV Memory"): a
 // full block whose token ids are known is registered under a key made of its
@@ -49,7 +56,8 @@ uint64_t block_key(uint64_t parent, const int32_t* tokens, int n) {
 }
 
 struct Sequence {
-    std::vector<int32_t> table;   // logical block -> physical block
+    std::vector<int32_t> table;   // logical block -> physical block (host block while swapped)
+    bool swapped = false;
     int32_t length = 0;           // cached positions
     bool has_tokens = false;      // token ids known: full blocks can be registered
     std::vector<int32_t> tokens;  // token id of every position (when has_tokens)
@@ -75,6 +83,11 @@ struct pa_alloc {
     std::vector<std::list<int32_t>::iterator> lru_pos;
     std::vector<char> in_lru;
     int64_t prompt_tokens = 0, cached_tokens = 0;
+    // swap space
+    int32_t num_host_blocks = 0;
+    std::vector<int32_t> host_free;                     // top = back()
+    std::vector<int32_t> host_refs;
+    int32_t num_swapped = 0;
 
     pa_alloc(int nb, int bs)
         : num_blocks(nb), block_size(bs), refs(nb, 0), registered(nb, 0), reg_key(nb, 0), reg_parent(nb, 0),
@@ -136,6 +149,7 @@ struct pa_alloc {
         auto it = seqs.find(seq);
         if (it == seqs.end()) return PA_ERR_UNKNOWN_SEQ;
         Sequence& s = it->second;
+        if (s.swapped) return PA_ERR_SWAPPED;
         const int32_t off = s.length % block_size;
         int32_t cs = -1, cd = -1, blk;
         if (off != 0) {
@@ -299,6 +313,7 @@ int pa_alloc_fork(pa_alloc_t* a, int64_t parent, int64_t child) {
     auto it = a->seqs.find(parent);
     if (it == a->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
     if (a->seqs.count(child)) return PA_ERR_DUPLICATE_SEQ;
+    if (it->second.swapped) return PA_ERR_SWAPPED;
     Sequence s = it->second;                 // copy before insert (rehash)
     for (int32_t b : s.table) a->refs[b] += 1;
     a->seqs.emplace(child, std::move(s));
@@ -347,7 +362,13 @@ int pa_alloc_free(pa_alloc_t* a, int64_t seq) {
     if (!a) return PA_ERR_INVALID_ARG;
     auto it = a->seqs.find(seq);
     if (it == a->seqs.end()) return PA_OK;
-    a->release_table(it->second.table);
+    if (it->second.swapped) {
+        for (int32_t h : it->second.table)
+            if (--a->host_refs[h] == 0) a->host_free.push_back(h);
+        --a->num_swapped;
+    } else {
+        a->release_table(it->second.table);
+    }
     a->seqs.erase(it);
     return PA_OK;
 }
@@ -370,6 +391,7 @@ int pa_alloc_build_tables(const pa_alloc_t* a, const int64_t* seqs, int n, int32
     for (int i = 0; i < n; ++i) {
         auto it = a->seqs.find(seqs[i]);
         if (it == a->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
+        if (it->second.swapped) return PA_ERR_SWAPPED;
         const auto& t = it->second.table;
         if ((int)t.size() > max_blocks) return PA_ERR_INVALID_ARG;
         int32_t* row = tables + (size_t)i * max_blocks;
@@ -385,6 +407,7 @@ int pa_alloc_slot_mapping(const pa_alloc_t* a, int64_t seq, int start, int n, in
     auto it = a->seqs.find(seq);
     if (it == a->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
     const Sequence& s = it->second;
+    if (s.swapped) return PA_ERR_SWAPPED;
     if ((int64_t)start + n > s.length) return PA_ERR_INVALID_ARG;
     const int B = a->block_size;
     for (int k = 0; k < n; ++k) {
@@ -443,6 +466,110 @@ int pa_alloc_enable_prefix_caching(pa_alloc_t* a, int enable) {
 }
 
 int pa_alloc_num_cached(const pa_alloc_t* a) { return a ? (int)a->lru.size() : -1; }
+
+int pa_alloc_enable_swap(pa_alloc_t* a, int num_host_blocks) {
+    if (!a || num_host_blocks < 0 || a->num_swapped != 0) return PA_ERR_INVALID_ARG;
+    a->num_host_blocks = num_host_blocks;
+    a->host_refs.assign(num_host_blocks, 0);
+    a->host_free.clear();
+    for (int b = num_host_blocks - 1; b >= 0; --b) a->host_free.push_back(b);
+    return PA_OK;
+}
+
+int pa_alloc_num_free_host(const pa_alloc_t* a) { return a ? (int)a->host_free.size() : -1; }
+
+int pa_alloc_is_swapped(const pa_alloc_t* a, int64_t seq) {
+    if (!a) return -1;
+    auto it = a->seqs.find(seq);
+    return it == a->seqs.end() ? -1 : (it->second.swapped ? 1 : 0);
+}
+
+// Shared by swap_out and swap_in: check the batch (known, distinct, all in
+// state `from_swapped`), collect its distinct blocks in first-appearance
+// order with the number of batch sequences referencing each.
+static int swap_plan(pa_alloc_t* a, const int64_t* seqs, int n, bool from_swapped, std::vector<int32_t>& blocks,
+                     std::vector<int32_t>& counts) {
+    if (n < 0 || (n > 0 && !seqs)) return PA_ERR_INVALID_ARG;
+    std::unordered_map<int32_t, int32_t> index;
+    std::unordered_map<int64_t, char> seen;
+    for (int i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seqs[i]);
+        if (it == a->seqs.end()) return PA_ERR_UNKNOWN_SEQ;
+        if (it->second.swapped != from_swapped) return from_swapped ? PA_ERR_INVALID_ARG : PA_ERR_SWAPPED;
+        if (seen.count(seqs[i])) return PA_ERR_INVALID_ARG;
+        seen.emplace(seqs[i], 1);
+        for (int32_t b : it->second.table) {
+            auto f = index.find(b);
+            if (f == index.end()) {
+                index.emplace(b, (int32_t)blocks.size());
+                blocks.push_back(b);
+                counts.push_back(1);
+            } else {
+                counts[f->second] += 1;
+            }
+        }
+    }
+    return PA_OK;
+}
+
+int pa_alloc_swap_out(pa_alloc_t* a, const int64_t* seqs, int n, int32_t* pairs_out, int pair_capacity,
+                      int* num_pairs) {
+    if (!a || !num_pairs) return PA_ERR_INVALID_ARG;
+    *num_pairs = 0;
+    std::vector<int32_t> blocks, counts;
+    int st = swap_plan(a, seqs, n, false, blocks, counts);
+    if (st != PA_OK) return st;
+    *num_pairs = (int)blocks.size();
+    if ((int)blocks.size() > pair_capacity || (!pairs_out && !blocks.empty())) return PA_ERR_INVALID_ARG;
+    if (blocks.size() > a->host_free.size()) return PA_FAIL_NO_BLOCKS;
+    std::unordered_map<int32_t, int32_t> to_host;
+    for (size_t i = 0; i < blocks.size(); ++i) {
+        const int32_t hb = a->host_free.back();
+        a->host_free.pop_back();
+        a->host_refs[hb] = counts[i];
+        to_host.emplace(blocks[i], hb);
+        pairs_out[2 * i] = blocks[i];
+        pairs_out[2 * i + 1] = hb;
+    }
+    for (int i = 0; i < n; ++i) {
+        Sequence& s = a->seqs.find(seqs[i])->second;
+        a->release_table(s.table);            // device references go (blocks freed or queued at 0)
+        for (int32_t& b : s.table) b = to_host[b];
+        s.swapped = true;
+        ++a->num_swapped;
+    }
+    return PA_OK;
+}
+
+int pa_alloc_swap_in(pa_alloc_t* a, const int64_t* seqs, int n, int32_t* pairs_out, int pair_capacity,
+                     int* num_pairs) {
+    if (!a || !num_pairs) return PA_ERR_INVALID_ARG;
+    *num_pairs = 0;
+    std::vector<int32_t> blocks, counts;
+    int st = swap_plan(a, seqs, n, true, blocks, counts);
+    if (st != PA_OK) return st;
+    *num_pairs = (int)blocks.size();
+    if ((int)blocks.size() > pair_capacity || (!pairs_out && !blocks.empty())) return PA_ERR_INVALID_ARG;
+    if ((int64_t)blocks.size() > a->available()) return PA_FAIL_NO_BLOCKS;
+    std::unordered_map<int32_t, int32_t> to_dev;
+    for (size_t i = 0; i < blocks.size(); ++i) {
+        const int32_t db = a->take();
+        a->refs[db] = counts[i];
+        to_dev.emplace(blocks[i], db);
+        pairs_out[2 * i] = blocks[i];
+        pairs_out[2 * i + 1] = db;
+    }
+    for (int i = 0; i < n; ++i) {
+        Sequence& s = a->seqs.find(seqs[i])->second;
+        for (int32_t& h : s.table) {
+            if (--a->host_refs[h] == 0) a->host_free.push_back(h);
+            h = to_dev[h];
+        }
+        s.swapped = false;
+        --a->num_swapped;
+    }
+    return PA_OK;
+}
 
 int pa_alloc_cached_list(const pa_alloc_t* a, int32_t* out, int cap) {
     if (!a) return -1;

@@ -95,6 +95,60 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const __grid_
     for (; i < chunks_per_block; i += kCopyThreads) d[i] = s[i];
 }
 
+struct SwapPtrs {
+    const uint4* src[2][kMaxLayersPerLaunch];   // [K / V][layer]
+    uint4* dst[2][kMaxLayersPerLaunch];
+};
+
+// grid: (pair, layer, 0 = K / 1 = V); each thread block moves one whole
+// block between two pools, either of which may be page-locked host memory:
+// 8 independent 16-byte loads in flight per thread to cover the link latency.
+__global__ void __launch_bounds__(kCopyThreads) swap_blocks_kernel(const __grid_constant__ SwapPtrs ptrs,
+                                                                   const int32_t* __restrict__ pairs,
+                                                                   long long chunks_per_block, int src_blocks,
+                                                                   int dst_blocks, int32_t* status) {
+    const int p = blockIdx.x;
+    const int layer = blockIdx.y;
+    const int src = pairs[2 * p];
+    const int dst = pairs[2 * p + 1];
+    if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+        if (threadIdx.x == 0) pa::set_status(status, PA_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    const uint4* s = ptrs.src[blockIdx.z][layer] + (size_t)src * chunks_per_block;
+    uint4* d = ptrs.dst[blockIdx.z][layer] + (size_t)dst * chunks_per_block;
+    constexpr int U = 8;
+    long long i = threadIdx.x;
+    for (; i + (U - 1) * kCopyThreads < chunks_per_block; i += U * kCopyThreads) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) r[u] = s[i + u * kCopyThreads];
+#pragma unroll
+        for (int u = 0; u < U; ++u) d[i + u * kCopyThreads] = r[u];
+    }
+    for (; i < chunks_per_block; i += kCopyThreads) d[i] = s[i];
+}
+
+// Device address of a device, managed or page-locked host pointer; nullptr
+// for pageable or unknown memory.
+const void* device_address(const void* p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    switch (attr.type) {
+        case cudaMemoryTypeDevice:
+        case cudaMemoryTypeManaged:
+            return p;
+        case cudaMemoryTypeHost:
+            return attr.devicePointer;
+        default:
+            return nullptr;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -143,6 +197,45 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
         }
         dim3 grid(num_pairs, nl, 2);
         copy_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(ptrs, block_pairs, chunks, num_blocks, status_dev);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+int pa_swap_blocks(void* const* dst_k, void* const* dst_v, const void* const* src_k, const void* const* src_v,
+                   int num_layers, const int32_t* block_pairs, int num_pairs, int n_kv_heads, int d_head, int block_size,
+                   int src_num_blocks, int dst_num_blocks, int32_t* status_dev, void* stream) {
+    if (num_layers < 0 || num_pairs < 0 || n_kv_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head)) return PA_ERR_UNSUPPORTED;
+    if (num_layers == 0 || num_pairs == 0) return PA_OK;
+    if (!dst_k || !dst_v || !src_k || !src_v || !block_pairs) return PA_ERR_INVALID_ARG;
+    if (num_pairs > 2147483647 / 2) return PA_ERR_UNSUPPORTED;
+    const int32_t* pairs = static_cast<const int32_t*>(device_address(block_pairs));
+    if (!pairs) return PA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(pairs) & 3u) return PA_ERR_MISALIGNED;
+    const long long chunks = (long long)n_kv_heads * block_size * d_head / 8;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
+        const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
+        SwapPtrs ptrs{};
+        for (int l = 0; l < nl; ++l) {
+            const void* sk = device_address(src_k[l0 + l]);
+            const void* sv = device_address(src_v[l0 + l]);
+            const void* dk = device_address(dst_k[l0 + l]);
+            const void* dv = device_address(dst_v[l0 + l]);
+            if (!sk || !sv || !dk || !dv) return PA_ERR_INVALID_ARG;
+            if (!pa_host::aligned16(sk) || !pa_host::aligned16(sv) || !pa_host::aligned16(dk) ||
+                !pa_host::aligned16(dv))
+                return PA_ERR_MISALIGNED;
+            ptrs.src[0][l] = static_cast<const uint4*>(sk);
+            ptrs.src[1][l] = static_cast<const uint4*>(sv);
+            ptrs.dst[0][l] = static_cast<uint4*>(const_cast<void*>(dk));
+            ptrs.dst[1][l] = static_cast<uint4*>(const_cast<void*>(dv));
+        }
+        dim3 grid(num_pairs, nl, 2);
+        swap_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(ptrs, pairs, chunks, src_num_blocks, dst_num_blocks,
+                                                          status_dev);
         if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;

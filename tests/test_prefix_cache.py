@@ -18,7 +18,8 @@ from _golden import load
 api = pytest.importorskip("paged_kv_cache_124_gb300.api")
 
 STATUS_MAP = {AL.OK: api.PA_OK, AL.FAIL_NO_BLOCKS: api.PA_FAIL_NO_BLOCKS, AL.ERR_INVALID_ARG: api.PA_ERR_INVALID_ARG,
-              AL.ERR_UNKNOWN_SEQ: api.PA_ERR_UNKNOWN_SEQ, AL.ERR_DUPLICATE_SEQ: api.PA_ERR_DUPLICATE_SEQ}
+              AL.ERR_UNKNOWN_SEQ: api.PA_ERR_UNKNOWN_SEQ, AL.ERR_DUPLICATE_SEQ: api.PA_ERR_DUPLICATE_SEQ,
+              AL.ERR_SWAPPED: api.PA_ERR_SWAPPED}
 TRACES = {k: v for k, v in load("p2_prefix_cache.json").items() if not k.startswith("_")}
 
 
@@ -67,6 +68,23 @@ class _OracleView:
     def cached_list(self):
         return self.m.cached_list()
 
+    def enable_swap(self, n):
+        return STATUS_MAP[self.m.enable_swap(n)]
+
+    def swap_out(self, seqs):
+        st, pairs = self.m.swap_out(seqs)
+        return STATUS_MAP[st], [tuple(p) for p in pairs]
+
+    def swap_in(self, seqs):
+        st, pairs = self.m.swap_in(seqs)
+        return STATUS_MAP[st], [tuple(p) for p in pairs]
+
+    def num_free_host(self):
+        return len(self.m.host_free)
+
+    def is_swapped(self, s):
+        return -1 if s not in self.m.block_tables else int(s in self.m.swapped)
+
 
 class _AbiView:
     def __init__(self, nb, bs):
@@ -107,6 +125,23 @@ class _AbiView:
 
     def cached_list(self):
         return self.m.cached_list()
+
+    def enable_swap(self, n):
+        return self.m.enable_swap(n)
+
+    def swap_out(self, seqs):
+        st, pairs = self.m.swap_out(seqs)
+        return st, [tuple(int(v) for v in p) for p in pairs]
+
+    def swap_in(self, seqs):
+        st, pairs = self.m.swap_in(seqs)
+        return st, [tuple(int(v) for v in p) for p in pairs]
+
+    def num_free_host(self):
+        return self.m.num_free_host()
+
+    def is_swapped(self, s):
+        return self.m.is_swapped(s)
 
 
 VIEWS = {"oracle": _OracleView, "abi": _AbiView}
