@@ -596,6 +596,185 @@ def run_prefill_reference(args, world, rank):
 
 
 # ----------------------------------------------------------------------------
+# swapping (blocks of preempted sequences to page-locked host memory and back)
+# ----------------------------------------------------------------------------
+
+SWAP_METRIC = "paged KV swap GB/s (device<->host block moves, 8B GQA shape; frac of measured link copy)"
+SWAP_LAYERS = 8
+SWAP_SEQS = 16
+
+
+def _link_copy_peak(dev, nbytes=1 << 30, reps=5):
+    """Plain copy-engine bandwidth of this GPU's host link, per direction:
+    cudaMemcpyAsync of one contiguous page-locked buffer (best of reps)."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = {}
+    for name, dst, src in (("d2h", h, d), ("h2d", d, h)):
+        t = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize(dev)
+            t.append(a.elapsed_time(b) / 1e3)
+        best[name] = nbytes / min(t) / 1e9
+    del h, d
+    return best
+
+
+def run_swap_ours(args, world, rank, local):
+    from paged_kv_cache_124_gb300 import api
+    from paged_kv_cache_124_gb300.runner import ScenarioRunner
+
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    seed = replica_seed(args.seed, rank)
+    sc = I.batch64_8b(seed, args.block_size)
+    run = ScenarioRunner(sc, device=dev, data_device="cpu").replay()
+    alloc = run.alloc
+    L = SWAP_LAYERS
+    # every layer holds the same block placement; the payload of layer 0 is real, the others are copies of it
+    kc = [run.k_caches[0]] + [run.k_caches[0].clone() for _ in range(L - 1)]
+    vc = [run.v_caches[0]] + [run.v_caches[0].clone() for _ in range(L - 1)]
+    victims = list(range(SWAP_SEQS))
+    n_blocks = sum(len(alloc.block_table(s)) for s in victims)
+    assert alloc.enable_swap(n_blocks) == 0
+    shape = (n_blocks,) + tuple(kc[0].shape[1:])
+    hk = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    hv = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    block_bytes = 2 * int(np.prod(shape[1:])) * 2 * L          # K and V, all layers
+    stream = torch.cuda.current_stream(dev)
+    before = [t.clone() for t in (kc[0], vc[0])]
+    tab0 = alloc.build_tables(victims, max(len(alloc.block_table(s)) for s in victims))[0]
+
+    # Page-locked pair lists, two per direction: a list is rewritten only once
+    # the copy that read it has run (its event), so the host never waits on
+    # the copy just issued.
+    ring = {d: [torch.empty((n_blocks, 2), dtype=torch.int32).pin_memory() for _ in range(2)] for d in ("out", "in")}
+    ring_ev = {d: [None, None] for d in ("out", "in")}
+    counter = [0]
+
+    def issue(direction, pairs, dst_k, dst_v, src_k, src_v):
+        slot = counter[0] & 1
+        if ring_ev[direction][slot] is not None:
+            ring_ev[direction][slot].synchronize()
+        buf = ring[direction][slot][:len(pairs)]
+        buf.copy_(torch.from_numpy(pairs))
+        api.pa_swap_blocks(dst_k, dst_v, src_k, src_v, buf, stream=stream)
+        ev_ = torch.cuda.Event()
+        ev_.record(stream)
+        ring_ev[direction][slot] = ev_
+
+    def step():
+        st, out_pairs = alloc.swap_out(victims)
+        assert st == 0
+        issue("out", out_pairs, hk, hv, kc, vc)
+        st, in_pairs = alloc.swap_in(victims)
+        assert st == 0
+        issue("in", in_pairs, kc, vc, hk, hv)
+        counter[0] += 1
+        return len(out_pairs) + len(in_pairs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    K = args.steps
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    moved = 0
+    for _ in range(K):
+        moved += step()
+    torch.cuda.synchronize(dev)
+    elapsed = time.perf_counter() - t0
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    total_s, total_bytes = reduce_timing(elapsed, moved * block_bytes, world, dev)
+    # one out-kernel and one in-kernel timed alone with events, for the roofline
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    st, out_pairs = alloc.swap_out(victims)
+    pairs_h = torch.from_numpy(out_pairs).pin_memory()
+    ev[0].record(stream)
+    api.pa_swap_blocks(hk, hv, kc, vc, pairs_h, stream=stream)
+    ev[1].record(stream)
+    st, in_pairs = alloc.swap_in(victims)
+    pairs_h2 = torch.from_numpy(in_pairs).pin_memory()
+    ev[2].record(stream)
+    api.pa_swap_blocks(kc, vc, hk, hv, pairs_h2, stream=stream)
+    ev[3].record(stream)
+    torch.cuda.synchronize(dev)
+    out_s = ev[0].elapsed_time(ev[1]) / 1e3
+    in_s = ev[2].elapsed_time(ev[3]) / 1e3
+    out_gbs = len(out_pairs) * block_bytes / out_s / 1e9
+    in_gbs = len(in_pairs) * block_bytes / in_s / 1e9
+    # payload check: after all the round trips the victims' blocks hold what they held at the start
+    tab_after, ctx_v = alloc.build_tables(victims, tab0.shape[1])
+    for i in range(len(victims)):
+        nb = -(-int(ctx_v[i]) // sc.block_size)
+        for a, b in ((before[0], kc[0]), (before[1], vc[0])):
+            # compare bit patterns: the blocks' unused tail slots hold NaN
+            if not torch.equal(a[torch.from_numpy(tab0[i, :nb]).long().to(dev)].view(torch.int16),
+                               b[torch.from_numpy(tab_after[i, :nb]).long().to(dev)].view(torch.int16)):
+                raise RuntimeError("swap round trip changed the payload of sequence %d" % victims[i])
+    if rank != 0:
+        return None
+    link = _link_copy_peak(dev)
+    peak = min(link["d2h"], link["h2d"])
+    line = {
+        "metric": SWAP_METRIC, "value": round(total_bytes / total_s / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes moved)", "data": "synthetic",
+        "config": {"workload": "swap_8b", "sequences_swapped": SWAP_SEQS, "layers": L, "blocks_per_direction":
+                   n_blocks, "block_bytes_all_layers_kv": block_bytes, "block_size": sc.block_size,
+                   "n_kv_heads": sc.n_kv_heads, "d_head": sc.d_head,
+                   "step": "swap_out plan + pa_swap_blocks to pinned host, swap_in plan + pa_swap_blocks back",
+                   "l2": "each direction moves %.2f GB (> 129 MB L2); no flush" % (n_blocks * block_bytes / 1e9)},
+        "roofline": {"bound": "host link", "kernel": "swap_blocks_kernel", "achieved": round(min(out_gbs, in_gbs), 1),
+                     "out_gbs": round(out_gbs, 1), "in_gbs": round(in_gbs, 1), "peak": round(peak, 1),
+                     "peak_kind": "measured in this run: cudaMemcpyAsync of 1 GiB page-locked (d2h %.1f, h2d %.1f GB/s)"
+                                  % (link["d2h"], link["h2d"]),
+                     "unit": "GB/s", "frac": round(min(out_gbs, in_gbs) / peak, 4), "traffic": None},
+        "e2e": {"value": round(total_bytes / total_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(n_blocks * block_bytes), "d2h_bytes_per_step": int(n_blocks * block_bytes),
+                "note": "swapping is host<->device by definition: value is already end to end (planning included)"},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = swap_cpu_baseline(sc, args.cpu_seconds)
+    return line
+
+
+def swap_cpu_baseline(sc, budget_s):
+    """The oracle's swap_blocks (NumPy copies of whole blocks) on host pools of
+    the same block shape, as many block moves as fit about budget_s."""
+    from oracle import cache_ops as C
+    shape = (sc.n_kv_heads, sc.block_size, sc.d_head)
+    nb = 4096
+    rng = np.random.default_rng(0)
+    src_k = rng.integers(0, 65535, size=(nb,) + shape, dtype=np.uint16)
+    src_v = src_k.copy()
+    dst_k, dst_v = np.zeros_like(src_k), np.zeros_like(src_v)
+    pairs = list(zip(rng.permutation(nb).tolist(), rng.permutation(nb).tolist()))
+    moved, t = 0, 0.0
+    t0 = time.perf_counter()
+    while t < budget_s:
+        C.swap_blocks(dst_k, dst_v, src_k, src_v, pairs)
+        moved += len(pairs)
+        t = time.perf_counter() - t0
+    per_block = 2 * int(np.prod(shape)) * 2
+    return {"value": round(moved * per_block / t / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "oracle swap_blocks between two host pools of %d blocks, %d block moves (K and V), %.1f s"
+                      % (nb, moved, t)}
+
+
+# ----------------------------------------------------------------------------
 # CPU oracle (the cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------
 
@@ -668,7 +847,8 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(PREFILL_WORKLOADS), default="batch64_8b")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(PREFILL_WORKLOADS) + ["swap_8b"],
+                   default="batch64_8b")
     p.add_argument("--block-size", type=int, default=16)
     p.add_argument("--partition", type=int, default=0, help="positions per partition (0 = library default)")
     p.add_argument("--seed", type=int, default=0)
@@ -680,7 +860,19 @@ def main(argv=None):
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     prefill = args.workload in PREFILL_WORKLOADS
-    if args.impl == "reference":
+    if args.workload == "swap_8b":
+        if args.impl == "reference":
+            line = None
+            if rank == 0:
+                cb = swap_cpu_baseline(I.batch64_8b(args.seed, args.block_size), args.cpu_seconds)
+                line = {"impl": "reference", "metric": SWAP_METRIC, "value": cb["value"], "unit": "GB/s",
+                        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bytes moved)", "data": "synthetic",
+                        "config": {"workload": "swap_8b"}, "cpu_baseline": cb,
+                        "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        else:
+            line = run_swap_ours(args, world, rank, local)
+    elif args.impl == "reference":
         line = (run_prefill_reference if prefill else run_reference)(args, world, rank)
     else:
         line = (run_prefill_ours if prefill else run_ours)(args, world, rank, local)

@@ -298,7 +298,9 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches,
  *                 [num_blocks][n_kv_heads][block_size][d_head] bf16, 16-byte
  *                 aligned.  Host pools are translated with
  *                 cudaPointerGetAttributes; pageable memory is rejected.
- *   block_pairs   int32 [num_pairs][2] (src, dst), device or page-locked host.
+ *   block_pairs   int32 [num_pairs][2] (src, dst), device or page-locked host;
+ *                 read by the kernel, so it must stay unchanged until the copy
+ *                 has run (stream order), like every input of an async call.
  * Ids outside [0, src_num_blocks) or [0, dst_num_blocks) are skipped and
  * flagged PA_DEV_BAD_BLOCK_ID.  Destinations must be distinct.
  * PA_ERR_INVALID_ARG (NULL, pageable or unknown pointer), PA_ERR_UNSUPPORTED,
