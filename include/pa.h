@@ -126,6 +126,26 @@ const char* pa_status_string(int status);
  * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED,
  * PA_ERR_WORKSPACE or PA_ERR_CUDA (launch failure).
  */
+/* FP8 caches ([P3] "Alternatives and ecosystem": quantised KV cuts the bytes
+ * per token; [P2] section 11: exactness is judged at the same KV precision).
+ * k_cache / v_cache hold E4M3 codes (1 byte per element, same
+ * [num_blocks][n_kv_heads][block_size][d_head] layout) written by
+ * pa_reshape_and_cache_fp8; element = E4M3(code) * k_scale (or v_scale).  The
+ * result is the attention over those dequantised keys and values, computed
+ * as pa_decode computes it (fp32 softmax and accumulation; f16 operands,
+ * which hold every E4M3 value exactly; q is rounded to f16 after a per-head
+ * power-of-two scaling, P is split into two f16 terms).  Same arguments and
+ * workspace as pa_decode, plus the two scales (finite, > 0).  d_head must be
+ * 128 (PA_ERR_UNSUPPORTED otherwise). */
+int pa_decode_fp8(void* out, int out_dtype, const void* q,
+                  const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens,
+                  int block_size, float scale, float k_scale, float v_scale,
+                  int n_q_heads, int n_kv_heads, int d_head, int num_seqs,
+                  int max_blocks_per_seq, int num_blocks, int max_context_len,
+                  int partition_size, void* workspace, size_t workspace_bytes,
+                  int32_t* status_dev, void* stream);
+
 /* Workspace bytes pa_decode needs for these sizes on the current device
  * (the default partition size depends on the device's SM count); 0 when no
  * sequence can span more than one partition. */
@@ -283,6 +303,18 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* k,
  * num_pairs == 0 or num_layers == 0 is a no-op returning PA_OK.
  * Must be ordered before the reshape_and_cache that writes into dst in the
  * same step (same stream, earlier launch). */
+/* pa_reshape_and_cache for FP8 caches: each element x of k (v) is stored as
+ * the E4M3 code of float32(x) / k_scale (v_scale): IEEE float32 division,
+ * then round to nearest even, saturating at +-448, NaN kept.  k, v are bf16
+ * [num_tokens][n_kv_heads][d_head] as for pa_reshape_and_cache; the caches
+ * are bytes [num_blocks][n_kv_heads][block_size][d_head].  Scales must be
+ * finite and > 0 (PA_ERR_INVALID_ARG). */
+int pa_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* k,
+                             const void* v, const int64_t* slot_mapping,
+                             int num_tokens, int n_kv_heads, int d_head,
+                             int block_size, int num_blocks, float k_scale,
+                             float v_scale, int32_t* status_dev, void* stream);
+
 int pa_copy_blocks(void* const* k_caches, void* const* v_caches,
                    int num_layers, const int32_t* block_pairs, int num_pairs,
                    int n_kv_heads, int d_head, int block_size, int num_blocks,

@@ -45,29 +45,25 @@ _POS_VALUES = _VALUES[_POS]                                            # increas
 def f64_to_e4m3(x):
     """Round each value to the nearest E4M3 value (ties to the even code),
     saturating at +-448; NaN gives the NaN code with the input's sign bit.
-    Input float values (any float dtype); returns uint8 codes."""
+    Input float values (any float dtype); returns uint8 codes.
+
+    For every magnitude a = min(|x|, 448): the neighbours are the largest
+    grid value <= a and the smallest >= a; the nearer wins, and on a tie the
+    one whose code is even."""
     x = np.asarray(x, dtype=np.float64)
-    out = np.empty(x.shape, dtype=np.uint8)
-    flat_x, flat_o = x.reshape(-1), out.reshape(-1)
-    for i, v in enumerate(flat_x):
-        if np.isnan(v):
-            flat_o[i] = NAN_CODE | (0x80 if np.signbit(v) else 0)
-            continue
-        a = min(abs(v), E4M3_MAX)
-        j = int(np.searchsorted(_POS_VALUES, a))          # first value >= a
-        if j < len(_POS_VALUES) and _POS_VALUES[j] == a:
-            code = int(_POS[j])
-        else:
-            lo, hi = j - 1, j                               # a lies strictly between
-            dlo, dhi = a - _POS_VALUES[lo], _POS_VALUES[hi] - a
-            if dlo < dhi:
-                code = int(_POS[lo])
-            elif dhi < dlo:
-                code = int(_POS[hi])
-            else:                                           # tie: the even code
-                code = int(_POS[lo]) if int(_POS[lo]) % 2 == 0 else int(_POS[hi])
-        flat_o[i] = code | (0x80 if np.signbit(v) else 0)
-    return out
+    nan = np.isnan(x)
+    a = np.minimum(np.abs(np.where(nan, 0.0, x)), E4M3_MAX)
+    hi = np.searchsorted(_POS_VALUES, a, side="left")              # first grid value >= a
+    hi = np.minimum(hi, len(_POS_VALUES) - 1)
+    lo = np.where(_POS_VALUES[hi] == a, hi, np.maximum(hi - 1, 0))
+    d_lo = a - _POS_VALUES[lo]
+    d_hi = _POS_VALUES[hi] - a
+    code_lo, code_hi = _POS[lo].astype(np.int64), _POS[hi].astype(np.int64)
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (code_hi % 2 == 0) & (code_lo % 2 != 0))
+    code = np.where(pick_hi, code_hi, code_lo)
+    code = np.where(nan, NAN_CODE, code)
+    sign = np.signbit(x).astype(np.int64) << 7
+    return (code | sign).astype(np.uint8)
 
 
 def quantize(x, scale):

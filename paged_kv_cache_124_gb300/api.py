@@ -68,6 +68,10 @@ _SIGS = {
                            _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
     "pa_decode_static_scratch": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_int, _c_int,
                                           _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
+    "pa_decode_fp8": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_float, _c_float, _c_int,
+                               _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
+    "pa_reshape_and_cache_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                          _c_float, _vp, _vp]),
     "pa_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                             _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp]),
     "pa_lse_merge": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
@@ -240,6 +244,51 @@ def pa_prefill(out, q, k_cache, v_cache, block_tables, query_start, context_lens
                          float(scale), int(n_q_heads), int(n_kv_heads), int(d_head),
                          _opt_dev(status, torch.int32, "status"), _stream(stream))
     return _check(st, "pa_prefill")
+
+
+def pa_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, k_scale, v_scale,
+                  n_q_heads, n_kv_heads, d_head, max_context_len, partition_size=0, workspace=None, status=None,
+                  stream=None):
+    """pa_decode over E4M3 caches (uint8 [num_blocks, Hkv, B, D]) with per-cache scales; see pa.h."""
+    if out.dtype == torch.bfloat16:
+        out_dtype = PA_DTYPE_BF16
+    elif out.dtype == torch.float32:
+        out_dtype = PA_DTYPE_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    num_seqs = q.shape[0]
+    if tuple(q.shape) != (num_seqs, n_q_heads, d_head) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("q/out must be [num_seqs, n_q_heads, d_head]")
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (n_kv_heads, block_size, d_head) or \
+            k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, n_kv_heads, block_size, d_head]")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, torch.uint8, "workspace")
+        ws_bytes = workspace.numel()
+    st = _lib.pa_decode_fp8(_opt_dev(out, out.dtype, "out"), out_dtype, _dev(q, torch.bfloat16, "q"),
+                            _dev(k_cache, torch.uint8, "k_cache"), _dev(v_cache, torch.uint8, "v_cache"),
+                            _dev(block_tables, torch.int32, "block_tables"),
+                            _dev(context_lens, torch.int32, "context_lens"), int(block_size), float(scale),
+                            float(k_scale), float(v_scale), int(n_q_heads), int(n_kv_heads), int(d_head),
+                            int(num_seqs), int(block_tables.shape[1]), int(k_cache.shape[0]), int(max_context_len),
+                            int(partition_size), ws_ptr, ws_bytes, _opt_dev(status, torch.int32, "status"),
+                            _stream(stream))
+    return _check(st, "pa_decode_fp8")
+
+
+def pa_reshape_and_cache_fp8(k_cache, v_cache, k, v, slot_mapping, k_scale, v_scale, status=None, stream=None):
+    """Quantise k[t], v[t] ([T, Hkv, D] bf16) to E4M3 codes in the slots slot_mapping[t] of uint8 caches."""
+    NB, Hkv, B, D = k_cache.shape
+    T = slot_mapping.shape[0]
+    if tuple(k.shape) != (T, Hkv, D) or k.shape != v.shape:
+        raise ValueError("k/v must be [num_tokens, n_kv_heads, d_head]")
+    st = _lib.pa_reshape_and_cache_fp8(_dev(k_cache, torch.uint8, "k_cache"), _dev(v_cache, torch.uint8, "v_cache"),
+                                       _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+                                       _dev(slot_mapping, torch.int64, "slot_mapping"), int(T), int(Hkv), int(D),
+                                       int(B), int(NB), float(k_scale), float(v_scale),
+                                       _opt_dev(status, torch.int32, "status"), _stream(stream))
+    return _check(st, "pa_reshape_and_cache_fp8")
 
 
 PA_STATIC_SCRATCH_BYTES = 16 << 20

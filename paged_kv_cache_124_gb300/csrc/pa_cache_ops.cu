@@ -60,6 +60,58 @@ __global__ void __launch_bounds__(128) reshape_and_cache_kernel(
     }
 }
 
+// Two floats to two E4M3 codes (round to nearest even, saturating to +-448,
+// NaN stays NaN): lo in the low byte, hi in the high byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight bf16 (one uint4) divided by scale (IEEE division) to eight E4M3 codes.
+__device__ __forceinline__ uint2 quant8(uint4 x, float scale) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = pa::bf16x2_to_float2(w[i]);
+        c[i] = e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// FP8 variant of reshape_and_cache: one thread block per token; each thread
+// turns 16 bf16 inputs (two 16-byte loads) into 16 codes (one 16-byte store).
+__global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const uint4* __restrict__ k,
+    const uint4* __restrict__ v, const int64_t* __restrict__ slot_mapping, int n_kv_heads, int chunks_per_row,
+    int block_size, long long num_slots, float k_scale, float v_scale, int32_t* status) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int t = blockIdx.x;
+    const long long slot = slot_mapping[t];
+    if (slot < 0) return;                                   // padding token
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0) pa::set_status(status, PA_DEV_BAD_SLOT);
+        return;
+    }
+    const long long blk = slot / block_size;
+    const int off = (int)(slot - blk * block_size);
+    const int per_token = n_kv_heads * chunks_per_row;       // 16-element chunks of one token's K
+    for (int c = threadIdx.x; c < 2 * per_token; c += blockDim.x) {
+        const bool is_v = c >= per_token;
+        const int cc = is_v ? c - per_token : c;
+        const uint4* src = (is_v ? v : k) + ((size_t)t * per_token + cc) * 2;
+        const uint4 a = src[0], b = src[1];
+        const float sc = is_v ? v_scale : k_scale;
+        const uint2 qa = quant8(a, sc), qb = quant8(b, sc);
+        const int h = cc / chunks_per_row;
+        const int x = cc - h * chunks_per_row;
+        const size_t dst = (((size_t)blk * n_kv_heads + h) * block_size + off) * chunks_per_row + x;
+        (is_v ? v_cache : k_cache)[dst] = make_uint4(qa.x, qa.y, qb.x, qb.y);
+    }
+}
+
 struct LayerPtrs {
     uint4* k[kMaxLayersPerLaunch];
     uint4* v[kMaxLayersPerLaunch];
@@ -169,6 +221,25 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* k, const void
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<const uint4*>(k),
         static_cast<const uint4*>(v), slot_mapping, n_kv_heads, d_head / 8, block_size,
         (long long)num_blocks * block_size, status_dev);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* k, const void* v,
+                             const int64_t* slot_mapping, int num_tokens, int n_kv_heads, int d_head, int block_size,
+                             int num_blocks, float k_scale, float v_scale, int32_t* status_dev, void* stream) {
+    if (num_tokens < 0 || n_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f)) return PA_ERR_INVALID_ARG;
+    if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head)) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_cache || !v_cache || !k || !v || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!pa_host::aligned16(k_cache) || !pa_host::aligned16(v_cache) || !pa_host::aligned16(k) ||
+        !pa_host::aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_MISALIGNED;
+    const cudaError_t e = pa_host::launch_dependent(
+        reshape_and_cache_fp8_kernel, dim3(num_tokens), dim3(128), 0, static_cast<cudaStream_t>(stream),
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<const uint4*>(k),
+        static_cast<const uint4*>(v), slot_mapping, n_kv_heads, d_head / 16, block_size,
+        (long long)num_blocks * block_size, k_scale, v_scale, status_dev);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

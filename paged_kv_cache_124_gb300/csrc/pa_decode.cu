@@ -92,11 +92,15 @@ struct DecodeArgs {
     int num_seqs;
     int partition_size;
     int max_parts;
+    float k_scale;           // FP8 caches: dequantisation scale of K (folded into the score scale)
+    float u_scale;           // factor on the weighted value sums (FP8: V scale / 2^15; else 1)
 };
 
-template <int D>
+// Shared-memory geometry; F8: one-byte (E4M3) cache elements, rows of d_head
+// bytes (d_head 128: one 128-byte box per row).
+template <int D, bool F8 = false>
 struct Geo {
-    static constexpr int kHalves = D / 64;                // 64-column (128-byte) boxes per row
+    static constexpr int kHalves = F8 ? 1 : D / 64;       // 128-byte boxes per row
     static constexpr int kBoxBytes = kTile * 128;         // one swizzled 16 x 128-byte region
     static constexpr int kTileBytes = kHalves * kBoxBytes;   // K or V of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
@@ -172,11 +176,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 // blocks, the next 8 rows from block blk1).  Returns nothing; the stage's
 // barrier expects exactly the bytes issued.  Boxes are always full: rows
 // past the context come along and are masked in the math.
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void issue_tile(uint8_t* stage, uint64_t* bar, const CUtensorMap* mk,
                                            const CUtensorMap* mv, int blk0, int blk1, int off0, int nv, int kvh,
                                            const DecodeArgs& a, uint64_t policy) {
-    using G = Geo<D>;
+    using G = Geo<D, F8>;
     const int B = a.block_size;
     const int box_rows = B < kTile ? B : kTile;
     const int n_rows = (nv + box_rows - 1) / box_rows;          // 1, or 2 for 8-position blocks
@@ -318,6 +322,183 @@ __device__ __forceinline__ void load_q(uint32_t (&qb)[Geo<D>::kSteps][2], const 
     }
 }
 
+// ---------------------------------------------------------------------------
+// FP8 (E4M3) caches.  Codes are turned into f16 in registers (exact: every
+// E4M3 value is an f16) and both products run as f16 MMAs:
+//   * S = K . Q^T: within each 16-wide k-step the d index is permuted so that
+//     a lane reads 4 consecutive codes of a K row with one 32-bit load (k
+//     columns 2t, 2t+1, 2t+8, 2t+9 hold d = 4t .. 4t+3); q's fragments use
+//     the same permutation.  q is converted to f16 after scaling each head
+//     by a power of two that puts its largest element in [2^14, 2^15); the
+//     score scale undoes it, together with the K scale.
+//   * O^T += V^T . P^T: row g of an m-tile holds d = 16m + 2g, row g + 8 holds
+//     d = 16m + 2g + 1, so a lane reads two consecutive codes of four V rows
+//     (16-bit loads) and pairs them by position with a byte permute.  P is
+//     scaled by 2^15 before the f16 split (hi + lo), which keeps weights down
+//     to 2^-39 of the row maximum; the V scale and 2^-15 multiply the final
+//     sums.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four E4M3 codes (bytes 0..3 of x) to two f16x2: bytes 0, 1 -> lo, bytes 2, 3 -> hi.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// q of query heads [qh0, qh0 + hpb) as f16 B fragments in the permuted order
+// (lane holds q[head g][16 k + 4 t4 + 0..3] times the head's power-of-two
+// scale); returns that scale for head g.
+template <int D>
+__device__ __forceinline__ float load_q_f8(uint32_t (&qb)[Geo<D>::kSteps][2], const __nv_bfloat16* qrow0, int hpb,
+                                           int lane) {
+    constexpr int kSteps = Geo<D>::kSteps;
+    const int g = lane >> 2, t4 = lane & 3;
+    const uint2* qrow = reinterpret_cast<const uint2*>(qrow0 + (size_t)(g < hpb ? g : 0) * D);
+    float v[kSteps][4];
+    float mx = 0.f;
+#pragma unroll
+    for (int k = 0; k < kSteps; ++k) {
+        const uint2 w = g < hpb ? qrow[4 * k + t4] : make_uint2(0u, 0u);
+        const float2 f01 = pa::bf16x2_to_float2(w.x), f23 = pa::bf16x2_to_float2(w.y);
+        v[k][0] = f01.x;
+        v[k][1] = f01.y;
+        v[k][2] = f23.x;
+        v[k][3] = f23.y;
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(f01.x), fabsf(f01.y)), fmaxf(fabsf(f23.x), fabsf(f23.y))));
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    int eb = (__float_as_int(mx) >> 23) & 0xff;             // biased exponent of the head's maximum
+    eb = eb < 14 ? 14 : (eb > 254 ? 254 : eb);
+    const float sh = __int_as_float((268 - eb) << 23);      // 2^(141 - eb): maximum into [2^14, 2^15)
+#pragma unroll
+    for (int k = 0; k < kSteps; ++k) {
+        qb[k][0] = pack_f16(v[k][0] * sh, v[k][1] * sh);
+        qb[k][1] = pack_f16(v[k][2] * sh, v[k][3] * sh);
+    }
+    return sh;
+}
+
+// consume_tile for an FP8 stage; c0 / c1: score scale of heads h0 / h1 (the
+// log2-domain softmax scale times the K scale over the heads' q scales).
+template <int D>
+__device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, uint32_t vs, int nv,
+                                                const uint32_t (&qb)[Geo<D>::kSteps][2], float c0, float c1,
+                                                int lane) {
+    constexpr int kSteps = Geo<D>::kSteps;
+    const int g = lane >> 2, t4 = lane & 3;
+
+    float s_a[4] = {0.f, 0.f, 0.f, 0.f}, s_b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kSteps; ++kk) {
+        const uint32_t off = ((uint32_t)(kk ^ g) << 4) + 4 * t4;   // rows g and g + 8 share the swizzle
+        const uint32_t w0 = lds_b32(ks + g * 128 + off);
+        const uint32_t w1 = lds_b32(ks + (g + 8) * 128 + off);
+        uint32_t af[4];
+        e4m3x4_to_f16(w0, af[0], af[2]);
+        e4m3x4_to_f16(w1, af[1], af[3]);
+        if (kk & 1)
+            mma16816_f16(s_b, af, qb[kk][0], qb[kk][1]);
+        else
+            mma16816_f16(s_a, af, qb[kk][0], qb[kk][1]);
+    }
+    float s[4];
+    s[0] = (s_a[0] + s_b[0]) * c0;
+    s[1] = (s_a[1] + s_b[1]) * c1;
+    s[2] = (s_a[2] + s_b[2]) * c0;
+    s[3] = (s_a[3] + s_b[3]) * c1;
+    if (g >= nv) s[0] = s[1] = -INFINITY;
+    if (g + 8 >= nv) s[2] = s[3] = -INFINITY;
+
+    float b0 = fmaxf(s[0], s[2]), b1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int msk = 4; msk <= 16; msk <<= 1) {
+        b0 = fmaxf(b0, __shfl_xor_sync(0xffffffffu, b0, msk));
+        b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, msk));
+    }
+    const float n0 = fmaxf(st.m0, b0), n1 = fmaxf(st.m1, b1);
+    const float al0 = fast_exp2(st.m0 - n0), al1 = fast_exp2(st.m1 - n1);
+    st.m0 = n0;
+    st.m1 = n1;
+    const float p0 = fast_exp2(s[0] - n0), p1 = fast_exp2(s[1] - n1);
+    const float p2 = fast_exp2(s[2] - n0), p3 = fast_exp2(s[3] - n1);
+    st.l0 = st.l0 * al0 + (p0 + p2);
+    st.l1 = st.l1 * al1 + (p1 + p3);
+#pragma unroll
+    for (int m = 0; m < kSteps; ++m) {
+        st.acc[m][0] *= al0;
+        st.acc[m][1] *= al1;
+        st.acc[m][2] *= al0;
+        st.acc[m][3] *= al1;
+    }
+
+    constexpr float kP = 32768.f;                                   // 2^15
+    const float q0 = p0 * kP, q1 = p1 * kP, q2 = p2 * kP, q3 = p3 * kP;
+    const uint32_t h01 = pack_f16(q0, q1), h23 = pack_f16(q2, q3);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    const uint32_t l01 = pack_f16(q0 - f01.x, q1 - f01.y), l23 = pack_f16(q2 - f23.x, q3 - f23.y);
+    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+    const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;      // zero V rows past the context
+    if (nv < kTile) {
+        const int t = 2 * t4;
+        mlo = (t < nv ? 0x0000ffffu : 0u) | (t + 1 < nv ? 0xffff0000u : 0u);
+        mhi = (t + 8 < nv ? 0x0000ffffu : 0u) | (t + 9 < nv ? 0xffff0000u : 0u);
+    }
+    const int r0 = 2 * t4;
+#pragma unroll
+    for (int m = 0; m < kSteps; ++m) {
+        const uint32_t col = 2 * g;
+        const uint32_t L0 = lds_u16(vs + r0 * 128 + ((uint32_t)(m ^ (r0 & 7)) << 4) + col);
+        const uint32_t L1 = lds_u16(vs + (r0 + 1) * 128 + ((uint32_t)(m ^ ((r0 + 1) & 7)) << 4) + col);
+        const uint32_t L2 = lds_u16(vs + (r0 + 8) * 128 + ((uint32_t)(m ^ (r0 & 7)) << 4) + col);
+        const uint32_t L3 = lds_u16(vs + (r0 + 9) * 128 + ((uint32_t)(m ^ ((r0 + 1) & 7)) << 4) + col);
+        uint32_t af[4];
+        e4m3x4_to_f16(prmt(L0, L1, 0x5140u), af[0], af[1]);   // d 16m+2g (rows g) and 16m+2g+1 (rows g+8)
+        e4m3x4_to_f16(prmt(L2, L3, 0x5140u), af[2], af[3]);
+        af[0] &= mlo;
+        af[1] &= mlo;
+        af[2] &= mhi;
+        af[3] &= mhi;
+        mma16816_f16(st.acc[m], af, bh0, bh1);
+        mma16816_f16(st.acc[m], af, bl0, bl1);
+    }
+}
+
 // Every lane waits for the stage itself (visibility of the async copies);
 // the decision to give up is warp-uniform.  On a timeout the status is
 // flagged and the warp's other stages are given a short bounded wait.
@@ -333,11 +514,11 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bars, int k, int lane, int3
 // ============================================================================
 // Fixed partitions: one thread block per (sequence, head group, partition)
 // ============================================================================
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                             const DecodeArgs a) {
-    using G = Geo<D>;
+    using G = Geo<D, F8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + G::kRingBytes);
@@ -366,7 +547,16 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
     for (int i = threadIdx.x; i < n_spec; i += kThreads) table[i] = trow[lb0 + i];
     const size_t row0 = ((size_t)seq * a.n_q_heads + qh0) * D;   // q / out offset of the block's first head
     uint32_t qb[G::kSteps][2];
-    load_q<D>(qb, a.q + row0, hpb, lane);
+    float c0 = 0.f, c1 = 0.f;
+    if constexpr (F8) {
+        const float sh = load_q_f8<D>(qb, a.q + row0, hpb, lane);
+        const int h0_ = 2 * (lane & 3);
+        const float sc = a.scale_log2 * a.k_scale;
+        c0 = sc / __shfl_sync(0xffffffffu, sh, 4 * h0_);
+        c1 = sc / __shfl_sync(0xffffffffu, sh, 4 * h0_ + 4);
+    } else {
+        load_q<D>(qb, a.q + row0, hpb, lane);
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWarps * kStages; ++i) pa::mbar_init(&bars[i], 1);
         pa::fence_mbar_init();
@@ -398,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
         const int nv = min(kTile, t_end - t0);
         const int e0 = (t0 >> a.log2_block) - lb0;
         const int blk1 = (B < kTile && nv > B) ? table[e0 + 1] : 0;
-        issue_tile<D>(wring + stage * G::kStageBytes, &wbars[stage], &tmap_k, &tmap_v, table[e0], blk1,
-                      t0 & (B - 1), nv, kvh, a, policy);
+        issue_tile<D, F8>(wring + stage * G::kStageBytes, &wbars[stage], &tmap_k, &tmap_v, table[e0], blk1,
+                          t0 & (B - 1), nv, kvh, a, policy);
     };
 
     WarpState<D> st;
@@ -415,8 +605,11 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
     for (int tile = warp; tile < n_tiles; tile += kWarps, ++k) {
         if (!wait_stage(wbars, k, lane, a.status)) break;
         const uint32_t ks = pa::smem_addr(wring + (k % kStages) * G::kStageBytes);
-        consume_tile<D>(st, ks, ks + G::kTileBytes, min(kTile, t_end - (t_begin + tile * kTile)), qb, a.scale_log2,
-                        lane);
+        const int nv_ = min(kTile, t_end - (t_begin + tile * kTile));
+        if constexpr (F8)
+            consume_tile_f8<D>(st, ks, ks + G::kTileBytes, nv_, qb, c0, c1, lane);
+        else
+            consume_tile<D>(st, ks, ks + G::kTileBytes, nv_, qb, a.scale_log2, lane);
         __syncwarp();
         if (lane == 0 && tile + kWarps * kStages < n_tiles) issue(tile + kWarps * kStages, k % kStages);
     }
@@ -434,14 +627,18 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
         lw[warp * kHeads + h0] = st.l0;
         lw[warp * kHeads + h0 + 1] = st.l1;
     }
+    // rows g and g + 8 of m-tile m are d = 16 m + g and 16 m + g + 8 (FP8:
+    // 16 m + 2 g and 16 m + 2 g + 1)
+    constexpr int kRow2 = F8 ? 1 : 8;
+    const int drow = F8 ? 2 * g : g;
 #pragma unroll
     for (int m = 0; m < G::kSteps; ++m) {
-        float* u0 = uw + (warp * kHeads + h0) * D + 16 * m + g;
+        float* u0 = uw + (warp * kHeads + h0) * D + 16 * m + drow;
         float* u1 = u0 + D;
         u0[0] = st.acc[m][0];
         u1[0] = st.acc[m][1];
-        u0[8] = st.acc[m][2];
-        u1[8] = st.acc[m][3];
+        u0[kRow2] = st.acc[m][2];
+        u1[kRow2] = st.acc[m][3];
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < hpb * D; idx += kThreads) {
@@ -458,10 +655,10 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
             U += f * uw[(w * kHeads + h) * D + d];
         }
         if (nparts == 1) {
-            store_out(a.out, a.out_f32, row0 + idx, U / Z);
+            store_out(a.out, a.out_f32, row0 + idx, U * a.u_scale / Z);
         } else {
             const size_t pi = ((size_t)seq * a.n_q_heads + qh0 + h) * a.max_parts + part;
-            a.part_acc[pi * D + d] = U;
+            a.part_acc[pi * D + d] = U * a.u_scale;
             if (d == 0) {
                 a.part_max[pi] = M * kLn2;      // back to natural-log units
                 a.part_sum[pi] = Z;
@@ -591,6 +788,20 @@ bool make_cache_map(CUtensorMap* map, const void* base, long long rows, int d_he
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same view of an FP8 cache [rows][d_head] bytes (d_head 128): boxes of
+// 128 columns x box_rows rows, 128-byte swizzle.
+bool make_cache_map_f8(CUtensorMap* map, const void* base, long long rows, int d_head, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)d_head, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)d_head};
+    const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -642,8 +853,8 @@ int launch(K kernel, dim3 grid, int smem, cudaStream_t st, const CUtensorMap& mk
 }
 
 int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, void* workspace,
-        size_t workspace_bytes, cudaStream_t st) {
-    static int attr128[64] = {0}, attr64[64] = {0};
+        size_t workspace_bytes, cudaStream_t st, bool f8 = false) {
+    static int attr128[64] = {0}, attr64[64] = {0}, attr128f8[64] = {0};
     const int P = a.partition_size;
     a.max_parts = (a.ctx_cap + P - 1) / P;
     if (a.max_parts < 1) a.max_parts = 1;
@@ -657,10 +868,13 @@ int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, 
         a.part_acc = reinterpret_cast<float*>(w + 2 * align256(4 * n));
     }
     const int table_ints = P / a.block_size + 2;
-    const int smem = 1024 + kWarps * kStages * 2 * kTile * d_head * 2 + kWarps * kStages * 8 + table_ints * 4;
+    const int ring = f8 ? Geo<128, true>::kRingBytes : kWarps * kStages * 2 * kTile * d_head * 2;
+    const int merge = kWarps * kHeads * (2 + d_head) * 4;          // the warp merge reuses the ring
+    const int smem = 1024 + (ring > merge ? ring : merge) + kWarps * kStages * 8 + table_ints * 4;
     dim3 grid(a.max_parts, a.n_kv_heads * a.n_sub, a.num_seqs);
-    const int rc = d_head == 128 ? launch(decode_partition_kernel<128>, grid, smem, st, mk, mv, a, attr128)
-                                 : launch(decode_partition_kernel<64>, grid, smem, st, mk, mv, a, attr64);
+    const int rc = f8 ? launch(decode_partition_kernel<128, true>, grid, smem, st, mk, mv, a, attr128f8)
+                      : d_head == 128 ? launch(decode_partition_kernel<128, false>, grid, smem, st, mk, mv, a, attr128)
+                                      : launch(decode_partition_kernel<64, false>, grid, smem, st, mk, mv, a, attr64);
     if (rc != PA_OK || a.max_parts <= 1) return rc;
     return launch_merge(true, st, a.out, a.out_f32, a.part_max, a.part_sum, a.part_acc, a.context_lens, a.ctx_cap, P,
                         a.max_parts, a.n_q_heads, a.num_seqs, d_head, 1);
@@ -677,14 +891,22 @@ size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int d_head, int max
     return workspace_bytes_for(num_seqs, n_q_heads, d_head, (max_context_len + P - 1) / P);
 }
 
-int pa_decode(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
-              const int32_t* block_tables, const int32_t* context_lens, int block_size, float scale,
-              int n_q_heads, int n_kv_heads, int d_head, int num_seqs, int max_blocks_per_seq,
-              int num_blocks, int max_context_len, int partition_size, void* workspace,
-              size_t workspace_bytes, int32_t* status_dev, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// pa_decode and pa_decode_fp8 (f8: E4M3 caches with scales k_scale, v_scale).
+int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+                const int32_t* block_tables, const int32_t* context_lens, int block_size, float scale,
+                int n_q_heads, int n_kv_heads, int d_head, int num_seqs, int max_blocks_per_seq, int num_blocks,
+                int max_context_len, int partition_size, void* workspace, size_t workspace_bytes,
+                int32_t* status_dev, void* stream, bool f8, float k_scale, float v_scale) {
     if (num_seqs < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
         num_blocks <= 0 || max_context_len < 0 || !(scale == scale))
         return PA_ERR_INVALID_ARG;
+    if (f8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !(k_scale < INFINITY) || !(v_scale < INFINITY)))
+        return PA_ERR_INVALID_ARG;
+    if (f8 && d_head != 128) return PA_ERR_UNSUPPORTED;
     if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
@@ -726,14 +948,42 @@ int pa_decode(void* out, int out_dtype, const void* q, const void* k_cache, cons
     a.ctx_cap = (int)(cap_tbl < max_context_len ? cap_tbl : max_context_len);
     a.num_seqs = num_seqs;
     a.partition_size = partition_size > 0 ? partition_size : default_partition(num_seqs, n_q_heads, max_context_len);
+    a.k_scale = f8 ? k_scale : 1.f;
+    a.u_scale = f8 ? v_scale / 32768.f : 1.f;
 
     const int box_rows = block_size < kTile ? block_size : kTile;
     CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, k_cache, cache_rows, d_head, box_rows) ||
-        !make_cache_map(&mv, v_cache, cache_rows, d_head, box_rows))
-        return PA_ERR_CUDA;
+    const bool maps_ok = f8 ? make_cache_map_f8(&mk, k_cache, cache_rows, d_head, box_rows) &&
+                                  make_cache_map_f8(&mv, v_cache, cache_rows, d_head, box_rows)
+                            : make_cache_map(&mk, k_cache, cache_rows, d_head, box_rows) &&
+                                  make_cache_map(&mv, v_cache, cache_rows, d_head, box_rows);
+    if (!maps_ok) return PA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return run(a, mk, mv, d_head, workspace, workspace_bytes, st);
+    return run(a, mk, mv, d_head, workspace, workspace_bytes, st, f8);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, int block_size, float scale,
+              int n_q_heads, int n_kv_heads, int d_head, int num_seqs, int max_blocks_per_seq,
+              int num_blocks, int max_context_len, int partition_size, void* workspace,
+              size_t workspace_bytes, int32_t* status_dev, void* stream) {
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, n_q_heads,
+                       n_kv_heads, d_head, num_seqs, max_blocks_per_seq, num_blocks, max_context_len, partition_size,
+                       workspace, workspace_bytes, status_dev, stream, false, 1.f, 1.f);
+}
+
+int pa_decode_fp8(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, int block_size, float scale,
+                  float k_scale, float v_scale, int n_q_heads, int n_kv_heads, int d_head, int num_seqs,
+                  int max_blocks_per_seq, int num_blocks, int max_context_len, int partition_size, void* workspace,
+                  size_t workspace_bytes, int32_t* status_dev, void* stream) {
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, n_q_heads,
+                       n_kv_heads, d_head, num_seqs, max_blocks_per_seq, num_blocks, max_context_len, partition_size,
+                       workspace, workspace_bytes, status_dev, stream, true, k_scale, v_scale);
 }
 
 int pa_lse_merge(void* out, int out_dtype, const float* part_max, const float* part_sum, const float* part_acc,
