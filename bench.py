@@ -108,19 +108,20 @@ def replica_seed(base_seed, rank):
 # byte accounting
 # ----------------------------------------------------------------------------
 
-def algorithmic_bytes(sc, ctx, n_new_tokens):
+def algorithmic_bytes(sc, ctx, n_new_tokens, kv_bytes=2):
     """Bytes one step must move at minimum: decode reads each cached K and V
     row of each KV head once, q, the block-table entries in use and the
     context lengths, and writes out; reshape_and_cache reads and writes each
-    new token's K and V rows."""
+    new token's K and V rows.  kv_bytes: bytes per cached element (2 for
+    bf16, 1 for FP8)."""
     ctx = np.asarray(ctx, dtype=np.int64)
     row = sc.d_head * 2
-    kv = int(ctx.sum()) * sc.n_kv_heads * row * 2
+    kv = int(ctx.sum()) * sc.n_kv_heads * sc.d_head * kv_bytes * 2
     S = len(ctx)
     qo = 2 * S * sc.n_q_heads * row
     tables = int((-(-ctx // sc.block_size)).sum()) * 4 + S * 4
     decode = kv + qo + tables
-    cache_write = 2 * n_new_tokens * sc.n_kv_heads * row * 2
+    cache_write = 2 * n_new_tokens * sc.n_kv_heads * (row + sc.d_head * kv_bytes)
     return decode, cache_write
 
 
@@ -246,16 +247,37 @@ def run_ours(args, world, rank, local):
     P = args.partition
     ws = api.decode_workspace(S, sc.n_q_heads, sc.d_head, max_ctx, P, device=dev)
     kc, vc = run.k_caches[0], run.v_caches[0]
+    fp8 = args.kv_dtype == "fp8"
+    if fp8:
+        # the same cache as E4M3 codes, scales from the data's range (setup, not timed)
+        k_scale = float(kc.float().nan_to_num(0.0).abs().amax()) / 448.0
+        v_scale = float(vc.float().nan_to_num(0.0).abs().amax()) / 448.0
+        kc = (kc.float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+        vc = (vc.float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
     stream = torch.cuda.current_stream(dev)
-    dec_bytes, write_bytes = algorithmic_bytes(sc, ctx_h, S)
+    dec_bytes, write_bytes = algorithmic_bytes(sc, ctx_h, S, 1 if fp8 else 2)
     # our kernels per step: reshape_and_cache, the partition kernel and, when a
     # sequence can span several partitions, the merge kernel
     launches_per_step = 2 + (1 if api.pa_decode_workspace_size(S, sc.n_q_heads, sc.d_head, max_ctx, P) else 0)
 
+    def cache_write(k_, v_, slots_, st_):
+        if fp8:
+            api.pa_reshape_and_cache_fp8(kc, vc, k_, v_, slots_, k_scale, v_scale, stream=st_)
+        else:
+            api.pa_reshape_and_cache(kc, vc, k_, v_, slots_, stream=st_)
+
+    def decode_call(q_, tables_, ctx_, st_):
+        if fp8:
+            api.pa_decode_fp8(out, q_, kc, vc, tables_, ctx_, sc.block_size, sc.scale, k_scale, v_scale,
+                              sc.n_q_heads, sc.n_kv_heads, sc.d_head, max_ctx, partition_size=P, workspace=ws,
+                              stream=st_)
+        else:
+            api.pa_decode(out, q_, kc, vc, tables_, ctx_, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
+                          sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=st_)
+
     def step():
-        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
-        api.pa_decode(out, q, kc, vc, tables, ctx, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
-                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=stream)
+        cache_write(k_new, v_new, slots, stream)
+        decode_call(q, tables, ctx, stream)
 
     clocks = ClockSampler(local) if rank == 0 else None
     if clocks:
@@ -273,14 +295,13 @@ def run_ours(args, world, rank, local):
               for _ in range((K + SAMPLE - 1) // SAMPLE)]
 
     def decode(q_, tables_, ctx_):
-        api.pa_decode(out, q_, kc, vc, tables_, ctx_, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
-                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=stream)
+        decode_call(q_, tables_, ctx_, stream)
 
     barrier(world)
     torch.cuda.synchronize(dev)
     ev_start.record(stream)
     for i in range(K):
-        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
+        cache_write(k_new, v_new, slots, stream)
         if i % SAMPLE == 0:
             a, b = ev_dec[i // SAMPLE]
             a.record(stream)
@@ -317,9 +338,8 @@ def run_ours(args, world, rank, local):
         for dst, src in ((q_d, q_h), (k_d, k_h), (v_d, v_h), (slots_d, slots_hp), (tables_d, tables_h),
                          (ctx_d, ctx_hp)):
             dst.copy_(src, non_blocking=True)
-        api.pa_reshape_and_cache(kc, vc, k_d, v_d, slots_d, stream=st)
-        api.pa_decode(out, q_d, kc, vc, tables_d, ctx_d, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
-                      sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=st)
+        cache_write(k_d, v_d, slots_d, st)
+        decode_call(q_d, tables_d, ctx_d, st)
         out_h.copy_(out, non_blocking=True)
 
     def eager_step():
@@ -359,7 +379,8 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "fp8_e4m3" if fp8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": sc.name, "num_seqs": S, "context_lens": "uniform [512, 4096]" if
                    args.workload == "batch64_8b" else "see workload", "total_context": int(ctx_h.sum()),
                    "n_q_heads": sc.n_q_heads, "n_kv_heads": sc.n_kv_heads, "d_head": sc.d_head,
@@ -369,9 +390,10 @@ def run_ours(args, world, rank, local):
                          (dec_bytes / 1e6),
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "single GPU"},
         "seqs_per_s": round(total_seqs / total_s, 1),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (decode_partition_kernel + lse_merge_kernel)",
+        "roofline": {"bound": "hbm", "kernel": "pa_decode%s (decode_partition_kernel + lse_merge_kernel)" %
+                     ("_fp8" if fp8 else ""),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "frac": round(achieved / peak, 4), "traffic": None if fp8 else profiled_traffic(),
                      "algorithmic_bytes_per_launch": int(dec_bytes),
                      "avg_launch_us": round(dec_s_avg * 1e6, 2)},
         "e2e": {"value": round(e2e_bytes / e2e_total_s / 1e9, 2), "unit": UNIT,
@@ -445,7 +467,7 @@ def run_prefill_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     ev_start.record(stream)
     for i in range(K):
-        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
+        cache_write(k_new, v_new, slots, stream)
         if i % SAMPLE == 0:
             a, b = ev_att[i // SAMPLE]
             a.record(stream)
@@ -850,6 +872,8 @@ def main(argv=None):
     p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(PREFILL_WORKLOADS) + ["swap_8b"],
                    default="batch64_8b")
     p.add_argument("--block-size", type=int, default=16)
+    p.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                   help="cache element type of the decode workloads (fp8: E4M3 with per-cache scales)")
     p.add_argument("--partition", type=int, default=0, help="positions per partition (0 = library default)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")

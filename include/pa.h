@@ -134,7 +134,8 @@ const char* pa_status_string(int status);
  * result is the attention over those dequantised keys and values, computed
  * as pa_decode computes it (fp32 softmax and accumulation; f16 operands,
  * which hold every E4M3 value exactly; q is rounded to f16 after a per-head
- * power-of-two scaling, P is split into two f16 terms).  Same arguments and
+ * power-of-two scaling, the softmax weights to f16 after a 2^15 scaling, a
+ * relative error of at most 2^-12).  Same arguments and
  * workspace as pa_decode, plus the two scales (finite, > 0).  d_head must be
  * 128 (PA_ERR_UNSUPPORTED otherwise). */
 int pa_decode_fp8(void* out, int out_dtype, const void* q,

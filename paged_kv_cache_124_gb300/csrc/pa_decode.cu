@@ -324,19 +324,25 @@ __device__ __forceinline__ void load_q(uint32_t (&qb)[Geo<D>::kSteps][2], const 
 
 // ---------------------------------------------------------------------------
 // FP8 (E4M3) caches.  Codes are turned into f16 in registers (exact: every
-// E4M3 value is an f16) and both products run as f16 MMAs:
-//   * S = K . Q^T: within each 16-wide k-step the d index is permuted so that
-//     a lane reads 4 consecutive codes of a K row with one 32-bit load (k
-//     columns 2t, 2t+1, 2t+8, 2t+9 hold d = 4t .. 4t+3); q's fragments use
-//     the same permutation.  q is converted to f16 after scaling each head
-//     by a power of two that puts its largest element in [2^14, 2^15); the
-//     score scale undoes it, together with the K scale.
-//   * O^T += V^T . P^T: row g of an m-tile holds d = 16m + 2g, row g + 8 holds
-//     d = 16m + 2g + 1, so a lane reads two consecutive codes of four V rows
-//     (16-bit loads) and pairs them by position with a byte permute.  P is
-//     scaled by 2^15 before the f16 split (hi + lo), which keeps weights down
-//     to 2^-39 of the row maximum; the V scale and 2^-15 multiply the final
-//     sums.
+// E4M3 value is an f16) and both products run as f16 MMAs.  The contraction
+// index of each product may be permuted freely as long as both operands use
+// the same order, and the output rows of O^T may be permuted if the final
+// write undoes it; both are used so that every shared-memory load returns
+// bytes that go straight into fragments:
+//   * S = K . Q^T, two k-steps (32 d) at a time: lane t4 reads 8 consecutive
+//     codes of K rows g and g + 8 (one 64-bit load each); k columns 2t4,
+//     2t4+1, 2t4+8, 2t4+9 of the first step hold d = 8t4 .. 8t4+3, those of
+//     the second d = 8t4+4 .. 8t4+7 (plus 32 per pair of steps).  q's
+//     fragments use the same order and are converted to f16 after scaling
+//     each head by a power of two that puts its largest element in
+//     [2^14, 2^15); the score scale undoes it, together with the K scale.
+//   * O^T += V^T . P^T, two m-tiles (32 d) at a time: lane g reads 4
+//     consecutive codes (d = 32j + 4g .. +3) of V rows (positions) 2t4,
+//     2t4+1, 2t4+8, 2t4+9 and pairs them by position with byte permutes; row
+//     g / g+8 of m-tile 2j hold d = 32j+4g / +1, of m-tile 2j+1 d = 32j+4g+2
+//     / +3.  P is scaled by 2^15 before it is rounded to f16 (11-bit
+//     significand, weights kept down to 2^-39 of the row maximum); the V
+//     scale and 2^-15 multiply the final sums.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -365,9 +371,9 @@ __device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
-    uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ uint2 lds_b64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
     return v;
 }
 
@@ -378,25 +384,27 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 
 // q of query heads [qh0, qh0 + hpb) as f16 B fragments in the permuted order
-// (lane holds q[head g][16 k + 4 t4 + 0..3] times the head's power-of-two
-// scale); returns that scale for head g.
+// (for the step pair j, lane holds q[head g][32 j + 8 t4 + 0..7] times the
+// head's power-of-two scale); returns that scale for head g.
 template <int D>
 __device__ __forceinline__ float load_q_f8(uint32_t (&qb)[Geo<D>::kSteps][2], const __nv_bfloat16* qrow0, int hpb,
                                            int lane) {
     constexpr int kSteps = Geo<D>::kSteps;
     const int g = lane >> 2, t4 = lane & 3;
-    const uint2* qrow = reinterpret_cast<const uint2*>(qrow0 + (size_t)(g < hpb ? g : 0) * D);
+    const uint4* qrow = reinterpret_cast<const uint4*>(qrow0 + (size_t)(g < hpb ? g : 0) * D);
     float v[kSteps][4];
     float mx = 0.f;
 #pragma unroll
-    for (int k = 0; k < kSteps; ++k) {
-        const uint2 w = g < hpb ? qrow[4 * k + t4] : make_uint2(0u, 0u);
-        const float2 f01 = pa::bf16x2_to_float2(w.x), f23 = pa::bf16x2_to_float2(w.y);
-        v[k][0] = f01.x;
-        v[k][1] = f01.y;
-        v[k][2] = f23.x;
-        v[k][3] = f23.y;
-        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(f01.x), fabsf(f01.y)), fmaxf(fabsf(f23.x), fabsf(f23.y))));
+    for (int j = 0; j < kSteps / 2; ++j) {
+        const uint4 w = g < hpb ? qrow[4 * j + t4] : make_uint4(0u, 0u, 0u, 0u);   // d = 32 j + 8 t4 .. +7
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = pa::bf16x2_to_float2(ww[i]);
+            v[2 * j + (i >> 1)][2 * (i & 1)] = f.x;
+            v[2 * j + (i >> 1)][2 * (i & 1) + 1] = f.y;
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -422,17 +430,18 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
 
     float s_a[4] = {0.f, 0.f, 0.f, 0.f}, s_b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int kk = 0; kk < kSteps; ++kk) {
-        const uint32_t off = ((uint32_t)(kk ^ g) << 4) + 4 * t4;   // rows g and g + 8 share the swizzle
-        const uint32_t w0 = lds_b32(ks + g * 128 + off);
-        const uint32_t w1 = lds_b32(ks + (g + 8) * 128 + off);
+    for (int j = 0; j < kSteps / 2; ++j) {
+        // 8 codes at d = 32 j + 8 t4: chunk 2 j + t4 / 2, byte 8 (t4 & 1); rows g and g + 8 share the swizzle
+        const uint32_t off = ((uint32_t)((2 * j + (t4 >> 1)) ^ g) << 4) + 8 * (t4 & 1);
+        const uint2 w0 = lds_b64(ks + g * 128 + off);
+        const uint2 w1 = lds_b64(ks + (g + 8) * 128 + off);
         uint32_t af[4];
-        e4m3x4_to_f16(w0, af[0], af[2]);
-        e4m3x4_to_f16(w1, af[1], af[3]);
-        if (kk & 1)
-            mma16816_f16(s_b, af, qb[kk][0], qb[kk][1]);
-        else
-            mma16816_f16(s_a, af, qb[kk][0], qb[kk][1]);
+        e4m3x4_to_f16(w0.x, af[0], af[2]);
+        e4m3x4_to_f16(w1.x, af[1], af[3]);
+        mma16816_f16(s_a, af, qb[2 * j][0], qb[2 * j][1]);
+        e4m3x4_to_f16(w0.y, af[0], af[2]);
+        e4m3x4_to_f16(w1.y, af[1], af[3]);
+        mma16816_f16(s_b, af, qb[2 * j + 1][0], qb[2 * j + 1][1]);
     }
     float s[4];
     s[0] = (s_a[0] + s_b[0]) * c0;
@@ -449,29 +458,29 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
         b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, msk));
     }
     const float n0 = fmaxf(st.m0, b0), n1 = fmaxf(st.m1, b1);
-    const float al0 = fast_exp2(st.m0 - n0), al1 = fast_exp2(st.m1 - n1);
-    st.m0 = n0;
-    st.m1 = n1;
+    // rescale only when some head's maximum grew (rare after the first tiles)
+    if (__any_sync(0xffffffffu, n0 != st.m0 || n1 != st.m1)) {
+        const float al0 = fast_exp2(st.m0 - n0), al1 = fast_exp2(st.m1 - n1);
+        st.l0 *= al0;
+        st.l1 *= al1;
+#pragma unroll
+        for (int m = 0; m < kSteps; ++m) {
+            st.acc[m][0] *= al0;
+            st.acc[m][1] *= al1;
+            st.acc[m][2] *= al0;
+            st.acc[m][3] *= al1;
+        }
+        st.m0 = n0;
+        st.m1 = n1;
+    }
     const float p0 = fast_exp2(s[0] - n0), p1 = fast_exp2(s[1] - n1);
     const float p2 = fast_exp2(s[2] - n0), p3 = fast_exp2(s[3] - n1);
-    st.l0 = st.l0 * al0 + (p0 + p2);
-    st.l1 = st.l1 * al1 + (p1 + p3);
-#pragma unroll
-    for (int m = 0; m < kSteps; ++m) {
-        st.acc[m][0] *= al0;
-        st.acc[m][1] *= al1;
-        st.acc[m][2] *= al0;
-        st.acc[m][3] *= al1;
-    }
+    st.l0 += p0 + p2;
+    st.l1 += p1 + p3;
 
     constexpr float kP = 32768.f;                                   // 2^15
-    const float q0 = p0 * kP, q1 = p1 * kP, q2 = p2 * kP, q3 = p3 * kP;
-    const uint32_t h01 = pack_f16(q0, q1), h23 = pack_f16(q2, q3);
-    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-    const uint32_t l01 = pack_f16(q0 - f01.x, q1 - f01.y), l23 = pack_f16(q2 - f23.x, q3 - f23.y);
-    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-    const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+    const uint32_t bh0 = movmatrix_trans(pack_f16(p0 * kP, p1 * kP));
+    const uint32_t bh1 = movmatrix_trans(pack_f16(p2 * kP, p3 * kP));
 
     uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;      // zero V rows past the context
     if (nv < kTile) {
@@ -481,21 +490,30 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
     }
     const int r0 = 2 * t4;
 #pragma unroll
-    for (int m = 0; m < kSteps; ++m) {
-        const uint32_t col = 2 * g;
-        const uint32_t L0 = lds_u16(vs + r0 * 128 + ((uint32_t)(m ^ (r0 & 7)) << 4) + col);
-        const uint32_t L1 = lds_u16(vs + (r0 + 1) * 128 + ((uint32_t)(m ^ ((r0 + 1) & 7)) << 4) + col);
-        const uint32_t L2 = lds_u16(vs + (r0 + 8) * 128 + ((uint32_t)(m ^ (r0 & 7)) << 4) + col);
-        const uint32_t L3 = lds_u16(vs + (r0 + 9) * 128 + ((uint32_t)(m ^ ((r0 + 1) & 7)) << 4) + col);
+    for (int j = 0; j < kSteps / 2; ++j) {
+        // 4 codes at d = 32 j + 4 g: chunk 2 j + g / 4, byte 4 (g & 3)
+        const int ch = 2 * j + (g >> 2);
+        const uint32_t col = 4 * (g & 3);
+        const uint32_t L0 = lds_b32(vs + r0 * 128 + ((uint32_t)(ch ^ (r0 & 7)) << 4) + col);
+        const uint32_t L1 = lds_b32(vs + (r0 + 1) * 128 + ((uint32_t)(ch ^ ((r0 + 1) & 7)) << 4) + col);
+        const uint32_t L2 = lds_b32(vs + (r0 + 8) * 128 + ((uint32_t)(ch ^ (r0 & 7)) << 4) + col);
+        const uint32_t L3 = lds_b32(vs + (r0 + 9) * 128 + ((uint32_t)(ch ^ ((r0 + 1) & 7)) << 4) + col);
         uint32_t af[4];
-        e4m3x4_to_f16(prmt(L0, L1, 0x5140u), af[0], af[1]);   // d 16m+2g (rows g) and 16m+2g+1 (rows g+8)
+        // m-tile 2j: d 32j+4g (rows g) and +1 (rows g+8); m-tile 2j+1: d +2 and +3
+        e4m3x4_to_f16(prmt(L0, L1, 0x5140u), af[0], af[1]);
         e4m3x4_to_f16(prmt(L2, L3, 0x5140u), af[2], af[3]);
         af[0] &= mlo;
         af[1] &= mlo;
         af[2] &= mhi;
         af[3] &= mhi;
-        mma16816_f16(st.acc[m], af, bh0, bh1);
-        mma16816_f16(st.acc[m], af, bl0, bl1);
+        mma16816_f16(st.acc[2 * j], af, bh0, bh1);
+        e4m3x4_to_f16(prmt(L0, L1, 0x7362u), af[0], af[1]);
+        e4m3x4_to_f16(prmt(L2, L3, 0x7362u), af[2], af[3]);
+        af[0] &= mlo;
+        af[1] &= mlo;
+        af[2] &= mhi;
+        af[3] &= mhi;
+        mma16816_f16(st.acc[2 * j + 1], af, bh0, bh1);
     }
 }
 
@@ -628,12 +646,12 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
         lw[warp * kHeads + h0 + 1] = st.l1;
     }
     // rows g and g + 8 of m-tile m are d = 16 m + g and 16 m + g + 8 (FP8:
-    // 16 m + 2 g and 16 m + 2 g + 1)
+    // 32 (m / 2) + 4 g + 2 (m % 2) and one more)
     constexpr int kRow2 = F8 ? 1 : 8;
-    const int drow = F8 ? 2 * g : g;
 #pragma unroll
     for (int m = 0; m < G::kSteps; ++m) {
-        float* u0 = uw + (warp * kHeads + h0) * D + 16 * m + drow;
+        const int drow = F8 ? 32 * (m >> 1) + 4 * g + 2 * (m & 1) : 16 * m + g;
+        float* u0 = uw + (warp * kHeads + h0) * D + drow;
         float* u1 = u0 + D;
         u0[0] = st.acc[m][0];
         u1[0] = st.acc[m][1];
