@@ -265,20 +265,25 @@ __device__ __forceinline__ void consume_tile(WarpState<D>& st, uint32_t ks, uint
         b1 = fmaxf(b1, __shfl_xor_sync(0xffffffffu, b1, msk));
     }
     const float n0 = fmaxf(st.m0, b0), n1 = fmaxf(st.m1, b1);
-    const float al0 = fast_exp2(st.m0 - n0), al1 = fast_exp2(st.m1 - n1);
-    st.m0 = n0;
-    st.m1 = n1;
+    // rescale only when some head's maximum grew (rare after the first tiles)
+    if (__any_sync(0xffffffffu, n0 != st.m0 || n1 != st.m1)) {
+        const float al0 = fast_exp2(st.m0 - n0), al1 = fast_exp2(st.m1 - n1);
+        st.l0 *= al0;
+        st.l1 *= al1;
+#pragma unroll
+        for (int m = 0; m < G::kSteps; ++m) {
+            st.acc[m][0] *= al0;
+            st.acc[m][1] *= al1;
+            st.acc[m][2] *= al0;
+            st.acc[m][3] *= al1;
+        }
+        st.m0 = n0;
+        st.m1 = n1;
+    }
     const float p0 = fast_exp2(s[0] - n0), p1 = fast_exp2(s[1] - n1);
     const float p2 = fast_exp2(s[2] - n0), p3 = fast_exp2(s[3] - n1);
-    st.l0 = st.l0 * al0 + (p0 + p2);
-    st.l1 = st.l1 * al1 + (p1 + p3);
-#pragma unroll
-    for (int m = 0; m < G::kSteps; ++m) {
-        st.acc[m][0] *= al0;
-        st.acc[m][1] *= al1;
-        st.acc[m][2] *= al0;
-        st.acc[m][3] *= al1;
-    }
+    st.l0 += p0 + p2;
+    st.l1 += p1 + p3;
 
     // ---- P^T as the B operand, split into bf16 hi + lo -------------------------
     const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
