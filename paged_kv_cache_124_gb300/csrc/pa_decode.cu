@@ -332,22 +332,23 @@ __device__ __forceinline__ void load_q(uint32_t (&qb)[Geo<D>::kSteps][2], const 
 // E4M3 value is an f16) and both products run as f16 MMAs.  The contraction
 // index of each product may be permuted freely as long as both operands use
 // the same order, and the output rows of O^T may be permuted if the final
-// write undoes it; both are used so that every shared-memory load returns
+// write undoes it; both are used so that ldmatrix, reading 8 x 16-byte
+// matrices from the swizzled tiles without bank conflicts, hands every lane
 // bytes that go straight into fragments:
-//   * S = K . Q^T, two k-steps (32 d) at a time: lane t4 reads 8 consecutive
-//     codes of K rows g and g + 8 (one 64-bit load each); k columns 2t4,
-//     2t4+1, 2t4+8, 2t4+9 of the first step hold d = 8t4 .. 8t4+3, those of
-//     the second d = 8t4+4 .. 8t4+7 (plus 32 per pair of steps).  q's
-//     fragments use the same order and are converted to f16 after scaling
-//     each head by a power of two that puts its largest element in
-//     [2^14, 2^15); the score scale undoes it, together with the K scale.
-//   * O^T += V^T . P^T, two m-tiles (32 d) at a time: lane g reads 4
-//     consecutive codes (d = 32j + 4g .. +3) of V rows (positions) 2t4,
-//     2t4+1, 2t4+8, 2t4+9 and pairs them by position with byte permutes; row
-//     g / g+8 of m-tile 2j hold d = 32j+4g / +1, of m-tile 2j+1 d = 32j+4g+2
-//     / +3.  P is scaled by 2^15 before it is rounded to f16 (11-bit
-//     significand, weights kept down to 2^-39 of the row maximum); the V
-//     scale and 2^-15 multiply the final sums.
+//   * S = K . Q^T: an ldmatrix row segment is 16 codes of one position; lane
+//     (g, t4) receives codes 4 t4 .. 4 t4 + 3, so k columns 2t4, 2t4+1,
+//     2t4+8, 2t4+9 of a 16-wide k-step hold d = 4t4 .. 4t4+3; q's fragments
+//     use the same order.  One ldmatrix.x4 covers two k-steps.  q is
+//     converted to f16 after scaling each head by a power of two that puts
+//     its largest element in [2^14, 2^15); the score scale undoes it,
+//     together with the K scale.
+//   * O^T += V^T . P^T: ldmatrix.trans on 16-bit elements hands lane (g, t4)
+//     codes 2g, 2g+1 of positions 2t4 and 2t4+1; one byte permute pairs them
+//     by position, so row g of m-tile m holds d = 16m + 2g and row g + 8 holds
+//     d = 16m + 2g + 1.  One ldmatrix.x4.trans covers two m-tiles.  P is
+//     scaled by 2^15 before it is rounded to f16 (11-bit significand,
+//     weights kept down to 2^-39 of the row maximum); the V scale and 2^-15
+//     multiply the final sums.
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ void mma16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -370,18 +371,6 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint2 lds_b64(uint32_t addr) {
-    uint2 v;
-    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-    return v;
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -389,27 +378,25 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 
 // q of query heads [qh0, qh0 + hpb) as f16 B fragments in the permuted order
-// (for the step pair j, lane holds q[head g][32 j + 8 t4 + 0..7] times the
-// head's power-of-two scale); returns that scale for head g.
+// (lane holds q[head g][16 k + 4 t4 + 0..3] times the head's power-of-two
+// scale); returns that scale for head g.
 template <int D>
 __device__ __forceinline__ float load_q_f8(uint32_t (&qb)[Geo<D>::kSteps][2], const __nv_bfloat16* qrow0, int hpb,
                                            int lane) {
     constexpr int kSteps = Geo<D>::kSteps;
     const int g = lane >> 2, t4 = lane & 3;
-    const uint4* qrow = reinterpret_cast<const uint4*>(qrow0 + (size_t)(g < hpb ? g : 0) * D);
+    const uint2* qrow = reinterpret_cast<const uint2*>(qrow0 + (size_t)(g < hpb ? g : 0) * D);
     float v[kSteps][4];
     float mx = 0.f;
 #pragma unroll
-    for (int j = 0; j < kSteps / 2; ++j) {
-        const uint4 w = g < hpb ? qrow[4 * j + t4] : make_uint4(0u, 0u, 0u, 0u);   // d = 32 j + 8 t4 .. +7
-        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = pa::bf16x2_to_float2(ww[i]);
-            v[2 * j + (i >> 1)][2 * (i & 1)] = f.x;
-            v[2 * j + (i >> 1)][2 * (i & 1) + 1] = f.y;
-            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
+    for (int k = 0; k < kSteps; ++k) {
+        const uint2 w = g < hpb ? qrow[4 * k + t4] : make_uint2(0u, 0u);   // d = 16 k + 4 t4 .. +3
+        const float2 f01 = pa::bf16x2_to_float2(w.x), f23 = pa::bf16x2_to_float2(w.y);
+        v[k][0] = f01.x;
+        v[k][1] = f01.y;
+        v[k][2] = f23.x;
+        v[k][3] = f23.y;
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(f01.x), fabsf(f01.y)), fmaxf(fabsf(f23.x), fabsf(f23.y))));
     }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -431,21 +418,22 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
                                                 const uint32_t (&qb)[Geo<D>::kSteps][2], float c0, float c1,
                                                 int lane) {
     constexpr int kSteps = Geo<D>::kSteps;
-    const int g = lane >> 2, t4 = lane & 3;
+    const int g = lane >> 2, t4 = lane & 3, mi = lane >> 3;
+    // ldmatrix lane addressing for both tiles: matrix mi covers positions
+    // (mi & 1) * 8 .. +7 of 16-byte chunk c + (mi >> 1)
+    const int row = ((mi & 1) << 3) + (lane & 7), cadd = mi >> 1;
 
     float s_a[4] = {0.f, 0.f, 0.f, 0.f}, s_b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < kSteps / 2; ++j) {
-        // 8 codes at d = 32 j + 8 t4: chunk 2 j + t4 / 2, byte 8 (t4 & 1); rows g and g + 8 share the swizzle
-        const uint32_t off = ((uint32_t)((2 * j + (t4 >> 1)) ^ g) << 4) + 8 * (t4 & 1);
-        const uint2 w0 = lds_b64(ks + g * 128 + off);
-        const uint2 w1 = lds_b64(ks + (g + 8) * 128 + off);
+        uint32_t r[4];
+        ldsm_x4(ks + swz(row, 2 * j + cadd), r);            // r0, r1: rows g, g+8 of chunk 2j; r2, r3: chunk 2j+1
         uint32_t af[4];
-        e4m3x4_to_f16(w0.x, af[0], af[2]);
-        e4m3x4_to_f16(w1.x, af[1], af[3]);
+        e4m3x4_to_f16(r[0], af[0], af[2]);
+        e4m3x4_to_f16(r[1], af[1], af[3]);
         mma16816_f16(s_a, af, qb[2 * j][0], qb[2 * j][1]);
-        e4m3x4_to_f16(w0.y, af[0], af[2]);
-        e4m3x4_to_f16(w1.y, af[1], af[3]);
+        e4m3x4_to_f16(r[2], af[0], af[2]);
+        e4m3x4_to_f16(r[3], af[1], af[3]);
         mma16816_f16(s_b, af, qb[2 * j + 1][0], qb[2 * j + 1][1]);
     }
     float s[4];
@@ -493,32 +481,23 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
         mlo = (t < nv ? 0x0000ffffu : 0u) | (t + 1 < nv ? 0xffff0000u : 0u);
         mhi = (t + 8 < nv ? 0x0000ffffu : 0u) | (t + 9 < nv ? 0xffff0000u : 0u);
     }
-    const int r0 = 2 * t4;
 #pragma unroll
     for (int j = 0; j < kSteps / 2; ++j) {
-        // 4 codes at d = 32 j + 4 g: chunk 2 j + g / 4, byte 4 (g & 3)
-        const int ch = 2 * j + (g >> 2);
-        const uint32_t col = 4 * (g & 3);
-        const uint32_t L0 = lds_b32(vs + r0 * 128 + ((uint32_t)(ch ^ (r0 & 7)) << 4) + col);
-        const uint32_t L1 = lds_b32(vs + (r0 + 1) * 128 + ((uint32_t)(ch ^ ((r0 + 1) & 7)) << 4) + col);
-        const uint32_t L2 = lds_b32(vs + (r0 + 8) * 128 + ((uint32_t)(ch ^ (r0 & 7)) << 4) + col);
-        const uint32_t L3 = lds_b32(vs + (r0 + 9) * 128 + ((uint32_t)(ch ^ ((r0 + 1) & 7)) << 4) + col);
-        uint32_t af[4];
-        // m-tile 2j: d 32j+4g (rows g) and +1 (rows g+8); m-tile 2j+1: d +2 and +3
-        e4m3x4_to_f16(prmt(L0, L1, 0x5140u), af[0], af[1]);
-        e4m3x4_to_f16(prmt(L2, L3, 0x5140u), af[2], af[3]);
-        af[0] &= mlo;
-        af[1] &= mlo;
-        af[2] &= mhi;
-        af[3] &= mhi;
-        mma16816_f16(st.acc[2 * j], af, bh0, bh1);
-        e4m3x4_to_f16(prmt(L0, L1, 0x7362u), af[0], af[1]);
-        e4m3x4_to_f16(prmt(L2, L3, 0x7362u), af[2], af[3]);
-        af[0] &= mlo;
-        af[1] &= mlo;
-        af[2] &= mhi;
-        af[3] &= mhi;
-        mma16816_f16(st.acc[2 * j + 1], af, bh0, bh1);
+        uint32_t r[4];
+        // r0 / r1: positions 2t4, 2t4+1 / 2t4+8, 2t4+9 of chunk 2j (codes 2g, 2g+1
+        // of each); r2 / r3: the same for chunk 2j+1
+        ldsm_x4_trans(vs + swz(row, 2 * j + cadd), r);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t af[4];
+            e4m3x4_to_f16(prmt(r[2 * h], r[2 * h], 0x3120u), af[0], af[1]);       // [p0 d0, p1 d0 | p0 d1, p1 d1]
+            e4m3x4_to_f16(prmt(r[2 * h + 1], r[2 * h + 1], 0x3120u), af[2], af[3]);
+            af[0] &= mlo;
+            af[1] &= mlo;
+            af[2] &= mhi;
+            af[3] &= mhi;
+            mma16816_f16(st.acc[2 * j + h], af, bh0, bh1);
+        }
     }
 }
 
@@ -537,8 +516,14 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bars, int k, int lane, int3
 // ============================================================================
 // Fixed partitions: one thread block per (sequence, head group, partition)
 // ============================================================================
+// FP8 stages are half the size and the kernel is bound by instruction latency,
+// not bytes: one more resident block per SM.
+#ifndef PA_DECODE_MIN_BLOCKS_F8
+#define PA_DECODE_MIN_BLOCKS_F8 4
+#endif
+
 template <int D, bool F8>
-__global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
+__global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DECODE_MIN_BLOCKS)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                             const DecodeArgs a) {
     using G = Geo<D, F8>;
@@ -651,11 +636,11 @@ __global__ void __launch_bounds__(kThreads, PA_DECODE_MIN_BLOCKS)
         lw[warp * kHeads + h0 + 1] = st.l1;
     }
     // rows g and g + 8 of m-tile m are d = 16 m + g and 16 m + g + 8 (FP8:
-    // 32 (m / 2) + 4 g + 2 (m % 2) and one more)
+    // 16 m + 2 g and 16 m + 2 g + 1)
     constexpr int kRow2 = F8 ? 1 : 8;
 #pragma unroll
     for (int m = 0; m < G::kSteps; ++m) {
-        const int drow = F8 ? 32 * (m >> 1) + 4 * g + 2 * (m & 1) : 16 * m + g;
+        const int drow = F8 ? 16 * m + 2 * g : 16 * m + g;
         float* u0 = uw + (warp * kHeads + h0) * D + drow;
         float* u1 = u0 + D;
         u0[0] = st.acc[m][0];
