@@ -73,7 +73,7 @@ _SIGS = {
     "pa_reshape_and_cache_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                           _c_float, _vp, _vp]),
     "pa_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
-                            _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp]),
+                            _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
     "pa_lse_merge": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                       _vp]),
@@ -217,10 +217,29 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, block_size, 
     return _check(st, "pa_decode")
 
 
+_prefill_counters = {}
+
+
+def prefill_counters(device, stream=None):
+    """The two zeroed int32 work-claim counters pa_prefill uses on this device
+    and stream (each call leaves them zero again); one pair per stream, since
+    calls sharing a pair must not overlap."""
+    dev = torch.device(device)
+    handle = _stream(stream).value or 0
+    key = (dev.index if dev.index is not None else torch.cuda.current_device(), handle)
+    t = _prefill_counters.get(key)
+    if t is None:
+        t = torch.zeros(2, dtype=torch.int32, device=dev)
+        _prefill_counters[key] = t
+    return t
+
+
 def pa_prefill(out, q, k_cache, v_cache, block_tables, query_start, context_lens, max_query_len, block_size,
-               scale, n_q_heads, n_kv_heads, d_head, status=None, stream=None):
+               scale, n_q_heads, n_kv_heads, d_head, status=None, stream=None, counters=None):
     """out [T, Hq, D] (bf16 or f32) <- causal paged prefill attention of the
-    new positions of each sequence; see pa.h."""
+    new positions of each sequence; see pa.h.  `counters`: the int32 [2]
+    work-claim pair (default: this stream's, from prefill_counters; False:
+    none, a fixed round-robin assignment of work)."""
     if out.dtype == torch.bfloat16:
         out_dtype = PA_DTYPE_BF16
     elif out.dtype == torch.float32:
@@ -233,6 +252,10 @@ def pa_prefill(out, q, k_cache, v_cache, block_tables, query_start, context_lens
     if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (n_kv_heads, block_size, d_head) or \
             k_cache.shape != v_cache.shape:
         raise ValueError("k_cache/v_cache must be [num_blocks, n_kv_heads, block_size, d_head]")
+    if counters is None:
+        counters = prefill_counters(q.device, stream)
+    if counters is not False and counters.numel() < 2:
+        raise ValueError("counters must hold 2 int32")
     num_seqs = block_tables.shape[0]
     if block_tables.dim() != 2 or context_lens.shape != (num_seqs,) or query_start.shape != (num_seqs + 1,):
         raise ValueError("block_tables [S, max_blocks], query_start [S + 1], context_lens [S]")
@@ -242,7 +265,9 @@ def pa_prefill(out, q, k_cache, v_cache, block_tables, query_start, context_lens
                          _dev(query_start, torch.int32, "query_start"), _dev(context_lens, torch.int32, "context_lens"),
                          int(num_seqs), int(num_tokens), int(max_query_len), int(k_cache.shape[0]), int(block_size),
                          float(scale), int(n_q_heads), int(n_kv_heads), int(d_head),
-                         _opt_dev(status, torch.int32, "status"), _stream(stream))
+                         _opt_dev(None if counters is False else counters, torch.int32, "counters"),
+                         _opt_dev(status, torch.int32, "status"),
+                         _stream(stream))
     return _check(st, "pa_prefill")
 
 

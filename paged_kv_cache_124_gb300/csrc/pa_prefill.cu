@@ -69,6 +69,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest weight allowed
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kSoftmaxThreads = 256;
+constexpr int kRing = 4;              // work items posted ahead by the producer
+constexpr int kItemReaders = 10;      // warps that read each posted item: 2 MMA + 8 softmax
 
 template <int D>
 struct PGeo {
@@ -83,7 +85,7 @@ struct PGeo {
     static constexpr int kBars = kRed + 2 * 2 * 2 * kRows * 4;
     // barriers, slots and alignment slack; at least 120 KiB so that two CTAs
     // never share an SM (each holds 512 tensor-memory columns)
-    static constexpr int kSmem = kBars + 256 + 1024 > 120 * 1024 ? kBars + 256 + 1024 : 120 * 1024;
+    static constexpr int kSmem = kBars + 512 + 1024 > 120 * 1024 ? kBars + 512 + 1024 : 120 * 1024;
 };
 
 struct PrefillArgs {
@@ -95,7 +97,7 @@ struct PrefillArgs {
     const int32_t* context_lens;
     int num_seqs;
     int num_tokens;
-    int tiles_per_seq;    // CTAs per sequence (each covers 2 * tq tokens)
+    int tiles_per_seq;    // work items per sequence and KV head (each covers 2 * tq tokens)
     int block_size;
     int n_kv_heads;
     int group;            // query heads per KV head
@@ -105,6 +107,7 @@ struct PrefillArgs {
     int oob_row;          // a row coordinate past the end of the cache view
     float scale_log2;     // scale * log2(e)
     int32_t* status;
+    int* sched;           // {next item, CTAs done} claimed with atomics, or null: fixed order
 };
 
 struct Bars {
@@ -115,11 +118,17 @@ struct Bars {
     uint64_t v_empty[2][kVStages];  // per Q tile and stage: its value products reading V are done
     uint64_t s_full[2];   // per Q tile: its scores are in tensor memory
     uint64_t p_full[2];   // per Q tile: its weights are in tensor memory (and O rescaled)
-    uint64_t o_done[2];   // per Q tile: its last product has finished
+    uint64_t o_done[2];   // per Q tile: its last product of an item has finished
+    uint64_t o_free[2];   // per Q tile: the softmax warps have read O out
+    uint64_t q_empty[2];  // per Q tile: its last score product of an item has finished
     uint64_t red[2];      // per Q tile: both halves of every row posted their value
+    uint64_t item_full[kRing];    // the producer posted the next work item
+    uint64_t item_empty[kRing];   // every consumer warp has read it
+    int item[kRing];
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block overflows its reserved space");
 
 // --- tcgen05 / TMA wrappers --------------------------------------------------
 
@@ -276,8 +285,53 @@ __device__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* b, int32_t* stat
 
 // --- the kernel ------------------------------------------------------------------
 
+// One work item: 2 x 128 query rows (Q tiles A, B) of one KV head of one
+// sequence.  Every role of a CTA decodes the same items in the same order.
+struct Item {
+    int seq, h, q0, n, ctx, t0;
+    int kv_end0, kv_end1, nt0, nt1, n_tiles;
+    bool has_b;
+    const int* table;
+};
+
+// Item i of the heavy-first order (latest token tiles first); false when it
+// holds no query row (past the sequence's new tokens) or is invalid.
+__device__ __forceinline__ bool decode_item(int i, const PrefillArgs& a, Item& it, bool flag) {
+    const int per_tile = a.num_seqs * a.n_kv_heads;
+    const int tile = a.tiles_per_seq - 1 - i / per_tile;
+    const int r = i - (i / per_tile) * per_tile;
+    it.seq = r % a.num_seqs;
+    it.h = r / a.num_seqs;
+    it.q0 = a.query_start[it.seq];
+    it.n = a.query_start[it.seq + 1] - it.q0;
+    it.ctx = a.context_lens[it.seq];
+    it.t0 = tile * 2 * a.tq;
+    if (it.t0 >= it.n || it.q0 < 0) return false;
+    if (it.ctx > a.max_blocks * a.block_size) {
+        if (flag) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
+        it.ctx = a.max_blocks * a.block_size;
+    }
+    if (it.ctx < it.n) {
+        if (flag) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
+        return false;
+    }
+    it.has_b = it.t0 + a.tq < it.n;
+    it.kv_end0 = it.ctx - it.n + min(it.n, it.t0 + a.tq);
+    it.kv_end1 = it.ctx - it.n + min(it.n, it.t0 + 2 * a.tq);
+    it.nt0 = (it.kv_end0 + kKv - 1) / kKv;
+    it.nt1 = it.has_b ? (it.kv_end1 + kKv - 1) / kKv : 0;
+    it.n_tiles = it.has_b ? it.nt1 : it.nt0;
+    it.table = a.block_tables + (size_t)it.seq * a.max_blocks;
+    return true;
+}
+
 // Ten warps on four SM sub-partitions: three share one 16K-register file,
 // so at most 168 registers per thread.
+//
+// Persistent: one CTA per SM walks items blockIdx.x, blockIdx.x + gridDim.x,
+// ...; every barrier's phase runs on across items, so the next item's Q and
+// K/V copies and score products overlap the current item's last products and
+// output.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -288,33 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars* bars = reinterpret_cast<Bars*>(sm + G::kBars);
     const uint32_t s_q = pa::smem_addr(sm + G::kQ);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // work item: heaviest tiles (latest tokens) launch first
-    const int seq = blockIdx.x % a.num_seqs;
-    const int tile = a.tiles_per_seq - 1 - (int)(blockIdx.x / a.num_seqs);
-    const int h = blockIdx.y;
-    const int q0 = a.query_start[seq];
-    const int n = a.query_start[seq + 1] - q0;
-    int ctx = a.context_lens[seq];
-    const int t0 = tile * 2 * a.tq;                      // first token of tile A
-    if (t0 >= n || q0 < 0) return;
-    if (ctx > a.max_blocks * a.block_size) {
-        if (threadIdx.x == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
-        ctx = a.max_blocks * a.block_size;
-    }
-    if (ctx < n) {
-        if (threadIdx.x == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
-        return;
-    }
-    const bool has_b = t0 + a.tq < n;
-    // keys needed by each Q tile: positions [0, kv_end[x])
-    const int kv_end0 = ctx - n + min(n, t0 + a.tq);
-    const int kv_end1 = ctx - n + min(n, t0 + 2 * a.tq);
-    const int nt0 = (kv_end0 + kKv - 1) / kKv;
-    const int nt1 = has_b ? (kv_end1 + kKv - 1) / kKv : 0;
-    const int kv_all = has_b ? kv_end1 : kv_end0;
-    const int n_tiles = has_b ? nt1 : nt0;
-    const int* table = a.block_tables + (size_t)seq * a.max_blocks;
+    const int n_items = a.tiles_per_seq * a.num_seqs * a.n_kv_heads;
 
     if (threadIdx.x == 0) {
         pa::mbar_init(&bars->q_full, 1);
@@ -328,10 +356,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             pa::mbar_init(&bars->v_empty[0][i], 1);
             pa::mbar_init(&bars->v_empty[1][i], 1);
         }
+        for (int i = 0; i < kRing; ++i) {
+            pa::mbar_init(&bars->item_full[i], 1);
+            pa::mbar_init(&bars->item_empty[i], kItemReaders);
+        }
         for (int i = 0; i < 2; ++i) {
+            pa::mbar_init(&bars->q_empty[i], 1);
             pa::mbar_init(&bars->s_full[i], 1);
             pa::mbar_init(&bars->p_full[i], kSoftmaxThreads);
             pa::mbar_init(&bars->o_done[i], 1);
+            pa::mbar_init(&bars->o_free[i], kSoftmaxThreads);
             pa::mbar_init(&bars->red[i], kSoftmaxThreads);
         }
         bars->abort = 0;
@@ -351,76 +385,112 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         // Lane i handles block i of each K/V tile: it reads that block's
-        // table entry before the stage is free (one memory round trip per
-        // tile, hidden behind the wait) and issues the block's copies.
+        // table entry before the stage is free and issues the block's copies.
         const int bpt = kKv / a.block_size;              // blocks per tile
-        if (lane == 0) {
-            pa::mbar_arrive_expect_tx(&bars->q_full, (has_b ? 2 : 1) * G::kQBytes);
-            for (int x = 0; x < (has_b ? 2 : 1); ++x)
-#pragma unroll
-                for (int hh = 0; hh < G::kHalves; ++hh)
-                    tma_3d(s_q + x * G::kQBytes + hh * G::kHalfBytes, &mq, hh * 64, h * a.group,
-                           q0 + t0 + x * a.tq, &bars->q_full);
-        }
-        int row = a.oob_row;
-        auto table_row = [&](int j) {
-            int r_ = a.oob_row;
-            const int pos = j * kKv + lane * a.block_size;
-            if (lane < bpt && pos < kv_all) {
-                const int blk = table[pos / a.block_size];
-                if (blk < 0 || blk >= a.num_blocks)
-                    pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
-                else
-                    r_ = (blk * a.n_kv_heads + h) * a.block_size;
+        int g = 0, c = 0;                                 // K/V tiles and items so far
+        int nq = 0, np = 0;                               // Q copies issued, ring entries posted
+        bool ok = true;
+        // post item i (-1: no more) to the other warps
+        auto post = [&](int i) {
+            const int slot = np % kRing;
+            if (np >= kRing && !wait_warp(&bars->item_empty[slot], (np / kRing - 1) & 1, bars, a.status))
+                return false;
+            if (lane == 0) {
+                *reinterpret_cast<volatile int*>(&bars->item[slot]) = i;
+                pa::mbar_arrive(&bars->item_full[slot]);
             }
-            return r_;
+            ++np;
+            return true;
         };
-        if (n_tiles > 0) row = table_row(0);
-        int issued = 0;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int ks = j % kKStages, vs = j % kVStages;
-            const uint32_t s_k = pa::smem_addr(sm + G::kK0 + ks * G::kKVBytes);
-            const uint32_t s_v = pa::smem_addr(sm + G::kV0 + vs * G::kKVBytes);
-            const uint32_t dst = lane * a.block_size * 128;
-            // the stage's previous tile must be done with by each Q tile that used it
-            if (j >= kKStages && !((j - kKStages >= nt0 ||
-                                    wait_warp(&bars->k_empty[0][ks], (j / kKStages - 1) & 1, bars, a.status)) &&
-                                   (j - kKStages >= nt1 ||
-                                    wait_warp(&bars->k_empty[1][ks], (j / kKStages - 1) & 1, bars, a.status))))
-                break;
-            if (lane == 0) pa::mbar_arrive_expect_tx(&bars->k_full[ks], G::kKVBytes);
-            __syncwarp();
-            if (lane < bpt)
-#pragma unroll
-                for (int hh = 0; hh < G::kHalves; ++hh)
-                    tma_2d(s_k + hh * G::kHalfBytes + dst, &mk, hh * 64, row, &bars->k_full[ks]);
-            if (j >= kVStages &&
-                !((j - kVStages >= nt0 || wait_warp(&bars->v_empty[0][vs], (j / kVStages - 1) & 1, bars, a.status)) &&
-                  (j - kVStages >= nt1 || wait_warp(&bars->v_empty[1][vs], (j / kVStages - 1) & 1, bars, a.status)))) {
-                issued = j * 2 + 1;                       // K of tile j is in flight, V is not
+        // Items are claimed in heavy-first order, from a counter shared by
+        // all CTAs (the next free CTA takes the next item) or, without one,
+        // round-robin.
+        for (int k = 0; ok; ++k) {
+            int i = 0;
+            if (lane == 0) i = a.sched ? atomicAdd(a.sched, 1) : (int)blockIdx.x + k * (int)gridDim.x;
+            i = __shfl_sync(0xffffffffu, i, 0);
+            if (i >= n_items) {
+                post(-1);
                 break;
             }
-            if (lane == 0) pa::mbar_arrive_expect_tx(&bars->v_full[vs], G::kKVBytes);
-            __syncwarp();
-            if (lane < bpt)
+            Item it;
+            if (!decode_item(i, a, it, lane == 0)) continue;
+            ok = post(i);
+            if (!ok) break;
+            // Q of this item replaces the previous item's once both tiles' last
+            // score products are done
+            if (c >= 1)
+                ok = wait_warp(&bars->q_empty[0], (c - 1) & 1, bars, a.status) &&
+                     wait_warp(&bars->q_empty[1], (c - 1) & 1, bars, a.status);
+            if (!ok) break;
+            if (lane == 0) {
+                pa::mbar_arrive_expect_tx(&bars->q_full, (it.has_b ? 2 : 1) * G::kQBytes);
+                for (int x = 0; x < (it.has_b ? 2 : 1); ++x)
 #pragma unroll
-                for (int hh = 0; hh < G::kHalves; ++hh)
-                    tma_2d(s_v + hh * G::kHalfBytes + dst, &mv, hh * 64, row, &bars->v_full[vs]);
-            issued = j * 2 + 2;
-            if (j + 1 < n_tiles) row = table_row(j + 1);
+                    for (int hh = 0; hh < G::kHalves; ++hh)
+                        tma_3d(s_q + x * G::kQBytes + hh * G::kHalfBytes, &mq, hh * 64, it.h * a.group,
+                               it.q0 + it.t0 + x * a.tq, &bars->q_full);
+            }
+            ++nq;
+            const int kv_all = it.has_b ? it.kv_end1 : it.kv_end0;
+            auto table_row = [&](int j) {
+                int r_ = a.oob_row;
+                const int pos = j * kKv + lane * a.block_size;
+                if (lane < bpt && pos < kv_all) {
+                    const int blk = it.table[pos / a.block_size];
+                    if (blk < 0 || blk >= a.num_blocks)
+                        pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
+                    else
+                        r_ = (blk * a.n_kv_heads + it.h) * a.block_size;
+                }
+                return r_;
+            };
+            int row = table_row(0);
+            for (int j = 0; j < it.n_tiles; ++j, ++g) {
+                const int ks = g % kKStages, vs = g % kVStages;
+                const uint32_t s_k = pa::smem_addr(sm + G::kK0 + ks * G::kKVBytes);
+                const uint32_t s_v = pa::smem_addr(sm + G::kV0 + vs * G::kKVBytes);
+                const uint32_t dst = lane * a.block_size * 128;
+                // both Q tiles' MMA warps release every K/V tile (used or not)
+                if (g >= kKStages)
+                    ok = wait_warp(&bars->k_empty[0][ks], (g / kKStages - 1) & 1, bars, a.status) &&
+                         wait_warp(&bars->k_empty[1][ks], (g / kKStages - 1) & 1, bars, a.status);
+                if (!ok) break;
+                if (lane == 0) pa::mbar_arrive_expect_tx(&bars->k_full[ks], G::kKVBytes);
+                __syncwarp();
+                if (lane < bpt)
+#pragma unroll
+                    for (int hh = 0; hh < G::kHalves; ++hh)
+                        tma_2d(s_k + hh * G::kHalfBytes + dst, &mk, hh * 64, row, &bars->k_full[ks]);
+                if (g >= kVStages)
+                    ok = wait_warp(&bars->v_empty[0][vs], (g / kVStages - 1) & 1, bars, a.status) &&
+                         wait_warp(&bars->v_empty[1][vs], (g / kVStages - 1) & 1, bars, a.status);
+                if (!ok) {
+                    // K of tile g is in flight, V is not
+                    if (lane == 0) pa::mbar_wait_bounded(&bars->k_full[ks], (g / kKStages) & 1, kMaxProbes);
+                    break;
+                }
+                if (lane == 0) pa::mbar_arrive_expect_tx(&bars->v_full[vs], G::kKVBytes);
+                __syncwarp();
+                if (lane < bpt)
+#pragma unroll
+                    for (int hh = 0; hh < G::kHalves; ++hh)
+                        tma_2d(s_v + hh * G::kHalfBytes + dst, &mv, hh * 64, row, &bars->v_full[vs]);
+                if (j + 1 < it.n_tiles) row = table_row(j + 1);
+            }
+            ++c;
         }
         // the copies this warp started must land before the CTA exits: the
         // last use of each stage (earlier uses completed before it was reused)
         if (lane == 0) {
-            pa::mbar_wait_bounded(&bars->q_full, 0, kMaxProbes);
-            const int nk = (issued + 1) / 2, nv = issued / 2;   // tiles whose K / V copies were issued
-            for (int i = 0; i < kKStages && i < nk; ++i) {
-                const int j = nk - 1 - i;
-                pa::mbar_wait_bounded(&bars->k_full[j % kKStages], (j / kKStages) & 1, kMaxProbes);
+            if (nq) pa::mbar_wait_bounded(&bars->q_full, (nq - 1) & 1, kMaxProbes);
+            for (int i = 0; i < kKStages && i < g; ++i) {
+                const int t = g - 1 - i;
+                pa::mbar_wait_bounded(&bars->k_full[t % kKStages], (t / kKStages) & 1, kMaxProbes);
             }
-            for (int i = 0; i < kVStages && i < nv; ++i) {
-                const int j = nv - 1 - i;
-                pa::mbar_wait_bounded(&bars->v_full[j % kVStages], (j / kVStages) & 1, kMaxProbes);
+            for (int i = 0; i < kVStages && i < g; ++i) {
+                const int t = g - 1 - i;
+                pa::mbar_wait_bounded(&bars->v_full[t % kVStages], (t / kVStages) & 1, kMaxProbes);
             }
         }
     } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
@@ -428,9 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One thread per Q tile: a single thread cannot issue N=128 products
         // fast enough to keep the tensor pipe busy, two can.
         const int x = warp - kMmaWarp0;
-        const int ntx = x ? nt1 : nt0;
-        const int kv_endx = x ? kv_end1 : kv_end0;
-        if (lane == 0 && ntx > 0) {
+        if (lane == 0) {
             constexpr uint32_t id_qk = idesc_bf16(kRows, kKv, 0);
             constexpr uint32_t id_pv = idesc_bf16(kRows, D, 1);
             const uint32_t t_s = tmem + kTmemS0 + x * 128;
@@ -451,56 +519,103 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(t_s, smem_desc(qx + off, 16, 1024), smem_desc(s_k + off, 16, 1024), id_qk, kk > 0);
                 }
             };
-            bool ok = wait1(&bars->q_full, 0, bars, a.status) && wait1(&bars->k_full[0], 0, bars, a.status);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-                commit(&bars->s_full[x], 0);
-                commit(&bars->k_empty[x][0], 0);
-            }
-            for (int j = 0; ok && j < ntx; ++j) {
-                const int vs = j % kVStages;
-                ok = wait1(&bars->v_full[vs], (j / kVStages) & 1, bars, a.status);
+            // A tile this Q tile does not read is released only once it has
+            // landed: the producer has then consumed the stage's previous
+            // release, so each barrier moves on by exactly one phase per tile.
+            auto skip_tile = [&](int gt) {
+                if (!wait1(&bars->k_full[gt % kKStages], (gt / kKStages) & 1, bars, a.status)) return false;
+                pa::mbar_arrive(&bars->k_empty[x][gt % kKStages]);
+                if (!wait1(&bars->v_full[gt % kVStages], (gt / kVStages) & 1, bars, a.status)) return false;
+                pa::mbar_arrive(&bars->v_empty[x][gt % kVStages]);
+                return true;
+            };
+            int g = 0, c = 0, ns = 0, nod = 0;            // K/V tiles, items, S products, outputs so far
+            bool ok = true;
+            for (int nc = 0;; ++nc) {
+                const int slot = nc % kRing;
+                ok = wait1(&bars->item_full[slot], (nc / kRing) & 1, bars, a.status);
                 if (!ok) break;
-                uint8_t* vbase = sm + G::kV0 + vs * G::kKVBytes;
-                const uint32_t s_v = pa::smem_addr(vbase);
-                const int valid = min(kKv, kv_endx - j * kKv);
-                const int ksteps = (valid + 15) >> 4;
-                // Rows at and past the context length inside the last block may
-                // hold anything (NaN included); their weights are 0, but 0 * NaN
-                // is not, so clear those V rows before the product reads them.
-                // Only rows past the context are touched (both issuers may clear
-                // the same rows; they write the same zeros).
-                const int zero_begin = max(valid, ctx - j * kKv);
-                const int zero_end = min(ksteps * 16, ((ctx + a.block_size - 1) / a.block_size) * a.block_size - j * kKv);
-                if (zero_begin < zero_end) {
-                    for (int r = zero_begin; r < zero_end; ++r)
-#pragma unroll
-                        for (int hh = 0; hh < G::kHalves; ++hh) {
-                            uint4* row = reinterpret_cast<uint4*>(vbase + hh * G::kHalfBytes + r * 128);
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) row[c] = make_uint4(0, 0, 0, 0);
-                        }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const int i = *reinterpret_cast<volatile int*>(&bars->item[slot]);
+                pa::mbar_arrive(&bars->item_empty[slot]);
+                if (i < 0) break;
+                Item it;
+                decode_item(i, a, it, false);
+                const int ntx = x ? it.nt1 : it.nt0;
+                const int kv_endx = x ? it.kv_end1 : it.kv_end0;
+                if (ntx == 0) {
+                    // this Q tile has no rows in the item: release Q and every K/V tile
+                    ok = wait1(&bars->q_full, c & 1, bars, a.status);
+                    if (!ok) break;
+                    pa::mbar_arrive(&bars->q_empty[x]);
+                    for (int j = 0; ok && j < it.n_tiles; ++j) ok = skip_tile(g + j);
+                    g += it.n_tiles;
+                    ++c;
+                    continue;
                 }
-                // K of the next tile too, so that the products of this one and
-                // the scores of the next go out back to back once P is ready
-                const int nks = (j + 1) % kKStages;
-                if (j + 1 < ntx) ok = wait1(&bars->k_full[nks], ((j + 1) / kKStages) & 1, bars, a.status);
-                if (ok) ok = wait1(&bars->p_full[x], j & 1, bars, a.status);
+                ok = wait1(&bars->q_full, c & 1, bars, a.status) && wait1(&bars->k_full[g % kKStages],
+                                                                            (g / kKStages) & 1, bars, a.status);
                 if (!ok) break;
                 tc_fence_after();
-                for (int kk = 0; kk < ksteps; ++kk)
-                    mma_bf16_ta(t_o, t_s + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                commit(&bars->v_empty[x][vs], (j / kVStages) & 1);
-                if (j == ntx - 1) {
-                    commit(&bars->o_done[x], 0);
-                } else {
-                    issue_s(nks);
-                    commit(&bars->s_full[x], (j + 1) & 1);
-                    commit(&bars->k_empty[x][nks], ((j + 1) / kKStages) & 1);
+                issue_s(g % kKStages);
+                commit(&bars->s_full[x], ns & 1);
+                ++ns;
+                commit(&bars->k_empty[x][g % kKStages], (g / kKStages) & 1);
+                if (ntx == 1) commit(&bars->q_empty[x], c & 1);
+                for (int j = 0; ok && j < it.n_tiles; ++j) {
+                    const int gj = g + j;
+                    const int vs = gj % kVStages;
+                    if (j >= ntx) {                       // tile beyond this Q tile's keys
+                        ok = skip_tile(gj);
+                        continue;
+                    }
+                    ok = wait1(&bars->v_full[vs], (gj / kVStages) & 1, bars, a.status);
+                    if (!ok) break;
+                    uint8_t* vbase = sm + G::kV0 + vs * G::kKVBytes;
+                    const uint32_t s_v = pa::smem_addr(vbase);
+                    const int valid = min(kKv, kv_endx - j * kKv);
+                    const int ksteps = (valid + 15) >> 4;
+                    // Rows at and past the context length inside the last block may
+                    // hold anything (NaN included); their weights are 0, but 0 * NaN
+                    // is not, so clear those V rows before the product reads them.
+                    // Only rows past the context are touched (both issuers may clear
+                    // the same rows; they write the same zeros).
+                    const int zero_begin = max(valid, it.ctx - j * kKv);
+                    const int zero_end =
+                        min(ksteps * 16, ((it.ctx + a.block_size - 1) / a.block_size) * a.block_size - j * kKv);
+                    if (zero_begin < zero_end) {
+                        for (int r = zero_begin; r < zero_end; ++r)
+#pragma unroll
+                            for (int hh = 0; hh < G::kHalves; ++hh) {
+                                uint4* rowp = reinterpret_cast<uint4*>(vbase + hh * G::kHalfBytes + r * 128);
+#pragma unroll
+                                for (int cc = 0; cc < 8; ++cc) rowp[cc] = make_uint4(0, 0, 0, 0);
+                            }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    const int nks = (gj + 1) % kKStages;
+                    if (j + 1 < ntx) ok = wait1(&bars->k_full[nks], ((gj + 1) / kKStages) & 1, bars, a.status);
+                    // O must have been read out by the previous item's epilogue
+                    if (ok && j == 0 && nod >= 1) ok = wait1(&bars->o_free[x], (nod - 1) & 1, bars, a.status);
+                    if (ok) ok = wait1(&bars->p_full[x], (ns - 1) & 1, bars, a.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < ksteps; ++kk)
+                        mma_bf16_ta(t_o, t_s + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    commit(&bars->v_empty[x][vs], (gj / kVStages) & 1);
+                    if (j == ntx - 1) {
+                        commit(&bars->o_done[x], nod & 1);
+                        ++nod;
+                    } else {
+                        issue_s(nks);
+                        commit(&bars->s_full[x], ns & 1);
+                        ++ns;
+                        commit(&bars->k_empty[x][nks], ((gj + 1) / kKStages) & 1);
+                        if (j + 1 == ntx - 1) commit(&bars->q_empty[x], c & 1);
+                    }
                 }
+                g += it.n_tiles;
+                ++c;
             }
             // products in flight must finish before the tensor memory is freed
             if (last) pa::mbar_wait_bounded(last, last_par, kMaxProbes);
@@ -509,23 +624,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ softmax warps
         const int quarter = warp & 3, hc = warp >> 2;     // lane quarter, column half
         const int r = quarter * 32 + lane;                // row = tensor-memory lane
-        const int t = r / a.group, g = r - t * a.group;
+        const int t = r / a.group, gq = r - t * a.group;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         float* red = reinterpret_cast<float*>(sm + G::kRed);
         const float c2 = a.scale_log2;
         constexpr int kHalfCols = kKv / 2;                // score columns per thread
         constexpr int kOCols = D / 2;                     // output columns per thread
-        float m_used[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-        int row_lim[2];
-        bool valid_row[2];
-        for (int x = 0; x < 2; ++x) {
-            const int tok = t0 + x * a.tq + t;
-            valid_row[x] = tok < n && q0 + tok < a.num_tokens;
-            const int kv_end = x ? kv_end1 : kv_end0;
-            row_lim[x] = valid_row[x] ? min(ctx - n + tok + 1, kv_end) : kv_end;    // keys [0, row_lim)
-        }
+        int ns[2] = {0, 0}, nred[2] = {0, 0}, nod[2] = {0, 0};
         // Post this half's value for row r of tile x and read the other half's.
-        auto exchange = [&](int x, int phase, float v, bool& ok_) {
+        auto exchange = [&](int x, float v, bool& ok_) {
+            const int phase = nred[x]++;
             float* slot = red + (((x * 2 + (phase & 1)) * 2) * kRows);
             slot[hc * kRows + r] = v;
             pa::mbar_arrive(&bars->red[x]);
@@ -533,104 +641,127 @@ __global__ void __launch_bounds__(kThreads, 1)
             return ok_ ? slot[(1 - hc) * kRows + r] : v;
         };
         bool ok = true;
-        for (int j = 0; ok && j < n_tiles; ++j) {
+        for (int nc = 0; ok; ++nc) {
+            const int slot = nc % kRing;
+            ok = wait_warp(&bars->item_full[slot], (nc / kRing) & 1, bars, a.status);
+            if (!ok) break;
+            const int i = *reinterpret_cast<volatile int*>(&bars->item[slot]);
+            __syncwarp();
+            if (lane == 0) pa::mbar_arrive(&bars->item_empty[slot]);
+            if (i < 0) break;
+            Item it;
+            decode_item(i, a, it, false);
+            const int nt[2] = {it.nt0, it.nt1};
+            float m_used[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+            int row_lim[2];
+            bool valid_row[2];
             for (int x = 0; x < 2; ++x) {
-                if (j >= (x ? nt1 : nt0)) continue;
-                ok = wait_warp(&bars->s_full[x], j & 1, bars, a.status);
+                const int tok = it.t0 + x * a.tq + t;
+                valid_row[x] = tok < it.n && it.q0 + tok < a.num_tokens;
+                const int kv_end = x ? it.kv_end1 : it.kv_end0;
+                row_lim[x] = valid_row[x] ? min(it.ctx - it.n + tok + 1, kv_end) : kv_end;   // keys [0, row_lim)
+            }
+            for (int j = 0; ok && j < it.n_tiles; ++j) {
+                for (int x = 0; x < 2; ++x) {
+                    if (j >= nt[x]) continue;
+                    ok = wait_warp(&bars->s_full[x], ns[x] & 1, bars, a.status);
+                    ++ns[x];
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t t_s = t_lane + kTmemS0 + x * 128;
+                    float s[kHalfCols];
+#pragma unroll
+                    for (int cc = 0; cc < kHalfCols / 32; ++cc) tmem_ld32(t_s + hc * kHalfCols + cc * 32, s + cc * 32);
+                    tmem_wait_ld();
+                    const int lim = row_lim[x] - j * kKv - hc * kHalfCols;     // valid columns of this half
+                    if (lim < kHalfCols) {
+#pragma unroll
+                        for (int cc = 0; cc < kHalfCols; ++cc) s[cc] = cc < lim ? s[cc] : -INFINITY;
+                    }
+                    float mp[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) mp[k] = max3(s[k], s[8 + k], s[16 + k]);
+#pragma unroll
+                    for (int cc = 24; cc + 16 <= kHalfCols; cc += 16)
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) mp[k] = max3(mp[k], s[cc + k], s[cc + 8 + k]);
+                    if ((kHalfCols - 24) % 16 == 8) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[kHalfCols - 8 + k]);
+                    }
+                    float mt = fmaxf(max3(mp[0], mp[1], mp[2]), fmaxf(max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                    mt = fmaxf(mt, exchange(x, mt, ok));
+                    if (!ok) break;
+                    const float mts = mt * c2;            // scale > 0: the maximum commutes with it
+                    const bool rescale = mts > m_used[x] + kRescaleThreshold;
+                    const float m_new = rescale ? mts : m_used[x];
+                    const float alpha = rescale ? fast_exp2(m_used[x] - m_new) : 1.f;   // exp2(-inf) = 0 at first
+                    if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+                        // O holds the products of tiles < j (complete: this tile's
+                        // scores were issued after them) and not yet this tile's
+                        const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
+#pragma unroll 1
+                        for (int cc = 0; cc < kOCols / 32; ++cc) {
+                            float o[32];
+                            tmem_ld32(t_o + cc * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) o[q] *= alpha;
+                            tmem_st32(t_o + cc * 32, o);
+                        }
+                    }
+                    l[x] *= alpha;
+                    m_used[x] = m_new;
+                    const float neg = -m_used[x];
+                    uint32_t w[kHalfCols / 2];
+                    float lp[4] = {0.f, 0.f, 0.f, 0.f};   // independent partial sums
+#pragma unroll
+                    for (int q = 0; q < kHalfCols / 2; ++q) {
+                        const float p0 = fast_exp2(fmaf(s[2 * q], c2, neg));
+                        const float p1 = fast_exp2(fmaf(s[2 * q + 1], c2, neg));
+                        lp[q & 3] += p0 + p1;
+                        w[q] = pack_bf16_rn(p0, p1);
+                    }
+                    l[x] += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+                    tmem_st32u(t_s + hc * (kHalfCols / 2), w);   // P columns over the first half of S
+                    tmem_wait_st();
+                    tc_fence_before();
+                    pa::mbar_arrive(&bars->p_full[x]);
+                }
+            }
+            for (int x = 0; x < 2 && ok; ++x) {
+                if (nt[x] == 0) continue;
+                const float l_all = l[x] + exchange(x, l[x], ok);
+                if (ok) ok = wait_warp(&bars->o_done[x], nod[x] & 1, bars, a.status);
+                ++nod[x];
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t t_s = t_lane + kTmemS0 + x * 128;
-                float s[kHalfCols];
+                const int tok = it.t0 + x * a.tq + t;
+                const float inv = 1.f / l_all;
+                const size_t orow = ((size_t)(it.q0 + tok) * a.n_q_heads + (size_t)it.h * a.group + gq) * D + hc * kOCols;
+                const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
+                float o[kOCols];
 #pragma unroll
-                for (int c = 0; c < kHalfCols / 32; ++c) tmem_ld32(t_s + hc * kHalfCols + c * 32, s + c * 32);
+                for (int cc = 0; cc < kOCols / 32; ++cc) tmem_ld32(t_o + cc * 32, o + cc * 32);
                 tmem_wait_ld();
-                const int lim = row_lim[x] - j * kKv - hc * kHalfCols;     // valid columns of this half
-                if (lim < kHalfCols) {
-#pragma unroll
-                    for (int c = 0; c < kHalfCols; ++c) s[c] = c < lim ? s[c] : -INFINITY;
-                }
-                float mp[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) mp[k] = max3(s[k], s[8 + k], s[16 + k]);
-#pragma unroll
-                for (int c = 24; c + 16 <= kHalfCols; c += 16)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mp[k] = max3(mp[k], s[c + k], s[c + 8 + k]);
-                if ((kHalfCols - 24) % 16 == 8) {
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[kHalfCols - 8 + k]);
-                }
-                float mt = fmaxf(max3(mp[0], mp[1], mp[2]), fmaxf(max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-                mt = fmaxf(mt, exchange(x, j, mt, ok));
-                if (!ok) break;
-                const float mts = mt * c2;                // scale > 0: the maximum commutes with it
-                const bool rescale = mts > m_used[x] + kRescaleThreshold;
-                const float m_new = rescale ? mts : m_used[x];
-                const float alpha = rescale ? fast_exp2(m_used[x] - m_new) : 1.f;   // exp2(-inf) = 0 at first
-                if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-                    // O holds the products of tiles < j (complete: this tile's
-                    // scores were issued after them) and not yet this tile's
-                    const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
-#pragma unroll 1
-                    for (int c = 0; c < kOCols / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(t_o + c * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(t_o + c * 32, o);
-                    }
-                }
-                l[x] *= alpha;
-                m_used[x] = m_new;
-                const float neg = -m_used[x];
-                uint32_t w[kHalfCols / 2];
-                float lp[4] = {0.f, 0.f, 0.f, 0.f};       // independent partial sums
-#pragma unroll
-                for (int i = 0; i < kHalfCols / 2; ++i) {
-                    const float p0 = fast_exp2(fmaf(s[2 * i], c2, neg));
-                    const float p1 = fast_exp2(fmaf(s[2 * i + 1], c2, neg));
-                    lp[i & 3] += p0 + p1;
-                    w[i] = pack_bf16_rn(p0, p1);
-                }
-                l[x] += (lp[0] + lp[1]) + (lp[2] + lp[3]);
-                tmem_st32u(t_s + hc * (kHalfCols / 2), w);   // P columns over the first half of S
-                tmem_wait_st();
+                // O is in registers: the next item's products may overwrite it
                 tc_fence_before();
-                pa::mbar_arrive(&bars->p_full[x]);
-            }
-        }
-        for (int x = 0; x < 2 && ok; ++x) {
-            const int ntx = x ? nt1 : nt0;
-            if (ntx == 0) continue;
-            const float l_all = l[x] + exchange(x, ntx, l[x], ok);
-            if (ok) ok = wait_warp(&bars->o_done[x], 0, bars, a.status);
-            if (!ok) break;
-            tc_fence_after();
-            const int tok = t0 + x * a.tq + t;
-            const float inv = 1.f / l_all;
-            const size_t orow = ((size_t)(q0 + tok) * a.n_q_heads + (size_t)h * a.group + g) * D + hc * kOCols;
-            const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
-#pragma unroll 1
-            for (int c = 0; c < kOCols / 32; ++c) {
-                float o[32];
-                tmem_ld32(t_o + c * 32, o);
-                tmem_wait_ld();
+                pa::mbar_arrive(&bars->o_free[x]);
                 if (valid_row[x]) {
                     if (a.out_f32) {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow + c * 32);
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                                 o[4 * i + 3] * inv);
+                        for (int q = 0; q < kOCols / 4; ++q)
+                            dst[q] = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv,
+                                                 o[4 * q + 3] * inv);
                     } else {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + c * 32);
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(pack_bf16_rn(o[8 * i] * inv, o[8 * i + 1] * inv),
-                                                pack_bf16_rn(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
-                                                pack_bf16_rn(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
-                                                pack_bf16_rn(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
+                        for (int q = 0; q < kOCols / 8; ++q)
+                            dst[q] = make_uint4(pack_bf16_rn(o[8 * q] * inv, o[8 * q + 1] * inv),
+                                                pack_bf16_rn(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
+                                                pack_bf16_rn(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
+                                                pack_bf16_rn(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
                     }
                 }
             }
@@ -643,6 +774,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+    if (threadIdx.x == 0 && a.sched) {
+        // every CTA has made its last claim once all have counted themselves
+        // done: the last one leaves both counters at zero for the next launch
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1) == (int)gridDim.x - 1) {
+            atomicExch(a.sched, 0);
+            atomicExch(a.sched + 1, 0);
+        }
     }
 }
 
@@ -676,6 +816,17 @@ bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims
 template <int D>
 int g_smem_done[64];   // per kernel instantiation: bytes opted in, by device
 
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev < 64 && cached[dev]) return cached[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
+
 template <int D>
 int launch(const PrefillArgs& a, const void* q, const void* k_cache, const void* v_cache, int num_tokens,
            long long cache_rows, dim3 grid, cudaStream_t st) {
@@ -702,8 +853,8 @@ extern "C" {
 int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start,
                const int32_t* context_lens, int num_seqs, int num_tokens, int max_query_len, int num_blocks,
-               int block_size, float scale, int n_q_heads, int n_kv_heads, int d_head, int32_t* status_dev,
-               void* stream) {
+               int block_size, float scale, int n_q_heads, int n_kv_heads, int d_head, int32_t* sched_dev,
+               int32_t* status_dev, void* stream) {
     if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_blocks <= 0 || max_blocks_per_seq < 0 ||
         n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
         return PA_ERR_INVALID_ARG;
@@ -716,7 +867,8 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
         return PA_ERR_INVALID_ARG;
     if (!pa_host::aligned16(out) || !pa_host::aligned16(q) || !pa_host::aligned16(k_cache) ||
         !pa_host::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
-        (reinterpret_cast<uintptr_t>(query_start) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        (reinterpret_cast<uintptr_t>(query_start) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sched_dev) & 3u))
         return PA_ERR_MISALIGNED;
     const long long cache_rows = (long long)num_blocks * n_kv_heads * block_size;
     if (cache_rows > INT_MAX - 64 || (long long)max_blocks_per_seq * block_size > INT_MAX / 2 ||
@@ -745,7 +897,11 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     a.oob_row = (int)cache_rows;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.status = status_dev;
-    const dim3 grid((unsigned)(tiles * num_seqs), (unsigned)n_kv_heads);
+    a.sched = reinterpret_cast<int*>(sched_dev);
+    const long long items = tiles * num_seqs * n_kv_heads;
+    if (items > INT_MAX - 4096) return PA_ERR_UNSUPPORTED;    // claims run past the last item by one per CTA
+    const int sms = num_sms();
+    const dim3 grid((unsigned)(items < sms ? items : sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return d_head == 128 ? launch<128>(a, q, k_cache, v_cache, num_tokens, cache_rows, grid, st)
                          : launch<64>(a, q, k_cache, v_cache, num_tokens, cache_rows, grid, st);

@@ -144,3 +144,30 @@ def test_prefill_host_errors():
         q_mis = flat[1:1 + q.numel()].view(q.shape)
         api.pa_prefill(out, q_mis, k, v, dev(tab), dev(qs), dev(ctx), 20, 16, 0.125, 8, 2, 64)
     assert e.value.status == api.PA_ERR_MISALIGNED
+
+
+def test_prefill_work_claiming_orders_agree():
+    """Several work items per thread block: the items claimed from the shared
+    counters (default), from a caller's pair, and in the fixed round-robin
+    order give identical bits, match the oracle, and leave the counters zero."""
+    rng = np.random.default_rng(11)
+    news = [int(x) for x in rng.integers(65, 400, size=24)]
+    ctxs = [n + int(p) for n, p in zip(news, rng.integers(0, 600, size=24))]
+    qb, kb, vb, tab, qs, ctx = _problem(12, 16, 4, 64, 16, ctxs, news)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    args = (from_bits(qb), from_bits(kb), from_bits(vb), dev(tab), dev(qs), dev(ctx), max(news), 16, 0.125, 16, 4, 64)
+    outs = []
+    mine = torch.zeros(2, dtype=torch.int32, device="cuda")
+    for counters in (None, mine, False, mine):
+        out = torch.full((qb.shape[0], 16, 64), float("nan"), dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        api.pa_prefill(out, *args, status=status, counters=counters)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        outs.append(out.cpu())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    assert mine.cpu().tolist() == [0, 0]
+    assert api.prefill_counters("cuda").cpu().tolist() == [0, 0]
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 0.125, 16, with_spread=True)
+    assert_prefill_close(out_to_f64(outs[0]), want, spread, True, "claimed items")
