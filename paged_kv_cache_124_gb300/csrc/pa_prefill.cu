@@ -253,8 +253,6 @@ __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
 // probes (then aborts the CTA and flags the timeout).
 __device__ bool wait1(uint64_t* bar, uint32_t parity, Bars* b, int32_t* status) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)                 // short spin first: most waits are nearly over
-        if (pa::mbar_test_wait(bar, parity)) return true;
     for (int i = 0; i < kMaxProbes; ++i) {
         if (pa::mbar_try_wait(bar, parity)) return true;
         if ((i & 63) == 63 && *reinterpret_cast<volatile int*>(&b->abort)) return false;
@@ -267,8 +265,6 @@ __device__ bool wait1(uint64_t* bar, uint32_t parity, Bars* b, int32_t* status) 
 // Whole warp, warp-uniform result.
 __device__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* b, int32_t* status) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-        if (__all_sync(0xffffffffu, pa::mbar_test_wait(bar, parity))) return true;
     for (int i = 0; i < kMaxProbes; ++i) {
         const bool done = pa::mbar_try_wait(bar, parity);
         if (__all_sync(0xffffffffu, done)) return true;
