@@ -56,9 +56,10 @@ namespace {
 
 constexpr int kRows = 128;                 // MMA M: query rows per tile
 constexpr int kKv = 128;                   // positions per K/V tile
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp0 = 9;               // MMA warps 9 (tile A) and 10 (tile B); 9 owns the tensor memory
-constexpr int kThreads = 352;              // 8 softmax warps, producer, 2 MMA warps
+constexpr int kProducerWarp = 8;           // claims work items, loads Q and K
+constexpr int kVProducerWarp = 9;          // loads V
+constexpr int kMmaWarp0 = 10;              // MMA warps 10 (tile A) and 11 (tile B); 10 owns the tensor memory
+constexpr int kThreads = 384;              // 8 softmax warps, 2 producers, 2 MMA warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS0 = 0;            // S_A; S_B at +128
 constexpr uint32_t kTmemO0 = 256;          // O_A; O_B at +128
@@ -70,7 +71,7 @@ constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kRing = 4;              // work items posted ahead by the producer
-constexpr int kItemReaders = 10;      // warps that read each posted item: 2 MMA + 8 softmax
+constexpr int kItemReaders = 11;      // warps that read each posted item: V producer, 2 MMA, 8 softmax
 
 template <int D>
 struct PGeo {
@@ -321,7 +322,7 @@ __device__ __forceinline__ bool decode_item(int i, const PrefillArgs& a, Item& i
     return true;
 }
 
-// Ten warps on four SM sub-partitions: three share one 16K-register file,
+// Twelve warps on four SM sub-partitions: three share one 16K-register file,
 // so at most 168 registers per thread.
 //
 // Persistent: one CTA per SM walks items blockIdx.x, blockIdx.x + gridDim.x,
@@ -378,13 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer
-        // Lane i handles block i of each K/V tile: it reads that block's
-        // table entry before the stage is free and issues the block's copies.
+    if (warp == kProducerWarp || warp == kVProducerWarp) {
+        // ------------------------------------------------------------ TMA producers
+        // A warp issues its copies one lane after another (tens of cycles
+        // each), so K and V have a producer warp each.  The K warp claims work
+        // items, posts them to the other warps and loads Q and K; the V warp
+        // follows the posted items.  Lane i handles block i of each tile.
+        const bool is_k = warp == kProducerWarp;
         const int bpt = kKv / a.block_size;              // blocks per tile
         int g = 0, c = 0;                                 // K/V tiles and items so far
-        int nq = 0, np = 0;                               // Q copies issued, ring entries posted
+        int nq = 0, np = 0;                               // Q copies issued, ring entries posted (K) or read (V)
         bool ok = true;
         // post item i (-1: no more) to the other warps
         auto post = [&](int i) {
@@ -402,77 +406,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         // all CTAs (the next free CTA takes the next item) or, without one,
         // round-robin.
         for (int k = 0; ok; ++k) {
-            int i = 0;
-            if (lane == 0) i = a.sched ? atomicAdd(a.sched, 1) : (int)blockIdx.x + k * (int)gridDim.x;
-            i = __shfl_sync(0xffffffffu, i, 0);
-            if (i >= n_items) {
-                post(-1);
-                break;
-            }
             Item it;
-            if (!decode_item(i, a, it, lane == 0)) continue;
-            ok = post(i);
-            if (!ok) break;
-            // Q of this item replaces the previous item's once both tiles' last
-            // score products are done
-            if (c >= 1)
-                ok = wait_warp(&bars->q_empty[0], (c - 1) & 1, bars, a.status) &&
-                     wait_warp(&bars->q_empty[1], (c - 1) & 1, bars, a.status);
-            if (!ok) break;
-            if (lane == 0) {
-                pa::mbar_arrive_expect_tx(&bars->q_full, (it.has_b ? 2 : 1) * G::kQBytes);
-                for (int x = 0; x < (it.has_b ? 2 : 1); ++x)
-#pragma unroll
-                    for (int hh = 0; hh < G::kHalves; ++hh)
-                        tma_3d(s_q + x * G::kQBytes + hh * G::kHalfBytes, &mq, hh * 64, it.h * a.group,
-                               it.q0 + it.t0 + x * a.tq, &bars->q_full);
-            }
-            ++nq;
-            const int kv_all = it.has_b ? it.kv_end1 : it.kv_end0;
-            auto table_row = [&](int j) {
-                int r_ = a.oob_row;
-                const int pos = j * kKv + lane * a.block_size;
-                if (lane < bpt && pos < kv_all) {
-                    const int blk = it.table[pos / a.block_size];
-                    if (blk < 0 || blk >= a.num_blocks)
-                        pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
-                    else
-                        r_ = (blk * a.n_kv_heads + it.h) * a.block_size;
-                }
-                return r_;
-            };
-            int row = table_row(0);
-            for (int j = 0; j < it.n_tiles; ++j, ++g) {
-                const int ks = g % kKStages, vs = g % kVStages;
-                const uint32_t s_k = pa::smem_addr(sm + G::kK0 + ks * G::kKVBytes);
-                const uint32_t s_v = pa::smem_addr(sm + G::kV0 + vs * G::kKVBytes);
-                const uint32_t dst = lane * a.block_size * 128;
-                // both Q tiles' MMA warps release every K/V tile (used or not)
-                if (g >= kKStages)
-                    ok = wait_warp(&bars->k_empty[0][ks], (g / kKStages - 1) & 1, bars, a.status) &&
-                         wait_warp(&bars->k_empty[1][ks], (g / kKStages - 1) & 1, bars, a.status);
-                if (!ok) break;
-                if (lane == 0) pa::mbar_arrive_expect_tx(&bars->k_full[ks], G::kKVBytes);
-                __syncwarp();
-                if (lane < bpt)
-#pragma unroll
-                    for (int hh = 0; hh < G::kHalves; ++hh)
-                        tma_2d(s_k + hh * G::kHalfBytes + dst, &mk, hh * 64, row, &bars->k_full[ks]);
-                if (g >= kVStages)
-                    ok = wait_warp(&bars->v_empty[0][vs], (g / kVStages - 1) & 1, bars, a.status) &&
-                         wait_warp(&bars->v_empty[1][vs], (g / kVStages - 1) & 1, bars, a.status);
-                if (!ok) {
-                    // K of tile g is in flight, V is not
-                    if (lane == 0) pa::mbar_wait_bounded(&bars->k_full[ks], (g / kKStages) & 1, kMaxProbes);
+            if (is_k) {
+                int i = 0;
+                if (lane == 0) i = a.sched ? atomicAdd(a.sched, 1) : (int)blockIdx.x + k * (int)gridDim.x;
+                i = __shfl_sync(0xffffffffu, i, 0);
+                if (i >= n_items) {
+                    post(-1);
                     break;
                 }
-                if (lane == 0) pa::mbar_arrive_expect_tx(&bars->v_full[vs], G::kKVBytes);
-                __syncwarp();
-                if (lane < bpt)
+                if (!decode_item(i, a, it, lane == 0)) continue;
+                ok = post(i);
+                if (!ok) break;
+                // Q of this item replaces the previous item's once both tiles'
+                // last score products are done
+                if (c >= 1)
+                    ok = wait_warp(&bars->q_empty[0], (c - 1) & 1, bars, a.status) &&
+                         wait_warp(&bars->q_empty[1], (c - 1) & 1, bars, a.status);
+                if (!ok) break;
+                if (lane == 0) {
+                    pa::mbar_arrive_expect_tx(&bars->q_full, (it.has_b ? 2 : 1) * G::kQBytes);
+                    for (int x = 0; x < (it.has_b ? 2 : 1); ++x)
 #pragma unroll
-                    for (int hh = 0; hh < G::kHalves; ++hh)
-                        tma_2d(s_v + hh * G::kHalfBytes + dst, &mv, hh * 64, row, &bars->v_full[vs]);
-                if (j + 1 < it.n_tiles) row = table_row(j + 1);
+                        for (int hh = 0; hh < G::kHalves; ++hh)
+                            tma_3d(s_q + x * G::kQBytes + hh * G::kHalfBytes, &mq, hh * 64, it.h * a.group,
+                                   it.q0 + it.t0 + x * a.tq, &bars->q_full);
+                }
+                ++nq;
+            } else {
+                const int slot = np % kRing;
+                ok = wait_warp(&bars->item_full[slot], (np / kRing) & 1, bars, a.status);
+                if (!ok) break;
+                const int i = *reinterpret_cast<volatile int*>(&bars->item[slot]);
+                __syncwarp();
+                if (lane == 0) pa::mbar_arrive(&bars->item_empty[slot]);
+                ++np;
+                if (i < 0) break;
+                decode_item(i, a, it, false);
+            }
+            const int kv_all = it.has_b ? it.kv_end1 : it.kv_end0;
+            // Block-table entries are fetched kAhead tiles before their copies
+            // and checked only when used, so no copy waits on a table load.
+            constexpr int kAhead = 4;
+            constexpr int kNoBlock = INT_MIN;             // past the needed range: nothing loaded
+            auto fetch = [&](int j) {
+                const int pos = j * kKv + lane * a.block_size;
+                return (lane < bpt && pos < kv_all) ? __ldg(it.table + pos / a.block_size) : kNoBlock;
+            };
+            auto to_row = [&](int blk) {
+                if (blk == kNoBlock) return a.oob_row;
+                if (blk < 0 || blk >= a.num_blocks) {
+                    if (is_k) pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
+                    return a.oob_row;
+                }
+                return (blk * a.n_kv_heads + it.h) * a.block_size;
+            };
+            int blks[kAhead];
+#pragma unroll
+            for (int u = 0; u < kAhead; ++u) blks[u] = fetch(u);
+            uint64_t* full = is_k ? bars->k_full : bars->v_full;
+            uint64_t* empty0 = is_k ? bars->k_empty[0] : bars->v_empty[0];
+            uint64_t* empty1 = is_k ? bars->k_empty[1] : bars->v_empty[1];
+            const CUtensorMap* map = is_k ? &mk : &mv;
+            const int stages = is_k ? kKStages : kVStages;
+            const int base = is_k ? G::kK0 : G::kV0;
+            for (int j0 = 0; ok && j0 < it.n_tiles; j0 += kAhead) {
+#pragma unroll
+                for (int u = 0; u < kAhead; ++u) {
+                    const int j = j0 + u;
+                    if (j >= it.n_tiles) break;
+                    const int row = to_row(blks[u]);
+                    blks[u] = fetch(j + kAhead);
+                    const int st = g % stages;
+                    const uint32_t s_t = pa::smem_addr(sm + base + st * G::kKVBytes) + lane * a.block_size * 128;
+                    // both Q tiles' MMA warps release every K/V tile (used or not)
+                    if (g >= stages)
+                        ok = wait_warp(&empty0[st], (g / stages - 1) & 1, bars, a.status) &&
+                             wait_warp(&empty1[st], (g / stages - 1) & 1, bars, a.status);
+                    if (!ok) break;
+                    if (lane == 0) pa::mbar_arrive_expect_tx(&full[st], G::kKVBytes);
+                    __syncwarp();
+                    if (lane < bpt)
+#pragma unroll
+                        for (int hh = 0; hh < G::kHalves; ++hh)
+                            tma_2d(s_t + hh * G::kHalfBytes, map, hh * 64, row, &full[st]);
+                    ++g;
+                }
             }
             ++c;
         }
@@ -480,13 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // last use of each stage (earlier uses completed before it was reused)
         if (lane == 0) {
             if (nq) pa::mbar_wait_bounded(&bars->q_full, (nq - 1) & 1, kMaxProbes);
-            for (int i = 0; i < kKStages && i < g; ++i) {
+            uint64_t* full = is_k ? bars->k_full : bars->v_full;
+            const int stages = is_k ? kKStages : kVStages;
+            for (int i = 0; i < stages && i < g; ++i) {
                 const int t = g - 1 - i;
-                pa::mbar_wait_bounded(&bars->k_full[t % kKStages], (t / kKStages) & 1, kMaxProbes);
-            }
-            for (int i = 0; i < kVStages && i < g; ++i) {
-                const int t = g - 1 - i;
-                pa::mbar_wait_bounded(&bars->v_full[t % kVStages], (t / kVStages) & 1, kMaxProbes);
+                pa::mbar_wait_bounded(&full[t % stages], (t / stages) & 1, kMaxProbes);
             }
         }
     } else if (warp == kMmaWarp0 || warp == kMmaWarp0 + 1) {
