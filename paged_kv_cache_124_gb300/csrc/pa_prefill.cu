@@ -111,6 +111,15 @@ struct PrefillArgs {
     int* sched;           // {next item, CTAs done} claimed with atomics, or null: fixed order
 };
 
+// One work item: query rows [t0, t0 + 2 tq) of sequence seq's n new tokens
+// (Q tiles A and B; has_b = 0: A only) and KV head h; tile x sees keys
+// [0, kv_end_x), nt_x tiles of them, n_tiles in all.  The producer decodes
+// it once and posts it; seq < 0 ends the stream.
+struct Item {
+    int seq, h, q0, n, ctx, t0;
+    int kv_end0, kv_end1, nt0, nt1, n_tiles, has_b;
+};
+
 struct Bars {
     uint64_t q_full;
     uint64_t k_full[kKStages];
@@ -125,7 +134,7 @@ struct Bars {
     uint64_t red[2];      // per Q tile: both halves of every row posted their value
     uint64_t item_full[kRing];    // the producer posted the next work item
     uint64_t item_empty[kRing];   // every consumer warp has read it
-    int item[kRing];
+    Item item[kRing];
     uint32_t tmem_base;
     int abort;
 };
@@ -284,12 +293,6 @@ __device__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* b, int32_t* stat
 
 // One work item: 2 x 128 query rows (Q tiles A, B) of one KV head of one
 // sequence.  Every role of a CTA decodes the same items in the same order.
-struct Item {
-    int seq, h, q0, n, ctx, t0;
-    int kv_end0, kv_end1, nt0, nt1, n_tiles;
-    bool has_b;
-    const int* table;
-};
 
 // Item i of the heavy-first order (latest token tiles first); false when it
 // holds no query row (past the sequence's new tokens) or is invalid.
@@ -312,14 +315,23 @@ __device__ __forceinline__ bool decode_item(int i, const PrefillArgs& a, Item& i
         if (flag) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
         return false;
     }
-    it.has_b = it.t0 + a.tq < it.n;
+    it.has_b = it.t0 + a.tq < it.n ? 1 : 0;
     it.kv_end0 = it.ctx - it.n + min(it.n, it.t0 + a.tq);
     it.kv_end1 = it.ctx - it.n + min(it.n, it.t0 + 2 * a.tq);
     it.nt0 = (it.kv_end0 + kKv - 1) / kKv;
     it.nt1 = it.has_b ? (it.kv_end1 + kKv - 1) / kKv : 0;
     it.n_tiles = it.has_b ? it.nt1 : it.nt0;
-    it.table = a.block_tables + (size_t)it.seq * a.max_blocks;
     return true;
+}
+
+// A posted ring entry, read once its item_full phase has completed.
+__device__ __forceinline__ Item read_item(const Item* src) {
+    const volatile int* p = reinterpret_cast<const volatile int*>(src);
+    Item it;
+    int* d = reinterpret_cast<int*>(&it);
+#pragma unroll
+    for (int k = 0; k < (int)(sizeof(Item) / sizeof(int)); ++k) d[k] = p[k];
+    return it;
 }
 
 // Twelve warps on four SM sub-partitions: three share one 16K-register file,
@@ -390,13 +402,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0, c = 0;                                 // K/V tiles and items so far
         int nq = 0, np = 0;                               // Q copies issued, ring entries posted (K) or read (V)
         bool ok = true;
-        // post item i (-1: no more) to the other warps
-        auto post = [&](int i) {
+        // post an item (seq < 0: no more) to the other warps
+        auto post = [&](const Item& it) {
             const int slot = np % kRing;
             if (np >= kRing && !wait_warp(&bars->item_empty[slot], (np / kRing - 1) & 1, bars, a.status))
                 return false;
             if (lane == 0) {
-                *reinterpret_cast<volatile int*>(&bars->item[slot]) = i;
+                volatile int* d = reinterpret_cast<volatile int*>(&bars->item[slot]);
+                const int* s_ = reinterpret_cast<const int*>(&it);
+#pragma unroll
+                for (int k = 0; k < (int)(sizeof(Item) / sizeof(int)); ++k) d[k] = s_[k];
                 pa::mbar_arrive(&bars->item_full[slot]);
             }
             ++np;
@@ -412,11 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) i = a.sched ? atomicAdd(a.sched, 1) : (int)blockIdx.x + k * (int)gridDim.x;
                 i = __shfl_sync(0xffffffffu, i, 0);
                 if (i >= n_items) {
-                    post(-1);
+                    it.seq = -1;
+                    post(it);
                     break;
                 }
                 if (!decode_item(i, a, it, lane == 0)) continue;
-                ok = post(i);
+                ok = post(it);
                 if (!ok) break;
                 // Q of this item replaces the previous item's once both tiles'
                 // last score products are done
@@ -437,21 +453,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = np % kRing;
                 ok = wait_warp(&bars->item_full[slot], (np / kRing) & 1, bars, a.status);
                 if (!ok) break;
-                const int i = *reinterpret_cast<volatile int*>(&bars->item[slot]);
+                it = read_item(&bars->item[slot]);
                 __syncwarp();
                 if (lane == 0) pa::mbar_arrive(&bars->item_empty[slot]);
                 ++np;
-                if (i < 0) break;
-                decode_item(i, a, it, false);
+                if (it.seq < 0) break;
             }
             const int kv_all = it.has_b ? it.kv_end1 : it.kv_end0;
+            const int32_t* table = a.block_tables + (size_t)it.seq * a.max_blocks;
             // Block-table entries are fetched kAhead tiles before their copies
             // and checked only when used, so no copy waits on a table load.
             constexpr int kAhead = 4;
             constexpr int kNoBlock = INT_MIN;             // past the needed range: nothing loaded
             auto fetch = [&](int j) {
                 const int pos = j * kKv + lane * a.block_size;
-                return (lane < bpt && pos < kv_all) ? __ldg(it.table + pos / a.block_size) : kNoBlock;
+                return (lane < bpt && pos < kv_all) ? __ldg(table + pos / a.block_size) : kNoBlock;
             };
             auto to_row = [&](int blk) {
                 if (blk == kNoBlock) return a.oob_row;
@@ -548,11 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot = nc % kRing;
                 ok = wait1(&bars->item_full[slot], (nc / kRing) & 1, bars, a.status);
                 if (!ok) break;
-                const int i = *reinterpret_cast<volatile int*>(&bars->item[slot]);
+                const Item it = read_item(&bars->item[slot]);
                 pa::mbar_arrive(&bars->item_empty[slot]);
-                if (i < 0) break;
-                Item it;
-                decode_item(i, a, it, false);
+                if (it.seq < 0) break;
                 const int ntx = x ? it.nt1 : it.nt0;
                 const int kv_endx = x ? it.kv_end1 : it.kv_end0;
                 if (ntx == 0) {
@@ -658,12 +672,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = nc % kRing;
             ok = wait_warp(&bars->item_full[slot], (nc / kRing) & 1, bars, a.status);
             if (!ok) break;
-            const int i = *reinterpret_cast<volatile int*>(&bars->item[slot]);
+            const Item it = read_item(&bars->item[slot]);
             __syncwarp();
             if (lane == 0) pa::mbar_arrive(&bars->item_empty[slot]);
-            if (i < 0) break;
-            Item it;
-            decode_item(i, a, it, false);
+            if (it.seq < 0) break;
             const int nt[2] = {it.nt0, it.nt1};
             float m_used[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
             int row_lim[2];
