@@ -467,7 +467,7 @@ def run_prefill_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     ev_start.record(stream)
     for i in range(K):
-        cache_write(k_new, v_new, slots, stream)
+        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
         if i % SAMPLE == 0:
             a, b = ev_att[i // SAMPLE]
             a.record(stream)

@@ -256,12 +256,12 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
  *   n_q_heads / n_kv_heads must be a power of two <= 128; d_head 64 or 128;
  *   block_size 8, 16 or 32.
  *   sched_dev     optional device int32 [2], zero before the first call; the
- *                 kernel's blocks claim work items from it (the latest query
- *                 rows, which see the most keys, first) and the last block
- *                 to finish zeroes it again.  Calls that
- *                 share one pair must be ordered (one stream).  NULL: a fixed
- *                 round-robin assignment, slower when sequences differ in
- *                 length.  Caller-owned.
+ *                 kernel's blocks claim work items from it (KV head by KV
+ *                 head, within a head the latest query rows, which see the
+ *                 most keys, first) and the last block to finish zeroes it
+ *                 again.  Calls that share one pair must be ordered (one
+ *                 stream).  NULL: a fixed round-robin assignment, slower when
+ *                 sequences differ in length.  Caller-owned.
  *   status_dev    optional device int32, see PA_DEV_* above.
  * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED or
  * PA_ERR_CUDA.

@@ -99,6 +99,7 @@ struct PrefillArgs {
     int num_seqs;
     int num_tokens;
     int tiles_per_seq;    // work items per sequence and KV head (each covers 2 * tq tokens)
+    int heads_per_group;  // KV heads whose items are claimed together
     int block_size;
     int n_kv_heads;
     int group;            // query heads per KV head
@@ -294,14 +295,21 @@ __device__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* b, int32_t* stat
 // One work item: 2 x 128 query rows (Q tiles A, B) of one KV head of one
 // sequence.  Every role of a CTA decodes the same items in the same order.
 
-// Item i of the heavy-first order (latest token tiles first); false when it
-// holds no query row (past the sequence's new tokens) or is invalid.
+// Item i of the claim order: by group of KV heads, and within a group the
+// latest token tiles (the most keys) first.  The CTAs then work on a few
+// heads' K/V at a time, which stays in L2 while every tile of it is read; a
+// group holds at least two items per CTA, so that its lightest items, not
+// heavy ones, end each group.  False when the item holds no query row (past
+// the sequence's new tokens) or is invalid.
 __device__ __forceinline__ bool decode_item(int i, const PrefillArgs& a, Item& it, bool flag) {
-    const int per_tile = a.num_seqs * a.n_kv_heads;
-    const int tile = a.tiles_per_seq - 1 - i / per_tile;
-    const int r = i - (i / per_tile) * per_tile;
-    it.seq = r % a.num_seqs;
-    it.h = r / a.num_seqs;
+    const int per_group = a.tiles_per_seq * a.num_seqs * a.heads_per_group;
+    const int grp = i / per_group;
+    const int r = i - grp * per_group;
+    const int per_tile = a.num_seqs * min(a.heads_per_group, a.n_kv_heads - grp * a.heads_per_group);
+    const int tile = a.tiles_per_seq - 1 - r / per_tile;
+    const int r2 = r % per_tile;
+    it.seq = r2 % a.num_seqs;
+    it.h = grp * a.heads_per_group + r2 / a.num_seqs;
     it.q0 = a.query_start[it.seq];
     it.n = a.query_start[it.seq + 1] - it.q0;
     it.ctx = a.context_lens[it.seq];
@@ -417,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++np;
             return true;
         };
-        // Items are claimed in heavy-first order, from a counter shared by
+        // Items are claimed in decode_item's order, from a counter shared by
         // all CTAs (the next free CTA takes the next item) or, without one,
         // round-robin.
         for (int k = 0; ok; ++k) {
@@ -927,6 +935,9 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     if (items > INT_MAX - 4096) return PA_ERR_UNSUPPORTED;    // claims run past the last item by one per CTA
     const int sms = num_sms();
     const dim3 grid((unsigned)(items < sms ? items : sms));
+    const long long per_head = tiles * num_seqs;
+    long long hpg = (2LL * grid.x + per_head - 1) / per_head;
+    a.heads_per_group = (int)(hpg < 1 ? 1 : hpg > n_kv_heads ? n_kv_heads : hpg);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return d_head == 128 ? launch<128>(a, q, k_cache, v_cache, num_tokens, cache_rows, grid, st)
                          : launch<64>(a, q, k_cache, v_cache, num_tokens, cache_rows, grid, st);
