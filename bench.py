@@ -48,6 +48,8 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_partition_kernel_batch64_8b.md")
 KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_decode.cu")
 PREFILL_PROFILE = os.path.join(ROOT, "profiles", "prefill_kernel_prefill_prompts_8b.md")
+CACHE_OPS_PROFILE = os.path.join(ROOT, "profiles", "copy_blocks_kernel_cache_ops_8b.md")
+CACHE_OPS_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_cache_ops.cu")
 PREFILL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_prefill.cu")
 
 PREFILL_METRIC = "paged prefill-attn TFLOP/s (causal, 8B GQA shape; frac of bf16 tensor peak)"
@@ -796,6 +798,177 @@ def swap_cpu_baseline(sc, budget_s):
                       % (nb, moved, t)}
 
 
+CACHE_OPS_METRIC = "paged KV cache write + CoW copy GB/s (HBM bytes read + written, frac of measured HBM)"
+CACHE_OPS_LAYERS = 32          # copy_blocks copies a block in every layer of the 8B model
+
+
+def _cache_ops_inputs(seed, block_size, api):
+    """The 16 x 2,003-token prompts of the CoW sampling config: their new K/V
+    rows and slots (block manager, seeded free order), and the copy-on-write
+    pairs that forking each prompt into 8 samples and appending one token to
+    every sample produces (the first 7 writers of each shared tail copy it)."""
+    sc = I.prefill_prompts(seed, block_size)
+    _, _, slots = _prefill_metadata(sc, api)
+    n_prompts, samples = len(sc.ctxs), 8
+    alloc = api.BlockAllocator(sc.num_blocks + n_prompts * samples, block_size)
+    assert alloc.set_free_order(list(sc.free_order) + list(range(sc.num_blocks, sc.num_blocks + n_prompts * samples))) == 0
+    pairs = []
+    for s_, c in enumerate(sc.ctxs):
+        assert alloc.allocate(s_ * samples, c) == 0
+        for f in range(1, samples):
+            assert alloc.fork(s_ * samples, s_ * samples + f) == 0
+    for s_ in range(n_prompts * samples):
+        st, _, src, dst = alloc.append_slot(s_)
+        assert st == 0
+        if src >= 0:
+            pairs.append((src, dst))
+    return sc, slots, np.asarray(pairs, dtype=np.int32), sc.num_blocks + n_prompts * samples
+
+
+def run_cache_ops_ours(args, world, rank, local):
+    from paged_kv_cache_124_gb300 import api
+
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    seed = replica_seed(args.seed, rank)
+    sc, slots_h, pairs_h, nb = _cache_ops_inputs(seed, args.block_size, api)
+    L = CACHE_OPS_LAYERS
+    shape = (nb, sc.n_kv_heads, sc.block_size, sc.d_head)
+    g = torch.Generator(device=dev).manual_seed(seed)
+    kc = [torch.randn(shape, generator=g, device=dev).bfloat16() for _ in range(L)]
+    vc = [torch.randn(shape, generator=g, device=dev).bfloat16() for _ in range(L)]
+    k_new, v_new = I.prefill_new_kv(sc, dev)
+    slots = torch.from_numpy(slots_h).to(dev)
+    pairs = torch.from_numpy(pairs_h).to(dev)
+    T, P = int(slots_h.shape[0]), int(pairs_h.shape[0])
+    row = sc.n_kv_heads * sc.d_head * 2
+    write_bytes = 2 * T * row * 2 + T * 8                         # K and V rows read and written, slots read
+    # K and V blocks: each distinct source read once (its copies to several
+    # destinations reread it from L2), each destination written once
+    blk_kv = 2 * sc.n_kv_heads * sc.block_size * sc.d_head * 2
+    copy_bytes = (len(set(pairs_h[:, 0].tolist())) + P) * L * blk_kv
+    stream = torch.cuda.current_stream(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(k_, v_, slots_, pairs_):
+        api.pa_reshape_and_cache(kc[0], vc[0], k_, v_, slots_, status=status, stream=stream)
+        api.pa_copy_blocks(kc, vc, pairs_, status=status, stream=stream)
+
+    for _ in range(args.warmup):
+        step(k_new, v_new, slots, pairs)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        a, b, c = ev[i]
+        a.record(stream)
+        api.pa_reshape_and_cache(kc[0], vc[0], k_new, v_new, slots, status=status, stream=stream)
+        b.record(stream)
+        api.pa_copy_blocks(kc, vc, pairs, status=status, stream=stream)
+        c.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    w_s = float(np.mean([a.elapsed_time(b) for a, b, _ in ev])) / 1e3
+    c_s = float(np.mean([b.elapsed_time(c) for _, b, c in ev])) / 1e3
+    total = ev[0][0].elapsed_time(ev[-1][2]) / 1e3
+    total_s, total_bytes = reduce_timing(total, K * (write_bytes + copy_bytes), world, dev)
+    if int(status.item()) != 0:
+        raise RuntimeError("cache ops flagged status %d" % int(status.item()))
+    # e2e through the same calls with host inputs: new K/V rows, slots and pairs copied in, the status word read back
+    hk, hv = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    hs, hp = torch.from_numpy(slots_h).pin_memory(), torch.from_numpy(pairs_h).pin_memory()
+    hst = torch.zeros(1, dtype=torch.int32).pin_memory()
+    dk, dv, ds, dp = torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(slots), torch.empty_like(pairs)
+    h2d = hk.numel() * 2 + hv.numel() * 2 + hs.numel() * 8 + hp.numel() * 4
+
+    def e2e_step():
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ds.copy_(hs, non_blocking=True)
+        dp.copy_(hp, non_blocking=True)
+        step(dk, dv, ds, dp)
+        hst.copy_(status, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    KE = max(3, K // 4)
+    e0.record(stream)
+    for _ in range(KE):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s, _ = reduce_timing(e0.elapsed_time(e1) / 1e3, 0, world, dev)
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak("hbm_gbs", FALLBACK_HBM_GBS)
+    copy_gbs, write_gbs = copy_bytes / c_s / 1e9, write_bytes / w_s / 1e9
+    line = {
+        "metric": CACHE_OPS_METRIC, "value": round(total_bytes / total_s / 1e9, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bit copies)", "data": "synthetic",
+        "config": {"workload": "cache_ops_8b", "tokens_written": T, "cow_pairs": P,
+                   "distinct_sources": len(set(pairs_h[:, 0].tolist())), "layers_copied": L,
+                   "n_kv_heads": sc.n_kv_heads, "d_head": sc.d_head, "block_size": sc.block_size,
+                   "pool_blocks_per_layer": nb,
+                   "step": "pa_reshape_and_cache of the 16 x 2,003 prompt tokens (one layer) + pa_copy_blocks of the "
+                           "copy-on-write pairs of forking each prompt into 8 samples (all %d layers)" % L,
+                   "l2": "%.0f MB written and %.0f MB copied per step (> 129 MB L2); no flush"
+                         % (write_bytes / 1e6, copy_bytes / 1e6)},
+        "roofline": {"bound": "hbm", "kernel": "copy_blocks_kernel", "achieved": round(copy_gbs, 1), "peak": peak,
+                     "peak_kind": peak_kind + " copy (read + write bytes)", "unit": "GB/s",
+                     "frac": round(copy_gbs / peak, 4),
+                     "traffic": profiled_traffic(CACHE_OPS_PROFILE, CACHE_OPS_SOURCE),
+                     "algorithmic_bytes_per_launch": copy_bytes, "avg_launch_us": round(c_s * 1e6, 2)},
+        "roofline_reshape_and_cache": {"bound": "hbm", "kernel": "reshape_and_cache_kernel",
+                                       "achieved": round(write_gbs, 1), "peak": peak, "unit": "GB/s",
+                                       "frac": round(write_gbs / peak, 4), "algorithmic_bytes_per_launch": write_bytes,
+                                       "avg_launch_us": round(w_s * 1e6, 2)},
+        "e2e": {"value": round((write_bytes + copy_bytes) / e2e_s * KE / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4, "ms_per_step": round(e2e_s / KE * 1e3, 4)},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cache_ops_cpu_baseline(sc, slots_h, pairs_h, nb, args.cpu_seconds)
+    return line
+
+
+def cache_ops_cpu_baseline(sc, slots_h, pairs_h, nb, budget_s):
+    """The oracle's reshape_and_cache and copy_blocks (plain loops over host
+    pools of the same shape), as many tokens and pairs as fit about budget_s;
+    bytes counted like the GPU's (read + written)."""
+    from oracle import cache_ops as C
+    rng = np.random.default_rng(0)
+    shape = (nb, sc.n_kv_heads, sc.block_size, sc.d_head)
+    kc = rng.integers(0, 65535, size=shape, dtype=np.uint16)
+    vc = kc.copy()
+    n_tok = 4096
+    k = rng.integers(0, 65535, size=(n_tok, sc.n_kv_heads, sc.d_head), dtype=np.uint16)
+    v = k.copy()
+    row = sc.n_kv_heads * sc.d_head * 2
+    blk = sc.n_kv_heads * sc.block_size * sc.d_head * 2
+    moved, t = 0, 0.0
+    t0 = time.perf_counter()
+    while t < budget_s:
+        C.reshape_and_cache(kc, vc, k, v, slots_h[:n_tok], sc.block_size)
+        C.copy_blocks([kc], [vc], [tuple(p) for p in pairs_h.tolist()])
+        moved += 2 * n_tok * row * 2 + 2 * len(pairs_h) * blk * 2
+        t = time.perf_counter() - t0
+    return {"value": round(moved / t / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "oracle reshape_and_cache of %d tokens + copy_blocks of %d pairs (one layer) per round, "
+                      "host pools of %d blocks, %.1f s" % (n_tok, len(pairs_h), nb, t)}
+
+
 # ----------------------------------------------------------------------------
 # CPU oracle (the cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------
@@ -869,7 +1042,7 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(PREFILL_WORKLOADS) + ["swap_8b"],
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(PREFILL_WORKLOADS) + ["swap_8b", "cache_ops_8b"],
                    default="batch64_8b")
     p.add_argument("--block-size", type=int, default=16)
     p.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
@@ -884,7 +1057,21 @@ def main(argv=None):
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     prefill = args.workload in PREFILL_WORKLOADS
-    if args.workload == "swap_8b":
+    if args.workload == "cache_ops_8b":
+        if args.impl == "reference":
+            line = None
+            if rank == 0:
+                from paged_kv_cache_124_gb300 import api
+                sc, slots_h, pairs_h, nb = _cache_ops_inputs(args.seed, args.block_size, api)
+                cb = cache_ops_cpu_baseline(sc, slots_h, pairs_h, nb, args.cpu_seconds)
+                line = {"impl": "reference", "metric": CACHE_OPS_METRIC, "value": cb["value"], "unit": "GB/s",
+                        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (bit copies)", "data": "synthetic",
+                        "config": {"workload": "cache_ops_8b"}, "cpu_baseline": cb,
+                        "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        else:
+            line = run_cache_ops_ours(args, world, rank, local)
+    elif args.workload == "swap_8b":
         if args.impl == "reference":
             line = None
             if rank == 0:
