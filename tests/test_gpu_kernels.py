@@ -31,10 +31,12 @@ def _bf16_bits_normal(rng, shape):
 # reshape_and_cache / copy_blocks: bit-exact, whole pool
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("D,B,Hkv,T", [(64, 16, 2, 5), (128, 8, 8, 300), (128, 32, 4, 77), (64, 8, 1, 1)])
+# 8,193 and 10,003 tokens: calls of prefill size
+@pytest.mark.parametrize("D,B,Hkv,T", [(64, 16, 2, 5), (128, 8, 8, 300), (128, 32, 4, 77), (64, 8, 1, 1),
+                                       (128, 16, 8, 8193), (64, 8, 2, 10003)])
 def test_reshape_and_cache_bit_exact(D, B, Hkv, T):
     rng = np.random.default_rng(D + B + T)
-    NB = 40
+    NB = max(40, -(-T // B) + 10)
     kc = _rand_bits(rng, (NB, Hkv, B, D))          # every bit pattern, NaNs included
     vc = _rand_bits(rng, (NB, Hkv, B, D))
     k = _rand_bits(rng, (T, Hkv, D))
@@ -63,6 +65,29 @@ def test_reshape_and_cache_out_of_range_slot_is_skipped_and_flagged():
     torch.cuda.synchronize()
     assert st.item() == api.PA_DEV_BAD_SLOT
     assert np.array_equal(to_bits(kd), kc)
+
+
+def test_reshape_and_cache_bad_slot_in_a_shared_block_skips_only_that_token():
+    """A bad slot and a padding token among thousands of good ones are
+    skipped alone."""
+    rng = np.random.default_rng(5)
+    NB, Hkv, B, D, T = 700, 2, 16, 64, 8195
+    kc = _rand_bits(rng, (NB, Hkv, B, D))
+    vc = _rand_bits(rng, (NB, Hkv, B, D))
+    k = _rand_bits(rng, (T, Hkv, D))
+    v = _rand_bits(rng, (T, Hkv, D))
+    slots = rng.permutation(NB * B)[:T].astype(np.int64)
+    slots[4101] = NB * B + 7                       # outside the pool
+    slots[4102] = -1                               # padding
+    kd, vd = from_bits(kc), from_bits(vc)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.pa_reshape_and_cache(kd, vd, from_bits(k), from_bits(v), torch.from_numpy(slots).cuda(), status=st)
+    want = slots.copy()
+    want[4101] = -1
+    C.reshape_and_cache(kc, vc, k, v, want, B)
+    torch.cuda.synchronize()
+    assert st.item() == api.PA_DEV_BAD_SLOT
+    assert np.array_equal(to_bits(kd), kc) and np.array_equal(to_bits(vd), vc)
 
 
 def test_reshape_and_cache_empty_is_noop():
