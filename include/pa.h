@@ -298,6 +298,18 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* k,
                          int block_size, int num_blocks, int32_t* status_dev,
                          void* stream);
 
+/* pa_reshape_and_cache for FP8 caches: each element x of k (v) is stored as
+ * the E4M3 code of float32(x) / k_scale (v_scale): IEEE float32 division,
+ * then round to nearest even, saturating at +-448, NaN kept.  k, v are bf16
+ * [num_tokens][n_kv_heads][d_head] as for pa_reshape_and_cache; the caches
+ * are bytes [num_blocks][n_kv_heads][block_size][d_head].  Scales must be
+ * finite and > 0 (PA_ERR_INVALID_ARG). */
+int pa_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* k,
+                             const void* v, const int64_t* slot_mapping,
+                             int num_tokens, int n_kv_heads, int d_head,
+                             int block_size, int num_blocks, float k_scale,
+                             float v_scale, int32_t* status_dev, void* stream);
+
 /* copy_blocks: the copy-on-write clone of a shared tail block ([P1]
  * sections 15 and 16): for every pair (src, dst) = (block_pairs[2i],
  * block_pairs[2i+1]) and every layer l, block dst of k_caches[l] and
@@ -312,22 +324,19 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* k,
  * num_pairs == 0 or num_layers == 0 is a no-op returning PA_OK.
  * Must be ordered before the reshape_and_cache that writes into dst in the
  * same step (same stream, earlier launch). */
-/* pa_reshape_and_cache for FP8 caches: each element x of k (v) is stored as
- * the E4M3 code of float32(x) / k_scale (v_scale): IEEE float32 division,
- * then round to nearest even, saturating at +-448, NaN kept.  k, v are bf16
- * [num_tokens][n_kv_heads][d_head] as for pa_reshape_and_cache; the caches
- * are bytes [num_blocks][n_kv_heads][block_size][d_head].  Scales must be
- * finite and > 0 (PA_ERR_INVALID_ARG). */
-int pa_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* k,
-                             const void* v, const int64_t* slot_mapping,
-                             int num_tokens, int n_kv_heads, int d_head,
-                             int block_size, int num_blocks, float k_scale,
-                             float v_scale, int32_t* status_dev, void* stream);
-
 int pa_copy_blocks(void* const* k_caches, void* const* v_caches,
                    int num_layers, const int32_t* block_pairs, int num_pairs,
                    int n_kv_heads, int d_head, int block_size, int num_blocks,
                    int32_t* status_dev, void* stream);
+
+/* pa_copy_blocks for FP8 caches: the same copy of whole blocks, each cache
+ * bytes [num_blocks][n_kv_heads][block_size][d_head] (E4M3 codes; the copy
+ * is of bits, so any one-byte element type serves). */
+int pa_copy_blocks_fp8(void* const* k_caches, void* const* v_caches,
+                       int num_layers, const int32_t* block_pairs,
+                       int num_pairs, int n_kv_heads, int d_head,
+                       int block_size, int num_blocks, int32_t* status_dev,
+                       void* stream);
 
 /* Copy whole blocks between two pools with the cache layout: for every pair
  * (src, dst) in block_pairs and every layer, the K block src of src_k[l] goes
@@ -352,6 +361,16 @@ int pa_swap_blocks(void* const* dst_k, void* const* dst_v,
                    int n_kv_heads, int d_head, int block_size,
                    int src_num_blocks, int dst_num_blocks,
                    int32_t* status_dev, void* stream);
+
+/* pa_swap_blocks for FP8 caches: pools of bytes
+ * [num_blocks][n_kv_heads][block_size][d_head] (E4M3 codes) on either side;
+ * everything else as for pa_swap_blocks. */
+int pa_swap_blocks_fp8(void* const* dst_k, void* const* dst_v,
+                       const void* const* src_k, const void* const* src_v,
+                       int num_layers, const int32_t* block_pairs,
+                       int num_pairs, int n_kv_heads, int d_head,
+                       int block_size, int src_num_blocks, int dst_num_blocks,
+                       int32_t* status_dev, void* stream);
 
 /* ===========================================================================
  * Host block manager ([P1] sections 14-17 and 20)

@@ -79,6 +79,8 @@ _SIGS = {
                                       _vp]),
     "pa_copy_blocks": (_c_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _c_int, _vp, _c_int, _c_int, _c_int,
                                 _c_int, _c_int, _vp, _vp]),
+    "pa_copy_blocks_fp8": (_c_int, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _c_int, _vp, _c_int, _c_int, _c_int,
+                                    _c_int, _c_int, _vp, _vp]),
     "pa_alloc_create": (_vp, [_c_int, _c_int]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_set_free_order": (_c_int, [_vp, _i32p, _c_int]),
@@ -107,6 +109,8 @@ _SIGS = {
     "pa_alloc_is_swapped": (_c_int, [_vp, ctypes.c_int64]),
     "pa_swap_blocks": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                 _vp]),
+    "pa_swap_blocks_fp8": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                    _vp, _vp]),
     "pa_alloc_cached_list": (_c_int, [_vp, _i32p, _c_int]),
 }
 
@@ -375,7 +379,8 @@ def pa_reshape_and_cache(k_cache, v_cache, k, v, slot_mapping, status=None, stre
 
 def pa_copy_blocks(k_caches, v_caches, block_pairs, status=None, stream=None):
     """For every (src, dst) row of block_pairs (int32 [P, 2], device) copy
-    block src onto block dst in every layer's caches."""
+    block src onto block dst in every layer's caches (bf16, or uint8 E4M3
+    codes: pa_copy_blocks_fp8)."""
     L = len(k_caches)
     if len(v_caches) != L:
         raise ValueError("k_caches and v_caches must have the same length")
@@ -386,11 +391,14 @@ def pa_copy_blocks(k_caches, v_caches, block_pairs, status=None, stream=None):
     for t in list(k_caches) + list(v_caches):
         if tuple(t.shape) != (NB, Hkv, B, D):
             raise ValueError("all caches must share one shape")
-    kp = (ctypes.c_void_p * L)(*[_dev(t, torch.bfloat16, "k_caches[i]").value for t in k_caches])
-    vp = (ctypes.c_void_p * L)(*[_dev(t, torch.bfloat16, "v_caches[i]").value for t in v_caches])
-    st = _lib.pa_copy_blocks(kp, vp, L, _dev(block_pairs, torch.int32, "block_pairs"), int(P), int(Hkv), int(D),
-                             int(B), int(NB), _opt_dev(status, torch.int32, "status"), _stream(stream))
-    return _check(st, "pa_copy_blocks")
+    fp8 = k_caches[0].dtype == torch.uint8
+    dt = torch.uint8 if fp8 else torch.bfloat16
+    fn = _lib.pa_copy_blocks_fp8 if fp8 else _lib.pa_copy_blocks
+    kp = (ctypes.c_void_p * L)(*[_dev(t, dt, "k_caches[i]").value for t in k_caches])
+    vp = (ctypes.c_void_p * L)(*[_dev(t, dt, "v_caches[i]").value for t in v_caches])
+    st = fn(kp, vp, L, _dev(block_pairs, torch.int32, "block_pairs"), int(P), int(Hkv), int(D),
+            int(B), int(NB), _opt_dev(status, torch.int32, "status"), _stream(stream))
+    return _check(st, "pa_copy_blocks_fp8" if fp8 else "pa_copy_blocks")
 
 
 def _dev_or_pinned(t, dtype, name):
@@ -409,8 +417,9 @@ def _dev_or_pinned(t, dtype, name):
 def pa_swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs, status=None, stream=None):
     """For every (src, dst) row of block_pairs (int32 [P, 2]) copy block src
     of every src pool onto block dst of the matching dst pool.  Pools are
-    lists (one per layer) of CUDA or pinned host bf16 tensors
-    [num_blocks, Hkv, B, D]; source and destination may differ in num_blocks."""
+    lists (one per layer) of CUDA or pinned host tensors [num_blocks, Hkv, B,
+    D], bf16 or uint8 E4M3 codes (pa_swap_blocks_fp8); source and destination
+    may differ in num_blocks."""
     L = len(src_k)
     if not (len(src_v) == len(dst_k) == len(dst_v) == L):
         raise ValueError("the four pool lists must have the same length")
@@ -425,11 +434,14 @@ def pa_swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs, status=None, stream=
     for t in list(dst_k) + list(dst_v):
         if tuple(t.shape) != (DNB, Hkv, B, D):
             raise ValueError("destination pools must share one shape")
-    arr = lambda ts, nm: (ctypes.c_void_p * L)(*[_dev_or_pinned(t, torch.bfloat16, nm).value for t in ts])
-    st = _lib.pa_swap_blocks(arr(dst_k, "dst_k"), arr(dst_v, "dst_v"), arr(src_k, "src_k"), arr(src_v, "src_v"), L,
-                             _dev_or_pinned(block_pairs, torch.int32, "block_pairs"), int(P), int(Hkv), int(D), int(B),
-                             int(SNB), int(DNB), _opt_dev(status, torch.int32, "status"), _stream(stream))
-    return _check(st, "pa_swap_blocks")
+    fp8 = src_k[0].dtype == torch.uint8
+    dt = torch.uint8 if fp8 else torch.bfloat16
+    fn = _lib.pa_swap_blocks_fp8 if fp8 else _lib.pa_swap_blocks
+    arr = lambda ts, nm: (ctypes.c_void_p * L)(*[_dev_or_pinned(t, dt, nm).value for t in ts])
+    st = fn(arr(dst_k, "dst_k"), arr(dst_v, "dst_v"), arr(src_k, "src_k"), arr(src_v, "src_v"), L,
+            _dev_or_pinned(block_pairs, torch.int32, "block_pairs"), int(P), int(Hkv), int(D), int(B),
+            int(SNB), int(DNB), _opt_dev(status, torch.int32, "status"), _stream(stream))
+    return _check(st, "pa_swap_blocks_fp8" if fp8 else "pa_swap_blocks")
 
 
 # ----------------------------------------------------------------------------

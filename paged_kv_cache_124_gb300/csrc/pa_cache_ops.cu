@@ -243,9 +243,16 @@ int pa_reshape_and_cache_fp8(void* k_cache, void* v_cache, const void* k, const 
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers, const int32_t* block_pairs,
-                   int num_pairs, int n_kv_heads, int d_head, int block_size, int num_blocks, int32_t* status_dev,
-                   void* stream) {
+}  // extern "C"
+
+namespace {
+
+// elem_bytes: 2 for bf16 caches, 1 for E4M3 codes; a block of one head is
+// block_size * d_head * elem_bytes bytes, a multiple of 16 for every
+// supported shape.
+int copy_blocks_impl(void* const* k_caches, void* const* v_caches, int num_layers, const int32_t* block_pairs,
+                     int num_pairs, int n_kv_heads, int d_head, int block_size, int num_blocks, int elem_bytes,
+                     int32_t* status_dev, void* stream) {
     if (num_layers < 0 || num_pairs < 0 || n_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
     if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head))
         return PA_ERR_UNSUPPORTED;
@@ -257,7 +264,7 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
         if (!pa_host::aligned16(k_caches[l]) || !pa_host::aligned16(v_caches[l])) return PA_ERR_MISALIGNED;
     }
     if (reinterpret_cast<uintptr_t>(block_pairs) & 3u) return PA_ERR_MISALIGNED;
-    const long long chunks = (long long)n_kv_heads * block_size * d_head / 8;
+    const long long chunks = (long long)n_kv_heads * block_size * d_head * elem_bytes / 16;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
         const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
@@ -273,9 +280,10 @@ int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
     return PA_OK;
 }
 
-int pa_swap_blocks(void* const* dst_k, void* const* dst_v, const void* const* src_k, const void* const* src_v,
-                   int num_layers, const int32_t* block_pairs, int num_pairs, int n_kv_heads, int d_head, int block_size,
-                   int src_num_blocks, int dst_num_blocks, int32_t* status_dev, void* stream) {
+int swap_blocks_impl(void* const* dst_k, void* const* dst_v, const void* const* src_k, const void* const* src_v,
+                     int num_layers, const int32_t* block_pairs, int num_pairs, int n_kv_heads, int d_head,
+                     int block_size, int src_num_blocks, int dst_num_blocks, int elem_bytes, int32_t* status_dev,
+                     void* stream) {
     if (num_layers < 0 || num_pairs < 0 || n_kv_heads <= 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
         return PA_ERR_INVALID_ARG;
     if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head)) return PA_ERR_UNSUPPORTED;
@@ -285,7 +293,7 @@ int pa_swap_blocks(void* const* dst_k, void* const* dst_v, const void* const* sr
     const int32_t* pairs = static_cast<const int32_t*>(device_address(block_pairs));
     if (!pairs) return PA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(pairs) & 3u) return PA_ERR_MISALIGNED;
-    const long long chunks = (long long)n_kv_heads * block_size * d_head / 8;
+    const long long chunks = (long long)n_kv_heads * block_size * d_head * elem_bytes / 16;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
         const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
@@ -310,6 +318,38 @@ int pa_swap_blocks(void* const* dst_k, void* const* dst_v, const void* const* sr
         if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers, const int32_t* block_pairs,
+                   int num_pairs, int n_kv_heads, int d_head, int block_size, int num_blocks, int32_t* status_dev,
+                   void* stream) {
+    return copy_blocks_impl(k_caches, v_caches, num_layers, block_pairs, num_pairs, n_kv_heads, d_head, block_size,
+                            num_blocks, 2, status_dev, stream);
+}
+
+int pa_copy_blocks_fp8(void* const* k_caches, void* const* v_caches, int num_layers, const int32_t* block_pairs,
+                       int num_pairs, int n_kv_heads, int d_head, int block_size, int num_blocks, int32_t* status_dev,
+                       void* stream) {
+    return copy_blocks_impl(k_caches, v_caches, num_layers, block_pairs, num_pairs, n_kv_heads, d_head, block_size,
+                            num_blocks, 1, status_dev, stream);
+}
+
+int pa_swap_blocks(void* const* dst_k, void* const* dst_v, const void* const* src_k, const void* const* src_v,
+                   int num_layers, const int32_t* block_pairs, int num_pairs, int n_kv_heads, int d_head, int block_size,
+                   int src_num_blocks, int dst_num_blocks, int32_t* status_dev, void* stream) {
+    return swap_blocks_impl(dst_k, dst_v, src_k, src_v, num_layers, block_pairs, num_pairs, n_kv_heads, d_head,
+                            block_size, src_num_blocks, dst_num_blocks, 2, status_dev, stream);
+}
+
+int pa_swap_blocks_fp8(void* const* dst_k, void* const* dst_v, const void* const* src_k, const void* const* src_v,
+                       int num_layers, const int32_t* block_pairs, int num_pairs, int n_kv_heads, int d_head,
+                       int block_size, int src_num_blocks, int dst_num_blocks, int32_t* status_dev, void* stream) {
+    return swap_blocks_impl(dst_k, dst_v, src_k, src_v, num_layers, block_pairs, num_pairs, n_kv_heads, d_head,
+                            block_size, src_num_blocks, dst_num_blocks, 1, status_dev, stream);
 }
 
 }  // extern "C"

@@ -169,3 +169,66 @@ def test_fp8_argument_errors():
         api.pa_reshape_and_cache_fp8(kc, kc, torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda"),
                                      torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda"),
                                      torch.zeros(1, dtype=torch.int64, device="cuda"), -1.0, 1.0)
+
+
+# --------------------------------------------------------------------------
+# copy-on-write and swapping of FP8 pools: bit copies of one-byte codes
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L,B,Hkv,Dh,P", [(1, 16, 8, 128, 7), (3, 8, 2, 64, 20), (2, 32, 4, 128, 1)])
+def test_copy_blocks_fp8_bit_exact(L, B, Hkv, Dh, P):
+    from oracle import cache_ops as C
+    rng = np.random.default_rng(L * 13 + P)
+    NB = 2 * P + 5
+    ks = [rng.integers(0, 256, size=(NB, Hkv, B, Dh), dtype=np.uint8) for _ in range(L)]   # NaN codes included
+    vs = [rng.integers(0, 256, size=(NB, Hkv, B, Dh), dtype=np.uint8) for _ in range(L)]
+    perm = rng.permutation(NB)
+    pairs = np.stack([perm[:P], perm[P:2 * P]], axis=1).astype(np.int32)
+    kd = [torch.from_numpy(x).cuda() for x in ks]
+    vd = [torch.from_numpy(x).cuda() for x in vs]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.pa_copy_blocks(kd, vd, torch.from_numpy(pairs).cuda(), status=st)
+    C.copy_blocks(ks, vs, pairs)
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert np.array_equal(kd[l].cpu().numpy(), ks[l]) and np.array_equal(vd[l].cpu().numpy(), vs[l])
+    assert st.item() == 0
+
+
+def test_swap_blocks_fp8_round_trip_bit_exact():
+    from oracle import cache_ops as C
+    rng = np.random.default_rng(21)
+    L, NB, HNB, Hkv, B, Dh = 2, 30, 12, 4, 16, 128
+    dk = [rng.integers(0, 256, size=(NB, Hkv, B, Dh), dtype=np.uint8) for _ in range(L)]
+    dv = [rng.integers(0, 256, size=(NB, Hkv, B, Dh), dtype=np.uint8) for _ in range(L)]
+    hk = [np.zeros((HNB, Hkv, B, Dh), dtype=np.uint8) for _ in range(L)]
+    hv = [np.zeros((HNB, Hkv, B, Dh), dtype=np.uint8) for _ in range(L)]
+    out_pairs = np.stack([rng.permutation(NB)[:HNB], rng.permutation(HNB)], axis=1).astype(np.int32)
+    gk, gv = [torch.from_numpy(x).cuda() for x in dk], [torch.from_numpy(x).cuda() for x in dv]
+    pk, pv = [torch.from_numpy(x).pin_memory() for x in hk], [torch.from_numpy(x).pin_memory() for x in hv]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # device -> pinned host, then back into other device blocks
+    api.pa_swap_blocks(pk, pv, gk, gv, torch.from_numpy(out_pairs).cuda(), status=st)
+    for l in range(L):
+        C.swap_blocks(hk[l], hv[l], dk[l], dv[l], out_pairs.tolist())
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert np.array_equal(pk[l].numpy(), hk[l]) and np.array_equal(pv[l].numpy(), hv[l])
+    in_pairs = np.stack([np.arange(HNB), rng.permutation(NB)[:HNB]], axis=1).astype(np.int32)
+    api.pa_swap_blocks(gk, gv, pk, pv, torch.from_numpy(in_pairs).pin_memory(), status=st)
+    for l in range(L):
+        C.swap_blocks(dk[l], dv[l], hk[l], hv[l], in_pairs.tolist())
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert np.array_equal(gk[l].cpu().numpy(), dk[l]) and np.array_equal(gv[l].cpu().numpy(), dv[l])
+    assert st.item() == 0
+
+
+def test_fp8_copy_and_swap_reject_mixed_element_types():
+    k8 = [torch.zeros((4, 2, 16, 64), dtype=torch.uint8, device="cuda")]
+    kb = [torch.zeros((4, 2, 16, 64), dtype=torch.bfloat16, device="cuda")]
+    pairs = torch.tensor([[0, 1]], dtype=torch.int32, device="cuda")
+    with pytest.raises(TypeError):
+        api.pa_copy_blocks(k8, kb, pairs)
+    with pytest.raises(TypeError):
+        api.pa_swap_blocks(kb, kb, k8, k8, pairs)
