@@ -92,6 +92,7 @@ struct PGeo {
 struct PrefillArgs {
     void* out;
     int out_f32;
+    int out_al32;         // out is 32-byte aligned: 256-bit stores
     const int32_t* block_tables;
     int max_blocks;
     const int32_t* query_start;
@@ -221,6 +222,13 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+
+// One 32-byte store (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -781,12 +789,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 pa::mbar_arrive(&bars->o_free[x]);
                 if (valid_row[x]) {
-                    if (a.out_f32) {
+                    // a thread writes its half row: whole 32-byte sectors when
+                    // out allows it (16-byte stores fill half a sector each and
+                    // cost as much as a whole one)
+                    if (a.out_f32 && a.out_al32) {
+                        float* dst = static_cast<float*>(a.out) + orow;
+#pragma unroll
+                        for (int q = 0; q < kOCols / 8; ++q) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(o[8 * q + e] * inv);
+                            st_global_v8(dst + 8 * q, w);
+                        }
+                    } else if (a.out_f32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
 #pragma unroll
                         for (int q = 0; q < kOCols / 4; ++q)
                             dst[q] = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv,
                                                  o[4 * q + 3] * inv);
+                    } else if (a.out_al32) {
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + orow;
+#pragma unroll
+                        for (int q = 0; q < kOCols / 16; ++q) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w[e] = pack_bf16_rn(o[16 * q + 2 * e] * inv, o[16 * q + 2 * e + 1] * inv);
+                            st_global_v8(dst + 16 * q, w);
+                        }
                     } else {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
 #pragma unroll
@@ -914,6 +943,7 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     PrefillArgs a;
     a.out = out;
     a.out_f32 = out_dtype == PA_DTYPE_F32;
+    a.out_al32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
     a.block_tables = block_tables;
     a.max_blocks = max_blocks_per_seq;
     a.query_start = query_start;

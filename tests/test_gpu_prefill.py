@@ -171,3 +171,26 @@ def test_prefill_work_claiming_orders_agree():
     assert api.prefill_counters("cuda").cpu().tolist() == [0, 0]
     want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 0.125, 16, with_spread=True)
     assert_prefill_close(out_to_f64(outs[0]), want, spread, True, "claimed items")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_prefill_output_16_and_32_byte_aligned_agree(out_dtype):
+    """Rows are written with 32-byte stores when out is 32-byte aligned and
+    with 16-byte stores otherwise: the same bits either way."""
+    Hq, Hkv, D, B = 16, 4, 128, 16
+    qb, kb, vb, tab, qs, ctx = _problem(13, Hq, Hkv, D, B, [300, 170], [300, 90])
+    dev = lambda a: torch.from_numpy(a).cuda()
+    T = qb.shape[0]
+    outs = []
+    for shift in (0, 16 // torch.tensor([], dtype=out_dtype).element_size()):
+        flat = torch.full((T * Hq * D + 64,), float("nan"), dtype=out_dtype, device="cuda")
+        base = (-flat.data_ptr() // flat.element_size()) % (32 // flat.element_size())   # 32-byte aligned start
+        out = flat[base + shift: base + shift + T * Hq * D].view(T, Hq, D)
+        assert (out.data_ptr() % 32 == 0) == (shift == 0)
+        api.pa_prefill(out, from_bits(qb), from_bits(kb), from_bits(vb), dev(tab), dev(qs), dev(ctx), 300, B,
+                       1.0 / math.sqrt(D), Hq, Hkv, D)
+        torch.cuda.synchronize()
+        outs.append(out.clone())
+    assert torch.equal(outs[0].view(torch.int8), outs[1].view(torch.int8))
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B, with_spread=True)
+    assert_prefill_close(out_to_f64(outs[0]), want, spread, out_dtype == torch.float32, "aligned")
