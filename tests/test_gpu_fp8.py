@@ -232,3 +232,37 @@ def test_fp8_copy_and_swap_reject_mixed_element_types():
         api.pa_copy_blocks(k8, kb, pairs)
     with pytest.raises(TypeError):
         api.pa_swap_blocks(kb, kb, k8, k8, pairs)
+
+
+def test_decode_fp8_full_size_batch_sampled_sequences():
+    """The bench's FP8 decode: the 64-sequence 8B-shaped batch quantised as
+    the bench does it, decoded in one call with the library's default
+    partitions; four sequences checked against the oracle over the
+    dequantised codes (each gathered into a compact pool of its own blocks)."""
+    from paged_kv_cache_124_gb300.runner import ScenarioRunner
+    sc = I.batch64_8b(0)
+    run = ScenarioRunner(sc, device="cuda", data_device="cpu").replay()
+    tables, ctx, max_ctx = run.decode_metadata()
+    kc, vc = run.k_caches[0], run.v_caches[0]
+    ks = float(kc.float().nan_to_num(0.0).abs().amax()) / 448.0
+    vs = float(vc.float().nan_to_num(0.0).abs().amax()) / 448.0
+    k8 = (kc.float() / ks).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (vc.float() / vs).to(torch.float8_e4m3fn).view(torch.uint8)
+    S = len(sc.decode_seqs)
+    q = I.decode_q(sc.seed, 0, S, sc.n_q_heads, sc.d_head).cuda()
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    ws = api.decode_workspace(S, sc.n_q_heads, sc.d_head, max_ctx, 0)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.pa_decode_fp8(out, q, k8, v8, tables, ctx, sc.block_size, sc.scale, ks, vs, sc.n_q_heads, sc.n_kv_heads,
+                      sc.d_head, max_ctx, workspace=ws, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    got, qb = out_to_f64(out), to_bits(q)
+    tab_h, ctx_h = tables.cpu().numpy(), ctx.cpu().numpy()
+    for s in (0, 17, 42, S - 1):
+        nb = -(-int(ctx_h[s]) // sc.block_size)
+        blocks = torch.from_numpy(tab_h[s, :nb].astype(np.int64)).cuda()
+        kq, vq = k8.index_select(0, blocks).cpu().numpy(), v8.index_select(0, blocks).cpu().numpy()
+        want = A.paged_decode(qb[s:s + 1], Q.dequantize(kq, ks), Q.dequantize(vq, vs),
+                              np.arange(nb, dtype=np.int32)[None, :], ctx_h[s:s + 1], sc.scale, sc.block_size)
+        assert_attention_close(got[s:s + 1], want, True, "batch64 fp8 seq %d" % s)

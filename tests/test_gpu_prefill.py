@@ -194,3 +194,50 @@ def test_prefill_output_16_and_32_byte_aligned_agree(out_dtype):
     assert torch.equal(outs[0].view(torch.int8), outs[1].view(torch.int8))
     want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B, with_spread=True)
     assert_prefill_close(out_to_f64(outs[0]), want, spread, out_dtype == torch.float32, "aligned")
+
+
+def _bench_metadata(sc):
+    """Tables and slots from the C++ block manager in the seeded free order,
+    as the prefill bench builds them."""
+    alloc = api.BlockAllocator(sc.num_blocks, sc.block_size)
+    assert alloc.set_free_order(sc.free_order) == 0
+    for s, c in enumerate(sc.ctxs):
+        assert alloc.allocate(s, c) == 0
+    seqs = list(range(len(sc.ctxs)))
+    tables, ctx = alloc.build_tables(seqs, max(len(alloc.block_table(s)) for s in seqs))
+    slots = np.concatenate([alloc.slot_mapping(s, c - n, n) for s, (c, n) in enumerate(zip(sc.ctxs, sc.news))])
+    return tables, ctx, slots
+
+
+@pytest.mark.parametrize("workload", ["prefill_prompts", "chunked_prefill"])
+def test_prefill_full_size_bench_workload_sampled_rows(workload):
+    """The bench's full-size workloads (16 prompts of 2,003 tokens; 8 chunks of
+    512 over 2K-8K contexts), written with reshape_and_cache and attended with
+    the bench's call (bf16 output, shared work-claim counters): windows of
+    rows at the start, the middle and the end of sequences against the oracle,
+    which computes a window as the same sequence cut after its last row."""
+    sc = getattr(I, workload)(0, 16)
+    dev = torch.device("cuda")
+    tables, ctx, slots = _bench_metadata(sc)
+    kc, vc = I.prefill_pool(sc, dev)
+    q = I.prefill_q(sc, dev)
+    k_new, v_new = I.prefill_new_kv(sc, dev)
+    api.pa_reshape_and_cache(kc, vc, k_new, v_new, torch.from_numpy(slots).to(dev))
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    api.pa_prefill(out, q, kc, vc, torch.from_numpy(tables).to(dev), torch.from_numpy(sc.query_start).to(dev),
+                   torch.from_numpy(ctx).to(dev), max(sc.news), sc.block_size, sc.scale, sc.n_q_heads,
+                   sc.n_kv_heads, sc.d_head, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    kb, vb, qb, got = to_bits(kc), to_bits(vc), to_bits(q), out_to_f64(out)
+    S = len(sc.ctxs)
+    for s in (0, S // 2, S - 1):
+        C, n, q0 = int(sc.ctxs[s]), int(sc.news[s]), int(sc.query_start[s])
+        for i0 in sorted({0, n // 2 - 16, n - 32}):
+            i1 = min(n, i0 + 32)
+            rows = slice(q0 + i0, q0 + i1)
+            want, spread = A.paged_prefill(qb[rows], kb, vb, tables[s:s + 1], np.array([0, i1 - i0], np.int32),
+                                           np.array([C - n + i1], np.int32), sc.scale, sc.block_size,
+                                           with_spread=True)
+            assert_prefill_close(got[rows], want, spread, False, "%s seq %d rows %d..%d" % (workload, s, i0, i1))
