@@ -14,41 +14,46 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kMaxLayersPerLaunch = 64;
 
-// One thread block per token: K rows of all heads, then V rows of all heads.
-// The slot and the token's rows are loaded together (one memory round trip),
-// then stored.  Launched as a programmatic dependent: it waits for the work
-// before it on the stream before reading its inputs, and lets the next kernel
-// start its launch right away.
-__global__ void __launch_bounds__(128) reshape_and_cache_kernel(
+// One warp per token, four tokens per thread block: the token's K rows of
+// all heads, then its V rows, as 16-byte chunks.  The slot and the rows are
+// loaded together (one memory round trip; at the 8B shape every lane has
+// eight chunks in flight), then stored.  Launched as a programmatic
+// dependent: it waits for the work before it on the stream before reading
+// its inputs, and lets the next kernel start its launch right away.
+constexpr int kTokensPerBlock = 4;
+
+__global__ void __launch_bounds__(32 * kTokensPerBlock, 8) reshape_and_cache_kernel(
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const uint4* __restrict__ k,
-    const uint4* __restrict__ v, const int64_t* __restrict__ slot_mapping, int n_kv_heads, int chunks_per_row,
-    int block_size, long long num_slots, int32_t* status) {
+    const uint4* __restrict__ v, const int64_t* __restrict__ slot_mapping, int num_tokens, int n_kv_heads,
+    int chunks_per_row, int block_size, long long num_slots, int32_t* status) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int t = blockIdx.x;
+    const int t = blockIdx.x * kTokensPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= num_tokens) return;
     const long long slot = slot_mapping[t];
     const int per_token = n_kv_heads * chunks_per_row;     // 16-B chunks of one token's K
     const int total = 2 * per_token;
     const uint4* ksrc = k + (size_t)t * per_token;
     const uint4* vsrc = v + (size_t)t * per_token;
-    constexpr int R = 4;                                    // chunks in flight per thread
-    for (int c0 = threadIdx.x; c0 < total; c0 += R * blockDim.x) {
+    constexpr int R = 8;                                    // chunks in flight per lane
+    for (int c0 = lane; c0 < total; c0 += R * 32) {
         uint4 r[R];
 #pragma unroll
         for (int u = 0; u < R; ++u) {
-            const int c = c0 + u * blockDim.x;
+            const int c = c0 + u * 32;
             if (c < total) r[u] = c < per_token ? ksrc[c] : vsrc[c - per_token];
         }
         if (slot < 0) return;                               // padding token
         if (slot >= num_slots) {
-            if (threadIdx.x == 0) pa::set_status(status, PA_DEV_BAD_SLOT);
+            if (lane == 0) pa::set_status(status, PA_DEV_BAD_SLOT);
             return;
         }
         const long long blk = slot / block_size;
         const int off = (int)(slot - blk * block_size);
 #pragma unroll
         for (int u = 0; u < R; ++u) {
-            const int c = c0 + u * blockDim.x;
+            const int c = c0 + u * 32;
             if (c >= total) break;
             const bool is_v = c >= per_token;
             const int cc = is_v ? c - per_token : c;
@@ -217,10 +222,10 @@ int pa_reshape_and_cache(void* k_cache, void* v_cache, const void* k, const void
         !pa_host::aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
         return PA_ERR_MISALIGNED;
     const cudaError_t e = pa_host::launch_dependent(
-        reshape_and_cache_kernel, dim3(num_tokens), dim3(128), 0, static_cast<cudaStream_t>(stream),
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<const uint4*>(k),
-        static_cast<const uint4*>(v), slot_mapping, n_kv_heads, d_head / 8, block_size,
-        (long long)num_blocks * block_size, status_dev);
+        reshape_and_cache_kernel, dim3((num_tokens + kTokensPerBlock - 1) / kTokensPerBlock),
+        dim3(32 * kTokensPerBlock), 0, static_cast<cudaStream_t>(stream), static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping,
+        num_tokens, n_kv_heads, d_head / 8, block_size, (long long)num_blocks * block_size, status_dev);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
