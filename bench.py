@@ -326,20 +326,28 @@ def run_ours(args, world, rank, local):
     # and the decode, copies the output back and waits for it.  The step is
     # issued once into a CUDA graph (the library's calls are capturable) and
     # replayed; the eager form is timed too.
-    q_h = q.cpu().pin_memory()
-    k_h, v_h = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    slots_hp = slots.cpu().pin_memory()
-    tables_h, ctx_hp = tables.cpu().pin_memory(), ctx.cpu().pin_memory()
+    # The inputs travel packed in one page-locked buffer (one copy per step;
+    # six small copies each paid their own latency), and the calls read views
+    # of its device twin.
+    inputs = (q, k_new, v_new, slots, tables, ctx)
+    offs, total = [], 0
+    for t in inputs:
+        offs.append(total)
+        total += -(-t.numel() * t.element_size() // 256) * 256
+    pack_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    pack_d = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = []
+    for t, o in zip(inputs, offs):
+        nb = t.numel() * t.element_size()
+        pack_h[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+        views.append(pack_d[o:o + nb].view(t.dtype).view(t.shape))
+    q_d, k_d, v_d, slots_d, tables_d, ctx_d = views
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    q_d, k_d, v_d = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-    slots_d, tables_d, ctx_d = torch.empty_like(slots), torch.empty_like(tables), torch.empty_like(ctx)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, slots_hp, tables_h, ctx_hp))
+    h2d = sum(t.numel() * t.element_size() for t in inputs)
     d2h = out_h.numel() * out_h.element_size()
 
     def e2e_body(st):
-        for dst, src in ((q_d, q_h), (k_d, k_h), (v_d, v_h), (slots_d, slots_hp), (tables_d, tables_h),
-                         (ctx_d, ctx_hp)):
-            dst.copy_(src, non_blocking=True)
+        pack_d.copy_(pack_h, non_blocking=True)
         cache_write(k_d, v_d, slots_d, st)
         decode_call(q_d, tables_d, ctx_d, st)
         out_h.copy_(out, non_blocking=True)
@@ -400,7 +408,8 @@ def run_ours(args, world, rank, local):
                      "avg_launch_us": round(dec_s_avg * 1e6, 2)},
         "e2e": {"value": round(e2e_bytes / e2e_total_s / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_total_s / K * 1e3, 4), "issue": "CUDA graph of the step, replayed",
+                "ms_per_step": round(e2e_total_s / K * 1e3, 4), "issue": "CUDA graph of the step, replayed; inputs in one packed page-locked buffer, one copy in "
+                "and one out per step, waited for",
                 "eager_value": round(e2e_bytes / eager_total_s / 1e9, 2),
                 "eager_ms_per_step": round(eager_total_s / K * 1e3, 4)},
         "gpu_launches": launches_per_step * K,
