@@ -293,22 +293,28 @@ __device__ __forceinline__ void consume_tile(WarpState<D>& st, uint32_t ks, uint
     const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
 
     // ---- O^T += V^T . P^T --------------------------------------------------------
-    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;      // zero V rows past the context
+    // in the context's last tile the V rows past its end are zeroed (0 * NaN)
+    auto pv = [&](uint32_t mlo, uint32_t mhi, bool masked) {
+#pragma unroll
+        for (int m = 0; m < G::kSteps; ++m) {
+            uint32_t af[4];
+            ldsm_x4_trans(vs + (m >> 2) * G::kBoxBytes + swz(v_row, 2 * (m & 3) + v_cadd), af);
+            if (masked) {
+                af[0] &= mlo;
+                af[1] &= mlo;
+                af[2] &= mhi;
+                af[3] &= mhi;
+            }
+            mma16816(st.acc[m], af, bh0, bh1);
+            mma16816(st.acc[m], af, bl0, bl1);
+        }
+    };
     if (nv < kTile) {
         const int t = 2 * t4;
-        mlo = (t < nv ? 0x0000ffffu : 0u) | (t + 1 < nv ? 0xffff0000u : 0u);
-        mhi = (t + 8 < nv ? 0x0000ffffu : 0u) | (t + 9 < nv ? 0xffff0000u : 0u);
-    }
-#pragma unroll
-    for (int m = 0; m < G::kSteps; ++m) {
-        uint32_t af[4];
-        ldsm_x4_trans(vs + (m >> 2) * G::kBoxBytes + swz(v_row, 2 * (m & 3) + v_cadd), af);
-        af[0] &= mlo;
-        af[1] &= mlo;
-        af[2] &= mhi;
-        af[3] &= mhi;
-        mma16816(st.acc[m], af, bh0, bh1);
-        mma16816(st.acc[m], af, bl0, bl1);
+        pv((t < nv ? 0x0000ffffu : 0u) | (t + 1 < nv ? 0xffff0000u : 0u),
+           (t + 8 < nv ? 0x0000ffffu : 0u) | (t + 9 < nv ? 0xffff0000u : 0u), true);
+    } else {
+        pv(0xffffffffu, 0xffffffffu, false);
     }
 }
 
@@ -475,29 +481,36 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
     const uint32_t bh0 = movmatrix_trans(pack_f16(p0 * kP, p1 * kP));
     const uint32_t bh1 = movmatrix_trans(pack_f16(p2 * kP, p3 * kP));
 
-    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;      // zero V rows past the context
+    // P.V over the tile; in the context's last tile the V rows past its end
+    // are zeroed (their codes may be NaN, and 0 * NaN is not 0)
+    auto pv = [&](uint32_t mlo, uint32_t mhi, bool masked) {
+#pragma unroll
+        for (int j = 0; j < kSteps / 2; ++j) {
+            uint32_t r[4];
+            // r0 / r1: positions 2t4, 2t4+1 / 2t4+8, 2t4+9 of chunk 2j (codes 2g, 2g+1
+            // of each); r2 / r3: the same for chunk 2j+1
+            ldsm_x4_trans(vs + swz(row, 2 * j + cadd), r);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t af[4];
+                e4m3x4_to_f16(prmt(r[2 * h], r[2 * h], 0x3120u), af[0], af[1]);       // [p0 d0, p1 d0 | p0 d1, p1 d1]
+                e4m3x4_to_f16(prmt(r[2 * h + 1], r[2 * h + 1], 0x3120u), af[2], af[3]);
+                if (masked) {
+                    af[0] &= mlo;
+                    af[1] &= mlo;
+                    af[2] &= mhi;
+                    af[3] &= mhi;
+                }
+                mma16816_f16(st.acc[2 * j + h], af, bh0, bh1);
+            }
+        }
+    };
     if (nv < kTile) {
         const int t = 2 * t4;
-        mlo = (t < nv ? 0x0000ffffu : 0u) | (t + 1 < nv ? 0xffff0000u : 0u);
-        mhi = (t + 8 < nv ? 0x0000ffffu : 0u) | (t + 9 < nv ? 0xffff0000u : 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < kSteps / 2; ++j) {
-        uint32_t r[4];
-        // r0 / r1: positions 2t4, 2t4+1 / 2t4+8, 2t4+9 of chunk 2j (codes 2g, 2g+1
-        // of each); r2 / r3: the same for chunk 2j+1
-        ldsm_x4_trans(vs + swz(row, 2 * j + cadd), r);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t af[4];
-            e4m3x4_to_f16(prmt(r[2 * h], r[2 * h], 0x3120u), af[0], af[1]);       // [p0 d0, p1 d0 | p0 d1, p1 d1]
-            e4m3x4_to_f16(prmt(r[2 * h + 1], r[2 * h + 1], 0x3120u), af[2], af[3]);
-            af[0] &= mlo;
-            af[1] &= mlo;
-            af[2] &= mhi;
-            af[3] &= mhi;
-            mma16816_f16(st.acc[2 * j + h], af, bh0, bh1);
-        }
+        pv((t < nv ? 0x0000ffffu : 0u) | (t + 1 < nv ? 0xffff0000u : 0u),
+           (t + 8 < nv ? 0x0000ffffu : 0u) | (t + 9 < nv ? 0xffff0000u : 0u), true);
+    } else {
+        pv(0xffffffffu, 0xffffffffu, false);
     }
 }
 
