@@ -11,35 +11,42 @@
 // (chunked prefill), or the suffix after a prefix-cache hit are all this
 // same call.
 //
-// Design (one CTA per two tiles of 128 query rows of one KV head):
+// Design (a persistent CTA per SM; a work item is two tiles of 128 query
+// rows of one KV head):
 //   * Rows are (token, grouped query head) pairs: 128 / G consecutive new
 //     tokens times the G query heads that share KV head h, so every K/V tile
 //     is read once for all G heads (GQA).  Each Q tile is one 3-D TMA box;
-//     the CTA's two tiles (A, B) are consecutive token ranges and share every
+//     an item's two tiles (A, B) are consecutive token ranges and share every
 //     K/V tile.
+//   * Items are claimed from a counter shared by all CTAs, by group of KV
+//     heads and heaviest first within a group (the group's K/V stays in L2);
+//     the claiming warp decodes each item once and posts it to a ring in
+//     shared memory for the other warps.  Barrier phases run on across
+//     items, so the next item's loads and first products overlap the
+//     current item's last products and output.
 //   * K/V tiles of 128 positions are gathered through the block table with
 //     one 2-D TMA box (64 columns x B rows, 128-byte swizzle) per block and
-//     64-column half, two tiles ahead; blocks past the needed range, and bad
-//     table entries, are loaded from outside the tensor, which fills zeros
-//     and reads no HBM.
+//     64-column half; a warp issues its boxes one lane after another, so K
+//     and V have a producer warp each, and table entries are fetched four
+//     tiles ahead.  Blocks past the needed range, and bad table entries, are
+//     loaded from outside the tensor, which fills zeros and reads no HBM.
 //   * S = Q K^T (M 128, N 128, K d) and O += P V (M 128, N d, K 128) are
-//     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) issued by one thread.
-//     Tensor memory holds S_A, S_B (128 columns each) and O_A, O_B (d
-//     columns each) for the whole loop.  P (bf16) is written over the first
-//     64 columns of its own S and read from there as the A operand of the
-//     second product; V is an MN-major operand read straight from the TMA
-//     layout.
+//     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate), one issuing thread
+//     per Q tile (two issuers hide most of the pipe drain between groups of
+//     products of different kinds).  Tensor memory holds S_A, S_B (128
+//     columns each) and O_A, O_B (d columns each); P (bf16) is written over
+//     the first 64 columns of its own S and read from there as the A operand
+//     of the second product; V is an MN-major operand read straight from the
+//     TMA layout.
 //   * Eight softmax warps work on tile A, then on tile B, then on tile A of
 //     the next K/V tile, ...: warps w and w + 4 share the 32 rows of lane
 //     quarter w (tensor-memory lane = row), each taking 64 of the 128
 //     columns; the two halves of a row exchange their maxima (and, at the
 //     end, their sums) through shared memory.  Per row: mask, online maximum
-//     in the log2 domain, exp2, running sum, P.  One MMA warp per Q tile
-//     issues PV(j) and S(j+1) as soon as that tile's P is ready, so the
-//     tensor pipe works for one tile while the other tile's softmax runs.
-//     O is rescaled in tensor memory only when a row's maximum grows by more
-//     than 2^8 (the weights stay below 256 otherwise), which is rare after
-//     the first tiles.
+//     in the log2 domain, exp2, running sum, P.  O is rescaled in tensor
+//     memory only when a row's maximum grows by more than 2^8 (the weights
+//     stay below 256 otherwise), which is rare after the first tiles.  At
+//     the end of an item each thread writes its half row with 32-byte stores.
 //   * Every wait is bounded; on a timeout the CTA flags PA_DEV_WAIT_TIMEOUT,
 //     waits (bounded) for its own copies and products in flight, frees its
 //     tensor memory and returns.
@@ -65,8 +72,8 @@ constexpr uint32_t kTmemS0 = 0;            // S_A; S_B at +128
 constexpr uint32_t kTmemO0 = 256;          // O_A; O_B at +128
 constexpr int kMaxProbes = 2000000;        // x <= ~1 us per probe
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest weight allowed before a rescale
-// K tiles are released as soon as their score products finish; V tiles only
-// after the value products, a whole tile pair later, so V gets a deeper ring.
+// Two stages each for K and V: a third K stage (the shared memory allows one)
+// measured no faster.
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kSoftmaxThreads = 256;
