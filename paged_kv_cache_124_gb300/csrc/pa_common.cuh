@@ -52,19 +52,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe: true if the phase with the given parity has completed.
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait: gives up after max_probes probes (each suspends <= ~1 us).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int max_probes) {
     for (int i = 0; i < max_probes; ++i)
