@@ -46,6 +46,7 @@ METRIC = "paged decode-attn KV GB/s (frac of HBM peak); seqs/s at 8B GQA shape"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_partition_kernel_batch64_8b.md")
+PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "decode_partition_kernel_fp8_batch64_8b.md")
 KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_decode.cu")
 PREFILL_PROFILE = os.path.join(ROOT, "profiles", "prefill_kernel_prefill_prompts_8b.md")
 CACHE_OPS_PROFILE = os.path.join(ROOT, "profiles", "copy_blocks_kernel_cache_ops_8b.md")
@@ -403,7 +404,7 @@ def run_ours(args, world, rank, local):
         "roofline": {"bound": "hbm", "kernel": "pa_decode%s (decode_partition_kernel + lse_merge_kernel)" %
                      ("_fp8" if fp8 else ""),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None if fp8 else profiled_traffic(),
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(PROFILE_SUMMARY_FP8 if fp8 else PROFILE_SUMMARY),
                      "algorithmic_bytes_per_launch": int(dec_bytes),
                      "avg_launch_us": round(dec_s_avg * 1e6, 2)},
         "e2e": {"value": round(e2e_bytes / e2e_total_s / 1e9, 2), "unit": UNIT,
