@@ -1013,10 +1013,16 @@ def cpu_baseline(sc, budget_s):
         seqs = list(range(n))
         rep, tab, lens, q = _oracle_sample(sc, seqs)
         t = _oracle_time(sc, rep, tab, lens, q)
+    # a workload the oracle finishes quickly is run again until about half the budget has passed
+    reps = 1
+    while t < budget_s / 2:
+        t += _oracle_time(sc, rep, tab, lens, q)
+        reps += 1
     dec_bytes, _ = algorithmic_bytes(sc, lens, 0)
-    return {"value": round(dec_bytes / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": round(reps * dec_bytes / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": "fp64 oracle decode of the first %d of %d sequences (%d positions, all %d query heads) "
-                      "of %s, %.1f s" % (n, len(sc.decode_seqs), int(np.sum(lens)), sc.n_q_heads, sc.name, t)}
+                      "of %s, %d time(s), %.1f s" % (n, len(sc.decode_seqs), int(np.sum(lens)), sc.n_q_heads,
+                                                     sc.name, reps, t)}
 
 
 def run_reference(args, world, rank):
