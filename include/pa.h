@@ -372,6 +372,14 @@ int pa_swap_blocks_fp8(void* const* dst_k, void* const* dst_v,
                        int block_size, int src_num_blocks, int dst_num_blocks,
                        int32_t* status_dev, void* stream);
 
+/* Self-test of the failure path of every kernel: one thread block waits on
+ * an mbarrier that nothing ever arrives on, with the bounded wait routine the
+ * decode pipeline uses (max_probes probes of at most ~1 us each), then
+ * records PA_DEV_WAIT_TIMEOUT in *status_dev and returns.  No fault and no
+ * hang: the context stays usable.  max_probes in [1, 10^7]; status_dev
+ * required (device int32).  Returns PA_OK, PA_ERR_INVALID_ARG or PA_ERR_CUDA. */
+int pa_check_bounded_wait(int max_probes, int32_t* status_dev, void* stream);
+
 /* ===========================================================================
  * Host block manager ([P1] sections 14-17 and 20)
  * ===========================================================================

@@ -74,6 +74,7 @@ _SIGS = {
                                           _c_float, _vp, _vp]),
     "pa_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                             _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+    "pa_check_bounded_wait": (_c_int, [_c_int, _vp, _vp]),
     "pa_lse_merge": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                       _vp]),
@@ -412,6 +413,13 @@ def _dev_or_pinned(t, dtype, name):
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     return ctypes.c_void_p(t.data_ptr())
+
+
+def pa_check_bounded_wait(status, max_probes=20000, stream=None):
+    """Run the kernels' bounded-wait failure path on a barrier nothing arrives
+    on: status (device int32) receives PA_DEV_WAIT_TIMEOUT; see pa.h."""
+    return _check(_lib.pa_check_bounded_wait(int(max_probes), _dev(status, torch.int32, "status"), _stream(stream)),
+                  "pa_check_bounded_wait")
 
 
 def pa_swap_blocks(dst_k, dst_v, src_k, src_v, block_pairs, status=None, stream=None):

@@ -326,3 +326,31 @@ def test_lse_merge_random_against_oracle_merge():
                     for p in range(npart)]
             m, z, u = A.merge_summaries(summ)
             np.testing.assert_allclose(got[s, h], u / z, rtol=1e-5, atol=1e-6)
+
+
+def test_bounded_wait_runs_out_and_the_gpu_stays_usable():
+    """A wait on a barrier that nothing arrives on gives up after its probe
+    limit and flags PA_DEV_WAIT_TIMEOUT; no fault, no hang, and the next
+    kernels run normally."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.pa_check_bounded_wait(status, max_probes=20000)
+    torch.cuda.synchronize()
+    assert status.item() == api.PA_DEV_WAIT_TIMEOUT
+    # the context is still usable: a decode right after matches the oracle
+    rng = np.random.default_rng(9)
+    D, B, Hq, Hkv = 64, 16, 4, 2
+    ctx = np.array([37, 5], dtype=np.int32)
+    NB = 8
+    kc = _bf16_bits_normal(rng, (NB, Hkv, B, D))
+    vc = _bf16_bits_normal(rng, (NB, Hkv, B, D))
+    tab = np.array([[3, 0, 6], [5, -1, -1]], dtype=np.int32)
+    qb = _bf16_bits_normal(rng, (2, Hq, D))
+    out = torch.empty((2, Hq, D), dtype=torch.float32, device="cuda")
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = api.decode_workspace(2, Hq, D, 37, 0)
+    api.pa_decode(out, from_bits(qb), from_bits(kc), from_bits(vc), torch.from_numpy(tab).cuda(),
+                  torch.from_numpy(ctx).cuda(), B, 1 / math.sqrt(D), Hq, Hkv, D, 37, workspace=ws, status=st2)
+    torch.cuda.synchronize()
+    assert st2.item() == 0
+    want = A.paged_decode(qb, kc, vc, tab, ctx, 1 / math.sqrt(D), B)
+    assert_attention_close(out_to_f64(out), want, True, "after a timed-out wait")
