@@ -354,3 +354,33 @@ def test_bounded_wait_runs_out_and_the_gpu_stays_usable():
     assert st2.item() == 0
     want = A.paged_decode(qb, kc, vc, tab, ctx, 1 / math.sqrt(D), B)
     assert_attention_close(out_to_f64(out), want, True, "after a timed-out wait")
+
+
+# --------------------------------------------------------------------------
+# maximum sizes
+# --------------------------------------------------------------------------
+
+def test_decode_262144_position_context_256_partitions():
+    """One sequence of 2^18 positions: 256 partitions of the library default
+    size, merged by the log-sum-exp kernel."""
+    rng = np.random.default_rng(21)
+    L = 1 << 18
+    q, kc, vc, tables, ctx = _paged_problem(rng, [L], 8, 2, 128, 16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = _run_decode(q, kc, vc, tables, ctx, 16, 1 / math.sqrt(128), 8, 2, 128, torch.float32, status=st)
+    assert st.item() == 0
+    ref = A.paged_decode(q, kc, vc, tables, ctx, 1 / math.sqrt(128), 16)
+    assert_attention_close(out_to_f64(out), ref, True, "2^18 positions")
+
+
+def test_decode_8192_short_sequences():
+    """A batch of 8,192 sequences of 1 to 64 positions (grid of 8,192 x heads
+    blocks, single-partition path)."""
+    rng = np.random.default_rng(22)
+    lens = rng.integers(1, 65, size=8192).tolist()
+    q, kc, vc, tables, ctx = _paged_problem(rng, lens, 8, 2, 64, 16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = _run_decode(q, kc, vc, tables, ctx, 16, 0.125, 8, 2, 64, torch.bfloat16, status=st)
+    assert st.item() == 0
+    ref = A.paged_decode(q, kc, vc, tables, ctx, 0.125, 16)
+    assert_attention_close(out_to_f64(out), ref, False, "8192 sequences")

@@ -241,3 +241,18 @@ def test_prefill_full_size_bench_workload_sampled_rows(workload):
                                            np.array([C - n + i1], np.int32), sc.scale, sc.block_size,
                                            with_spread=True)
             assert_prefill_close(got[rows], want, spread, False, "%s seq %d rows %d..%d" % (workload, s, i0, i1))
+
+
+def test_prefill_32768_token_prompt_windows():
+    """One prompt of 32,768 tokens (512 work items per KV head, keys up to
+    32,768 per row): windows of rows at the start, the middle and the end."""
+    Hq, Hkv, D, B, L = 8, 2, 128, 16, 32768
+    qb, kb, vb, tab, qs, ctx = _problem(14, Hq, Hkv, D, B, [L], [L])
+    out, status = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, torch.bfloat16)
+    assert status == 0
+    got = out_to_f64(out)
+    for i0 in (0, L // 2 - 16, L - 32):
+        i1 = i0 + 32
+        want, spread = A.paged_prefill(qb[i0:i1], kb, vb, tab, np.array([0, 32], np.int32),
+                                       np.array([i1], np.int32), 1.0 / math.sqrt(D), B, with_spread=True)
+        assert_prefill_close(got[i0:i1], want, spread, False, "rows %d..%d" % (i0, i1))
