@@ -43,7 +43,9 @@
 //     quarter w (tensor-memory lane = row), each taking 64 of the 128
 //     columns; the two halves of a row exchange their maxima (and, at the
 //     end, their sums) through shared memory.  Per row: mask, online maximum
-//     in the log2 domain, exp2, running sum, P.  O is rescaled in tensor
+//     in the log2 domain, exp2, running sum, P; the scale-and-subtract and
+//     the running sums use packed f32x2 arithmetic (one instruction for two
+//     columns), which the softmax's instruction issue is bound by.  O is rescaled in tensor
 //     memory only when a row's maximum grows by more than 2^8 (the weights
 //     stay below 256 otherwise), which is rare after the first tiles.  At
 //     the end of an item each thread writes its half row with 32-byte stores.
@@ -266,6 +268,44 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Two fp32 values in one 64-bit register pair, for the packed f32x2
+// arithmetic (one instruction for both lanes of the pair).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void f32x2_split(uint64_t r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// v[0 .. n) *= k, two at a time
+template <int n>
+__device__ __forceinline__ void scale_f32x2(float* v, float k) {
+    const uint64_t kk = f32x2(k, k);
+#pragma unroll
+    for (int i = 0; i < n; i += 2) f32x2_split(mul_f32x2(f32x2(v[i], v[i + 1]), kk), v[i], v[i + 1]);
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
@@ -753,8 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float o[32];
                             tmem_ld32(t_o + cc * 32, o);
                             tmem_wait_ld();
-#pragma unroll
-                            for (int q = 0; q < 32; ++q) o[q] *= alpha;
+                            scale_f32x2<32>(o, alpha);
                             tmem_st32(t_o + cc * 32, o);
                         }
                     }
@@ -762,15 +801,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_used[x] = m_new;
                     const float neg = -m_used[x];
                     uint32_t w[kHalfCols / 2];
-                    float lp[4] = {0.f, 0.f, 0.f, 0.f};   // independent partial sums
+                    // column pairs in packed f32x2 arithmetic: one FMA and one
+                    // add per two weights
+                    const uint64_t c2x2 = f32x2(c2, c2), negx2 = f32x2(neg, neg);
+                    uint64_t lp[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};   // independent partial sums
 #pragma unroll
                     for (int q = 0; q < kHalfCols / 2; ++q) {
-                        const float p0 = fast_exp2(fmaf(s[2 * q], c2, neg));
-                        const float p1 = fast_exp2(fmaf(s[2 * q + 1], c2, neg));
-                        lp[q & 3] += p0 + p1;
+                        float x0, x1;
+                        f32x2_split(fma_f32x2(f32x2(s[2 * q], s[2 * q + 1]), c2x2, negx2), x0, x1);
+                        const float p0 = fast_exp2(x0);
+                        const float p1 = fast_exp2(x1);
+                        lp[q & 1] = add_f32x2(lp[q & 1], f32x2(p0, p1));
                         w[q] = pack_bf16_rn(p0, p1);
                     }
-                    l[x] += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+                    float l0, l1, l2, l3;
+                    f32x2_split(lp[0], l0, l1);
+                    f32x2_split(lp[1], l2, l3);
+                    l[x] += (l0 + l1) + (l2 + l3);
                     tmem_st32u(t_s + hc * (kHalfCols / 2), w);   // P columns over the first half of S
                     tmem_wait_st();
                     tc_fence_before();
@@ -796,6 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 pa::mbar_arrive(&bars->o_free[x]);
                 if (valid_row[x]) {
+                    scale_f32x2<kOCols>(o, inv);
                     // a thread writes its half row: whole 32-byte sectors when
                     // out allows it (16-byte stores fill half a sector each and
                     // cost as much as a whole one)
@@ -805,32 +853,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int q = 0; q < kOCols / 8; ++q) {
                             uint32_t w[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(o[8 * q + e] * inv);
+                            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(o[8 * q + e]);
                             st_global_v8(dst + 8 * q, w);
                         }
                     } else if (a.out_f32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
 #pragma unroll
                         for (int q = 0; q < kOCols / 4; ++q)
-                            dst[q] = make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv,
-                                                 o[4 * q + 3] * inv);
+                            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
                     } else if (a.out_al32) {
                         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + orow;
 #pragma unroll
                         for (int q = 0; q < kOCols / 16; ++q) {
                             uint32_t w[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) w[e] = pack_bf16_rn(o[16 * q + 2 * e] * inv, o[16 * q + 2 * e + 1] * inv);
+                            for (int e = 0; e < 8; ++e) w[e] = pack_bf16_rn(o[16 * q + 2 * e], o[16 * q + 2 * e + 1]);
                             st_global_v8(dst + 16 * q, w);
                         }
                     } else {
                         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
 #pragma unroll
                         for (int q = 0; q < kOCols / 8; ++q)
-                            dst[q] = make_uint4(pack_bf16_rn(o[8 * q] * inv, o[8 * q + 1] * inv),
-                                                pack_bf16_rn(o[8 * q + 2] * inv, o[8 * q + 3] * inv),
-                                                pack_bf16_rn(o[8 * q + 4] * inv, o[8 * q + 5] * inv),
-                                                pack_bf16_rn(o[8 * q + 6] * inv, o[8 * q + 7] * inv));
+                            dst[q] = make_uint4(pack_bf16_rn(o[8 * q], o[8 * q + 1]), pack_bf16_rn(o[8 * q + 2], o[8 * q + 3]),
+                                                pack_bf16_rn(o[8 * q + 4], o[8 * q + 5]), pack_bf16_rn(o[8 * q + 6], o[8 * q + 7]));
                     }
                 }
             }
