@@ -111,6 +111,53 @@ def test_prefill_chunked_equals_whole_prompt():
     assert_prefill_close(out_to_f64(whole), want, spread, True, "whole")
 
 
+def test_prefill_row_maxima_growing_across_tiles():
+    """Rows whose maximum score keeps growing: every q row shares a component
+    along d = 0, and the first key of every later 128-key tile is a spike
+    along it, so a row's maximum grows by about 5 to 9 (natural log) per tile,
+    around the kernel's bound of 2^8 on a weight.  O is then rescaled in
+    tensor memory for some rows and tiles and not for others (checked on the
+    inputs below), and the output still matches the oracle."""
+    Hq, Hkv, D, B, L = 16, 4, 128, 16, 600
+    G = Hq // Hkv
+    qb, kb, vb, tab, qs, ctx = _problem(9, Hq, Hkv, D, B, [L], [L])
+    scale = 1.0 / math.sqrt(D)
+    q = from_bits(qb, "cpu").float()
+    q[:, :, 0] += 4.0
+    qb = to_bits(q.to(torch.bfloat16))
+    k = from_bits(kb, "cpu").float()
+    for t in range(1, -(-L // 128)):
+        blk, off = tab[0, (128 * t) // B], (128 * t) % B
+        k[blk, :, off, :] = 0.0
+        k[blk, :, off, 0] = 7.0 * t / (4.0 * scale)
+    kb = to_bits(k.to(torch.bfloat16))
+    # the inputs reach both sides of the bound: simulate the kernel's rule (the
+    # running maximum moves only when a tile's maximum exceeds it by more than
+    # 8 in log2 units) on the rows that see more than one tile
+    qf = from_bits(qb, "cpu").double().numpy()
+    kf = from_bits(kb, "cpu").double().numpy()
+    kseq = np.stack([kf[tab[0, j // B], :, j % B, :] for j in range(L)], axis=1)     # [Hkv][L][D]
+    c = scale / math.log(2.0)
+    moved = still = 0
+    for i in range(128, L, 7):
+        for g in range(0, Hq, 3):
+            s = (kseq[g // G, :i + 1] @ qf[i, g]) * c
+            m_used = s[:128].max()
+            n = 0
+            for t in range(1, i // 128 + 1):
+                mt = s[128 * t:128 * (t + 1)].max()
+                if mt > m_used + 8.0:
+                    m_used, n = mt, n + 1
+            moved += n > 0
+            still += n == 0
+    assert moved > 0 and still > 0, (moved, still)
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, scale, B, with_spread=True)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        got, status = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, out_dtype)
+        assert status == 0
+        assert_prefill_close(out_to_f64(got), want, spread, out_dtype == torch.float32, "growing maxima")
+
+
 def test_prefill_device_flags():
     qb, kb, vb, tab, qs, ctx = _problem(7, 8, 2, 64, 16, [40, 20], [40, 20])
     bad_ctx = ctx.copy()
