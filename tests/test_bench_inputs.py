@@ -1,4 +1,6 @@
-"""Host-side inputs of the bench workloads, pinned to the oracle: the
+"""Host-side inputs and work counts of the bench workloads.  The FLOP and
+byte counts behind the roofline figures are recounted term by term from the
+workloads' drawn sizes.  And the
 copy-on-write pairs of the CoW sampling config (16 prompts of 2,003 tokens,
 8 samples each, one appended token per sample) that the cache-ops workload
 copies come from the C++ block manager; the oracle allocator replaying the
@@ -44,3 +46,31 @@ def test_prefill_slots_are_the_new_positions_of_each_prompt():
     assert len(slots) == sum(sc.news) == 16 * 2003
     assert len(set(slots.tolist())) == len(slots)                   # one slot per position
     assert slots.min() >= 0 and slots.max() < sc.num_blocks * sc.block_size
+
+
+def test_prefill_flops_closed_form_and_pair_count():
+    """The prefill roofline's numerator: 4 d FLOPs per (query head, visible
+    key) pair.  Whole prompts see p + 1 keys at position p, n (n + 1) / 2
+    pairs per head; a chunk over a cached prefix is counted pair by pair."""
+    assert bench.prefill_flops([2003] * 16, [2003] * 16, 32, 128) == 16 * (2003 * 2004 // 2) * 4 * 128 * 32
+    ctxs, news = [10, 7, 1, 300], [4, 7, 1, 17]
+    pairs = sum(1 for c, n in zip(ctxs, news) for p in range(c - n, c) for j in range(c) if j <= p)
+    assert bench.prefill_flops(ctxs, news, 3, 64) == pairs * 4 * 64 * 3
+
+
+def test_decode_algorithmic_bytes_of_the_headline_batch():
+    """The decode roofline's numerator for the 64-sequence 8B-shaped batch,
+    counted term by term from its drawn contexts: one K and one V row of
+    d_head bf16 values per cached position and KV head, q read and the
+    output written once, and the 4-byte table entries and context lengths in
+    use; the cache write reads and writes each new token's K and V rows."""
+    from paged_kv_cache_124_gb300 import inputs as I
+    sc = I.batch64_8b(0)
+    ctx = np.asarray(I.uniform_ints(64, 512, 4096, 1), dtype=np.int64)
+    assert int(ctx.sum()) == 143905
+    kv = sum(int(c) * sc.d_head * 2 * 2 for c in ctx for _ in range(sc.n_kv_heads))
+    qo = 64 * sc.n_q_heads * sc.d_head * 2 * 2
+    tab = sum((int(c) + sc.block_size - 1) // sc.block_size for c in ctx) * 4 + 64 * 4
+    dec, write = bench.algorithmic_bytes(sc, ctx, 64)
+    assert dec == kv + qo + tab == 590519796
+    assert write == 64 * sc.n_kv_heads * 2 * sc.d_head * 2 * 2
