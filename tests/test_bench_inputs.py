@@ -1,6 +1,6 @@
 """Host-side inputs and work counts of the bench workloads.  The FLOP and
 byte counts behind the roofline figures are recounted term by term from the
-workloads' drawn sizes.  And the
+workloads' drawn sizes.  The
 copy-on-write pairs of the CoW sampling config (16 prompts of 2,003 tokens,
 8 samples each, one appended token per sample) that the cache-ops workload
 copies come from the C++ block manager; the oracle allocator replaying the
