@@ -158,6 +158,19 @@ def test_prefill_row_maxima_growing_across_tiles():
         assert_prefill_close(out_to_f64(got), want, spread, out_dtype == torch.float32, "growing maxima")
 
 
+@pytest.mark.parametrize("Hq,Hkv,D", [(128, 2, 64), (128, 1, 128), (64, 1, 64)], ids=["g64_d64", "g128_d128", "g64_one_kv"])
+def test_prefill_largest_groups(Hq, Hkv, D):
+    """Group sizes 64 and 128 (the largest the call takes): a 128-row Q tile
+    then holds 2 tokens or 1 token of all the group's heads."""
+    ctxs, news = [70, 33, 129], [70, 5, 40]
+    qb, kb, vb, tab, qs, ctx = _problem(11, Hq, Hkv, D, 16, ctxs, news)
+    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), 16, with_spread=True)
+    for out_dtype in (torch.float32, torch.bfloat16):
+        got, status = _run(qb, kb, vb, tab, qs, ctx, 16, Hq, Hkv, D, out_dtype)
+        assert status == 0
+        assert_prefill_close(out_to_f64(got), want, spread, out_dtype == torch.float32, "G=%d" % (Hq // Hkv))
+
+
 def test_prefill_device_flags():
     qb, kb, vb, tab, qs, ctx = _problem(7, 8, 2, 64, 16, [40, 20], [40, 20])
     bad_ctx = ctx.copy()
