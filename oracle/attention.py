@@ -137,8 +137,7 @@ def dense_decode(q, K_dense, V_dense, context_lens, scale):
 # Prefill: many query positions per sequence, causal ([P2] sections 4 and 8)
 # ----------------------------------------------------------------------------
 
-def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, scale, block_size,
-                  with_spread=False):
+def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, scale, block_size):
     """Causal attention of the new positions of each sequence.
 
     Sequence s has context length C = context_lens[s]; its last
@@ -150,15 +149,13 @@ def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, 
     block table exactly as for decode.
 
     q: [T, n_q_heads, d_head] float64 or uint16 bf16 bits; returns
-    [T, n_q_heads, d_head] float64 (rows not covered by any sequence are 0),
-    and with with_spread also weight_spread of every output row.
+    [T, n_q_heads, d_head] float64 (rows not covered by any sequence are 0).
     """
     if q.dtype == np.uint16:
         q = bf16_to_f64(q)
     T, n_q_heads, d_head = q.shape
     n_kv_heads = k_cache.shape[1]
     out = np.zeros((T, n_q_heads, d_head), dtype=np.float64)
-    spread = np.zeros((T, n_q_heads, d_head), dtype=np.float64) if with_spread else None
     for s in range(len(context_lens)):
         C = int(context_lens[s])
         row0, n = int(query_start[s]), int(query_start[s + 1]) - int(query_start[s])
@@ -170,20 +167,7 @@ def paged_prefill(q, k_cache, v_cache, block_tables, query_start, context_lens, 
             for g in range(n_q_heads):
                 h = kv_head_of(g, n_q_heads, n_kv_heads)
                 out[row0 + i, g] = softmax_attention(q[row0 + i, g], K[h, :p + 1], V[h, :p + 1], scale)
-                if with_spread:
-                    spread[row0 + i, g] = weight_spread(q[row0 + i, g], K[h, :p + 1], V[h, :p + 1], scale)
-    return (out, spread) if with_spread else out
-
-
-def weight_spread(q, K, V, scale):
-    """sum_j a_j |V_j| per output element, with a = softmax(scale q.K^T):
-    how far o = a V can move when every weight in the weighted sum is
-    perturbed by a relative amount eps while the normaliser is kept (at most
-    eps times this)."""
-    s = scale * (K @ q)
-    e = np.exp(s - s.max())
-    a = e / e.sum()
-    return a @ np.abs(V)
+    return out
 
 
 # ----------------------------------------------------------------------------

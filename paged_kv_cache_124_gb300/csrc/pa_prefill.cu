@@ -34,10 +34,12 @@
 //     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate), one issuing thread
 //     per Q tile (two issuers hide most of the pipe drain between groups of
 //     products of different kinds).  Tensor memory holds S_A, S_B (128
-//     columns each) and O_A, O_B (d columns each); P (bf16) is written over
-//     the first 64 columns of its own S and read from there as the A operand
-//     of the second product; V is an MN-major operand read straight from the
-//     TMA layout.
+//     columns each) and O_A, O_B (d columns each).  Each weight is split
+//     into two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), written over
+//     the first and the second 64 columns of its own S; both are read from
+//     there as A operands (O += P_hi V + P_lo V), so the weights reach the
+//     products to a relative 2^-16, not bf16's 2^-8.  V is an MN-major
+//     operand read straight from the TMA layout.
 //   * Eight softmax warps work on tile A, then on tile B, then on tile A of
 //     the next K/V tile, ...: warps w and w + 4 share the 32 rows of lane
 //     quarter w (tensor-memory lane = row), each taking 64 of the 128
@@ -214,14 +216,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31])));
 }
 
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w) {
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* w) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]),
-        "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]), "r"(w[16]),
-        "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]), "r"(w[24]),
-        "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31]));
+        "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]));
 }
 
 // A operand from tensor memory (M rows in lanes, two bf16 per column).
@@ -305,6 +305,12 @@ __device__ __forceinline__ void scale_f32x2(float* v, float k) {
 __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 
@@ -689,9 +695,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok) ok = wait1(&bars->p_full[x], (ns - 1) & 1, bars, a.status);
                     if (!ok) break;
                     tc_fence_after();
+                    // O += P_hi V, then O += P_lo V (the weights' two bf16 terms)
                     for (int kk = 0; kk < ksteps; ++kk)
                         mma_bf16_ta(t_o, t_s + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
                                     (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < ksteps; ++kk)
+                        mma_bf16_ta(t_o, t_s + kKv / 2 + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024),
+                                    id_pv, 1u);
                     commit(&bars->v_empty[x][vs], (gj / kVStages) & 1);
                     if (j == ntx - 1) {
                         commit(&bars->o_done[x], nod & 1);
@@ -800,25 +810,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l[x] *= alpha;
                     m_used[x] = m_new;
                     const float neg = -m_used[x];
-                    uint32_t w[kHalfCols / 2];
                     // column pairs in packed f32x2 arithmetic: one FMA and one
-                    // add per two weights
+                    // add per two weights.  Each weight p goes to the tensor
+                    // cores as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi)
+                    // (p - hi is exact in fp32), so that hi + lo carries p to a
+                    // relative 2^-16 instead of bf16's 2^-8; P_hi is written over
+                    // the first 64 columns of S and P_lo over the other 64.
                     const uint64_t c2x2 = f32x2(c2, c2), negx2 = f32x2(neg, neg);
                     uint64_t lp[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};   // independent partial sums
 #pragma unroll
-                    for (int q = 0; q < kHalfCols / 2; ++q) {
-                        float x0, x1;
-                        f32x2_split(fma_f32x2(f32x2(s[2 * q], s[2 * q + 1]), c2x2, negx2), x0, x1);
-                        const float p0 = fast_exp2(x0);
-                        const float p1 = fast_exp2(x1);
-                        lp[q & 1] = add_f32x2(lp[q & 1], f32x2(p0, p1));
-                        w[q] = pack_bf16_rn(p0, p1);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t w[kHalfCols / 4], wl[kHalfCols / 4];
+#pragma unroll
+                        for (int qq = 0; qq < kHalfCols / 4; ++qq) {
+                            const int q = h2 * (kHalfCols / 4) + qq;
+                            float x0, x1;
+                            f32x2_split(fma_f32x2(f32x2(s[2 * q], s[2 * q + 1]), c2x2, negx2), x0, x1);
+                            const uint64_t pp = f32x2(fast_exp2(x0), fast_exp2(x1));
+                            lp[q & 1] = add_f32x2(lp[q & 1], pp);
+                            float p0, p1;
+                            f32x2_split(pp, p0, p1);
+                            const uint32_t hi = pack_bf16_rn(p0, p1);
+                            float r0, r1;
+                            f32x2_split(sub_f32x2(pp, f32x2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))),
+                                        r0, r1);
+                            w[qq] = hi;
+                            wl[qq] = pack_bf16_rn(r0, r1);
+                        }
+                        tmem_st16u(t_s + hc * (kHalfCols / 2) + h2 * (kHalfCols / 4), w);
+                        tmem_st16u(t_s + kKv / 2 + hc * (kHalfCols / 2) + h2 * (kHalfCols / 4), wl);
                     }
                     float l0, l1, l2, l3;
                     f32x2_split(lp[0], l0, l1);
                     f32x2_split(lp[1], l2, l3);
                     l[x] += (l0 + l1) + (l2 + l3);
-                    tmem_st32u(t_s + hc * (kHalfCols / 2), w);   // P columns over the first half of S
                     tmem_wait_st();
                     tc_fence_before();
                     pa::mbar_arrive(&bars->p_full[x]);

@@ -39,27 +39,3 @@ def assert_attention_close(got, ref, f32_out, what=""):
     if f32_out:
         assert d.max() <= ATOL, msg
     return float(d.max()), max_rel
-
-
-# Prefill rounds the softmax weights to bf16 (unit roundoff 2^-8) before the
-# weighted sum of values, and normalises by the sum of the unrounded weights.
-# Perturbing every weight of the sum by a relative eps moves an output
-# element by at most eps times sum_j a_j |V_j| (the oracle's weight_spread),
-# so that term is added to the decode tolerance.
-P_ROUND = 2.0 ** -8
-
-
-def assert_prefill_close(got, ref, spread, f32_out, what=""):
-    got = np.asarray(got, dtype=np.float64)
-    ref = np.asarray(ref, dtype=np.float64)
-    assert got.shape == ref.shape == spread.shape
-    assert np.all(np.isfinite(got)), "%s: non-finite output" % what
-    d = np.abs(got - ref)
-    extra = P_ROUND * spread
-    bad = d > ATOL + RTOL * np.abs(ref) + extra
-    msg = "%s: max abs %.3g, max abs/(tol) %.3g, %d/%d outside tolerance" % (
-        what, d.max(), float((d / (ATOL + RTOL * np.abs(ref) + extra)).max()), int(bad.sum()), d.size)
-    assert not bad.any(), msg
-    if f32_out:
-        assert (d <= ATOL + extra).all(), msg
-    return float(d.max())

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from oracle import attention as A
-from _gpu_util import assert_prefill_close, from_bits, out_to_f64, to_bits
+from _gpu_util import assert_attention_close, from_bits, out_to_f64, to_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -69,21 +69,21 @@ CASES = [
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_prefill_matches_oracle(name, Hq, Hkv, D, B, ctxs, news, out_dtype):
     qb, kb, vb, tab, qs, ctx = _problem(3, Hq, Hkv, D, B, ctxs, news)
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B, with_spread=True)
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B)
     got, status = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, out_dtype)
     assert status == 0
-    assert_prefill_close(out_to_f64(got), want, spread, out_dtype == torch.float32, name)
+    assert_attention_close(out_to_f64(got), want, out_dtype == torch.float32, name)
 
 
 def test_prefill_uncovered_rows_and_empty_sequences_untouched():
     # a sequence with no new tokens in the middle, and two rows past the last sequence
     qb, kb, vb, tab, qs, ctx = _problem(4, 8, 2, 128, 16, [50, 30, 90], [50, 0, 17], extra_rows=2)
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16, with_spread=True)
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16)
     got, status = _run(qb, kb, vb, tab, qs, ctx, 16, 8, 2, 128, torch.float32, fill=-7.0)
     assert status == 0
     g = out_to_f64(got)
     assert (g[67:] == -7.0).all()
-    assert_prefill_close(g[:67], want[:67], spread[:67], True, "covered rows")
+    assert_attention_close(g[:67], want[:67], True, "covered rows")
 
 
 def test_prefill_equals_decode_for_single_tokens():
@@ -93,8 +93,8 @@ def test_prefill_equals_decode_for_single_tokens():
     qb, kb, vb, tab, qs, ctx = _problem(5, 32, 8, 128, 16, ctxs, [1] * 4)
     got, status = _run(qb, kb, vb, tab, qs, ctx, 16, 32, 8, 128, torch.float32)
     assert status == 0
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16, with_spread=True)
-    assert_prefill_close(out_to_f64(got), want, spread, True, "n=1")
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16)
+    assert_attention_close(out_to_f64(got), want, True, "n=1")
     np.testing.assert_array_equal(want, A.paged_decode(qb, kb, vb, tab, ctx, 1.0 / math.sqrt(128), 16))
 
 
@@ -106,9 +106,9 @@ def test_prefill_chunked_equals_whole_prompt():
     whole, st1 = _run(qb, kb, vb, tab, qs, ctx, 16, 32, 8, 128, torch.float32)
     part, st2 = _run(qb[cut:], kb, vb, tab, np.array([0, L - cut], np.int32), ctx, 16, 32, 8, 128, torch.float32)
     assert st1 == st2 == 0
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16, with_spread=True)
-    assert_prefill_close(out_to_f64(part), want[cut:], spread[cut:], True, "chunk")
-    assert_prefill_close(out_to_f64(whole), want, spread, True, "whole")
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(128), 16)
+    assert_attention_close(out_to_f64(part), want[cut:], True, "chunk")
+    assert_attention_close(out_to_f64(whole), want, True, "whole")
 
 
 def test_prefill_row_maxima_growing_across_tiles():
@@ -151,11 +151,48 @@ def test_prefill_row_maxima_growing_across_tiles():
             moved += n > 0
             still += n == 0
     assert moved > 0 and still > 0, (moved, still)
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, scale, B, with_spread=True)
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, scale, B)
     for out_dtype in (torch.float32, torch.bfloat16):
         got, status = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, out_dtype)
         assert status == 0
-        assert_prefill_close(out_to_f64(got), want, spread, out_dtype == torch.float32, "growing maxima")
+        assert_attention_close(out_to_f64(got), want, out_dtype == torch.float32, "growing maxima")
+
+
+def test_prefill_weights_finer_than_bf16():
+    """Rows whose softmax weights bf16 cannot carry: 64 two-position
+    sequences, key 0 all zeros and key 1 with one component c, so row 1's
+    weights are 1 and e^c (relative to the maximum) with V rows -4 and +4.
+    The values of c are the bf16 numbers in [-4, 0) whose e^c lies farthest
+    from a bf16 number (checked below: weights rounded to bf16 would move
+    these outputs by up to ~7e-3, past the 2e-3 bound).  The kernel carries
+    each weight as two bf16 terms, so the fp32 outputs stay within 2e-3."""
+    S, Hq, Hkv, D, B = 64, 1, 1, 64, 16
+    cand = torch.arange(-4.0, 0.0, 2.0 ** -9, dtype=torch.float64).to(torch.bfloat16).unique()
+    cand = cand[cand < 0].double()
+    p = torch.exp(cand)
+    p_bf16 = p.float().to(torch.bfloat16).double()
+    moved = (p_bf16 - p).abs() * 8.0 / (1.0 + p) ** 2        # |d o / d p| = |V1 - V0| / (1 + p)^2
+    c = cand[torch.argsort(moved, descending=True)[:S]]
+    assert float(moved.max()) > 5e-3
+    qb, kb, vb, tab, qs, ctx = _problem(15, Hq, Hkv, D, B, [2] * S, [2] * S)
+    q = torch.zeros((2 * S, Hq, D))
+    q[:, :, 0] = math.sqrt(D)                              # scale * q . k = k[0]
+    kf = torch.zeros((kb.shape[0], Hkv, B, D))
+    vf = torch.full((kb.shape[0], Hkv, B, D), float("nan"))
+    for s_ in range(S):
+        blk = tab[s_, 0]
+        kf[blk, :, 1, 0] = float(c[s_])
+        vf[blk, :, 0, :] = -4.0
+        vf[blk, :, 1, :] = 4.0
+    qb, kb, vb = to_bits(q.to(torch.bfloat16)), to_bits(kf.to(torch.bfloat16)), to_bits(vf.to(torch.bfloat16))
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B)
+    # what bf16-rounded weights (normalised by the unrounded sum) would give
+    p_row = torch.exp(c)
+    bf_row = (-4.0 + 4.0 * p_row.float().to(torch.bfloat16).double()) / (1.0 + p_row)
+    assert np.abs(bf_row.numpy() - want[1::2, 0, 0]).max() > 2e-3
+    got, status = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, torch.float32)
+    assert status == 0
+    assert_attention_close(out_to_f64(got), want, True, "weights finer than bf16")
 
 
 @pytest.mark.parametrize("Hq,Hkv,D", [(128, 2, 64), (128, 1, 128), (64, 1, 64)], ids=["g64_d64", "g128_d128", "g64_one_kv"])
@@ -164,11 +201,11 @@ def test_prefill_largest_groups(Hq, Hkv, D):
     then holds 2 tokens or 1 token of all the group's heads."""
     ctxs, news = [70, 33, 129], [70, 5, 40]
     qb, kb, vb, tab, qs, ctx = _problem(11, Hq, Hkv, D, 16, ctxs, news)
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), 16, with_spread=True)
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), 16)
     for out_dtype in (torch.float32, torch.bfloat16):
         got, status = _run(qb, kb, vb, tab, qs, ctx, 16, Hq, Hkv, D, out_dtype)
         assert status == 0
-        assert_prefill_close(out_to_f64(got), want, spread, out_dtype == torch.float32, "G=%d" % (Hq // Hkv))
+        assert_attention_close(out_to_f64(got), want, out_dtype == torch.float32, "G=%d" % (Hq // Hkv))
 
 
 def test_prefill_device_flags():
@@ -178,8 +215,8 @@ def test_prefill_device_flags():
     got, status = _run(qb, kb, vb, tab, qs, bad_ctx, 16, 8, 2, 64, torch.float32, fill=-3.0)
     assert status & api.PA_DEV_BAD_CONTEXT
     assert (out_to_f64(got)[40:] == -3.0).all()
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs[:2], ctx[:1], 1.0 / 8.0, 16, with_spread=True)
-    assert_prefill_close(out_to_f64(got)[:40], want[:40], spread[:40], True, "good sequence")
+    want = A.paged_prefill(qb, kb, vb, tab, qs[:2], ctx[:1], 1.0 / 8.0, 16)
+    assert_attention_close(out_to_f64(got)[:40], want[:40], True, "good sequence")
     bad_tab = tab.copy()
     bad_tab[0, 1] = kb.shape[0] + 5                 # outside the pool
     _, status = _run(qb, kb, vb, bad_tab, qs, ctx, 16, 8, 2, 64, torch.float32)
@@ -229,8 +266,8 @@ def test_prefill_work_claiming_orders_agree():
         assert torch.equal(o, outs[0])
     assert mine.cpu().tolist() == [0, 0]
     assert api.prefill_counters("cuda").cpu().tolist() == [0, 0]
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 0.125, 16, with_spread=True)
-    assert_prefill_close(out_to_f64(outs[0]), want, spread, True, "claimed items")
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 0.125, 16)
+    assert_attention_close(out_to_f64(outs[0]), want, True, "claimed items")
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
@@ -252,8 +289,8 @@ def test_prefill_output_16_and_32_byte_aligned_agree(out_dtype):
         torch.cuda.synchronize()
         outs.append(out.clone())
     assert torch.equal(outs[0].view(torch.int8), outs[1].view(torch.int8))
-    want, spread = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B, with_spread=True)
-    assert_prefill_close(out_to_f64(outs[0]), want, spread, out_dtype == torch.float32, "aligned")
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B)
+    assert_attention_close(out_to_f64(outs[0]), want, out_dtype == torch.float32, "aligned")
 
 
 def _bench_metadata(sc):
@@ -297,10 +334,9 @@ def test_prefill_full_size_bench_workload_sampled_rows(workload):
         for i0 in sorted({0, n // 2 - 16, n - 32}):
             i1 = min(n, i0 + 32)
             rows = slice(q0 + i0, q0 + i1)
-            want, spread = A.paged_prefill(qb[rows], kb, vb, tables[s:s + 1], np.array([0, i1 - i0], np.int32),
-                                           np.array([C - n + i1], np.int32), sc.scale, sc.block_size,
-                                           with_spread=True)
-            assert_prefill_close(got[rows], want, spread, False, "%s seq %d rows %d..%d" % (workload, s, i0, i1))
+            want = A.paged_prefill(qb[rows], kb, vb, tables[s:s + 1], np.array([0, i1 - i0], np.int32),
+                                           np.array([C - n + i1], np.int32), sc.scale, sc.block_size)
+            assert_attention_close(got[rows], want, False, "%s seq %d rows %d..%d" % (workload, s, i0, i1))
 
 
 def test_prefill_32768_token_prompt_windows():
@@ -313,6 +349,6 @@ def test_prefill_32768_token_prompt_windows():
     got = out_to_f64(out)
     for i0 in (0, L // 2 - 16, L - 32):
         i1 = i0 + 32
-        want, spread = A.paged_prefill(qb[i0:i1], kb, vb, tab, np.array([0, 32], np.int32),
-                                       np.array([i1], np.int32), 1.0 / math.sqrt(D), B, with_spread=True)
-        assert_prefill_close(got[i0:i1], want, spread, False, "rows %d..%d" % (i0, i1))
+        want = A.paged_prefill(qb[i0:i1], kb, vb, tab, np.array([0, 32], np.int32),
+                                       np.array([i1], np.int32), 1.0 / math.sqrt(D), B)
+        assert_attention_close(got[i0:i1], want, False, "rows %d..%d" % (i0, i1))

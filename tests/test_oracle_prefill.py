@@ -126,24 +126,3 @@ def test_rows_outside_every_sequence_stay_zero():
     q = np.concatenate([q, rng.normal(size=(2, 2, 4))])
     out = A.paged_prefill(q, kc, vc, tab, qs, ctx, 0.5, 4)
     assert (out[3:] == 0).all() and np.isfinite(out[:3]).all()
-
-
-def test_weight_spread_closed_forms():
-    # one dominant position: the weighted absolute value is that row's
-    K = np.array([[1000.0], [0.0]])
-    V = np.array([[3.0, -1.0], [5.0, -7.0]])
-    np.testing.assert_allclose(A.weight_spread(np.array([1.0]), K, V, 1.0), [3.0, 1.0])
-    # two equal weights: the mean absolute value
-    K = np.array([[0.0], [0.0]])
-    np.testing.assert_allclose(A.weight_spread(np.array([1.0]), K, V, 1.0), [4.0, 4.0])
-    # perturbing each weight by at most eps (normaliser kept) moves o by at most eps * spread
-    rng = np.random.default_rng(58)
-    K, V, q = rng.normal(size=(50, 4)), rng.normal(size=(50, 3)), rng.normal(size=4)
-    s = K @ q
-    a = np.exp(s - s.max()); a /= a.sum()
-    eps = 2.0 ** -8
-    worst = np.zeros(3)
-    for _ in range(200):
-        at = a * (1 + rng.uniform(-eps, eps, size=50))
-        worst = np.maximum(worst, np.abs(at @ V - a @ V))
-    assert (worst <= eps * A.weight_spread(q, K, V, 1.0)).all()
