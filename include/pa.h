@@ -12,8 +12,12 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All tensors are caller-owned.  Device pointers point to CUDA device
- *    memory of the current device; the library never allocates, frees or
- *    retains device memory.  Host pointers are only read during the call.
+ *    memory of the current device; the library never allocates or frees
+ *    device memory and keeps no pointer to caller memory after a call
+ *    returns.  The only device memory the library owns is the static array
+ *    of pa_decode_static_scratch (PA_STATIC_SCRATCH_BYTES on every device
+ *    that loads the library, held until the process exits).  Host pointers
+ *    are only read during the call.
  *  - Element types: K/V caches, q, new keys/values are bf16 (2 bytes);
  *    attention output is bf16 or fp32 (see PA_DTYPE_*).  Integers are the
  *    fixed-width types named in each signature.
@@ -197,7 +201,10 @@ int pa_lse_merge(void* out, int out_dtype, const float* part_max,
  *    anything is launched.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is cached per CUDA context: a
+ *    context created anew on the device (after cudaDeviceReset, say) holds
+ *    its own copy of the array, and the first call in it looks the address
+ *    up again.
  *  - All calls share the one array and it keeps whatever the last call left
  *    there.  Nothing in it needs to start at zero: every value the merge
  *    reads was written earlier in the same call.  Calls whose kernels
@@ -436,8 +443,11 @@ int pa_alloc_sequence(pa_alloc_t* a, int64_t seq, int num_tokens);
  * eviction queue, which drops that block's key.  Partly filled blocks are
  * never registered; when a block fills under a key that another block
  * already holds, it is left unregistered and returns to the free list when
- * released.  Keys are 64-bit chained hashes; a lookup also compares the
- * block's token ids and parent key.
+ * released.  Keys are exact: each distinct token prefix ending on a block
+ * boundary is interned once (its parent prefix and its block's token ids),
+ * and a 64-bit chained hash serves only to find candidates, every one of
+ * which is compared in full, so a hash collision can never match the wrong
+ * prefix.
  * ------------------------------------------------------------------------- */
 
 /* Switch caching on (enable != 0) or off.  Only while no sequence exists;
@@ -445,6 +455,17 @@ int pa_alloc_sequence(pa_alloc_t* a, int64_t seq, int num_tokens);
  * list (oldest first, so the newest is handed out first).
  * PA_ERR_INVALID_ARG otherwise. */
 int pa_alloc_enable_prefix_caching(pa_alloc_t* a, int enable);
+
+/* Testing hook: the 64-bit hash that buckets the interned prefixes is ANDed
+ * with mask (all bits by default); mask = 0 puts every prefix in one bucket,
+ * so every lookup meets colliding candidates and must tell them apart by
+ * content.  Only while no sequence exists and no prefix is interned
+ * (PA_ERR_INVALID_ARG otherwise).  Results never depend on the mask. */
+int pa_alloc_set_key_mask(pa_alloc_t* a, uint64_t mask);
+
+/* Number of interned prefixes (held by registered blocks, sequences, or
+ * longer prefixes); -1 if a is NULL. */
+int pa_alloc_num_prefix_nodes(const pa_alloc_t* a);
 
 /* New sequence with known prompt token ids tokens[0 .. num_tokens-1].
  * With caching on, its leading full blocks are looked up in order and the

@@ -100,6 +100,8 @@ _SIGS = {
     "pa_alloc_free_list": (_c_int, [_vp, _i32p, _c_int]),
     "pa_alloc_get_stats": (_c_int, [_vp, ctypes.POINTER(AllocStats)]),
     "pa_alloc_enable_prefix_caching": (_c_int, [_vp, _c_int]),
+    "pa_alloc_set_key_mask": (_c_int, [_vp, ctypes.c_uint64]),
+    "pa_alloc_num_prefix_nodes": (_c_int, [_vp]),
     "pa_alloc_sequence_tokens": (_c_int, [_vp, ctypes.c_int64, _i32p, _c_int, ctypes.POINTER(_c_int)]),
     "pa_alloc_append_token": (_c_int, [_vp, ctypes.c_int64, ctypes.c_int32, _i64p, _i32p, _i32p]),
     "pa_alloc_num_cached": (_c_int, [_vp]),
@@ -494,6 +496,14 @@ class BlockAllocator:
 
     def enable_prefix_caching(self, enable=True):
         return _lib.pa_alloc_enable_prefix_caching(self._h, 1 if enable else 0)
+
+    def set_key_mask(self, mask):
+        """Testing hook: bucket the interned prefixes by hash & mask (0: one
+        bucket, every lookup meets colliding candidates)."""
+        return _lib.pa_alloc_set_key_mask(self._h, int(mask) & 0xFFFFFFFFFFFFFFFF)
+
+    def num_prefix_nodes(self):
+        return _lib.pa_alloc_num_prefix_nodes(self._h)
 
     def allocate_tokens(self, seq, tokens):
         """New sequence with known prompt token ids.  Returns (status,

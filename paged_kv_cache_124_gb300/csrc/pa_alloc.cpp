@@ -25,9 +25,13 @@
 // but kept, least recently released first, in an eviction queue; a later
 // prompt with the same prefix revives it (count 0 -> 1) instead of writing
 // it again.  Fresh blocks come from the free list first and only then by
-// evicting the queue's oldest block.  Keys are 64-bit chained hashes; a
-// lookup also compares the block's own tokens and its parent's key, so a
-// wrong match needs two different prefixes whose 64-bit parent keys collide.
+// evicting the queue's oldest block.  The key of a block is exact: every
+// distinct token prefix that ends on a block boundary is interned once as a
+// node (its parent prefix's node id and the block's token ids), and two keys
+// are equal only when they are the same node.  A 64-bit chained hash only
+// buckets the nodes; a lookup compares the parent node id and the token ids,
+// so a hash collision costs a comparison and can never reuse the wrong KV.
+// A node lives while a registered block, a sequence or a child node holds it.
 
 #include <algorithm>
 #include <cstdint>
@@ -61,7 +65,16 @@ struct Sequence {
     int32_t length = 0;           // cached positions
     bool has_tokens = false;      // token ids known: full blocks can be registered
     std::vector<int32_t> tokens;  // token id of every position (when has_tokens)
-    std::vector<uint64_t> keys;   // key of every full block (when has_tokens)
+    std::vector<int64_t> keys;    // prefix node of every full block (when has_tokens and caching)
+};
+
+// One interned prefix: the prefix of its parent node (0 = the empty prefix)
+// followed by one block of token ids.
+struct PrefixNode {
+    int64_t parent;
+    uint64_t hash;
+    int64_t holders;              // registered blocks, sequences and child nodes holding it
+    std::vector<int32_t> tokens;
 };
 
 }  // namespace
@@ -75,10 +88,13 @@ struct pa_alloc {
     int64_t num_cow_copies = 0;
     // prefix cache
     bool caching = false;
-    std::unordered_map<uint64_t, int32_t> index;       // key -> registered block
+    std::unordered_map<int64_t, PrefixNode> nodes;      // node id -> interned prefix
+    std::unordered_multimap<uint64_t, int64_t> by_hash; // bucket -> node ids
+    int64_t next_node = 1;
+    uint64_t hash_mask = ~0ull;                         // test hook: fewer bits, more collisions
+    std::unordered_map<int64_t, int32_t> index;         // node -> registered block
     std::vector<char> registered;
-    std::vector<uint64_t> reg_key, reg_parent;
-    std::vector<std::vector<int32_t>> reg_tokens;
+    std::vector<int64_t> reg_node;
     std::list<int32_t> lru;                             // zero-count registered blocks, oldest first
     std::vector<std::list<int32_t>::iterator> lru_pos;
     std::vector<char> in_lru;
@@ -90,38 +106,93 @@ struct pa_alloc {
     int32_t num_swapped = 0;
 
     pa_alloc(int nb, int bs)
-        : num_blocks(nb), block_size(bs), refs(nb, 0), registered(nb, 0), reg_key(nb, 0), reg_parent(nb, 0),
-          reg_tokens(nb), lru_pos(nb), in_lru(nb, 0) {
+        : num_blocks(nb), block_size(bs), refs(nb, 0), registered(nb, 0), reg_node(nb, 0), lru_pos(nb),
+          in_lru(nb, 0) {
         free_stack.reserve(nb);
         for (int b = nb - 1; b >= 0; --b) free_stack.push_back(b);
     }
 
     int64_t available() const { return (int64_t)free_stack.size() + (int64_t)lru.size(); }
 
+    // The node of prefix `parent` + tokens[0 .. block_size), or -1.
+    int64_t find_node(int64_t parent, const int32_t* tokens) const {
+        const uint64_t h = block_key(parent ? nodes.at(parent).hash : kRootKey, tokens, block_size) & hash_mask;
+        auto range = by_hash.equal_range(h);
+        for (auto it = range.first; it != range.second; ++it) {
+            const PrefixNode& n = nodes.at(it->second);
+            if (n.parent == parent && std::equal(tokens, tokens + block_size, n.tokens.begin())) return it->second;
+        }
+        return -1;
+    }
+
+    // That node, created if new; the caller holds it (release with drop_node).
+    int64_t intern(int64_t parent, const int32_t* tokens) {
+        int64_t id = find_node(parent, tokens);
+        if (id >= 0) {
+            nodes.at(id).holders += 1;
+            return id;
+        }
+        id = next_node++;
+        PrefixNode n;
+        n.parent = parent;
+        n.hash = block_key(parent ? nodes.at(parent).hash : kRootKey, tokens, block_size);
+        n.holders = 1;
+        n.tokens.assign(tokens, tokens + block_size);
+        by_hash.emplace(n.hash & hash_mask, id);
+        nodes.emplace(id, std::move(n));
+        if (parent) nodes.at(parent).holders += 1;
+        return id;
+    }
+
+    void hold_node(int64_t id) {
+        if (id) nodes.at(id).holders += 1;
+    }
+
+    // Let go of a node; one that nothing holds any more is forgotten, and so
+    // is its parent in turn.
+    void drop_node(int64_t id) {
+        while (id) {
+            auto it = nodes.find(id);
+            if (--it->second.holders > 0) return;
+            auto range = by_hash.equal_range(it->second.hash & hash_mask);
+            for (auto h = range.first; h != range.second; ++h)
+                if (h->second == id) {
+                    by_hash.erase(h);
+                    break;
+                }
+            const int64_t parent = it->second.parent;
+            nodes.erase(it);
+            id = parent;
+        }
+    }
+
+    void drop_keys(Sequence& s) {
+        for (int64_t k : s.keys) drop_node(k);
+        s.keys.clear();
+    }
+
     void unregister(int32_t b) {
         if (!registered[b]) return;
-        auto it = index.find(reg_key[b]);
+        auto it = index.find(reg_node[b]);
         if (it != index.end() && it->second == b) index.erase(it);
         registered[b] = 0;
-        reg_tokens[b].clear();
+        drop_node(reg_node[b]);
+        reg_node[b] = 0;
     }
 
-    void register_block(int32_t b, uint64_t key, uint64_t parent, const int32_t* tokens) {
-        if (index.count(key)) return;           // another block already holds this content
-        index.emplace(key, b);
+    void register_block(int32_t b, int64_t node) {
+        if (index.count(node)) return;          // another block already holds this prefix
+        index.emplace(node, b);
         registered[b] = 1;
-        reg_key[b] = key;
-        reg_parent[b] = parent;
-        reg_tokens[b].assign(tokens, tokens + block_size);
+        reg_node[b] = node;
+        hold_node(node);
     }
 
-    // Registered block with this key, parent and tokens, or -1.
-    int32_t lookup(uint64_t key, uint64_t parent, const int32_t* tokens) const {
-        auto it = index.find(key);
-        if (it == index.end()) return -1;
-        const int32_t b = it->second;
-        if (reg_parent[b] != parent || !std::equal(tokens, tokens + block_size, reg_tokens[b].begin())) return -1;
-        return b;
+    // Registered block holding this prefix node, or -1.
+    int32_t lookup(int64_t node) const {
+        if (node < 0) return -1;
+        auto it = index.find(node);
+        return it == index.end() ? -1 : it->second;
     }
 
     void lru_remove(int32_t b) {
@@ -177,15 +248,14 @@ struct pa_alloc {
         if (!token) {
             s.has_tokens = false;                        // content no longer known
             s.tokens.clear();
-            s.keys.clear();
+            drop_keys(s);
         } else if (s.has_tokens) {
             s.tokens.push_back(*token);
             if (caching && off == block_size - 1) {      // the block just became full
-                const uint64_t parent = s.keys.empty() ? kRootKey : s.keys.back();
-                const int32_t* t = s.tokens.data() + (s.length - block_size);
-                const uint64_t key = block_key(parent, t, block_size);
-                s.keys.push_back(key);
-                register_block(blk, key, parent, t);
+                const int64_t parent = s.keys.empty() ? 0 : s.keys.back();
+                const int64_t node = intern(parent, s.tokens.data() + (s.length - block_size));
+                s.keys.push_back(node);
+                register_block(blk, node);
             }
         }
         return PA_OK;
@@ -258,28 +328,19 @@ int pa_alloc_sequence_tokens(pa_alloc_t* a, int64_t seq, const int32_t* tokens, 
     const int B = a->block_size;
     const int64_t need = ((int64_t)num_tokens + B - 1) / B;
     const int full = num_tokens / B;
-    // plan: keys of the full blocks, and the leading blocks already cached
-    std::vector<uint64_t> keys, parents;
+    // plan: the leading full blocks already cached (a registered block's
+    // prefix node exists, so the walk stops at the first prefix without one)
     std::vector<int32_t> hits;
     int64_t revived_from_queue = 0;
     if (a->caching) {
-        uint64_t parent = kRootKey;
-        bool matching = true;
+        int64_t parent = 0;
         for (int i = 0; i < full; ++i) {
-            const int32_t* t = tokens + (size_t)i * B;
-            const uint64_t key = block_key(parent, t, B);
-            if (matching) {
-                const int32_t b = a->lookup(key, parent, t);
-                if (b >= 0) {
-                    hits.push_back(b);
-                    revived_from_queue += a->in_lru[b] ? 1 : 0;
-                } else {
-                    matching = false;
-                }
-            }
-            keys.push_back(key);
-            parents.push_back(parent);
-            parent = key;
+            const int64_t node = a->find_node(parent, tokens + (size_t)i * B);
+            const int32_t b = a->lookup(node);
+            if (b < 0) break;
+            hits.push_back(b);
+            revived_from_queue += a->in_lru[b] ? 1 : 0;
+            parent = node;
         }
     }
     const int64_t fresh = need - (int64_t)hits.size();
@@ -292,15 +353,18 @@ int pa_alloc_sequence_tokens(pa_alloc_t* a, int64_t seq, const int32_t* tokens, 
         a->refs[b] += 1;
         s.table.push_back(b);
     }
-    for (int64_t i = (int64_t)hits.size(); i < need; ++i) {
-        const int32_t b = a->take();
-        s.table.push_back(b);
-        if (a->caching && i < full) a->register_block(b, keys[i], parents[i], tokens + (size_t)i * B);
+    for (int64_t i = (int64_t)hits.size(); i < need; ++i) s.table.push_back(a->take());
+    if (a->caching) {                      // every full block's prefix node; fresh ones registered
+        int64_t parent = 0;
+        for (int i = 0; i < full; ++i) {
+            parent = a->intern(parent, tokens + (size_t)i * B);
+            s.keys.push_back(parent);
+            if (i >= (int)hits.size()) a->register_block(s.table[i], parent);
+        }
     }
     s.length = num_tokens;
     s.has_tokens = true;
     s.tokens.assign(tokens, tokens + num_tokens);
-    s.keys = std::move(keys);
     a->seqs.emplace(seq, std::move(s));
     *num_cached_tokens = (int)hits.size() * B;
     a->prompt_tokens += num_tokens;
@@ -316,6 +380,7 @@ int pa_alloc_fork(pa_alloc_t* a, int64_t parent, int64_t child) {
     if (it->second.swapped) return PA_ERR_SWAPPED;
     Sequence s = it->second;                 // copy before insert (rehash)
     for (int32_t b : s.table) a->refs[b] += 1;
+    for (int64_t k : s.keys) a->hold_node(k);
     a->seqs.emplace(child, std::move(s));
     return PA_OK;
 }
@@ -369,6 +434,7 @@ int pa_alloc_free(pa_alloc_t* a, int64_t seq) {
     } else {
         a->release_table(it->second.table);
     }
+    a->drop_keys(it->second);
     a->seqs.erase(it);
     return PA_OK;
 }
@@ -464,6 +530,14 @@ int pa_alloc_enable_prefix_caching(pa_alloc_t* a, int enable) {
     a->caching = enable != 0;
     return PA_OK;
 }
+
+int pa_alloc_set_key_mask(pa_alloc_t* a, uint64_t mask) {
+    if (!a || !a->seqs.empty() || !a->nodes.empty()) return PA_ERR_INVALID_ARG;
+    a->hash_mask = mask;
+    return PA_OK;
+}
+
+int pa_alloc_num_prefix_nodes(const pa_alloc_t* a) { return a ? (int)a->nodes.size() : -1; }
 
 int pa_alloc_num_cached(const pa_alloc_t* a) { return a ? (int)a->lru.size() : -1; }
 

@@ -285,10 +285,16 @@ def test_content_invariant_under_churn(view, seed, nb, bs):
     assert m.num_cached() >= 0
 
 
+@pytest.mark.parametrize("mask", [0xFFFFFFFFFFFFFFFF, 0x3, 0], ids=["hash", "4_buckets", "all_collide"])
 @pytest.mark.parametrize("seed,nb,bs", [(5, 16, 4), (6, 48, 8), (7, 20, 2)])
-def test_abi_matches_oracle_operation_by_operation(seed, nb, bs):
+def test_abi_matches_oracle_operation_by_operation(seed, nb, bs, mask):
+    """The C++ manager against the oracle's exact (whole token prefix) keys,
+    op by op; with the hash that buckets its prefixes cut to 2 bits or to
+    none, every lookup meets colliding candidates, and the results must not
+    change."""
     rng = np.random.default_rng(seed)
     ref, dut = _OracleView(nb, bs), _AbiView(nb, bs)
+    assert dut.m.set_key_mask(mask) == 0
     assert ref.enable(True) == dut.enable(True) == 0
     docs = [[int(x) for x in rng.integers(0, 4, size=5 * bs)] for _ in range(3)]
     seqs = list(range(10))
@@ -325,6 +331,50 @@ def test_abi_matches_oracle_operation_by_operation(seed, nb, bs):
     assert st["num_prompt_tokens"] == ref.m.num_prompt_tokens
     assert st["num_cached_tokens"] == ref.m.num_cached_tokens
     assert st["num_used"] + st["num_free"] + st["num_cached"] == nb
+    # every interned prefix is let go once nothing holds it
+    for s_ in seqs:
+        assert dut.free(s_) == 0
+    assert dut.m.num_prefix_nodes() >= dut.num_cached()
+    assert dut.enable(False) == 0
+    assert dut.m.num_prefix_nodes() == 0
+
+
+def test_colliding_keys_never_match_another_prefix():
+    """Two prefixes that end in the same block of tokens after different
+    first blocks: with every hash colliding (mask 0), the second block of one
+    must not be taken for the other's, however their parents' hashes
+    compare.  The oracle's keys are whole token prefixes."""
+    B = 4
+    A_, B_, X, Y = [1, 1, 1, 1], [2, 2, 2, 2], [7, 7, 7, 7], [8, 8, 8, 8]
+    for mask in (0xFFFFFFFFFFFFFFFF, 0):
+        m = api.BlockAllocator(16, B)
+        assert m.set_key_mask(mask) == 0
+        assert m.enable_prefix_caching(True) == 0
+        assert m.allocate_tokens(1, A_ + X) == (0, 0)
+        assert m.allocate_tokens(2, B_ + Y) == (0, 0)
+        assert m.allocate_tokens(3, B_ + X + [5]) == (0, B)          # B_ hits, then B_ + X is new
+        assert m.block_table(3)[0] == m.block_table(2)[0]
+        assert m.block_table(3)[1] not in (m.block_table(1)[1], m.block_table(2)[1])
+        assert m.allocate_tokens(4, A_ + X + [6]) == (0, 2 * B)      # the real match is still found
+        assert m.block_table(4)[:2] == m.block_table(1)
+        assert m.allocate_tokens(5, B_ + X) == (0, 2 * B)            # and the one registered by sequence 3
+        assert m.block_table(5) == m.block_table(3)[:2]
+        ref = _OracleView(16, B)
+        assert ref.enable(True) == 0
+        for s_, ids in ((1, A_ + X), (2, B_ + Y), (3, B_ + X + [5]), (4, A_ + X + [6]), (5, B_ + X)):
+            ref.tokens(s_, ids)
+            assert ref.table(s_) == m.block_table(s_)
+
+
+def test_key_mask_only_before_use():
+    m = api.BlockAllocator(8, 4)
+    assert m.enable_prefix_caching(True) == 0
+    assert m.allocate_tokens(1, list(range(8))) == (0, 0)
+    assert m.set_key_mask(0) == api.PA_ERR_INVALID_ARG          # a sequence exists
+    assert m.free(1) == 0
+    assert m.set_key_mask(0) == api.PA_ERR_INVALID_ARG          # its prefixes are still cached
+    assert m.enable_prefix_caching(False) == 0 and m.num_prefix_nodes() == 0
+    assert m.set_key_mask(0) == 0
 
 
 def test_switching_off_releases_the_cache():
