@@ -18,8 +18,9 @@ workload instead.
 """
 import os
 
-# The oracle's NumPy work is timed single-threaded; fix BLAS threads before
-# NumPy loads.
+# The oracle's NumPy work runs BLAS on one thread per process (the all-core
+# CPU leg starts one worker process per core); fix BLAS threads before NumPy
+# loads.
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -60,12 +61,19 @@ PREFILL_WORKLOADS = {
 }
 
 WORKLOADS = {
-    "batch64_8b": lambda seed, B: I.batch64_8b(seed, B),
-    "long_context": lambda seed, B: I.long_context(seed, B),
-    "cow_sampling": lambda seed, B: I.cow_sampling(seed, block_size=B),
-    "mixed_batch": lambda seed, B: I.mixed_batch(seed, B, n_layers=1),
-    "tiny_gqa": lambda seed, B: I.tiny_gqa(seed),
+    "batch64_8b": lambda seed, B, L: I.batch64_8b(seed, B),
+    "long_context": lambda seed, B, L: I.long_context(seed, B),
+    "cow_sampling": lambda seed, B, L: I.cow_sampling(seed, block_size=B),
+    "mixed_batch": lambda seed, B, L: I.mixed_batch(seed, B, n_layers=L),
+    "tiny_gqa": lambda seed, B, L: I.tiny_gqa(seed),
 }
+
+
+def workload_scenario(args, seed):
+    """The decode workload's scenario; the continuous-batching step runs
+    every one of its 32 layers unless --layers says otherwise."""
+    layers = args.layers or 32
+    return WORKLOADS[args.workload](seed, args.block_size, layers)
 
 
 # ----------------------------------------------------------------------------
@@ -227,6 +235,12 @@ class ClockSampler:
 # our implementation
 # ----------------------------------------------------------------------------
 
+def _quantiles(xs):
+    xs = sorted(xs)
+    pick = lambda f: xs[min(len(xs) - 1, max(0, int(round(f * (len(xs) - 1)))))]
+    return statistics.median(xs), pick(0.1), pick(0.9)
+
+
 def run_ours(args, world, rank, local):
     from paged_kv_cache_124_gb300 import api
     from paged_kv_cache_124_gb300.runner import ScenarioRunner
@@ -235,52 +249,62 @@ def run_ours(args, world, rank, local):
     init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     seed = replica_seed(args.seed, rank)
-    sc = WORKLOADS[args.workload](seed, args.block_size)
-    run = ScenarioRunner(sc, device=dev, data_device="cpu").replay()
+    sc = workload_scenario(args, seed)
+    L = sc.n_layers
+    # token data on the GPU generator for multi-layer workloads (tens of GB)
+    run = ScenarioRunner(sc, device=dev, data_device="cpu" if L == 1 else dev).replay()
     tables, ctx, max_ctx = run.decode_metadata()
     S = len(sc.decode_seqs)
     ctx_h = ctx.cpu().numpy()
     # the step's new token per sequence: the last position of each context
+    # (the same slot in every layer: the layers share the block tables)
     slots_h = np.array([run.alloc.slot_mapping(s, run.alloc.seq_len(s) - 1, 1)[0] for s in sc.decode_seqs])
     slots = torch.from_numpy(slots_h).to(dev)
-    k_new, v_new = I.append_kv(sc.seed, 0, 10 ** 6, S, sc.n_kv_heads, sc.d_head)
-    k_new, v_new = k_new.to(dev), v_new.to(dev)
-    q = I.decode_q(sc.seed, 0, S, sc.n_q_heads, sc.d_head).to(dev)
+    kv_new = [I.append_kv(sc.seed, l, 10 ** 6, S, sc.n_kv_heads, sc.d_head) for l in range(L)]
+    k_new = torch.stack([k for k, _ in kv_new]).to(dev)          # [L, S, Hkv, D]
+    v_new = torch.stack([v for _, v in kv_new]).to(dev)
+    q = torch.stack([I.decode_q(sc.seed, l, S, sc.n_q_heads, sc.d_head) for l in range(L)]).to(dev)
     out = torch.empty_like(q)
     P = args.partition
     ws = api.decode_workspace(S, sc.n_q_heads, sc.d_head, max_ctx, P, device=dev)
-    kc, vc = run.k_caches[0], run.v_caches[0]
+    kcs, vcs = run.k_caches, run.v_caches
     fp8 = args.kv_dtype == "fp8"
+    scales = [(1.0, 1.0)] * L
     if fp8:
-        # the same cache as E4M3 codes, scales from the data's range (setup, not timed)
-        k_scale = float(kc.float().nan_to_num(0.0).abs().amax()) / 448.0
-        v_scale = float(vc.float().nan_to_num(0.0).abs().amax()) / 448.0
-        kc = (kc.float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
-        vc = (vc.float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+        # the same caches as E4M3 codes, scales from the data's range (setup, not timed)
+        scales, k8, v8 = [], [], []
+        for kc, vc in zip(kcs, vcs):
+            ks = float(kc.float().nan_to_num(0.0).abs().amax()) / 448.0
+            vs = float(vc.float().nan_to_num(0.0).abs().amax()) / 448.0
+            scales.append((ks, vs))
+            k8.append((kc.float() / ks).to(torch.float8_e4m3fn).view(torch.uint8))
+            v8.append((vc.float() / vs).to(torch.float8_e4m3fn).view(torch.uint8))
+        kcs, vcs = k8, v8
     stream = torch.cuda.current_stream(dev)
-    dec_bytes, write_bytes = algorithmic_bytes(sc, ctx_h, S, 1 if fp8 else 2)
-    # our kernels per step: reshape_and_cache, the partition kernel and, when a
-    # sequence can span several partitions, the merge kernel
-    launches_per_step = 2 + (1 if api.pa_decode_workspace_size(S, sc.n_q_heads, sc.d_head, max_ctx, P) else 0)
+    dec_bytes, write_bytes = algorithmic_bytes(sc, ctx_h, S, 1 if fp8 else 2)     # per layer
+    # our kernels per layer: reshape_and_cache, the partition kernel and, when
+    # a sequence can span several partitions, the merge kernel
+    launches_per_layer = 2 + (1 if api.pa_decode_workspace_size(S, sc.n_q_heads, sc.d_head, max_ctx, P) else 0)
 
-    def cache_write(k_, v_, slots_, st_):
+    def cache_write(l, k_, v_, slots_, st_):
         if fp8:
-            api.pa_reshape_and_cache_fp8(kc, vc, k_, v_, slots_, k_scale, v_scale, stream=st_)
+            api.pa_reshape_and_cache_fp8(kcs[l], vcs[l], k_, v_, slots_, scales[l][0], scales[l][1], stream=st_)
         else:
-            api.pa_reshape_and_cache(kc, vc, k_, v_, slots_, stream=st_)
+            api.pa_reshape_and_cache(kcs[l], vcs[l], k_, v_, slots_, stream=st_)
 
-    def decode_call(q_, tables_, ctx_, st_):
+    def decode_call(l, q_, tables_, ctx_, st_):
         if fp8:
-            api.pa_decode_fp8(out, q_, kc, vc, tables_, ctx_, sc.block_size, sc.scale, k_scale, v_scale,
-                              sc.n_q_heads, sc.n_kv_heads, sc.d_head, max_ctx, partition_size=P, workspace=ws,
-                              stream=st_)
+            api.pa_decode_fp8(out[l], q_, kcs[l], vcs[l], tables_, ctx_, sc.block_size, sc.scale, scales[l][0],
+                              scales[l][1], sc.n_q_heads, sc.n_kv_heads, sc.d_head, max_ctx, partition_size=P,
+                              workspace=ws, stream=st_)
         else:
-            api.pa_decode(out, q_, kc, vc, tables_, ctx_, sc.block_size, sc.scale, sc.n_q_heads, sc.n_kv_heads,
-                          sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=st_)
+            api.pa_decode(out[l], q_, kcs[l], vcs[l], tables_, ctx_, sc.block_size, sc.scale, sc.n_q_heads,
+                          sc.n_kv_heads, sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=st_)
 
     def step():
-        cache_write(k_new, v_new, slots, stream)
-        decode_call(q, tables, ctx, stream)
+        for l in range(L):
+            cache_write(l, k_new[l], v_new[l], slots, stream)
+            decode_call(l, q[l], tables, ctx, stream)
 
     clocks = ClockSampler(local) if rank == 0 else None
     if clocks:
@@ -288,48 +312,69 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         step()
     K = args.steps
-    # Timed region: K steps between two events.  The decode call of every
-    # SAMPLE-th step is also bracketed by events (an event between two kernels
-    # stops the second from overlapping the first's drain, so only a sample of
-    # steps carries them); their mean is the kernels' average duration.
+    # Timed region: K whole steps (every layer's cache write and decode)
+    # between two events.  The decode call of layer 0 of every SAMPLE-th step
+    # is also bracketed by events: the isolated duration of one call (an event
+    # between two kernels stops the second from overlapping the first's drain,
+    # so only a sample of steps carries them).
     SAMPLE = 8
     ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range((K + SAMPLE - 1) // SAMPLE)]
-
-    def decode(q_, tables_, ctx_):
-        decode_call(q_, tables_, ctx_, stream)
-
     barrier(world)
     torch.cuda.synchronize(dev)
     ev_start.record(stream)
     for i in range(K):
-        cache_write(k_new, v_new, slots, stream)
-        if i % SAMPLE == 0:
-            a, b = ev_dec[i // SAMPLE]
-            a.record(stream)
-            decode(q, tables, ctx)
-            b.record(stream)
-        else:
-            decode(q, tables, ctx)
+        for l in range(L):
+            cache_write(l, k_new[l], v_new[l], slots, stream)
+            if l == 0 and i % SAMPLE == 0:
+                a, b = ev_dec[i // SAMPLE]
+                a.record(stream)
+                decode_call(l, q[l], tables, ctx, stream)
+                b.record(stream)
+            else:
+                decode_call(l, q[l], tables, ctx, stream)
     ev_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    clk = clocks.stop() if clocks else None
     step_s = ev_start.elapsed_time(ev_end) / 1e3
-    dec_s_avg = sum(a.elapsed_time(b) for a, b in ev_dec) / len(ev_dec) / 1e3
-    total_s, total_bytes = reduce_timing(step_s, (dec_bytes + write_bytes) * K, world, dev)
+    isolated_s = sum(a.elapsed_time(b) for a, b in ev_dec) / len(ev_dec) / 1e3
+    total_s, total_bytes = reduce_timing(step_s, (dec_bytes + write_bytes) * L * K, world, dev)
     _, total_seqs = reduce_timing(step_s, S * K, world, dev)
 
+    # ---- decode calls back to back: the kernels' average duration ----------
+    # Repetitions of CALLS pa_decode calls (layers in turn) between two
+    # events, run for at least MIN_LOOP_S in all, so that the clock sampler
+    # sees the load; median, p10 and p90 of the per-call time over the
+    # repetitions.
+    CALLS, MIN_REPS, MIN_LOOP_S = 200, 5, 1.2
+    per_call = []
+    t_loop = time.perf_counter()
+    while len(per_call) < MIN_REPS or (time.perf_counter() - t_loop < MIN_LOOP_S and len(per_call) < 500):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for c in range(CALLS):
+            decode_call(c % L, q[c % L], tables, ctx, stream)
+        e1.record(stream)
+        e1.synchronize()
+        per_call.append(e0.elapsed_time(e1) / 1e3 / CALLS)
+    loop_s = time.perf_counter() - t_loop
+    clk = clocks.stop() if clocks else None
+    dec_med, dec_p10, dec_p90 = _quantiles(per_call)
+    step_per_layer_s = total_s / K / L
+    if dec_med > step_per_layer_s * 1.0001:
+        raise RuntimeError("decode call (%.2f us back to back) longer than a whole step's layer (%.2f us): the "
+                           "timing is inconsistent" % (dec_med * 1e6, step_per_layer_s * 1e6))
+
     # ---- end to end through the public API with host buffers ---------------
-    # Every step copies its inputs from pinned host memory (q, the new K/V
-    # rows, slot mapping, block tables, context lengths), runs the cache write
-    # and the decode, copies the output back and waits for it.  The step is
-    # issued once into a CUDA graph (the library's calls are capturable) and
-    # replayed; the eager form is timed too.
-    # The inputs travel packed in one page-locked buffer (one copy per step;
-    # six small copies each paid their own latency), and the calls read views
-    # of its device twin.
+    # Every step copies its inputs from pinned host memory (q and the new K/V
+    # rows of every layer, slot mapping, block tables, context lengths), runs
+    # every layer's cache write and decode, copies the outputs back and waits
+    # for them.  The step is issued once into a CUDA graph (the library's
+    # calls are capturable) and replayed; the eager form is timed too.  The
+    # inputs travel packed in one page-locked buffer (one copy per step; six
+    # small copies each paid their own latency), and the calls read views of
+    # its device twin.
     inputs = (q, k_new, v_new, slots, tables, ctx)
     offs, total = [], 0
     for t in inputs:
@@ -349,8 +394,9 @@ def run_ours(args, world, rank, local):
 
     def e2e_body(st):
         pack_d.copy_(pack_h, non_blocking=True)
-        cache_write(k_d, v_d, slots_d, st)
-        decode_call(q_d, tables_d, ctx_d, st)
+        for l in range(L):
+            cache_write(l, k_d[l], v_d[l], slots_d, st)
+            decode_call(l, q_d[l], tables_d, ctx_d, st)
         out_h.copy_(out, non_blocking=True)
 
     def eager_step():
@@ -379,42 +425,54 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(dev)
         e2e_times[name] = time.perf_counter() - t0
         barrier(world)
-    e2e_total_s, e2e_bytes = reduce_timing(e2e_times["graph"], (dec_bytes + write_bytes) * K, world, dev)
+    e2e_total_s, e2e_bytes = reduce_timing(e2e_times["graph"], (dec_bytes + write_bytes) * L * K, world, dev)
     eager_total_s, _ = reduce_timing(e2e_times["eager"], 0, world, dev)
 
     if rank != 0:
         return None
     peak, peak_kind = measured_peak()
-    achieved = dec_bytes / dec_s_avg / 1e9
+    achieved = dec_bytes / dec_med / 1e9
     value = total_bytes / total_s / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "fp8_e4m3" if fp8 else "bf16",
         "data": "synthetic",
-        "config": {"workload": sc.name, "num_seqs": S, "context_lens": "uniform [512, 4096]" if
-                   args.workload == "batch64_8b" else "see workload", "total_context": int(ctx_h.sum()),
+        "config": {"workload": sc.name, "num_seqs": S, "n_layers": L,
+                   "context_lens": {"batch64_8b": "uniform [512, 4096]", "long_context": "32,768 each",
+                                    "mixed_batch": "lognormal (median 700, sigma 1) clipped to [1, 16384]"}.get(
+                                        args.workload, "see workload"), "total_context": int(ctx_h.sum()),
                    "n_q_heads": sc.n_q_heads, "n_kv_heads": sc.n_kv_heads, "d_head": sc.d_head,
                    "block_size": sc.block_size, "num_blocks": sc.num_blocks, "placement": "seeded random",
                    "partition_size": P or "library default",
-                   "l2": "inputs larger than L2 (%.0f MB KV read per step vs 129 MB L2); no flush" %
+                   "l2": "inputs larger than L2 (%.0f MB KV read per layer vs 129 MB L2); no flush" %
                          (dec_bytes / 1e6),
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "single GPU"},
         "seqs_per_s": round(total_seqs / total_s, 1),
+        "ms_per_layer": round(total_s / K / L * 1e3, 5),
         "roofline": {"bound": "hbm", "kernel": "pa_decode%s (decode_partition_kernel + lse_merge_kernel)" %
                      ("_fp8" if fp8 else ""),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(PROFILE_SUMMARY_FP8 if fp8 else PROFILE_SUMMARY),
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(PROFILE_SUMMARY_FP8 if fp8 else PROFILE_SUMMARY)
+                     if args.workload == "batch64_8b" and sc.block_size == 16 and P == 0 else None,
                      "algorithmic_bytes_per_launch": int(dec_bytes),
-                     "avg_launch_us": round(dec_s_avg * 1e6, 2)},
+                     "avg_launch_us": round(dec_med * 1e6, 2),
+                     "launch_us_p10_p90": [round(dec_p10 * 1e6, 2), round(dec_p90 * 1e6, 2)],
+                     "timing": "median over %d repetitions of %d pa_decode calls back to back between two events "
+                               "(%.2f s of calls)" % (len(per_call), CALLS, loop_s),
+                     "isolated_call_us": round(isolated_s * 1e6, 2),
+                     "isolated_call_timing": "events around layer 0's pa_decode on every %d-th timed step (%d "
+                                             "samples; the event pair keeps the call from overlapping the "
+                                             "kernel before it)" % (SAMPLE, len(ev_dec)),
+                     "step_frac": round(value / peak, 4)},
         "e2e": {"value": round(e2e_bytes / e2e_total_s / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_total_s / K * 1e3, 4), "issue": "CUDA graph of the step, replayed; inputs in one packed page-locked buffer, one copy in "
                 "and one out per step, waited for",
                 "eager_value": round(e2e_bytes / eager_total_s / 1e9, 2),
                 "eager_ms_per_step": round(eager_total_s / K * 1e3, 4)},
-        "gpu_launches": launches_per_step * K,
-        "decode_timing": "events around pa_decode on every %d-th timed step (%d samples)" % (SAMPLE, len(ev_dec)),
+        "gpu_launches": launches_per_layer * L * K,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -984,14 +1042,23 @@ def cache_ops_cpu_baseline(sc, slots_h, pairs_h, nb, budget_s):
 # ----------------------------------------------------------------------------
 
 def _oracle_sample(sc, seqs):
-    """Oracle replay of the workload with only `seqs` materialised."""
+    """Oracle replay of the workload's layer 0 with only `seqs` materialised
+    (every layer does the same work)."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     from _oracle_replay import OracleReplay
     sub = dataclasses.replace(sc, decode_seqs=list(seqs))
-    rep = OracleReplay(sub).replay()
+    rep = OracleReplay(sub, layers=[0]).replay()
     tab, lens = rep.tables()
     q = I.bf16_bits(I.decode_q(sc.seed, 0, len(sc.decode_seqs), sc.n_q_heads, sc.d_head))[list(seqs)]
     return rep, tab, lens, q
+
+
+def host_threads():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def _oracle_time(sc, rep, tab, lens, q):
@@ -1001,54 +1068,132 @@ def _oracle_time(sc, rep, tab, lens, q):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(sc, budget_s):
-    """The oracle as it stands, on a bounded sample: the first sequences of
-    the workload, as many as fit the time budget (about budget_s)."""
-    n = 1
-    seqs = [0]
-    rep, tab, lens, q = _oracle_sample(sc, seqs)
-    t = _oracle_time(sc, rep, tab, lens, q)
+def _oracle_time_procs(sc, rep, tab, lens, q, procs, reps):
+    """Seconds the oracle takes to decode the sample `reps` times on `procs`
+    host cores at once: the sample (its blocks compacted into a small pool)
+    goes to a temporary directory, and one worker process per core
+    (tests/_oracle_pool.py, started fresh, not forked from this process)
+    decodes its share of the sequences (longest first, each to the least
+    loaded worker).  All start together; the slowest worker's time counts."""
+    import shutil
+    B = sc.block_size
+    nblk = [-(-int(c) // B) for c in lens]
+    used = sorted(set(int(b) for i, n in enumerate(nblk) for b in tab[i, :n]))
+    remap = {b: i for i, b in enumerate(used)}
+    ctab = np.full(tab.shape, -1, dtype=np.int64)
+    for i, n in enumerate(nblk):
+        ctab[i, :n] = [remap[int(b)] for b in tab[i, :n]]
+    load = [0] * procs
+    assign = [[] for _ in range(procs)]
+    for i in sorted(range(len(lens)), key=lambda i: -int(lens[i])):
+        w = load.index(min(load))
+        assign[w].append(i)
+        load[w] += int(lens[i])
+    d = tempfile.mkdtemp(prefix="oracle_pool_")
+    try:
+        np.save(os.path.join(d, "k.npy"), rep.k[0][used])
+        np.save(os.path.join(d, "v.npy"), rep.v[0][used])
+        np.save(os.path.join(d, "tab.npy"), ctab)
+        np.save(os.path.join(d, "lens.npy"), np.asarray(lens, dtype=np.int64))
+        np.save(os.path.join(d, "q.npy"), np.asarray(q))
+        with open(os.path.join(d, "meta.json"), "w") as f:
+            json.dump({"assign": assign, "block_size": B, "scale": sc.scale, "reps": reps}, f)
+        worker = os.path.join(ROOT, "tests", "_oracle_pool.py")
+        ps = [subprocess.Popen([sys.executable, worker, d, str(w)], stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                               text=True) for w in range(procs)]
+        try:
+            for p_ in ps:
+                if p_.stdout.readline().strip() != "ready":
+                    raise RuntimeError("oracle worker failed to start")
+            for p_ in ps:
+                p_.stdin.write("go\n")
+                p_.stdin.flush()
+            elapsed = [json.loads(p_.stdout.readline())["elapsed"] for p_ in ps]
+        finally:
+            for p_ in ps:
+                if p_.poll() is None:
+                    p_.wait(timeout=600)
+        return max(elapsed)
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+
+
+def host_threads():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _cpu_leg(sc, budget_s, procs):
+    """The oracle as it stands on a bounded sample: the first sequences of
+    the workload, as many as fit about budget_s on `procs` cores, repeated
+    while a pass takes under half of it."""
+    def timed(rep, tab, lens, q, reps):
+        if procs <= 1:
+            return sum(_oracle_time(sc, rep, tab, lens, q) for _ in range(reps))
+        return _oracle_time_procs(sc, rep, tab, lens, q, procs, reps)
+
+    n = min(len(sc.decode_seqs), max(1, procs))
+    rep, tab, lens, q = _oracle_sample(sc, list(range(n)))
+    t = timed(rep, tab, lens, q, 1)
     while t < budget_s / 2 and n < len(sc.decode_seqs):
         n = min(len(sc.decode_seqs), max(n + 1, int(n * min(8.0, budget_s / max(t, 1e-3)))))
-        seqs = list(range(n))
-        rep, tab, lens, q = _oracle_sample(sc, seqs)
-        t = _oracle_time(sc, rep, tab, lens, q)
-    # a workload the oracle finishes quickly is run again until about half the budget has passed
+        rep, tab, lens, q = _oracle_sample(sc, list(range(n)))
+        t = timed(rep, tab, lens, q, 1)
     reps = 1
-    while t < budget_s / 2:
-        t += _oracle_time(sc, rep, tab, lens, q)
-        reps += 1
+    if t < budget_s / 2:
+        reps = max(1, int(budget_s / 2 / max(t, 1e-3)))
+        t = timed(rep, tab, lens, q, reps)
     dec_bytes, _ = algorithmic_bytes(sc, lens, 0)
-    return {"value": round(reps * dec_bytes / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "fp64 oracle decode of the first %d of %d sequences (%d positions, all %d query heads) "
-                      "of %s, %d time(s), %.1f s" % (n, len(sc.decode_seqs), int(np.sum(lens)), sc.n_q_heads,
-                                                     sc.name, reps, t)}
+    value = reps * dec_bytes / t / 1e9
+    sample = ("fp64 oracle decode of the first %d of %d sequences (%d positions, all %d query heads) of %s, "
+              "layer 0, %d time(s), %.1f s, %s" % (n, len(sc.decode_seqs), int(np.sum(lens)), sc.n_q_heads,
+                                                   sc.name, reps, t, "1 thread" if procs <= 1 else
+                                                   "%d worker processes at once, whole sequences each" % procs))
+    return value, sample, t
+
+
+def cpu_baseline(sc, budget_s):
+    """The oracle as it stands, on every host core at once (one worker
+    process per core) and on one core; each leg gets about half the
+    budget."""
+    procs = host_threads()
+    v1, s1, _ = _cpu_leg(sc, budget_s / 2, 1)
+    vn, sn, _ = _cpu_leg(sc, budget_s / 2, procs) if procs > 1 else (v1, s1, 0)
+    return {"value": round(vn, 4), "unit": UNIT, "cores": procs, "kind": "oracle", "sample": sn,
+            "single_thread": {"value": round(v1, 4), "cores": 1, "sample": s1},
+            "speedup_all_cores": round(vn / v1, 2)}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return None
-    sc = WORKLOADS[args.workload](args.seed, args.block_size)
-    per_step = max(1, args.ref_seqs_per_step)
+    sc = workload_scenario(args, args.seed)
+    threads = host_threads()
+    per_step = max(1, args.ref_seqs_per_step or threads)
     samples = []
     S = len(sc.decode_seqs)
     for i in range(args.warmup + args.steps):
         seqs = [(i * per_step + j) % S for j in range(per_step)]
         rep, tab, lens, q = _oracle_sample(sc, seqs)
-        t = _oracle_time(sc, rep, tab, lens, q)
+        t = (_oracle_time_procs(sc, rep, tab, lens, q, threads, 1) if threads > 1 else
+             _oracle_time(sc, rep, tab, lens, q))
         if i >= args.warmup:
             samples.append((t, algorithmic_bytes(sc, lens, 0)[0], len(seqs)))
     tot_t = sum(s[0] for s in samples)
     tot_b = sum(s[1] for s in samples)
     value = tot_b / tot_t / 1e9
-    desc = ("fp64 oracle decode, %d sequence(s) of %s per step (rotating), all %d query heads"
-            % (per_step, sc.name, sc.n_q_heads))
+    desc = ("fp64 oracle decode, %d sequence(s) of %s per step (rotating), layer 0, all %d query heads, "
+            "%d worker process(es) at once, whole sequences each" % (per_step, sc.name, sc.n_q_heads, threads))
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / len(samples) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": sc.name, "num_seqs_per_step": per_step},
             "seqs_per_s": round(sum(s[2] for s in samples) / tot_t, 3),
-            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": desc},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -1064,10 +1209,13 @@ def main(argv=None):
     p.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                    help="cache element type of the decode workloads (fp8: E4M3 with per-cache scales)")
     p.add_argument("--partition", type=int, default=0, help="positions per partition (0 = library default)")
+    p.add_argument("--layers", type=int, default=0,
+                   help="layers of the mixed_batch step (0 = all 32: 32 x (reshape_and_cache + pa_decode))")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
-    p.add_argument("--ref-seqs-per-step", type=int, default=2)
+    p.add_argument("--ref-seqs-per-step", type=int, default=0,
+                   help="sequences the reference arm decodes per step (0 = one per host core)")
     args = p.parse_args(argv)
     world, rank, local = dist_env()
     if args.warmup < 3:

@@ -516,12 +516,19 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
 
 // Every lane waits for the stage itself (visibility of the async copies);
 // the decision to give up is warp-uniform.  On a timeout the status is
-// flagged and the warp's other stages are given a short bounded wait.
-__device__ __forceinline__ bool wait_stage(uint64_t* bars, int k, int lane, int32_t* status) {
+// flagged and the warp waits again, each with the full bound, for every
+// stage it has issued and not consumed (stages k .. issued - 1, this one
+// included), so that no copy lands in shared memory after the block has
+// moved on; `drained` is cleared if one of them still has not landed.
+__device__ __forceinline__ bool wait_stage(uint64_t* bars, int k, int issued, int lane, int32_t* status,
+                                           bool& drained) {
     const bool ok = __all_sync(0xffffffffu, pa::mbar_wait_bounded(&bars[k % kStages], (k / kStages) & 1, kMaxProbes));
     if (!ok) {
         if (lane == 0) pa::set_status(status, PA_DEV_WAIT_TIMEOUT);
-        for (int kk = k + 1; kk < k + kStages; ++kk) pa::mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, 1000);
+        bool landed = true;
+        for (int kk = k; kk < issued; ++kk)
+            landed = pa::mbar_wait_bounded(&bars[kk % kStages], (kk / kStages) & 1, kMaxProbes) && landed;
+        drained = __all_sync(0xffffffffu, landed);
     }
     return ok;
 }
@@ -622,9 +629,12 @@ __global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DE
             if (tile < n_tiles) issue(tile, k);
         }
     }
+    // this warp's tiles; stages issued before consuming local tile k: min(n_mine, k + kStages)
+    const int n_mine = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
+    bool drained = true;
     int k = 0;
     for (int tile = warp; tile < n_tiles; tile += kWarps, ++k) {
-        if (!wait_stage(wbars, k, lane, a.status)) break;
+        if (!wait_stage(wbars, k, min(n_mine, k + kStages), lane, a.status, drained)) break;
         const uint32_t ks = pa::smem_addr(wring + (k % kStages) * G::kStageBytes);
         const int nv_ = min(kTile, t_end - (t_begin + tile * kTile));
         if constexpr (F8)
@@ -637,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DE
     st.finish_sums();
 
     // ---- merge the 4 warps (exact, as in the block merge) ----------------------
-    __syncthreads();                                   // ring no longer in use
+    // Ring no longer in use, unless a timed-out copy may still land in it: then
+    // the block leaves it alone and returns (outputs unspecified, status set).
+    if (!__syncthreads_and(drained ? 1 : 0)) return;
     float* mw = reinterpret_cast<float*>(ring);        // [warp][8]
     float* lw = mw + kWarps * kHeads;                  // [warp][8]
     float* uw = lw + kWarps * kHeads;                  // [warp][8][D]
@@ -1031,9 +1043,14 @@ int pa_lse_merge(void* out, int out_dtype, const float* part_max, const float* p
 // The split path's partition statistics live in this file-scope device
 // array instead of a caller workspace.  Host code must not use the name
 // `g_static_scratch` as an address (on the host it is only a stand-in
-// symbol); the device address is looked up once per device with
-// cudaGetSymbolAddress and cached.
+// symbol); the device address is looked up with cudaGetSymbolAddress, with
+// the device current, once per CUDA context and cached.  The cache is keyed
+// by the context's unique id, so a context created anew on the same device
+// (after cudaDeviceReset, for instance), whose copy of the array may sit
+// elsewhere, gets a fresh lookup instead of a stale address.
 // ---------------------------------------------------------------------------
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 static __device__ __align__(256) uint8_t g_static_scratch[PA_STATIC_SCRATCH_BYTES];
@@ -1043,17 +1060,45 @@ namespace {
 constexpr int kMaxScratchDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxScratchDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxScratchDevices] = {0};
 
-// Device address of g_static_scratch on the current device (looked up on the
-// first call for that device).  Returns nullptr on failure.
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_fn_once;
+
+// Unique id of the calling thread's current context (0 if unknown).
+unsigned long long current_context_id() {
+    std::call_once(g_ctx_fn_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!g_ctx_current || !g_ctx_id || g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        g_ctx_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_static_scratch in the current device's context (looked
+// up on the first call in that context).  Returns nullptr on failure.
 void* static_scratch_address() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
+    const unsigned long long ctx = current_context_id();   // 0 before the runtime has made one current
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || ctx == 0 || g_scratch_ctx[dev] != ctx) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return nullptr;
         g_scratch_addr[dev] = ptr;
+        g_scratch_ctx[dev] = ctx ? ctx : current_context_id();
     }
     return g_scratch_addr[dev];
 }

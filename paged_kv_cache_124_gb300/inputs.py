@@ -33,9 +33,9 @@ def bf16_bits(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def nan_pool(shape):
-    """A CPU bf16 tensor whose every element is the NaN sentinel pattern."""
-    return torch.full(shape, NAN_BF16_BITS, dtype=torch.int16).view(torch.bfloat16)
+def nan_pool(shape, device="cpu"):
+    """A bf16 tensor whose every element is the NaN sentinel pattern."""
+    return torch.full(shape, NAN_BF16_BITS, dtype=torch.int16, device=device).view(torch.bfloat16)
 
 
 def permutation(n, seed):

@@ -32,8 +32,8 @@ class ScenarioRunner:
         self.n_layers = sc.n_layers if n_layers is None else n_layers
         self.alloc = api.BlockAllocator(sc.num_blocks, sc.block_size)
         shape = (sc.num_blocks, sc.n_kv_heads, sc.block_size, sc.d_head)
-        self.k_caches = [I.nan_pool(shape).to(self.device) for _ in range(self.n_layers)]
-        self.v_caches = [I.nan_pool(shape).to(self.device) for _ in range(self.n_layers)]
+        self.k_caches = [I.nan_pool(shape, self.device) for _ in range(self.n_layers)]
+        self.v_caches = [I.nan_pool(shape, self.device) for _ in range(self.n_layers)]
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.decoded = set(sc.decode_seqs)
         self.cow_pairs_total = 0
