@@ -54,6 +54,10 @@ CACHE_OPS_PROFILE = os.path.join(ROOT, "profiles", "copy_blocks_kernel_cache_ops
 CACHE_OPS_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_cache_ops.cu")
 PREFILL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_prefill.cu")
 
+# NVTX range around each arm's K timed steps (an ncu launch list can be
+# limited to it with --nvtx --nvtx-include "timed_steps/")
+TIMED_RANGE = "timed_steps"
+
 PREFILL_METRIC = "paged prefill-attn TFLOP/s (causal, 8B GQA shape; frac of bf16 tensor peak)"
 PREFILL_WORKLOADS = {
     "prefill_prompts_8b": lambda seed, B: I.prefill_prompts(seed, B),
@@ -323,6 +327,7 @@ def run_ours(args, world, rank, local):
               for _ in range((K + SAMPLE - 1) // SAMPLE)]
     barrier(world)
     torch.cuda.synchronize(dev)
+    torch.cuda.nvtx.range_push(TIMED_RANGE)
     ev_start.record(stream)
     for i in range(K):
         for l in range(L):
@@ -335,6 +340,7 @@ def run_ours(args, world, rank, local):
             else:
                 decode_call(l, q[l], tables, ctx, stream)
     ev_end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     barrier(world)
     step_s = ev_start.elapsed_time(ev_end) / 1e3
@@ -535,6 +541,7 @@ def run_prefill_ours(args, world, rank, local):
               for _ in range((K + SAMPLE - 1) // SAMPLE)]
     barrier(world)
     torch.cuda.synchronize(dev)
+    torch.cuda.nvtx.range_push(TIMED_RANGE)
     ev_start.record(stream)
     for i in range(K):
         api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
@@ -546,6 +553,7 @@ def run_prefill_ours(args, world, rank, local):
         else:
             attention(q, tables, qs, ctx, stream)
     ev_end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop() if clocks else None

@@ -140,7 +140,8 @@ struct Bars {
     uint64_t k_empty[2][kKStages];  // per Q tile and stage: its score products reading K are done
     uint64_t v_empty[2][kVStages];  // per Q tile and stage: its value products reading V are done
     uint64_t s_full[2];   // per Q tile: its scores are in tensor memory
-    uint64_t p_full[2];   // per Q tile: its weights are in tensor memory (and O rescaled)
+    uint64_t p_full[2];   // per Q tile: its weights' hi terms are in tensor memory (and O rescaled)
+    uint64_t plo_full[2]; // per Q tile: its weights' lo terms are in tensor memory
     uint64_t o_done[2];   // per Q tile: its last product of an item has finished
     uint64_t o_free[2];   // per Q tile: the softmax warps have read O out
     uint64_t q_empty[2];  // per Q tile: its last score product of an item has finished
@@ -442,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pa::mbar_init(&bars->q_empty[i], 1);
             pa::mbar_init(&bars->s_full[i], 1);
             pa::mbar_init(&bars->p_full[i], kSoftmaxThreads);
+            pa::mbar_init(&bars->plo_full[i], kSoftmaxThreads);
             pa::mbar_init(&bars->o_done[i], 1);
             pa::mbar_init(&bars->o_free[i], kSoftmaxThreads);
             pa::mbar_init(&bars->red[i], kSoftmaxThreads);
@@ -695,10 +697,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok) ok = wait1(&bars->p_full[x], (ns - 1) & 1, bars, a.status);
                     if (!ok) break;
                     tc_fence_after();
-                    // O += P_hi V, then O += P_lo V (the weights' two bf16 terms)
+                    // O += P_hi V as soon as the hi terms are written, then
+                    // O += P_lo V (the softmax writes lo meanwhile)
                     for (int kk = 0; kk < ksteps; ++kk)
                         mma_bf16_ta(t_o, t_s + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
                                     (j > 0 || kk > 0) ? 1u : 0u);
+                    ok = wait1(&bars->plo_full[x], (ns - 1) & 1, bars, a.status);
+                    if (!ok) break;
+                    tc_fence_after();
                     for (int kk = 0; kk < ksteps; ++kk)
                         mma_bf16_ta(t_o, t_s + kKv / 2 + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024),
                                     id_pv, 1u);
@@ -810,43 +816,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                     l[x] *= alpha;
                     m_used[x] = m_new;
                     const float neg = -m_used[x];
-                    // column pairs in packed f32x2 arithmetic: one FMA and one
+                    // Column pairs in packed f32x2 arithmetic: one FMA and one
                     // add per two weights.  Each weight p goes to the tensor
                     // cores as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi)
                     // (p - hi is exact in fp32), so that hi + lo carries p to a
-                    // relative 2^-16 instead of bf16's 2^-8; P_hi is written over
-                    // the first 64 columns of S and P_lo over the other 64.
+                    // relative 2^-16 instead of bf16's 2^-8.  P_hi is written over
+                    // the first 64 columns of S and posted first, so the value
+                    // products on it start while lo is computed and written over
+                    // the other 64 columns.
                     const uint64_t c2x2 = f32x2(c2, c2), negx2 = f32x2(neg, neg);
                     uint64_t lp[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};   // independent partial sums
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t w[kHalfCols / 4], wl[kHalfCols / 4];
+                        uint32_t w[kHalfCols / 4];
 #pragma unroll
                         for (int qq = 0; qq < kHalfCols / 4; ++qq) {
                             const int q = h2 * (kHalfCols / 4) + qq;
                             float x0, x1;
                             f32x2_split(fma_f32x2(f32x2(s[2 * q], s[2 * q + 1]), c2x2, negx2), x0, x1);
-                            const uint64_t pp = f32x2(fast_exp2(x0), fast_exp2(x1));
-                            lp[q & 1] = add_f32x2(lp[q & 1], pp);
-                            float p0, p1;
-                            f32x2_split(pp, p0, p1);
-                            const uint32_t hi = pack_bf16_rn(p0, p1);
-                            float r0, r1;
-                            f32x2_split(sub_f32x2(pp, f32x2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))),
-                                        r0, r1);
-                            w[qq] = hi;
-                            wl[qq] = pack_bf16_rn(r0, r1);
+                            s[2 * q] = fast_exp2(x0);
+                            s[2 * q + 1] = fast_exp2(x1);
+                            lp[q & 1] = add_f32x2(lp[q & 1], f32x2(s[2 * q], s[2 * q + 1]));
+                            w[qq] = pack_bf16_rn(s[2 * q], s[2 * q + 1]);
                         }
                         tmem_st16u(t_s + hc * (kHalfCols / 2) + h2 * (kHalfCols / 4), w);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    pa::mbar_arrive(&bars->p_full[x]);
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t wl[kHalfCols / 4];
+#pragma unroll
+                        for (int qq = 0; qq < kHalfCols / 4; ++qq) {
+                            const int q = h2 * (kHalfCols / 4) + qq;
+                            const uint32_t hi = pack_bf16_rn(s[2 * q], s[2 * q + 1]);
+                            float r0, r1;
+                            f32x2_split(sub_f32x2(f32x2(s[2 * q], s[2 * q + 1]),
+                                                  f32x2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))),
+                                        r0, r1);
+                            wl[qq] = pack_bf16_rn(r0, r1);
+                        }
                         tmem_st16u(t_s + kKv / 2 + hc * (kHalfCols / 2) + h2 * (kHalfCols / 4), wl);
                     }
                     float l0, l1, l2, l3;
                     f32x2_split(lp[0], l0, l1);
                     f32x2_split(lp[1], l2, l3);
                     l[x] += (l0 + l1) + (l2 + l3);
-                    tmem_wait_st();
                     tc_fence_before();
-                    pa::mbar_arrive(&bars->p_full[x]);
+                    pa::mbar_arrive(&bars->plo_full[x]);
                 }
             }
             for (int x = 0; x < 2 && ok; ++x) {
