@@ -118,8 +118,8 @@ const char* pa_status_string(int status);
  *                 device values are clamped to it and flagged with
  *                 PA_DEV_BAD_CONTEXT.
  *   partition_size   positions per partition: 0 lets the library choose
- *                 from the batch shape and the device (256 to 1024), else a
- *                 multiple of 64 in [64, 8192].
+ *                 from the batch shape, the device and the cache type (256
+ *                 to 1024), else a multiple of 64 in [64, 8192].
  *   workspace     device scratch of at least pa_decode_workspace_size(...)
  *                 bytes (same arguments, same current device), 256-byte
  *                 aligned; may be NULL (bytes 0) when that size is 0 (every
@@ -141,7 +141,9 @@ const char* pa_status_string(int status);
  * power-of-two scaling, the softmax weights to f16 after a 2^15 scaling, a
  * relative error of at most 2^-12).  Same arguments and
  * workspace as pa_decode, plus the two scales (finite, > 0).  d_head must be
- * 128 (PA_ERR_UNSUPPORTED otherwise). */
+ * 128 (PA_ERR_UNSUPPORTED otherwise).  With G = 4 and an even n_kv_heads a
+ * thread block covers two adjacent KV heads (their 8 query heads fill the
+ * products' columns), so the grid has n_kv_heads / 2 head groups. */
 int pa_decode_fp8(void* out, int out_dtype, const void* q,
                   const void* k_cache, const void* v_cache,
                   const int32_t* block_tables, const int32_t* context_lens,
@@ -151,9 +153,10 @@ int pa_decode_fp8(void* out, int out_dtype, const void* q,
                   int partition_size, void* workspace, size_t workspace_bytes,
                   int32_t* status_dev, void* stream);
 
-/* Workspace bytes pa_decode needs for these sizes on the current device
- * (the default partition size depends on the device's SM count); 0 when no
- * sequence can span more than one partition. */
+/* Workspace bytes pa_decode or pa_decode_fp8 needs for these sizes on the
+ * current device (the default partition size depends on the device's SM
+ * count and, with partition_size 0, on the call: the size returned serves
+ * both); 0 when no sequence can span more than one partition. */
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int d_head,
                                 int max_context_len, int partition_size);
 

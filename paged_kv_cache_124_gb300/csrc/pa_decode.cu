@@ -98,11 +98,14 @@ struct DecodeArgs {
 
 // Shared-memory geometry; F8: one-byte (E4M3) cache elements, rows of d_head
 // bytes (d_head 128: one 128-byte box per row).
-template <int D, bool F8 = false>
+// NK: KV heads per tile (2: two adjacent KV heads of the same positions, whose
+// 2 x 4 query heads fill the 8 columns of the products; FP8 with G = 4).
+template <int D, bool F8 = false, int NK = 1>
 struct Geo {
     static constexpr int kHalves = F8 ? 1 : D / 64;       // 128-byte boxes per row
     static constexpr int kBoxBytes = kTile * 128;         // one swizzled 16 x 128-byte region
-    static constexpr int kTileBytes = kHalves * kBoxBytes;   // K or V of one tile
+    static constexpr int kHeadBytes = kHalves * kBoxBytes;   // K or V of one KV head's tile
+    static constexpr int kTileBytes = NK * kHeadBytes;    // K or V of one tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
     static constexpr int kSteps = D / 16;                 // k-steps of S, m-tiles of O^T
@@ -176,27 +179,30 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 // blocks, the next 8 rows from block blk1).  Returns nothing; the stage's
 // barrier expects exactly the bytes issued.  Boxes are always full: rows
 // past the context come along and are masked in the math.
-template <int D, bool F8>
+template <int D, bool F8, int NK = 1>
 __device__ __forceinline__ void issue_tile(uint8_t* stage, uint64_t* bar, const CUtensorMap* mk,
                                            const CUtensorMap* mv, int blk0, int blk1, int off0, int nv, int kvh,
                                            const DecodeArgs& a, uint64_t policy) {
-    using G = Geo<D, F8>;
+    using G = Geo<D, F8, NK>;
     const int B = a.block_size;
     const int box_rows = B < kTile ? B : kTile;
     const int n_rows = (nv + box_rows - 1) / box_rows;          // 1, or 2 for 8-position blocks
-    pa::mbar_arrive_expect_tx(bar, (uint32_t)(2 * G::kHalves * n_rows * box_rows * 128));
+    pa::mbar_arrive_expect_tx(bar, (uint32_t)(2 * NK * G::kHalves * n_rows * box_rows * 128));
     for (int r = 0; r < n_rows; ++r) {
         int blk = r == 0 ? blk0 : blk1;
         if (blk < 0 || blk >= a.num_blocks) {
             pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
             blk = 0;
         }
-        const int row = (blk * a.n_kv_heads + kvh) * B + (r == 0 ? off0 : 0);
 #pragma unroll
-        for (int h = 0; h < G::kHalves; ++h) {
-            uint8_t* dst = stage + h * G::kBoxBytes + r * box_rows * 128;
-            tma_load_2d(dst, mk, h * 64, row, bar, policy);
-            tma_load_2d(dst + G::kTileBytes, mv, h * 64, row, bar, policy);
+        for (int hh = 0; hh < NK; ++hh) {
+            const int row = (blk * a.n_kv_heads + kvh + hh) * B + (r == 0 ? off0 : 0);
+#pragma unroll
+            for (int h = 0; h < G::kHalves; ++h) {
+                uint8_t* dst = stage + hh * G::kHeadBytes + h * G::kBoxBytes + r * box_rows * 128;
+                tma_load_2d(dst, mk, h * 64, row, bar, policy);
+                tma_load_2d(dst + G::kTileBytes, mv, h * 64, row, bar, policy);
+            }
         }
     }
 }
@@ -419,11 +425,16 @@ __device__ __forceinline__ float load_q_f8(uint32_t (&qb)[Geo<D>::kSteps][2], co
 
 // consume_tile for an FP8 stage; c0 / c1: score scale of heads h0 / h1 (the
 // log2-domain softmax scale times the K scale over the heads' q scales).
-template <int D>
+// NK = 2: the stage holds two KV heads (K0, K1, then V0, V1, kHeadBytes
+// apart); query heads 0-3 of the 8 product columns read KV head 0 and 4-7 KV
+// head 1, so qb[hh] is q with the other head's columns zeroed, and P^T is
+// masked the same way for each head's value product.
+template <int D, int NK = 1>
 __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, uint32_t vs, int nv,
-                                                const uint32_t (&qb)[Geo<D>::kSteps][2], float c0, float c1,
+                                                const uint32_t (&qb)[NK][Geo<D>::kSteps][2], float c0, float c1,
                                                 int lane) {
     constexpr int kSteps = Geo<D>::kSteps;
+    constexpr uint32_t kHeadBytes = Geo<D, true, NK>::kHeadBytes;
     const int g = lane >> 2, t4 = lane & 3, mi = lane >> 3;
     // ldmatrix lane addressing for both tiles: matrix mi covers positions
     // (mi & 1) * 8 .. +7 of 16-byte chunk c + (mi >> 1)
@@ -432,15 +443,18 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
     float s_a[4] = {0.f, 0.f, 0.f, 0.f}, s_b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j = 0; j < kSteps / 2; ++j) {
-        uint32_t r[4];
-        ldsm_x4(ks + swz(row, 2 * j + cadd), r);            // r0, r1: rows g, g+8 of chunk 2j; r2, r3: chunk 2j+1
-        uint32_t af[4];
-        e4m3x4_to_f16(r[0], af[0], af[2]);
-        e4m3x4_to_f16(r[1], af[1], af[3]);
-        mma16816_f16(s_a, af, qb[2 * j][0], qb[2 * j][1]);
-        e4m3x4_to_f16(r[2], af[0], af[2]);
-        e4m3x4_to_f16(r[3], af[1], af[3]);
-        mma16816_f16(s_b, af, qb[2 * j + 1][0], qb[2 * j + 1][1]);
+#pragma unroll
+        for (int hh = 0; hh < NK; ++hh) {
+            uint32_t r[4];
+            ldsm_x4(ks + hh * kHeadBytes + swz(row, 2 * j + cadd), r);   // r0, r1: rows g, g+8 of chunk 2j; r2, r3: chunk 2j+1
+            uint32_t af[4];
+            e4m3x4_to_f16(r[0], af[0], af[2]);
+            e4m3x4_to_f16(r[1], af[1], af[3]);
+            mma16816_f16(s_a, af, qb[hh][2 * j][0], qb[hh][2 * j][1]);
+            e4m3x4_to_f16(r[2], af[0], af[2]);
+            e4m3x4_to_f16(r[3], af[1], af[3]);
+            mma16816_f16(s_b, af, qb[hh][2 * j + 1][0], qb[hh][2 * j + 1][1]);
+        }
     }
     float s[4];
     s[0] = (s_a[0] + s_b[0]) * c0;
@@ -480,28 +494,39 @@ __device__ __forceinline__ void consume_tile_f8(WarpState<D>& st, uint32_t ks, u
     constexpr float kP = 32768.f;                                   // 2^15
     const uint32_t bh0 = movmatrix_trans(pack_f16(p0 * kP, p1 * kP));
     const uint32_t bh1 = movmatrix_trans(pack_f16(p2 * kP, p3 * kP));
+    // B fragment lane (g, t4) holds column g: query head g reads KV head g / 4
+    uint32_t bp[NK][2];
+#pragma unroll
+    for (int hh = 0; hh < NK; ++hh) {
+        const bool mine = NK == 1 || (g >> 2) == hh;
+        bp[hh][0] = mine ? bh0 : 0u;
+        bp[hh][1] = mine ? bh1 : 0u;
+    }
 
     // P.V over the tile; in the context's last tile the V rows past its end
     // are zeroed (their codes may be NaN, and 0 * NaN is not 0)
     auto pv = [&](uint32_t mlo, uint32_t mhi, bool masked) {
 #pragma unroll
         for (int j = 0; j < kSteps / 2; ++j) {
-            uint32_t r[4];
-            // r0 / r1: positions 2t4, 2t4+1 / 2t4+8, 2t4+9 of chunk 2j (codes 2g, 2g+1
-            // of each); r2 / r3: the same for chunk 2j+1
-            ldsm_x4_trans(vs + swz(row, 2 * j + cadd), r);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t af[4];
-                e4m3x4_to_f16(prmt(r[2 * h], r[2 * h], 0x3120u), af[0], af[1]);       // [p0 d0, p1 d0 | p0 d1, p1 d1]
-                e4m3x4_to_f16(prmt(r[2 * h + 1], r[2 * h + 1], 0x3120u), af[2], af[3]);
-                if (masked) {
-                    af[0] &= mlo;
-                    af[1] &= mlo;
-                    af[2] &= mhi;
-                    af[3] &= mhi;
+            for (int hh = 0; hh < NK; ++hh) {
+                uint32_t r[4];
+                // r0 / r1: positions 2t4, 2t4+1 / 2t4+8, 2t4+9 of chunk 2j (codes 2g, 2g+1
+                // of each); r2 / r3: the same for chunk 2j+1
+                ldsm_x4_trans(vs + hh * kHeadBytes + swz(row, 2 * j + cadd), r);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t af[4];
+                    e4m3x4_to_f16(prmt(r[2 * h], r[2 * h], 0x3120u), af[0], af[1]);   // [p0 d0, p1 d0 | p0 d1, p1 d1]
+                    e4m3x4_to_f16(prmt(r[2 * h + 1], r[2 * h + 1], 0x3120u), af[2], af[3]);
+                    if (masked) {
+                        af[0] &= mlo;
+                        af[1] &= mlo;
+                        af[2] &= mhi;
+                        af[3] &= mhi;
+                    }
+                    mma16816_f16(st.acc[2 * j + h], af, bp[hh][0], bp[hh][1]);
                 }
-                mma16816_f16(st.acc[2 * j + h], af, bh0, bh1);
             }
         }
     };
@@ -542,11 +567,15 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bars, int k, int issued, in
 #define PA_DECODE_MIN_BLOCKS_F8 4
 #endif
 
-template <int D, bool F8>
-__global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DECODE_MIN_BLOCKS)
+// NK = 2 (FP8, G = 4): a block covers two adjacent KV heads (8 query heads);
+// its stages are twice as large, so one block fewer fits an SM.
+template <int D, bool F8, int NK = 1>
+__global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS_F8 - 1 : PA_DECODE_MIN_BLOCKS_F8)
+                                               : PA_DECODE_MIN_BLOCKS)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                             const DecodeArgs a) {
-    using G = Geo<D, F8>;
+    static_assert(NK == 1 || F8, "two KV heads per block are built for FP8 caches only");
+    using G = Geo<D, F8, NK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + G::kRingBytes);
@@ -554,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DE
 
     const int part = blockIdx.x;
     const int seq = blockIdx.z;
-    const int kvh = blockIdx.y / a.n_sub;
+    const int kvh = NK == 1 ? blockIdx.y / a.n_sub : blockIdx.y * NK;
     const int hpb = a.heads_per_block;
     const int qh0 = kvh * a.group + (blockIdx.y % a.n_sub) * hpb;
     const int warp = threadIdx.x >> 5;
@@ -575,6 +604,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DE
     for (int i = threadIdx.x; i < n_spec; i += kThreads) table[i] = trow[lb0 + i];
     const size_t row0 = ((size_t)seq * a.n_q_heads + qh0) * D;   // q / out offset of the block's first head
     uint32_t qb[G::kSteps][2];
+    uint32_t qbk[NK][G::kSteps][2];      // FP8: q per KV head of the tile (the other head's columns zero)
     float c0 = 0.f, c1 = 0.f;
     if constexpr (F8) {
         const float sh = load_q_f8<D>(qb, a.q + row0, hpb, lane);
@@ -582,6 +612,15 @@ __global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DE
         const float sc = a.scale_log2 * a.k_scale;
         c0 = sc / __shfl_sync(0xffffffffu, sh, 4 * h0_);
         c1 = sc / __shfl_sync(0xffffffffu, sh, 4 * h0_ + 4);
+#pragma unroll
+        for (int hh = 0; hh < NK; ++hh) {
+            const bool mine = NK == 1 || ((lane >> 2) >> 2) == hh;     // B column g = query head g
+#pragma unroll
+            for (int k = 0; k < G::kSteps; ++k) {
+                qbk[hh][k][0] = mine ? qb[k][0] : 0u;
+                qbk[hh][k][1] = mine ? qb[k][1] : 0u;
+            }
+        }
     } else {
         load_q<D>(qb, a.q + row0, hpb, lane);
     }
@@ -616,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DE
         const int nv = min(kTile, t_end - t0);
         const int e0 = (t0 >> a.log2_block) - lb0;
         const int blk1 = (B < kTile && nv > B) ? table[e0 + 1] : 0;
-        issue_tile<D, F8>(wring + stage * G::kStageBytes, &wbars[stage], &tmap_k, &tmap_v, table[e0], blk1,
+        issue_tile<D, F8, NK>(wring + stage * G::kStageBytes, &wbars[stage], &tmap_k, &tmap_v, table[e0], blk1,
                           t0 & (B - 1), nv, kvh, a, policy);
     };
 
@@ -638,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, F8 ? PA_DECODE_MIN_BLOCKS_F8 : PA_DE
         const uint32_t ks = pa::smem_addr(wring + (k % kStages) * G::kStageBytes);
         const int nv_ = min(kTile, t_end - (t_begin + tile * kTile));
         if constexpr (F8)
-            consume_tile_f8<D>(st, ks, ks + G::kTileBytes, nv_, qb, c0, c1, lane);
+            consume_tile_f8<D, NK>(st, ks, ks + G::kTileBytes, nv_, qbk, c0, c1, lane);
         else
             consume_tile<D>(st, ks, ks + G::kTileBytes, nv_, qb, a.scale_log2, lane);
         __syncwarp();
@@ -857,12 +896,16 @@ int ilog2(int x) {
 }
 
 
-// Positions per partition when the caller passes 0: enough thread blocks for
-// about two waves of 3 blocks per SM (counting 4 query heads per block), at
-// least 256 and at most 1024 positions.
-int default_partition(int num_seqs, int n_q_heads, int max_context_len) {
+// Positions per partition when the caller passes 0, at least 256 and at most
+// 1024: enough thread blocks for about two waves of 3 blocks per SM
+// (counting 4 query heads per block); for the FP8 kernel that covers two KV
+// heads per block (8 query heads, 3 blocks per SM), about three waves, which
+// measured best on the 64-sequence batch and on 32K contexts (768 positions
+// there) while batches of many short sequences keep 1024.
+int default_partition(int num_seqs, int n_q_heads, int max_context_len, bool f8_pair = false) {
     const long long work = (long long)num_seqs * n_q_heads * max_context_len;
-    const long long target = 4LL * 2 * PA_DECODE_MIN_BLOCKS * sm_count();
+    const long long target = f8_pair ? 8LL * 3 * (PA_DECODE_MIN_BLOCKS_F8 - 1) * sm_count()
+                                     : 4LL * 2 * PA_DECODE_MIN_BLOCKS * sm_count();
     long long p = target > 0 ? (work + target - 1) / target : 1024;
     p = (p + 63) / 64 * 64;
     return (int)(p < 256 ? 256 : (p > 1024 ? 1024 : p));
@@ -886,8 +929,8 @@ int launch(K kernel, dim3 grid, int smem, cudaStream_t st, const CUtensorMap& mk
 }
 
 int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, void* workspace,
-        size_t workspace_bytes, cudaStream_t st, bool f8 = false) {
-    static int attr128[64] = {0}, attr64[64] = {0}, attr128f8[64] = {0};
+        size_t workspace_bytes, cudaStream_t st, bool f8 = false, bool pair = false) {
+    static int attr128[64] = {0}, attr64[64] = {0}, attr128f8[64] = {0}, attr128f8p[64] = {0};
     const int P = a.partition_size;
     a.max_parts = (a.ctx_cap + P - 1) / P;
     if (a.max_parts < 1) a.max_parts = 1;
@@ -901,11 +944,13 @@ int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, 
         a.part_acc = reinterpret_cast<float*>(w + 2 * align256(4 * n));
     }
     const int table_ints = P / a.block_size + 2;
-    const int ring = f8 ? Geo<128, true>::kRingBytes : kWarps * kStages * 2 * kTile * d_head * 2;
+    const int ring = f8 ? (pair ? Geo<128, true, 2>::kRingBytes : Geo<128, true>::kRingBytes)
+                        : kWarps * kStages * 2 * kTile * d_head * 2;
     const int merge = kWarps * kHeads * (2 + d_head) * 4;          // the warp merge reuses the ring
     const int smem = 1024 + (ring > merge ? ring : merge) + kWarps * kStages * 8 + table_ints * 4;
-    dim3 grid(a.max_parts, a.n_kv_heads * a.n_sub, a.num_seqs);
-    const int rc = f8 ? launch(decode_partition_kernel<128, true>, grid, smem, st, mk, mv, a, attr128f8)
+    dim3 grid(a.max_parts, pair ? a.n_kv_heads / 2 : a.n_kv_heads * a.n_sub, a.num_seqs);
+    const int rc = f8 ? (pair ? launch(decode_partition_kernel<128, true, 2>, grid, smem, st, mk, mv, a, attr128f8p)
+                              : launch(decode_partition_kernel<128, true>, grid, smem, st, mk, mv, a, attr128f8))
                       : d_head == 128 ? launch(decode_partition_kernel<128, false>, grid, smem, st, mk, mv, a, attr128)
                                       : launch(decode_partition_kernel<64, false>, grid, smem, st, mk, mv, a, attr64);
     if (rc != PA_OK || a.max_parts <= 1) return rc;
@@ -920,7 +965,14 @@ extern "C" {
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int d_head, int max_context_len,
                                 int partition_size) {
     if (num_seqs <= 0 || n_q_heads <= 0 || d_head <= 0 || max_context_len < 0 || partition_size < 0) return 0;
-    const int P = partition_size > 0 ? partition_size : default_partition(num_seqs, n_q_heads, max_context_len);
+    // the library's own choice may differ between pa_decode and pa_decode_fp8:
+    // size for the smaller partition (more of them), which serves both
+    int P = partition_size;
+    if (P == 0) {
+        const int p1 = default_partition(num_seqs, n_q_heads, max_context_len);
+        const int p2 = default_partition(num_seqs, n_q_heads, max_context_len, true);
+        P = p1 < p2 ? p1 : p2;
+    }
     return workspace_bytes_for(num_seqs, n_q_heads, d_head, (max_context_len + P - 1) / P);
 }
 
@@ -954,8 +1006,11 @@ int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, co
     if (partition_size < 0 || (partition_size > 0 && (partition_size % 64 || partition_size > kMaxPartition)))
         return PA_ERR_INVALID_ARG;
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PA_ERR_WORKSPACE;
-    const int hpb = group < kHeads ? group : kHeads;
-    const int n_sub = group / hpb;
+    // FP8 with G = 4: each block covers two adjacent KV heads (their 8 query
+    // heads fill the products' 8 columns)
+    const bool pair = f8 && group == 4 && n_kv_heads % 2 == 0;
+    const int hpb = pair ? kHeads : (group < kHeads ? group : kHeads);
+    const int n_sub = pair ? 1 : group / hpb;
     if ((long long)n_kv_heads * n_sub > 65535 || num_seqs > 65535) return PA_ERR_UNSUPPORTED;
     const long long cache_rows = (long long)num_blocks * n_kv_heads * block_size;
     if (cache_rows > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
@@ -980,7 +1035,8 @@ int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, co
     const long long cap_tbl = (long long)max_blocks_per_seq * block_size;
     a.ctx_cap = (int)(cap_tbl < max_context_len ? cap_tbl : max_context_len);
     a.num_seqs = num_seqs;
-    a.partition_size = partition_size > 0 ? partition_size : default_partition(num_seqs, n_q_heads, max_context_len);
+    a.partition_size =
+        partition_size > 0 ? partition_size : default_partition(num_seqs, n_q_heads, max_context_len, pair);
     a.k_scale = f8 ? k_scale : 1.f;
     a.u_scale = f8 ? v_scale / 32768.f : 1.f;
 
@@ -992,7 +1048,7 @@ int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, co
                                   make_cache_map(&mv, v_cache, cache_rows, d_head, box_rows);
     if (!maps_ok) return PA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return run(a, mk, mv, d_head, workspace, workspace_bytes, st, f8);
+    return run(a, mk, mv, d_head, workspace, workspace_bytes, st, f8, pair);
 }
 
 }  // namespace
