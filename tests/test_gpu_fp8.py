@@ -65,6 +65,8 @@ def _decode_fp8(qb, kc, vc, tables, ctx, B, Hq, Hkv, k_scale, v_scale, out_dtype
 CASES = [
     ("tiny_g2_b16", 4, 2, 16, [1, 15, 16, 37], 0),
     ("g4_b16_batch", 32, 8, 16, [512, 777, 1024, 1500, 2048, 4096], 0),
+    ("g4_odd_kv_heads", 12, 3, 16, [300, 1100, 17], 0),              # G = 4, one KV head per block
+    ("g4_two_kv_heads_b8", 8, 2, 8, [1, 8, 9, 2000], 0),
     ("g4_b8_split", 32, 8, 8, [3000, 257, 64], 256),
     ("g4_b32_split", 32, 8, 32, [5000, 100], 512),
     ("g8_b16", 32, 4, 16, [900, 33], 0),
@@ -91,6 +93,26 @@ def test_decode_fp8_heads_of_very_different_magnitude():
     got, st = _decode_fp8(qb, kc, vc, tab, ctx, 16, Hq, Hkv, 0.01, 0.02, torch.float32)
     assert st == 0
     assert_attention_close(out_to_f64(got), want, True, "magnitudes")
+
+
+@pytest.mark.parametrize("B,P", [(16, 256), (8, 512), (32, 0)])
+def test_decode_fp8_two_head_blocks_equal_one_head_blocks(B, P):
+    """With G = 4 and an even KV head count a thread block covers two KV
+    heads (8 query heads).  Each head's products only add exact zeros for the
+    other head's columns, so at the same partition size the result must equal,
+    bit for bit, decoding each KV head alone (G = 4 with a single KV head takes
+    one head per block)."""
+    Hq, Hkv, ks, vs = 16, 4, 0.01, 0.02
+    ctxs = [1, 700, 2049, 64]
+    qb, kc, vc, tab, ctx = _fp8_problem(9, Hq, Hkv, B, ctxs, ks, vs)
+    part = P or 768
+    both, st = _decode_fp8(qb, kc, vc, tab, ctx, B, Hq, Hkv, ks, vs, torch.float32, part)
+    assert st == 0
+    for h in range(Hkv):
+        one, st = _decode_fp8(np.ascontiguousarray(qb[:, 4 * h:4 * h + 4]), np.ascontiguousarray(kc[:, h:h + 1]),
+                              np.ascontiguousarray(vc[:, h:h + 1]), tab, ctx, B, 4, 1, ks, vs, torch.float32, part)
+        assert st == 0
+        assert torch.equal(one, both[:, 4 * h:4 * h + 4]), "KV head %d" % h
 
 
 @pytest.mark.parametrize("scale", [4.0 / 448, 0.001])
