@@ -119,7 +119,7 @@ const char* pa_status_string(int status);
  *                 PA_DEV_BAD_CONTEXT.
  *   partition_size   positions per partition: 0 lets the library choose
  *                 from the batch shape, the device and the cache type (256
- *                 to 1024), else a multiple of 64 in [64, 8192].
+ *                 to 1536), else a multiple of 64 in [64, 8192].
  *   workspace     device scratch of at least pa_decode_workspace_size(...)
  *                 bytes (same arguments, same current device), 256-byte
  *                 aligned; may be NULL (bytes 0) when that size is 0 (every

@@ -896,13 +896,21 @@ int ilog2(int x) {
 }
 
 
-// Positions per partition when the caller passes 0, at least 256 and at most
-// 1024: enough thread blocks for about two waves of 3 blocks per SM
-// (counting 4 query heads per block); for the FP8 kernel that covers two KV
-// heads per block (8 query heads, 3 blocks per SM), about three waves, which
-// measured best on the 64-sequence batch and on 32K contexts (768 positions
-// there) while batches of many short sequences keep 1024.
-int default_partition(int num_seqs, int n_q_heads, int max_context_len, bool f8_pair = false) {
+// Positions per partition when the caller passes 0.  `units` is the number of
+// (sequence, head group) thread blocks per partition index (0: unknown).
+// When the units alone fill two waves of resident blocks, sequences are not
+// split for parallelism: 1536 positions, so that most short sequences of a
+// large batch finish in their own block without a merge (measured best on
+// 256 mixed-length sequences, 4-5 % faster than 1024).  Otherwise at least
+// 256 and at most 1024: enough thread blocks for about two waves of 3 blocks
+// per SM (counting 4 query heads per block); for the FP8 kernel that covers
+// two KV heads per block (8 query heads, 3 blocks per SM), about three waves,
+// which measured best on the 64-sequence batch and on 32K contexts (768
+// positions there).
+int default_partition(int num_seqs, int n_q_heads, int max_context_len, bool f8_pair = false,
+                      long long units = 0) {
+    const long long slots = (long long)(f8_pair ? PA_DECODE_MIN_BLOCKS_F8 - 1 : PA_DECODE_MIN_BLOCKS) * sm_count();
+    if (units > 0 && slots > 0 && units >= 2 * slots) return 1536;
     const long long work = (long long)num_seqs * n_q_heads * max_context_len;
     const long long target = f8_pair ? 8LL * 3 * (PA_DECODE_MIN_BLOCKS_F8 - 1) * sm_count()
                                      : 4LL * 2 * PA_DECODE_MIN_BLOCKS * sm_count();
@@ -965,8 +973,9 @@ extern "C" {
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int d_head, int max_context_len,
                                 int partition_size) {
     if (num_seqs <= 0 || n_q_heads <= 0 || d_head <= 0 || max_context_len < 0 || partition_size < 0) return 0;
-    // the library's own choice may differ between pa_decode and pa_decode_fp8:
-    // size for the smaller partition (more of them), which serves both
+    // the library's own choice may differ between pa_decode and pa_decode_fp8
+    // and may be larger when the batch has many head groups: size for the
+    // smaller work-based partition (more of them), which serves every case
     int P = partition_size;
     if (P == 0) {
         const int p1 = default_partition(num_seqs, n_q_heads, max_context_len);
@@ -1035,8 +1044,9 @@ int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, co
     const long long cap_tbl = (long long)max_blocks_per_seq * block_size;
     a.ctx_cap = (int)(cap_tbl < max_context_len ? cap_tbl : max_context_len);
     a.num_seqs = num_seqs;
-    a.partition_size =
-        partition_size > 0 ? partition_size : default_partition(num_seqs, n_q_heads, max_context_len, pair);
+    const long long units = (long long)num_seqs * (pair ? n_kv_heads / 2 : n_kv_heads * n_sub);
+    a.partition_size = partition_size > 0 ? partition_size
+                                          : default_partition(num_seqs, n_q_heads, max_context_len, pair, units);
     a.k_scale = f8 ? k_scale : 1.f;
     a.u_scale = f8 ? v_scale / 32768.f : 1.f;
 
