@@ -863,6 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     f32x2_split(lp[0], l0, l1);
                     f32x2_split(lp[1], l2, l3);
                     l[x] += (l0 + l1) + (l2 + l3);
+                    tmem_wait_st();
                     tc_fence_before();
                     pa::mbar_arrive(&bars->plo_full[x]);
                 }
