@@ -640,6 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it.seq < 0) break;
                 const int ntx = x ? it.nt1 : it.nt0;
                 const int kv_endx = x ? it.kv_end1 : it.kv_end0;
+                // end of the context's last block: rows from ctx up to it may hold junk
+                const int ctx_blocks_end = ((it.ctx + a.block_size - 1) / a.block_size) * a.block_size;
                 if (ntx == 0) {
                     // this Q tile has no rows in the item: release Q and every K/V tile
                     ok = wait1(&bars->q_full, c & 1, bars, a.status);
@@ -678,8 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Only rows past the context are touched (both issuers may clear
                     // the same rows; they write the same zeros).
                     const int zero_begin = max(valid, it.ctx - j * kKv);
-                    const int zero_end =
-                        min(ksteps * 16, ((it.ctx + a.block_size - 1) / a.block_size) * a.block_size - j * kKv);
+                    const int zero_end = min(ksteps * 16, ctx_blocks_end - j * kKv);
                     if (zero_begin < zero_end) {
                         for (int r = zero_begin; r < zero_end; ++r)
 #pragma unroll
