@@ -74,3 +74,30 @@ def test_decode_algorithmic_bytes_of_the_headline_batch():
     dec, write = bench.algorithmic_bytes(sc, ctx, 64)
     assert dec == kv + qo + tab == 590519796
     assert write == 64 * sc.n_kv_heads * 2 * sc.d_head * 2 * 2
+
+
+def test_cpu_baseline_runs_the_oracle_on_every_core_and_on_one():
+    """The all-core leg starts one worker process per host core on a
+    compacted copy of the sample; both legs report positive rates and the
+    all-core leg says how many cores it used."""
+    from paged_kv_cache_124_gb300 import inputs as I
+    sc = I.tiny_gqa(0)
+    line = bench.cpu_baseline(sc, 0.2)
+    assert line["kind"] == "oracle" and line["value"] > 0
+    assert "all_cores_failed" not in line, line.get("all_cores_failed")
+    if bench.host_threads() > 1:
+        assert line["cores"] == bench.host_threads()
+        assert line["single_thread"]["cores"] == 1 and line["single_thread"]["value"] > 0
+
+
+def test_worker_pool_time_is_the_slowest_worker():
+    from paged_kv_cache_124_gb300 import inputs as I
+    sc = I.tiny_gqa(0)
+    rep, tab, lens, q = bench._oracle_sample(sc, list(range(len(sc.decode_seqs))))
+    t = bench._oracle_time_procs(sc, rep, tab, lens, q, 2, 3)
+    assert 0 < t < 60
+
+
+def test_quantiles():
+    assert bench._quantiles([5.0, 1.0, 3.0, 2.0, 4.0]) == (3.0, 1.0, 5.0)
+    assert bench._quantiles([2.0]) == (2.0, 2.0, 2.0)
