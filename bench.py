@@ -260,10 +260,13 @@ def run_ours(args, world, rank, local):
     tables, ctx, max_ctx = run.decode_metadata()
     S = len(sc.decode_seqs)
     ctx_h = ctx.cpu().numpy()
-    # the step's new token per sequence: the last position of each context
-    # (the same slot in every layer: the layers share the block tables)
+    # the step's new token per sequence is the last position of each context;
+    # the slot the block manager planned for it is the one the fused call
+    # derives from the block table (the same in every layer)
     slots_h = np.array([run.alloc.slot_mapping(s, run.alloc.seq_len(s) - 1, 1)[0] for s in sc.decode_seqs])
-    slots = torch.from_numpy(slots_h).to(dev)
+    tab_h = tables.cpu().numpy()
+    B_ = sc.block_size
+    assert slots_h.tolist() == [int(tab_h[i, (c - 1) // B_]) * B_ + (int(c) - 1) % B_ for i, c in enumerate(ctx_h)]
     kv_new = [I.append_kv(sc.seed, l, 10 ** 6, S, sc.n_kv_heads, sc.d_head) for l in range(L)]
     k_new = torch.stack([k for k, _ in kv_new]).to(dev)          # [L, S, Hkv, D]
     v_new = torch.stack([v for _, v in kv_new]).to(dev)
@@ -286,29 +289,21 @@ def run_ours(args, world, rank, local):
         kcs, vcs = k8, v8
     stream = torch.cuda.current_stream(dev)
     dec_bytes, write_bytes = algorithmic_bytes(sc, ctx_h, S, 1 if fp8 else 2)     # per layer
-    # our kernels per layer: reshape_and_cache, the partition kernel and, when
-    # a sequence can span several partitions, the merge kernel
-    launches_per_layer = 2 + (1 if api.pa_decode_workspace_size(S, sc.n_q_heads, sc.d_head, max_ctx, P) else 0)
+    # our kernels per layer: the partition kernel (which also writes the new
+    # token's K/V into the cache) and, when a sequence can span several
+    # partitions, the merge kernel
+    launches_per_layer = 1 + (1 if api.pa_decode_workspace_size(S, sc.n_q_heads, sc.d_head, max_ctx, P) else 0)
 
-    def cache_write(l, k_, v_, slots_, st_):
-        if fp8:
-            api.pa_reshape_and_cache_fp8(kcs[l], vcs[l], k_, v_, slots_, scales[l][0], scales[l][1], stream=st_)
-        else:
-            api.pa_reshape_and_cache(kcs[l], vcs[l], k_, v_, slots_, stream=st_)
-
-    def decode_call(l, q_, tables_, ctx_, st_):
-        if fp8:
-            api.pa_decode_fp8(out[l], q_, kcs[l], vcs[l], tables_, ctx_, sc.block_size, sc.scale, scales[l][0],
-                              scales[l][1], sc.n_q_heads, sc.n_kv_heads, sc.d_head, max_ctx, partition_size=P,
-                              workspace=ws, stream=st_)
-        else:
-            api.pa_decode(out[l], q_, kcs[l], vcs[l], tables_, ctx_, sc.block_size, sc.scale, sc.n_q_heads,
-                          sc.n_kv_heads, sc.d_head, max_ctx, partition_size=P, workspace=ws, stream=st_)
+    def decode_call(l, q_, k_, v_, tables_, ctx_, st_):
+        """One layer of the step: the new token's K/V appended at position
+        ctx - 1 and decode attention over the cache (pa_decode_append)."""
+        api.pa_decode_append(out[l], q_, kcs[l], vcs[l], k_, v_, tables_, ctx_, sc.block_size, sc.scale,
+                             sc.n_q_heads, sc.n_kv_heads, sc.d_head, max_ctx, partition_size=P, workspace=ws,
+                             stream=st_, k_scale=scales[l][0] if fp8 else None, v_scale=scales[l][1] if fp8 else None)
 
     def step():
         for l in range(L):
-            cache_write(l, k_new[l], v_new[l], slots, stream)
-            decode_call(l, q[l], tables, ctx, stream)
+            decode_call(l, q[l], k_new[l], v_new[l], tables, ctx, stream)
 
     clocks = ClockSampler(local) if rank == 0 else None
     if clocks:
@@ -316,11 +311,11 @@ def run_ours(args, world, rank, local):
     for _ in range(args.warmup):
         step()
     K = args.steps
-    # Timed region: K whole steps (every layer's cache write and decode)
-    # between two events.  The decode call of layer 0 of every SAMPLE-th step
-    # is also bracketed by events: the isolated duration of one call (an event
-    # between two kernels stops the second from overlapping the first's drain,
-    # so only a sample of steps carries them).
+    # Timed region: K whole steps (every layer's cache write and decode, one
+    # fused call each) between two events.  The call of layer 0 of every
+    # SAMPLE-th step is also bracketed by events: the isolated duration of one
+    # call (an event between two kernels stops the second from overlapping the
+    # first's drain, so only a sample of steps carries them).
     SAMPLE = 8
     ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -331,14 +326,13 @@ def run_ours(args, world, rank, local):
     ev_start.record(stream)
     for i in range(K):
         for l in range(L):
-            cache_write(l, k_new[l], v_new[l], slots, stream)
             if l == 0 and i % SAMPLE == 0:
                 a, b = ev_dec[i // SAMPLE]
                 a.record(stream)
-                decode_call(l, q[l], tables, ctx, stream)
+                decode_call(l, q[l], k_new[l], v_new[l], tables, ctx, stream)
                 b.record(stream)
             else:
-                decode_call(l, q[l], tables, ctx, stream)
+                decode_call(l, q[l], k_new[l], v_new[l], tables, ctx, stream)
     ev_end.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
@@ -348,11 +342,11 @@ def run_ours(args, world, rank, local):
     total_s, total_bytes = reduce_timing(step_s, (dec_bytes + write_bytes) * L * K, world, dev)
     _, total_seqs = reduce_timing(step_s, S * K, world, dev)
 
-    # ---- decode calls back to back: the kernels' average duration ----------
-    # Repetitions of CALLS pa_decode calls (layers in turn) between two
-    # events, run for at least MIN_LOOP_S in all, so that the clock sampler
-    # sees the load; median, p10 and p90 of the per-call time over the
-    # repetitions.
+    # ---- calls back to back: the kernels' average duration ------------------
+    # Repetitions of CALLS pa_decode_append calls (layers in turn; each
+    # rewrites the same rows) between two events, run for at least MIN_LOOP_S
+    # in all, so that the clock sampler sees the load; median, p10 and p90 of
+    # the per-call time over the repetitions.
     CALLS, MIN_REPS, MIN_LOOP_S = 200, 5, 1.2
     per_call = []
     t_loop = time.perf_counter()
@@ -360,7 +354,7 @@ def run_ours(args, world, rank, local):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for c in range(CALLS):
-            decode_call(c % L, q[c % L], tables, ctx, stream)
+            decode_call(c % L, q[c % L], k_new[c % L], v_new[c % L], tables, ctx, stream)
         e1.record(stream)
         e1.synchronize()
         per_call.append(e0.elapsed_time(e1) / 1e3 / CALLS)
@@ -369,19 +363,19 @@ def run_ours(args, world, rank, local):
     dec_med, dec_p10, dec_p90 = _quantiles(per_call)
     step_per_layer_s = total_s / K / L
     if dec_med > step_per_layer_s * 1.02:
-        raise RuntimeError("decode call (%.2f us back to back) longer than a whole step's layer (%.2f us): the "
+        raise RuntimeError("call (%.2f us back to back) longer than a whole step's layer (%.2f us): the "
                            "timing is inconsistent" % (dec_med * 1e6, step_per_layer_s * 1e6))
 
     # ---- end to end through the public API with host buffers ---------------
     # Every step copies its inputs from pinned host memory (q and the new K/V
-    # rows of every layer, slot mapping, block tables, context lengths), runs
-    # every layer's cache write and decode, copies the outputs back and waits
-    # for them.  The step is issued once into a CUDA graph (the library's
+    # rows of every layer, block tables, context lengths), runs every layer's
+    # fused cache write and decode, copies the outputs back and waits for
+    # them.  The step is issued once into a CUDA graph (the library's
     # calls are capturable) and replayed; the eager form is timed too.  The
     # inputs travel packed in one page-locked buffer (one copy per step; six
     # small copies each paid their own latency), and the calls read views of
     # its device twin.
-    inputs = (q, k_new, v_new, slots, tables, ctx)
+    inputs = (q, k_new, v_new, tables, ctx)
     offs, total = [], 0
     for t in inputs:
         offs.append(total)
@@ -393,7 +387,7 @@ def run_ours(args, world, rank, local):
         nb = t.numel() * t.element_size()
         pack_h[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
         views.append(pack_d[o:o + nb].view(t.dtype).view(t.shape))
-    q_d, k_d, v_d, slots_d, tables_d, ctx_d = views
+    q_d, k_d, v_d, tables_d, ctx_d = views
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in inputs)
     d2h = out_h.numel() * out_h.element_size()
@@ -401,8 +395,7 @@ def run_ours(args, world, rank, local):
     def e2e_body(st):
         pack_d.copy_(pack_h, non_blocking=True)
         for l in range(L):
-            cache_write(l, k_d[l], v_d[l], slots_d, st)
-            decode_call(l, q_d[l], tables_d, ctx_d, st)
+            decode_call(l, q_d[l], k_d[l], v_d[l], tables_d, ctx_d, st)
         out_h.copy_(out, non_blocking=True)
 
     def eager_step():
@@ -437,7 +430,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return None
     peak, peak_kind = measured_peak()
-    achieved = dec_bytes / dec_med / 1e9
+    achieved = (dec_bytes + write_bytes) / dec_med / 1e9
     value = total_bytes / total_s / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -456,19 +449,19 @@ def run_ours(args, world, rank, local):
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "single GPU"},
         "seqs_per_s": round(total_seqs / total_s, 1),
         "ms_per_layer": round(total_s / K / L * 1e3, 5),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode%s (decode_partition_kernel + lse_merge_kernel)" %
-                     ("_fp8" if fp8 else ""),
+        "roofline": {"bound": "hbm", "kernel": "pa_decode_append%s (decode_partition_kernel, which also "
+                     "writes the new rows, + lse_merge_kernel)" % ("_fp8" if fp8 else ""),
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(PROFILE_SUMMARY_FP8 if fp8 else PROFILE_SUMMARY)
                      if args.workload == "batch64_8b" and sc.block_size == 16 and P == 0 else None,
-                     "algorithmic_bytes_per_launch": int(dec_bytes),
+                     "algorithmic_bytes_per_launch": int(dec_bytes + write_bytes),
                      "avg_launch_us": round(dec_med * 1e6, 2),
                      "launch_us_p10_p90": [round(dec_p10 * 1e6, 2), round(dec_p90 * 1e6, 2)],
-                     "timing": "median over %d repetitions of %d pa_decode calls back to back between two events "
+                     "timing": "median over %d repetitions of %d pa_decode_append calls back to back between two events "
                                "(%.2f s of calls)" % (len(per_call), CALLS, loop_s),
                      "isolated_call_us": round(isolated_s * 1e6, 2),
-                     "isolated_call_timing": "events around layer 0's pa_decode on every %d-th timed step (%d "
+                     "isolated_call_timing": "events around layer 0's call on every %d-th timed step (%d "
                                              "samples; the event pair keeps the call from overlapping the "
                                              "kernel before it)" % (SAMPLE, len(ev_dec)),
                      "step_frac": round(value / peak, 4)},

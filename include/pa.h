@@ -169,6 +169,56 @@ int pa_decode(void* out, int out_dtype, const void* q,
               void* workspace, size_t workspace_bytes,
               int32_t* status_dev, void* stream);
 
+/* One decode step's cache write and attention in one call: the token each
+ * sequence appended this step (its keys and values join the cache when it is
+ * fed back for the next decode pass, [P1] section 16; the decode kernel
+ * reading the blocks, section 13) is written into the cache and attended to,
+ * with the result, the
+ * cache contents and the status bits equal, bit for bit, to
+ * pa_reshape_and_cache of those rows followed by pa_decode.
+ *   k_cache, v_cache   as pa_decode, written at one slot per sequence.
+ *   k_new, v_new       device bf16 [num_seqs][n_kv_heads][d_head], 16-byte
+ *                      aligned: the keys and values of position
+ *                      context_lens[s] - 1 of sequence s (the position just
+ *                      appended; context_lens counts it).  Its slot is the
+ *                      one the block table gives for that position:
+ *                      block_tables[s][(ctx - 1) / block_size] at offset
+ *                      (ctx - 1) % block_size.
+ * The thread block that reads that position's tile writes the rows into the
+ * cache and into its own copy of the tile, so the step needs no separate
+ * cache-write kernel before the attention.  Sequences with context length 0
+ * append nothing; a context above its stated maximum is clamped and flagged
+ * (PA_DEV_BAD_CONTEXT) and appends nothing; a bad block id is flagged
+ * (PA_DEV_BAD_BLOCK_ID) and nothing is written.  Other arguments, the
+ * workspace and the return codes are those of pa_decode (PA_ERR_INVALID_ARG
+ * if k_new or v_new is NULL). */
+int pa_decode_append(void* out, int out_dtype, const void* q,
+                     void* k_cache, void* v_cache,
+                     const void* k_new, const void* v_new,
+                     const int32_t* block_tables, const int32_t* context_lens,
+                     int block_size, float scale, int n_q_heads,
+                     int n_kv_heads, int d_head, int num_seqs,
+                     int max_blocks_per_seq, int num_blocks,
+                     int max_context_len, int partition_size,
+                     void* workspace, size_t workspace_bytes,
+                     int32_t* status_dev, void* stream);
+
+/* pa_decode_append for FP8 caches: the appended rows are quantised exactly
+ * as pa_reshape_and_cache_fp8 quantises them (code = E4M3(float(x) / scale),
+ * IEEE division, round to nearest even, saturating), then attended to as by
+ * pa_decode_fp8; bit-equal to those two calls. */
+int pa_decode_append_fp8(void* out, int out_dtype, const void* q,
+                         void* k_cache, void* v_cache,
+                         const void* k_new, const void* v_new,
+                         const int32_t* block_tables,
+                         const int32_t* context_lens, int block_size,
+                         float scale, float k_scale, float v_scale,
+                         int n_q_heads, int n_kv_heads, int d_head,
+                         int num_seqs, int max_blocks_per_seq, int num_blocks,
+                         int max_context_len, int partition_size,
+                         void* workspace, size_t workspace_bytes,
+                         int32_t* status_dev, void* stream);
+
 /* Exact merge of partition statistics ([P2] section 11):
  *   M = max_p m_p,  Z = sum_p exp(m_p - M) z_p,  U = sum_p exp(m_p - M) u_p,
  *   out = U / Z,

@@ -70,6 +70,11 @@ _SIGS = {
                                           _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp]),
     "pa_decode_fp8": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_float, _c_float, _c_int,
                                _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
+    "pa_decode_append": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_int, _c_int,
+                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp]),
+    "pa_decode_append_fp8": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_float, _c_float,
+                                      _c_float, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
+                                      _c_size, _vp, _vp]),
     "pa_reshape_and_cache_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                           _c_float, _vp, _vp]),
     "pa_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
@@ -222,6 +227,49 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, block_size, 
                         int(k_cache.shape[0]), int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
                         _opt_dev(status, torch.int32, "status"), _stream(stream))
     return _check(st, "pa_decode")
+
+
+def pa_decode_append(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens, block_size, scale,
+                     n_q_heads, n_kv_heads, d_head, max_context_len, partition_size=0, workspace=None, status=None,
+                     stream=None, k_scale=None, v_scale=None):
+    """The step's cache write and decode in one call: k_new / v_new [S, Hkv, D]
+    bf16 are the keys and values of position context_lens[s] - 1, written at
+    its slot and attended to (bit-equal to pa_reshape_and_cache + pa_decode);
+    with k_scale / v_scale, the E4M3 form (uint8 caches); see pa.h."""
+    f8 = k_scale is not None
+    if out.dtype == torch.bfloat16:
+        out_dtype = PA_DTYPE_BF16
+    elif out.dtype == torch.float32:
+        out_dtype = PA_DTYPE_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    num_seqs = q.shape[0]
+    if tuple(q.shape) != (num_seqs, n_q_heads, d_head) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("q/out must be [num_seqs, n_q_heads, d_head]")
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (n_kv_heads, block_size, d_head) or \
+            k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, n_kv_heads, block_size, d_head]")
+    if tuple(k_new.shape) != (num_seqs, n_kv_heads, d_head) or k_new.shape != v_new.shape:
+        raise ValueError("k_new/v_new must be [num_seqs, n_kv_heads, d_head]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or context_lens.shape != (num_seqs,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks], context_lens [num_seqs]")
+    ws_ptr, ws_bytes = ctypes.c_void_p(0), 0
+    if workspace is not None:
+        ws_ptr = _dev(workspace, torch.uint8, "workspace")
+        ws_bytes = workspace.numel()
+    cache_dtype = torch.uint8 if f8 else torch.bfloat16
+    args = [_opt_dev(out, out.dtype, "out"), out_dtype, _dev(q, torch.bfloat16, "q"),
+            _dev(k_cache, cache_dtype, "k_cache"), _dev(v_cache, cache_dtype, "v_cache"),
+            _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+            _dev(block_tables, torch.int32, "block_tables"), _dev(context_lens, torch.int32, "context_lens"),
+            int(block_size), float(scale)]
+    if f8:
+        args += [float(k_scale), float(v_scale)]
+    args += [int(n_q_heads), int(n_kv_heads), int(d_head), int(num_seqs), int(block_tables.shape[1]),
+             int(k_cache.shape[0]), int(max_context_len), int(partition_size), ws_ptr, ws_bytes,
+             _opt_dev(status, torch.int32, "status"), _stream(stream)]
+    name = "pa_decode_append_fp8" if f8 else "pa_decode_append"
+    return _check(getattr(_lib, name)(*args), name)
 
 
 _prefill_counters = {}

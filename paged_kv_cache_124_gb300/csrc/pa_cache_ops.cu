@@ -65,25 +65,6 @@ __global__ void __launch_bounds__(32 * kTokensPerBlock, 8) reshape_and_cache_ker
     }
 }
 
-// Two floats to two E4M3 codes (round to nearest even, saturating to +-448,
-// NaN stays NaN): lo in the low byte, hi in the high byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Eight bf16 (one uint4) divided by scale (IEEE division) to eight E4M3 codes.
-__device__ __forceinline__ uint2 quant8(uint4 x, float scale) {
-    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-    uint32_t c[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = pa::bf16x2_to_float2(w[i]);
-        c[i] = e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
-    }
-    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
 
 // FP8 variant of reshape_and_cache: one thread block per token; each thread
 // turns 16 bf16 inputs (two 16-byte loads) into 16 codes (one 16-byte store).
@@ -109,7 +90,7 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
         const uint4* src = (is_v ? v : k) + ((size_t)t * per_token + cc) * 2;
         const uint4 a = src[0], b = src[1];
         const float sc = is_v ? v_scale : k_scale;
-        const uint2 qa = quant8(a, sc), qb = quant8(b, sc);
+        const uint2 qa = pa::quant8(a, sc), qb = pa::quant8(b, sc);
         const int h = cc / chunks_per_row;
         const int x = cc - h * chunks_per_row;
         const size_t dst = (((size_t)blk * n_kv_heads + h) * block_size + off) * chunks_per_row + x;

@@ -75,6 +75,27 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
+// Two floats to two E4M3 codes (round to nearest even, saturating to +-448,
+// NaN stays NaN): lo in the low byte, hi in the high byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight bf16 (one uint4) divided by scale (IEEE division) to eight E4M3 codes:
+// the quantisation of every FP8 cache write.
+__device__ __forceinline__ uint2 quant8(uint4 x, float scale) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = bf16x2_to_float2(w[i]);
+        c[i] = e4m3x2(__fdiv_rn(f.x, scale), __fdiv_rn(f.y, scale));
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }

@@ -94,6 +94,14 @@ struct DecodeArgs {
     int max_parts;
     float k_scale;           // FP8 caches: dequantisation scale of K (folded into the score scale)
     float u_scale;           // factor on the weighted value sums (FP8: V scale / 2^15; else 1)
+    float v_scale;           // FP8 caches: V scale (quantises appended values)
+    // Fused append (pa_decode_append*): the token at position ctx - 1 of
+    // sequence s has keys k_new[s] and values v_new[s] ([S][Hkv][D] bf16);
+    // null: plain decode.
+    const __nv_bfloat16* k_new;
+    const __nv_bfloat16* v_new;
+    uint8_t* k_cache;        // the caches, written at the appended positions
+    uint8_t* v_cache;
 };
 
 // Shared-memory geometry; F8: one-byte (E4M3) cache elements, rows of d_head
@@ -567,6 +575,66 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bars, int k, int issued, in
 #define PA_DECODE_MIN_BLOCKS_F8 4
 #endif
 
+// Fused append.  prefetch_row loads this lane's share of the new token's K
+// and V rows (position ctx - 1), and for FP8 quantises it, early, so that the
+// load's latency and the divisions overlap the pipeline; append_row writes them into the stage the warp has just
+// received (row r of the tile, over the stale slot contents the copy
+// brought) and, when `to_cache`, into the cache at that position's slot
+// (block blk, offset off).  bf16: a row is D / 8 16-byte chunks per K or V,
+// chunk c in box c / 8 at swizzled chunk c % 8.  FP8: a row is D / 16 chunks
+// of 16 codes, quantised exactly as pa_reshape_and_cache_fp8 does; NK heads.
+// The stage holds the block's last tile, so no copy refills it after these
+// generic-proxy writes (the warp merge that reuses the ring writes through
+// the generic proxy too): no proxy fence is needed.
+template <int D, bool F8, int NK>
+struct AppendLane {
+    static constexpr int kCpr = F8 ? D / 16 : D / 8;      // chunks per K (or V) row
+    static constexpr int kLanes = 2 * kCpr * NK;          // lanes with a chunk
+    int hh, c;
+    bool is_v;
+    __device__ __forceinline__ explicit AppendLane(int lane) {
+        hh = lane / (2 * kCpr);
+        const int rem = lane - hh * 2 * kCpr;
+        is_v = rem >= kCpr;
+        c = is_v ? rem - kCpr : rem;
+    }
+};
+
+template <int D, bool F8, int NK>
+__device__ __forceinline__ void prefetch_row(const DecodeArgs& a, int seq, int kvh, int lane, uint4& x0) {
+    using L = AppendLane<D, F8, NK>;
+    if (lane >= L::kLanes) return;
+    const L l(lane);
+    const uint4* src = reinterpret_cast<const uint4*>((l.is_v ? a.v_new : a.k_new) +
+                                                      ((size_t)seq * a.n_kv_heads + kvh + l.hh) * D);
+    if constexpr (F8) {
+        // quantised here, while the warp waits for its first tiles
+        const float sc = l.is_v ? a.v_scale : a.k_scale;
+        const uint2 qa = pa::quant8(__ldg(src + 2 * l.c), sc), qb = pa::quant8(__ldg(src + 2 * l.c + 1), sc);
+        x0 = make_uint4(qa.x, qa.y, qb.x, qb.y);
+    } else {
+        x0 = __ldg(src + l.c);
+    }
+}
+
+template <int D, bool F8, int NK>
+__device__ __forceinline__ void append_row(uint8_t* stage, int r, const DecodeArgs& a, int kvh, int blk, int off,
+                                           bool to_cache, int lane, uint4 x0) {
+    using G = Geo<D, F8, NK>;
+    using L = AppendLane<D, F8, NK>;
+    if (lane < L::kLanes) {
+        const L l(lane);
+        const uint4 val = x0;                     // bf16 chunk, or 16 E4M3 codes
+        uint8_t* row = stage + (l.is_v ? G::kTileBytes : 0) + l.hh * G::kHeadBytes + (F8 ? 0 : (l.c >> 3) * G::kBoxBytes);
+        *reinterpret_cast<uint4*>(row + swz(r, F8 ? l.c : (l.c & 7))) = val;
+        if (to_cache) {
+            const size_t row_elems = (((size_t)blk * a.n_kv_heads + kvh + l.hh) * a.block_size + off) * D;
+            reinterpret_cast<uint4*>((l.is_v ? a.v_cache : a.k_cache) + row_elems * (F8 ? 1 : 2))[l.c] = val;
+        }
+    }
+    __syncwarp();
+}
+
 // NK = 2 (FP8, G = 4): a block covers two adjacent KV heads (8 query heads);
 // its stages are twice as large, so one block fewer fits an SM.
 template <int D, bool F8, int NK = 1>
@@ -629,7 +697,8 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
         pa::fence_mbar_init();
     }
 
-    if (ctx < 0 || ctx > a.ctx_cap) {
+    const bool ctx_ok = ctx >= 0 && ctx <= a.ctx_cap;
+    if (!ctx_ok) {
         if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
         ctx = ctx < 0 ? 0 : a.ctx_cap;
     }
@@ -672,8 +741,21 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
     const int n_mine = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
     bool drained = true;
     int k = 0;
+    // the fused append lands in the tile holding position ctx - 1 (the last
+    // tile of the last partition); a clamped context appends nothing
+    const bool append = a.k_new != nullptr && ctx_ok && t_end == ctx;
+    uint4 app = make_uint4(0, 0, 0, 0);
+    if (append && warp == (n_tiles - 1) % kWarps) prefetch_row<D, F8, NK>(a, seq, kvh, lane, app);
     for (int tile = warp; tile < n_tiles; tile += kWarps, ++k) {
         if (!wait_stage(wbars, k, min(n_mine, k + kStages), lane, a.status, drained)) break;
+        if (append && tile == n_tiles - 1) {
+            const int pos = ctx - 1;
+            int blk = table[(pos >> a.log2_block) - lb0];
+            const bool blk_ok = blk >= 0 && blk < a.num_blocks;     // a bad id was flagged when the tile was issued
+            append_row<D, F8, NK>(wring + (k % kStages) * G::kStageBytes, pos - (t_begin + tile * kTile), a, kvh,
+                                  blk_ok ? blk : 0, pos & (B - 1), blk_ok && (NK == 2 || blockIdx.y % a.n_sub == 0),
+                                  lane, app);
+        }
         const uint32_t ks = pa::smem_addr(wring + (k % kStages) * G::kStageBytes);
         const int nv_ = min(kTile, t_end - (t_begin + tile * kTile));
         if constexpr (F8)
@@ -994,7 +1076,8 @@ int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, co
                 const int32_t* block_tables, const int32_t* context_lens, int block_size, float scale,
                 int n_q_heads, int n_kv_heads, int d_head, int num_seqs, int max_blocks_per_seq, int num_blocks,
                 int max_context_len, int partition_size, void* workspace, size_t workspace_bytes,
-                int32_t* status_dev, void* stream, bool f8, float k_scale, float v_scale) {
+                int32_t* status_dev, void* stream, bool f8, float k_scale, float v_scale,
+                const void* k_new = nullptr, const void* v_new = nullptr) {
     if (num_seqs < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
         num_blocks <= 0 || max_context_len < 0 || !(scale == scale))
         return PA_ERR_INVALID_ARG;
@@ -1004,6 +1087,8 @@ int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, co
     if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+    if (k_new && (!pa_host::aligned16(k_new) || !pa_host::aligned16(v_new))) return PA_ERR_MISALIGNED;
     if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head))
         return PA_ERR_UNSUPPORTED;
     if (n_q_heads % n_kv_heads) return PA_ERR_UNSUPPORTED;
@@ -1049,6 +1134,11 @@ int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, co
                                           : default_partition(num_seqs, n_q_heads, max_context_len, pair, units);
     a.k_scale = f8 ? k_scale : 1.f;
     a.u_scale = f8 ? v_scale / 32768.f : 1.f;
+    a.v_scale = f8 ? v_scale : 1.f;
+    a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    a.k_cache = static_cast<uint8_t*>(const_cast<void*>(k_cache));
+    a.v_cache = static_cast<uint8_t*>(const_cast<void*>(v_cache));
 
     const int box_rows = block_size < kTile ? block_size : kTile;
     CUtensorMap mk, mv;
@@ -1083,6 +1173,29 @@ int pa_decode_fp8(void* out, int out_dtype, const void* q, const void* k_cache, 
     return decode_impl(out, out_dtype, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, n_q_heads,
                        n_kv_heads, d_head, num_seqs, max_blocks_per_seq, num_blocks, max_context_len, partition_size,
                        workspace, workspace_bytes, status_dev, stream, true, k_scale, v_scale);
+}
+
+int pa_decode_append(void* out, int out_dtype, const void* q, void* k_cache, void* v_cache, const void* k_new,
+                     const void* v_new, const int32_t* block_tables, const int32_t* context_lens, int block_size,
+                     float scale, int n_q_heads, int n_kv_heads, int d_head, int num_seqs, int max_blocks_per_seq,
+                     int num_blocks, int max_context_len, int partition_size, void* workspace, size_t workspace_bytes,
+                     int32_t* status_dev, void* stream) {
+    if (!k_new || !v_new) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, n_q_heads,
+                       n_kv_heads, d_head, num_seqs, max_blocks_per_seq, num_blocks, max_context_len, partition_size,
+                       workspace, workspace_bytes, status_dev, stream, false, 1.f, 1.f, k_new, v_new);
+}
+
+int pa_decode_append_fp8(void* out, int out_dtype, const void* q, void* k_cache, void* v_cache, const void* k_new,
+                         const void* v_new, const int32_t* block_tables, const int32_t* context_lens, int block_size,
+                         float scale, float k_scale, float v_scale, int n_q_heads, int n_kv_heads, int d_head,
+                         int num_seqs, int max_blocks_per_seq, int num_blocks, int max_context_len,
+                         int partition_size, void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                         void* stream) {
+    if (!k_new || !v_new) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, out_dtype, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, n_q_heads,
+                       n_kv_heads, d_head, num_seqs, max_blocks_per_seq, num_blocks, max_context_len, partition_size,
+                       workspace, workspace_bytes, status_dev, stream, true, k_scale, v_scale, k_new, v_new);
 }
 
 int pa_lse_merge(void* out, int out_dtype, const float* part_max, const float* part_sum, const float* part_acc,
