@@ -139,7 +139,7 @@ const char* pa_status_string(int status);
  * as pa_decode computes it (fp32 softmax and accumulation; f16 operands,
  * which hold every E4M3 value exactly; q is rounded to f16 after a per-head
  * power-of-two scaling, the softmax weights to f16 after a 2^15 scaling, a
- * relative error of at most 2^-12).  Same arguments and
+ * relative error of at most 2^-11).  Same arguments and
  * workspace as pa_decode, plus the two scales (finite, > 0).  d_head must be
  * 128 (PA_ERR_UNSUPPORTED otherwise).  With G = 4 and an even n_kv_heads a
  * thread block covers two adjacent KV heads (their 8 query heads fill the
@@ -292,10 +292,17 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
  * chunk of a prompt, or the part of a prompt after a prefix-cache hit, is
  * n < C.  Positions are read through block_tables as for decode.
  *
- * Scores and sums are fp32 (tensor cores, bf16 inputs); the softmax weights
- * are rounded to bf16 before the weighted sum of values (the normaliser sums
- * them unrounded), so an output element can differ from the exact value by
- * up to 2^-8 * sum_j a_j |V_j| besides fp32 rounding.
+ * Scores and sums are fp32 (tensor cores; bf16 q and K).  The weighted sum
+ * of values takes fp16 operands: first, V is gathered through the block
+ * table into the caller's workspace (each 128-position tile of each
+ * sequence and KV head contiguous), as fp16, which holds every bf16
+ * magnitude in [2^-14, 2^16) exactly and is within 2^-25 below it; the
+ * softmax weights are rounded to fp16 (a relative 2^-11; the normaliser
+ * sums them unrounded), so an output element can differ from the exact
+ * value by up to about 2^-11 * sum_j a_j |V_j| besides fp32 rounding.  A
+ * tile holding a value of magnitude 2^16 or more, or a non-finite one,
+ * stays bf16, and its weights go as two bf16 terms (hi + lo, a relative
+ * 2^-16).
  *
  * Arguments
  *   out           device [num_tokens][n_q_heads][d_head], bf16 or fp32 per
@@ -315,6 +322,15 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
  *                 computed).
  *   n_q_heads / n_kv_heads must be a power of two <= 128; d_head 64 or 128;
  *   block_size 8, 16 or 32.
+ *   workspace     device, 16-byte aligned, at least
+ *                 pa_prefill_workspace_size(num_seqs, max_blocks_per_seq,
+ *                 block_size, n_kv_heads, d_head) bytes (workspace_bytes):
+ *                 the V staging (n_kv_heads x num_seqs x L positions x
+ *                 d_head x 2 bytes, L = max_blocks_per_seq * block_size
+ *                 rounded up to 128) and one format byte per 128 positions.
+ *                 Caller-owned; overwritten by each call, so calls that
+ *                 share one must be ordered (one stream).  Missing or too
+ *                 small: PA_ERR_WORKSPACE.  num_seqs at most 65535.
  *   sched_dev     optional device int32 [2], zero before the first call; the
  *                 kernel's blocks claim work items from it (KV head by KV
  *                 head, within a head the latest query rows, which see the
@@ -323,8 +339,8 @@ int pa_decode_static_scratch(void* out, int out_dtype, const void* q,
  *                 stream).  NULL: a fixed round-robin assignment, slower when
  *                 sequences differ in length.  Caller-owned.
  *   status_dev    optional device int32, see PA_DEV_* above.
- * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED or
- * PA_ERR_CUDA.
+ * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED,
+ * PA_ERR_WORKSPACE or PA_ERR_CUDA.
  */
 int pa_prefill(void* out, int out_dtype, const void* q,
                const void* k_cache, const void* v_cache,
@@ -332,8 +348,12 @@ int pa_prefill(void* out, int out_dtype, const void* q,
                const int32_t* query_start, const int32_t* context_lens,
                int num_seqs, int num_tokens, int max_query_len, int num_blocks,
                int block_size, float scale, int n_q_heads, int n_kv_heads,
-               int d_head, int32_t* sched_dev, int32_t* status_dev,
-               void* stream);
+               int d_head, void* workspace, size_t workspace_bytes,
+               int32_t* sched_dev, int32_t* status_dev, void* stream);
+
+/* Bytes of workspace pa_prefill needs (0 for a non-positive argument). */
+size_t pa_prefill_workspace_size(int num_seqs, int max_blocks_per_seq,
+                                 int block_size, int n_kv_heads, int d_head);
 
 /* ===========================================================================
  * Cache writes

@@ -78,7 +78,8 @@ _SIGS = {
     "pa_reshape_and_cache_fp8": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                           _c_float, _vp, _vp]),
     "pa_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
-                            _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _vp, _vp]),
+                            _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp, _vp]),
+    "pa_prefill_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_check_bounded_wait": (_c_int, [_c_int, _vp, _vp]),
     "pa_lse_merge": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
@@ -289,12 +290,25 @@ def prefill_counters(device, stream=None):
     return t
 
 
+def pa_prefill_workspace_size(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head):
+    return int(_lib.pa_prefill_workspace_size(int(num_seqs), int(max_blocks_per_seq), int(block_size),
+                                              int(n_kv_heads), int(d_head)))
+
+
+def prefill_workspace(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head, device=None):
+    """A caller-owned workspace tensor (uint8) of the size pa_prefill needs."""
+    n = pa_prefill_workspace_size(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device or "cuda")
+
+
 def pa_prefill(out, q, k_cache, v_cache, block_tables, query_start, context_lens, max_query_len, block_size,
-               scale, n_q_heads, n_kv_heads, d_head, status=None, stream=None, counters=None):
+               scale, n_q_heads, n_kv_heads, d_head, status=None, stream=None, counters=None, workspace=None):
     """out [T, Hq, D] (bf16 or f32) <- causal paged prefill attention of the
     new positions of each sequence; see pa.h.  `counters`: the int32 [2]
     work-claim pair (default: this stream's, from prefill_counters; False:
-    none, a fixed round-robin assignment of work)."""
+    none, a fixed round-robin assignment of work).  `workspace`: a uint8
+    device tensor of at least pa_prefill_workspace_size bytes (default: one
+    allocated for this call through PyTorch's caching allocator)."""
     if out.dtype == torch.bfloat16:
         out_dtype = PA_DTYPE_BF16
     elif out.dtype == torch.float32:
@@ -314,12 +328,15 @@ def pa_prefill(out, q, k_cache, v_cache, block_tables, query_start, context_lens
     num_seqs = block_tables.shape[0]
     if block_tables.dim() != 2 or context_lens.shape != (num_seqs,) or query_start.shape != (num_seqs + 1,):
         raise ValueError("block_tables [S, max_blocks], query_start [S + 1], context_lens [S]")
+    if workspace is None:
+        workspace = prefill_workspace(num_seqs, block_tables.shape[1], block_size, n_kv_heads, d_head, q.device)
     st = _lib.pa_prefill(_opt_dev(out, out.dtype, "out"), out_dtype, _dev(q, torch.bfloat16, "q"),
                          _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
                          _dev(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
                          _dev(query_start, torch.int32, "query_start"), _dev(context_lens, torch.int32, "context_lens"),
                          int(num_seqs), int(num_tokens), int(max_query_len), int(k_cache.shape[0]), int(block_size),
                          float(scale), int(n_q_heads), int(n_kv_heads), int(d_head),
+                         _dev(workspace, torch.uint8, "workspace"), int(workspace.numel()),
                          _opt_dev(None if counters is False else counters, torch.int32, "counters"),
                          _opt_dev(status, torch.int32, "status"),
                          _stream(stream))

@@ -24,7 +24,7 @@
 //    form needs about 150.
 //  * Softmax is online, in fp32, with a running maximum per head in the log2
 //    domain.  P enters P.V as two bf16 terms (hi + lo), which keeps its
-//    rounding near 2^-17 relative instead of bf16's 2^-9.
+//    rounding within about 2^-16 relative instead of bf16's 2^-8.
 //  * One thread block of 4 warps per (sequence, head group, partition of
 //    partition_size positions); the hardware hands blocks to SMs as others
 //    finish, which balances ragged batches.  The 4 warps of a block are

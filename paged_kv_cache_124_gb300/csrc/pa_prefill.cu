@@ -31,15 +31,21 @@
 //     tiles ahead.  Blocks past the needed range, and bad table entries, are
 //     loaded from outside the tensor, which fills zeros and reads no HBM.
 //   * S = Q K^T (M 128, N 128, K d) and O += P V (M 128, N d, K 128) are
-//     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate), one issuing thread
-//     per Q tile (two issuers hide most of the pipe drain between groups of
+//     tcgen05.mma kind::f16 (fp32 accumulate), one issuing thread per Q
+//     tile (two issuers hide most of the pipe drain between groups of
 //     products of different kinds).  Tensor memory holds S_A, S_B (128
-//     columns each) and O_A, O_B (d columns each).  Each weight is split
-//     into two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), written over
-//     the first and the second 64 columns of its own S; both are read from
-//     there as A operands (O += P_hi V + P_lo V), so the weights reach the
-//     products to a relative 2^-16, not bf16's 2^-8.  V is an MN-major
-//     operand read straight from the TMA layout.
+//     columns each) and O_A, O_B (d columns each).  S takes bf16 Q and K.
+//     P V takes fp16 weights (written over the first 64 columns of their
+//     own S and read from there as the A operand) and fp16 values: the V
+//     warp turns each landed V tile into fp16 in place, which is exact for
+//     every bf16 magnitude in [2^-14, 2^16) and off by at most 2^-25 below
+//     it, and fp16 carries each weight to a relative 2^-11 where bf16 would
+//     give 2^-8.  A V tile holding a magnitude of 2^16 or more (or a
+//     non-finite value) is copied again and stays bf16; for it each weight
+//     is split into two bf16 terms, hi = bf16(p) and lo = bf16(p - hi),
+//     written over the first and the second 64 columns of S (O += P_hi V +
+//     P_lo V, a relative 2^-16).  V is an MN-major operand read straight
+//     from the TMA layout.
 //   * Eight softmax warps work on tile A, then on tile B, then on tile A of
 //     the next K/V tile, ...: warps w and w + 4 share the 32 rows of lane
 //     quarter w (tensor-memory lane = row), each taking 64 of the 128
@@ -59,6 +65,7 @@
 #include <cudaTypedefs.h>
 
 #include <climits>
+#include <type_traits>
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -76,6 +83,7 @@ constexpr uint32_t kTmemS0 = 0;            // S_A; S_B at +128
 constexpr uint32_t kTmemO0 = 256;          // O_A; O_B at +128
 constexpr int kMaxProbes = 2000000;        // x <= ~1 us per probe
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest weight allowed before a rescale
+constexpr float kWeightShift = 7.0f;       // weights carry 2^7: at most 2^15, within fp16's range
 // Two stages each for K and V: a third K stage (the shared memory allows one)
 // measured no faster.
 constexpr int kKStages = 2;
@@ -120,6 +128,9 @@ struct PrefillArgs {
     int num_blocks;
     int oob_row;          // a row coordinate past the end of the cache view
     float scale_log2;     // scale * log2(e)
+    const uint8_t* v_fmt; // per (KV head, sequence, 128-position tile) of the V staging: 0 fp16, 1 bf16
+    int l_slot;           // positions per (KV head, sequence) in the V staging, a multiple of 128
+    int t_slot;           // l_slot / 128
     int32_t* status;
     int* sched;           // {next item, CTAs done} claimed with atomics, or null: fixed order
 };
@@ -131,6 +142,7 @@ struct PrefillArgs {
 struct Item {
     int seq, h, q0, n, ctx, t0;
     int kv_end0, kv_end1, nt0, nt1, n_tiles, has_b;
+    int wide;             // some V tile of the item is staged as bf16
 };
 
 struct Bars {
@@ -140,8 +152,8 @@ struct Bars {
     uint64_t k_empty[2][kKStages];  // per Q tile and stage: its score products reading K are done
     uint64_t v_empty[2][kVStages];  // per Q tile and stage: its value products reading V are done
     uint64_t s_full[2];   // per Q tile: its scores are in tensor memory
-    uint64_t p_full[2];   // per Q tile: its weights' hi terms are in tensor memory (and O rescaled)
-    uint64_t plo_full[2]; // per Q tile: its weights' lo terms are in tensor memory
+    uint64_t p_full[2];   // per Q tile: its weights (fp16, or the bf16 hi terms) are in tensor memory (and O rescaled)
+    uint64_t plo_full[2]; // per Q tile: the bf16 lo terms of a wide tile's weights are in tensor memory
     uint64_t o_done[2];   // per Q tile: its last product of an item has finished
     uint64_t o_free[2];   // per Q tile: the softmax warps have read O out
     uint64_t q_empty[2];  // per Q tile: its last score product of an item has finished
@@ -163,14 +175,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            ((uint64_t)((sbo & 0x3FFFF) >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, A K-major,
-// B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
-           ((uint32_t)(m >> 4) << 24);
+// kind::f16 instruction descriptor: fp32 accumulator, A and B both bf16 (bf = 1)
+// or both fp16 (bf = 0), A K-major, B K-major (b_mn = 0) or MN-major
+// (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, int b_mn, int bf) {
+    return (1u << 4) | ((uint32_t)bf << 7) | ((uint32_t)bf << 10) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
@@ -225,8 +238,8 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* w) {
         "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]));
 }
 
-// A operand from tensor memory (M rows in lanes, two bf16 per column).
-__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+// A operand from tensor memory (M rows in lanes, two 16-bit values per column).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                             uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -320,6 +333,53 @@ __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_f16_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two bf16 values to two fp16 values (each bf16 value is exact in fp32; the
+// fp16 rounding is exact for magnitudes in [2^-14, 65536)).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    return pack_f16_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// The largest bf16 magnitude pattern (sign cleared) that fp16 still holds:
+// 0x4780 is 2^16, the first bf16 magnitude that fp16 rounds to infinity;
+// patterns at or above it also cover infinities and NaNs.
+constexpr uint32_t kF16Wide = 0x4780u;
+
+// The weights of one thread's kHalfCols scores s (in place: s becomes the
+// fp32 weights p = 2^(s * c2 + neg)), their sums (into lp) and, at t_p in
+// tensor memory, their kHalfCols / 2 columns of packed pairs: fp16, or the
+// bf16 hi terms (kBf16) whose lo terms the caller writes next.
+template <int kHalfCols, bool kBf16>
+__device__ __forceinline__ void write_weights(float (&s)[kHalfCols], uint64_t c2x2, uint64_t negx2, uint64_t (&lp)[2],
+                                              uint32_t t_p) {
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t w[kHalfCols / 4];
+#pragma unroll
+        for (int qq = 0; qq < kHalfCols / 4; ++qq) {
+            const int q = h2 * (kHalfCols / 4) + qq;
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(s[2 * q], s[2 * q + 1]), c2x2, negx2), x0, x1);
+            s[2 * q] = fast_exp2(x0);
+            s[2 * q + 1] = fast_exp2(x1);
+            lp[q & 1] = add_f32x2(lp[q & 1], f32x2(s[2 * q], s[2 * q + 1]));
+            w[qq] = kBf16 ? pack_bf16_rn(s[2 * q], s[2 * q + 1]) : pack_f16_rn(s[2 * q], s[2 * q + 1]);
+        }
+        tmem_st16u(t_p + h2 * (kHalfCols / 4), w);
+    }
+}
+
 // --- bounded waits -------------------------------------------------------------
 
 // One thread.  Gives up when another role has aborted or after kMaxProbes
@@ -363,15 +423,21 @@ __device__ bool wait_warp(uint64_t* bar, uint32_t parity, Bars* b, int32_t* stat
 // group holds at least two items per CTA, so that its lightest items, not
 // heavy ones, end each group.  False when the item holds no query row (past
 // the sequence's new tokens) or is invalid.
-__device__ __forceinline__ bool decode_item(int i, const PrefillArgs& a, Item& it, bool flag) {
+// Item i's sequence, KV head and query tile pair (arithmetic only).
+__device__ __forceinline__ void item_coords(int i, const PrefillArgs& a, int& seq, int& h, int& tile) {
     const int per_group = a.tiles_per_seq * a.num_seqs * a.heads_per_group;
     const int grp = i / per_group;
     const int r = i - grp * per_group;
     const int per_tile = a.num_seqs * min(a.heads_per_group, a.n_kv_heads - grp * a.heads_per_group);
-    const int tile = a.tiles_per_seq - 1 - r / per_tile;
+    tile = a.tiles_per_seq - 1 - r / per_tile;
     const int r2 = r % per_tile;
-    it.seq = r2 % a.num_seqs;
-    it.h = grp * a.heads_per_group + r2 / a.num_seqs;
+    seq = r2 % a.num_seqs;
+    h = grp * a.heads_per_group + r2 / a.num_seqs;
+}
+
+__device__ __forceinline__ bool decode_item(int i, const PrefillArgs& a, Item& it, bool flag) {
+    int tile;
+    item_coords(i, a, it.seq, it.h, tile);
     it.q0 = a.query_start[it.seq];
     it.n = a.query_start[it.seq + 1] - it.q0;
     it.ctx = a.context_lens[it.seq];
@@ -502,7 +568,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     post(it);
                     break;
                 }
+                // Do any of the item's V tiles stay bf16?  (The other warps
+                // then check tile by tile.)  The first 32 format bytes are
+                // loaded alongside the item's own loads.
+                int fseq, fh, ftile;
+                item_coords(i, a, fseq, fh, ftile);
+                const uint8_t* fmt = a.v_fmt + (size_t)(fh * a.num_seqs + fseq) * a.t_slot;
+                int w = lane < a.t_slot ? fmt[lane] : 0;
                 if (!decode_item(i, a, it, lane == 0)) continue;
+                w = lane < it.n_tiles ? w : 0;
+                for (int jj = lane + 32; jj < it.n_tiles; jj += 32) w |= fmt[jj];
+                it.wide = __any_sync(0xffffffffu, w != 0) ? 1 : 0;
                 ok = post(it);
                 if (!ok) break;
                 // Q of this item replaces the previous item's once both tiles'
@@ -532,13 +608,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int kv_all = it.has_b ? it.kv_end1 : it.kv_end0;
             const int32_t* table = a.block_tables + (size_t)it.seq * a.max_blocks;
-            // Block-table entries are fetched kAhead tiles before their copies
-            // and checked only when used, so no copy waits on a table load.
+            // K: block-table entries are fetched kAhead tiles before their
+            // copies and checked only when used, so no copy waits on a table
+            // load.  V comes from the staging buffer, whose tiles are
+            // contiguous (one box of 128 rows per 64 columns).
             constexpr int kAhead = 4;
             constexpr int kNoBlock = INT_MIN;             // past the needed range: nothing loaded
+            const int vrow0 = (it.h * a.num_seqs + it.seq) * a.l_slot;
             auto fetch = [&](int j) {
                 const int pos = j * kKv + lane * a.block_size;
-                return (lane < bpt && pos < kv_all) ? __ldg(table + pos / a.block_size) : kNoBlock;
+                return (is_k && lane < bpt && pos < kv_all) ? __ldg(table + pos / a.block_size) : kNoBlock;
             };
             auto to_row = [&](int blk) {
                 if (blk == kNoBlock) return a.oob_row;
@@ -562,10 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = 0; u < kAhead; ++u) {
                     const int j = j0 + u;
                     if (j >= it.n_tiles) break;
-                    const int row = to_row(blks[u]);
+                    const int row = is_k ? to_row(blks[u]) : vrow0 + j * kKv;
                     blks[u] = fetch(j + kAhead);
                     const int st = g % stages;
-                    const uint32_t s_t = pa::smem_addr(sm + base + st * G::kKVBytes) + lane * a.block_size * 128;
+                    const uint32_t s_t =
+                        pa::smem_addr(sm + base + st * G::kKVBytes) + (is_k ? lane * a.block_size * 128 : 0);
                     // both Q tiles' MMA warps release every K/V tile (used or not)
                     if (g >= stages)
                         ok = wait_warp(&empty0[st], (g / stages - 1) & 1, bars, a.status) &&
@@ -573,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     if (lane == 0) pa::mbar_arrive_expect_tx(&full[st], G::kKVBytes);
                     __syncwarp();
-                    if (lane < bpt)
+                    if (is_k ? lane < bpt : lane == 0)
 #pragma unroll
                         for (int hh = 0; hh < G::kHalves; ++hh)
                             tma_2d(s_t + hh * G::kHalfBytes, map, hh * 64, row, &full[st]);
@@ -599,8 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // fast enough to keep the tensor pipe busy, two can.
         const int x = warp - kMmaWarp0;
         if (lane == 0) {
-            constexpr uint32_t id_qk = idesc_bf16(kRows, kKv, 0);
-            constexpr uint32_t id_pv = idesc_bf16(kRows, D, 1);
+            constexpr uint32_t id_qk = idesc_f16(kRows, kKv, 0, 1);
+            constexpr uint32_t id_pv = idesc_f16(kRows, D, 1, 0);      // fp16 weights and values
+            constexpr uint32_t id_pv_bf = idesc_f16(kRows, D, 1, 1);   // a wide tile's bf16 hi and lo terms
             const uint32_t t_s = tmem + kTmemS0 + x * 128;
             const uint32_t t_o = tmem + kTmemO0 + x * 128;
             const uint32_t qx = s_q + x * G::kQBytes;
@@ -616,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * G::kHalfBytes + (kk & 3) * 32;
-                    mma_bf16(t_s, smem_desc(qx + off, 16, 1024), smem_desc(s_k + off, 16, 1024), id_qk, kk > 0);
+                    mma_f16_ss(t_s, smem_desc(qx + off, 16, 1024), smem_desc(s_k + off, 16, 1024), id_qk, kk > 0);
                 }
             };
             // A tile this Q tile does not read is released only once it has
@@ -629,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pa::mbar_arrive(&bars->v_empty[x][gt % kVStages]);
                 return true;
             };
-            int g = 0, c = 0, ns = 0, nod = 0;            // K/V tiles, items, S products, outputs so far
+            int g = 0, c = 0, ns = 0, nod = 0, nw = 0;    // K/V tiles, items, S products, outputs, wide tiles so far
             bool ok = true;
             for (int nc = 0;; ++nc) {
                 const int slot = nc % kRing;
@@ -640,8 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it.seq < 0) break;
                 const int ntx = x ? it.nt1 : it.nt0;
                 const int kv_endx = x ? it.kv_end1 : it.kv_end0;
-                // end of the context's last block: rows from ctx up to it may hold junk
-                const int ctx_blocks_end = ((it.ctx + a.block_size - 1) / a.block_size) * a.block_size;
+                const size_t fmt0 = (size_t)(it.h * a.num_seqs + it.seq) * a.t_slot;
                 if (ntx == 0) {
                     // this Q tile has no rows in the item: release Q and every K/V tile
                     ok = wait1(&bars->q_full, c & 1, bars, a.status);
@@ -661,66 +741,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++ns;
                 commit(&bars->k_empty[x][g % kKStages], (g / kKStages) & 1);
                 if (ntx == 1) commit(&bars->q_empty[x], c & 1);
-                for (int j = 0; ok && j < it.n_tiles; ++j) {
-                    const int gj = g + j;
-                    const int vs = gj % kVStages;
-                    if (j >= ntx) {                       // tile beyond this Q tile's keys
-                        ok = skip_tile(gj);
-                        continue;
+                // The item's tiles, in one of two forms (as the softmax warps):
+                // all V tiles fp16, or some bf16, checked tile by tile.
+                auto run_tiles = [&](auto may_be_wide) {
+                    constexpr bool kMayBeWide = decltype(may_be_wide)::value;
+                    for (int j = 0; ok && j < it.n_tiles; ++j) {
+                        const int gj = g + j;
+                        const int vs = gj % kVStages;
+                        if (j >= ntx) {                       // tile beyond this Q tile's keys
+                            ok = skip_tile(gj);
+                            continue;
+                        }
+                        // the staged tile's format (loaded before the waits below hide its latency)
+                        const bool wide = kMayBeWide && a.v_fmt[fmt0 + j] != 0;
+                        ok = wait1(&bars->v_full[vs], (gj / kVStages) & 1, bars, a.status);
+                        if (!ok) break;
+                        const uint32_t s_v = pa::smem_addr(sm + G::kV0 + vs * G::kKVBytes);
+                        const int valid = min(kKv, kv_endx - j * kKv);
+                        const int ksteps = (valid + 15) >> 4;
+                        const int nks = (gj + 1) % kKStages;
+                        if (j + 1 < ntx) ok = wait1(&bars->k_full[nks], ((gj + 1) / kKStages) & 1, bars, a.status);
+                        // O must have been read out by the previous item's epilogue
+                        if (ok && j == 0 && nod >= 1) ok = wait1(&bars->o_free[x], (nod - 1) & 1, bars, a.status);
+                        if (ok) ok = wait1(&bars->p_full[x], (ns - 1) & 1, bars, a.status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // O += P V with fp16 weights and values; for a wide tile
+                        // O += P_hi V as soon as the hi terms are written, then
+                        // O += P_lo V (the softmax writes lo meanwhile).  Each
+                        // loop keeps its instruction descriptor a constant (a
+                        // descriptor chosen at run time slowed the issue by 4 %).
+                        if (!wide) {
+                            for (int kk = 0; kk < ksteps; ++kk)
+                                mma_f16_ta(t_o, t_s + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
+                                           (j > 0 || kk > 0) ? 1u : 0u);
+                        } else {
+                            for (int kk = 0; kk < ksteps; ++kk)
+                                mma_f16_ta(t_o, t_s + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv_bf,
+                                           (j > 0 || kk > 0) ? 1u : 0u);
+                            ok = wait1(&bars->plo_full[x], nw & 1, bars, a.status);
+                            ++nw;
+                            if (!ok) break;
+                            tc_fence_after();
+                            for (int kk = 0; kk < ksteps; ++kk)
+                                mma_f16_ta(t_o, t_s + kKv / 2 + kk * 8,
+                                            smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv_bf, 1u);
+                        }
+                        commit(&bars->v_empty[x][vs], (gj / kVStages) & 1);
+                        if (j == ntx - 1) {
+                            commit(&bars->o_done[x], nod & 1);
+                            ++nod;
+                        } else {
+                            issue_s(nks);
+                            commit(&bars->s_full[x], ns & 1);
+                            ++ns;
+                            commit(&bars->k_empty[x][nks], ((gj + 1) / kKStages) & 1);
+                            if (j + 1 == ntx - 1) commit(&bars->q_empty[x], c & 1);
+                        }
                     }
-                    ok = wait1(&bars->v_full[vs], (gj / kVStages) & 1, bars, a.status);
-                    if (!ok) break;
-                    uint8_t* vbase = sm + G::kV0 + vs * G::kKVBytes;
-                    const uint32_t s_v = pa::smem_addr(vbase);
-                    const int valid = min(kKv, kv_endx - j * kKv);
-                    const int ksteps = (valid + 15) >> 4;
-                    // Rows at and past the context length inside the last block may
-                    // hold anything (NaN included); their weights are 0, but 0 * NaN
-                    // is not, so clear those V rows before the product reads them.
-                    // Only rows past the context are touched (both issuers may clear
-                    // the same rows; they write the same zeros).
-                    const int zero_begin = max(valid, it.ctx - j * kKv);
-                    const int zero_end = min(ksteps * 16, ctx_blocks_end - j * kKv);
-                    if (zero_begin < zero_end) {
-                        for (int r = zero_begin; r < zero_end; ++r)
-#pragma unroll
-                            for (int hh = 0; hh < G::kHalves; ++hh) {
-                                uint4* rowp = reinterpret_cast<uint4*>(vbase + hh * G::kHalfBytes + r * 128);
-#pragma unroll
-                                for (int cc = 0; cc < 8; ++cc) rowp[cc] = make_uint4(0, 0, 0, 0);
-                            }
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    }
-                    const int nks = (gj + 1) % kKStages;
-                    if (j + 1 < ntx) ok = wait1(&bars->k_full[nks], ((gj + 1) / kKStages) & 1, bars, a.status);
-                    // O must have been read out by the previous item's epilogue
-                    if (ok && j == 0 && nod >= 1) ok = wait1(&bars->o_free[x], (nod - 1) & 1, bars, a.status);
-                    if (ok) ok = wait1(&bars->p_full[x], (ns - 1) & 1, bars, a.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // O += P_hi V as soon as the hi terms are written, then
-                    // O += P_lo V (the softmax writes lo meanwhile)
-                    for (int kk = 0; kk < ksteps; ++kk)
-                        mma_bf16_ta(t_o, t_s + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024), id_pv,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
-                    ok = wait1(&bars->plo_full[x], (ns - 1) & 1, bars, a.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    for (int kk = 0; kk < ksteps; ++kk)
-                        mma_bf16_ta(t_o, t_s + kKv / 2 + kk * 8, smem_desc(s_v + kk * 2048, G::kHalfBytes, 1024),
-                                    id_pv, 1u);
-                    commit(&bars->v_empty[x][vs], (gj / kVStages) & 1);
-                    if (j == ntx - 1) {
-                        commit(&bars->o_done[x], nod & 1);
-                        ++nod;
-                    } else {
-                        issue_s(nks);
-                        commit(&bars->s_full[x], ns & 1);
-                        ++ns;
-                        commit(&bars->k_empty[x][nks], ((gj + 1) / kKStages) & 1);
-                        if (j + 1 == ntx - 1) commit(&bars->q_empty[x], c & 1);
-                    }
-                }
+                };
+                if (it.wide)
+                    run_tiles(std::true_type{});
+                else
+                    run_tiles(std::false_type{});
                 g += it.n_tiles;
                 ++c;
             }
@@ -766,109 +849,120 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kv_end = x ? it.kv_end1 : it.kv_end0;
                 row_lim[x] = valid_row[x] ? min(it.ctx - it.n + tok + 1, kv_end) : kv_end;   // keys [0, row_lim)
             }
-            for (int j = 0; ok && j < it.n_tiles; ++j) {
-                for (int x = 0; x < 2; ++x) {
-                    if (j >= nt[x]) continue;
-                    ok = wait_warp(&bars->s_full[x], ns[x] & 1, bars, a.status);
-                    ++ns[x];
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t t_s = t_lane + kTmemS0 + x * 128;
-                    float s[kHalfCols];
+            const uint8_t* fmt = a.v_fmt + (size_t)(it.h * a.num_seqs + it.seq) * a.t_slot;
+            // The item's tiles, in one of two forms: all V tiles fp16 (the
+            // common case, with no per-tile format check) or some bf16.
+            auto run_tiles = [&](auto may_be_wide) {
+                constexpr bool kMayBeWide = decltype(may_be_wide)::value;
+                for (int j = 0; ok && j < it.n_tiles; ++j) {
+                    const int wide = kMayBeWide ? fmt[j] : 0;   // V tile j staged as fp16 (0) or bf16 (1)
+                    for (int x = 0; x < 2; ++x) {
+                        if (j >= nt[x]) continue;
+                        ok = wait_warp(&bars->s_full[x], ns[x] & 1, bars, a.status);
+                        ++ns[x];
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t t_s = t_lane + kTmemS0 + x * 128;
+                        float s[kHalfCols];
 #pragma unroll
-                    for (int cc = 0; cc < kHalfCols / 32; ++cc) tmem_ld32(t_s + hc * kHalfCols + cc * 32, s + cc * 32);
-                    tmem_wait_ld();
-                    const int lim = row_lim[x] - j * kKv - hc * kHalfCols;     // valid columns of this half
-                    if (lim < kHalfCols) {
+                        for (int cc = 0; cc < kHalfCols / 32; ++cc)
+                            tmem_ld32(t_s + hc * kHalfCols + cc * 32, s + cc * 32);
+                        tmem_wait_ld();
+                        const int lim = row_lim[x] - j * kKv - hc * kHalfCols;     // valid columns of this half
+                        if (lim < kHalfCols) {
 #pragma unroll
-                        for (int cc = 0; cc < kHalfCols; ++cc) s[cc] = cc < lim ? s[cc] : -INFINITY;
-                    }
-                    float mp[8];
+                            for (int cc = 0; cc < kHalfCols; ++cc) s[cc] = cc < lim ? s[cc] : -INFINITY;
+                        }
+                        float mp[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) mp[k] = max3(s[k], s[8 + k], s[16 + k]);
+                        for (int k = 0; k < 8; ++k) mp[k] = max3(s[k], s[8 + k], s[16 + k]);
 #pragma unroll
-                    for (int cc = 24; cc + 16 <= kHalfCols; cc += 16)
+                        for (int cc = 24; cc + 16 <= kHalfCols; cc += 16)
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) mp[k] = max3(mp[k], s[cc + k], s[cc + 8 + k]);
-                    if ((kHalfCols - 24) % 16 == 8) {
+                            for (int k = 0; k < 8; ++k) mp[k] = max3(mp[k], s[cc + k], s[cc + 8 + k]);
+                        if ((kHalfCols - 24) % 16 == 8) {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[kHalfCols - 8 + k]);
-                    }
-                    float mt = fmaxf(max3(mp[0], mp[1], mp[2]), fmaxf(max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-                    mt = fmaxf(mt, exchange(x, mt, ok));
-                    if (!ok) break;
-                    const float mts = mt * c2;            // scale > 0: the maximum commutes with it
-                    const bool rescale = mts > m_used[x] + kRescaleThreshold;
-                    const float m_new = rescale ? mts : m_used[x];
-                    const float alpha = rescale ? fast_exp2(m_used[x] - m_new) : 1.f;   // exp2(-inf) = 0 at first
-                    if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-                        // O holds the products of tiles < j (complete: this tile's
-                        // scores were issued after them) and not yet this tile's
-                        const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
+                            for (int k = 0; k < 8; ++k) mp[k] = fmaxf(mp[k], s[kHalfCols - 8 + k]);
+                        }
+                        float mt = fmaxf(max3(mp[0], mp[1], mp[2]),
+                                         fmaxf(max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+                        mt = fmaxf(mt, exchange(x, mt, ok));
+                        if (!ok) break;
+                        const float mts = mt * c2;            // scale > 0: the maximum commutes with it
+                        const bool rescale = mts > m_used[x] + kRescaleThreshold;
+                        const float m_new = rescale ? mts : m_used[x];
+                        const float alpha = rescale ? fast_exp2(m_used[x] - m_new) : 1.f;   // exp2(-inf) = 0 at first
+                        if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+                            // O holds the products of tiles < j (complete: this tile's
+                            // scores were issued after them) and not yet this tile's
+                            const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
 #pragma unroll 1
-                        for (int cc = 0; cc < kOCols / 32; ++cc) {
-                            float o[32];
-                            tmem_ld32(t_o + cc * 32, o);
-                            tmem_wait_ld();
-                            scale_f32x2<32>(o, alpha);
-                            tmem_st32(t_o + cc * 32, o);
+                            for (int cc = 0; cc < kOCols / 32; ++cc) {
+                                float o[32];
+                                tmem_ld32(t_o + cc * 32, o);
+                                tmem_wait_ld();
+                                scale_f32x2<32>(o, alpha);
+                                tmem_st32(t_o + cc * 32, o);
+                            }
+                        }
+                        l[x] *= alpha;
+                        m_used[x] = m_new;
+                        // Weights are p = 2^(s * c2 - m_used + 7): the 2^7 (the sums
+                        // carry it too, so it cancels) puts them in [0, 2^15], where
+                        // fp16 rounds every weight above 2^-21 of the row maximum to
+                        // a relative 2^-11.
+                        const float neg = kWeightShift - m_used[x];
+                        // Column pairs in packed f32x2 arithmetic: one FMA and one
+                        // add per two weights.  The weights go to the tensor cores
+                        // as fp16, written over the first 64 columns of S.  For a
+                        // wide value tile (bf16) each weight p goes as two bf16
+                        // terms instead, hi = bf16(p) and lo = bf16(p - hi) (p - hi
+                        // is exact in fp32), so that hi + lo carries p to a relative
+                        // 2^-16 instead of bf16's 2^-8.  P_hi is written over the
+                        // first 64 columns of S and posted first, so the value
+                        // products on it start while lo is computed and written over
+                        // the other 64 columns.
+                        const uint64_t c2x2 = f32x2(c2, c2), negx2 = f32x2(neg, neg);
+                        uint64_t lp[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};   // independent partial sums
+                        if (!wide)
+                            write_weights<kHalfCols, false>(s, c2x2, negx2, lp, t_s + hc * (kHalfCols / 2));
+                        else
+                            write_weights<kHalfCols, true>(s, c2x2, negx2, lp, t_s + hc * (kHalfCols / 2));
+                        tmem_wait_st();
+                        tc_fence_before();
+                        pa::mbar_arrive(&bars->p_full[x]);
+                        float l0, l1, l2, l3;
+                        f32x2_split(lp[0], l0, l1);
+                        f32x2_split(lp[1], l2, l3);
+                        l[x] += (l0 + l1) + (l2 + l3);
+                        if (wide) {
+#pragma unroll
+                            for (int h2 = 0; h2 < 2; ++h2) {
+                                uint32_t wl[kHalfCols / 4];
+#pragma unroll
+                                for (int qq = 0; qq < kHalfCols / 4; ++qq) {
+                                    const int q = h2 * (kHalfCols / 4) + qq;
+                                    const uint32_t hi = pack_bf16_rn(s[2 * q], s[2 * q + 1]);
+                                    float r0, r1;
+                                    f32x2_split(sub_f32x2(f32x2(s[2 * q], s[2 * q + 1]),
+                                                          f32x2(__uint_as_float(hi << 16),
+                                                                __uint_as_float(hi & 0xffff0000u))),
+                                                r0, r1);
+                                    wl[qq] = pack_bf16_rn(r0, r1);
+                                }
+                                tmem_st16u(t_s + kKv / 2 + hc * (kHalfCols / 2) + h2 * (kHalfCols / 4), wl);
+                            }
+                            tmem_wait_st();
+                            tc_fence_before();
+                            pa::mbar_arrive(&bars->plo_full[x]);
                         }
                     }
-                    l[x] *= alpha;
-                    m_used[x] = m_new;
-                    const float neg = -m_used[x];
-                    // Column pairs in packed f32x2 arithmetic: one FMA and one
-                    // add per two weights.  Each weight p goes to the tensor
-                    // cores as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi)
-                    // (p - hi is exact in fp32), so that hi + lo carries p to a
-                    // relative 2^-16 instead of bf16's 2^-8.  P_hi is written over
-                    // the first 64 columns of S and posted first, so the value
-                    // products on it start while lo is computed and written over
-                    // the other 64 columns.
-                    const uint64_t c2x2 = f32x2(c2, c2), negx2 = f32x2(neg, neg);
-                    uint64_t lp[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};   // independent partial sums
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t w[kHalfCols / 4];
-#pragma unroll
-                        for (int qq = 0; qq < kHalfCols / 4; ++qq) {
-                            const int q = h2 * (kHalfCols / 4) + qq;
-                            float x0, x1;
-                            f32x2_split(fma_f32x2(f32x2(s[2 * q], s[2 * q + 1]), c2x2, negx2), x0, x1);
-                            s[2 * q] = fast_exp2(x0);
-                            s[2 * q + 1] = fast_exp2(x1);
-                            lp[q & 1] = add_f32x2(lp[q & 1], f32x2(s[2 * q], s[2 * q + 1]));
-                            w[qq] = pack_bf16_rn(s[2 * q], s[2 * q + 1]);
-                        }
-                        tmem_st16u(t_s + hc * (kHalfCols / 2) + h2 * (kHalfCols / 4), w);
-                    }
-                    tmem_wait_st();
-                    tc_fence_before();
-                    pa::mbar_arrive(&bars->p_full[x]);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t wl[kHalfCols / 4];
-#pragma unroll
-                        for (int qq = 0; qq < kHalfCols / 4; ++qq) {
-                            const int q = h2 * (kHalfCols / 4) + qq;
-                            const uint32_t hi = pack_bf16_rn(s[2 * q], s[2 * q + 1]);
-                            float r0, r1;
-                            f32x2_split(sub_f32x2(f32x2(s[2 * q], s[2 * q + 1]),
-                                                  f32x2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u))),
-                                        r0, r1);
-                            wl[qq] = pack_bf16_rn(r0, r1);
-                        }
-                        tmem_st16u(t_s + kKv / 2 + hc * (kHalfCols / 2) + h2 * (kHalfCols / 4), wl);
-                    }
-                    float l0, l1, l2, l3;
-                    f32x2_split(lp[0], l0, l1);
-                    f32x2_split(lp[1], l2, l3);
-                    l[x] += (l0 + l1) + (l2 + l3);
-                    tmem_wait_st();
-                    tc_fence_before();
-                    pa::mbar_arrive(&bars->plo_full[x]);
                 }
-            }
+            };
+            if (it.wide)
+                run_tiles(std::true_type{});
+            else
+                run_tiles(std::false_type{});
             for (int x = 0; x < 2 && ok; ++x) {
                 if (nt[x] == 0) continue;
                 const float l_all = l[x] + exchange(x, l[x], ok);
@@ -945,6 +1039,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// --- V staging -------------------------------------------------------------------
+
+struct StageArgs {
+    const int32_t* block_tables;
+    int max_blocks;
+    const int32_t* context_lens;
+    int num_seqs;
+    int block_size;
+    int n_kv_heads;
+    int num_blocks;
+    int l_slot;           // positions per (KV head, sequence)
+    int t_slot;
+    uint16_t* v_stage;    // [n_kv_heads][num_seqs][l_slot][D]
+    uint8_t* v_fmt;       // [n_kv_heads][num_seqs][t_slot]
+    int32_t* status;
+};
+
+// One thread block per (128-position tile, sequence, KV head): gathers the
+// tile's V rows through the block table into the staging buffer, where each
+// (KV head, sequence) owns l_slot consecutive rows, so the prefill kernel
+// loads a whole tile as one box per 64 columns.  Rows at and past the
+// context (anything there, NaN included, would meet weights of 0, and
+// 0 * NaN is not 0) become zeros.  The tile is stored as fp16 (exact for
+// every bf16 magnitude in [2^-14, 2^16), within 2^-25 below it) unless one
+// of its values has a magnitude of 2^16 or more or is not finite; then it
+// stays bf16, and its format byte says so.  Tiles at or past the context
+// are not read by the prefill kernel and are skipped.
+template <int D>
+__global__ void __launch_bounds__(256) stage_v_kernel(const uint4* __restrict__ v_cache, const StageArgs a) {
+    constexpr int kChunksPerRow = D / 8;                      // 16-byte chunks
+    constexpr int kPer = kKv * kChunksPerRow / 256;           // chunks per thread
+    const int j = blockIdx.x, s = blockIdx.y, h = blockIdx.z;
+    int ctx = a.context_lens[s];
+    ctx = min(max(ctx, 0), a.max_blocks * a.block_size);     // the prefill kernel flags and clamps the same
+    if (j * kKv >= ctx) return;
+    const int32_t* table = a.block_tables + (size_t)s * a.max_blocks;
+    uint4 v[kPer];
+    uint32_t amax = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int c = threadIdx.x + 256 * i;
+        const int pos = j * kKv + c / kChunksPerRow;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (pos < ctx) {
+            const int blk = __ldg(table + pos / a.block_size);
+            if (blk >= 0 && blk < a.num_blocks)
+                v[i] = __ldg(v_cache + (((size_t)blk * a.n_kv_heads + h) * a.block_size + pos % a.block_size) *
+                                           kChunksPerRow + c % kChunksPerRow);
+            // a bad entry reads zeros; the prefill kernel's K loads flag it
+        }
+        amax = max_u16x2(amax, max_u16x2(v[i].x & 0x7fff7fffu, v[i].y & 0x7fff7fffu));
+        amax = max_u16x2(amax, max_u16x2(v[i].z & 0x7fff7fffu, v[i].w & 0x7fff7fffu));
+    }
+    const bool wide = __syncthreads_or((amax & 0xffffu) >= kF16Wide || (amax >> 16) >= kF16Wide) != 0;
+    uint4* dst = reinterpret_cast<uint4*>(a.v_stage + ((size_t)(h * a.num_seqs + s) * a.l_slot + (size_t)j * kKv) * D);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+        dst[threadIdx.x + 256 * i] = wide ? v[i]
+                                          : make_uint4(bf16x2_to_f16x2(v[i].x), bf16x2_to_f16x2(v[i].y),
+                                                       bf16x2_to_f16x2(v[i].z), bf16x2_to_f16x2(v[i].w));
+    if (threadIdx.x == 0) a.v_fmt[(size_t)(h * a.num_seqs + s) * a.t_slot + j] = wide ? 1 : 0;
+}
+
+// Layout of the caller's workspace: the V staging buffer, then the format
+// bytes (each part 256-byte aligned).
+struct Workspace {
+    int l_slot, t_slot;
+    size_t stage_bytes, fmt_off, total;
+};
+
+Workspace workspace_layout(int num_seqs, int max_blocks, int block_size, int n_kv_heads, int d_head) {
+    Workspace w;
+    const long long pos = (long long)max_blocks * block_size;
+    w.t_slot = (int)((pos + kKv - 1) / kKv);
+    w.l_slot = w.t_slot * kKv;
+    w.stage_bytes = (size_t)n_kv_heads * num_seqs * w.l_slot * d_head * 2;
+    w.fmt_off = (w.stage_bytes + 255) & ~(size_t)255;
+    w.total = w.fmt_off + (((size_t)n_kv_heads * num_seqs * w.t_slot + 255) & ~(size_t)255);
+    return w;
+}
+
 // --- host side -------------------------------------------------------------------
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -987,8 +1162,8 @@ int num_sms() {
 }
 
 template <int D>
-int launch(const PrefillArgs& a, const void* q, const void* k_cache, const void* v_cache, int num_tokens,
-           long long cache_rows, dim3 grid, cudaStream_t st) {
+int launch(const PrefillArgs& a, const StageArgs& sa, const void* q, const void* k_cache, const void* v_cache,
+           int num_tokens, long long cache_rows, dim3 grid, cudaStream_t st) {
     CUtensorMap mq, mk, mv;
     const cuuint64_t qdims[3] = {(cuuint64_t)D, (cuuint64_t)a.n_q_heads, (cuuint64_t)num_tokens};
     const cuuint64_t qstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.n_q_heads * D * 2};
@@ -996,11 +1171,16 @@ int launch(const PrefillArgs& a, const void* q, const void* k_cache, const void*
     const cuuint64_t cdims[2] = {(cuuint64_t)D, (cuuint64_t)cache_rows};
     const cuuint64_t cstr[1] = {(cuuint64_t)D * 2};
     const cuuint32_t cbox[2] = {64u, (cuuint32_t)a.block_size};
+    const cuuint64_t vdims[2] = {(cuuint64_t)D, (cuuint64_t)a.n_kv_heads * a.num_seqs * a.l_slot};
+    const cuuint32_t vbox[2] = {64u, (cuuint32_t)kKv};
     if (!encode(&mq, q, 3, qdims, qstr, qbox) || !encode(&mk, k_cache, 2, cdims, cstr, cbox) ||
-        !encode(&mv, v_cache, 2, cdims, cstr, cbox))
+        !encode(&mv, sa.v_stage, 2, vdims, cstr, vbox))
         return PA_ERR_CUDA;
     if (pa_host::ensure_smem_attr(prefill_kernel<D>, PGeo<D>::kSmem, g_smem_done<D>) != cudaSuccess)
         return PA_ERR_CUDA;
+    stage_v_kernel<D><<<dim3((unsigned)sa.t_slot, (unsigned)sa.num_seqs, (unsigned)sa.n_kv_heads), 256, 0, st>>>(
+        static_cast<const uint4*>(v_cache), sa);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
     prefill_kernel<D><<<grid, kThreads, PGeo<D>::kSmem, st>>>(mq, mk, mv, a);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -1009,11 +1189,17 @@ int launch(const PrefillArgs& a, const void* q, const void* k_cache, const void*
 
 extern "C" {
 
+size_t pa_prefill_workspace_size(int num_seqs, int max_blocks_per_seq, int block_size, int n_kv_heads,
+                                 int d_head) {
+    if (num_seqs <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || n_kv_heads <= 0 || d_head <= 0) return 0;
+    return workspace_layout(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head).total;
+}
+
 int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
                const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start,
                const int32_t* context_lens, int num_seqs, int num_tokens, int max_query_len, int num_blocks,
-               int block_size, float scale, int n_q_heads, int n_kv_heads, int d_head, int32_t* sched_dev,
-               int32_t* status_dev, void* stream) {
+               int block_size, float scale, int n_q_heads, int n_kv_heads, int d_head, void* workspace,
+               size_t workspace_bytes, int32_t* sched_dev, int32_t* status_dev, void* stream) {
     if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_blocks <= 0 || max_blocks_per_seq < 0 ||
         n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
         return PA_ERR_INVALID_ARG;
@@ -1024,8 +1210,14 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !query_start || !context_lens)
         return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq == 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    const Workspace ws = workspace_layout(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head);
+    if ((long long)n_kv_heads * num_seqs * ws.l_slot > INT_MAX - kKv) return PA_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < ws.total) return PA_ERR_WORKSPACE;
     if (!pa_host::aligned16(out) || !pa_host::aligned16(q) || !pa_host::aligned16(k_cache) ||
-        !pa_host::aligned16(v_cache) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        !pa_host::aligned16(v_cache) || !pa_host::aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
         (reinterpret_cast<uintptr_t>(query_start) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
         (reinterpret_cast<uintptr_t>(sched_dev) & 3u))
         return PA_ERR_MISALIGNED;
@@ -1056,6 +1248,9 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     a.num_blocks = num_blocks;
     a.oob_row = (int)cache_rows;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.v_fmt = static_cast<const uint8_t*>(workspace) + ws.fmt_off;
+    a.l_slot = ws.l_slot;
+    a.t_slot = ws.t_slot;
     a.status = status_dev;
     a.sched = reinterpret_cast<int*>(sched_dev);
     const long long items = tiles * num_seqs * n_kv_heads;
@@ -1065,9 +1260,22 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     const long long per_head = tiles * num_seqs;
     long long hpg = (2LL * grid.x + per_head - 1) / per_head;
     a.heads_per_group = (int)(hpg < 1 ? 1 : hpg > n_kv_heads ? n_kv_heads : hpg);
+    StageArgs sa;
+    sa.block_tables = block_tables;
+    sa.max_blocks = max_blocks_per_seq;
+    sa.context_lens = context_lens;
+    sa.num_seqs = num_seqs;
+    sa.block_size = block_size;
+    sa.n_kv_heads = n_kv_heads;
+    sa.num_blocks = num_blocks;
+    sa.l_slot = ws.l_slot;
+    sa.t_slot = ws.t_slot;
+    sa.v_stage = static_cast<uint16_t*>(workspace);
+    sa.v_fmt = static_cast<uint8_t*>(workspace) + ws.fmt_off;
+    sa.status = status_dev;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return d_head == 128 ? launch<128>(a, q, k_cache, v_cache, num_tokens, cache_rows, grid, st)
-                         : launch<64>(a, q, k_cache, v_cache, num_tokens, cache_rows, grid, st);
+    return d_head == 128 ? launch<128>(a, sa, q, k_cache, v_cache, num_tokens, cache_rows, grid, st)
+                         : launch<64>(a, sa, q, k_cache, v_cache, num_tokens, cache_rows, grid, st);
 }
 
 }  // extern "C"

@@ -6,7 +6,7 @@ import torch
 # Attention tolerance (fp32 accumulation over bf16 inputs): an element passes
 # when |gpu - oracle| <= ATOL + RTOL * |oracle|.  With an fp32 output the
 # maximum absolute error must also stay within ATOL.  A bf16 output adds its
-# own rounding (up to 2^-9 relative), which the RTOL term covers.
+# own rounding (up to 2^-8 relative), which the RTOL term covers.
 ATOL = 2e-3
 RTOL = 1e-2
 

@@ -29,6 +29,19 @@ def test_fixed_partition_workspace_size():
     assert n >= parts * 4 * 2 + parts * 128 * 4 and n % 256 == 0
 
 
+def test_prefill_workspace_size():
+    """V staging (KV heads x sequences x positions rounded up to 128 x d_head
+    x 2 bytes) plus one format byte per 128 positions, each part rounded up
+    to 256 bytes."""
+    # 16 prompts of 126 blocks of 16 (2,016 positions -> 2,048), 8 KV heads, d 128
+    stage = 8 * 16 * 2048 * 128 * 2
+    assert api.pa_prefill_workspace_size(16, 126, 16, 8, 128) == stage + 256 * -(-(8 * 16 * 16) // 256)
+    # 300 positions -> 384 (3 tiles): 2 x 3 x 384 x 64 x 2 = 294,912 bytes, 18 format bytes -> 256
+    assert api.pa_prefill_workspace_size(3, 10, 30, 2, 64) == 294912 + 256
+    assert api.pa_prefill_workspace_size(0, 10, 16, 2, 64) == 0
+    assert api.pa_prefill_workspace_size(3, 10, 16, 2, -1) == 0
+
+
 STATUS_MAP = {AL.OK: api.PA_OK, AL.FAIL_NO_BLOCKS: api.PA_FAIL_NO_BLOCKS, AL.ERR_INVALID_ARG: api.PA_ERR_INVALID_ARG,
               AL.ERR_UNKNOWN_SEQ: api.PA_ERR_UNKNOWN_SEQ, AL.ERR_DUPLICATE_SEQ: api.PA_ERR_DUPLICATE_SEQ}
 

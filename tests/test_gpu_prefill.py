@@ -165,7 +165,8 @@ def test_prefill_weights_finer_than_bf16():
     The values of c are the bf16 numbers in [-4, 0) whose e^c lies farthest
     from a bf16 number (checked below: weights rounded to bf16 would move
     these outputs by up to ~7e-3, past the 2e-3 bound).  The kernel carries
-    each weight as two bf16 terms, so the fp32 outputs stay within 2e-3."""
+    each weight in fp16 (a relative 2^-11, moving these outputs by at most
+    ~5e-4), so the fp32 outputs stay within 2e-3."""
     S, Hq, Hkv, D, B = 64, 1, 1, 64, 16
     cand = torch.arange(-4.0, 0.0, 2.0 ** -9, dtype=torch.float64).to(torch.bfloat16).unique()
     cand = cand[cand < 0].double()
@@ -193,6 +194,60 @@ def test_prefill_weights_finer_than_bf16():
     got, status = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, torch.float32)
     assert status == 0
     assert_attention_close(out_to_f64(got), want, True, "weights finer than bf16")
+
+
+def _set_v(vb, tab, B, s, pos, cols, val):
+    """V of sequence s, position pos, columns cols, every KV head, to val (bf16)."""
+    blk, off = tab[s, pos // B], pos % B
+    vb[blk, :, off, cols] = to_bits(torch.tensor(float(val)).to(torch.bfloat16).reshape(1))[0]
+
+
+def test_prefill_values_beyond_fp16_range():
+    """The value products run in fp16 where V allows it: a 128-position V
+    tile whose values are all of magnitude below 2^16 (and finite) goes as
+    fp16, exactly for magnitudes down to 2^-14; a tile holding 2^16 or more
+    stays bf16 and its weights go as bf16 hi + lo terms.  Here tiles of
+    both kinds alternate in the same rows: spikes of +-2^17 in columns 0
+    and 1 at one position of the odd tiles (and of each sequence's last,
+    ragged tile, whose rows past the context hold NaN), and +-65280 (the
+    largest bf16 below 2^16) and 2^-20 in columns 2 to 4 of the even
+    tiles.  Columns 5 and up hold ordinary values and meet the fp32 bound;
+    the large columns meet the element rule (2e-3 + 1e-2 relative)."""
+    Hq, Hkv, D, B = 16, 4, 128, 16
+    ctxs, news = [700, 300, 129], [700, 172, 129]
+    qb, kb, vb, tab, qs, ctx = _problem(21, Hq, Hkv, D, B, ctxs, news)
+    for s_, c in enumerate(ctxs):
+        last = (c - 1) // 128
+        for t in range(last + 1):
+            pos = min(128 * t + 5 + 11 * s_, c - 1)
+            if t % 2 == 1 or t == last:
+                _set_v(vb, tab, B, s_, pos, 0, 2.0 ** 17)
+                _set_v(vb, tab, B, s_, pos, 1, -3.0 * 2.0 ** 16)
+            else:
+                _set_v(vb, tab, B, s_, pos, 2, 65280.0)
+                _set_v(vb, tab, B, s_, pos + 1, 3, -65280.0)
+                _set_v(vb, tab, B, s_, pos, 4, 2.0 ** -20)
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B)
+    got, status = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, torch.float32)
+    assert status == 0
+    g = out_to_f64(got)
+    assert_attention_close(g[:, :, 5:], want[:, :, 5:], True, "ordinary columns")
+    assert_attention_close(g[:, :, :5], want[:, :, :5], False, "large columns")
+
+
+def test_prefill_all_values_beyond_fp16_range():
+    """Every V value scaled by 2^17 (so every tile stays bf16, with bf16
+    hi + lo weights): attention is linear in V and the scaling is exact, so
+    the output over 2^17 must meet the fp32 bound against the oracle on the
+    unscaled values."""
+    Hq, Hkv, D, B = 8, 2, 64, 16
+    ctxs, news = [400, 260], [400, 100]
+    qb, kb, vb, tab, qs, ctx = _problem(22, Hq, Hkv, D, B, ctxs, news)
+    want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B)
+    vs = (from_bits(vb, "cpu").float() * 2.0 ** 17).to(torch.bfloat16)       # exact; NaN junk stays NaN
+    got, status = _run(qb, kb, to_bits(vs), tab, qs, ctx, B, Hq, Hkv, D, torch.float32)
+    assert status == 0
+    assert_attention_close(out_to_f64(got) / 2.0 ** 17, want, True, "V x 2^17")
 
 
 @pytest.mark.parametrize("Hq,Hkv,D", [(128, 2, 64), (128, 1, 128), (64, 1, 64)], ids=["g64_d64", "g128_d128", "g64_one_kv"])
@@ -241,6 +296,37 @@ def test_prefill_host_errors():
         q_mis = flat[1:1 + q.numel()].view(q.shape)
         api.pa_prefill(out, q_mis, k, v, dev(tab), dev(qs), dev(ctx), 20, 16, 0.125, 8, 2, 64)
     assert e.value.status == api.PA_ERR_MISALIGNED
+    need = api.pa_prefill_workspace_size(1, tab.shape[1], 16, 2, 64)
+    small = torch.empty(need - 1, dtype=torch.uint8, device="cuda")
+    with pytest.raises(api.PAError) as e:         # workspace too small
+        api.pa_prefill(out, q, k, v, dev(tab), dev(qs), dev(ctx), 20, 16, 0.125, 8, 2, 64, workspace=small)
+    assert e.value.status == api.PA_ERR_WORKSPACE
+    assert (out == -1.0).all()
+
+
+def test_prefill_workspace_reused_across_calls():
+    """One caller workspace for calls of different shapes in a row (each call
+    restages V over whatever the last one left): every result equals the
+    call with a fresh workspace, bit for bit, and the oracle."""
+    D, B = 64, 16
+    problems = [(31, 8, 2, [300, 90], [300, 40]), (32, 16, 4, [129, 700, 5], [129, 260, 5]),
+                (33, 8, 2, [1000], [17])]
+    ws = torch.empty(max(api.pa_prefill_workspace_size(len(c), -(-max(c) // B) + 2, B, hkv, D)
+                         for _, _, hkv, c, _ in problems), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xFF)                                   # junk format bytes and values
+    for seed, Hq, Hkv, ctxs, news in problems:
+        qb, kb, vb, tab, qs, ctx = _problem(seed, Hq, Hkv, D, B, ctxs, news)
+        fresh, st0 = _run(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, torch.float32)
+        dev = lambda a: torch.from_numpy(a).cuda()
+        out = torch.full((qb.shape[0], Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        api.pa_prefill(out, from_bits(qb), from_bits(kb), from_bits(vb), dev(tab), dev(qs), dev(ctx), max(news), B,
+                       1.0 / math.sqrt(D), Hq, Hkv, D, status=status, workspace=ws)
+        torch.cuda.synchronize()
+        assert st0 == 0 and int(status.item()) == 0
+        assert torch.equal(out.view(torch.int32), fresh.view(torch.int32)), "seed %d" % seed
+        want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B)
+        assert_attention_close(out_to_f64(out), want, True, "reused workspace")
 
 
 def test_prefill_work_claiming_orders_agree():
