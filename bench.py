@@ -1082,14 +1082,6 @@ def _oracle_sample(sc, seqs):
     return rep, tab, lens, q
 
 
-def host_threads():
-    """Host cores this process may run on."""
-    try:
-        return len(os.sched_getaffinity(0))
-    except AttributeError:
-        return os.cpu_count() or 1
-
-
 def _oracle_time(sc, rep, tab, lens, q):
     from oracle import attention as A
     t0 = time.perf_counter()

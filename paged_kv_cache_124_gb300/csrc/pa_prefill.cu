@@ -11,8 +11,15 @@
 // (chunked prefill), or the suffix after a prefix-cache hit are all this
 // same call.
 //
-// Design (a persistent CTA per SM; a work item is two tiles of 128 query
-// rows of one KV head):
+// Design (a staging pass, then a persistent CTA per SM; a work item is two
+// tiles of 128 query rows of one KV head):
+//   * stage_v_kernel gathers V through the block table into the caller's
+//     workspace, each (KV head, sequence) owning consecutive rows, so that a
+//     128-position V tile is contiguous.  It stores a tile as fp16, which
+//     holds every bf16 magnitude in [2^-14, 2^16) exactly and is off by at
+//     most 2^-25 below that range, with the rows past the context zeroed; a
+//     tile holding a magnitude of 2^16 or more (or a non-finite value)
+//     stays bf16, and a format byte per tile says which.
 //   * Rows are (token, grouped query head) pairs: 128 / G consecutive new
 //     tokens times the G query heads that share KV head h, so every K/V tile
 //     is read once for all G heads (GQA).  Each Q tile is one 3-D TMA box;
@@ -24,28 +31,28 @@
 //     shared memory for the other warps.  Barrier phases run on across
 //     items, so the next item's loads and first products overlap the
 //     current item's last products and output.
-//   * K/V tiles of 128 positions are gathered through the block table with
+//   * K tiles of 128 positions are gathered through the block table with
 //     one 2-D TMA box (64 columns x B rows, 128-byte swizzle) per block and
 //     64-column half; a warp issues its boxes one lane after another, so K
 //     and V have a producer warp each, and table entries are fetched four
 //     tiles ahead.  Blocks past the needed range, and bad table entries, are
-//     loaded from outside the tensor, which fills zeros and reads no HBM.
+//     loaded from outside the tensor, which fills zeros and reads no HBM.  A
+//     staged V tile is one box of 128 rows per 64 columns.
 //   * S = Q K^T (M 128, N 128, K d) and O += P V (M 128, N d, K 128) are
 //     tcgen05.mma kind::f16 (fp32 accumulate), one issuing thread per Q
 //     tile (two issuers hide most of the pipe drain between groups of
 //     products of different kinds).  Tensor memory holds S_A, S_B (128
 //     columns each) and O_A, O_B (d columns each).  S takes bf16 Q and K.
 //     P V takes fp16 weights (written over the first 64 columns of their
-//     own S and read from there as the A operand) and fp16 values: the V
-//     warp turns each landed V tile into fp16 in place, which is exact for
-//     every bf16 magnitude in [2^-14, 2^16) and off by at most 2^-25 below
-//     it, and fp16 carries each weight to a relative 2^-11 where bf16 would
-//     give 2^-8.  A V tile holding a magnitude of 2^16 or more (or a
-//     non-finite value) is copied again and stays bf16; for it each weight
-//     is split into two bf16 terms, hi = bf16(p) and lo = bf16(p - hi),
-//     written over the first and the second 64 columns of S (O += P_hi V +
-//     P_lo V, a relative 2^-16).  V is an MN-major operand read straight
-//     from the TMA layout.
+//     own S and read from there as the A operand) and the staged fp16
+//     values: fp16 carries each weight to a relative 2^-11 where bf16 would
+//     give 2^-8.  For a V tile that stayed bf16 each weight is split into
+//     two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), written over the
+//     first and the second 64 columns of S (O += P_hi V + P_lo V, a relative
+//     2^-16).  An item learns once whether any of its V tiles stayed bf16,
+//     and the softmax and MMA warps run one of two compiled forms of their
+//     tile loop (the fp16-only form checks no formats).  V is an MN-major
+//     operand read straight from the TMA layout.
 //   * Eight softmax warps work on tile A, then on tile B, then on tile A of
 //     the next K/V tile, ...: warps w and w + 4 share the 32 rows of lane
 //     quarter w (tensor-memory lane = row), each taking 64 of the 128
@@ -53,10 +60,11 @@
 //     end, their sums) through shared memory.  Per row: mask, online maximum
 //     in the log2 domain, exp2, running sum, P; the scale-and-subtract and
 //     the running sums use packed f32x2 arithmetic (one instruction for two
-//     columns), which the softmax's instruction issue is bound by.  O is rescaled in tensor
-//     memory only when a row's maximum grows by more than 2^8 (the weights
-//     stay below 256 otherwise), which is rare after the first tiles.  At
-//     the end of an item each thread writes its half row with 32-byte stores.
+//     columns), which the softmax's instruction issue is bound by.  O is
+//     rescaled in tensor memory only when a row's maximum grows by more than
+//     2^8 (the weights, which carry a factor 2^7, stay below 2^15 otherwise),
+//     which is rare after the first tiles.  At the end of an item each
+//     thread writes its half row with 32-byte stores.
 //   * Every wait is bounded; on a timeout the CTA flags PA_DEV_WAIT_TIMEOUT,
 //     waits (bounded) for its own copies and products in flight, frees its
 //     tensor memory and returns.
@@ -351,9 +359,10 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
-// The largest bf16 magnitude pattern (sign cleared) that fp16 still holds:
-// 0x4780 is 2^16, the first bf16 magnitude that fp16 rounds to infinity;
-// patterns at or above it also cover infinities and NaNs.
+// The smallest bf16 magnitude pattern (sign cleared) that fp16 cannot
+// hold: 0x4780 is 2^16, which fp16 rounds to infinity (the bf16 value below
+// it, 65280, is exact in fp16); patterns above it also cover infinities and
+// NaNs.
 constexpr uint32_t kF16Wide = 0x4780u;
 
 // The weights of one thread's kHalfCols scores s (in place: s becomes the
