@@ -536,6 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // Launched as a programmatic dependent of the V staging: everything above
+    // (barriers, tensor memory) overlaps its end; every input is read below.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == kProducerWarp || warp == kVProducerWarp) {
         // ------------------------------------------------------------ TMA producers
@@ -1074,11 +1077,16 @@ struct StageArgs {
 // every bf16 magnitude in [2^-14, 2^16), within 2^-25 below it) unless one
 // of its values has a magnitude of 2^16 or more or is not finite; then it
 // stays bf16, and its format byte says so.  Tiles at or past the context
-// are not read by the prefill kernel and are skipped.
+// are not read by the prefill kernel and are skipped.  Launched as a
+// programmatic dependent: it waits for the work before it on the stream (the
+// cache write, or an earlier call still reading this workspace) before it
+// reads or writes anything, then lets the prefill kernel begin its launch.
 template <int D>
 __global__ void __launch_bounds__(256) stage_v_kernel(const uint4* __restrict__ v_cache, const StageArgs a) {
     constexpr int kChunksPerRow = D / 8;                      // 16-byte chunks
     constexpr int kPer = kKv * kChunksPerRow / 256;           // chunks per thread
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int j = blockIdx.x, s = blockIdx.y, h = blockIdx.z;
     int ctx = a.context_lens[s];
     ctx = min(max(ctx, 0), a.max_blocks * a.block_size);     // the prefill kernel flags and clamps the same
@@ -1187,11 +1195,14 @@ int launch(const PrefillArgs& a, const StageArgs& sa, const void* q, const void*
         return PA_ERR_CUDA;
     if (pa_host::ensure_smem_attr(prefill_kernel<D>, PGeo<D>::kSmem, g_smem_done<D>) != cudaSuccess)
         return PA_ERR_CUDA;
-    stage_v_kernel<D><<<dim3((unsigned)sa.t_slot, (unsigned)sa.num_seqs, (unsigned)sa.n_kv_heads), 256, 0, st>>>(
-        static_cast<const uint4*>(v_cache), sa);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    prefill_kernel<D><<<grid, kThreads, PGeo<D>::kSmem, st>>>(mq, mk, mv, a);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    if (pa_host::launch_dependent(stage_v_kernel<D>, dim3((unsigned)sa.t_slot, (unsigned)sa.num_seqs,
+                                                          (unsigned)sa.n_kv_heads),
+                                  dim3(256), 0, st, static_cast<const uint4*>(v_cache), sa) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return pa_host::launch_dependent(prefill_kernel<D>, grid, dim3(kThreads), PGeo<D>::kSmem, st, mq, mk, mv, a) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 }  // namespace
