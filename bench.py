@@ -517,18 +517,43 @@ def run_prefill_ours(args, world, rank, local):
     flops = prefill_flops(sc.ctxs, sc.news, sc.n_q_heads, sc.d_head)
     T = int(sum(sc.news))
 
-    # the call's workspace (V staged as fp16) is allocated once, outside the timed region
-    workspace = api.prefill_workspace(len(sc.news), tables_h.shape[1], sc.block_size, sc.n_kv_heads, sc.d_head, dev)
+    fp8 = args.kv_dtype == "fp8"
+    ks = vs = 1.0
+    if fp8:
+        # the same caches as E4M3 codes, scales from the data's range (setup, not timed); the step's new
+        # rows are then quantised by pa_reshape_and_cache_fp8
+        ks = float(kc.float().nan_to_num(0.0).abs().amax()) / 448.0
+        vs = float(vc.float().nan_to_num(0.0).abs().amax()) / 448.0
+        kc = (kc.float() / ks).to(torch.float8_e4m3fn).view(torch.uint8)
+        vc = (vc.float() / vs).to(torch.float8_e4m3fn).view(torch.uint8)
+    # the call's workspace (V, and for FP8 also K, staged) is
+    # allocated once, outside the timed region
+    if fp8:
+        workspace = api.prefill_fp8_workspace(len(sc.news), tables_h.shape[1], sc.block_size, sc.n_kv_heads,
+                                              sc.d_head, dev)
+    else:
+        workspace = api.prefill_workspace(len(sc.news), tables_h.shape[1], sc.block_size, sc.n_kv_heads, sc.d_head,
+                                          dev)
+
+    def cache_write(k_, v_, slots_, st):
+        if fp8:
+            api.pa_reshape_and_cache_fp8(kc, vc, k_, v_, slots_, ks, vs, stream=st)
+        else:
+            api.pa_reshape_and_cache(kc, vc, k_, v_, slots_, stream=st)
 
     def attention(q_, tables_, qs_, ctx_, st):
-        api.pa_prefill(out, q_, kc, vc, tables_, qs_, ctx_, max_q, sc.block_size, sc.scale, sc.n_q_heads,
-                       sc.n_kv_heads, sc.d_head, stream=st, workspace=workspace)
+        if fp8:
+            api.pa_prefill_fp8(out, q_, kc, vc, tables_, qs_, ctx_, max_q, sc.block_size, sc.scale, ks, vs,
+                               sc.n_q_heads, sc.n_kv_heads, sc.d_head, stream=st, workspace=workspace)
+        else:
+            api.pa_prefill(out, q_, kc, vc, tables_, qs_, ctx_, max_q, sc.block_size, sc.scale, sc.n_q_heads,
+                           sc.n_kv_heads, sc.d_head, stream=st, workspace=workspace)
 
     clocks = ClockSampler(local) if rank == 0 else None
     if clocks:
         clocks.start()
     for _ in range(args.warmup):
-        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
+        cache_write(k_new, v_new, slots, stream)
         attention(q, tables, qs, ctx, stream)
     K = args.steps
     SAMPLE = 4
@@ -540,7 +565,7 @@ def run_prefill_ours(args, world, rank, local):
     torch.cuda.nvtx.range_push(TIMED_RANGE)
     ev_start.record(stream)
     for i in range(K):
-        api.pa_reshape_and_cache(kc, vc, k_new, v_new, slots, stream=stream)
+        cache_write(k_new, v_new, slots, stream)
         if i % SAMPLE == 0:
             a, b = ev_att[i // SAMPLE]
             a.record(stream)
@@ -595,7 +620,7 @@ def run_prefill_ours(args, world, rank, local):
     def e2e_step():
         for dst, src in pairs:
             dst.copy_(src, non_blocking=True)
-        api.pa_reshape_and_cache(kc, vc, k_d, v_d, slots_d, stream=stream)
+        cache_write(k_d, v_d, slots_d, stream)
         attention(q_d, tables_d, qs_d, ctx_d, stream)
         out_h.copy_(out, non_blocking=True)
         stream.synchronize()
@@ -616,11 +641,12 @@ def run_prefill_ours(args, world, rank, local):
     peak, peak_kind = measured_peak("bf16_tflops", 1900.0)
     peak_sus, _ = measured_peak("bf16_tflops_sustained", 1700.0)
     achieved = flops / att_s / 1e12
-    kv_bytes = sum(sc.ctxs) * sc.n_kv_heads * sc.d_head * 2 * 2
+    kv_bytes = sum(sc.ctxs) * sc.n_kv_heads * sc.d_head * 2 * (1 if fp8 else 2)
     line = {
         "metric": PREFILL_METRIC, "value": round(total_flops / total_s / 1e12, 2), "unit": "TFLOP/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(total_s / K * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "kv_dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "kv_dtype": "fp8_e4m3" if fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": sc.name, "num_seqs": len(sc.ctxs), "new_tokens": T, "context_lens":
                    "all %d" % sc.ctxs[0] if len(set(sc.ctxs)) == 1 else "prefix U[2048, 8192] + 512",
@@ -631,11 +657,12 @@ def run_prefill_ours(args, world, rank, local):
                          (kv_bytes / 1e6, 2 * q.numel() * 2 / 1e6),
                    "parallelism": "replicas (one batch per GPU)" if world > 1 else "single GPU"},
         "tokens_per_s": round(total_tokens / total_s, 1),
-        "roofline": {"bound": "tensor", "kernel": "pa_prefill (stage_v_kernel<128> + prefill_kernel<128>)", "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": "pa_prefill_fp8 (stage_kv_f8_kernel + prefill_kernel<128, fp8>)" if fp8
+                     else "pa_prefill (stage_v_kernel<128> + prefill_kernel<128>)", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind + " bf16 burst", "peak_sustained": peak_sus,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(PREFILL_PROFILE, PREFILL_SOURCE) if sc.name == "prefill_prompts_8b"
-                     else None,
+                     "traffic": profiled_traffic(PREFILL_PROFILE, PREFILL_SOURCE)
+                     if sc.name == "prefill_prompts_8b" and not fp8 else None,
                      "algorithmic_flops_per_launch": flops, "avg_launch_us": round(att_s * 1e6, 2),
                      "launch_us_p10_p90": [round(att_p10 * 1e6, 2), round(att_p90 * 1e6, 2)],
                      "timing": "median over %d repetitions of %d pa_prefill calls back to back between two events "
@@ -646,7 +673,8 @@ def run_prefill_ours(args, world, rank, local):
                      "step_frac": round(total_flops / total_s / 1e12 / peak, 4)},
         "e2e": {"value": round(e2e_flops / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_s / K * 1e3, 4)},
-        "gpu_launches": 3 * K,       # reshape_and_cache, stage_v_kernel, prefill_kernel
+        # reshape_and_cache, the staging (V; FP8: K and V), prefill_kernel
+        "gpu_launches": 3 * K,
         "clocks": clk,
     }
     if not args.no_cpu_baseline:

@@ -355,6 +355,33 @@ int pa_prefill(void* out, int out_dtype, const void* q,
 size_t pa_prefill_workspace_size(int num_seqs, int max_blocks_per_seq,
                                  int block_size, int n_kv_heads, int d_head);
 
+/* pa_prefill over FP8 caches (E4M3 codes written by pa_reshape_and_cache_fp8,
+ * element = E4M3(code) * k_scale or v_scale, the layout of pa_decode_fp8).
+ * The result is the causal attention over those dequantised keys and values,
+ * computed as pa_prefill computes it: the codes are staged in the workspace,
+ * K as bf16 (the score products take q as given) and V as fp16 (the value
+ * products take fp16 weights), both of which hold every E4M3 value exactly;
+ * k_scale joins the score scale and v_scale the output's.  Arguments as
+ * pa_prefill plus the two scales (finite, > 0); d_head must be 128
+ * (PA_ERR_UNSUPPORTED otherwise); workspace of at least
+ * pa_prefill_fp8_workspace_size(...) bytes (the V staging and its format
+ * bytes, then the K staging).  A table entry outside the pool reads zeros and
+ * is flagged PA_DEV_BAD_BLOCK_ID. */
+int pa_prefill_fp8(void* out, int out_dtype, const void* q,
+                   const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, int max_blocks_per_seq,
+                   const int32_t* query_start, const int32_t* context_lens,
+                   int num_seqs, int num_tokens, int max_query_len,
+                   int num_blocks, int block_size, float scale, float k_scale,
+                   float v_scale, int n_q_heads, int n_kv_heads, int d_head,
+                   void* workspace, size_t workspace_bytes, int32_t* sched_dev,
+                   int32_t* status_dev, void* stream);
+
+/* Bytes of workspace pa_prefill_fp8 needs (0 for a non-positive argument). */
+size_t pa_prefill_fp8_workspace_size(int num_seqs, int max_blocks_per_seq,
+                                     int block_size, int n_kv_heads,
+                                     int d_head);
+
 /* ===========================================================================
  * Cache writes
  * ===========================================================================

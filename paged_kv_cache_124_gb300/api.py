@@ -80,6 +80,10 @@ _SIGS = {
     "pa_prefill": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                             _c_int, _c_float, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp, _vp]),
     "pa_prefill_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "pa_prefill_fp8": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                _c_int, _c_float, _c_float, _c_float, _c_int, _c_int, _c_int, _vp, _c_size, _vp, _vp,
+                                _vp]),
+    "pa_prefill_fp8_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "pa_check_bounded_wait": (_c_int, [_c_int, _vp, _vp]),
     "pa_lse_merge": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp]),
     "pa_reshape_and_cache": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
@@ -341,6 +345,55 @@ def pa_prefill(out, q, k_cache, v_cache, block_tables, query_start, context_lens
                          _opt_dev(status, torch.int32, "status"),
                          _stream(stream))
     return _check(st, "pa_prefill")
+
+
+def pa_prefill_fp8_workspace_size(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head):
+    return int(_lib.pa_prefill_fp8_workspace_size(int(num_seqs), int(max_blocks_per_seq), int(block_size),
+                                                  int(n_kv_heads), int(d_head)))
+
+
+def prefill_fp8_workspace(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head, device=None):
+    """A caller-owned workspace tensor (uint8) of the size pa_prefill_fp8 needs."""
+    n = pa_prefill_fp8_workspace_size(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def pa_prefill_fp8(out, q, k_cache, v_cache, block_tables, query_start, context_lens, max_query_len, block_size,
+                   scale, k_scale, v_scale, n_q_heads, n_kv_heads, d_head, status=None, stream=None, counters=None,
+                   workspace=None):
+    """pa_prefill over E4M3 caches (uint8 [num_blocks, Hkv, B, D]) with per-cache scales; see pa.h."""
+    if out.dtype == torch.bfloat16:
+        out_dtype = PA_DTYPE_BF16
+    elif out.dtype == torch.float32:
+        out_dtype = PA_DTYPE_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    num_tokens = q.shape[0]
+    if tuple(q.shape) != (num_tokens, n_q_heads, d_head) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("q/out must be [num_tokens, n_q_heads, d_head]")
+    if k_cache.dim() != 4 or tuple(k_cache.shape[1:]) != (n_kv_heads, block_size, d_head) or \
+            k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache/v_cache must be [num_blocks, n_kv_heads, block_size, d_head]")
+    if counters is None:
+        counters = prefill_counters(q.device, stream)
+    if counters is not False and counters.numel() < 2:
+        raise ValueError("counters must hold 2 int32")
+    num_seqs = block_tables.shape[0]
+    if block_tables.dim() != 2 or context_lens.shape != (num_seqs,) or query_start.shape != (num_seqs + 1,):
+        raise ValueError("block_tables [S, max_blocks], query_start [S + 1], context_lens [S]")
+    if workspace is None:
+        workspace = prefill_fp8_workspace(num_seqs, block_tables.shape[1], block_size, n_kv_heads, d_head, q.device)
+    st = _lib.pa_prefill_fp8(_opt_dev(out, out.dtype, "out"), out_dtype, _dev(q, torch.bfloat16, "q"),
+                             _dev(k_cache, torch.uint8, "k_cache"), _dev(v_cache, torch.uint8, "v_cache"),
+                             _dev(block_tables, torch.int32, "block_tables"), int(block_tables.shape[1]),
+                             _dev(query_start, torch.int32, "query_start"),
+                             _dev(context_lens, torch.int32, "context_lens"), int(num_seqs), int(num_tokens),
+                             int(max_query_len), int(k_cache.shape[0]), int(block_size), float(scale), float(k_scale),
+                             float(v_scale), int(n_q_heads), int(n_kv_heads), int(d_head),
+                             _dev(workspace, torch.uint8, "workspace"), int(workspace.numel()),
+                             _opt_dev(None if counters is False else counters, torch.int32, "counters"),
+                             _opt_dev(status, torch.int32, "status"), _stream(stream))
+    return _check(st, "pa_prefill_fp8")
 
 
 def pa_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, k_scale, v_scale,

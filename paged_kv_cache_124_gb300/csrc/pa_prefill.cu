@@ -137,6 +137,8 @@ struct PrefillArgs {
     int oob_row;          // a row coordinate past the end of the cache view
     float scale_log2;     // scale * log2(e)
     const uint8_t* v_fmt; // per (KV head, sequence, 128-position tile) of the V staging: 0 fp16, 1 bf16
+    float k_scale;        // FP8: dequantisation scales of K and V
+    float v_scale;
     int l_slot;           // positions per (KV head, sequence) in the V staging, a multiple of 128
     int t_slot;           // l_slot / 128
     int32_t* status;
@@ -486,7 +488,9 @@ __device__ __forceinline__ Item read_item(const Item* src) {
 // ...; every barrier's phase runs on across items, so the next item's Q and
 // K/V copies and score products overlap the current item's last products and
 // output.
-template <int D>
+// kF8: the caches hold E4M3 codes; K comes staged as bf16 and V as fp16 (both
+// exact), the K scale joins the score scale and the V scale the output's.
+template <int D, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const PrefillArgs a) {
@@ -580,17 +584,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     post(it);
                     break;
                 }
-                // Do any of the item's V tiles stay bf16?  (The other warps
-                // then check tile by tile.)  The first 32 format bytes are
-                // loaded alongside the item's own loads.
-                int fseq, fh, ftile;
-                item_coords(i, a, fseq, fh, ftile);
-                const uint8_t* fmt = a.v_fmt + (size_t)(fh * a.num_seqs + fseq) * a.t_slot;
-                int w = lane < a.t_slot ? fmt[lane] : 0;
-                if (!decode_item(i, a, it, lane == 0)) continue;
-                w = lane < it.n_tiles ? w : 0;
-                for (int jj = lane + 32; jj < it.n_tiles; jj += 32) w |= fmt[jj];
-                it.wide = __any_sync(0xffffffffu, w != 0) ? 1 : 0;
+                if constexpr (kF8) {
+                    // E4M3 values are all exact in fp16: no tile stays bf16
+                    if (!decode_item(i, a, it, lane == 0)) continue;
+                    it.wide = 0;
+                } else {
+                    // Do any of the item's V tiles stay bf16?  (The other
+                    // warps then check tile by tile.)  The first 32 format
+                    // bytes are loaded alongside the item's own loads.
+                    int fseq, fh, ftile;
+                    item_coords(i, a, fseq, fh, ftile);
+                    const uint8_t* fmt = a.v_fmt + (size_t)(fh * a.num_seqs + fseq) * a.t_slot;
+                    int w = lane < a.t_slot ? fmt[lane] : 0;
+                    if (!decode_item(i, a, it, lane == 0)) continue;
+                    w = lane < it.n_tiles ? w : 0;
+                    for (int jj = lane + 32; jj < it.n_tiles; jj += 32) w |= fmt[jj];
+                    it.wide = __any_sync(0xffffffffu, w != 0) ? 1 : 0;
+                }
                 ok = post(it);
                 if (!ok) break;
                 // Q of this item replaces the previous item's once both tiles'
@@ -627,9 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int kAhead = 4;
             constexpr int kNoBlock = INT_MIN;             // past the needed range: nothing loaded
             const int vrow0 = (it.h * a.num_seqs + it.seq) * a.l_slot;
+            const bool gather = is_k && !kF8;              // FP8: K is staged like V
             auto fetch = [&](int j) {
                 const int pos = j * kKv + lane * a.block_size;
-                return (is_k && lane < bpt && pos < kv_all) ? __ldg(table + pos / a.block_size) : kNoBlock;
+                return (gather && lane < bpt && pos < kv_all) ? __ldg(table + pos / a.block_size) : kNoBlock;
             };
             auto to_row = [&](int blk) {
                 if (blk == kNoBlock) return a.oob_row;
@@ -653,11 +664,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = 0; u < kAhead; ++u) {
                     const int j = j0 + u;
                     if (j >= it.n_tiles) break;
-                    const int row = is_k ? to_row(blks[u]) : vrow0 + j * kKv;
+                    const int row = gather ? to_row(blks[u]) : vrow0 + j * kKv;
                     blks[u] = fetch(j + kAhead);
                     const int st = g % stages;
                     const uint32_t s_t =
-                        pa::smem_addr(sm + base + st * G::kKVBytes) + (is_k ? lane * a.block_size * 128 : 0);
+                        pa::smem_addr(sm + base + st * G::kKVBytes) + (gather ? lane * a.block_size * 128 : 0);
                     // both Q tiles' MMA warps release every K/V tile (used or not)
                     if (g >= stages)
                         ok = wait_warp(&empty0[st], (g / stages - 1) & 1, bars, a.status) &&
@@ -665,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     if (lane == 0) pa::mbar_arrive_expect_tx(&full[st], G::kKVBytes);
                     __syncwarp();
-                    if (is_k ? lane < bpt : lane == 0)
+                    if (gather ? lane < bpt : lane == 0)
 #pragma unroll
                         for (int hh = 0; hh < G::kHalves; ++hh)
                             tma_2d(s_t + hh * G::kHalfBytes, map, hh * 64, row, &full[st]);
@@ -812,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 };
-                if (it.wide)
+                if (!kF8 && it.wide)
                     run_tiles(std::true_type{});
                 else
                     run_tiles(std::false_type{});
@@ -829,7 +840,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = r / a.group, gq = r - t * a.group;
         const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
         float* red = reinterpret_cast<float*>(sm + G::kRed);
-        const float c2 = a.scale_log2;
+        // score scale (log2 domain; FP8: times the K scale)
+        const float c2s = kF8 ? a.scale_log2 * a.k_scale : a.scale_log2;
+        const float c2x[2] = {c2s, c2s};
         constexpr int kHalfCols = kKv / 2;                // score columns per thread
         constexpr int kOCols = D / 2;                     // output columns per thread
         int ns[2] = {0, 0}, nred[2] = {0, 0}, nod[2] = {0, 0};
@@ -900,6 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          fmaxf(max3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])));
                         mt = fmaxf(mt, exchange(x, mt, ok));
                         if (!ok) break;
+                        const float c2 = c2x[x];
                         const float mts = mt * c2;            // scale > 0: the maximum commutes with it
                         const bool rescale = mts > m_used[x] + kRescaleThreshold;
                         const float m_new = rescale ? mts : m_used[x];
@@ -971,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             };
-            if (it.wide)
+            if (!kF8 && it.wide)
                 run_tiles(std::true_type{});
             else
                 run_tiles(std::false_type{});
@@ -983,7 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 const int tok = it.t0 + x * a.tq + t;
-                const float inv = 1.f / l_all;
+                const float inv = (kF8 ? a.v_scale : 1.f) / l_all;
                 const size_t orow = ((size_t)(it.q0 + tok) * a.n_q_heads + (size_t)it.h * a.group + gq) * D + hc * kOCols;
                 const uint32_t t_o = t_lane + kTmemO0 + x * 128 + hc * kOCols;
                 float o[kOCols];
@@ -1119,21 +1133,92 @@ __global__ void __launch_bounds__(256) stage_v_kernel(const uint4* __restrict__ 
     if (threadIdx.x == 0) a.v_fmt[(size_t)(h * a.num_seqs + s) * a.t_slot + j] = wide ? 1 : 0;
 }
 
-// Layout of the caller's workspace: the V staging buffer, then the format
-// bytes (each part 256-byte aligned).
+// FP8 caches: one thread block per (128-position tile, sequence, KV head)
+// gathers the tile's K and V codes (E4M3, one byte each) through the block
+// table and stores K as bf16 (for the score products with the caller's bf16
+// q) and V as fp16 (for the value products with fp16 weights), in staging
+// buffers of the bf16 V staging's layout: both hold every E4M3 value
+// exactly.  Rows at and past the context are zeros, and a table entry
+// outside the pool reads zeros and is flagged.  The scales are applied by
+// the prefill kernel.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t c) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+    return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) stage_kv_f8_kernel(const uint4* __restrict__ k_cache,
+                                                          const uint4* __restrict__ v_cache, uint16_t* k_stage,
+                                                          const StageArgs a) {
+    constexpr int kChunksPerRow = D / 16;                     // 16 codes per 16-byte chunk
+    constexpr int kPer = kKv * kChunksPerRow / 256;           // chunks per thread
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int j = blockIdx.x, s = blockIdx.y, h = blockIdx.z;
+    int ctx = a.context_lens[s];
+    ctx = min(max(ctx, 0), a.max_blocks * a.block_size);
+    if (j * kKv >= ctx) return;
+    const int32_t* table = a.block_tables + (size_t)s * a.max_blocks;
+    const size_t row0 = ((size_t)(h * a.num_seqs + s) * a.l_slot + (size_t)j * kKv) * D;
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+        const uint4* src = kv ? v_cache : k_cache;
+        uint4* dst = reinterpret_cast<uint4*>((kv ? a.v_stage : k_stage) + row0);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int c = threadIdx.x + 256 * i;
+            const int pos = j * kKv + c / kChunksPerRow;
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (pos < ctx) {
+                const int blk = __ldg(table + pos / a.block_size);
+                if (blk >= 0 && blk < a.num_blocks)
+                    w = __ldg(src + (((size_t)blk * a.n_kv_heads + h) * a.block_size + pos % a.block_size) *
+                                        kChunksPerRow + c % kChunksPerRow);
+                else if (kv == 0)
+                    pa::set_status(a.status, PA_DEV_BAD_BLOCK_ID);
+            }
+            const uint32_t cw[4] = {w.x, w.y, w.z, w.w};
+            uint32_t f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = e4m3x2_to_f16x2((uint16_t)(cw[e] & 0xffffu));
+                f[2 * e + 1] = e4m3x2_to_f16x2((uint16_t)(cw[e] >> 16));
+            }
+            if (kv == 0) {
+                // K: fp16 -> fp32 -> bf16, exact at each step for E4M3 values
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const __half2 hv = *reinterpret_cast<const __half2*>(&f[e]);
+                    const float2 fv = __half22float2(hv);
+                    f[e] = pack_bf16_rn(fv.x, fv.y);
+                }
+            }
+            dst[2 * c] = make_uint4(f[0], f[1], f[2], f[3]);
+            dst[2 * c + 1] = make_uint4(f[4], f[5], f[6], f[7]);
+        }
+    }
+}
+
+// Layout of the caller's workspace (each part 256-byte aligned): the V
+// staging, then the format bytes; FP8 caches add the K staging.
 struct Workspace {
     int l_slot, t_slot;
-    size_t stage_bytes, fmt_off, total;
+    size_t stage_bytes, fmt_off, k_off, total;
 };
 
-Workspace workspace_layout(int num_seqs, int max_blocks, int block_size, int n_kv_heads, int d_head) {
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+Workspace workspace_layout(int num_seqs, int max_blocks, int block_size, int n_kv_heads, int d_head, bool f8 = false) {
     Workspace w;
     const long long pos = (long long)max_blocks * block_size;
     w.t_slot = (int)((pos + kKv - 1) / kKv);
     w.l_slot = w.t_slot * kKv;
     w.stage_bytes = (size_t)n_kv_heads * num_seqs * w.l_slot * d_head * 2;
-    w.fmt_off = (w.stage_bytes + 255) & ~(size_t)255;
-    w.total = w.fmt_off + (((size_t)n_kv_heads * num_seqs * w.t_slot + 255) & ~(size_t)255);
+    w.fmt_off = align256(w.stage_bytes);
+    w.k_off = w.fmt_off + align256((size_t)n_kv_heads * num_seqs * w.t_slot);
+    w.total = w.k_off;
+    if (f8) w.total = w.k_off + align256(w.stage_bytes);
     return w;
 }
 
@@ -1164,7 +1249,7 @@ bool encode(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kF8>
 int g_smem_done[64];   // per kernel instantiation: bytes opted in, by device
 
 int num_sms() {
@@ -1178,9 +1263,9 @@ int num_sms() {
     return n;
 }
 
-template <int D>
+template <int D, bool kF8>
 int launch(const PrefillArgs& a, const StageArgs& sa, const void* q, const void* k_cache, const void* v_cache,
-           int num_tokens, long long cache_rows, dim3 grid, cudaStream_t st) {
+           uint16_t* k_stage, int num_tokens, long long cache_rows, dim3 grid, cudaStream_t st) {
     CUtensorMap mq, mk, mv;
     const cuuint64_t qdims[3] = {(cuuint64_t)D, (cuuint64_t)a.n_q_heads, (cuuint64_t)num_tokens};
     const cuuint64_t qstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.n_q_heads * D * 2};
@@ -1188,43 +1273,47 @@ int launch(const PrefillArgs& a, const StageArgs& sa, const void* q, const void*
     const cuuint64_t cdims[2] = {(cuuint64_t)D, (cuuint64_t)cache_rows};
     const cuuint64_t cstr[1] = {(cuuint64_t)D * 2};
     const cuuint32_t cbox[2] = {64u, (cuuint32_t)a.block_size};
-    const cuuint64_t vdims[2] = {(cuuint64_t)D, (cuuint64_t)a.n_kv_heads * a.num_seqs * a.l_slot};
-    const cuuint32_t vbox[2] = {64u, (cuuint32_t)kKv};
-    if (!encode(&mq, q, 3, qdims, qstr, qbox) || !encode(&mk, k_cache, 2, cdims, cstr, cbox) ||
-        !encode(&mv, sa.v_stage, 2, vdims, cstr, vbox))
+    const cuuint64_t sdims[2] = {(cuuint64_t)D, (cuuint64_t)a.n_kv_heads * a.num_seqs * a.l_slot};
+    const cuuint32_t sbox[2] = {64u, (cuuint32_t)kKv};
+    // q from the caller; K from the caller's cache (bf16) or from the staging
+    // (FP8); V from the staging (the maps only move 16-bit elements)
+    if (!encode(&mq, q, 3, qdims, qstr, qbox) ||
+        !(kF8 ? encode(&mk, k_stage, 2, sdims, cstr, sbox) : encode(&mk, k_cache, 2, cdims, cstr, cbox)) ||
+        !encode(&mv, sa.v_stage, 2, sdims, cstr, sbox))
         return PA_ERR_CUDA;
-    if (pa_host::ensure_smem_attr(prefill_kernel<D>, PGeo<D>::kSmem, g_smem_done<D>) != cudaSuccess)
+    if (pa_host::ensure_smem_attr(prefill_kernel<D, kF8>, PGeo<D>::kSmem, g_smem_done<D, kF8>) != cudaSuccess)
         return PA_ERR_CUDA;
-    if (pa_host::launch_dependent(stage_v_kernel<D>, dim3((unsigned)sa.t_slot, (unsigned)sa.num_seqs,
-                                                          (unsigned)sa.n_kv_heads),
-                                  dim3(256), 0, st, static_cast<const uint4*>(v_cache), sa) != cudaSuccess)
-        return PA_ERR_CUDA;
-    return pa_host::launch_dependent(prefill_kernel<D>, grid, dim3(kThreads), PGeo<D>::kSmem, st, mq, mk, mv, a) ==
-                   cudaSuccess
+    const dim3 sgrid((unsigned)sa.t_slot, (unsigned)sa.num_seqs, (unsigned)sa.n_kv_heads);
+    if constexpr (kF8) {
+        if (pa_host::launch_dependent(stage_kv_f8_kernel<D>, sgrid, dim3(256), 0, st,
+                                      static_cast<const uint4*>(k_cache), static_cast<const uint4*>(v_cache), k_stage,
+                                      sa) != cudaSuccess)
+            return PA_ERR_CUDA;
+    } else {
+        if (pa_host::launch_dependent(stage_v_kernel<D>, sgrid, dim3(256), 0, st, static_cast<const uint4*>(v_cache),
+                                      sa) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    return pa_host::launch_dependent(prefill_kernel<D, kF8>, grid, dim3(kThreads), PGeo<D>::kSmem, st, mq, mk, mv,
+                                     a) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t pa_prefill_workspace_size(int num_seqs, int max_blocks_per_seq, int block_size, int n_kv_heads,
-                                 int d_head) {
-    if (num_seqs <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || n_kv_heads <= 0 || d_head <= 0) return 0;
-    return workspace_layout(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head).total;
-}
-
-int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
-               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start,
-               const int32_t* context_lens, int num_seqs, int num_tokens, int max_query_len, int num_blocks,
-               int block_size, float scale, int n_q_heads, int n_kv_heads, int d_head, void* workspace,
-               size_t workspace_bytes, int32_t* sched_dev, int32_t* status_dev, void* stream) {
+int prefill_impl(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start,
+                 const int32_t* context_lens, int num_seqs, int num_tokens, int max_query_len, int num_blocks,
+                 int block_size, float scale, int n_q_heads, int n_kv_heads, int d_head, void* workspace,
+                 size_t workspace_bytes, int32_t* sched_dev, int32_t* status_dev, void* stream, bool f8,
+                 float k_scale, float v_scale) {
     if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_blocks <= 0 || max_blocks_per_seq < 0 ||
         n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
         return PA_ERR_INVALID_ARG;
     if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
+    if (f8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !(k_scale < INFINITY) || !(v_scale < INFINITY)))
+        return PA_ERR_INVALID_ARG;
     if (!pa_host::supported_block_size(block_size) || !pa_host::supported_d_head(d_head)) return PA_ERR_UNSUPPORTED;
+    if (f8 && d_head != 128) return PA_ERR_UNSUPPORTED;
     const int group = n_q_heads / n_kv_heads;
     if (group > kRows || kRows % group != 0) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PA_OK;
@@ -1232,7 +1321,7 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
         return PA_ERR_INVALID_ARG;
     if (max_blocks_per_seq == 0) return PA_ERR_INVALID_ARG;
     if (num_seqs > 65535) return PA_ERR_UNSUPPORTED;
-    const Workspace ws = workspace_layout(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head);
+    const Workspace ws = workspace_layout(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head, f8);
     if ((long long)n_kv_heads * num_seqs * ws.l_slot > INT_MAX - kKv) return PA_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < ws.total) return PA_ERR_WORKSPACE;
     if (!pa_host::aligned16(out) || !pa_host::aligned16(q) || !pa_host::aligned16(k_cache) ||
@@ -1249,6 +1338,7 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     const long long tiles = (max_query_len + 2 * tq - 1) / (2 * tq);
     if (tiles * num_seqs > INT_MAX) return PA_ERR_UNSUPPORTED;
 
+    uint8_t* w8 = static_cast<uint8_t*>(workspace);
     PrefillArgs a;
     a.out = out;
     a.out_f32 = out_dtype == PA_DTYPE_F32;
@@ -1268,9 +1358,11 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     a.num_blocks = num_blocks;
     a.oob_row = (int)cache_rows;
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.v_fmt = static_cast<const uint8_t*>(workspace) + ws.fmt_off;
+    a.v_fmt = w8 + ws.fmt_off;
     a.l_slot = ws.l_slot;
     a.t_slot = ws.t_slot;
+    a.k_scale = f8 ? k_scale : 1.f;
+    a.v_scale = f8 ? v_scale : 1.f;
     a.status = status_dev;
     a.sched = reinterpret_cast<int*>(sched_dev);
     const long long items = tiles * num_seqs * n_kv_heads;
@@ -1290,12 +1382,53 @@ int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, con
     sa.num_blocks = num_blocks;
     sa.l_slot = ws.l_slot;
     sa.t_slot = ws.t_slot;
-    sa.v_stage = static_cast<uint16_t*>(workspace);
-    sa.v_fmt = static_cast<uint8_t*>(workspace) + ws.fmt_off;
+    sa.v_stage = reinterpret_cast<uint16_t*>(w8);
+    sa.v_fmt = w8 + ws.fmt_off;
     sa.status = status_dev;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return d_head == 128 ? launch<128>(a, sa, q, k_cache, v_cache, num_tokens, cache_rows, grid, st)
-                         : launch<64>(a, sa, q, k_cache, v_cache, num_tokens, cache_rows, grid, st);
+    if (f8)
+        return launch<128, true>(a, sa, q, k_cache, v_cache, reinterpret_cast<uint16_t*>(w8 + ws.k_off), num_tokens,
+                                 cache_rows, grid, st);
+    return d_head == 128 ? launch<128, false>(a, sa, q, k_cache, v_cache, nullptr, num_tokens, cache_rows, grid, st)
+                         : launch<64, false>(a, sa, q, k_cache, v_cache, nullptr, num_tokens, cache_rows, grid, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_prefill_workspace_size(int num_seqs, int max_blocks_per_seq, int block_size, int n_kv_heads,
+                                 int d_head) {
+    if (num_seqs <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || n_kv_heads <= 0 || d_head <= 0) return 0;
+    return workspace_layout(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head).total;
+}
+
+size_t pa_prefill_fp8_workspace_size(int num_seqs, int max_blocks_per_seq, int block_size, int n_kv_heads,
+                                     int d_head) {
+    if (num_seqs <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 || n_kv_heads <= 0 || d_head <= 0) return 0;
+    return workspace_layout(num_seqs, max_blocks_per_seq, block_size, n_kv_heads, d_head, true).total;
+}
+
+int pa_prefill(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+               const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start,
+               const int32_t* context_lens, int num_seqs, int num_tokens, int max_query_len, int num_blocks,
+               int block_size, float scale, int n_q_heads, int n_kv_heads, int d_head, void* workspace,
+               size_t workspace_bytes, int32_t* sched_dev, int32_t* status_dev, void* stream) {
+    return prefill_impl(out, out_dtype, q, k_cache, v_cache, block_tables, max_blocks_per_seq, query_start,
+                        context_lens, num_seqs, num_tokens, max_query_len, num_blocks, block_size, scale, n_q_heads,
+                        n_kv_heads, d_head, workspace, workspace_bytes, sched_dev, status_dev, stream, false, 1.f, 1.f);
+}
+
+int pa_prefill_fp8(void* out, int out_dtype, const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, int max_blocks_per_seq, const int32_t* query_start,
+                   const int32_t* context_lens, int num_seqs, int num_tokens, int max_query_len, int num_blocks,
+                   int block_size, float scale, float k_scale, float v_scale, int n_q_heads, int n_kv_heads,
+                   int d_head, void* workspace, size_t workspace_bytes, int32_t* sched_dev, int32_t* status_dev,
+                   void* stream) {
+    return prefill_impl(out, out_dtype, q, k_cache, v_cache, block_tables, max_blocks_per_seq, query_start,
+                        context_lens, num_seqs, num_tokens, max_query_len, num_blocks, block_size, scale, n_q_heads,
+                        n_kv_heads, d_head, workspace, workspace_bytes, sched_dev, status_dev, stream, true, k_scale,
+                        v_scale);
 }
 
 }  // extern "C"
