@@ -1,4 +1,5 @@
-"""Seeded sweeps over the supported shape space, GPU against the oracle.
+"""Seeded sweeps over the supported shape space (decode and prefill, bf16 and
+FP8 caches), GPU against the oracle.
 
 Each case draws d_head, block size, KV heads, group size, batch, context
 lengths (a mix of the lengths around block, 16-position tile, partition and
@@ -110,4 +111,31 @@ def test_prefill_random_config(i):
     want = A.paged_prefill(qb, kb, vb, tab, qs, ctx, 1.0 / math.sqrt(D), B)
     got, status = _run_prefill(qb, kb, vb, tab, qs, ctx, B, Hq, Hkv, D, out_dtype)
     assert status == 0, what
+    assert_attention_close(out_to_f64(got), want, out_dtype == torch.float32, what)
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_prefill_fp8_random_config(i):
+    from test_gpu_prefill_fp8 import _problem as _fp8_prefill_problem, _run as _run_fp8_prefill
+    rng = np.random.default_rng(5000 + i)
+    B = int(rng.choice([8, 16, 32]))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    while G * Hkv > 64:                      # keep the oracle's work small
+        G //= 2
+    S = int(rng.integers(1, 5))
+    ctxs = _lengths(rng, S, 700)
+    news = []
+    for c in ctxs:
+        u = rng.random()
+        news.append(c if u < 0.4 else (1 if u < 0.55 else int(rng.integers(1, c + 1))))
+    ks, vs = float(rng.choice([4.0 / 448, 0.01, 0.05])), float(rng.choice([3.0 / 448, 0.02]))
+    out_dtype = torch.float32 if rng.random() < 0.5 else torch.bfloat16
+    Hq = G * Hkv
+    qb, kc, vc, tab, qs, ctx = _fp8_prefill_problem(70 + i, Hq, Hkv, B, ctxs, news, ks, vs)
+    want = A.paged_prefill(qb, Q.dequantize(kc, ks), Q.dequantize(vc, vs), tab, qs, ctx, 1 / math.sqrt(128), B)
+    got, st = _run_fp8_prefill(qb, kc, vc, tab, qs, ctx, B, Hq, Hkv, ks, vs, out_dtype)
+    what = "fp8 prefill case %d: B %d Hkv %d G %d ctxs %s news %s scales %g %g %s" % (
+        i, B, Hkv, G, ctxs, news, ks, vs, out_dtype)
+    assert st == 0, what
     assert_attention_close(out_to_f64(got), want, out_dtype == torch.float32, what)
