@@ -708,15 +708,32 @@ def _prefill_oracle_time(sc, seq, rows):
 def prefill_cpu_baseline(sc, budget_s):
     """The oracle as it stands, on a bounded sample: the last query rows of
     the first sequence (all heads, over its whole context), as many as fit
-    about budget_s."""
+    about budget_s, on one thread and (the reported value) on every host
+    core at once, one worker process per core with a share of the rows."""
     rows = 1
     t, f = _prefill_oracle_time(sc, 0, rows)
     while t < budget_s / 2 and rows < sc.news[0]:
         rows = min(sc.news[0], max(rows + 1, int(rows * min(8.0, budget_s / max(t, 1e-3)))))
         t, f = _prefill_oracle_time(sc, 0, rows)
-    return {"value": round(f / t / 1e12, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+    desc = ("fp64 oracle prefill of the last %d of %d new positions of sequence 0 (context %d, all %d query heads) "
+            "of %s" % (rows, sc.news[0], sc.ctxs[0], sc.n_q_heads, sc.name))
+    one = {"value": round(f / t / 1e12, 8), "cores": 1, "sample": desc + ", %.1f s, 1 thread" % t}
+    procs = host_threads()
+    if procs <= 1:
+        return dict(one, unit="TFLOP/s", kind="oracle")
+    rows_all = min(sc.news[0], rows * procs)            # about as long per core as the one-thread leg
+    try:
+        t_all = _prefill_oracle_time_procs(sc, rows_all, procs, 1)
+    except Exception as e:                             # the one-thread leg stands alone
+        return dict(one, unit="TFLOP/s", kind="oracle", all_cores_failed=str(e)[:200])
+    c = sc.ctxs[0]
+    f_all = prefill_flops([c], [rows_all], sc.n_q_heads, sc.d_head)
+    value = f_all / t_all / 1e12
+    return {"value": round(value, 8), "unit": "TFLOP/s", "cores": procs, "kind": "oracle",
             "sample": "fp64 oracle prefill of the last %d of %d new positions of sequence 0 (context %d, all %d "
-                      "query heads) of %s, %.1f s" % (rows, sc.news[0], sc.ctxs[0], sc.n_q_heads, sc.name, t)}
+                      "query heads) of %s, %.1f s, %d worker processes at once, a share of the rows each" %
+                      (rows_all, sc.news[0], c, sc.n_q_heads, sc.name, t_all, procs),
+            "single_thread": one, "speedup_all_cores": round(value / max(one["value"], 1e-12), 1)}
 
 
 def run_prefill_reference(args, world, rank):
@@ -1147,22 +1164,54 @@ def _oracle_time_procs(sc, rep, tab, lens, q, procs, reps):
         np.save(os.path.join(d, "q.npy"), np.asarray(q))
         with open(os.path.join(d, "meta.json"), "w") as f:
             json.dump({"assign": assign, "block_size": B, "scale": sc.scale, "reps": reps}, f)
-        worker = os.path.join(ROOT, "tests", "_oracle_pool.py")
-        ps = [subprocess.Popen([sys.executable, worker, d, str(w)], stdin=subprocess.PIPE, stdout=subprocess.PIPE,
-                               text=True) for w in range(procs)]
-        try:
-            for p_ in ps:
-                if p_.stdout.readline().strip() != "ready":
-                    raise RuntimeError("oracle worker failed to start")
-            for p_ in ps:
-                p_.stdin.write("go\n")
-                p_.stdin.flush()
-            elapsed = [json.loads(p_.stdout.readline())["elapsed"] for p_ in ps]
-        finally:
-            for p_ in ps:
-                if p_.poll() is None:
-                    p_.wait(timeout=600)
-        return max(elapsed)
+        return _pool_elapsed(d, procs)
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+
+
+def _pool_elapsed(d, procs):
+    """Start one oracle worker per core on the sample in directory d
+    (tests/_oracle_pool.py), release them together once all are ready, and
+    return the slowest one's seconds."""
+    worker = os.path.join(ROOT, "tests", "_oracle_pool.py")
+    ps = [subprocess.Popen([sys.executable, worker, d, str(w)], stdin=subprocess.PIPE, stdout=subprocess.PIPE,
+                           text=True) for w in range(procs)]
+    try:
+        for p_ in ps:
+            if p_.stdout.readline().strip() != "ready":
+                raise RuntimeError("oracle worker failed to start")
+        for p_ in ps:
+            p_.stdin.write("go\n")
+            p_.stdin.flush()
+        elapsed = [json.loads(p_.stdout.readline())["elapsed"] for p_ in ps]
+    finally:
+        for p_ in ps:
+            if p_.poll() is None:
+                p_.wait(timeout=600)
+    return max(elapsed)
+
+
+def _prefill_oracle_time_procs(sc, rows, procs, reps):
+    """Seconds the oracle takes to compute the last `rows` new positions of
+    sequence 0 `reps` times on `procs` host cores at once: each worker
+    process takes a contiguous share of the rows (as one chunk at their
+    positions) over the sequence's whole context."""
+    import shutil
+    q, kc, vc, tables, _, ctx = _prefill_oracle_sample(sc, 0, rows)
+    first_pos = int(ctx[0]) - rows                    # position of sampled row 0
+    # shares of equal work: row r attends to first_pos + r + 1 keys
+    work = np.cumsum(np.arange(first_pos + 1, first_pos + rows + 1, dtype=np.float64))
+    cuts = [0] + [int(np.searchsorted(work, work[-1] * w / procs)) for w in range(1, procs)] + [rows]
+    d = tempfile.mkdtemp(prefix="oracle_pool_")
+    try:
+        np.save(os.path.join(d, "k.npy"), kc)
+        np.save(os.path.join(d, "v.npy"), vc)
+        np.save(os.path.join(d, "tab.npy"), tables)
+        np.save(os.path.join(d, "q.npy"), q)
+        with open(os.path.join(d, "meta.json"), "w") as f:
+            json.dump({"mode": "prefill", "assign": [[cuts[w], cuts[w + 1]] for w in range(procs)],
+                       "block_size": sc.block_size, "scale": sc.scale, "reps": reps, "first_pos": first_pos}, f)
+        return _pool_elapsed(d, procs)
     finally:
         shutil.rmtree(d, ignore_errors=True)
 

@@ -98,6 +98,29 @@ def test_worker_pool_time_is_the_slowest_worker():
     assert 0 < t < 60
 
 
+def _small_prefill():
+    from types import SimpleNamespace
+    return SimpleNamespace(name="small_prefill", ctxs=[300, 200], news=[300, 64], block_size=16, n_kv_heads=2,
+                           n_q_heads=8, d_head=64, scale=0.125)
+
+
+def test_prefill_worker_pool_time_is_the_slowest_worker():
+    """Each worker takes a contiguous share of the sampled rows as one chunk
+    at their positions (chunking leaves the oracle's output unchanged: pinned
+    in the oracle's prefill tests)."""
+    t = bench._prefill_oracle_time_procs(_small_prefill(), 40, 2, 2)
+    assert 0 < t < 60
+
+
+def test_prefill_cpu_baseline_reports_both_legs():
+    line = bench.prefill_cpu_baseline(_small_prefill(), 0.2)
+    assert line["kind"] == "oracle" and line["value"] > 0 and line["unit"] == "TFLOP/s"
+    assert "all_cores_failed" not in line, line.get("all_cores_failed")
+    if bench.host_threads() > 1:
+        assert line["cores"] == bench.host_threads()
+        assert line["single_thread"]["cores"] == 1 and line["single_thread"]["value"] > 0
+
+
 def test_quantiles():
     assert bench._quantiles([5.0, 1.0, 3.0, 2.0, 4.0]) == (3.0, 1.0, 5.0)
     assert bench._quantiles([2.0]) == (2.0, 2.0, 2.0)
