@@ -438,3 +438,38 @@ def test_prefill_32768_token_prompt_windows():
         want = A.paged_prefill(qb[i0:i1], kb, vb, tab, np.array([0, 32], np.int32),
                                        np.array([i1], np.int32), 1.0 / math.sqrt(D), B)
         assert_attention_close(got[i0:i1], want, False, "rows %d..%d" % (i0, i1))
+
+
+def test_prefill_captured_in_a_cuda_graph_equals_eager():
+    """pa_prefill is a chain of programmatic dependent launches (the V
+    staging, then the prefill kernel); captured in a CUDA graph and replayed
+    twice (the work-claim counters come back to zero after each call), it
+    must give the eager call's output bit for bit."""
+    Hq, Hkv, D, B = 16, 4, 128, 16
+    ctxs, news = [700, 300], [500, 300]
+    qb, kb, vb, tab, qs, ctx = _problem(41, Hq, Hkv, D, B, ctxs, news)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    args = (from_bits(qb), from_bits(kb), from_bits(vb), dev(tab), dev(qs), dev(ctx), max(news), B,
+            1 / math.sqrt(D), Hq, Hkv, D)
+    ws = api.prefill_workspace(len(ctxs), tab.shape[1], B, Hkv, D)
+    cnt = torch.zeros(2, dtype=torch.int32, device="cuda")
+    eager = torch.full((qb.shape[0], Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+    api.pa_prefill(eager, *args, workspace=ws, counters=cnt)
+    torch.cuda.synchronize()
+    out = torch.full_like(eager, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        api.pa_prefill(out, *args, workspace=ws, counters=cnt, stream=s)      # warm-up off the default stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    out.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        api.pa_prefill(out, *args, workspace=ws, counters=cnt, stream=torch.cuda.current_stream())
+    for _ in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int32), eager.view(torch.int32))
+        out.fill_(float("nan"))
+    assert int(cnt.abs().sum().item()) == 0

@@ -170,3 +170,32 @@ def test_prefill_fp8_errors_and_flags():
     bad[0, 1] = kc.shape[0] + 3                           # outside the pool
     _, st = _run(qb, kc, vc, bad, qs, ctx, B, Hq, Hkv, 0.01, 0.01, torch.float32)
     assert st & api.PA_DEV_BAD_BLOCK_ID
+
+
+def test_prefill_fp8_captured_in_a_cuda_graph_equals_eager():
+    """The FP8 call (K and V staging, then the prefill kernel) captured in a
+    CUDA graph and replayed twice gives the eager call's output bit for bit."""
+    Hq, Hkv, B, ks, vs = 16, 4, 16, 4.0 / 448, 3.0 / 448
+    qb, kc, vc, tab, qs, ctx = _problem(10, Hq, Hkv, B, [600, 257], [600, 100], ks, vs)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    args = (from_bits(qb), dev(kc), dev(vc), dev(tab), dev(qs), dev(ctx), 600, B, 1 / math.sqrt(D), ks, vs, Hq, Hkv, D)
+    ws = api.prefill_fp8_workspace(2, tab.shape[1], B, Hkv, D)
+    cnt = torch.zeros(2, dtype=torch.int32, device="cuda")
+    eager = torch.full((qb.shape[0], Hq, D), float("nan"), dtype=torch.float32, device="cuda")
+    api.pa_prefill_fp8(eager, *args, workspace=ws, counters=cnt)
+    torch.cuda.synchronize()
+    out = torch.full_like(eager, float("nan"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        api.pa_prefill_fp8(out, *args, workspace=ws, counters=cnt, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        api.pa_prefill_fp8(out, *args, workspace=ws, counters=cnt, stream=torch.cuda.current_stream())
+    for _ in range(2):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int32), eager.view(torch.int32))
