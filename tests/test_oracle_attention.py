@@ -167,6 +167,19 @@ def test_large_scores_do_not_overflow_and_shift_invariance():
     np.testing.assert_allclose(shifted, base, rtol=1e-9, atol=1e-12)
 
 
+def test_dominant_score_gives_its_value_row():
+    """One score 1,000 above all others ([P2] section 11: subtracting the
+    maximum keeps every exponential at most 1): each other weight is
+    exp(-1000), which is 0 in float64, so the output is exactly that value
+    row.  Exponentials of the raw or minimum-shifted scores overflow."""
+    rng = np.random.default_rng(5)
+    K = np.zeros((6, 3))
+    K[4, 0] = 1000.0
+    V = rng.normal(size=(6, 3))
+    o = A.softmax_attention(np.array([1.0, 0.0, 0.0]), K, V, 1.0)
+    assert np.array_equal(o, V[4])
+
+
 def test_zero_context_gives_zero_row():
     q = np.ones((1, 2, 4))
     kc = np.ones((2, 1, 4, 4))

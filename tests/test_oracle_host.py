@@ -248,6 +248,22 @@ def test_verification_suite_2_and_5_with_payload():
     assert alloc.num_free() == t5["free_after_release"] and all(r == 0 for r in alloc.ref_counts)
 
 
+def test_release_order_is_table_order():
+    """[P1] section 20's teaching allocator: the free list starts as the
+    block ids in reverse, allocation takes from its end, and freeing a
+    sequence appends its blocks in table order.  Derived by hand for a pool
+    of 8 blocks of 4 slots: A (10 tokens) takes 0, 1, 2; after A is freed
+    the list ends ..., 3, 0, 1, 2, so B (4 tokens) takes 2 and C (8 tokens)
+    takes 1, then 0."""
+    al = AL.RefAllocator(8, 4)
+    assert al.allocate("A", 10) == AL.OK
+    assert al.block_tables["A"] == [0, 1, 2]
+    assert al.free("A") == AL.OK
+    assert al.free_blocks == [7, 6, 5, 4, 3, 0, 1, 2]
+    assert al.allocate("B", 4) == AL.OK and al.block_tables["B"] == [2]
+    assert al.allocate("C", 8) == AL.OK and al.block_tables["C"] == [1, 0]
+
+
 def test_allocator_argument_errors_and_transactional_failures():
     with pytest.raises(ValueError):
         AL.RefAllocator(0, 4)
@@ -315,7 +331,9 @@ def test_reshape_and_cache_writes_only_its_slots():
     v = rng.integers(0, 1 << 16, size=(NB, H, B, D), dtype=np.uint16)
     kn = rng.integers(0, 1 << 16, size=(4, H, D), dtype=np.uint16)
     vn = rng.integers(0, 1 << 16, size=(4, H, D), dtype=np.uint16)
-    slots = [5, -1, 23, 0]
+    # a negative slot is skipped (reading O7); written, -1 would land on
+    # block 5, offset 3, which no other token writes
+    slots = [5, -1, 22, 0]
     k2, v2 = C.reshape_and_cache(k.copy(), v.copy(), kn, vn, slots, B)
     touched = np.zeros((NB, B), dtype=bool)
     for t, s in enumerate(slots):

@@ -1,0 +1,168 @@
+"""Planted mistakes in the oracle are caught by its pins.  CPU only.
+
+Each case copies one oracle module's source, makes one plausible mistake in
+it (a dropped term or factor, a wrong sign, index or bound, swapped
+operands, a changed constant of the number format, a changed list order),
+loads the copy as a module of its own and runs the pin tests of that module
+against the copy (page-printed worked examples and traces, closed forms,
+format definitions, brute force, invariants): at least one of them must
+fail.  The oracle's files are not changed; a mistake that no pin catches
+makes its case fail here."""
+import inspect
+import os
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+import test_oracle_attention as TA
+import test_oracle_host as TH
+import test_oracle_prefill as TP
+import test_oracle_quant as TQ
+
+ORACLE_DIR = os.path.dirname(os.path.abspath(oracle.__file__))
+
+# The test modules that pin each oracle module, and the name they import it as.
+PINS = {
+    "attention": [(TA, "A"), (TP, "A"), (TH, "A")],
+    "quant": [(TQ, "Q")],
+    "cache_ops": [(TH, "C")],
+    "sizing": [(TH, "Z")],
+    "allocator": [(TH, "AL")],
+}
+
+# (module, original text, planted mistake, what the mistake is)
+MUTANTS = [
+    # attention: the definition, the paging, the grouping, the causal mask, the merge
+    ("attention", "s = scale * (K @ q)\n", "s = K @ q\n", "score scale dropped"),
+    ("attention", "a = e / e.sum()", "a = e / e.max()", "softmax normalised by its largest term"),
+    ("attention", "    m = s.max()\n    e = np.exp(s - m)\n    a = e / e.sum()",
+     "    m = s.min()\n    e = np.exp(s - m)\n    a = e / e.sum()", "minimum subtracted instead of maximum"),
+    ("attention", "return a @ V", "return a @ V[::-1]", "value rows in reverse order"),
+    ("attention", "logical_block = i // block_size", "logical_block = i % block_size",
+     "logical block from the offset"),
+    ("attention", "phys, _ = translate(b * block_size, block_size, block_table_row)",
+     "phys, _ = translate(b, block_size, block_table_row)", "block index passed as a position"),
+    ("attention", "valid = min(block_size, context_len - b * block_size)",
+     "valid = min(block_size, context_len - b * block_size - 1)", "last position of each block dropped"),
+    ("attention", "return q_head // (n_q_heads // n_kv_heads)", "return q_head % n_kv_heads",
+     "interleaved instead of contiguous query-head groups"),
+    ("attention", "K[h, :p + 1], V[h, :p + 1]", "K[h, :p + 2], V[h, :p + 2]",
+     "causal mask lets a row see the next position"),
+    ("attention", "K[h, :p + 1], V[h, :p + 1]", "K[h, :p], V[h, :p]", "causal mask hides the row's own position"),
+    ("attention", "            p = C - n + i\n", "            p = i\n", "new positions counted from 0, not after the prefix"),
+    ("attention", "w = np.exp(m_b - m)", "w = np.exp(m - m_b)", "merge weight with the wrong sign"),
+    ("attention", "return m, e.sum(), e @ np.asarray(V, dtype=np.float64)",
+     "return m, e.sum(), np.exp(s) @ np.asarray(V, dtype=np.float64)", "block value sum not shifted by its maximum"),
+    ("attention", "return e @ np.asarray(V, dtype=np.float64), e.sum()",
+     "return e @ np.asarray(V, dtype=np.float64), e.max()", "page normaliser is the largest term"),
+    ("attention", "<< np.uint32(16)", "<< np.uint32(15)", "bf16 pattern shifted one bit short"),
+    # quant: the E4M3 format definition and the rounding rule
+    ("quant", "(1.0 + m / 8.0) * 2.0 ** (e - 7)", "(1.0 + m / 8.0) * 2.0 ** (e - 8)", "exponent bias 8"),
+    ("quant", "m * 2.0 ** -9", "m * 2.0 ** -10", "subnormal step 2^-10"),
+    ("quant", "(1.0 + m / 8.0)", "(1.0 + m / 16.0)", "four fraction bits"),
+    ("quant", "code = np.where(nan, NAN_CODE, code)", "code = np.where(nan | (np.abs(x) > 448.0), NAN_CODE, code)",
+     "overflow gives NaN instead of saturating"),
+    ("quant", "pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (code_hi % 2 == 0) & (code_lo % 2 != 0))",
+     "pick_hi = d_hi <= d_lo", "ties rounded up instead of to the even code"),
+    ("quant", "mag = np.where((e == 15) & (m == 7), np.nan, mag)", "mag = mag", "no NaN code"),
+    ("quant", "sign = np.signbit(x).astype(np.int64) << 7", "sign = np.signbit(x).astype(np.int64) << 6",
+     "sign bit in the wrong place"),
+    ("quant", "np.asarray(x, dtype=np.float32) / np.float32(scale)", "np.asarray(x, dtype=np.float64) / float(scale)",
+     "division in float64 instead of float32"),
+    # cache_ops: slot arithmetic and copy direction
+    ("cache_ops", "block, offset = divmod(int(slot), block_size)", "offset, block = divmod(int(slot), block_size)",
+     "block and offset swapped"),
+    ("cache_ops", "if slot < 0:\n            continue", "if slot < -1:\n            continue",
+     "slot -1 written instead of skipped"),
+    ("cache_ops", "k_out[layer][dst] = k_out[layer][src]", "k_out[layer][src] = k_out[layer][dst]",
+     "copy direction swapped for K"),
+    ("cache_ops", "v_out[layer][dst] = v_out[layer][src]", "pass", "V not copied"),
+    # sizing: the closed forms
+    ("sizing", "return 2 * n_layers * n_kv_heads * d_head * elem_bytes",
+     "return n_layers * n_kv_heads * d_head * elem_bytes", "K only, V forgotten"),
+    ("sizing", "return -(-n_tokens // block_size)", "return n_tokens // block_size", "floor instead of ceiling"),
+    ("sizing", "return blocks_needed(n_tokens, block_size) * entry_bytes",
+     "return blocks_needed(n_tokens, block_size) * 8", "8-byte table entries"),
+    # allocator: free-list order, reference counts, copy on write
+    ("allocator", "self.free_blocks = list(reversed(range(num_blocks)))", "self.free_blocks = list(range(num_blocks))",
+     "free list not reversed"),
+    ("allocator", "b = self.free_blocks.pop()", "b = self.free_blocks.pop(0)", "free list taken from the front"),
+    ("allocator", "if self.ref_counts[tail] > 1:", "if self.ref_counts[tail] > 2:", "copy only when three share"),
+    ("allocator", "                self.ref_counts[tail] -= 1\n", "", "shared tail keeps the writer's reference"),
+    ("allocator", "for b in self.block_tables[parent]:\n            self.ref_counts[b] += 1",
+     "for b in self.block_tables[parent]:\n            pass", "fork does not count the child's references"),
+    ("allocator", "for b in self.block_tables[seq]:\n            self.ref_counts[b] -= 1",
+     "for b in reversed(self.block_tables[seq]):\n            self.ref_counts[b] -= 1", "blocks released in reverse order"),
+    ("allocator", "needed = -(-num_tokens // self.block_size)", "needed = num_tokens // self.block_size + 1",
+     "one block too many for exact multiples"),
+    ("allocator", "slot = tail * B + offset", "slot = tail * B + offset - 1", "append slot one before the tail position"),
+]
+
+
+def _mutant(module, old, new):
+    with open(os.path.join(ORACLE_DIR, module + ".py")) as f:
+        src = f.read()
+    assert src.count(old) == 1, "the mistake's site must occur exactly once in oracle/%s.py" % module
+    mod = types.ModuleType("oracle_mutant_" + module)
+    mod.__package__ = "oracle"
+    exec(compile(src.replace(old, new), "<oracle/%s.py with a planted mistake>" % module, "exec"), mod.__dict__)
+    return mod
+
+
+def _worked():
+    """The worked-example fixture of the attention pins."""
+    g = TA.load("p2_worked_attention.json")
+    return {"g": g, "q": np.array(TA.ev_all(g["q"])), "K": np.array(TA.ev_all(g["K"])),
+            "V": np.array(TA.ev_all(g["V"])), "scale": TA.ev(g["scale"])}
+
+
+def _calls(fn):
+    """The keyword-argument sets pytest would call a pin test with."""
+    names, sets = [], [()]
+    for mark in getattr(fn, "pytestmark", []):
+        if mark.name != "parametrize":
+            continue
+        argnames = mark.args[0]
+        argnames = [a.strip() for a in argnames.split(",")] if isinstance(argnames, str) else list(argnames)
+        values = [v if len(argnames) > 1 else (v,) for v in mark.args[1]]
+        names += argnames
+        sets = [s + tuple(v) for s in sets for v in values]
+    params = inspect.signature(fn).parameters
+    for s in sets:
+        kw = dict(zip(names, s))
+        if "worked" in params:
+            kw["worked"] = _worked()
+        yield kw
+
+
+def _pin_tests(module):
+    for tm, _ in PINS[module]:
+        for name, fn in inspect.getmembers(tm, inspect.isfunction):
+            if name.startswith("test_") and fn.__module__ == tm.__name__:
+                yield tm.__name__ + "." + name, fn
+
+
+def _first_failing_pin(module):
+    for name, fn in _pin_tests(module):
+        for kw in _calls(fn):
+            try:
+                with np.errstate(all="ignore"):
+                    fn(**kw)
+            except Exception:          # a failed assertion, or the mistake breaking the call
+                return name
+    return None
+
+
+def test_pins_pass_on_the_oracle_itself():
+    for module in PINS:
+        assert _first_failing_pin(module) is None
+
+
+@pytest.mark.parametrize("module,old,new,what", MUTANTS, ids=["%s: %s" % (m[0], m[3]) for m in MUTANTS])
+def test_planted_mistake_is_caught(module, old, new, what, monkeypatch):
+    mutant = _mutant(module, old, new)
+    for tm, alias in PINS[module]:
+        monkeypatch.setattr(tm, alias, mutant)
+    assert _first_failing_pin(module) is not None, "no pin catches: " + what

@@ -61,3 +61,17 @@ def test_quantize_uses_float32_division():
     assert np.array_equal(Q.quantize(x, s), want)
     np.testing.assert_array_equal(Q.dequantize(Q.quantize(x, s), s),
                                   Q.e4m3_to_f64(want) * float(s))
+    # An input whose float32 quotient is exactly the midpoint 1.0625 of the
+    # codes for 1.0 (even) and 1.125 (odd) while the exact quotient lies
+    # above it: a float32 division rounds it to 1.0 (tie to the even code),
+    # a float64 one to 1.125.
+    x0 = np.float32(1.0625 * float(s))
+    pick = None
+    for k in range(-64, 65):
+        xc = np.float32(x0 + np.float32(k) * np.spacing(x0))
+        if np.float32(xc) / s == np.float32(1.0625) and float(xc) / float(s) > 1.0625:
+            pick = xc
+            break
+    assert pick is not None
+    assert Q.e4m3_to_f64(Q.quantize(np.array([pick], dtype=np.float32), s))[0] == 1.0
+    assert Q.e4m3_to_f64(Q.f64_to_e4m3(np.array([float(pick) / float(s)])))[0] == 1.125
