@@ -20,6 +20,8 @@ import test_oracle_attention as TA
 import test_oracle_host as TH
 import test_oracle_prefill as TP
 import test_oracle_quant as TQ
+import test_prefix_cache as TPC
+import test_swap as TS
 
 ORACLE_DIR = os.path.dirname(os.path.abspath(oracle.__file__))
 
@@ -29,8 +31,15 @@ PINS = {
     "quant": [(TQ, "Q")],
     "cache_ops": [(TH, "C")],
     "sizing": [(TH, "Z")],
-    "allocator": [(TH, "AL")],
+    "allocator": [(TH, "AL"), (TPC, "AL")],
 }
+# Tests that compare the oracle with the library's own block manager are not
+# pins (they would catch a planted mistake by disagreeing with product code);
+# tests run on both views run on the oracle's only.  test_swap reaches the
+# oracle through test_prefix_cache's view.
+NOT_PINS = ("abi_matches_oracle", "colliding_keys", "key_mask", "hit_rate", "prefix_argument_errors",
+            "swap_argument_errors")
+EXTRA_PIN_MODULES = {"allocator": [TS]}
 
 # (module, original text, planted mistake, what the mistake is)
 MUTANTS = [
@@ -98,6 +107,19 @@ MUTANTS = [
     ("allocator", "needed = -(-num_tokens // self.block_size)", "needed = num_tokens // self.block_size + 1",
      "one block too many for exact multiples"),
     ("allocator", "slot = tail * B + offset", "slot = tail * B + offset - 1", "append slot one before the tail position"),
+    # allocator: prefix caching ([P1] sections 18-19, [P2] section 6) and swap planning ([P1] section 19)
+    ("allocator", "keys = [tuple(tokens[:(i + 1) * B]) for i in range(full)]",
+     "keys = [tuple(tokens[i * B:(i + 1) * B]) for i in range(full)]", "a block's key is its own tokens, not its prefix"),
+    ("allocator", "b, _ = self.evict_queue.popitem(last=False)", "b, _ = self.evict_queue.popitem(last=True)",
+     "the newest idle cached block evicted first"),
+    ("allocator", "            self.evict_queue.pop(b, None)\n            self.ref_counts[b] += 1",
+     "            self.ref_counts[b] += 1", "a revived block stays in the eviction queue"),
+    ("allocator", "if self.caching and offset == B - 1:", "if self.caching and offset == B - 2:",
+     "a generated block registered one position early"),
+    ("allocator", "self.host_refs[h] = counts[b]", "self.host_refs[h] = 1", "host block of a shared block counted once"),
+    ("allocator", "self.ref_counts[b] = counts[h]", "self.ref_counts[b] = 1", "swapped-in shared block counted once"),
+    ("allocator", "if b not in counts:\n                    counts[b] = 0\n                    blocks.append(b)\n                counts[b] += 1",
+     "counts[b] = counts.get(b, 0) + 1\n                blocks.append(b)", "a shared block swapped once per sharer"),
 ]
 
 
@@ -132,15 +154,18 @@ def _calls(fn):
     params = inspect.signature(fn).parameters
     for s in sets:
         kw = dict(zip(names, s))
+        if kw.get("view", "oracle") != "oracle":
+            continue
         if "worked" in params:
             kw["worked"] = _worked()
         yield kw
 
 
 def _pin_tests(module):
-    for tm, _ in PINS[module]:
+    mods = [tm for tm, _ in PINS[module]] + EXTRA_PIN_MODULES.get(module, [])
+    for tm in mods:
         for name, fn in inspect.getmembers(tm, inspect.isfunction):
-            if name.startswith("test_") and fn.__module__ == tm.__name__:
+            if name.startswith("test_") and fn.__module__ == tm.__name__ and not any(x in name for x in NOT_PINS):
                 yield tm.__name__ + "." + name, fn
 
 
