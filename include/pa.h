@@ -97,7 +97,11 @@ const char* pa_status_string(int status);
  *
  * Each sequence is split into partitions of partition_size positions, one
  * thread block per (sequence, group of up to 8 query heads, partition).  A
- * sequence that fits one partition is finished by its block.  Otherwise
+ * sequence that fits one partition is finished by its block.  When the batch
+ * has many head groups (at least two waves of resident blocks) and some
+ * sequence spans several partitions, the resident blocks instead claim the
+ * (sequence, head group, partition) items that exist, so that no block is
+ * spent on the partitions past a short sequence's end.  Otherwise
  * every block leaves its partition's maximum m, weight sum z and
  * unnormalised weighted value sum u (the statistics of [P2] section 11) in
  * `workspace`, and a second kernel merges them exactly (the "secondary
@@ -123,9 +127,13 @@ const char* pa_status_string(int status);
  *   workspace     device scratch of at least pa_decode_workspace_size(...)
  *                 bytes (same arguments, same current device), 256-byte
  *                 aligned; may be NULL (bytes 0) when that size is 0 (every
- *                 sequence fits one partition).  Nothing in it needs to be
- *                 initialised; its contents are not preserved across calls,
- *                 and calls that share a workspace must be stream-ordered.
+ *                 sequence fits one partition).  Its first 8 bytes are two
+ *                 int32 counters through which blocks claim work: they must
+ *                 be zero before the workspace's first use, and every call
+ *                 leaves them zero (the last block to finish resets them).
+ *                 Nothing else in it needs to be initialised; its contents
+ *                 are not preserved across calls, and calls that share a
+ *                 workspace must be stream-ordered.
  *   status_dev    optional device int32, see PA_DEV_* above.
  * Returns PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_MISALIGNED,
  * PA_ERR_WORKSPACE or PA_ERR_CUDA (launch failure).
@@ -259,7 +267,8 @@ int pa_lse_merge(void* out, int out_dtype, const float* part_max,
  *    its own copy of the array, and the first call in it looks the address
  *    up again.
  *  - All calls share the one array and it keeps whatever the last call left
- *    there.  Nothing in it needs to start at zero: every value the merge
+ *    there.  Its first 8 bytes are pa_decode's claim counters, zero when the
+ *    library is loaded and left zero by every call; every value the merge
  *    reads was written earlier in the same call.  Calls whose kernels
  *    overlap on the GPU (other streams, other host threads) race on it; order
  *    them on one stream.

@@ -198,7 +198,8 @@ def decode_workspace(num_seqs, n_q_heads, d_head, max_context_len, partition_siz
     n = pa_decode_workspace_size(num_seqs, n_q_heads, d_head, max_context_len, partition_size)
     if n == 0:
         return None
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    # zeroed: the header's claim counters must be zero before the first call
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, block_size, scale, n_q_heads,

@@ -102,7 +102,16 @@ struct DecodeArgs {
     const __nv_bfloat16* v_new;
     uint8_t* k_cache;        // the caches, written at the appended positions
     uint8_t* v_cache;
+    // Claimed work (many short sequences): {next item, blocks done} in the
+    // workspace's header, zero between calls; n_units head groups per
+    // sequence.
+    int* claim;
+    int n_units;
 };
+
+// Claimed work: at most this many sequences (their item offsets live in
+// shared memory).
+constexpr int kClaimMaxSeqs = 1024;
 
 // Shared-memory geometry; F8: one-byte (E4M3) cache elements, rows of d_head
 // bytes (d_head 128: one 128-byte box per row).
@@ -637,7 +646,11 @@ __device__ __forceinline__ void append_row(uint8_t* stage, int r, const DecodeAr
 
 // NK = 2 (FP8, G = 4): a block covers two adjacent KV heads (8 query heads);
 // its stages are twice as large, so one block fewer fits an SM.
-template <int D, bool F8, int NK = 1>
+// kClaim: the grid is the resident blocks, and each claims work items
+// (sequence, head group, partition) until none is left, so that no block is
+// spent on a partition past its sequence's end; otherwise one block per
+// (partition, head group, sequence) of the grid, some of them empty.
+template <int D, bool F8, int NK = 1, bool kClaim = false>
 __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS_F8 - 1 : PA_DECODE_MIN_BLOCKS_F8)
                                                : PA_DECODE_MIN_BLOCKS)
     decode_partition_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -649,22 +662,99 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + G::kRingBytes);
     int32_t* table = reinterpret_cast<int32_t*>(bars + kWarps * kStages);
 
-    const int part = blockIdx.x;
-    const int seq = blockIdx.z;
-    const int kvh = NK == 1 ? blockIdx.y / a.n_sub : blockIdx.y * NK;
-    const int hpb = a.heads_per_block;
-    const int qh0 = kvh * a.group + (blockIdx.y % a.n_sub) * hpb;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int B = a.block_size;
+    const int P = a.partition_size;
+    const int table_ints = (P >> a.log2_block) + 2;
+    // claimed work: item offsets per sequence, and the claimed item
+    int32_t* pre = table + table_ints;                 // [num_seqs + 1]
+    int32_t* claimed = pre + kClaimMaxSeqs + 1;
 
     // Launched as a programmatic dependent: inputs may come from the kernel
     // before this one on the stream, so nothing is read before this wait.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (kClaim) {
+        // Items, in order: sequence, head group, partition; sequence s holds
+        // n_units * max(1, partitions of s) of them (a context of 0 is one
+        // item, which writes zeros).  pre[s] = items before sequence s.
+        // (Handing out every sequence's whole partitions before the last,
+        // shorter ones measured 2 % slower on a ragged batch.)
+        const int S = a.num_seqs;
+        constexpr int kPer = (kClaimMaxSeqs + kThreads - 1) / kThreads;
+        int cnt[kPer];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int s_ = threadIdx.x * kPer + i;
+            int c = 0;
+            if (s_ < S) {
+                int ctx_ = a.context_lens[s_];
+                ctx_ = ctx_ < 0 ? 0 : (ctx_ > a.ctx_cap ? a.ctx_cap : ctx_);
+                const int np_ = (ctx_ + P - 1) / P;
+                c = a.n_units * (np_ > 0 ? np_ : 1);
+            }
+            cnt[i] = c;
+            sum += c;
+        }
+        // exclusive scan of the threads' sums: within the warp, then across warps
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) claimed[1 + warp] = incl;
+        __syncthreads();
+        int base = incl - sum;
+        for (int w = 0; w < warp; ++w) base += claimed[1 + w];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int s_ = threadIdx.x * kPer + i;
+            if (s_ < S) pre[s_] = base;
+            base += cnt[i];
+        }
+        if (threadIdx.x == kThreads - 1) pre[S] = base;
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < kWarps * kStages; ++i) pa::mbar_init(&bars[i], 1);
+            pa::fence_mbar_init();
+        }
+        // every block has made its claims' inputs its own: the merge kernel
+        // may begin its launch
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+    int kg = 0;                      // this warp's stages consumed by earlier items
+    bool aborted = false;
+    for (;;) {
+    int part, seq, yb;
+    if constexpr (kClaim) {
+        __syncthreads();             // pre is complete, the previous item's readers are done
+        if (threadIdx.x == 0) claimed[0] = atomicAdd(a.claim, 1);
+        __syncthreads();
+        const int v = claimed[0];
+        if (v >= pre[a.num_seqs]) break;
+        int lo = 0, hi = a.num_seqs - 1;              // the sequence s with pre[s] <= v < pre[s + 1]
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= v) lo = mid; else hi = mid - 1;
+        }
+        seq = lo;
+        const int np_ = (pre[seq + 1] - pre[seq]) / a.n_units;
+        const int r = v - pre[seq];
+        yb = r / np_;
+        part = r - yb * np_;
+    } else {
+        part = blockIdx.x;
+        seq = blockIdx.z;
+        yb = blockIdx.y;
+    }
+    const int kvh = NK == 1 ? yb / a.n_sub : yb * NK;
+    const int hpb = a.heads_per_block;
+    const int qh0 = kvh * a.group + (yb % a.n_sub) * hpb;
+
     // Independent loads first: the context length, a speculative slice of the
     // block table (this partition's entries, read before the length is known)
     // and q; one memory round trip instead of three.
-    const int B = a.block_size;
-    const int P = a.partition_size;
     const int lb0 = (part * P) >> a.log2_block;
     const int32_t* trow = a.block_tables + (size_t)seq * a.max_blocks_per_seq;
     const int n_spec = max(0, min(P >> a.log2_block, a.max_blocks_per_seq - lb0));
@@ -692,28 +782,32 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
     } else {
         load_q<D>(qb, a.q + row0, hpb, lane);
     }
-    if (threadIdx.x == 0) {
+    if (!kClaim && threadIdx.x == 0) {
         for (int i = 0; i < kWarps * kStages; ++i) pa::mbar_init(&bars[i], 1);
         pa::fence_mbar_init();
     }
 
     const bool ctx_ok = ctx >= 0 && ctx <= a.ctx_cap;
     if (!ctx_ok) {
-        if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
+        if (threadIdx.x == 0 && part == 0 && yb == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
         ctx = ctx < 0 ? 0 : a.ctx_cap;
     }
     const int nparts = (ctx + P - 1) / P;
-    if (part >= (nparts > 0 ? nparts : 1)) return;
+    if (part >= (nparts > 0 ? nparts : 1)) {
+        if constexpr (kClaim) continue;               // not handed out (the offsets use the same clamp)
+        else return;
+    }
     if (ctx == 0) {
         for (int i = threadIdx.x; i < hpb * D; i += kThreads) store_out(a.out, a.out_f32, row0 + i, 0.f);
-        return;
+        if constexpr (kClaim) continue;
+        else return;
     }
     const int t_begin = part * P;
     const int t_end = min(t_begin + P, ctx);
     const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
     // Once every block has started, the merge kernel may be scheduled onto
     // free SM slots; it waits for this grid's results before reading them.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if constexpr (!kClaim) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __syncthreads();
 
     const uint64_t policy = pa::l2_evict_first_policy();
@@ -730,11 +824,13 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
 
     WarpState<D> st;
     st.reset();
+    // this warp's stages carry on from earlier items: its k-th tile here is
+    // stage (kg + k) % kStages
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kStages; ++k) {
             const int tile = warp + k * kWarps;
-            if (tile < n_tiles) issue(tile, k);
+            if (tile < n_tiles) issue(tile, (kg + k) % kStages);
         }
     }
     // this warp's tiles; stages issued before consuming local tile k: min(n_mine, k + kStages)
@@ -747,30 +843,35 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
     uint4 app = make_uint4(0, 0, 0, 0);
     if (append && warp == (n_tiles - 1) % kWarps) prefetch_row<D, F8, NK>(a, seq, kvh, lane, app);
     for (int tile = warp; tile < n_tiles; tile += kWarps, ++k) {
-        if (!wait_stage(wbars, k, min(n_mine, k + kStages), lane, a.status, drained)) break;
+        if (!wait_stage(wbars, kg + k, kg + min(n_mine, k + kStages), lane, a.status, drained)) break;
+        const int stg = (kg + k) % kStages;
         if (append && tile == n_tiles - 1) {
             const int pos = ctx - 1;
             int blk = table[(pos >> a.log2_block) - lb0];
             const bool blk_ok = blk >= 0 && blk < a.num_blocks;     // a bad id was flagged when the tile was issued
-            append_row<D, F8, NK>(wring + (k % kStages) * G::kStageBytes, pos - (t_begin + tile * kTile), a, kvh,
-                                  blk_ok ? blk : 0, pos & (B - 1), blk_ok && (NK == 2 || blockIdx.y % a.n_sub == 0),
+            append_row<D, F8, NK>(wring + stg * G::kStageBytes, pos - (t_begin + tile * kTile), a, kvh,
+                                  blk_ok ? blk : 0, pos & (B - 1), blk_ok && (NK == 2 || yb % a.n_sub == 0),
                                   lane, app);
         }
-        const uint32_t ks = pa::smem_addr(wring + (k % kStages) * G::kStageBytes);
+        const uint32_t ks = pa::smem_addr(wring + stg * G::kStageBytes);
         const int nv_ = min(kTile, t_end - (t_begin + tile * kTile));
         if constexpr (F8)
             consume_tile_f8<D, NK>(st, ks, ks + G::kTileBytes, nv_, qbk, c0, c1, lane);
         else
             consume_tile<D>(st, ks, ks + G::kTileBytes, nv_, qb, a.scale_log2, lane);
         __syncwarp();
-        if (lane == 0 && tile + kWarps * kStages < n_tiles) issue(tile + kWarps * kStages, k % kStages);
+        if (lane == 0 && tile + kWarps * kStages < n_tiles) issue(tile + kWarps * kStages, stg);
     }
+    kg += n_mine;
     st.finish_sums();
 
     // ---- merge the 4 warps (exact, as in the block merge) ----------------------
     // Ring no longer in use, unless a timed-out copy may still land in it: then
-    // the block leaves it alone and returns (outputs unspecified, status set).
-    if (!__syncthreads_and(drained ? 1 : 0)) return;
+    // the block leaves it alone and stops (outputs unspecified, status set).
+    if (!__syncthreads_and(drained ? 1 : 0)) {
+        aborted = true;
+        break;
+    }
     float* mw = reinterpret_cast<float*>(ring);        // [warp][8]
     float* lw = mw + kWarps * kHeads;                  // [warp][8]
     float* uw = lw + kWarps * kHeads;                  // [warp][8][D]
@@ -819,6 +920,24 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
             }
         }
     }
+    if constexpr (!kClaim) break;
+    // the next item's copies write the ring, which this one's merge (and
+    // append) wrote through the generic proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if constexpr (kClaim) {
+        // Every block has made its last claim once all have counted themselves
+        // done: the last one leaves both counters at zero for the next call.
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(a.claim + 1, 1) == (int)gridDim.x - 1) {
+                atomicExch(a.claim, 0);
+                atomicExch(a.claim + 1, 0);
+            }
+        }
+    }
+    (void)aborted;
 }
 
 // Fold partitions [0, np) of one (sequence, head) row into (M, Z, U) for
@@ -1015,13 +1134,15 @@ int default_partition(int num_seqs, int n_q_heads, int max_context_len, bool f8_
     return (int)p;
 }
 
-// Workspace layout for max_parts partitions: part_max and part_sum
-// [S][Hq][max_parts] f32, then part_acc [S][Hq][max_parts][D] f32; every
-// section 256-byte aligned.
+// Workspace layout for max_parts partitions: a 256-byte header whose first
+// two int32 are the claim counters (zero between calls), then part_max and
+// part_sum [S][Hq][max_parts] f32, then part_acc [S][Hq][max_parts][D] f32;
+// every section 256-byte aligned.
+constexpr size_t kWsHeader = 256;
 size_t workspace_bytes_for(int num_seqs, int n_q_heads, int d_head, int max_parts) {
     if (max_parts <= 1) return 0;
     const size_t n = (size_t)num_seqs * n_q_heads * max_parts;
-    return 2 * align256(4 * n) + align256(4 * n * d_head);
+    return kWsHeader + 2 * align256(4 * n) + align256(4 * n * d_head);
 }
 
 template <typename K>
@@ -1035,6 +1156,7 @@ int launch(K kernel, dim3 grid, int smem, cudaStream_t st, const CUtensorMap& mk
 int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, void* workspace,
         size_t workspace_bytes, cudaStream_t st, bool f8 = false, bool pair = false) {
     static int attr128[64] = {0}, attr64[64] = {0}, attr128f8[64] = {0}, attr128f8p[64] = {0};
+    static int attr128c[64] = {0}, attr64c[64] = {0}, attr128f8c[64] = {0}, attr128f8pc[64] = {0};
     const int P = a.partition_size;
     a.max_parts = (a.ctx_cap + P - 1) / P;
     if (a.max_parts < 1) a.max_parts = 1;
@@ -1043,6 +1165,8 @@ int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, 
             return PA_ERR_WORKSPACE;
         const size_t n = (size_t)a.num_seqs * a.n_q_heads * a.max_parts;
         uint8_t* w = static_cast<uint8_t*>(workspace);
+        a.claim = reinterpret_cast<int*>(w);
+        w += kWsHeader;
         a.part_max = reinterpret_cast<float*>(w);
         a.part_sum = reinterpret_cast<float*>(w + align256(4 * n));
         a.part_acc = reinterpret_cast<float*>(w + 2 * align256(4 * n));
@@ -1052,11 +1176,32 @@ int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, 
                         : kWarps * kStages * 2 * kTile * d_head * 2;
     const int merge = kWarps * kHeads * (2 + d_head) * 4;          // the warp merge reuses the ring
     const int smem = 1024 + (ring > merge ? ring : merge) + kWarps * kStages * 8 + table_ints * 4;
-    dim3 grid(a.max_parts, pair ? a.n_kv_heads / 2 : a.n_kv_heads * a.n_sub, a.num_seqs);
-    const int rc = f8 ? (pair ? launch(decode_partition_kernel<128, true, 2>, grid, smem, st, mk, mv, a, attr128f8p)
-                              : launch(decode_partition_kernel<128, true>, grid, smem, st, mk, mv, a, attr128f8))
-                      : d_head == 128 ? launch(decode_partition_kernel<128, false>, grid, smem, st, mk, mv, a, attr128)
-                                      : launch(decode_partition_kernel<64, false>, grid, smem, st, mk, mv, a, attr64);
+    dim3 grid(a.max_parts, a.n_units, a.num_seqs);
+    // Many head groups (at least two waves of resident blocks without any
+    // split) and sequences split into partitions: the grid above would hold a
+    // block for every partition up to the longest context in every head
+    // group, most of them empty when the lengths are ragged, and an empty
+    // block still costs a memory round trip.  Instead the resident blocks
+    // claim the (sequence, head group, partition) items that exist.
+    const int per_sm = f8 ? (pair ? PA_DECODE_MIN_BLOCKS_F8 - 1 : PA_DECODE_MIN_BLOCKS_F8) : PA_DECODE_MIN_BLOCKS;
+    const long long slots = (long long)per_sm * sm_count();
+    const long long units = (long long)a.num_seqs * a.n_units;
+    const bool claim = a.max_parts > 1 && a.num_seqs <= kClaimMaxSeqs && units >= 2 * slots;
+    int rc;
+    if (claim) {
+        const int smem_c = smem + (kClaimMaxSeqs + 2 + kWarps) * 4;
+        const long long items = units * a.max_parts;
+        const dim3 grid_c((unsigned)(items < slots ? items : slots));
+        rc = f8 ? (pair ? launch(decode_partition_kernel<128, true, 2, true>, grid_c, smem_c, st, mk, mv, a, attr128f8pc)
+                        : launch(decode_partition_kernel<128, true, 1, true>, grid_c, smem_c, st, mk, mv, a, attr128f8c))
+                : d_head == 128 ? launch(decode_partition_kernel<128, false, 1, true>, grid_c, smem_c, st, mk, mv, a, attr128c)
+                                : launch(decode_partition_kernel<64, false, 1, true>, grid_c, smem_c, st, mk, mv, a, attr64c);
+    } else {
+        rc = f8 ? (pair ? launch(decode_partition_kernel<128, true, 2>, grid, smem, st, mk, mv, a, attr128f8p)
+                        : launch(decode_partition_kernel<128, true>, grid, smem, st, mk, mv, a, attr128f8))
+                : d_head == 128 ? launch(decode_partition_kernel<128, false>, grid, smem, st, mk, mv, a, attr128)
+                                : launch(decode_partition_kernel<64, false>, grid, smem, st, mk, mv, a, attr64);
+    }
     if (rc != PA_OK || a.max_parts <= 1) return rc;
     return launch_merge(true, st, a.out, a.out_f32, a.part_max, a.part_sum, a.part_acc, a.context_lens, a.ctx_cap, P,
                         a.max_parts, a.n_q_heads, a.num_seqs, d_head, 1);
@@ -1143,7 +1288,8 @@ int decode_impl(void* out, int out_dtype, const void* q, const void* k_cache, co
     const long long cap_tbl = (long long)max_blocks_per_seq * block_size;
     a.ctx_cap = (int)(cap_tbl < max_context_len ? cap_tbl : max_context_len);
     a.num_seqs = num_seqs;
-    const long long units = (long long)num_seqs * (pair ? n_kv_heads / 2 : n_kv_heads * n_sub);
+    a.n_units = pair ? n_kv_heads / 2 : n_kv_heads * n_sub;
+    const long long units = (long long)num_seqs * a.n_units;
     a.partition_size = partition_size > 0 ? partition_size
                                           : default_partition(num_seqs, n_q_heads, max_context_len, pair, units);
     a.k_scale = f8 ? k_scale : 1.f;

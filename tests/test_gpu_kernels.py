@@ -277,6 +277,8 @@ def test_split_partials_match_oracle_partition_summaries():
     n = S * Hq * NP
     al = lambda x: (x + 255) // 256 * 256
     w = ws.cpu().numpy()
+    assert not w[:8].any()               # the claim counters in the 256-byte header are left at zero
+    w = w[256:]
     pm = w[:4 * n].view(np.float32).reshape(S, Hq, NP)
     ps = w[al(4 * n):al(4 * n) + 4 * n].view(np.float32).reshape(S, Hq, NP)
     pa_ = w[2 * al(4 * n):2 * al(4 * n) + 4 * n * D].view(np.float32).reshape(S, Hq, NP, D)
