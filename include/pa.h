@@ -98,10 +98,10 @@ const char* pa_status_string(int status);
  * Each sequence is split into partitions of partition_size positions, one
  * thread block per (sequence, group of up to 8 query heads, partition).  A
  * sequence that fits one partition is finished by its block.  When the batch
- * has many head groups (at least two waves of resident blocks) and some
- * sequence spans several partitions, the resident blocks instead claim the
- * (sequence, head group, partition) items that exist, so that no block is
- * spent on the partitions past a short sequence's end.  Otherwise
+ * has many head groups (at least two waves of resident blocks) and
+ * max_context_len spans four partitions or more, the resident blocks
+ * instead claim the (sequence, head group, partition) items that exist, so
+ * that no block is spent on the partitions past a short sequence's end.  Otherwise
  * every block leaves its partition's maximum m, weight sum z and
  * unnormalised weighted value sum u (the statistics of [P2] section 11) in
  * `workspace`, and a second kernel merges them exactly (the "secondary

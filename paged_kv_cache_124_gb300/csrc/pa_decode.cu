@@ -728,6 +728,9 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
     for (;;) {
     int part, seq, yb;
     if constexpr (kClaim) {
+        // claimed once the block is free (claiming the next item while this
+        // one runs measured 4-9 % slower: the block holds it back while
+        // others run out of work)
         __syncthreads();             // pre is complete, the previous item's readers are done
         if (threadIdx.x == 0) claimed[0] = atomicAdd(a.claim, 1);
         __syncthreads();
@@ -1178,15 +1181,18 @@ int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, 
     const int smem = 1024 + (ring > merge ? ring : merge) + kWarps * kStages * 8 + table_ints * 4;
     dim3 grid(a.max_parts, a.n_units, a.num_seqs);
     // Many head groups (at least two waves of resident blocks without any
-    // split) and sequences split into partitions: the grid above would hold a
-    // block for every partition up to the longest context in every head
-    // group, most of them empty when the lengths are ragged, and an empty
-    // block still costs a memory round trip.  Instead the resident blocks
-    // claim the (sequence, head group, partition) items that exist.
+    // split) and contexts of up to four or more partitions: the grid above
+    // would hold a block for every partition up to the longest context in
+    // every head group, most of them empty when the lengths are ragged, and
+    // an empty block still costs a memory round trip.  Instead the resident
+    // blocks claim the (sequence, head group, partition) items that exist.
+    // (With two or three partitions at most there is little to save: claims
+    // cost 6.6 % on 128 sequences of about 2,000 positions, two partitions
+    // each and no empty block.)
     const int per_sm = f8 ? (pair ? PA_DECODE_MIN_BLOCKS_F8 - 1 : PA_DECODE_MIN_BLOCKS_F8) : PA_DECODE_MIN_BLOCKS;
     const long long slots = (long long)per_sm * sm_count();
     const long long units = (long long)a.num_seqs * a.n_units;
-    const bool claim = a.max_parts > 1 && a.num_seqs <= kClaimMaxSeqs && units >= 2 * slots;
+    const bool claim = a.max_parts >= 4 && a.num_seqs <= kClaimMaxSeqs && units >= 2 * slots;
     int rc;
     if (claim) {
         const int smem_c = smem + (kClaimMaxSeqs + 2 + kWarps) * 4;
