@@ -27,7 +27,11 @@
 //    rounding within about 2^-16 relative instead of bf16's 2^-8.
 //  * One thread block of 4 warps per (sequence, head group, partition of
 //    partition_size positions); the hardware hands blocks to SMs as others
-//    finish, which balances ragged batches.  The 4 warps of a block are
+//    finish, which balances ragged batches.  When the head groups alone fill
+//    two waves and the longest context spans four partitions or more, most
+//    of that grid would be empty partitions of short sequences, so instead
+//    the resident blocks claim the (sequence, head group, partition) items
+//    that exist from a counter in the workspace.  The 4 warps of a block are
 //    merged in shared memory; a sequence that fits one partition is written
 //    directly.  Otherwise each block leaves its partition's statistics
 //    (m, z, u) in the workspace and lse_merge_kernel -- launched as a
