@@ -1107,9 +1107,16 @@ int ilog2(int x) {
 // Positions per partition when the caller passes 0.  `units` is the number of
 // (sequence, head group) thread blocks per partition index (0: unknown).
 // When the units alone fill two waves of resident blocks, sequences are not
-// split for parallelism: 1536 positions, so that most short sequences of a
-// large batch finish in their own block without a merge (measured best on
-// 256 mixed-length sequences, 4-5 % faster than 1024).  Otherwise at least
+// split for parallelism.  If the longest context then spans at least four
+// partitions of 1024 positions, the resident blocks claim the items that
+// exist (see run()), so no block is spent on an empty partition and smaller
+// partitions balance the blocks' loads better: 1024 (on 256 mixed-length
+// sequences, 32 layers: FP8 1024 / 768 / 1536 / 2048 positions 3.19 / 3.21 /
+// 3.25 / 3.40 ms per step, bf16 5.24 / 5.23 / 5.32 / 5.47 ms).  Otherwise
+// 1536, so that most short sequences of a large batch finish in their own
+// block without a merge and the one-block-per-partition grid holds few empty
+// blocks (4-5 % faster than 1024 on that batch before its blocks claimed
+// work).  Otherwise at least
 // 256 and at most 1024: enough thread blocks for about two waves of 3 blocks
 // per SM (counting 4 query heads per block); for the FP8 kernel that covers
 // two KV heads per block (8 query heads, 3 blocks per SM), about three waves,
@@ -1118,7 +1125,7 @@ int ilog2(int x) {
 int default_partition(int num_seqs, int n_q_heads, int max_context_len, bool f8_pair = false,
                       long long units = 0) {
     const long long slots = (long long)(f8_pair ? PA_DECODE_MIN_BLOCKS_F8 - 1 : PA_DECODE_MIN_BLOCKS) * sm_count();
-    if (units > 0 && slots > 0 && units >= 2 * slots) return 1536;
+    if (units > 0 && slots > 0 && units >= 2 * slots) return max_context_len >= 4 * 1024 ? 1024 : 1536;
     const long long work = (long long)num_seqs * n_q_heads * max_context_len;
     const long long target = f8_pair ? 8LL * 3 * (PA_DECODE_MIN_BLOCKS_F8 - 1) * sm_count()
                                      : 4LL * 2 * PA_DECODE_MIN_BLOCKS * sm_count();
