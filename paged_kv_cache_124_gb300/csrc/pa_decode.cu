@@ -1203,7 +1203,9 @@ int run(DecodeArgs a, const CUtensorMap& mk, const CUtensorMap& mv, int d_head, 
     const int per_sm = f8 ? (pair ? PA_DECODE_MIN_BLOCKS_F8 - 1 : PA_DECODE_MIN_BLOCKS_F8) : PA_DECODE_MIN_BLOCKS;
     const long long slots = (long long)per_sm * sm_count();
     const long long units = (long long)a.num_seqs * a.n_units;
-    const bool claim = a.max_parts >= 4 && a.num_seqs <= kClaimMaxSeqs && units >= 2 * slots;
+    // (items and claims are counted in int32)
+    const bool claim = a.max_parts >= 4 && a.num_seqs <= kClaimMaxSeqs && units >= 2 * slots &&
+                       units * a.max_parts + slots < 0x40000000LL;
     int rc;
     if (claim) {
         const int smem_c = smem + (kClaimMaxSeqs + 2 + kWarps) * 4;
