@@ -346,6 +346,27 @@ def test_reshape_and_cache_writes_only_its_slots():
     assert np.array_equal(k2[mask], k[mask]) and np.array_equal(v2[mask], v[mask])
 
 
+def test_swap_blocks_moves_whole_blocks():
+    """[P1] section 19, item 4: a swapped block moves whole, K and V, from
+    one pool to the other; each pair names (source block, destination
+    block), the other blocks are untouched, and swapping back into other
+    blocks restores the payload."""
+    rng = np.random.default_rng(9)
+    dev_k = rng.integers(0, 1 << 16, size=(6, 2, 4, 3), dtype=np.uint16)
+    dev_v = rng.integers(0, 1 << 16, size=(6, 2, 4, 3), dtype=np.uint16)
+    host_k = np.zeros((4, 2, 4, 3), dtype=np.uint16)
+    host_v = np.zeros((4, 2, 4, 3), dtype=np.uint16)
+    C.swap_blocks(host_k, host_v, dev_k, dev_v, [(5, 0), (2, 3)])
+    assert np.array_equal(host_k[0], dev_k[5]) and np.array_equal(host_v[0], dev_v[5])
+    assert np.array_equal(host_k[3], dev_k[2]) and np.array_equal(host_v[3], dev_v[2])
+    assert not host_k[1:3].any() and not host_v[1:3].any()
+    back_k = np.zeros_like(dev_k)
+    back_v = np.zeros_like(dev_v)
+    C.swap_blocks(back_k, back_v, host_k, host_v, [(0, 1), (3, 4)])
+    assert np.array_equal(back_k[1], dev_k[5]) and np.array_equal(back_v[4], dev_v[2])
+    assert not back_k[[0, 2, 3, 5]].any() and not back_v[[0, 2, 3, 5]].any()
+
+
 def test_copy_blocks_cow_trace_payload():
     """[P1] section 16: after the copy, block 13 holds positions 32..34 of the
     shared tail; the other blocks are untouched, in every layer."""

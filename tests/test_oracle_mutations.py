@@ -67,6 +67,12 @@ MUTANTS = [
     ("attention", "return e @ np.asarray(V, dtype=np.float64), e.sum()",
      "return e @ np.asarray(V, dtype=np.float64), e.max()", "page normaliser is the largest term"),
     ("attention", "<< np.uint32(16)", "<< np.uint32(15)", "bf16 pattern shifted one bit short"),
+    ("attention", "stop = min(start + partition_size, len(s))", "stop = min(start + partition_size - 1, len(s))",
+     "each partition drops its last position"),
+    ("attention", "V[:, b * block_size: b * block_size + valid, :] = to_f64(v_cache[phys, :, :valid, :])",
+     "V[:, b * block_size: b * block_size + valid, :] = to_f64(k_cache[phys, :, :valid, :])", "values gathered from the key pool"),
+    ("attention", "K_dense[s, h, :ctx], V_dense[s, h, :ctx]", "K_dense[s, h, :ctx], V_dense[s, h, 1:ctx + 1]",
+     "dense reference reads values one position late"),
     # quant: the E4M3 format definition and the rounding rule
     ("quant", "(1.0 + m / 8.0) * 2.0 ** (e - 7)", "(1.0 + m / 8.0) * 2.0 ** (e - 8)", "exponent bias 8"),
     ("quant", "m * 2.0 ** -9", "m * 2.0 ** -10", "subnormal step 2^-10"),
@@ -80,6 +86,8 @@ MUTANTS = [
      "sign bit in the wrong place"),
     ("quant", "np.asarray(x, dtype=np.float32) / np.float32(scale)", "np.asarray(x, dtype=np.float64) / float(scale)",
      "division in float64 instead of float32"),
+    ("quant", "return e4m3_to_f64(codes) * float(np.float32(scale))", "return e4m3_to_f64(codes) / float(np.float32(scale))",
+     "dequantisation divides by the scale"),
     # cache_ops: slot arithmetic and copy direction
     ("cache_ops", "block, offset = divmod(int(slot), block_size)", "offset, block = divmod(int(slot), block_size)",
      "block and offset swapped"),
@@ -88,6 +96,7 @@ MUTANTS = [
     ("cache_ops", "k_out[layer][dst] = k_out[layer][src]", "k_out[layer][src] = k_out[layer][dst]",
      "copy direction swapped for K"),
     ("cache_ops", "v_out[layer][dst] = v_out[layer][src]", "pass", "V not copied"),
+    ("cache_ops", "        dst_k[dst] = src_k[src]\n", "        dst_k[src] = src_k[dst]\n", "swap copies K in the wrong direction"),
     # sizing: the closed forms
     ("sizing", "return 2 * n_layers * n_kv_heads * d_head * elem_bytes",
      "return n_layers * n_kv_heads * d_head * elem_bytes", "K only, V forgotten"),
