@@ -728,209 +728,207 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     int kg = 0;                      // this warp's stages consumed by earlier items
-    bool aborted = false;
     for (;;) {
-    int part, seq, yb;
-    if constexpr (kClaim) {
-        // claimed once the block is free (claiming the next item while this
-        // one runs measured 4-9 % slower: the block holds it back while
-        // others run out of work)
-        __syncthreads();             // pre is complete, the previous item's readers are done
-        if (threadIdx.x == 0) claimed[0] = atomicAdd(a.claim, 1);
-        __syncthreads();
-        const int v = claimed[0];
-        if (v >= pre[a.num_seqs]) break;
-        int lo = 0, hi = a.num_seqs - 1;              // the sequence s with pre[s] <= v < pre[s + 1]
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (pre[mid] <= v) lo = mid; else hi = mid - 1;
-        }
-        seq = lo;
-        const int np_ = (pre[seq + 1] - pre[seq]) / a.n_units;
-        const int r = v - pre[seq];
-        yb = r / np_;
-        part = r - yb * np_;
-    } else {
-        part = blockIdx.x;
-        seq = blockIdx.z;
-        yb = blockIdx.y;
-    }
-    const int kvh = NK == 1 ? yb / a.n_sub : yb * NK;
-    const int hpb = a.heads_per_block;
-    const int qh0 = kvh * a.group + (yb % a.n_sub) * hpb;
-
-    // Independent loads first: the context length, a speculative slice of the
-    // block table (this partition's entries, read before the length is known)
-    // and q; one memory round trip instead of three.
-    const int lb0 = (part * P) >> a.log2_block;
-    const int32_t* trow = a.block_tables + (size_t)seq * a.max_blocks_per_seq;
-    const int n_spec = max(0, min(P >> a.log2_block, a.max_blocks_per_seq - lb0));
-    int ctx = a.context_lens[seq];
-    for (int i = threadIdx.x; i < n_spec; i += kThreads) table[i] = trow[lb0 + i];
-    const size_t row0 = ((size_t)seq * a.n_q_heads + qh0) * D;   // q / out offset of the block's first head
-    uint32_t qb[G::kSteps][2];
-    uint32_t qbk[NK][G::kSteps][2];      // FP8: q per KV head of the tile (the other head's columns zero)
-    float c0 = 0.f, c1 = 0.f;
-    if constexpr (F8) {
-        const float sh = load_q_f8<D>(qb, a.q + row0, hpb, lane);
-        const int h0_ = 2 * (lane & 3);
-        const float sc = a.scale_log2 * a.k_scale;
-        c0 = sc / __shfl_sync(0xffffffffu, sh, 4 * h0_);
-        c1 = sc / __shfl_sync(0xffffffffu, sh, 4 * h0_ + 4);
-#pragma unroll
-        for (int hh = 0; hh < NK; ++hh) {
-            const bool mine = NK == 1 || ((lane >> 2) >> 2) == hh;     // B column g = query head g
-#pragma unroll
-            for (int k = 0; k < G::kSteps; ++k) {
-                qbk[hh][k][0] = mine ? qb[k][0] : 0u;
-                qbk[hh][k][1] = mine ? qb[k][1] : 0u;
+        int part, seq, yb;
+        if constexpr (kClaim) {
+            // claimed once the block is free (claiming the next item while this
+            // one runs measured 4-9 % slower: the block holds it back while
+            // others run out of work)
+            __syncthreads();             // pre is complete, the previous item's readers are done
+            if (threadIdx.x == 0) claimed[0] = atomicAdd(a.claim, 1);
+            __syncthreads();
+            const int v = claimed[0];
+            if (v >= pre[a.num_seqs]) break;
+            int lo = 0, hi = a.num_seqs - 1;              // the sequence s with pre[s] <= v < pre[s + 1]
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (pre[mid] <= v) lo = mid; else hi = mid - 1;
             }
-        }
-    } else {
-        load_q<D>(qb, a.q + row0, hpb, lane);
-    }
-    if (!kClaim && threadIdx.x == 0) {
-        for (int i = 0; i < kWarps * kStages; ++i) pa::mbar_init(&bars[i], 1);
-        pa::fence_mbar_init();
-    }
-
-    const bool ctx_ok = ctx >= 0 && ctx <= a.ctx_cap;
-    if (!ctx_ok) {
-        if (threadIdx.x == 0 && part == 0 && yb == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
-        ctx = ctx < 0 ? 0 : a.ctx_cap;
-    }
-    const int nparts = (ctx + P - 1) / P;
-    if (part >= (nparts > 0 ? nparts : 1)) {
-        if constexpr (kClaim) continue;               // not handed out (the offsets use the same clamp)
-        else return;
-    }
-    if (ctx == 0) {
-        for (int i = threadIdx.x; i < hpb * D; i += kThreads) store_out(a.out, a.out_f32, row0 + i, 0.f);
-        if constexpr (kClaim) continue;
-        else return;
-    }
-    const int t_begin = part * P;
-    const int t_end = min(t_begin + P, ctx);
-    const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
-    // Once every block has started, the merge kernel may be scheduled onto
-    // free SM slots; it waits for this grid's results before reading them.
-    if constexpr (!kClaim) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __syncthreads();
-
-    const uint64_t policy = pa::l2_evict_first_policy();
-    uint64_t* wbars = bars + warp * kStages;
-    uint8_t* wring = ring + warp * kStages * G::kStageBytes;
-    auto issue = [&](int tile, int stage) {
-        const int t0 = t_begin + tile * kTile;
-        const int nv = min(kTile, t_end - t0);
-        const int e0 = (t0 >> a.log2_block) - lb0;
-        const int blk1 = (B < kTile && nv > B) ? table[e0 + 1] : 0;
-        issue_tile<D, F8, NK>(wring + stage * G::kStageBytes, &wbars[stage], &tmap_k, &tmap_v, table[e0], blk1,
-                          t0 & (B - 1), nv, kvh, a, policy);
-    };
-
-    WarpState<D> st;
-    st.reset();
-    // this warp's stages carry on from earlier items: its k-th tile here is
-    // stage (kg + k) % kStages
-    if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < kStages; ++k) {
-            const int tile = warp + k * kWarps;
-            if (tile < n_tiles) issue(tile, (kg + k) % kStages);
-        }
-    }
-    // this warp's tiles; stages issued before consuming local tile k: min(n_mine, k + kStages)
-    const int n_mine = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
-    bool drained = true;
-    int k = 0;
-    // the fused append lands in the tile holding position ctx - 1 (the last
-    // tile of the last partition); a clamped context appends nothing
-    const bool append = a.k_new != nullptr && ctx_ok && t_end == ctx;
-    uint4 app = make_uint4(0, 0, 0, 0);
-    if (append && warp == (n_tiles - 1) % kWarps) prefetch_row<D, F8, NK>(a, seq, kvh, lane, app);
-    for (int tile = warp; tile < n_tiles; tile += kWarps, ++k) {
-        if (!wait_stage(wbars, kg + k, kg + min(n_mine, k + kStages), lane, a.status, drained)) break;
-        const int stg = (kg + k) % kStages;
-        if (append && tile == n_tiles - 1) {
-            const int pos = ctx - 1;
-            int blk = table[(pos >> a.log2_block) - lb0];
-            const bool blk_ok = blk >= 0 && blk < a.num_blocks;     // a bad id was flagged when the tile was issued
-            append_row<D, F8, NK>(wring + stg * G::kStageBytes, pos - (t_begin + tile * kTile), a, kvh,
-                                  blk_ok ? blk : 0, pos & (B - 1), blk_ok && (NK == 2 || yb % a.n_sub == 0),
-                                  lane, app);
-        }
-        const uint32_t ks = pa::smem_addr(wring + stg * G::kStageBytes);
-        const int nv_ = min(kTile, t_end - (t_begin + tile * kTile));
-        if constexpr (F8)
-            consume_tile_f8<D, NK>(st, ks, ks + G::kTileBytes, nv_, qbk, c0, c1, lane);
-        else
-            consume_tile<D>(st, ks, ks + G::kTileBytes, nv_, qb, a.scale_log2, lane);
-        __syncwarp();
-        if (lane == 0 && tile + kWarps * kStages < n_tiles) issue(tile + kWarps * kStages, stg);
-    }
-    kg += n_mine;
-    st.finish_sums();
-
-    // ---- merge the 4 warps (exact, as in the block merge) ----------------------
-    // Ring no longer in use, unless a timed-out copy may still land in it: then
-    // the block leaves it alone and stops (outputs unspecified, status set).
-    if (!__syncthreads_and(drained ? 1 : 0)) {
-        aborted = true;
-        break;
-    }
-    float* mw = reinterpret_cast<float*>(ring);        // [warp][8]
-    float* lw = mw + kWarps * kHeads;                  // [warp][8]
-    float* uw = lw + kWarps * kHeads;                  // [warp][8][D]
-    const int g = lane >> 2, h0 = 2 * (lane & 3);
-    if (g == 0) {
-        mw[warp * kHeads + h0] = st.m0;
-        mw[warp * kHeads + h0 + 1] = st.m1;
-        lw[warp * kHeads + h0] = st.l0;
-        lw[warp * kHeads + h0 + 1] = st.l1;
-    }
-    // rows g and g + 8 of m-tile m are d = 16 m + g and 16 m + g + 8 (FP8:
-    // 16 m + 2 g and 16 m + 2 g + 1)
-    constexpr int kRow2 = F8 ? 1 : 8;
-#pragma unroll
-    for (int m = 0; m < G::kSteps; ++m) {
-        const int drow = F8 ? 16 * m + 2 * g : 16 * m + g;
-        float* u0 = uw + (warp * kHeads + h0) * D + drow;
-        float* u1 = u0 + D;
-        u0[0] = st.acc[m][0];
-        u1[0] = st.acc[m][1];
-        u0[kRow2] = st.acc[m][2];
-        u1[kRow2] = st.acc[m][3];
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < hpb * D; idx += kThreads) {
-        const int h = idx / D;
-        const int d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * kHeads + h]);
-        float Z = 0.f, U = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float f = fast_exp2(mw[w * kHeads + h] - M);
-            Z += f * lw[w * kHeads + h];
-            U += f * uw[(w * kHeads + h) * D + d];
-        }
-        if (nparts == 1) {
-            store_out(a.out, a.out_f32, row0 + idx, U * a.u_scale / Z);
+            seq = lo;
+            const int np_ = (pre[seq + 1] - pre[seq]) / a.n_units;
+            const int r = v - pre[seq];
+            yb = r / np_;
+            part = r - yb * np_;
         } else {
-            const size_t pi = ((size_t)seq * a.n_q_heads + qh0 + h) * a.max_parts + part;
-            a.part_acc[pi * D + d] = U * a.u_scale;
-            if (d == 0) {
-                a.part_max[pi] = M * kLn2;      // back to natural-log units
-                a.part_sum[pi] = Z;
+            part = blockIdx.x;
+            seq = blockIdx.z;
+            yb = blockIdx.y;
+        }
+        const int kvh = NK == 1 ? yb / a.n_sub : yb * NK;
+        const int hpb = a.heads_per_block;
+        const int qh0 = kvh * a.group + (yb % a.n_sub) * hpb;
+
+        // Independent loads first: the context length, a speculative slice of the
+        // block table (this partition's entries, read before the length is known)
+        // and q; one memory round trip instead of three.
+        const int lb0 = (part * P) >> a.log2_block;
+        const int32_t* trow = a.block_tables + (size_t)seq * a.max_blocks_per_seq;
+        const int n_spec = max(0, min(P >> a.log2_block, a.max_blocks_per_seq - lb0));
+        int ctx = a.context_lens[seq];
+        for (int i = threadIdx.x; i < n_spec; i += kThreads) table[i] = trow[lb0 + i];
+        const size_t row0 = ((size_t)seq * a.n_q_heads + qh0) * D;   // q / out offset of the block's first head
+        uint32_t qb[G::kSteps][2];
+        uint32_t qbk[NK][G::kSteps][2];      // FP8: q per KV head of the tile (the other head's columns zero)
+        float c0 = 0.f, c1 = 0.f;
+        if constexpr (F8) {
+            const float sh = load_q_f8<D>(qb, a.q + row0, hpb, lane);
+            const int h0_ = 2 * (lane & 3);
+            const float sc = a.scale_log2 * a.k_scale;
+            c0 = sc / __shfl_sync(0xffffffffu, sh, 4 * h0_);
+            c1 = sc / __shfl_sync(0xffffffffu, sh, 4 * h0_ + 4);
+#pragma unroll
+            for (int hh = 0; hh < NK; ++hh) {
+                const bool mine = NK == 1 || ((lane >> 2) >> 2) == hh;     // B column g = query head g
+#pragma unroll
+                for (int k = 0; k < G::kSteps; ++k) {
+                    qbk[hh][k][0] = mine ? qb[k][0] : 0u;
+                    qbk[hh][k][1] = mine ? qb[k][1] : 0u;
+                }
+            }
+        } else {
+            load_q<D>(qb, a.q + row0, hpb, lane);
+        }
+        if (!kClaim && threadIdx.x == 0) {
+            for (int i = 0; i < kWarps * kStages; ++i) pa::mbar_init(&bars[i], 1);
+            pa::fence_mbar_init();
+        }
+
+        const bool ctx_ok = ctx >= 0 && ctx <= a.ctx_cap;
+        if (!ctx_ok) {
+            if (threadIdx.x == 0 && part == 0 && yb == 0) pa::set_status(a.status, PA_DEV_BAD_CONTEXT);
+            ctx = ctx < 0 ? 0 : a.ctx_cap;
+        }
+        const int nparts = (ctx + P - 1) / P;
+        if (part >= (nparts > 0 ? nparts : 1)) {
+            if constexpr (kClaim) continue;               // not handed out (the offsets use the same clamp)
+            else return;
+        }
+        if (ctx == 0) {
+            for (int i = threadIdx.x; i < hpb * D; i += kThreads) store_out(a.out, a.out_f32, row0 + i, 0.f);
+            if constexpr (kClaim) continue;
+            else return;
+        }
+        const int t_begin = part * P;
+        const int t_end = min(t_begin + P, ctx);
+        const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+        // Once every block has started, the merge kernel may be scheduled onto
+        // free SM slots; it waits for this grid's results before reading them.
+        if constexpr (!kClaim) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        __syncthreads();
+
+        const uint64_t policy = pa::l2_evict_first_policy();
+        uint64_t* wbars = bars + warp * kStages;
+        uint8_t* wring = ring + warp * kStages * G::kStageBytes;
+        auto issue = [&](int tile, int stage) {
+            const int t0 = t_begin + tile * kTile;
+            const int nv = min(kTile, t_end - t0);
+            const int e0 = (t0 >> a.log2_block) - lb0;
+            const int blk1 = (B < kTile && nv > B) ? table[e0 + 1] : 0;
+            issue_tile<D, F8, NK>(wring + stage * G::kStageBytes, &wbars[stage], &tmap_k, &tmap_v, table[e0], blk1,
+                              t0 & (B - 1), nv, kvh, a, policy);
+        };
+
+        WarpState<D> st;
+        st.reset();
+        // this warp's stages carry on from earlier items: its k-th tile here is
+        // stage (kg + k) % kStages
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < kStages; ++k) {
+                const int tile = warp + k * kWarps;
+                if (tile < n_tiles) issue(tile, (kg + k) % kStages);
             }
         }
-    }
-    if constexpr (!kClaim) break;
-    // the next item's copies write the ring, which this one's merge (and
-    // append) wrote through the generic proxy
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // this warp's tiles; stages issued before consuming local tile k: min(n_mine, k + kStages)
+        const int n_mine = warp < n_tiles ? (n_tiles - warp + kWarps - 1) / kWarps : 0;
+        bool drained = true;
+        int k = 0;
+        // the fused append lands in the tile holding position ctx - 1 (the last
+        // tile of the last partition); a clamped context appends nothing
+        const bool append = a.k_new != nullptr && ctx_ok && t_end == ctx;
+        uint4 app = make_uint4(0, 0, 0, 0);
+        if (append && warp == (n_tiles - 1) % kWarps) prefetch_row<D, F8, NK>(a, seq, kvh, lane, app);
+        for (int tile = warp; tile < n_tiles; tile += kWarps, ++k) {
+            if (!wait_stage(wbars, kg + k, kg + min(n_mine, k + kStages), lane, a.status, drained)) break;
+            const int stg = (kg + k) % kStages;
+            if (append && tile == n_tiles - 1) {
+                const int pos = ctx - 1;
+                int blk = table[(pos >> a.log2_block) - lb0];
+                const bool blk_ok = blk >= 0 && blk < a.num_blocks;     // a bad id was flagged when the tile was issued
+                append_row<D, F8, NK>(wring + stg * G::kStageBytes, pos - (t_begin + tile * kTile), a, kvh,
+                                      blk_ok ? blk : 0, pos & (B - 1), blk_ok && (NK == 2 || yb % a.n_sub == 0),
+                                      lane, app);
+            }
+            const uint32_t ks = pa::smem_addr(wring + stg * G::kStageBytes);
+            const int nv_ = min(kTile, t_end - (t_begin + tile * kTile));
+            if constexpr (F8)
+                consume_tile_f8<D, NK>(st, ks, ks + G::kTileBytes, nv_, qbk, c0, c1, lane);
+            else
+                consume_tile<D>(st, ks, ks + G::kTileBytes, nv_, qb, a.scale_log2, lane);
+            __syncwarp();
+            if (lane == 0 && tile + kWarps * kStages < n_tiles) issue(tile + kWarps * kStages, stg);
+        }
+        kg += n_mine;
+        st.finish_sums();
+
+        // ---- merge the 4 warps (exact, as in the block merge) ----------------------
+        // Ring no longer in use, unless a timed-out copy may still land in it: then
+        // the block leaves it alone and stops (outputs unspecified, status set).
+        if (!__syncthreads_and(drained ? 1 : 0)) {
+            break;
+        }
+        float* mw = reinterpret_cast<float*>(ring);        // [warp][8]
+        float* lw = mw + kWarps * kHeads;                  // [warp][8]
+        float* uw = lw + kWarps * kHeads;                  // [warp][8][D]
+        const int g = lane >> 2, h0 = 2 * (lane & 3);
+        if (g == 0) {
+            mw[warp * kHeads + h0] = st.m0;
+            mw[warp * kHeads + h0 + 1] = st.m1;
+            lw[warp * kHeads + h0] = st.l0;
+            lw[warp * kHeads + h0 + 1] = st.l1;
+        }
+        // rows g and g + 8 of m-tile m are d = 16 m + g and 16 m + g + 8 (FP8:
+        // 16 m + 2 g and 16 m + 2 g + 1)
+        constexpr int kRow2 = F8 ? 1 : 8;
+#pragma unroll
+        for (int m = 0; m < G::kSteps; ++m) {
+            const int drow = F8 ? 16 * m + 2 * g : 16 * m + g;
+            float* u0 = uw + (warp * kHeads + h0) * D + drow;
+            float* u1 = u0 + D;
+            u0[0] = st.acc[m][0];
+            u1[0] = st.acc[m][1];
+            u0[kRow2] = st.acc[m][2];
+            u1[kRow2] = st.acc[m][3];
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < hpb * D; idx += kThreads) {
+            const int h = idx / D;
+            const int d = idx % D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[w * kHeads + h]);
+            float Z = 0.f, U = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float f = fast_exp2(mw[w * kHeads + h] - M);
+                Z += f * lw[w * kHeads + h];
+                U += f * uw[(w * kHeads + h) * D + d];
+            }
+            if (nparts == 1) {
+                store_out(a.out, a.out_f32, row0 + idx, U * a.u_scale / Z);
+            } else {
+                const size_t pi = ((size_t)seq * a.n_q_heads + qh0 + h) * a.max_parts + part;
+                a.part_acc[pi * D + d] = U * a.u_scale;
+                if (d == 0) {
+                    a.part_max[pi] = M * kLn2;      // back to natural-log units
+                    a.part_sum[pi] = Z;
+                }
+            }
+        }
+        if constexpr (!kClaim) break;
+        // the next item's copies write the ring, which this one's merge (and
+        // append) wrote through the generic proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if constexpr (kClaim) {
         // Every block has made its last claim once all have counted themselves
@@ -944,7 +942,6 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
             }
         }
     }
-    (void)aborted;
 }
 
 // Fold partitions [0, np) of one (sequence, head) row into (M, Z, U) for
