@@ -1307,8 +1307,9 @@ int prefill_impl(void* out, int out_dtype, const void* q, const void* k_cache, c
                  size_t workspace_bytes, int32_t* sched_dev, int32_t* status_dev, void* stream, bool f8,
                  float k_scale, float v_scale) {
     if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || num_blocks <= 0 || max_blocks_per_seq < 0 ||
-        n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
+        n_q_heads <= 0 || n_kv_heads <= 0)
         return PA_ERR_INVALID_ARG;
+    if (n_q_heads % n_kv_heads != 0) return PA_ERR_UNSUPPORTED;         // as pa_decode
     if (out_dtype != PA_DTYPE_BF16 && out_dtype != PA_DTYPE_F32) return PA_ERR_INVALID_ARG;
     if (f8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !(k_scale < INFINITY) || !(v_scale < INFINITY)))
         return PA_ERR_INVALID_ARG;

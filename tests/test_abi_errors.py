@@ -1,0 +1,122 @@
+"""Host-side argument checks of the C ABI (include/pa.h: host-detected errors
+are returned before anything is enqueued), called through the raw entry
+points with stand-in device addresses that are never dereferenced: every
+case here is rejected before the library makes its first CUDA call, so no
+GPU is needed.  Plus the binding's refusal of host tensors.  CPU only."""
+
+import pytest
+import torch
+
+from paged_kv_cache_124_gb300 import api
+
+L = api._lib
+A = 0x100000            # a 256-byte-aligned stand-in address (never dereferenced)
+
+
+def decode(**kw):
+    a = dict(out=A, out_dtype=api.PA_DTYPE_BF16, q=A, k=A, v=A, tables=A, ctx=A, block_size=16, scale=0.088,
+             hq=32, hkv=8, d=128, num_seqs=4, max_blocks=8, num_blocks=64, max_ctx=128, partition=0, ws=None,
+             ws_bytes=0, status=None)
+    a.update(kw)
+    return L.pa_decode(a["out"], a["out_dtype"], a["q"], a["k"], a["v"], a["tables"], a["ctx"], a["block_size"],
+                       a["scale"], a["hq"], a["hkv"], a["d"], a["num_seqs"], a["max_blocks"], a["num_blocks"],
+                       a["max_ctx"], a["partition"], a["ws"], a["ws_bytes"], a["status"], None)
+
+
+def decode_fp8(**kw):
+    a = dict(out=A, out_dtype=api.PA_DTYPE_F32, q=A, k=A, v=A, tables=A, ctx=A, block_size=16, scale=0.088,
+             k_scale=0.01, v_scale=0.01, hq=32, hkv=8, d=128, num_seqs=4, max_blocks=8, num_blocks=64, max_ctx=128,
+             partition=0)
+    a.update(kw)
+    return L.pa_decode_fp8(a["out"], a["out_dtype"], a["q"], a["k"], a["v"], a["tables"], a["ctx"],
+                           a["block_size"], a["scale"], a["k_scale"], a["v_scale"], a["hq"], a["hkv"], a["d"],
+                           a["num_seqs"], a["max_blocks"], a["num_blocks"], a["max_ctx"], a["partition"], None, 0,
+                           None, None)
+
+
+def prefill(**kw):
+    a = dict(out=A, out_dtype=api.PA_DTYPE_BF16, q=A, k=A, v=A, tables=A, max_blocks=8, qs=A, ctx=A, num_seqs=2,
+             num_tokens=100, max_q=64, num_blocks=64, block_size=16, scale=0.088, hq=32, hkv=8, d=128, ws=A,
+             ws_bytes=1 << 30, sched=None)
+    a.update(kw)
+    return L.pa_prefill(a["out"], a["out_dtype"], a["q"], a["k"], a["v"], a["tables"], a["max_blocks"], a["qs"],
+                        a["ctx"], a["num_seqs"], a["num_tokens"], a["max_q"], a["num_blocks"], a["block_size"],
+                        a["scale"], a["hq"], a["hkv"], a["d"], a["ws"], a["ws_bytes"], a["sched"], None, None)
+
+
+def reshape(**kw):
+    a = dict(k_cache=A, v_cache=A, k=A, v=A, slots=A, num_tokens=4, hkv=8, d=128, block_size=16, num_blocks=64)
+    a.update(kw)
+    return L.pa_reshape_and_cache(a["k_cache"], a["v_cache"], a["k"], a["v"], a["slots"], a["num_tokens"], a["hkv"],
+                                  a["d"], a["block_size"], a["num_blocks"], None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(num_seqs=0), api.PA_OK),                                    # nothing to do, nothing read
+    (dict(num_seqs=-1), api.PA_ERR_INVALID_ARG),
+    (dict(out_dtype=7), api.PA_ERR_INVALID_ARG),
+    (dict(out=None), api.PA_ERR_INVALID_ARG),
+    (dict(ctx=None), api.PA_ERR_INVALID_ARG),
+    (dict(block_size=12), api.PA_ERR_UNSUPPORTED),
+    (dict(d=96), api.PA_ERR_UNSUPPORTED),
+    (dict(hq=12, hkv=8), api.PA_ERR_UNSUPPORTED),                     # not a whole group per KV head
+    (dict(hq=32, hkv=1), api.PA_ERR_UNSUPPORTED),                     # G = 32 > 16
+    (dict(q=A + 8), api.PA_ERR_MISALIGNED),
+    (dict(partition=100), api.PA_ERR_INVALID_ARG),                    # not a multiple of 64
+    (dict(partition=16384), api.PA_ERR_INVALID_ARG),                  # above 8192
+    (dict(ws=A + 16, ws_bytes=1 << 20), api.PA_ERR_WORKSPACE),        # workspace not 256-byte aligned
+    (dict(scale=float("nan")), api.PA_ERR_INVALID_ARG),
+])
+def test_decode_host_checks(kw, want):
+    assert decode(**kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(k_scale=0.0), api.PA_ERR_INVALID_ARG),
+    (dict(v_scale=float("inf")), api.PA_ERR_INVALID_ARG),
+    (dict(d=64), api.PA_ERR_UNSUPPORTED),                             # E4M3 caches: d_head 128 only
+    (dict(num_seqs=0), api.PA_OK),
+])
+def test_decode_fp8_host_checks(kw, want):
+    assert decode_fp8(**kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(num_seqs=0), api.PA_OK),
+    (dict(num_tokens=0), api.PA_OK),
+    (dict(hq=12, hkv=8), api.PA_ERR_UNSUPPORTED),                     # not a whole group per KV head, as decode
+    (dict(hq=24, hkv=8), api.PA_ERR_UNSUPPORTED),                     # G = 3 does not divide a 128-row tile
+    (dict(out_dtype=9), api.PA_ERR_INVALID_ARG),
+    (dict(block_size=64), api.PA_ERR_UNSUPPORTED),
+    (dict(qs=None), api.PA_ERR_INVALID_ARG),
+    (dict(max_blocks=0), api.PA_ERR_INVALID_ARG),
+    (dict(num_seqs=70000), api.PA_ERR_UNSUPPORTED),
+    (dict(ws=None), api.PA_ERR_WORKSPACE),
+    (dict(ws_bytes=16), api.PA_ERR_WORKSPACE),
+    (dict(out=A + 8), api.PA_ERR_MISALIGNED),
+    (dict(sched=A + 2), api.PA_ERR_MISALIGNED),
+])
+def test_prefill_host_checks(kw, want):
+    assert prefill(**kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(num_tokens=0), api.PA_OK),
+    (dict(num_tokens=-1), api.PA_ERR_INVALID_ARG),
+    (dict(block_size=12), api.PA_ERR_UNSUPPORTED),
+    (dict(slots=None), api.PA_ERR_INVALID_ARG),
+    (dict(k=A + 4), api.PA_ERR_MISALIGNED),
+])
+def test_reshape_and_cache_host_checks(kw, want):
+    assert reshape(**kw) == want
+
+
+def test_binding_refuses_host_tensors():
+    q = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 2, 16, 64, dtype=torch.bfloat16)
+    tables = torch.zeros(2, 2, dtype=torch.int32)
+    ctx = torch.ones(2, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.pa_decode(torch.empty_like(q), q, kc, kc, tables, ctx, 16, 0.125, 4, 2, 64, 16)
+    with pytest.raises(ValueError, match="CUDA"):
+        api.pa_reshape_and_cache(kc, kc, q[:, :2], q[:, :2], torch.zeros(2, dtype=torch.int64))
