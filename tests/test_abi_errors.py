@@ -4,6 +4,8 @@ points with stand-in device addresses that are never dereferenced: every
 case here is rejected before the library makes its first CUDA call, so no
 GPU is needed.  Plus the binding's refusal of host tensors.  CPU only."""
 
+import ctypes
+
 import pytest
 import torch
 
@@ -120,3 +122,56 @@ def test_binding_refuses_host_tensors():
         api.pa_decode(torch.empty_like(q), q, kc, kc, tables, ctx, 16, 0.125, 4, 2, 64, 16)
     with pytest.raises(ValueError, match="CUDA"):
         api.pa_reshape_and_cache(kc, kc, q[:, :2], q[:, :2], torch.zeros(2, dtype=torch.int64))
+
+
+def copy_blocks(layers_k, layers_v, pairs=A, num_pairs=3, block_size=16, d=128, hkv=8, num_blocks=64):
+    arr = lambda xs: (ctypes.c_void_p * max(1, len(xs)))(*xs)
+    return L.pa_copy_blocks(arr(layers_k), arr(layers_v), len(layers_k), pairs, num_pairs, hkv, d, block_size,
+                            num_blocks, None, None)
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(layers_k=[], layers_v=[]), api.PA_OK),                     # no layers: nothing to do
+    (dict(layers_k=[A], layers_v=[A], num_pairs=0), api.PA_OK),
+    (dict(layers_k=[A], layers_v=[A], num_pairs=-1), api.PA_ERR_INVALID_ARG),
+    (dict(layers_k=[A], layers_v=[A], block_size=4), api.PA_ERR_UNSUPPORTED),
+    (dict(layers_k=[A, None], layers_v=[A, A]), api.PA_ERR_INVALID_ARG),
+    (dict(layers_k=[A, A + 8], layers_v=[A, A]), api.PA_ERR_MISALIGNED),
+    (dict(layers_k=[A], layers_v=[A], pairs=A + 2), api.PA_ERR_MISALIGNED),
+    (dict(layers_k=[A], layers_v=[A], pairs=None), api.PA_ERR_INVALID_ARG),
+])
+def test_copy_blocks_host_checks(args, want):
+    assert copy_blocks(**args) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(num_seqs=0), api.PA_OK),
+    (dict(max_parts=0), api.PA_ERR_INVALID_ARG),
+    (dict(partition=0), api.PA_ERR_INVALID_ARG),
+    (dict(out_dtype=3), api.PA_ERR_INVALID_ARG),
+    (dict(pm=None), api.PA_ERR_INVALID_ARG),
+    (dict(d=2048), api.PA_ERR_UNSUPPORTED),
+    (dict(ps=A + 2), api.PA_ERR_MISALIGNED),
+])
+def test_lse_merge_host_checks(kw, want):
+    a = dict(out=A, out_dtype=api.PA_DTYPE_F32, pm=A, ps=A, pacc=A, ctx=A, partition=512, max_parts=4, num_seqs=2,
+             hq=8, d=128)
+    a.update(kw)
+    assert L.pa_lse_merge(a["out"], a["out_dtype"], a["pm"], a["ps"], a["pacc"], a["ctx"], a["partition"],
+                          a["max_parts"], a["num_seqs"], a["hq"], a["d"], None) == want
+
+
+def test_append_and_fp8_host_checks():
+    # the fused append needs both new-row arrays, 16-byte aligned
+    common = (A, api.PA_DTYPE_BF16, A, A, A)
+    rest = (A, A, 16, 0.088, 32, 8, 128, 4, 8, 64, 128, 0, None, 0, None, None)
+    assert L.pa_decode_append(*common, None, A, *rest) == api.PA_ERR_INVALID_ARG
+    assert L.pa_decode_append(*common, A + 8, A + 8, *rest) == api.PA_ERR_MISALIGNED
+    # E4M3 cache write: scales finite and > 0
+    assert L.pa_reshape_and_cache_fp8(A, A, A, A, A, 4, 8, 128, 16, 64, 0.0, 1.0, None, None) == api.PA_ERR_INVALID_ARG
+    assert L.pa_reshape_and_cache_fp8(A, A, A, A, A, 0, 8, 128, 16, 64, 1.0, 1.0, None, None) == api.PA_OK
+    # E4M3 prefill: scales, d_head 128 only
+    pf = lambda ks, d: L.pa_prefill_fp8(A, api.PA_DTYPE_BF16, A, A, A, A, 8, A, A, 2, 100, 64, 64, 16, 0.088, ks, 0.01,
+                                        32, 8, d, A, 1 << 30, None, None, None)
+    assert pf(-1.0, 128) == api.PA_ERR_INVALID_ARG
+    assert pf(0.01, 64) == api.PA_ERR_UNSUPPORTED
