@@ -723,8 +723,8 @@ __global__ void __launch_bounds__(kThreads, F8 ? (NK == 2 ? PA_DECODE_MIN_BLOCKS
             for (int i = 0; i < kWarps * kStages; ++i) pa::mbar_init(&bars[i], 1);
             pa::fence_mbar_init();
         }
-        // every block has made its claims' inputs its own: the merge kernel
-        // may begin its launch
+        // the merge kernel may begin its launch (it waits for this grid's
+        // results before it reads them)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     int kg = 0;                      // this warp's stages consumed by earlier items
