@@ -6,7 +6,10 @@ copy-on-write pairs of the CoW sampling config (16 prompts of 2,003 tokens,
 copies come from the C++ block manager; the oracle allocator replaying the
 same operations must plan the same pairs, and their number follows from the
 pages' rule that each writer of a shared tail block copies it except the
-last ("PagedAttention: Virtual Memory for the KV Cache", sections 15-16)."""
+last ("PagedAttention: Virtual Memory for the KV Cache", sections 15-16).
+The continuous-batching workload's lengths follow its stated recipe."""
+import math
+
 import numpy as np
 import pytest
 
@@ -14,6 +17,7 @@ api = pytest.importorskip("paged_kv_cache_124_gb300.api")
 
 import bench  # noqa: E402
 from oracle.allocator import RefAllocator  # noqa: E402
+from paged_kv_cache_124_gb300 import inputs as I  # noqa: E402
 
 
 def test_cow_pairs_match_the_oracle_allocator():
@@ -124,3 +128,32 @@ def test_prefill_cpu_baseline_reports_both_legs():
 def test_quantiles():
     assert bench._quantiles([5.0, 1.0, 3.0, 2.0, 4.0]) == (3.0, 1.0, 5.0)
     assert bench._quantiles([2.0]) == (2.0, 2.0, 2.0)
+
+
+def test_lognormal_lengths_have_the_requested_median_and_sigma():
+    """The continuous-batching lengths: lognormal with median 700 and
+    log-space sigma 1 (reading O11), rounded and clipped."""
+    x = I.lognormal_ints(200000, 700, 1.0, 1, 10 ** 9, 5)
+    assert abs(np.median(x) / 700 - 1) < 0.01
+    assert abs(np.std(np.log(x)) - 1.0) < 0.01
+    y = I.lognormal_ints(5000, 700, 1.0, 1, 16384, 6)
+    assert y.min() >= 1 and y.max() <= 16384 and (y == 16384).any()
+
+
+def test_mixed_batch_recipe():
+    """256 sequences whose decode contexts are the lognormal draw (each a
+    prompt of ctx - 1 tokens and one appended token), the 8B head shape, 32
+    layers, and a pool sized for 90 % occupancy."""
+    sc = I.mixed_batch(0, 16)
+    ctx = I.lognormal_ints(256, 700, 1.0, 1, 16384, 1)
+    toks = {}
+    for op in sc.ops:
+        if op[0] == "alloc" and op[1] < 256:
+            toks[op[1]] = op[2]
+        elif op[0] == "append":
+            toks[op[1]] += 1
+    assert [toks[i] for i in range(256)] == ctx.tolist()
+    assert sc.decode_seqs == list(range(256))
+    assert (sc.n_q_heads, sc.n_kv_heads, sc.d_head, sc.n_layers) == (32, 8, 128, 32)
+    need = sum(-(-int(c) // 16) for c in ctx)
+    assert sc.num_blocks == math.ceil(need / 0.9)
