@@ -129,6 +129,54 @@ MUTANTS = [
     ("allocator", "self.ref_counts[b] = counts[h]", "self.ref_counts[b] = 1", "swapped-in shared block counted once"),
     ("allocator", "if b not in counts:\n                    counts[b] = 0\n                    blocks.append(b)\n                counts[b] += 1",
      "counts[b] = counts.get(b, 0) + 1\n                blocks.append(b)", "a shared block swapped once per sharer"),
+    # sizing: the tail waste and the capacity decision
+    ("sizing", "return blocks_needed(n_tokens, block_size) * block_size - n_tokens", "return n_tokens % block_size",
+     "tail waste as S mod B"),
+    ("sizing", '"fits": slots <= pool_slots,', '"fits": slots < pool_slots,', "a batch that exactly fills the pool rejected"),
+    ("sizing", '"deficit_slots": max(0, slots - pool_slots),', '"deficit_slots": max(0, pool_slots - slots),',
+     "deficit with the wrong sign"),
+    ("sizing", '"waste_frac": waste / slots if slots else 0.0,', '"waste_frac": waste / sum(lengths) if slots else 0.0,',
+     "waste fraction of the tokens, not the slots"),
+    # attention: translation offsets, the merge weights, partition scores, row and table indexing
+    ("attention", "    offset = i % block_size\n", "    offset = i // block_size\n", "offset from the logical block"),
+    ("attention", "m = max(sb[0] for sb in summaries)", "m = min(sb[0] for sb in summaries)",
+     "merge takes the smallest block maximum"),
+    ("attention", "z = z + w * z_b", "z = z + z_b", "block normalisers merged unweighted"),
+    ("attention", "u = u + w * np.asarray(u_b, dtype=np.float64)", "u = u + np.asarray(u_b, dtype=np.float64)",
+     "block value sums merged unweighted"),
+    ("attention", "    s = scale * (K @ q_row)\n", "    s = K @ q_row\n", "partition scores unscaled"),
+    ("attention", "out[row0 + i, g] = softmax_attention(q[row0 + i, g]", "out[row0 + i, g] = softmax_attention(q[i, g]",
+     "prefill query rows not offset by the sequence's start"),
+    ("attention", "K, V = gather_kv(k_cache, v_cache, block_tables[s], ctx, block_size)",
+     "K, V = gather_kv(k_cache, v_cache, block_tables[0], ctx, block_size)", "every sequence read through the first table"),
+    ("attention", "            out[s, g] = softmax_attention(q[s, g], K[h], V[h], scale)",
+     "            out[s, g] = softmax_attention(q[s, g], K[0], V[0], scale)", "decode reads KV head 0 for every query head"),
+    # quant: the sign of zero and NaN, subnormal codes
+    ("quant", "sign = np.signbit(x).astype(np.int64) << 7", "sign = (x < 0).astype(np.int64) << 7",
+     "negative zero and signed NaN lose their sign"),
+    ("quant", "mag = np.where(e == 0, m * 2.0 ** -9,", "mag = np.where((e == 0) & (m == 0), m * 2.0 ** -9,",
+     "subnormal codes read as normals"),
+    # cache_ops: which rows land in the value pool
+    ("cache_ops", "v_out[block, :, offset, :] = v[t]", "v_out[block, :, offset, :] = k[t]", "values written from the key rows"),
+    ("cache_ops", "dst_v[dst] = src_v[src]", "dst_v[dst] = src_k[src]", "swap moves keys into the value pool"),
+    # allocator: key registration, the eviction queue's order and accounting, host blocks, slot queries
+    ("allocator", "        if key in self.cache_index:\n            return\n", "",
+     "a later block with a known key replaces the first in the index"),
+    ("allocator", "for b in reversed(idle_cached):\n            self.evict_queue[b] = None\n        del self.block_tables[seq]",
+     "for b in idle_cached:\n            self.evict_queue[b] = None\n        del self.block_tables[seq]",
+     "the shallowest idle block queued first"),
+    ("allocator", "if self.caching and i < full:", "if self.caching and i < full - 1:", "the last full prompt block not registered"),
+    ("allocator", "from_queue = sum(1 for b in hits if b in self.evict_queue)", "from_queue = 0",
+     "hits taken out of the queue still counted as available"),
+    ("allocator", "if self.free_blocks:\n            b = self.free_blocks.pop()",
+     "if not self.evict_queue:\n            b = self.free_blocks.pop()", "cached blocks evicted while free blocks remain"),
+    ("allocator", "return self.block_tables[seq][i // B] * B + i % B", "return self.block_tables[seq][i // B] * B + i // B",
+     "slot offset from the logical block"),
+    ("allocator", "self.host_free = list(reversed(range(num_host_blocks)))", "self.host_free = list(range(num_host_blocks))",
+     "host blocks handed out from the top"),
+    ("allocator", "            self.block_tables[q] = [to_dev[h] for h in self.block_tables[q]]",
+     "            self.block_tables[q] = [to_dev[h] for h in reversed(self.block_tables[q])]",
+     "swapped-in table in reverse order"),
 ]
 
 
