@@ -9,6 +9,7 @@ rebuilt when the library is newer than every source and header.
 
 import concurrent.futures
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -40,9 +41,26 @@ def _inputs():
     return sources() + hdrs + [os.path.abspath(__file__)]
 
 
+# ELF e_machine of a shared object built for this host (x86-64 or AArch64)
+_ELF_MACHINE = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}
+
+
+def elf_matches_host(header, machine=None):
+    """True if `header` (the first 20 bytes of a file) starts a 64-bit
+    little-endian ELF object for this host's machine."""
+    want = _ELF_MACHINE.get((machine or platform.machine()).lower())
+    return (len(header) >= 20 and header[:4] == b"\x7fELF" and header[4] == 2 and header[5] == 1 and
+            want is not None and int.from_bytes(header[18:20], "little") == want)
+
+
 def up_to_date():
+    """The library exists, was built for this host's machine, and is newer
+    than every source and header."""
     if not os.path.exists(LIB):
         return False
+    with open(LIB, "rb") as f:
+        if not elf_matches_host(f.read(20)):
+            return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 

@@ -4,7 +4,9 @@ header gives it: the same number of arguments, each of the same kind
 and the statistics structure has the header's fields in the header's order.
 ctypes converts arguments by the declared types without looking at the
 library, so a binding that drifted from include/pa.h would pass wrong values
-silently.  CPU only: the header is parsed as text and nothing is called."""
+silently.  And the in-tree build loads only a library built for this
+host's machine.  CPU only: the header is parsed as text and nothing is
+called."""
 
 import ctypes
 import os
@@ -90,3 +92,23 @@ def test_stats_structure_matches_the_header():
     fields = [tuple(f.split()) for f in body.split(";") if f.strip()]
     want = [(name, {"int32_t": ctypes.c_int32, "int64_t": ctypes.c_int64}[t]) for t, name in fields]
     assert [(n, t) for n, t in api.AllocStats._fields_] == want
+
+
+def test_build_freshness_checks_the_library_machine():
+    """The in-tree build counts a library as current only if it is a 64-bit
+    little-endian ELF object for this host's machine, so a library built on
+    the other architecture is rebuilt rather than loaded."""
+    from paged_kv_cache_124_gb300 import build as b
+
+    def elf(machine, cls=2, data=1):
+        return b"\x7fELF" + bytes([cls, data]) + bytes(12) + machine.to_bytes(2, "little")
+
+    assert b.elf_matches_host(elf(62), "x86_64") and not b.elf_matches_host(elf(183), "x86_64")
+    assert b.elf_matches_host(elf(183), "aarch64") and not b.elf_matches_host(elf(62), "aarch64")
+    assert not b.elf_matches_host(elf(62, cls=1), "x86_64")          # 32-bit
+    assert not b.elf_matches_host(elf(62, data=2), "x86_64")         # big-endian
+    assert not b.elf_matches_host(b"#!/bin/sh\n" + bytes(10), "x86_64")
+    assert not b.elf_matches_host(elf(62)[:19], "x86_64")
+    assert not b.elf_matches_host(elf(62), "riscv64")                # no library for an unknown machine
+    with open(b.LIB, "rb") as f:
+        assert b.elf_matches_host(f.read(20))                       # the library built here
