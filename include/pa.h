@@ -168,6 +168,8 @@ int pa_decode_fp8(void* out, int out_dtype, const void* q,
 size_t pa_decode_workspace_size(int num_seqs, int n_q_heads, int d_head,
                                 int max_context_len, int partition_size);
 
+/* Decode attention over a bf16 cache: the operation, the arguments and the
+ * return codes are those of the "Decode attention" block above. */
 int pa_decode(void* out, int out_dtype, const void* q,
               const void* k_cache, const void* v_cache,
               const int32_t* block_tables, const int32_t* context_lens,
@@ -525,6 +527,7 @@ typedef struct pa_alloc_stats {
 
 /* NULL if num_blocks <= 0 or block_size <= 0 or on allocation failure. */
 pa_alloc_t* pa_alloc_create(int num_blocks, int block_size);
+/* Frees the manager and everything it holds; NULL is ignored. */
 void pa_alloc_destroy(pa_alloc_t* a);
 
 /* Replace the free list by order[0 .. n-1] (blocks leave from the end), e.g.
@@ -698,9 +701,11 @@ int pa_alloc_slot_mapping(const pa_alloc_t* a, int64_t seq, int start, int n,
 
 int pa_alloc_seq_len(const pa_alloc_t* a, int64_t seq);      /* -1 if unknown */
 int pa_alloc_ref_count(const pa_alloc_t* a, int32_t block);  /* -1 if out of range */
+/* Blocks on the free list, not counting zero-count cached blocks (-1 for NULL). */
 int pa_alloc_num_free(const pa_alloc_t* a);
 /* Copy the free stack bottom-to-top into out (cap entries); returns its size. */
 int pa_alloc_free_list(const pa_alloc_t* a, int32_t* out, int cap);
+/* Fill *out with the counts above; PA_ERR_INVALID_ARG if a or out is NULL. */
 int pa_alloc_get_stats(const pa_alloc_t* a, pa_alloc_stats_t* out);
 
 #ifdef __cplusplus
