@@ -49,6 +49,7 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_partition_kernel_batch64_8b.md")
 PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "decode_partition_kernel_fp8_batch64_8b.md")
 KERNEL_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_decode.cu")
+COMMON_HEADER = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_common.cuh")
 PREFILL_PROFILE = os.path.join(ROOT, "profiles", "prefill_kernel_prefill_prompts_8b.md")
 CACHE_OPS_PROFILE = os.path.join(ROOT, "profiles", "copy_blocks_kernel_cache_ops_8b.md")
 CACHE_OPS_SOURCE = os.path.join(ROOT, "paged_kv_cache_124_gb300", "csrc", "pa_cache_ops.cu")
@@ -160,15 +161,21 @@ def prefill_flops(ctxs, news, n_q_heads, d_head):
     return f
 
 
-def profiled_traffic(summary=PROFILE_SUMMARY, source=KERNEL_SOURCE):
+def _sha16(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def profiled_traffic(summary=PROFILE_SUMMARY, source=KERNEL_SOURCE, common=COMMON_HEADER):
     """DRAM bytes per launch of a kernel from its committed ncu summary, if
-    the summary was taken on the current kernel source; else None."""
+    the summary was taken on the current kernel source and the current
+    device helpers it includes; else None."""
     try:
         text = open(summary).read()
-        src_hash = hashlib.sha256(open(source, "rb").read()).hexdigest()[:16]
         m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+        m_common = re.search(r"common_header_sha256_16:\s*([0-9a-f]+)", text)
         m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-        if m_hash and m_tr and m_hash.group(1) == src_hash:
+        if (m_hash and m_common and m_tr and m_hash.group(1) == _sha16(source) and
+                m_common.group(1) == _sha16(common)):
             return int(m_tr.group(1))
     except OSError:
         pass

@@ -157,3 +157,14 @@ def test_mixed_batch_recipe():
     assert (sc.n_q_heads, sc.n_kv_heads, sc.d_head, sc.n_layers) == (32, 8, 128, 32)
     need = sum(-(-int(c) // 16) for c in ctx)
     assert sc.num_blocks == math.ceil(need / 0.9)
+
+
+def test_profiled_traffic_needs_both_source_hashes():
+    """A committed ncu traffic figure is reported only while both the kernel's
+    source and the device helpers it includes hash as they did at capture;
+    either one changed gives no traffic (null in the bench line)."""
+    other = bench.PREFILL_SOURCE                                       # any file with another hash
+    assert bench.profiled_traffic(bench.PROFILE_SUMMARY, other) is None
+    assert bench.profiled_traffic(bench.PROFILE_SUMMARY, bench.KERNEL_SOURCE, other) is None
+    text = open(bench.PROFILE_SUMMARY).read()
+    assert "common_header_sha256_16:" in text and "kernel_source_sha256_16:" in text
