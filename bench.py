@@ -220,26 +220,34 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.out.close()
-        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        text = open(self.path).read()
         os.unlink(self.path)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-            except ValueError:
-                continue
-            for n, val in zip(names, r[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return summarize_clocks(text)
+
+
+def summarize_clocks(text):
+    """Median SM clock, the highest maximum clock and the throttle reasons
+    seen Active, from nvidia-smi rows of ClockSampler.FIELDS (csv, no header,
+    no units); rows that do not parse are skipped.  None without a sample."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        r = [x.strip() for x in line.split(",")]
+        if len(r) < 9:
+            continue
+        try:
+            clk, clk_max = float(r[1]), float(r[2])
+        except ValueError:
+            continue
+        sm.append(clk)
+        mx.append(clk_max)
+        for n, val in zip(names, r[5:9]):
+            if val.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+            "reasons": sorted(reasons)}
 
 
 # ----------------------------------------------------------------------------
