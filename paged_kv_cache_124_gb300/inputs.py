@@ -8,8 +8,12 @@ scatter or copy arithmetic; both the CUDA path and the CPU oracle replay the
 same scenario with their own code.  The only arithmetic here is pool sizing
 (how many blocks a pool has), which is part of a scenario's definition.
 
-All draws come from CPU generators seeded explicitly, so every side sees the
-same bits.  Tensor values are N(0, 1) rounded to bf16.
+Every draw comes from an explicitly seeded generator that it owns (never the
+global one), so every side that draws on the CPU sees the same bits.  Large
+multi-layer workloads may draw their keys and values on the device with a
+seeded device generator instead; a side that compares against those copies
+the drawn tensors back rather than drawing them again.  Tensor values are
+N(0, 1) rounded to bf16.
 """
 
 import dataclasses

@@ -168,3 +168,31 @@ def test_profiled_traffic_needs_both_source_hashes():
     assert bench.profiled_traffic(bench.PROFILE_SUMMARY, bench.KERNEL_SOURCE, other) is None
     text = open(bench.PROFILE_SUMMARY).read()
     assert "common_header_sha256_16:" in text and "kernel_source_sha256_16:" in text
+
+
+def test_seeded_draws_are_reproducible_and_leave_the_global_generators_alone():
+    """Both sides of every comparison draw their inputs from these generators,
+    so a draw must depend on its seed only: the same seed gives the same bits
+    whatever was drawn before, another seed other bits, and the global torch
+    and NumPy generators are neither read nor advanced."""
+    import torch
+    torch.manual_seed(123)
+    np.random.seed(123)
+    want_torch = torch.rand(4)
+    want_np = np.random.rand(4)
+    torch.manual_seed(123)
+    np.random.seed(123)
+    a = I.bf16_bits(I.bf16_normal((3, 5, 7), 42))
+    k1, v1 = I.prefill_kv(0, 1, 2, 9, 2, 8)
+    p1 = I.permutation(50, 7)
+    n1 = I.lognormal_ints(20, 700, 1.0, 1, 16384, 3)
+    assert torch.equal(torch.rand(4), want_torch) and np.array_equal(np.random.rand(4), want_np)
+    torch.rand(1000)                                  # the global state moves; the draws must not
+    assert np.array_equal(I.bf16_bits(I.bf16_normal((3, 5, 7), 42)), a)
+    k2, v2 = I.prefill_kv(0, 1, 2, 9, 2, 8)
+    assert torch.equal(k1.view(torch.int16), k2.view(torch.int16)) and torch.equal(v1.view(torch.int16),
+                                                                                  v2.view(torch.int16))
+    assert np.array_equal(I.permutation(50, 7), p1) and np.array_equal(I.lognormal_ints(20, 700, 1.0, 1, 16384, 3), n1)
+    assert not np.array_equal(I.bf16_bits(I.bf16_normal((3, 5, 7), 43)), a)
+    assert not torch.equal(I.prefill_kv(0, 1, 3, 9, 2, 8)[0].view(torch.int16), k1.view(torch.int16))
+    assert not torch.equal(k1.view(torch.int16), v1.view(torch.int16))   # keys and values are separate draws
