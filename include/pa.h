@@ -513,6 +513,11 @@ int pa_check_bounded_wait(int max_probes, int32_t* status_dev, void* stream);
  * A handle is not thread-safe; use one per thread or lock around it. */
 typedef struct pa_alloc pa_alloc_t;
 
+/* Pool counters, filled by pa_alloc_get_stats.  They give the operational
+ * metrics of [P3] "Operational metrics": block-pool usage (num_used /
+ * num_blocks), preemptions by swapping (num_swap_outs), the prefix-cache hit
+ * rate (num_cached_tokens / num_prompt_tokens) and the mean sequence length
+ * (num_context_tokens / num_seqs). */
 typedef struct pa_alloc_stats {
     int32_t num_blocks;
     int32_t num_free;           /* on the free list                        */
@@ -520,9 +525,11 @@ typedef struct pa_alloc_stats {
     int32_t num_seqs;
     int64_t num_cow_copies;     /* CoW pairs emitted since creation        */
     int32_t num_cached;         /* count 0, kept for prefix reuse          */
-    int32_t reserved;
+    int32_t num_swapped;        /* sequences whose blocks are in host memory */
     int64_t num_prompt_tokens;  /* prompt positions admitted since creation */
     int64_t num_cached_tokens;  /* of those, found in the prefix cache     */
+    int64_t num_swap_outs;      /* sequences swapped out since creation    */
+    int64_t num_context_tokens; /* sum of every live sequence's length     */
 } pa_alloc_stats_t;
 
 /* NULL if num_blocks <= 0 or block_size <= 0 or on allocation failure. */

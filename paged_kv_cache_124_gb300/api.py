@@ -56,8 +56,9 @@ _f32p = ctypes.POINTER(ctypes.c_float)
 class AllocStats(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("num_free", ctypes.c_int32), ("num_used", ctypes.c_int32),
                 ("num_seqs", ctypes.c_int32), ("num_cow_copies", ctypes.c_int64), ("num_cached", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("num_prompt_tokens", ctypes.c_int64),
-                ("num_cached_tokens", ctypes.c_int64)]
+                ("num_swapped", ctypes.c_int32), ("num_prompt_tokens", ctypes.c_int64),
+                ("num_cached_tokens", ctypes.c_int64), ("num_swap_outs", ctypes.c_int64),
+                ("num_context_tokens", ctypes.c_int64)]
 
 
 _SIGS = {
@@ -737,6 +738,19 @@ class BlockAllocator:
     def stats(self):
         s = AllocStats()
         _check(_lib.pa_alloc_get_stats(self._h, ctypes.byref(s)), "pa_alloc_get_stats")
-        d = {f: getattr(s, f) for f, _ in AllocStats._fields_ if f != "reserved"}
+        d = {f: getattr(s, f) for f, _ in AllocStats._fields_}
         d["prefix_cache_hit_rate"] = d["num_cached_tokens"] / d["num_prompt_tokens"] if d["num_prompt_tokens"] else 0.0
         return d
+
+    def metrics(self):
+        """The pool's operational metrics: the share of blocks held by
+        sequences (percent; zero-count cached blocks are reclaimable and not
+        counted), sequences swapped out to host memory since creation (each
+        swap-out is a preemption), the share of admitted prompt positions
+        found in the prefix cache, and the mean length of the live
+        sequences."""
+        st = self.stats()
+        return {"gpu_cache_usage_perc": 100.0 * st["num_used"] / st["num_blocks"],
+                "num_preemption": st["num_swap_outs"],
+                "prefix_cache_hit_rate": st["prefix_cache_hit_rate"],
+                "avg_sequence_length": st["num_context_tokens"] / st["num_seqs"] if st["num_seqs"] else 0.0}

@@ -104,6 +104,7 @@ struct pa_alloc {
     std::vector<int32_t> host_free;                     // top = back()
     std::vector<int32_t> host_refs;
     int32_t num_swapped = 0;
+    int64_t swap_outs = 0;                              // sequences swapped out since creation
 
     pa_alloc(int nb, int bs)
         : num_blocks(nb), block_size(bs), refs(nb, 0), registered(nb, 0), reg_node(nb, 0), lru_pos(nb),
@@ -511,8 +512,13 @@ int pa_alloc_get_stats(const pa_alloc_t* a, pa_alloc_stats_t* out) {
     out->num_used = a->num_blocks - out->num_free - out->num_cached;
     out->num_seqs = (int32_t)a->seqs.size();
     out->num_cow_copies = a->num_cow_copies;
+    out->num_swapped = a->num_swapped;
     out->num_prompt_tokens = a->prompt_tokens;
     out->num_cached_tokens = a->cached_tokens;
+    out->num_swap_outs = a->swap_outs;
+    int64_t ctx = 0;
+    for (const auto& kv : a->seqs) ctx += kv.second.length;
+    out->num_context_tokens = ctx;
     return PA_OK;
 }
 
@@ -611,6 +617,7 @@ int pa_alloc_swap_out(pa_alloc_t* a, const int64_t* seqs, int n, int32_t* pairs_
         for (int32_t& b : s.table) b = to_host[b];
         s.swapped = true;
         ++a->num_swapped;
+        ++a->swap_outs;
     }
     return PA_OK;
 }

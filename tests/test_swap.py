@@ -207,3 +207,44 @@ def test_swap_argument_errors():
     with pytest.raises(api.PAError):
         a.build_tables([1], 4)
     assert a.seq_len(1) == 5 and a.is_swapped(1) == 1
+
+
+def test_operational_metrics_follow_the_operations():
+    """The pool's operational metrics ("PagedAttention and KV Memory",
+    Operational metrics: block-pool usage, preemptions by swapping, prefix
+    cache hit rate, mean sequence length), counted by hand along a short
+    history of admissions, a fork, swaps, appends and releases."""
+    a = api.BlockAllocator(64, 16)
+    assert a.enable_swap(32) == 0
+    assert a.allocate(1, 40) == 0 and a.allocate(2, 16) == 0            # 3 + 1 blocks
+    assert a.fork(1, 3) == 0                                            # shares seq 1's 3 blocks
+    m = a.metrics()
+    assert m == {"gpu_cache_usage_perc": 100.0 * 4 / 64, "num_preemption": 0, "prefix_cache_hit_rate": 0.0,
+                 "avg_sequence_length": (40 + 16 + 40) / 3}
+    st, pairs = a.swap_out([1, 3])                                      # one preemption per sequence
+    assert st == 0 and len(pairs) == 3
+    s = a.stats()
+    assert s["num_swapped"] == 2 and s["num_swap_outs"] == 2 and s["num_used"] == 1
+    assert a.metrics()["gpu_cache_usage_perc"] == 100.0 / 64
+    st, pairs = a.swap_in([1])                                          # seq 3 stays on the host
+    assert st == 0 and len(pairs) == 3
+    s = a.stats()
+    assert s["num_swapped"] == 1 and s["num_swap_outs"] == 2 and s["num_used"] == 4
+    assert a.free(3) == 0                                               # releases its host blocks
+    assert a.stats()["num_swapped"] == 0
+    assert a.append_slot(2)[0] == 0                                     # 17 positions: a second block
+    assert a.swap_out([2])[0] == 0
+    m = a.metrics()
+    assert m["num_preemption"] == 3 and m["avg_sequence_length"] == (40 + 17) / 2
+    assert m["gpu_cache_usage_perc"] == 100.0 * 3 / 64
+    assert a.stats()["num_context_tokens"] == 57
+
+
+def test_metrics_of_an_empty_pool_and_prefix_hits():
+    a = api.BlockAllocator(8, 4)
+    assert a.metrics() == {"gpu_cache_usage_perc": 0.0, "num_preemption": 0, "prefix_cache_hit_rate": 0.0,
+                           "avg_sequence_length": 0.0}
+    assert a.enable_prefix_caching(True) == 0
+    assert a.allocate_tokens(1, [5, 6, 7, 8, 9]) == (0, 0)
+    assert a.allocate_tokens(2, [5, 6, 7, 8, 1, 2]) == (0, 4)           # the first full block is found
+    assert a.metrics()["prefix_cache_hit_rate"] == 4 / 11
