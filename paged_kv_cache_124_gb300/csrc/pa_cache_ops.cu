@@ -7,6 +7,8 @@
 // section 7; "PagedAttention in vLLM: scattered memory, exact attention",
 // section 2): slot = physical_block * B + offset.
 
+#include <vector>
+
 #include "pa_common.cuh"
 
 namespace {
@@ -280,23 +282,30 @@ int swap_blocks_impl(void* const* dst_k, void* const* dst_v, const void* const* 
     if (!pairs) return PA_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(pairs) & 3u) return PA_ERR_MISALIGNED;
     const long long chunks = (long long)n_kv_heads * block_size * d_head * elem_bytes / 16;
+    // every layer's pools are translated and checked before the first launch,
+    // so that a rejected call has enqueued nothing
+    std::vector<const void*> dev((size_t)num_layers * 4);      // per layer: src K, src V, dst K, dst V
+    for (int l = 0; l < num_layers; ++l) {
+        const void** d = dev.data() + (size_t)l * 4;
+        d[0] = device_address(src_k[l]);
+        d[1] = device_address(src_v[l]);
+        d[2] = device_address(dst_k[l]);
+        d[3] = device_address(dst_v[l]);
+        if (!d[0] || !d[1] || !d[2] || !d[3]) return PA_ERR_INVALID_ARG;
+        if (!pa_host::aligned16(d[0]) || !pa_host::aligned16(d[1]) || !pa_host::aligned16(d[2]) ||
+            !pa_host::aligned16(d[3]))
+            return PA_ERR_MISALIGNED;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     for (int l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
         const int nl = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0 : kMaxLayersPerLaunch;
         SwapPtrs ptrs{};
         for (int l = 0; l < nl; ++l) {
-            const void* sk = device_address(src_k[l0 + l]);
-            const void* sv = device_address(src_v[l0 + l]);
-            const void* dk = device_address(dst_k[l0 + l]);
-            const void* dv = device_address(dst_v[l0 + l]);
-            if (!sk || !sv || !dk || !dv) return PA_ERR_INVALID_ARG;
-            if (!pa_host::aligned16(sk) || !pa_host::aligned16(sv) || !pa_host::aligned16(dk) ||
-                !pa_host::aligned16(dv))
-                return PA_ERR_MISALIGNED;
-            ptrs.src[0][l] = static_cast<const uint4*>(sk);
-            ptrs.src[1][l] = static_cast<const uint4*>(sv);
-            ptrs.dst[0][l] = static_cast<uint4*>(const_cast<void*>(dk));
-            ptrs.dst[1][l] = static_cast<uint4*>(const_cast<void*>(dv));
+            const void* const* d = dev.data() + (size_t)(l0 + l) * 4;
+            ptrs.src[0][l] = static_cast<const uint4*>(d[0]);
+            ptrs.src[1][l] = static_cast<const uint4*>(d[1]);
+            ptrs.dst[0][l] = static_cast<uint4*>(const_cast<void*>(d[2]));
+            ptrs.dst[1][l] = static_cast<uint4*>(const_cast<void*>(d[3]));
         }
         dim3 grid(num_pairs, nl, 2);
         swap_blocks_kernel<<<grid, kCopyThreads, 0, st>>>(ptrs, pairs, chunks, src_num_blocks, dst_num_blocks,

@@ -175,3 +175,28 @@ def test_append_and_fp8_host_checks():
                                         32, 8, d, A, 1 << 30, None, None, None)
     assert pf(-1.0, 128) == api.PA_ERR_INVALID_ARG
     assert pf(0.01, 64) == api.PA_ERR_UNSUPPORTED
+
+
+def swap_blocks(**kw):
+    arr = lambda xs: (ctypes.c_void_p * max(1, len(xs)))(*xs)
+    a = dict(dst_k=[A], dst_v=[A], src_k=[A], src_v=[A], layers=1, pairs=A, num_pairs=2, hkv=8, d=128, block_size=16,
+             src_nb=64, dst_nb=64)
+    a.update(kw)
+    conv = lambda xs: None if xs is None else arr(xs)
+    return L.pa_swap_blocks(conv(a["dst_k"]), conv(a["dst_v"]), conv(a["src_k"]), conv(a["src_v"]), a["layers"],
+                            a["pairs"], a["num_pairs"], a["hkv"], a["d"], a["block_size"], a["src_nb"], a["dst_nb"],
+                            None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(layers=0), api.PA_OK),                                      # nothing to move
+    (dict(num_pairs=0), api.PA_OK),
+    (dict(num_pairs=-1), api.PA_ERR_INVALID_ARG),
+    (dict(src_nb=0), api.PA_ERR_INVALID_ARG),
+    (dict(block_size=12), api.PA_ERR_UNSUPPORTED),
+    (dict(d=96), api.PA_ERR_UNSUPPORTED),
+    (dict(dst_k=None), api.PA_ERR_INVALID_ARG),
+    (dict(pairs=None), api.PA_ERR_INVALID_ARG),
+])
+def test_swap_blocks_host_checks(kw, want):
+    assert swap_blocks(**kw) == want
