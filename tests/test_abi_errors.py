@@ -200,3 +200,33 @@ def swap_blocks(**kw):
 ])
 def test_swap_blocks_host_checks(kw, want):
     assert swap_blocks(**kw) == want
+
+
+def test_remaining_entry_points_host_checks():
+    """The FP8 copy and swap, the FP8 fused append, the static-scratch decode
+    and the bounded-wait self-test reject bad arguments on the host too."""
+    arr = lambda xs: (ctypes.c_void_p * max(1, len(xs)))(*xs)
+    # FP8 block copies: the same checks as their bf16 forms
+    cp8 = lambda ks, bs=16: L.pa_copy_blocks_fp8(arr(ks), arr(ks), len(ks), A, 3, 8, 128, bs, 64, None, None)
+    assert cp8([]) == api.PA_OK
+    assert cp8([A], bs=4) == api.PA_ERR_UNSUPPORTED
+    assert cp8([A + 8]) == api.PA_ERR_MISALIGNED
+    sw8 = lambda layers, bs=16: L.pa_swap_blocks_fp8(arr([A]), arr([A]), arr([A]), arr([A]), layers, A, 2, 8, 128,
+                                                     bs, 64, 64, None, None)
+    assert sw8(0) == api.PA_OK
+    assert sw8(1, bs=12) == api.PA_ERR_UNSUPPORTED
+    # FP8 fused append: both new-row arrays, finite positive scales
+    app8 = lambda kn, ks: L.pa_decode_append_fp8(A, api.PA_DTYPE_F32, A, A, A, kn, A, A, A, 16, 0.088, ks, 0.01, 32, 8,
+                                                 128, 4, 8, 64, 128, 0, None, 0, None, None)
+    assert app8(None, 0.01) == api.PA_ERR_INVALID_ARG
+    assert app8(A, 0.0) == api.PA_ERR_INVALID_ARG
+    assert app8(A, float("nan")) == api.PA_ERR_INVALID_ARG
+    # static scratch: a problem whose partition statistics exceed the array is refused up front
+    ss = lambda S, hq, max_ctx, P: L.pa_decode_static_scratch(A, api.PA_DTYPE_BF16, A, A, A, A, A, 16, 0.088, hq, 8,
+                                                              128, S, 8, 64, max_ctx, P, None, None)
+    assert ss(1024, 64, 1 << 20, 256) == api.PA_ERR_WORKSPACE
+    assert ss(0, 32, 128, 512) == api.PA_OK
+    # the bounded-wait self-test: probe limit in [1, 10^7] and a status word
+    assert L.pa_check_bounded_wait(0, A, None) == api.PA_ERR_INVALID_ARG
+    assert L.pa_check_bounded_wait(10 ** 7 + 1, A, None) == api.PA_ERR_INVALID_ARG
+    assert L.pa_check_bounded_wait(100, None, None) == api.PA_ERR_INVALID_ARG
